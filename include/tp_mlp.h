@@ -1,0 +1,180 @@
+/*
+ * tp_mlp.h - C ABI of libtpmlp: the Megatron-LM intra-layer tensor-parallel
+ * transformer MLP block on one GB300 (sm_103a).
+ *
+ * What the block computes (Megatron-LM explainer, azimuth.plus, section "The
+ * core idea: slicing the feed-forward network across units"; Megatron-LM
+ * notes, notes.yuuk.io, section "MLP block split"):
+ *
+ *     Xn  = LayerNorm(X)            (optional pre-LN, explainer section
+ *                                    "Fixing BERT: reordering layer
+ *                                    normalisation for scaling")
+ *     Y_i = GeLU(Xn A_i + b1_i)     A = [A_1 .. A_t] split by columns
+ *     Z   = sum_{i=0}^{t-1} Y_i B_i + b2    B split by rows into B_i
+ *
+ * The t shards are logical: they run as independent tiles on one GPU.  The
+ * operator g (explainer section "The f and g operators: two lines of code"),
+ * an all-reduce of the partial outputs Y_i B_i on the pages, becomes a sum of
+ * fp32 partials in the fixed order i = 0 .. t-1 inside the second GEMM's
+ * epilogue, each partial with a fresh accumulator.  Its conjugate f (identity
+ * forward, all-reduce of input gradients backward) becomes the same fixed-
+ * order sum in the dX GEMM.  There are no atomics and no split-K with
+ * atomic adds: every output element has exactly one writer and every
+ * reduction runs in a fixed order, so two calls with the same inputs give
+ * bit-identical outputs (the determinism rule of the Megatron Core article,
+ * news.hamidun.com, "bitwise determinism at 2432 GPUs": fixed-order
+ * reductions and private output space per writer).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Shapes: T = tokens (batch * sequence), h = hidden, f = ffn, t = shards,
+ *   f_t = f / t.  Shard i owns ffn columns [i f_t, (i+1) f_t).
+ * - Layouts: every matrix is row-major and contiguous: X, Z, dZ, dX [T, h];
+ *   A and dA [h, f]; B and dB [f, h].  Vectors b1, db1 [f]; b2, db2, gamma,
+ *   beta, dgamma, dbeta [h].
+ * - Element types: X, A, B, Z, dZ, dX are bf16 (TPMLP_BF16) or fp32
+ *   (TPMLP_FP32) as the configuration says.  Biases, LayerNorm parameters
+ *   and every weight/bias/LayerNorm gradient are fp32.  Accumulation is fp32.
+ * - Pointers: every data pointer is a DEVICE pointer to memory the caller
+ *   owns, 16-byte aligned.  The library never allocates, frees or retains
+ *   device memory; it owns only the host-side handle.
+ * - Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *   default stream).  Calls only enqueue work and return without waiting;
+ *   tp_mlp_check() waits and reports device-side errors.
+ * - Errors: every function returns a status code (TPMLP_OK = 0, negative on
+ *   error); nothing is thrown across the ABI and no output is touched when
+ *   argument validation fails.
+ */
+#ifndef TP_MLP_H_
+#define TP_MLP_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---------------------------------------------------- */
+#define TPMLP_OK              0
+#define TPMLP_ERR_ARG        -1  /* null handle/pointer, bad enum value      */
+#define TPMLP_ERR_SHAPE      -2  /* h % 64, f % (64 t), tokens > max_tokens  */
+#define TPMLP_ERR_ALIGN      -3  /* a pointer is not 16-byte aligned         */
+#define TPMLP_ERR_ARCH       -4  /* current device is not compute cap. 10.3  */
+#define TPMLP_ERR_CUDA       -5  /* a CUDA runtime/driver call failed        */
+#define TPMLP_ERR_TIMEOUT    -6  /* a bounded on-device wait gave up         */
+#define TPMLP_ERR_WORKSPACE  -7  /* workspace too small for this call        */
+
+/* ---- configuration values --------------------------------------------- */
+#define TPMLP_BF16        0      /* bf16 storage, fp32 accumulate (tcgen05) */
+#define TPMLP_FP32        1      /* fp32 storage and arithmetic (CUDA cores) */
+#define TPMLP_GELU_ERF    0      /* GeLU(x) = x Phi(x) (default)             */
+#define TPMLP_GELU_TANH   1      /* tanh approximation of GeLU               */
+
+typedef struct tp_mlp_config {
+  int   hidden;          /* h; multiple of 64                                */
+  int   ffn;             /* f; f / shards must be a multiple of 64           */
+  int   shards;          /* t >= 1, the number of column/row shards          */
+  int   max_tokens;      /* largest T any call will pass                     */
+  int   dtype;           /* TPMLP_BF16 or TPMLP_FP32                         */
+  int   use_layernorm;   /* 1: pre-LayerNorm on X before the first GEMM      */
+  float ln_eps;          /* LayerNorm epsilon (added to the biased variance) */
+  int   gelu_mode;       /* TPMLP_GELU_ERF or TPMLP_GELU_TANH                */
+} tp_mlp_config;
+
+typedef struct tp_mlp_handle tp_mlp_handle;
+
+/* Validate `cfg` and create a host-side handle (no device work, no device
+ * memory).  Returns TPMLP_ERR_ARG / TPMLP_ERR_SHAPE for invalid
+ * configurations; *out is set only on success. */
+int tp_mlp_create(const tp_mlp_config* cfg, tp_mlp_handle** out);
+
+/* Release the handle.  Passing NULL is allowed and returns TPMLP_OK. */
+int tp_mlp_destroy(tp_mlp_handle* handle);
+
+/* Bytes of device workspace a call with `tokens` tokens needs.  training = 1
+ * sizes it for tp_mlp_forward(training = 1) followed by tp_mlp_backward on
+ * the same workspace; training = 0 for inference-only forward calls.
+ * Returns 0 for a NULL handle or a negative token count. */
+size_t tp_mlp_workspace_bytes(const tp_mlp_handle* handle, int tokens,
+                              int training);
+
+/* Forward pass (pages: f forward = identity; Y_i = GeLU(X A_i); Z_i = Y_i
+ * B_i; g forward = sum of the Z_i).
+ *   tokens      T, 0 <= T <= max_tokens (T = 0 enqueues nothing)
+ *   X  [T,h]    input activations (dtype)
+ *   A  [h,f], B [f,h]  weights (dtype)
+ *   bias1 [f], bias2 [h]  fp32, each may be NULL (treated as zero)
+ *   ln_gamma, ln_beta [h] fp32, required iff use_layernorm
+ *   Z  [T,h]    output (dtype), overwritten
+ *   workspace   device scratch of at least
+ *               tp_mlp_workspace_bytes(handle, T, training) bytes; with
+ *               training = 1 it keeps what tp_mlp_backward needs (LayerNorm
+ *               output and statistics, H = Xn A + b1, Y) and must be passed
+ *               to tp_mlp_backward unchanged.
+ *   training    1 to save activations for backward, 0 for inference
+ *   stream      cudaStream_t the work is enqueued on */
+int tp_mlp_forward(tp_mlp_handle* handle, int tokens, const void* X,
+                   const void* A, const void* B, const float* bias1,
+                   const float* bias2, const float* ln_gamma,
+                   const float* ln_beta, void* Z, void* workspace,
+                   size_t workspace_bytes, int training, void* stream);
+
+/* Backward pass given dZ = dL/dZ (pages: g backward = identity; f backward =
+ * sum of the per-shard input gradients, here in fixed shard order):
+ *   dB_i = Y_i^T dZ;  db2 = sum_T dZ;  dH_i = (dZ B_i^T) * GeLU'(H_i);
+ *   db1_i = sum_T dH_i;  dA_i = Xn^T dH_i;  dXn = sum_{i=0}^{t-1} dH_i A_i^T;
+ *   dX = LayerNorm-backward(dXn) (or dXn), dgamma, dbeta.
+ *   dZ [T,h] (dtype); X, A, B, ln_gamma as passed to the forward call.
+ *   workspace   the forward call's workspace (training = 1), unchanged.
+ *   dX [T,h] (dtype); dA [h,f], dB [f,h] fp32; all overwritten.
+ *   dbias1 [f], dbias2 [h], dgamma, dbeta [h] fp32: overwritten; each may be
+ *   NULL to skip it (dgamma/dbeta are ignored without LayerNorm).
+ * With T = 0 the weight and bias gradients are set to zero. */
+int tp_mlp_backward(tp_mlp_handle* handle, int tokens, const void* dZ,
+                    const void* X, const void* A, const void* B,
+                    const float* ln_gamma, void* workspace,
+                    size_t workspace_bytes, void* dX, float* dA, float* dB,
+                    float* dbias1, float* dbias2, float* dgamma, float* dbeta,
+                    void* stream);
+
+/* Wait for `stream`, then read and clear the device status word kept in
+ * `workspace`.  Returns TPMLP_OK, TPMLP_ERR_TIMEOUT (a bounded wait inside a
+ * GEMM kernel gave up; the outputs of that call are undefined) or
+ * TPMLP_ERR_CUDA. */
+int tp_mlp_check(tp_mlp_handle* handle, void* workspace, void* stream);
+
+/* Human-readable text for a status code (static storage). */
+const char* tp_mlp_status_string(int status);
+
+/* Detail of the most recent failure on the calling thread (which CUDA call
+ * failed and why, or the device status word's role/block); thread-local
+ * storage, overwritten by the next failure. */
+const char* tp_mlp_last_detail(void);
+
+/* ---- instrumentation --------------------------------------------------- */
+
+/* Number of kernels this handle has launched since creation (memsets not
+ * counted). */
+long long tp_mlp_launch_count(const tp_mlp_handle* handle);
+
+/* Enable (1) or disable (0) per-kernel timing: when enabled every launch is
+ * bracketed by CUDA events on its stream.  Costs one event pair per launch. */
+int tp_mlp_set_timing(tp_mlp_handle* handle, int enable);
+
+/* Wait for the recorded events and fold them into per-kernel totals, then
+ * report kernel `index` (0-based): its name (static storage), launches and
+ * total milliseconds.  Returns TPMLP_ERR_ARG once `index` is past the last
+ * kernel.  tp_mlp_timing_reset() clears the totals. */
+int tp_mlp_timing_get(tp_mlp_handle* handle, int index, const char** name,
+                      long long* launches, double* total_ms);
+int tp_mlp_timing_reset(tp_mlp_handle* handle);
+
+/* Budget, in nanoseconds, for each bounded wait inside the GEMM kernels
+ * (default 2e9).  A wait that exceeds it makes the kernel record
+ * TPMLP_ERR_TIMEOUT in the status word and return early. */
+int tp_mlp_set_wait_budget(tp_mlp_handle* handle, unsigned long long ns);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TP_MLP_H_ */

@@ -1,0 +1,69 @@
+// Launchers shared between the translation units of libtpmlp (host side).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace tpmlp {
+
+// Tensor-core GEMM tile: 128 x 256 output tile, 64-deep k-blocks (one
+// 128-byte swizzle row of bf16).
+constexpr int TC_BM = 128;
+constexpr int TC_BN = 256;
+constexpr int TC_BK = 64;
+
+// D = Aop * Bop on the tensor cores.  a_mn / b_mn select M/N-major operands
+// (the tensor map's innermost dimension runs along M or N) instead of
+// K-major ones.  Supported combinations: (K, MN, GELU_FWD), (K, MN,
+// SHARDSUM), (K, K, GELU_BWD), (K, K, SHARDSUM), (MN, MN, STORE_F32).
+cudaError_t launch_gemm_tc(int epi, bool a_mn, bool b_mn, const CUtensorMap& ta,
+                           const CUtensorMap& tb, const GemmArgs& args,
+                           int grid, cudaStream_t stream);
+
+// fp32 CUDA-core GEMM with the same epilogues.  Element (m, k) of the first
+// operand is a[m * a_sm + k * a_sk]; element (k, n) of the second is
+// b[k * b_sk + n * b_sn].  args.kb_per_seg is the shard segment length in K.
+struct SimtOperands {
+  const float* a;
+  long long a_sm, a_sk;
+  const float* b;
+  long long b_sk, b_sn;
+};
+cudaError_t launch_gemm_simt(int epi, const SimtOperands& ops,
+                             const GemmArgs& args, cudaStream_t stream);
+
+// LayerNorm forward: Xn = (X - mean) * rstd * gamma + beta per row of h.
+cudaError_t launch_ln_fwd(bool bf16, const void* X, const float* gamma,
+                          const float* beta, void* Xn, float* mean,
+                          float* rstd, int rows, int h, float eps,
+                          cudaStream_t stream);
+
+// LayerNorm backward for dX given dXn (fp32).
+cudaError_t launch_ln_bwd(bool bf16, const float* dXn, const void* X,
+                          const float* mean, const float* rstd,
+                          const float* gamma, void* dX, int rows, int h,
+                          cudaStream_t stream);
+
+// Rows per chunk of the two-stage fixed-order column sums.
+constexpr int COLSUM_CHUNK_ROWS = 256;
+inline int colsum_chunks(int rows) {
+  return (rows + COLSUM_CHUNK_ROWS - 1) / COLSUM_CHUNK_ROWS;
+}
+
+// part[chunk][c] = sum over the chunk's rows of src[r][c] (src bf16/fp32).
+cudaError_t launch_colsum_partial(bool bf16, const void* src, float* part,
+                                  int rows, int cols, cudaStream_t stream);
+
+// LayerNorm parameter gradients, stage 1: part_g[chunk][c] = sum dXn * xhat,
+// part_b[chunk][c] = sum dXn over the chunk's rows.
+cudaError_t launch_ln_param_partial(bool bf16, const float* dXn, const void* X,
+                                    const float* mean, const float* rstd,
+                                    float* part_g, float* part_b, int rows,
+                                    int h, cudaStream_t stream);
+
+// out[c] = sum over chunks (in chunk order) of part[chunk][c].
+cudaError_t launch_colsum_finalize(const float* part, float* out, int chunks,
+                                   int cols, cudaStream_t stream);
+
+}  // namespace tpmlp

@@ -1,0 +1,331 @@
+// Bandwidth-bound kernels around the GEMMs: LayerNorm forward/backward and
+// the fixed-order column sums behind db1, db2, dgamma and dbeta.
+//
+// LayerNorm (pre-LN placement: Megatron-LM explainer, section "Fixing BERT:
+// reordering layer normalisation for scaling"): one warp per token row,
+// 16-byte vector loads, warp-shuffle (butterfly) reductions in fp32, mean
+// and biased variance in two passes over the row (the second pass hits L1).
+//
+// Column sums are deterministic by construction (the Megatron Core
+// determinism article: fixed-order reductions, private output per writer):
+// stage 1 gives every block a fixed chunk of COLSUM_CHUNK_ROWS rows and a
+// fixed 128-column strip; inside the block warp w takes rows w, w+8, ... of
+// the chunk in order and the 8 warp partials are added in warp order; stage
+// 2 adds the chunk partials in chunk order.  No atomics anywhere.
+#include "internal.h"
+
+namespace tpmlp {
+namespace {
+
+constexpr int LN_WARPS = 8;  // rows per LayerNorm block
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// 16-byte vectors: 8 bf16 or 4 fp32.
+template <typename T>
+struct Vec;
+template <>
+struct Vec<__nv_bfloat16> {
+  static constexpr int N = 8;
+  __device__ static void load(const __nv_bfloat16* p, float (&v)[8]) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    unpack_bf16x2(u.x, v[0], v[1]);
+    unpack_bf16x2(u.y, v[2], v[3]);
+    unpack_bf16x2(u.z, v[4], v[5]);
+    unpack_bf16x2(u.w, v[6], v[7]);
+  }
+  __device__ static void store(__nv_bfloat16* p, const float (&v)[8]) {
+    *reinterpret_cast<uint4*>(p) =
+        make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                   pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+  }
+};
+template <>
+struct Vec<float> {
+  static constexpr int N = 4;
+  __device__ static void load(const float* p, float (&v)[4]) {
+    const float4 u = *reinterpret_cast<const float4*>(p);
+    v[0] = u.x;
+    v[1] = u.y;
+    v[2] = u.z;
+    v[3] = u.w;
+  }
+  __device__ static void store(float* p, const float (&v)[4]) {
+    *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+  }
+};
+
+template <int N>
+__device__ __forceinline__ void load_f32(const float* p, float (&v)[N]) {
+#pragma unroll
+  for (int i = 0; i < N; i += 4) {
+    const float4 u = __ldg(reinterpret_cast<const float4*>(p + i));
+    v[i] = u.x;
+    v[i + 1] = u.y;
+    v[i + 2] = u.z;
+    v[i + 3] = u.w;
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(LN_WARPS * 32)
+    ln_fwd_kernel(const T* __restrict__ X, const float* __restrict__ gamma,
+                  const float* __restrict__ beta, T* __restrict__ Xn,
+                  float* __restrict__ mean_out, float* __restrict__ rstd_out,
+                  int rows, int h, float eps) {
+  constexpr int V = Vec<T>::N;
+  const int row = blockIdx.x * LN_WARPS + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const T* x = X + static_cast<size_t>(row) * h;
+  const int nv = h / V;
+  float s = 0.f;
+  for (int i = lane; i < nv; i += 32) {
+    float v[V];
+    Vec<T>::load(x + i * V, v);
+#pragma unroll
+    for (int k = 0; k < V; ++k) s += v[k];
+  }
+  const float mu = warp_sum(s) / static_cast<float>(h);
+  float ss = 0.f;
+  for (int i = lane; i < nv; i += 32) {
+    float v[V];
+    Vec<T>::load(x + i * V, v);
+#pragma unroll
+    for (int k = 0; k < V; ++k) {
+      const float d = v[k] - mu;
+      ss += d * d;
+    }
+  }
+  const float rs = rsqrtf(warp_sum(ss) / static_cast<float>(h) + eps);
+  T* y = Xn + static_cast<size_t>(row) * h;
+  for (int i = lane; i < nv; i += 32) {
+    float v[V], g[V], b[V];
+    Vec<T>::load(x + i * V, v);
+    load_f32<V>(gamma + i * V, g);
+    load_f32<V>(beta + i * V, b);
+#pragma unroll
+    for (int k = 0; k < V; ++k) v[k] = (v[k] - mu) * rs * g[k] + b[k];
+    Vec<T>::store(y + i * V, v);
+  }
+  if (lane == 0) {
+    mean_out[row] = mu;
+    rstd_out[row] = rs;
+  }
+}
+
+// dX = rstd * (g - mean(g) - xhat * mean(g * xhat)), g = gamma * dXn.
+template <typename T>
+__global__ void __launch_bounds__(LN_WARPS * 32)
+    ln_bwd_kernel(const float* __restrict__ dXn, const T* __restrict__ X,
+                  const float* __restrict__ mean, const float* __restrict__ rstd,
+                  const float* __restrict__ gamma, T* __restrict__ dX, int rows,
+                  int h) {
+  constexpr int V = Vec<T>::N;
+  const int row = blockIdx.x * LN_WARPS + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const size_t base = static_cast<size_t>(row) * h;
+  const float mu = mean[row], rs = rstd[row];
+  const int nv = h / V;
+  float sg = 0.f, sgx = 0.f;
+  for (int i = lane; i < nv; i += 32) {
+    float x[V], d[V], g[V];
+    Vec<T>::load(X + base + i * V, x);
+    load_f32<V>(dXn + base + i * V, d);
+    load_f32<V>(gamma + i * V, g);
+#pragma unroll
+    for (int k = 0; k < V; ++k) {
+      const float gg = g[k] * d[k];
+      sg += gg;
+      sgx += gg * (x[k] - mu) * rs;
+    }
+  }
+  const float inv_h = 1.0f / static_cast<float>(h);
+  const float c_g = warp_sum(sg) * inv_h;
+  const float c_gx = warp_sum(sgx) * inv_h;
+  for (int i = lane; i < nv; i += 32) {
+    float x[V], d[V], g[V], o[V];
+    Vec<T>::load(X + base + i * V, x);
+    load_f32<V>(dXn + base + i * V, d);
+    load_f32<V>(gamma + i * V, g);
+#pragma unroll
+    for (int k = 0; k < V; ++k) {
+      const float xhat = (x[k] - mu) * rs;
+      o[k] = rs * (g[k] * d[k] - c_g - xhat * c_gx);
+    }
+    Vec<T>::store(dX + base + i * V, o);
+  }
+}
+
+// ------------------------------------------------------- column sums --
+
+constexpr int CS_WARPS = 8;
+constexpr int CS_COLS = 128;  // columns per block: 4 per lane
+
+template <typename T>
+__device__ __forceinline__ void load4(const T* p, float (&v)[4]);
+template <>
+__device__ __forceinline__ void load4<float>(const float* p, float (&v)[4]) {
+  const float4 u = *reinterpret_cast<const float4*>(p);
+  v[0] = u.x;
+  v[1] = u.y;
+  v[2] = u.z;
+  v[3] = u.w;
+}
+template <>
+__device__ __forceinline__ void load4<__nv_bfloat16>(const __nv_bfloat16* p,
+                                                     float (&v)[4]) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  unpack_bf16x2(u.x, v[0], v[1]);
+  unpack_bf16x2(u.y, v[2], v[3]);
+}
+
+// MODE 0: part1 = sum src.  MODE 1 (LayerNorm parameters): part1 = sum
+// dXn * xhat, part2 = sum dXn, with xhat recomputed from X, mean, rstd.
+template <typename T, int MODE>
+__global__ void __launch_bounds__(CS_WARPS * 32)
+    colsum_partial_kernel(const T* __restrict__ src,
+                          const float* __restrict__ dxn,
+                          const float* __restrict__ mean,
+                          const float* __restrict__ rstd,
+                          float* __restrict__ part1, float* __restrict__ part2,
+                          int rows, int cols) {
+  __shared__ float red[2][CS_WARPS][CS_COLS];
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.x * CS_COLS + lane * 4;
+  const int chunk = blockIdx.y;
+  const int r0 = chunk * COLSUM_CHUNK_ROWS;
+  const int r1 = min(rows, r0 + COLSUM_CHUNK_ROWS);
+  float a1[4] = {0.f, 0.f, 0.f, 0.f}, a2[4] = {0.f, 0.f, 0.f, 0.f};
+  if (c < cols) {
+    for (int r = r0 + w; r < r1; r += CS_WARPS) {
+      const size_t off = static_cast<size_t>(r) * cols + c;
+      if constexpr (MODE == 0) {
+        float v[4];
+        load4<T>(src + off, v);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) a1[k] += v[k];
+      } else {
+        float x[4], d[4];
+        load4<T>(src + off, x);
+        load4<float>(dxn + off, d);
+        const float mu = mean[r], rs = rstd[r];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          a1[k] += d[k] * ((x[k] - mu) * rs);
+          a2[k] += d[k];
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    red[0][w][lane * 4 + k] = a1[k];
+    red[1][w][lane * 4 + k] = a2[k];
+  }
+  __syncthreads();
+  const int nout = (MODE == 0) ? 1 : 2;
+  for (int idx = threadIdx.x; idx < nout * CS_COLS; idx += blockDim.x) {
+    const int which = idx / CS_COLS, cc = idx % CS_COLS;
+    const int col = blockIdx.x * CS_COLS + cc;
+    if (col >= cols) continue;
+    float s = 0.f;
+#pragma unroll
+    for (int ww = 0; ww < CS_WARPS; ++ww) s += red[which][ww][cc];
+    float* dst = which == 0 ? part1 : part2;
+    dst[static_cast<size_t>(chunk) * cols + col] = s;
+  }
+}
+
+__global__ void colsum_finalize_kernel(const float* __restrict__ part,
+                                       float* __restrict__ out, int chunks,
+                                       int cols) {
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= cols) return;
+  float s = 0.f;
+  for (int k = 0; k < chunks; ++k) s += part[static_cast<size_t>(k) * cols + c];
+  out[c] = s;
+}
+
+}  // namespace
+
+cudaError_t launch_ln_fwd(bool bf16, const void* X, const float* gamma,
+                          const float* beta, void* Xn, float* mean,
+                          float* rstd, int rows, int h, float eps,
+                          cudaStream_t stream) {
+  const int grid = (rows + LN_WARPS - 1) / LN_WARPS;
+  if (bf16) {
+    ln_fwd_kernel<__nv_bfloat16><<<grid, LN_WARPS * 32, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(X), gamma, beta,
+        static_cast<__nv_bfloat16*>(Xn), mean, rstd, rows, h, eps);
+  } else {
+    ln_fwd_kernel<float><<<grid, LN_WARPS * 32, 0, stream>>>(
+        static_cast<const float*>(X), gamma, beta, static_cast<float*>(Xn),
+        mean, rstd, rows, h, eps);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ln_bwd(bool bf16, const float* dXn, const void* X,
+                          const float* mean, const float* rstd,
+                          const float* gamma, void* dX, int rows, int h,
+                          cudaStream_t stream) {
+  const int grid = (rows + LN_WARPS - 1) / LN_WARPS;
+  if (bf16) {
+    ln_bwd_kernel<__nv_bfloat16><<<grid, LN_WARPS * 32, 0, stream>>>(
+        dXn, static_cast<const __nv_bfloat16*>(X), mean, rstd, gamma,
+        static_cast<__nv_bfloat16*>(dX), rows, h);
+  } else {
+    ln_bwd_kernel<float><<<grid, LN_WARPS * 32, 0, stream>>>(
+        dXn, static_cast<const float*>(X), mean, rstd, gamma,
+        static_cast<float*>(dX), rows, h);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_colsum_partial(bool bf16, const void* src, float* part,
+                                  int rows, int cols, cudaStream_t stream) {
+  const dim3 grid((cols + CS_COLS - 1) / CS_COLS, colsum_chunks(rows));
+  if (bf16) {
+    colsum_partial_kernel<__nv_bfloat16, 0><<<grid, CS_WARPS * 32, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(src), nullptr, nullptr, nullptr,
+        part, nullptr, rows, cols);
+  } else {
+    colsum_partial_kernel<float, 0><<<grid, CS_WARPS * 32, 0, stream>>>(
+        static_cast<const float*>(src), nullptr, nullptr, nullptr, part,
+        nullptr, rows, cols);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ln_param_partial(bool bf16, const float* dXn, const void* X,
+                                    const float* mean, const float* rstd,
+                                    float* part_g, float* part_b, int rows,
+                                    int h, cudaStream_t stream) {
+  const dim3 grid((h + CS_COLS - 1) / CS_COLS, colsum_chunks(rows));
+  if (bf16) {
+    colsum_partial_kernel<__nv_bfloat16, 1><<<grid, CS_WARPS * 32, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(X), dXn, mean, rstd, part_g, part_b,
+        rows, h);
+  } else {
+    colsum_partial_kernel<float, 1><<<grid, CS_WARPS * 32, 0, stream>>>(
+        static_cast<const float*>(X), dXn, mean, rstd, part_g, part_b, rows,
+        h);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_colsum_finalize(const float* part, float* out, int chunks,
+                                   int cols, cudaStream_t stream) {
+  const int threads = 256;
+  colsum_finalize_kernel<<<(cols + threads - 1) / threads, threads, 0,
+                           stream>>>(part, out, chunks, cols);
+  return cudaGetLastError();
+}
+
+}  // namespace tpmlp
