@@ -1,0 +1,416 @@
+"""Throughput of the tensor-parallel MLP block (forward + backward) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference] [--sweep]
+
+One step = one training pass of the block over one batch: tp_mlp_forward
+(training) followed by tp_mlp_backward, i.e. every kernel of the path
+(GEMM1+GeLU, GEMM2 + shard sum, dH GEMM + GeLU', column sums, the two
+weight-gradient GEMMs, dX GEMM + shard sum, and the LayerNorm kernels when the
+workload has pre-LN).  Algorithmic work: 12 T h f flops per step (forward
+4 T h f), whatever the shard count.  Inputs are seeded synthetic tensors of
+the workload's shapes, resident in device memory before timing starts; the
+weights alone exceed the 129 MB L2, so no flush is inserted between steps.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the fp64 CPU
+oracle on a bounded token slice of the same workload instead.  With
+WORLD_SIZE > 1 (torchrun) every rank runs an independent replica on its own
+GPU; ranks meet only at a barrier and a max-reduce of the timings (gloo), no
+collective touches the data path.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "TP-MLP fwd+bwd TFLOP/s and tokens/s on 1 GB300, % of dense bf16 peak"
+DEFAULT_WORKLOAD = "gpt3_13b"
+
+# DRAM traffic per launch of the dominant kernel from an ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by kernel name, with
+# the SHA-256 of the kernel source the capture was taken on.  Reported as
+# null once the source has changed.
+NCU_TRAFFIC = {}
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            p = json.load(fh)
+        return (p["bf16_tflops"], p.get("bf16_tflops_sustained", p["bf16_tflops"]),
+                p["hbm_gbs"], "measured")
+    except (OSError, KeyError, ValueError):
+        return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+def _src_sha():
+    path = os.path.join(ROOT, "tensor_transformer_mlp_tcgen05_gb300", "csrc",
+                        "gemm_tc.cu")
+    with open(path, "rb") as fh:
+        return hashlib.sha256(fh.read()).hexdigest()[:16]
+
+
+# ------------------------------------------------------------ clocks ----
+
+class ClockSampler:
+    """nvidia-smi sampling every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------- distributed ----
+
+def dist_info():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """Max of a float over ranks (gloo, host side); identity for world 1."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------ oracle ----
+
+def oracle_sample(w, inp, tokens, mode="erf"):
+    """Time the fp64 oracle's forward + backward on the first `tokens` rows."""
+    from oracle import mlp as O
+    f64 = lambda t: None if t is None else t[:tokens].double().numpy() \
+        if t.dim() == 2 and t.shape[0] == w.tokens else t.double().numpy()
+    X, dZ = f64(inp["X"]), f64(inp["dZ"])
+    A, B = inp["A"].double().numpy(), inp["B"].double().numpy()
+    gamma, beta = f64(inp["gamma"]), f64(inp["beta"])
+    t0 = time.perf_counter()
+    fwd = O.forward(X, A, B, f64(inp["b1"]), f64(inp["b2"]), gamma, beta, mode=mode)
+    if w.backward:
+        O.backward(dZ, X, A, B, fwd, gamma, mode)
+    return time.perf_counter() - t0
+
+
+def oracle_tokens(w):
+    """Token slice sized for roughly 10-30 s of fp64 work on the host."""
+    per_token = (12.0 if w.backward else 4.0) * w.hidden * w.ffn
+    return int(max(16, min(w.tokens, 1.5e12 / per_token)))
+
+
+# -------------------------------------------------------------- ours ----
+
+def run_ours(args, w, rank, world, local_rank):
+    import torch
+    from tensor_transformer_mlp_tcgen05_gb300 import binding as Bn
+    from tensor_transformer_mlp_tcgen05_gb300 import workloads as W
+    from tensor_transformer_mlp_tcgen05_gb300.mlp import TensorParallelMLP
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    inp = W.make_inputs(w, seed=0)
+    d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
+    m = TensorParallelMLP(w.hidden, w.ffn, w.shards, w.tokens, dtype=w.dtype,
+                          layernorm=w.layernorm)
+    stream = torch.cuda.current_stream()
+    T = w.tokens
+    Z = torch.empty((T, w.hidden), dtype=w.torch_dtype, device=dev)
+    grads = {}
+
+    def step(Xd=None, dZd=None):
+        Xd = d["X"] if Xd is None else Xd
+        dZd = d["dZ"] if dZd is None else dZd
+        m.forward(Xd, d["A"], d["B"], d["b1"], d["b2"], d["gamma"], d["beta"],
+                  training=w.backward, out=Z)
+        if w.backward:
+            m.backward(dZd, Xd, d["A"], d["B"], d["gamma"], bias_grads=True,
+                       out=grads)
+
+    for _ in range(args.warmup):
+        step()
+    if m.check() != 0:
+        raise RuntimeError("device status after warm-up: "
+                           + Bn.tp_mlp_last_detail())
+    torch.cuda.synchronize()
+
+    # Bitwise run-to-run identity of every output (two consecutive steps).
+    snap = {"Z": Z.clone(), **{k: v.clone() for k, v in grads.items()}}
+    step()
+    torch.cuda.synchronize()
+    identical = all(torch.equal(snap[k], (Z if k == "Z" else grads[k]))
+                    for k in snap)
+
+    # ---- timed region: K steps, events on the launching stream ----
+    Bn.tp_mlp_set_timing(m.handle, True)
+    Bn.tp_mlp_timing_reset(m.handle)
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    n0 = Bn.tp_mlp_launch_count(m.handle)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    launches = Bn.tp_mlp_launch_count(m.handle) - n0
+    ms = e0.elapsed_time(e1) / args.steps
+    if m.check() != 0:
+        raise RuntimeError("device status after timing: " + Bn.tp_mlp_last_detail())
+    kernels = Bn.tp_mlp_timing_get(m.handle)
+    Bn.tp_mlp_set_timing(m.handle, False)
+    ms_max = max_over_ranks(ms, world)
+
+    # ---- end to end: pinned host inputs in, results out, every step ----
+    hX = inp["X"].pin_memory()
+    hdZ = inp["dZ"].pin_memory() if w.backward else None
+    hZ = torch.empty_like(inp["X"]).pin_memory()
+    hdX = torch.empty_like(inp["X"]).pin_memory() if w.backward else None
+    Xd = torch.empty_like(d["X"])
+    dZd = torch.empty_like(d["X"]) if w.backward else None
+    h2d = hX.numel() * hX.element_size() * (2 if w.backward else 1)
+    d2h = hZ.numel() * hZ.element_size() * (2 if w.backward else 1)
+
+    def e2e_step():
+        Xd.copy_(hX, non_blocking=True)
+        if w.backward:
+            dZd.copy_(hdZ, non_blocking=True)
+        step(Xd, dZd)
+        hZ.copy_(Z, non_blocking=True)
+        if w.backward:
+            hdX.copy_(grads["dX"], non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e2 = torch.cuda.Event(enable_timing=True)
+    e3 = torch.cuda.Event(enable_timing=True)
+    e2.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e3.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e2.elapsed_time(e3) / args.steps, world)
+
+    flops = w.flops_fwd_bwd() if w.backward else w.flops_fwd()
+    peak_b, peak_s, hbm, peak_src = _peaks()
+    tflops = world * flops / (ms_max * 1e-3) / 1e12
+    total_ms = sum(k[2] for k in kernels) or 1.0
+    krep = [{"name": n, "launches": c, "avg_ms": round(t / max(c, 1), 4),
+             "share": round(t / total_ms, 4)} for n, c, t in kernels]
+    krep.sort(key=lambda r: -r["share"])
+    top = krep[0]
+    roof = None
+    gemm_flops = {
+        "gemm1_gelu": 2.0 * w.tokens * w.hidden * w.ffn,
+        "gemm2_shardsum": 2.0 * w.tokens * w.hidden * w.ffn,
+        "gemm_dh_gelu_bwd": 2.0 * w.tokens * w.hidden * w.ffn,
+        "gemm_wgrad_dB": 2.0 * w.tokens * w.hidden * w.ffn,
+        "gemm_wgrad_dA": 2.0 * w.tokens * w.hidden * w.ffn,
+        "gemm_dx_shardsum": 2.0 * w.tokens * w.hidden * w.ffn,
+    }
+    if top["name"] in gemm_flops:
+        ach = gemm_flops[top["name"]] / (top["avg_ms"] * 1e-3) / 1e12
+        tr = NCU_TRAFFIC.get(top["name"])
+        traffic = tr["bytes"] if tr and tr.get("src") == _src_sha() else None
+        roof = {"kernel": top["name"], "bound": "tensor",
+                "achieved": round(ach, 1), "peak": peak_s, "unit": "TFLOP/s",
+                "frac": round(ach / peak_s, 4),
+                "peak_kind": f"bf16 sustained ({peak_src})",
+                "traffic": traffic}
+
+    line = {
+        "metric": METRIC, "value": round(tflops, 2), "unit": "TFLOP/s",
+        "tokens_per_s": round(world * w.tokens / (ms_max * 1e-3), 1),
+        "frac_of_peak": round(tflops / (world * peak_b), 4),
+        "peak_tflops": peak_b, "peak_kind": f"bf16 burst ({peak_src})",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_max, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic: seeded N(0,1) activations and upstream gradient, "
+                f"N(0,{w.w_std}^2) weights",
+        "config": {"workload": w.name, "tokens": w.tokens, "batch": w.batch,
+                   "seq": w.seq, "hidden": w.hidden, "ffn": w.ffn,
+                   "shards": w.shards, "layernorm": w.layernorm,
+                   "pass": "fwd+bwd" if w.backward else "fwd",
+                   "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "l2": "inputs larger than L2 (no flush)"},
+        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2),
+                "unit": "TFLOP/s", "ms_per_step": round(e2e_ms, 4),
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "bitwise_identical_two_runs": identical,
+        "clocks": clocks,
+        "roofline": roof,
+        "kernels": krep,
+    }
+    m.close()
+    return line, inp
+
+
+def run_cpu_baseline(w, inp):
+    import numpy as np  # noqa: F401  (BLAS threads are set at import)
+    tokens = oracle_tokens(w)
+    secs = oracle_sample(w, inp, tokens)
+    flops = (w.flops_fwd_bwd(tokens) if w.backward else w.flops_fwd(tokens))
+    return {"value": round(flops / secs / 1e12, 5), "unit": "TFLOP/s",
+            "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"first {tokens} of {w.tokens} tokens, fp64 "
+                      f"{'fwd+bwd' if w.backward else 'fwd'} ({secs:.1f} s)"}
+
+
+def run_reference(args, w):
+    """The oracle as the reference arm: each step is one bounded token slice
+    of the workload through the fp64 CPU oracle, on the host cores."""
+    from tensor_transformer_mlp_tcgen05_gb300 import workloads as W
+    tokens = max(16, oracle_tokens(w) // max(1, args.steps + args.warmup) * 2)
+    tokens = min(tokens, w.tokens)
+    inp = W.make_inputs(w.with_(tokens=tokens), seed=0)
+    ws = w.with_(tokens=tokens)
+    for _ in range(args.warmup):
+        oracle_sample(ws, inp, tokens)
+    t = 0.0
+    for _ in range(args.steps):
+        t += oracle_sample(ws, inp, tokens)
+    sec = t / args.steps
+    flops = ws.flops_fwd_bwd() if w.backward else ws.flops_fwd()
+    val = flops / sec / 1e12
+    sample = f"{tokens} of {w.tokens} tokens per step, fp64"
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(val, 5),
+        "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "tokens": w.tokens, "hidden": w.hidden,
+                   "ffn": w.ffn, "shards": w.shards},
+        "cpu_baseline": {"value": round(val, 5), "unit": "TFLOP/s",
+                         "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(val, 5), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--tokens", type=int, default=None)
+    ap.add_argument("--shards", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    from tensor_transformer_mlp_tcgen05_gb300 import workloads as W
+    w = W.WORKLOADS[args.workload]
+    if args.tokens:
+        w = w.with_(tokens=args.tokens)
+    if args.shards:
+        w = w.with_(shards=args.shards)
+    rank, world, local_rank = dist_info()
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, w)), flush=True)
+        return 0
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    from tensor_transformer_mlp_tcgen05_gb300 import build as b
+    if rank == 0:
+        b.build()
+    barrier(world)
+    line, inp = run_ours(args, w, rank, world, local_rank)
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = run_cpu_baseline(w, inp)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -100,7 +100,8 @@ size_t tp_mlp_workspace_bytes(const tp_mlp_handle* handle, int tokens,
 
 /* Forward pass (pages: f forward = identity; Y_i = GeLU(X A_i); Z_i = Y_i
  * B_i; g forward = sum of the Z_i).
- *   tokens      T, 0 <= T <= max_tokens (T = 0 enqueues nothing)
+ *   tokens      T, 0 <= T <= max_tokens (T = 0 enqueues nothing; X and Z
+ *               may then be NULL)
  *   X  [T,h]    input activations (dtype)
  *   A  [h,f], B [f,h]  weights (dtype)
  *   bias1 [f], bias2 [h]  fp32, each may be NULL (treated as zero)
@@ -129,7 +130,8 @@ int tp_mlp_forward(tp_mlp_handle* handle, int tokens, const void* X,
  *   dX [T,h] (dtype); dA [h,f], dB [f,h] fp32; all overwritten.
  *   dbias1 [f], dbias2 [h], dgamma, dbeta [h] fp32: overwritten; each may be
  *   NULL to skip it (dgamma/dbeta are ignored without LayerNorm).
- * With T = 0 the weight and bias gradients are set to zero. */
+ * With T = 0 the weight and bias gradients are set to zero (dZ, X and dX
+ * may then be NULL). */
 int tp_mlp_backward(tp_mlp_handle* handle, int tokens, const void* dZ,
                     const void* X, const void* A, const void* B,
                     const float* ln_gamma, void* workspace,

@@ -1,0 +1,209 @@
+"""ctypes binding of libtpmlp, with the C ABI's names (argument marshalling
+only: every step of the block runs in the library's CUDA kernels).
+
+Tensor arguments may be torch tensors (their ``data_ptr()`` is passed), raw
+integer device addresses, or None for the C ABI's nullable pointers.  Status
+codes other than TPMLP_OK raise :class:`TPMLPError`, except from
+``tp_mlp_check`` and the plain queries, which return the code.  There is no
+fallback: if the shared library is missing, loading it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+LIB_PATH = _build.LIB_PATH
+
+TPMLP_OK = 0
+TPMLP_ERR_ARG = -1
+TPMLP_ERR_SHAPE = -2
+TPMLP_ERR_ALIGN = -3
+TPMLP_ERR_ARCH = -4
+TPMLP_ERR_CUDA = -5
+TPMLP_ERR_TIMEOUT = -6
+TPMLP_ERR_WORKSPACE = -7
+
+TPMLP_BF16 = 0
+TPMLP_FP32 = 1
+TPMLP_GELU_ERF = 0
+TPMLP_GELU_TANH = 1
+
+# Every function the header declares, for the export check.
+EXPORTED = (
+    "tp_mlp_create", "tp_mlp_destroy", "tp_mlp_workspace_bytes",
+    "tp_mlp_forward", "tp_mlp_backward", "tp_mlp_check",
+    "tp_mlp_status_string", "tp_mlp_last_detail", "tp_mlp_launch_count",
+    "tp_mlp_set_timing", "tp_mlp_timing_get", "tp_mlp_timing_reset",
+    "tp_mlp_set_wait_budget",
+)
+
+
+class tp_mlp_config(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int), ("ffn", ctypes.c_int),
+                ("shards", ctypes.c_int), ("max_tokens", ctypes.c_int),
+                ("dtype", ctypes.c_int), ("use_layernorm", ctypes.c_int),
+                ("ln_eps", ctypes.c_float), ("gelu_mode", ctypes.c_int)]
+
+
+class TPMLPError(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(message)
+        self.code = code
+
+
+_lib = None
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+_sz = ctypes.c_size_t
+
+
+def lib(path: str | None = None) -> ctypes.CDLL:
+    """Load libtpmlp.so (once) and declare its signatures."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(
+            f"{p} is missing: build it with "
+            "tensor_transformer_mlp_tcgen05_gb300.build.build() (nvcc, sm_103a)")
+    L = ctypes.CDLL(p)
+    L.tp_mlp_create.argtypes = [ctypes.POINTER(tp_mlp_config),
+                                ctypes.POINTER(_vp)]
+    L.tp_mlp_create.restype = _i
+    L.tp_mlp_destroy.argtypes = [_vp]
+    L.tp_mlp_destroy.restype = _i
+    L.tp_mlp_workspace_bytes.argtypes = [_vp, _i, _i]
+    L.tp_mlp_workspace_bytes.restype = _sz
+    L.tp_mlp_forward.argtypes = [_vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                 _vp, _vp, _sz, _i, _vp]
+    L.tp_mlp_forward.restype = _i
+    L.tp_mlp_backward.argtypes = [_vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _sz,
+                                  _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+    L.tp_mlp_backward.restype = _i
+    L.tp_mlp_check.argtypes = [_vp, _vp, _vp]
+    L.tp_mlp_check.restype = _i
+    L.tp_mlp_status_string.argtypes = [_i]
+    L.tp_mlp_status_string.restype = ctypes.c_char_p
+    L.tp_mlp_last_detail.argtypes = []
+    L.tp_mlp_last_detail.restype = ctypes.c_char_p
+    L.tp_mlp_launch_count.argtypes = [_vp]
+    L.tp_mlp_launch_count.restype = ctypes.c_longlong
+    L.tp_mlp_set_timing.argtypes = [_vp, _i]
+    L.tp_mlp_set_timing.restype = _i
+    L.tp_mlp_timing_get.argtypes = [_vp, _i, ctypes.POINTER(ctypes.c_char_p),
+                                    ctypes.POINTER(ctypes.c_longlong),
+                                    ctypes.POINTER(ctypes.c_double)]
+    L.tp_mlp_timing_get.restype = _i
+    L.tp_mlp_timing_reset.argtypes = [_vp]
+    L.tp_mlp_timing_reset.restype = _i
+    L.tp_mlp_set_wait_budget.argtypes = [_vp, ctypes.c_ulonglong]
+    L.tp_mlp_set_wait_budget.restype = _i
+    if path is None:
+        _lib = L
+    return L
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(s):
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def tp_mlp_status_string(code: int) -> str:
+    return lib().tp_mlp_status_string(code).decode()
+
+
+def tp_mlp_last_detail() -> str:
+    return lib().tp_mlp_last_detail().decode()
+
+
+def _check(code: int, what: str):
+    if code != TPMLP_OK:
+        raise TPMLPError(code, f"{what}: {tp_mlp_status_string(code)} "
+                               f"[{tp_mlp_last_detail()}]")
+
+
+def tp_mlp_create(config: tp_mlp_config) -> int:
+    h = _vp()
+    _check(lib().tp_mlp_create(ctypes.byref(config), ctypes.byref(h)),
+           "tp_mlp_create")
+    return h.value
+
+
+def tp_mlp_destroy(handle: int) -> None:
+    _check(lib().tp_mlp_destroy(handle), "tp_mlp_destroy")
+
+
+def tp_mlp_workspace_bytes(handle: int, tokens: int, training: int) -> int:
+    return int(lib().tp_mlp_workspace_bytes(handle, tokens, training))
+
+
+def tp_mlp_forward(handle, tokens, X, A, B, bias1, bias2, ln_gamma, ln_beta,
+                   Z, workspace, workspace_bytes, training, stream=None):
+    _check(lib().tp_mlp_forward(
+        handle, tokens, _ptr(X), _ptr(A), _ptr(B), _ptr(bias1), _ptr(bias2),
+        _ptr(ln_gamma), _ptr(ln_beta), _ptr(Z), _ptr(workspace),
+        workspace_bytes, training, _stream(stream)), "tp_mlp_forward")
+
+
+def tp_mlp_backward(handle, tokens, dZ, X, A, B, ln_gamma, workspace,
+                    workspace_bytes, dX, dA, dB, dbias1, dbias2, dgamma, dbeta,
+                    stream=None):
+    _check(lib().tp_mlp_backward(
+        handle, tokens, _ptr(dZ), _ptr(X), _ptr(A), _ptr(B), _ptr(ln_gamma),
+        _ptr(workspace), workspace_bytes, _ptr(dX), _ptr(dA), _ptr(dB),
+        _ptr(dbias1), _ptr(dbias2), _ptr(dgamma), _ptr(dbeta),
+        _stream(stream)), "tp_mlp_backward")
+
+
+def tp_mlp_check(handle, workspace, stream=None) -> int:
+    return int(lib().tp_mlp_check(handle, _ptr(workspace), _stream(stream)))
+
+
+def tp_mlp_launch_count(handle) -> int:
+    return int(lib().tp_mlp_launch_count(handle))
+
+
+def tp_mlp_set_timing(handle, enable: bool) -> None:
+    _check(lib().tp_mlp_set_timing(handle, 1 if enable else 0),
+           "tp_mlp_set_timing")
+
+
+def tp_mlp_timing_get(handle):
+    """All per-kernel totals: list of (name, launches, total_ms)."""
+    out = []
+    i = 0
+    while True:
+        name = ctypes.c_char_p()
+        n = ctypes.c_longlong()
+        ms = ctypes.c_double()
+        rc = lib().tp_mlp_timing_get(handle, i, ctypes.byref(name),
+                                     ctypes.byref(n), ctypes.byref(ms))
+        if rc == TPMLP_ERR_ARG:
+            break
+        _check(rc, "tp_mlp_timing_get")
+        out.append((name.value.decode(), n.value, ms.value))
+        i += 1
+    return out
+
+
+def tp_mlp_timing_reset(handle) -> None:
+    _check(lib().tp_mlp_timing_reset(handle), "tp_mlp_timing_reset")
+
+
+def tp_mlp_set_wait_budget(handle, ns: int) -> None:
+    _check(lib().tp_mlp_set_wait_budget(handle, ns), "tp_mlp_set_wait_budget")

@@ -353,7 +353,8 @@ int tp_mlp_forward(tp_mlp_handle* H, int tokens, const void* X, const void* A,
   if (H == nullptr) return TPMLP_ERR_ARG;
   const tp_mlp_config& c = H->cfg;
   if (tokens < 0 || tokens > c.max_tokens) return TPMLP_ERR_SHAPE;
-  if (!X || !A || !B || !Z || !workspace) return TPMLP_ERR_ARG;
+  // Token-sized arrays may be NULL when there are no tokens.
+  if (!A || !B || !workspace || (tokens > 0 && (!X || !Z))) return TPMLP_ERR_ARG;
   if (c.use_layernorm && (!ln_gamma || !ln_beta)) return TPMLP_ERR_ARG;
   const void* ptrs[] = {X, A, B, Z, workspace, bias1, bias2, ln_gamma, ln_beta};
   for (const void* p : ptrs)
@@ -431,7 +432,8 @@ int tp_mlp_backward(tp_mlp_handle* H, int tokens, const void* dZ,
   if (H == nullptr) return TPMLP_ERR_ARG;
   const tp_mlp_config& c = H->cfg;
   if (tokens < 0 || tokens > c.max_tokens) return TPMLP_ERR_SHAPE;
-  if (!dZ || !X || !A || !B || !workspace || !dX || !dA || !dB)
+  if (!A || !B || !workspace || !dA || !dB ||
+      (tokens > 0 && (!dZ || !X || !dX)))
     return TPMLP_ERR_ARG;
   if (c.use_layernorm && !ln_gamma) return TPMLP_ERR_ARG;
   const void* ptrs[] = {dZ, X, A, B, ln_gamma, workspace, dX, dA, dB,

@@ -1,0 +1,110 @@
+"""A small object wrapper over the C ABI: owns a handle and a workspace
+tensor, checks tensor shapes/dtypes/devices, and calls tp_mlp_forward /
+tp_mlp_backward.  All arithmetic happens in libtpmlp's kernels; PyTorch only
+provides device memory and the stream."""
+from __future__ import annotations
+
+import torch
+
+from . import binding as B_
+
+
+class TensorParallelMLP:
+    """Megatron-style column/row-split MLP block with t logical shards."""
+
+    def __init__(self, hidden: int, ffn: int, shards: int, max_tokens: int,
+                 dtype: str = "bf16", layernorm: bool = False,
+                 ln_eps: float = 1e-5, gelu: str = "erf", device=None):
+        self.cfg = B_.tp_mlp_config(
+            hidden=hidden, ffn=ffn, shards=shards, max_tokens=max_tokens,
+            dtype=B_.TPMLP_BF16 if dtype == "bf16" else B_.TPMLP_FP32,
+            use_layernorm=1 if layernorm else 0, ln_eps=ln_eps,
+            gelu_mode=B_.TPMLP_GELU_ERF if gelu == "erf" else B_.TPMLP_GELU_TANH)
+        if dtype not in ("bf16", "fp32") or gelu not in ("erf", "tanh"):
+            raise ValueError("dtype must be bf16|fp32 and gelu erf|tanh")
+        self.handle = B_.tp_mlp_create(self.cfg)
+        self.hidden, self.ffn, self.shards = hidden, ffn, shards
+        self.max_tokens = max_tokens
+        self.layernorm = layernorm
+        self.dtype = torch.bfloat16 if dtype == "bf16" else torch.float32
+        self.device = torch.device(device or "cuda")
+        self._ws = None
+        self._ws_tokens = None
+
+    def close(self):
+        if self.handle:
+            B_.tp_mlp_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # ---------------------------------------------------------------- ---
+    def workspace(self, tokens: int, training: bool = True) -> torch.Tensor:
+        need = B_.tp_mlp_workspace_bytes(self.handle, tokens, 1 if training else 0)
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = torch.empty(max(need, 256), dtype=torch.uint8,
+                                   device=self.device)
+        return self._ws
+
+    def _chk(self, name, t, shape, dtype):
+        if t is None:
+            return
+        if tuple(t.shape) != tuple(shape) or t.dtype != dtype:
+            raise ValueError(f"{name}: expected {tuple(shape)} {dtype}, got "
+                             f"{tuple(t.shape)} {t.dtype}")
+        if not t.is_contiguous() or t.device.type != "cuda":
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+
+    def forward(self, X, A, B, b1=None, b2=None, gamma=None, beta=None,
+                training: bool = True, out=None, stream=None):
+        T = X.shape[0]
+        h, f = self.hidden, self.ffn
+        self._chk("X", X, (T, h), self.dtype)
+        self._chk("A", A, (h, f), self.dtype)
+        self._chk("B", B, (f, h), self.dtype)
+        self._chk("b1", b1, (f,), torch.float32)
+        self._chk("b2", b2, (h,), torch.float32)
+        self._chk("gamma", gamma, (h,), torch.float32)
+        self._chk("beta", beta, (h,), torch.float32)
+        Z = out if out is not None else torch.empty((T, h), dtype=self.dtype,
+                                                   device=X.device)
+        self._chk("Z", Z, (T, h), self.dtype)
+        ws = self.workspace(T, training)
+        B_.tp_mlp_forward(self.handle, T, X, A, B, b1, b2, gamma, beta, Z, ws,
+                          ws.numel(), 1 if training else 0, stream)
+        return Z
+
+    def backward(self, dZ, X, A, B, gamma=None, bias_grads: bool = True,
+                 out=None, stream=None):
+        """Gradients after a training forward on the same workspace.
+        Returns a dict with dX, dA, dB and (optionally) db1, db2, dgamma,
+        dbeta."""
+        T = dZ.shape[0]
+        h, f = self.hidden, self.ffn
+        self._chk("dZ", dZ, (T, h), self.dtype)
+        dev = dZ.device
+        g = out or {}
+        g.setdefault("dX", torch.empty((T, h), dtype=self.dtype, device=dev))
+        g.setdefault("dA", torch.empty((h, f), dtype=torch.float32, device=dev))
+        g.setdefault("dB", torch.empty((f, h), dtype=torch.float32, device=dev))
+        if bias_grads:
+            g.setdefault("db1", torch.empty(f, dtype=torch.float32, device=dev))
+            g.setdefault("db2", torch.empty(h, dtype=torch.float32, device=dev))
+        if self.layernorm:
+            g.setdefault("dgamma", torch.empty(h, dtype=torch.float32, device=dev))
+            g.setdefault("dbeta", torch.empty(h, dtype=torch.float32, device=dev))
+        ws = self.workspace(T, True)
+        B_.tp_mlp_backward(self.handle, T, dZ, X, A, B, gamma, ws, ws.numel(),
+                           g["dX"], g["dA"], g["dB"], g.get("db1"), g.get("db2"),
+                           g.get("dgamma"), g.get("dbeta"), stream)
+        return g
+
+    def check(self, stream=None) -> int:
+        """Synchronise and return the device status (TPMLP_OK or an error)."""
+        if self._ws is None:
+            return B_.TPMLP_OK
+        return B_.tp_mlp_check(self.handle, self._ws, stream)
