@@ -87,7 +87,7 @@ class TensorParallelMLP:
         h, f = self.hidden, self.ffn
         self._chk("dZ", dZ, (T, h), self.dtype)
         dev = dZ.device
-        g = out or {}
+        g = out if out is not None else {}
         g.setdefault("dX", torch.empty((T, h), dtype=self.dtype, device=dev))
         g.setdefault("dA", torch.empty((h, f), dtype=torch.float32, device=dev))
         g.setdefault("dB", torch.empty((f, h), dtype=torch.float32, device=dev))
