@@ -139,6 +139,34 @@ int tp_mlp_backward(tp_mlp_handle* handle, int tokens, const void* dZ,
                     float* dbias1, float* dbias2, float* dgamma, float* dbeta,
                     void* stream);
 
+/* Bias gradient without any device allocation: dbias[c] = sum over the
+ * `tokens` rows of grad[r][c], for a row-major [tokens, cols] gradient
+ * (e.g. dZ, giving db2).  The pages have no counterpart for this entry
+ * point; it exists for callers that cannot allocate device memory, such as
+ * a host engine that reserves the whole device memory pool for itself at
+ * start-up, or a tool that must not change the process's device-memory
+ * footprint while it runs, and so cannot provide the workspace that
+ * tp_mlp_backward takes its scratch from.
+ *   tokens  T >= 0 (T = 0 writes zeros); cols > 0, a multiple of 64
+ *   dtype   TPMLP_BF16 or TPMLP_FP32: the element type of `grad`
+ *   grad    device pointer, [T, cols]; may be NULL when T = 0
+ *   dbias   device pointer, [cols] fp32, overwritten
+ * The partial sums go to one static device array of
+ * TPMLP_NOALLOC_SCRATCH_FLOATS floats (4 MiB), which every GPU that loads
+ * the library holds until the process exits; calls need
+ * ceil(T / 256) * cols <= TPMLP_NOALLOC_SCRATCH_FLOATS and return
+ * TPMLP_ERR_SHAPE (with tp_mlp_last_detail() saying why) otherwise.  The
+ * first call on a device looks the array's device address up with that
+ * device current; make that first call before any stream capture.  Every
+ * call shares the array and it keeps the last call's contents (each call
+ * overwrites all it reads, so nothing needs clearing); calls that overlap on
+ * the GPU, on different streams, race on it.  The result is bit-identical to
+ * tp_mlp_backward's bias gradients for the same input.  No cudaMalloc,
+ * cudaFree or allocating library routine is called. */
+#define TPMLP_NOALLOC_SCRATCH_FLOATS (1 << 20)
+int tp_mlp_bias_grad_noalloc(int tokens, int cols, int dtype, const void* grad,
+                             float* dbias, void* stream);
+
 /* Wait for `stream`, then read and clear the device status word kept in
  * `workspace`.  Returns TPMLP_OK, TPMLP_ERR_TIMEOUT (a bounded wait inside a
  * GEMM kernel gave up; the outputs of that call are undefined) or

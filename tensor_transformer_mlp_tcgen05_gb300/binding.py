@@ -36,8 +36,10 @@ EXPORTED = (
     "tp_mlp_forward", "tp_mlp_backward", "tp_mlp_check",
     "tp_mlp_status_string", "tp_mlp_last_detail", "tp_mlp_launch_count",
     "tp_mlp_set_timing", "tp_mlp_timing_get", "tp_mlp_timing_reset",
-    "tp_mlp_set_wait_budget",
+    "tp_mlp_set_wait_budget", "tp_mlp_bias_grad_noalloc",
 )
+
+TPMLP_NOALLOC_SCRATCH_FLOATS = 1 << 20
 
 
 class tp_mlp_config(ctypes.Structure):
@@ -101,6 +103,8 @@ def lib(path: str | None = None) -> ctypes.CDLL:
     L.tp_mlp_timing_reset.restype = _i
     L.tp_mlp_set_wait_budget.argtypes = [_vp, ctypes.c_ulonglong]
     L.tp_mlp_set_wait_budget.restype = _i
+    L.tp_mlp_bias_grad_noalloc.argtypes = [_i, _i, _i, _vp, _vp, _vp]
+    L.tp_mlp_bias_grad_noalloc.restype = _i
     if path is None:
         _lib = L
     return L
@@ -207,3 +211,12 @@ def tp_mlp_timing_reset(handle) -> None:
 
 def tp_mlp_set_wait_budget(handle, ns: int) -> None:
     _check(lib().tp_mlp_set_wait_budget(handle, ns), "tp_mlp_set_wait_budget")
+
+
+def tp_mlp_bias_grad_noalloc(tokens, cols, dtype, grad, dbias, stream=None):
+    """Column sums of a [tokens, cols] gradient into dbias, with the partial
+    sums in the library's static device scratch instead of a workspace (for
+    callers that cannot allocate device memory)."""
+    _check(lib().tp_mlp_bias_grad_noalloc(tokens, cols, dtype, _ptr(grad),
+                                          _ptr(dbias), _stream(stream)),
+           "tp_mlp_bias_grad_noalloc")

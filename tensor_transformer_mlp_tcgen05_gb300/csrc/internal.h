@@ -66,4 +66,7 @@ cudaError_t launch_ln_param_partial(bool bf16, const float* dXn, const void* X,
 cudaError_t launch_colsum_finalize(const float* part, float* out, int chunks,
                                    int cols, cudaStream_t stream);
 
+// Record a message for tp_mlp_last_detail() on the calling thread.
+void set_last_detail(const char* msg);
+
 }  // namespace tpmlp

@@ -190,6 +190,8 @@ bool aligned16(const void* p) {
 
 }  // namespace
 
+void tpmlp::set_last_detail(const char* msg) { set_detail_msg(msg); }
+
 // ------------------------------------------------------------- handle --
 
 struct tp_mlp_handle {
