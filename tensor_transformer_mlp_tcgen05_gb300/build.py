@@ -22,7 +22,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG, "libtpmlp.so")
 
-SOURCES = ["gemm_tc.cu", "rowops.cu", "simt.cu", "tp_mlp_host.cu", "noalloc.cu"]
+SOURCES = ["gemm_tc.cu", "gemm_tc2.cu", "rowops.cu", "simt.cu",
+           "tp_mlp_host.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
           "--expt-relaxed-constexpr", "-I" + INCLUDE, "-I" + CSRC]

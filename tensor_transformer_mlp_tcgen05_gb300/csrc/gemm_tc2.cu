@@ -1,0 +1,418 @@
+// CTA-pair tcgen05 GEMM for sm_103a (cta_group::2), same operands, shard
+// sum and epilogues as gemm_tc.cu, with a 256 x 256 output tile per pair.
+//
+// Clusters of 2 CTAs; the pair (CTA ranks 0 and 1) owns one 256 x 256 tile
+// at a time, persistent over the tile list.  Per k-block each CTA loads only
+// its half of the operands into its own shared memory: rank r loads A rows
+// [m0 + 128 r, +128) and B columns [n0 + 128 r, +128), 32 KB per stage, so a
+// 6-stage ring fits where the one-CTA kernel held 4 stages, and each CTA
+// moves half as many B bytes per flop.  The even CTA issues
+// tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16): the tensor cores of
+// both SMs read A from their own CTA and B from both, and each CTA receives
+// its 128 rows of D (all 256 columns) in its own TMEM.
+//
+// Synchronisation:
+//   full[s]   (rank 0 only) counts the TMA bytes of both CTAs: rank 0 arms it
+//             with the pair's 64 KB, both CTAs' copies complete on it.
+//   empty[s]  (each CTA) arrived by the MMA issuer's multicast commit when the
+//             MMAs have read stage s, releasing both producers.
+//   tfull[b]  (each CTA) arrived by a multicast commit when accumulator b is
+//             ready in both TMEMs.
+//   tempty[b] (rank 0 only) 16 arrivals: 8 epilogue warps of each CTA, the
+//             peer's arriving remotely.
+// Registers, the shard sum, the epilogue, the bounded waits and the abort
+// path are as in the one-CTA kernel; in addition both CTAs meet at cluster
+// barriers before the first copy and before TMEM is freed, so no CTA leaves
+// while its peer may still touch its shared memory or barriers.
+#include "gemm_common.cuh"
+
+namespace tpmlp {
+namespace {
+
+using namespace gemm;
+
+constexpr int PM = 256;  // tile rows per pair
+constexpr int PN = 256;  // tile columns per pair
+constexpr int HM = 128;  // rows per CTA
+constexpr int HN = 128;  // B columns staged per CTA
+constexpr int BK = TC_BK;
+constexpr int STAGES = 6;
+constexpr int NUM_THREADS = 384;
+constexpr int NUM_EPI_WARPS = 8;
+constexpr int FIRST_EPI_WARP = 4;
+constexpr int REGS_LAUNCH = 168;
+constexpr int REGS_CONTROL = 56;
+constexpr int REGS_EPILOGUE = 224;
+static_assert(REGS_CONTROL * 128 + REGS_EPILOGUE * 256 <=
+                  REGS_LAUNCH * NUM_THREADS,
+              "register split exceeds the launch allocation");
+constexpr uint32_t A_STAGE_BYTES = HM * BK * 2;  // 16 KiB
+constexpr uint32_t B_STAGE_BYTES = HN * BK * 2;  // 16 KiB
+constexpr uint32_t STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr uint32_t PAIR_STAGE_BYTES = 2 * STAGE_BYTES;
+constexpr uint32_t TMEM_COLS = 2 * PN;
+constexpr int NUM_BARRIERS = 2 * STAGES + 5;
+constexpr size_t SMEM_BYTES =
+    1024 + size_t(STAGES) * STAGE_BYTES + NUM_BARRIERS * 8 + 16;
+// On an abort, copies this CTA issued may still be landing in its shared
+// memory (their completions are counted on the peer's barrier), so the CTA
+// waits this long before freeing its resources.
+constexpr unsigned long long ABORT_SETTLE_NS = 2000000ull;
+
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+
+__device__ __forceinline__ void cta_barrier() {
+  asm volatile("bar.sync 1, %0;" ::"n"(NUM_THREADS) : "memory");
+}
+
+// Bounded wait with cluster-scope acquire (tempty: arrivals from both CTAs).
+__device__ __forceinline__ bool wait_bounded_cluster(uint32_t bar,
+                                                     uint32_t parity,
+                                                     const Ctl& c, int role) {
+  if (ptx::mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (true) {
+    if (ptx::mbar_try_wait_cluster(bar, parity)) return true;
+    if (*c.abort_flag) return false;
+    if (ptx::globaltimer_ns() - t0 > c.budget) {
+      *c.abort_flag = 1;
+      if (atomicCAS(c.status, 0, TPMLP_ERR_TIMEOUT) == 0) {
+        c.status[1] = role;
+        c.status[2] = static_cast<int>(blockIdx.x);
+      }
+      __threadfence();
+      return false;
+    }
+  }
+}
+
+template <bool A_MN, bool B_MN, int EPI>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA,
+                    const __grid_constant__ CUtensorMap tmB,
+                    const GemmArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t s_a = ptx::smem_u32(smem);
+  const uint32_t s_b = s_a + STAGES * A_STAGE_BYTES;
+  uint64_t* bars =
+      reinterpret_cast<uint64_t*>(smem + size_t(STAGES) * STAGE_BYTES);
+  const uint32_t bar0 = ptx::smem_u32(bars);
+  const uint32_t full0 = bar0;
+  const uint32_t empty0 = bar0 + 8u * STAGES;
+  const uint32_t tfull0 = bar0 + 16u * STAGES;
+  const uint32_t tempty0 = tfull0 + 16u;
+  const uint32_t done_bar = tempty0 + 16u;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARRIERS);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = ptx::cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1;
+  const int num_pairs = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(full0 + 8u * s, 1);
+      ptx::mbar_init(empty0 + 8u * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(tfull0 + 8u * b, 1);
+      ptx::mbar_init(tempty0 + 8u * b, 2 * NUM_EPI_WARPS);
+    }
+    ptx::mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&tmA);
+    ptx::prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc_pair(ptx::smem_u32(tmem_slot), TMEM_COLS);
+    ptx::tmem_relinquish_pair();
+  }
+  ptx::tc_fence_before();
+  ptx::cluster_sync();  // barriers of both CTAs initialised, TMEM allocated
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+  const Ctl ctl{abort_flag, args.status, args.budget_ns};
+  const int num_m = (args.M + PM - 1) / PM;
+  const int num_n = (args.N + PN - 1) / PN;
+  const int num_tiles = num_m * num_n;
+  const int kb_total = args.kb_per_seg * args.num_seg;
+  // The even CTA's full and tempty barriers, as cluster addresses.
+  const uint32_t lead_full0 = ptx::mapa_shared(full0, 0);
+  const uint32_t lead_tempty0 = ptx::mapa_shared(tempty0, 0);
+
+  if (warp < FIRST_EPI_WARP) {
+    ptx::setmaxnreg_dec<REGS_CONTROL>();
+    if (warp == 0 && lane == 0) {
+      // ---------------------------------------------------- producer --
+      uint32_t stage = 0, phase = 0;
+      bool alive = true;
+      for (int tile = pair; alive && tile < num_tiles; tile += num_pairs) {
+        int mb, nb;
+        tile_coords(tile, num_m, num_n, args.group_m, mb, nb);
+        const int m0 = mb * PM + static_cast<int>(rank) * HM;
+        const int n0 = nb * PN + static_cast<int>(rank) * HN;
+        for (int kb = 0; kb < kb_total; ++kb) {
+          if (!wait_bounded(empty0 + 8u * stage, phase ^ 1u, ctl,
+                            ROLE_PRODUCER)) {
+            alive = false;
+            break;
+          }
+          if (leader) ptx::mbar_arrive_expect_tx(full0 + 8u * stage,
+                                                 PAIR_STAGE_BYTES);
+          const uint32_t fb = lead_full0 + 8u * stage;
+          const int k0 = kb * BK;
+          const uint32_t da = s_a + stage * A_STAGE_BYTES;
+          const uint32_t db = s_b + stage * B_STAGE_BYTES;
+          if constexpr (!A_MN) {
+            ptx::tma_load_2d_pair(da, &tmA, fb, k0, m0);
+          } else {
+#pragma unroll
+            for (int j = 0; j < HM / 64; ++j)
+              ptx::tma_load_2d_pair(da + j * (BK * 128), &tmA, fb, m0 + 64 * j,
+                                    k0);
+          }
+          if constexpr (!B_MN) {
+            ptx::tma_load_2d_pair(db, &tmB, fb, k0, n0);
+          } else {
+#pragma unroll
+            for (int j = 0; j < HN / 64; ++j)
+              ptx::tma_load_2d_pair(db + j * (BK * 128), &tmB, fb, n0 + 64 * j,
+                                    k0);
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    } else if (warp == 1 && lane == 0 && leader) {
+      // -------------------------------------------------- MMA issuer --
+      constexpr uint32_t IDESC = idesc_bf16_f32(PM, PN, A_MN, B_MN);
+      constexpr uint32_t A_KSTEP = A_MN ? 16 * 128 : 32;
+      constexpr uint32_t B_KSTEP = B_MN ? 16 * 128 : 32;
+      constexpr uint32_t A_LBO = A_MN ? BK * 128 : 16;
+      constexpr uint32_t B_LBO = B_MN ? BK * 128 : 16;
+      constexpr uint16_t BOTH = 0x3;
+      uint32_t stage = 0, phase = 0, acc = 0;
+      bool alive = true;
+      for (int tile = pair; alive && tile < num_tiles; tile += num_pairs) {
+        for (int seg = 0; alive && seg < args.num_seg; ++seg, ++acc) {
+          const uint32_t b = acc & 1u;
+          const uint32_t aph = (acc >> 1) & 1u;
+          if (!wait_bounded_cluster(tempty0 + 8u * b, aph ^ 1u, ctl,
+                                    ROLE_MMA)) {
+            alive = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t d_tmem = tmem_base + b * PN;
+          for (int kb = 0; kb < args.kb_per_seg; ++kb) {
+            if (!wait_bounded(full0 + 8u * stage, phase, ctl, ROLE_MMA)) {
+              alive = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t a_addr = s_a + stage * A_STAGE_BYTES;
+            const uint32_t b_addr = s_b + stage * B_STAGE_BYTES;
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k) {
+              const uint64_t adesc =
+                  ptx::sdesc_sw128(a_addr + k * A_KSTEP, A_LBO, 1024);
+              const uint64_t bdesc =
+                  ptx::sdesc_sw128(b_addr + k * B_KSTEP, B_LBO, 1024);
+              ptx::mma_bf16_pair(d_tmem, adesc, bdesc, IDESC,
+                                 (kb > 0 || k > 0) ? 1u : 0u);
+            }
+            ptx::mma_commit_pair(empty0 + 8u * stage, BOTH);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (alive) ptx::mma_commit_pair(tfull0 + 8u * b, BOTH);
+        }
+      }
+      if (*reinterpret_cast<volatile int*>(abort_flag)) {
+        // Wait for every MMA this thread issued before TMEM is freed.
+        ptx::mma_commit_pair(done_bar, 0x1);
+        wait_teardown(done_bar, 0);
+      }
+    }
+    // ------------------------------------------------------ teardown --
+    cta_barrier();
+    if (*reinterpret_cast<volatile int*>(abort_flag) && warp == 0 &&
+        lane == 0) {
+      const uint64_t t0 = ptx::globaltimer_ns();
+      while (ptx::globaltimer_ns() - t0 < ABORT_SETTLE_NS) {
+      }
+    }
+    cta_barrier();
+    ptx::cluster_sync();
+    if (warp == 1) {
+      __syncwarp();
+      ptx::tc_fence_after();
+      ptx::tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    }
+  } else {
+    ptx::setmaxnreg_inc<REGS_EPILOGUE>();
+    // ------------------------------------------------------ epilogue --
+    const int ew = warp - FIRST_EPI_WARP;
+    const int q = warp & 3;
+    const int half = ew >> 2;
+    uint32_t acc = 0;
+    bool alive = true;
+    for (int tile = pair; alive && tile < num_tiles; tile += num_pairs) {
+      int mb, nb;
+      tile_coords(tile, num_m, num_n, args.group_m, mb, nb);
+      const int row = mb * PM + static_cast<int>(rank) * HM + q * 32 + lane;
+      const int col_base = nb * PN + half * 128;
+      const bool row_ok = row < args.M;
+      float S[EPI == EPI_SHARDSUM ? 128 : 1];
+      for (int seg = 0; seg < args.num_seg; ++seg, ++acc) {
+        const uint32_t b = acc & 1u;
+        const uint32_t aph = (acc >> 1) & 1u;
+        bool ok = wait_bounded(tfull0 + 8u * b, aph, ctl, ROLE_EPILOGUE);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) {
+          alive = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t taddr =
+            tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * PN +
+            half * 128;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t r[32];
+          ptx::tmem_ld_32x32b_x32(taddr + j * 32, r);
+          ptx::tmem_ld_wait();
+          if constexpr (EPI == EPI_SHARDSUM) {
+            if (seg == 0) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) S[j * 32 + i] = __uint_as_float(r[i]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) S[j * 32 + i] += __uint_as_float(r[i]);
+            }
+          } else {
+            const int c0 = col_base + j * 32;
+            if (row_ok && c0 < args.N) {
+              float v[32];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+              epilogue_chunk<EPI>(args, row, c0, v);
+            }
+          }
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (leader) {
+            ptx::mbar_arrive(tempty0 + 8u * b);
+          } else {
+            ptx::mbar_arrive_cluster(lead_tempty0 + 8u * b);
+          }
+        }
+      }
+      if constexpr (EPI == EPI_SHARDSUM) {
+        if (alive && row_ok) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int c0 = col_base + j * 32;
+            if (c0 < args.N) {
+              float v[32];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = S[j * 32 + i];
+              add_bias32(args.bias, c0, v);
+              const size_t off = static_cast<size_t>(row) * args.ldo + c0;
+              if (args.out_f32) {
+                store_f32x32(static_cast<float*>(args.out) + off, v);
+              } else {
+                store_bf16x32(static_cast<__nv_bfloat16*>(args.out) + off, v);
+              }
+            }
+          }
+        }
+      }
+    }
+    cta_barrier();
+    cta_barrier();
+    ptx::cluster_sync();
+  }
+}
+
+template <bool A_MN, bool B_MN, int EPI>
+cudaError_t launch_impl(const CUtensorMap& ta, const CUtensorMap& tb,
+                        const GemmArgs& args, int max_pairs,
+                        cudaStream_t stream) {
+  auto kern = gemm_tc2_kernel<A_MN, B_MN, EPI>;
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs * NUM_THREADS <
+      REGS_CONTROL * 128 + REGS_EPILOGUE * NUM_EPI_WARPS * 32)
+    return cudaErrorInvalidConfiguration;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(SMEM_BYTES));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // Never more pairs than can be resident at once (the kernel is persistent).
+  cfg.gridDim = dim3(2 * max_pairs);
+  int resident = 0;
+  e = cudaOccupancyMaxActiveClusters(&resident, kern, &cfg);
+  if (e != cudaSuccess) return e;
+  if (resident <= 0) return cudaErrorInvalidConfiguration;
+  const long long tiles =
+      static_cast<long long>((args.M + PM - 1) / PM) * ((args.N + PN - 1) / PN);
+  long long pairs = tiles < max_pairs ? tiles : max_pairs;
+  if (pairs > resident) pairs = resident;
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
+  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, args);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_tc2(int epi, bool a_mn, bool b_mn,
+                            const CUtensorMap& ta, const CUtensorMap& tb,
+                            const GemmArgs& args, int max_pairs,
+                            cudaStream_t stream) {
+  if (!a_mn && b_mn && epi == EPI_GELU_FWD)
+    return launch_impl<false, true, EPI_GELU_FWD>(ta, tb, args, max_pairs,
+                                                  stream);
+  if (!a_mn && b_mn && epi == EPI_SHARDSUM)
+    return launch_impl<false, true, EPI_SHARDSUM>(ta, tb, args, max_pairs,
+                                                  stream);
+  if (!a_mn && !b_mn && epi == EPI_GELU_BWD)
+    return launch_impl<false, false, EPI_GELU_BWD>(ta, tb, args, max_pairs,
+                                                   stream);
+  if (!a_mn && !b_mn && epi == EPI_SHARDSUM)
+    return launch_impl<false, false, EPI_SHARDSUM>(ta, tb, args, max_pairs,
+                                                   stream);
+  if (a_mn && b_mn && epi == EPI_STORE_F32)
+    return launch_impl<true, true, EPI_STORE_F32>(ta, tb, args, max_pairs,
+                                                  stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace tpmlp

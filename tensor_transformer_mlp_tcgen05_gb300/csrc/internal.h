@@ -21,6 +21,15 @@ cudaError_t launch_gemm_tc(int epi, bool a_mn, bool b_mn, const CUtensorMap& ta,
                            const CUtensorMap& tb, const GemmArgs& args,
                            int grid, cudaStream_t stream);
 
+// The same GEMM on CTA pairs (tcgen05 cta_group::2, 256 x 256 tile per pair).
+// K-major B operands must be encoded with 128-row boxes (each CTA stages half
+// of the tile's N).  At most `max_pairs` clusters are launched.
+constexpr int TC2_BN_HALF = 128;
+cudaError_t launch_gemm_tc2(int epi, bool a_mn, bool b_mn,
+                            const CUtensorMap& ta, const CUtensorMap& tb,
+                            const GemmArgs& args, int max_pairs,
+                            cudaStream_t stream);
+
 // fp32 CUDA-core GEMM with the same epilogues.  Element (m, k) of the first
 // operand is a[m * a_sm + k * a_sk]; element (k, n) of the second is
 // b[k * b_sk + n * b_sn].  args.kb_per_seg is the shard segment length in K.

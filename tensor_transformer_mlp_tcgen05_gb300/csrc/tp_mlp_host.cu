@@ -16,6 +16,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -278,9 +279,27 @@ GemmArgs base_args(const tp_mlp_handle* H, void* ws, const Layout& L) {
     if (rc_ != TPMLP_OK) return rc_; \
   } while (0)
 
+// GEMM kernel selection: CTA pairs (256 x 256 tiles) by default; setting
+// TPMLP_GEMM_VARIANT=single in the environment selects the one-CTA kernel.
+bool use_pairs() {
+  static const bool pairs = [] {
+    const char* v = std::getenv("TPMLP_GEMM_VARIANT");
+    return !(v != nullptr && std::strcmp(v, "single") == 0);
+  }();
+  return pairs;
+}
+
+// Box height of a K-major B operand for the selected kernel.
+int b_box_rows() { return use_pairs() ? TC2_BN_HALF : TC_BN; }
+
 int tc_gemm(tp_mlp_handle* H, const char* name, cudaStream_t s, int sms,
             int epi, bool a_mn, bool b_mn, const CUtensorMap& ta,
             const CUtensorMap& tb, const GemmArgs& args) {
+  if (use_pairs()) {
+    return run(H, name, s, [&] {
+      return launch_gemm_tc2(epi, a_mn, b_mn, ta, tb, args, sms / 2, s);
+    });
+  }
   const int grid = grid_for(args.M, args.N, sms);
   return run(H, name, s, [&] {
     return launch_gemm_tc(epi, a_mn, b_mn, ta, tb, args, grid, s);
@@ -497,7 +516,7 @@ int tp_mlp_backward(tp_mlp_handle* H, int tokens, const void* dZ,
     CUtensorMap ta, tb;
     gy.kb_per_seg = h / TC_BK;
     TRY(kmajor_map(&ta, dZ, T, h, TC_BM));
-    TRY(kmajor_map(&tb, B, f, h, TC_BN));
+    TRY(kmajor_map(&tb, B, f, h, b_box_rows()));
     TRY(tc_gemm(H, "gemm_dh_gelu_bwd", s, sms, EPI_GELU_BWD, false, false, ta,
                 tb, gy));
     if (dbias2) TRY(colsum(H, "colsum_db2", s, true, dZ, part, dbias2, T, h));
@@ -517,7 +536,7 @@ int tp_mlp_backward(tp_mlp_handle* H, int tokens, const void* dZ,
                 ga));
     gx.kb_per_seg = ft / TC_BK;
     TRY(kmajor_map(&ta, dH, T, f, TC_BM));
-    TRY(kmajor_map(&tb, A, h, f, TC_BN));
+    TRY(kmajor_map(&tb, A, h, f, b_box_rows()));
     TRY(tc_gemm(H, "gemm_dx_shardsum", s, sms, EPI_SHARDSUM, false, false, ta,
                 tb, gx));
   } else {
