@@ -125,5 +125,66 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, int row,
   }
 }
 
+// ---------------------------------------------- TMA-store epilogue ----
+// Each epilogue warp owns 32 output rows (its TMEM lanes) and stages one
+// 32-row x 128-byte chunk at a time in shared memory, laid out as the
+// 128-byte-swizzled box of the output's tensor map (16-byte unit c of row r
+// at unit c ^ (r % 8)), so the 32 lanes' 16-byte writes hit distinct banks.
+// Lane 0 then issues one asynchronous TMA store of the chunk; two staging
+// buffers per warp alternate.
+constexpr uint32_t STAGE_CHUNK_BYTES = 32 * 128;
+
+struct ChunkStager {
+  uint32_t base;   // this warp's two buffers (1024-byte aligned)
+  uint32_t count;  // chunks issued so far (lane 0's bulk groups)
+
+  // Write this lane's 128-byte row `w` and store the chunk at element
+  // coordinates (c0, r0) of `map`.
+  __device__ __forceinline__ void put(const CUtensorMap* map, int c0, int r0,
+                                      const uint32_t (&w)[32], int lane) {
+    const uint32_t buf = base + (count & 1u) * STAGE_CHUNK_BYTES;
+    if (lane == 0) ptx::bulk_wait_read<1>();  // buffer used two chunks ago
+    __syncwarp();
+    const uint32_t row = buf + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint32_t u = static_cast<uint32_t>(c ^ (lane & 7));
+      ptx::st_shared_v4(row + u * 16u, w[4 * c], w[4 * c + 1], w[4 * c + 2],
+                        w[4 * c + 3]);
+    }
+    ptx::fence_proxy_async_shared();
+    __syncwarp();
+    if (lane == 0) {
+      ptx::tma_store_2d(map, buf, c0, r0);
+      ptx::bulk_commit();
+    }
+    ++count;
+  }
+
+  __device__ __forceinline__ void drain(int lane) {
+    if (lane == 0) ptx::bulk_wait_all();
+    __syncwarp();
+  }
+};
+
+__device__ __forceinline__ void pack_bf16x64(const float* v, uint32_t (&w)[32]) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+}
+
+__device__ __forceinline__ void add_bias_n(const float* bias, int c0, float* v,
+                                           int n) {
+  if (bias == nullptr) return;
+  const float4* b = reinterpret_cast<const float4*>(bias + c0);
+#pragma unroll
+  for (int i = 0; i < n / 4; ++i) {
+    const float4 t = __ldg(b + i);
+    v[4 * i + 0] += t.x;
+    v[4 * i + 1] += t.y;
+    v[4 * i + 2] += t.z;
+    v[4 * i + 3] += t.w;
+  }
+}
+
 }  // namespace gemm
 }  // namespace tpmlp

@@ -4,12 +4,12 @@
 // Clusters of 2 CTAs; the pair (CTA ranks 0 and 1) owns one 256 x 256 tile
 // at a time, persistent over the tile list.  Per k-block each CTA loads only
 // its half of the operands into its own shared memory: rank r loads A rows
-// [m0 + 128 r, +128) and B columns [n0 + 128 r, +128), 32 KB per stage, so a
-// 6-stage ring fits where the one-CTA kernel held 4 stages, and each CTA
-// moves half as many B bytes per flop.  The even CTA issues
+// [m0 + 128 r, +128) and B columns [n0 + 128 r, +128), 32 KB per stage, and
+// each CTA moves half as many B bytes per flop as the one-CTA kernel.  The even CTA issues
 // tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16): the tensor cores of
 // both SMs read A from their own CTA and B from both, and each CTA receives
-// its 128 rows of D (all 256 columns) in its own TMEM.
+// its 128 rows of D (all 256 columns) in its own TMEM.  The ring has 5
+// stages (160 KB) next to 64 KB of epilogue staging.
 //
 // Synchronisation:
 //   full[s]   (rank 0 only) counts the TMA bytes of both CTAs: rank 0 arms it
@@ -20,10 +20,15 @@
 //             ready in both TMEMs.
 //   tempty[b] (rank 0 only) 16 arrivals: 8 epilogue warps of each CTA, the
 //             peer's arriving remotely.
-// Registers, the shard sum, the epilogue, the bounded waits and the abort
-// path are as in the one-CTA kernel; in addition both CTAs meet at cluster
-// barriers before the first copy and before TMEM is freed, so no CTA leaves
-// while its peer may still touch its shared memory or barriers.
+// Epilogue: each warp turns its 32 TMEM lanes into 32-row x 128-byte chunks
+// (64 bf16 or 32 fp32 columns), stages them in shared memory and writes them
+// with asynchronous TMA stores (coalesced full-line writes; rows or columns
+// past the tensor's edge are clipped by the TMA unit), double-buffered per
+// warp, so the epilogue never issues row-strided global stores.
+// Registers, the shard sum, the bounded waits and the abort path are as in
+// the one-CTA kernel; in addition both CTAs meet at cluster barriers before
+// the first copy and before TMEM is freed, so no CTA leaves while its peer may
+// still touch its shared memory or barriers.
 #include "gemm_common.cuh"
 
 namespace tpmlp {
@@ -36,7 +41,7 @@ constexpr int PN = 256;  // tile columns per pair
 constexpr int HM = 128;  // rows per CTA
 constexpr int HN = 128;  // B columns staged per CTA
 constexpr int BK = TC_BK;
-constexpr int STAGES = 6;
+constexpr int STAGES = 5;
 constexpr int NUM_THREADS = 384;
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int FIRST_EPI_WARP = 4;
@@ -52,8 +57,9 @@ constexpr uint32_t STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
 constexpr uint32_t PAIR_STAGE_BYTES = 2 * STAGE_BYTES;
 constexpr uint32_t TMEM_COLS = 2 * PN;
 constexpr int NUM_BARRIERS = 2 * STAGES + 5;
-constexpr size_t SMEM_BYTES =
-    1024 + size_t(STAGES) * STAGE_BYTES + NUM_BARRIERS * 8 + 16;
+constexpr uint32_t EPI_STAGING_BYTES = NUM_EPI_WARPS * 2 * STAGE_CHUNK_BYTES;
+constexpr size_t SMEM_BYTES = 1024 + size_t(STAGES) * STAGE_BYTES +
+                              EPI_STAGING_BYTES + NUM_BARRIERS * 8 + 16;
 // On an abort, copies this CTA issued may still be landing in its shared
 // memory (their completions are counted on the peer's barrier), so the CTA
 // waits this long before freeing its resources.
@@ -90,14 +96,17 @@ template <bool A_MN, bool B_MN, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmO,
+                    const __grid_constant__ CUtensorMap tmO2,
                     const GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t s_a = ptx::smem_u32(smem);
   const uint32_t s_b = s_a + STAGES * A_STAGE_BYTES;
-  uint64_t* bars =
-      reinterpret_cast<uint64_t*>(smem + size_t(STAGES) * STAGE_BYTES);
+  const uint32_t s_epi = s_a + STAGES * STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(
+      smem + size_t(STAGES) * STAGE_BYTES + EPI_STAGING_BYTES);
   const uint32_t bar0 = ptx::smem_u32(bars);
   const uint32_t full0 = bar0;
   const uint32_t empty0 = bar0 + 8u * STAGES;
@@ -130,6 +139,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tmap(&tmA);
     ptx::prefetch_tmap(&tmB);
+    ptx::prefetch_tmap(&tmO);
   }
   if (warp == 1) {
     ptx::tmem_alloc_pair(ptx::smem_u32(tmem_slot), TMEM_COLS);
@@ -266,16 +276,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ptx::setmaxnreg_inc<REGS_EPILOGUE>();
     // ------------------------------------------------------ epilogue --
     const int ew = warp - FIRST_EPI_WARP;
-    const int q = warp & 3;
-    const int half = ew >> 2;
+    const int q = warp & 3;      // TMEM sub-partition this warp may read
+    const int half = ew >> 2;    // which 128-column half of the tile
+    ChunkStager st{s_epi + static_cast<uint32_t>(ew) * 2u * STAGE_CHUNK_BYTES,
+                   0u};
     uint32_t acc = 0;
     bool alive = true;
     for (int tile = pair; alive && tile < num_tiles; tile += num_pairs) {
       int mb, nb;
       tile_coords(tile, num_m, num_n, args.group_m, mb, nb);
-      const int row = mb * PM + static_cast<int>(rank) * HM + q * 32 + lane;
+      const int row0 = mb * PM + static_cast<int>(rank) * HM + q * 32;
+      const int row = row0 + lane;
+      const bool live = row0 < args.M;  // warp-uniform: any row in range
       const int col_base = nb * PN + half * 128;
-      const bool row_ok = row < args.M;
       float S[EPI == EPI_SHARDSUM ? 128 : 1];
       for (int seg = 0; seg < args.num_seg; ++seg, ++acc) {
         const uint32_t b = acc & 1u;
@@ -290,12 +303,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t taddr =
             tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * PN +
             half * 128;
+        if constexpr (EPI == EPI_SHARDSUM) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint32_t r[32];
-          ptx::tmem_ld_32x32b_x32(taddr + j * 32, r);
-          ptx::tmem_ld_wait();
-          if constexpr (EPI == EPI_SHARDSUM) {
+          for (int j = 0; j < 4; ++j) {
+            uint32_t r[32];
+            ptx::tmem_ld_32x32b_x32(taddr + j * 32, r);
+            ptx::tmem_ld_wait();
             if (seg == 0) {
 #pragma unroll
               for (int i = 0; i < 32; ++i) S[j * 32 + i] = __uint_as_float(r[i]);
@@ -303,13 +316,62 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
               for (int i = 0; i < 32; ++i) S[j * 32 + i] += __uint_as_float(r[i]);
             }
-          } else {
-            const int c0 = col_base + j * 32;
-            if (row_ok && c0 < args.N) {
-              float v[32];
+          }
+        } else if constexpr (EPI == EPI_STORE_F32) {
 #pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-              epilogue_chunk<EPI>(args, row, c0, v);
+          for (int j = 0; j < 4; ++j) {
+            uint32_t r[32];
+            ptx::tmem_ld_32x32b_x32(taddr + j * 32, r);
+            ptx::tmem_ld_wait();
+            const int c0 = col_base + j * 32;
+            if (live && c0 < args.N) st.put(&tmO, c0, row0, r, lane);
+          }
+        } else {
+          // GeLU forward / backward: two 64-column bf16 chunks.
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            uint32_t r0[32], r1[32];
+            ptx::tmem_ld_32x32b_x32(taddr + j * 64, r0);
+            ptx::tmem_ld_32x32b_x32(taddr + j * 64 + 32, r1);
+            ptx::tmem_ld_wait();
+            const int c0 = col_base + j * 64;
+            if (live && c0 < args.N) {
+              float v[64];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                v[i] = __uint_as_float(r0[i]);
+                v[32 + i] = __uint_as_float(r1[i]);
+              }
+              uint32_t w[32];
+              if constexpr (EPI == EPI_GELU_FWD) {
+                add_bias_n(args.bias, c0, v, 64);
+                if (args.out2 != nullptr) {
+                  pack_bf16x64(v, w);
+                  st.put(&tmO2, c0, row0, w, lane);
+                }
+#pragma unroll
+                for (int i = 0; i < 64; ++i) v[i] = gelu_f32(v[i], args.gelu_mode);
+              } else {
+                if (row < args.M) {
+                  const uint4* hp = reinterpret_cast<const uint4*>(
+                      static_cast<const __nv_bfloat16*>(args.aux) +
+                      static_cast<size_t>(row) * args.ldaux + c0);
+#pragma unroll
+                  for (int i = 0; i < 8; ++i) {
+                    const uint4 u = hp[i];
+                    const uint32_t hw[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                      float h0, h1;
+                      unpack_bf16x2(hw[k], h0, h1);
+                      v[8 * i + 2 * k + 0] *= gelu_grad_f32(h0, args.gelu_mode);
+                      v[8 * i + 2 * k + 1] *= gelu_grad_f32(h1, args.gelu_mode);
+                    }
+                  }
+                }
+              }
+              pack_bf16x64(v, w);
+              st.put(&tmO, c0, row0, w, lane);
             }
           }
         }
@@ -324,26 +386,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
       if constexpr (EPI == EPI_SHARDSUM) {
-        if (alive && row_ok) {
+        if (alive && live) {
+          if (args.out_f32) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int c0 = col_base + j * 32;
-            if (c0 < args.N) {
-              float v[32];
+            for (int j = 0; j < 4; ++j) {
+              const int c0 = col_base + j * 32;
+              if (c0 < args.N) {
+                add_bias_n(args.bias, c0, &S[j * 32], 32);
+                uint32_t w[32];
 #pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] = S[j * 32 + i];
-              add_bias32(args.bias, c0, v);
-              const size_t off = static_cast<size_t>(row) * args.ldo + c0;
-              if (args.out_f32) {
-                store_f32x32(static_cast<float*>(args.out) + off, v);
-              } else {
-                store_bf16x32(static_cast<__nv_bfloat16*>(args.out) + off, v);
+                for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(S[j * 32 + i]);
+                st.put(&tmO, c0, row0, w, lane);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              const int c0 = col_base + j * 64;
+              if (c0 < args.N) {
+                add_bias_n(args.bias, c0, &S[j * 64], 64);
+                uint32_t w[32];
+                pack_bf16x64(&S[j * 64], w);
+                st.put(&tmO, c0, row0, w, lane);
               }
             }
           }
         }
       }
     }
+    st.drain(lane);
     cta_barrier();
     cta_barrier();
     ptx::cluster_sync();
@@ -352,6 +423,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 template <bool A_MN, bool B_MN, int EPI>
 cudaError_t launch_impl(const CUtensorMap& ta, const CUtensorMap& tb,
+                        const CUtensorMap& to, const CUtensorMap& to2,
                         const GemmArgs& args, int max_pairs,
                         cudaStream_t stream) {
   auto kern = gemm_tc2_kernel<A_MN, B_MN, EPI>;
@@ -386,7 +458,7 @@ cudaError_t launch_impl(const CUtensorMap& ta, const CUtensorMap& tb,
   long long pairs = tiles < max_pairs ? tiles : max_pairs;
   if (pairs > resident) pairs = resident;
   cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
-  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, args);
+  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, to, to2, args);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -395,22 +467,23 @@ cudaError_t launch_impl(const CUtensorMap& ta, const CUtensorMap& tb,
 
 cudaError_t launch_gemm_tc2(int epi, bool a_mn, bool b_mn,
                             const CUtensorMap& ta, const CUtensorMap& tb,
+                            const CUtensorMap& to, const CUtensorMap& to2,
                             const GemmArgs& args, int max_pairs,
                             cudaStream_t stream) {
   if (!a_mn && b_mn && epi == EPI_GELU_FWD)
-    return launch_impl<false, true, EPI_GELU_FWD>(ta, tb, args, max_pairs,
+    return launch_impl<false, true, EPI_GELU_FWD>(ta, tb, to, to2, args, max_pairs,
                                                   stream);
   if (!a_mn && b_mn && epi == EPI_SHARDSUM)
-    return launch_impl<false, true, EPI_SHARDSUM>(ta, tb, args, max_pairs,
+    return launch_impl<false, true, EPI_SHARDSUM>(ta, tb, to, to2, args, max_pairs,
                                                   stream);
   if (!a_mn && !b_mn && epi == EPI_GELU_BWD)
-    return launch_impl<false, false, EPI_GELU_BWD>(ta, tb, args, max_pairs,
+    return launch_impl<false, false, EPI_GELU_BWD>(ta, tb, to, to2, args, max_pairs,
                                                    stream);
   if (!a_mn && !b_mn && epi == EPI_SHARDSUM)
-    return launch_impl<false, false, EPI_SHARDSUM>(ta, tb, args, max_pairs,
+    return launch_impl<false, false, EPI_SHARDSUM>(ta, tb, to, to2, args, max_pairs,
                                                    stream);
   if (a_mn && b_mn && epi == EPI_STORE_F32)
-    return launch_impl<true, true, EPI_STORE_F32>(ta, tb, args, max_pairs,
+    return launch_impl<true, true, EPI_STORE_F32>(ta, tb, to, to2, args, max_pairs,
                                                   stream);
   return cudaErrorInvalidValue;
 }

@@ -23,10 +23,14 @@ cudaError_t launch_gemm_tc(int epi, bool a_mn, bool b_mn, const CUtensorMap& ta,
 
 // The same GEMM on CTA pairs (tcgen05 cta_group::2, 256 x 256 tile per pair).
 // K-major B operands must be encoded with 128-row boxes (each CTA stages half
-// of the tile's N).  At most `max_pairs` clusters are launched.
+// of the tile's N).  Outputs are written through tensor maps: `to` for
+// args.out and `to2` for args.out2 (EPI_GELU_FWD's H), 128-byte-swizzled
+// boxes of 32 rows x 128 bytes (64 bf16 or 32 fp32 columns).  At most
+// `max_pairs` clusters are launched.
 constexpr int TC2_BN_HALF = 128;
 cudaError_t launch_gemm_tc2(int epi, bool a_mn, bool b_mn,
                             const CUtensorMap& ta, const CUtensorMap& tb,
+                            const CUtensorMap& to, const CUtensorMap& to2,
                             const GemmArgs& args, int max_pairs,
                             cudaStream_t stream);
 

@@ -145,35 +145,49 @@ EncodeTiledFn get_encoder() {
   return fn;
 }
 
-// bf16 matrix stored row-major [outer, inner] (inner contiguous, pitch in
-// elements); box = {64 inner elements (one 128-byte swizzle row), box_outer}.
-int encode_map(CUtensorMap* m, const void* base, uint64_t inner,
-               uint64_t outer, uint64_t pitch, uint32_t box_outer) {
+// Row-major matrix [outer, inner] (inner contiguous, pitch in elements) of
+// bf16 or fp32, 128-byte swizzle, box = {box_inner, box_outer} elements.
+int encode_map_t(CUtensorMap* m, const void* base, bool f32, uint64_t inner,
+                 uint64_t outer, uint64_t pitch, uint32_t box_inner,
+                 uint32_t box_outer) {
   EncodeTiledFn enc = get_encoder();
   if (enc == nullptr) {
     set_detail_msg("cuTensorMapEncodeTiled entry point not available");
     return TPMLP_ERR_CUDA;
   }
+  const uint64_t es = f32 ? 4 : 2;
   const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {pitch * 2};
-  const cuuint32_t box[2] = {64, box_outer};
+  const cuuint64_t strides[1] = {pitch * es};
+  const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                         const_cast<void*>(base), dims, strides, box, estr,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE,
-                         CU_TENSOR_MAP_SWIZZLE_128B,
-                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const CUresult r =
+      enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+          2, const_cast<void*>(base), dims, strides, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     std::snprintf(g_detail, sizeof(g_detail),
                   "cuTensorMapEncodeTiled failed (%d): inner=%llu outer=%llu "
-                  "pitch=%llu box_outer=%u",
+                  "pitch=%llu box=%ux%u",
                   static_cast<int>(r), (unsigned long long)inner,
                   (unsigned long long)outer, (unsigned long long)pitch,
-                  box_outer);
+                  box_inner, box_outer);
     return TPMLP_ERR_CUDA;
   }
   return TPMLP_OK;
+}
+
+// bf16 operand: box = {64 inner elements (one 128-byte swizzle row), box_outer}.
+int encode_map(CUtensorMap* m, const void* base, uint64_t inner,
+               uint64_t outer, uint64_t pitch, uint32_t box_outer) {
+  return encode_map_t(m, base, false, inner, outer, pitch, 64, box_outer);
+}
+
+// GEMM output [rows, cols] with leading dimension ld: 32-row boxes of 128
+// bytes (64 bf16 or 32 fp32 columns), the pair kernel's store chunk.
+int out_map(CUtensorMap* m, const void* p, bool f32, int rows, int cols,
+            long long ld) {
+  return encode_map_t(m, p, f32, cols, rows, ld, f32 ? 32 : 64, 32);
 }
 
 // K-major operand [rows, K] with box rows = the tile's M or N extent.
@@ -292,12 +306,24 @@ bool use_pairs() {
 // Box height of a K-major B operand for the selected kernel.
 int b_box_rows() { return use_pairs() ? TC2_BN_HALF : TC_BN; }
 
+// One GEMM launch.  The pair kernel writes through output tensor maps,
+// encoded here from args.out / args.out2 (row-major, leading dimension
+// args.ldo, element type fp32 for the fp32-output epilogues).
 int tc_gemm(tp_mlp_handle* H, const char* name, cudaStream_t s, int sms,
             int epi, bool a_mn, bool b_mn, const CUtensorMap& ta,
             const CUtensorMap& tb, const GemmArgs& args) {
   if (use_pairs()) {
+    const bool f32 = epi == EPI_STORE_F32 || (epi == EPI_SHARDSUM && args.out_f32);
+    CUtensorMap to, to2;
+    TRY(out_map(&to, args.out, f32, args.M, args.N, args.ldo));
+    if (args.out2 != nullptr) {
+      TRY(out_map(&to2, args.out2, false, args.M, args.N, args.ldo));
+    } else {
+      to2 = to;  // unused by the kernel
+    }
     return run(H, name, s, [&] {
-      return launch_gemm_tc2(epi, a_mn, b_mn, ta, tb, args, sms / 2, s);
+      return launch_gemm_tc2(epi, a_mn, b_mn, ta, tb, to, to2, args, sms / 2,
+                             s);
     });
   }
   const int grid = grid_for(args.M, args.N, sms);
