@@ -41,7 +41,16 @@ DEFAULT_WORKLOAD = "gpt3_13b"
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by kernel name, with
 # the SHA-256 of the kernel source the capture was taken on.  Reported as
 # null once the source has changed.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # GPT-3-13B-shaped step (T=8192, h=5120, f=20480, t=8), CTA-pair kernel
+    # with TMA-store epilogue; see profiles/gemm_tc2_dram_gpt3_13b.md.
+    "gemm_dh_gelu_bwd": {"bytes": 1812.1e6, "src": "723cfc1bae55725c"},
+    "gemm1_gelu": {"bytes": 1820.1e6, "src": "723cfc1bae55725c"},
+    "gemm_wgrad_dA": {"bytes": 2315.9e6, "src": "723cfc1bae55725c"},
+    "gemm_wgrad_dB": {"bytes": 2500.1e6, "src": "723cfc1bae55725c"},
+    "gemm2_shardsum": {"bytes": 2239.8e6, "src": "723cfc1bae55725c"},
+    "gemm_dx_shardsum": {"bytes": 2240.6e6, "src": "723cfc1bae55725c"},
+}
 
 
 def _peaks():
@@ -55,16 +64,20 @@ def _peaks():
 
 
 def _src_sha():
-    path = os.path.join(ROOT, "tensor_transformer_mlp_tcgen05_gb300", "csrc",
-                        "gemm_tc.cu")
-    with open(path, "rb") as fh:
-        return hashlib.sha256(fh.read()).hexdigest()[:16]
+    """Hash of the GEMM kernel sources the traffic figures depend on."""
+    h = hashlib.sha256()
+    for name in ("gemm_tc2.cu", "gemm_common.cuh", "ptx.cuh"):
+        path = os.path.join(ROOT, "tensor_transformer_mlp_tcgen05_gb300",
+                            "csrc", name)
+        with open(path, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
 
 
 # ------------------------------------------------------------ clocks ----
 
 class ClockSampler:
-    """nvidia-smi sampling every 200 ms while the timed region runs."""
+    """nvidia-smi sampling every 100 ms while the timed region runs."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,"
               "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
@@ -81,7 +94,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             threading.Thread(target=self._read, daemon=True).start()
         except OSError:
@@ -99,7 +112,7 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        sm, mx, reasons = [], [], set()
+        sm, mx, pw, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
                  "sw_power_cap"]
         for ln in self.lines:
@@ -109,6 +122,7 @@ class ClockSampler:
             try:
                 sm.append(float(parts[1]))
                 mx.append(float(parts[2]))
+                pw.append(float(parts[3]))
             except ValueError:
                 continue
             for n, v in zip(names, parts[5:9]):
@@ -117,6 +131,7 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "power_w_max": max(pw) if pw else None,
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
@@ -214,7 +229,7 @@ def run_ours(args, w, rank, world, local_rank):
     Bn.tp_mlp_timing_reset(m.handle)
     sampler = ClockSampler(local_rank)
     sampler.start()
-    time.sleep(0.3)
+    time.sleep(0.25)
     barrier(world)
     torch.cuda.synchronize()
     n0 = Bn.tp_mlp_launch_count(m.handle)
@@ -370,8 +385,8 @@ def run_reference(args, w):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--tokens", type=int, default=None)
