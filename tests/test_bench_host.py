@@ -1,0 +1,75 @@
+"""Host-side logic of bench.py that needs no GPU: the max-over-ranks timing
+reduction of the replica mode (world size 2, gloo), the clock-sample parser
+and the oracle slice sizing."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port),
+                      RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    bench.barrier(world)
+    q.put((rank, bench.max_over_ranks(1.5 + rank, world)))
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_world2():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    got = dict(q.get(timeout=10) for _ in range(2))
+    assert got == {0: 2.5, 1: 2.5}
+
+
+def test_max_over_ranks_single_process_is_identity():
+    assert bench.max_over_ranks(3.25, 1) == 3.25
+
+
+def test_clock_sampler_parses_nvidia_smi_lines():
+    s = bench.ClockSampler(0)
+    s.lines = [
+        "0, 1650, 2070, 1361.2, 0x4, Not Active, Not Active, Not Active, Active",
+        "0, 1605, 2070, 1370.0, 0x4, Not Active, Not Active, Not Active, Active",
+        "garbage",
+    ]
+
+    class FinishedProcess:  # stand-in for the nvidia-smi child process
+        def terminate(self):
+            pass
+
+        def wait(self, timeout=None):
+            return 0
+
+    s.proc = FinishedProcess()
+    out = s.stop()
+    assert out["sm_mhz"] == pytest.approx(1627.5)
+    assert out["sm_max_mhz"] == 2070
+    assert out["reasons"] == ["sw_power_cap"]
+    assert out["samples"] == 2
+
+
+def test_oracle_slice_is_bounded():
+    from tensor_transformer_mlp_tcgen05_gb300 import workloads as W
+    for name, w in W.WORKLOADS.items():
+        n = bench.oracle_tokens(w)
+        assert 16 <= n <= max(16, w.tokens)
+        assert (12 if w.backward else 4) * n * w.hidden * w.ffn <= 1.6e12

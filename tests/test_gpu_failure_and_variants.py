@@ -1,0 +1,64 @@
+"""Bounded-wait failure reporting and the one-CTA GEMM variant, on the GPU.
+
+The timeout test makes every bounded wait inside the GEMM kernels give up at
+once (a 1 ns budget): the kernels must return on their own, report
+TPMLP_ERR_TIMEOUT through the status word, and leave the CUDA context usable
+(a normal call afterwards still matches the oracle).  Nothing here faults,
+traps or hangs the GPU: every wait, including the teardown ones, is bounded.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+import torch
+
+from tensor_transformer_mlp_tcgen05_gb300 import binding as B
+from tensor_transformer_mlp_tcgen05_gb300 import workloads as W
+from tensor_transformer_mlp_tcgen05_gb300.mlp import TensorParallelMLP
+
+from parity_helpers import assert_close, oracle_full, to_dev
+
+pytestmark = pytest.mark.gpu
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_wait_timeout_is_reported_and_context_survives():
+    w = W.Workload("timeout", 1024, 256, 2048, 2, "bf16", False, True)
+    inp = W.make_inputs(w, seed=31)
+    d = {k: to_dev(v) for k, v in inp.items()}
+    m = TensorParallelMLP(w.hidden, w.ffn, w.shards, w.tokens)
+    B.tp_mlp_set_wait_budget(m.handle, 1)
+    m.forward(d["X"], d["A"], d["B"])
+    rc = m.check()
+    assert rc == B.TPMLP_ERR_TIMEOUT, (rc, B.tp_mlp_last_detail())
+    assert "role" in B.tp_mlp_last_detail()
+    # The status word is cleared by the check; with the default budget the
+    # same handle and context compute the right answer again.
+    B.tp_mlp_set_wait_budget(m.handle, 2_000_000_000)
+    Z = m.forward(d["X"], d["A"], d["B"])
+    assert m.check() == B.TPMLP_OK
+    assert_close("Z after timeout", Z.cpu(), oracle_full(inp, backward=False)["Z"])
+    m.close()
+
+
+_SINGLE_SCRIPT = r"""
+import sys
+sys.path.insert(0, {root!r}); sys.path.insert(0, {tests!r})
+from tensor_transformer_mlp_tcgen05_gb300 import workloads as W
+from parity_helpers import run_cuda, oracle_full, compare_full
+for (T, h, f, t, ln) in [(300, 256, 1024, 2, True), (513, 192, 768, 4, False)]:
+    w = W.Workload("single", T, h, f, t, "bf16", ln, True)
+    inp = W.make_inputs(w, seed=41, with_bias=True)
+    compare_full(run_cuda(w, inp), oracle_full(inp))
+print("single-cta ok")
+"""
+
+
+def test_one_cta_gemm_variant_matches_oracle():
+    env = dict(os.environ, TPMLP_GEMM_VARIANT="single")
+    script = _SINGLE_SCRIPT.format(root=ROOT, tests=os.path.join(ROOT, "tests"))
+    r = subprocess.run([sys.executable, "-c", script], env=env,
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]
+    assert "single-cta ok" in r.stdout
