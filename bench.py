@@ -382,6 +382,51 @@ def run_reference(args, w):
     }
 
 
+def run_sweep(args):
+    """BLOOM-shaped token x shard sweep: one JSON line per point (not the
+    headline; each point times `steps` fwd+bwd steps after `warmup`)."""
+    import torch
+    from tensor_transformer_mlp_tcgen05_gb300 import workloads as W
+    from tensor_transformer_mlp_tcgen05_gb300.mlp import TensorParallelMLP
+    base = W.WORKLOADS[args.workload]
+    tmax = max(W.BLOOM_SWEEP_TOKENS)
+    inp = W.make_inputs(base.with_(tokens=tmax), seed=0)
+    d = {k: (None if v is None else v.cuda()) for k, v in inp.items()}
+    peak_b = _peaks()[0]
+    for t in W.BLOOM_SWEEP_SHARDS:
+        for T in W.BLOOM_SWEEP_TOKENS:
+            w = base.with_(tokens=T, shards=t)
+            m = TensorParallelMLP(w.hidden, w.ffn, t, T)
+            X, dZ = d["X"][:T], d["dZ"][:T]
+            g = {}
+
+            def step():
+                m.forward(X, d["A"], d["B"])
+                m.backward(dZ, X, d["A"], d["B"], out=g)
+
+            for _ in range(args.warmup):
+                step()
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(args.steps):
+                step()
+            e1.record()
+            torch.cuda.synchronize()
+            if m.check() != 0:
+                raise RuntimeError("device status in sweep")
+            ms = e0.elapsed_time(e1) / args.steps
+            tf = w.flops_fwd_bwd() / (ms * 1e-3) / 1e12
+            print(json.dumps({"sweep": w.name, "tokens": T, "shards": t,
+                              "ms_per_step": round(ms, 4),
+                              "value": round(tf, 1), "unit": "TFLOP/s",
+                              "frac_of_peak": round(tf / peak_b, 4)}),
+                  flush=True)
+            m.close()
+            del g
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -392,6 +437,9 @@ def main(argv=None):
     ap.add_argument("--tokens", type=int, default=None)
     ap.add_argument("--shards", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="token x shard sweep of the workload (one line per "
+                         "point) instead of the headline measurement")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -407,6 +455,12 @@ def main(argv=None):
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args, w)), flush=True)
+        return 0
+
+    if args.sweep:
+        from tensor_transformer_mlp_tcgen05_gb300 import build as b
+        b.build()
+        run_sweep(args)
         return 0
 
     if world > 1:
