@@ -20,7 +20,8 @@ What it computes, and where each piece comes from:
 * Same explainer, section "Fixing BERT: reordering layer normalisation for
   scaling", and the notes' section "Changing the placement of layer
   normalisation (BERT scaling)": LayerNorm is applied to the input of the
-  sub-block (pre-LN).
+  sub-block (pre-LN) and the residual path carries the raw input, added
+  linearly: the whole sub-block is X + MLP(LN(X)) (``residual=True``).
 
 Readings where the pages are silent (each is listed in the design notes):
 
@@ -122,9 +123,10 @@ def layernorm_backward(dXn, X, mean, rstd, gamma):
 # ------------------------------------------------- unsharded MLP block ----
 
 def forward(X, A, B, b1=None, b2=None, gamma=None, beta=None, eps=1e-5,
-            mode="erf"):
+            mode="erf", residual=False):
     """Unsharded block: Xn = LN(X) or X; H = Xn A + b1; Y = GeLU(H);
-    Z = Y B + b2.  Returns a dict with Xn, mean, rstd, H, Y, Z (fp64)."""
+    Z = Y B + b2 (+ X with the residual connection).  Returns a dict with
+    Xn, mean, rstd, H, Y, Z (fp64)."""
     X, A, B = _f64(X), _f64(A), _f64(B)
     mean = rstd = None
     if gamma is not None:
@@ -138,15 +140,18 @@ def forward(X, A, B, b1=None, b2=None, gamma=None, beta=None, eps=1e-5,
     Z = Y @ B
     if b2 is not None:
         Z = Z + _f64(b2)[None, :]
+    if residual:
+        Z = Z + X
     return dict(Xn=Xn, mean=mean, rstd=rstd, H=H, Y=Y, Z=Z)
 
 
-def backward(dZ, X, A, B, fwd, gamma=None, mode="erf"):
+def backward(dZ, X, A, B, fwd, gamma=None, mode="erf", residual=False):
     """Analytic gradients of the unsharded block given dZ = dL/dZ.
 
     db2 = sum_T dZ; dB = Y^T dZ; dY = dZ B^T; dH = dY * GeLU'(H);
     db1 = sum_T dH; dA = Xn^T dH; dXn = dH A^T; dX = LN-backward(dXn) (or
-    dXn without LayerNorm), with dgamma and dbeta.
+    dXn without LayerNorm), with dgamma and dbeta; the residual connection
+    adds dZ to dX.
     """
     dZ, X, A, B = _f64(dZ), _f64(X), _f64(A), _f64(B)
     db2 = dZ.sum(axis=0)
@@ -162,6 +167,8 @@ def backward(dZ, X, A, B, fwd, gamma=None, mode="erf"):
                                                fwd["rstd"], gamma)
     else:
         dX = dXn
+    if residual:
+        dX = dX + dZ
     return dict(dX=dX, dA=dA, dB=dB, db1=db1, db2=db2, dgamma=dgamma,
                 dbeta=dbeta, dH=dH, dXn=dXn)
 
@@ -184,7 +191,7 @@ def _f_backward(partials):
 
 
 def forward_sharded(X, A, B, t, b1=None, b2=None, gamma=None, beta=None,
-                    eps=1e-5, mode="erf"):
+                    eps=1e-5, mode="erf", residual=False):
     """The block as t column/row shards joined by f and g.
 
     Shard i owns columns [i f/t, (i+1) f/t) of A (and of b1) and the same
@@ -213,10 +220,13 @@ def forward_sharded(X, A, B, t, b1=None, b2=None, gamma=None, beta=None,
     Z = _g_forward(Zs)
     if b2 is not None:
         Z = Z + _f64(b2)[None, :]
+    if residual:
+        Z = Z + X                               # outside the parallel region
     return dict(Xn=Xn, mean=mean, rstd=rstd, H=Hs, Y=Ys, Z_parts=Zs, Z=Z)
 
 
-def backward_sharded(dZ, X, A, B, t, fwd_sh, gamma=None, mode="erf"):
+def backward_sharded(dZ, X, A, B, t, fwd_sh, gamma=None, mode="erf",
+                     residual=False):
     """Backward of ``forward_sharded``: g passes dZ unchanged to every shard;
     each shard forms its own dA_i, dB_i, db1_i and dXn_i; f sums the dXn_i."""
     dZ, X, A, B = _f64(dZ), _f64(X), _f64(A), _f64(B)
@@ -238,6 +248,8 @@ def backward_sharded(dZ, X, A, B, t, fwd_sh, gamma=None, mode="erf"):
                                                fwd_sh["rstd"], gamma)
     else:
         dX = dXn
+    if residual:
+        dX = dX + dZ
     return dict(dX=dX, dA=np.concatenate(dA_parts, axis=1),
                 dB=np.concatenate(dB_parts, axis=0),
                 db1=np.concatenate(db1_parts), db2=dZ.sum(axis=0),
@@ -256,7 +268,7 @@ def _normalized(X, gamma, beta, eps, rows=None):
 
 
 def forward_rows(X, A, B, rows, b1=None, b2=None, gamma=None, beta=None,
-                 eps=1e-5, mode="erf"):
+                 eps=1e-5, mode="erf", residual=False):
     """Z[rows, :] (each token row depends only on its own input row)."""
     Xn = _normalized(X, gamma, beta, eps, rows)
     H = Xn @ _f64(A)
@@ -265,6 +277,8 @@ def forward_rows(X, A, B, rows, b1=None, b2=None, gamma=None, beta=None,
     Z = gelu(H, mode) @ _f64(B)
     if b2 is not None:
         Z = Z + _f64(b2)[None, :]
+    if residual:
+        Z = Z + _f64(X)[rows]
     return Z
 
 

@@ -96,7 +96,7 @@ def test_layernorm_output_moments():
 
 # ------------------------------------------------ brute force forward ----
 
-def _brute_forward(X, A, B, b1, b2, gamma, beta, eps, mode):
+def _brute_forward(X, A, B, b1, b2, gamma, beta, eps, mode, residual=False):
     """Per-element loops with math.erf / math.tanh; no numpy, no helpers
     from the oracle."""
     T, h = len(X), len(X[0])
@@ -125,42 +125,49 @@ def _brute_forward(X, A, B, b1, b2, gamma, beta, eps, mode):
         if b2 is not None:
             for c in range(h):
                 Z[r][c] += b2[c]
+        if residual:
+            for c in range(h):
+                Z[r][c] += X[r][c]
     return np.array(Z)
 
 
-@pytest.mark.parametrize("ln,bias,mode", [(False, False, "erf"),
-                                          (True, True, "erf"),
-                                          (True, False, "tanh"),
-                                          (False, True, "tanh")])
-def test_forward_matches_brute_force(ln, bias, mode):
+@pytest.mark.parametrize("ln,bias,mode,res", [(False, False, "erf", False),
+                                              (True, True, "erf", False),
+                                              (True, False, "tanh", False),
+                                              (False, True, "tanh", False),
+                                              (True, True, "erf", True),
+                                              (False, False, "tanh", True)])
+def test_forward_matches_brute_force(ln, bias, mode, res):
     p = _problem(seed=3, T=3, h=5, f=7, ln=ln, bias=bias)
     got = O.forward(p["X"], p["A"], p["B"], p["b1"], p["b2"], p["gamma"],
-                    p["beta"], eps=1e-5, mode=mode)["Z"]
+                    p["beta"], eps=1e-5, mode=mode, residual=res)["Z"]
     want = _brute_forward(p["X"].tolist(), p["A"].tolist(), p["B"].tolist(),
                           None if p["b1"] is None else p["b1"].tolist(),
                           None if p["b2"] is None else p["b2"].tolist(),
                           None if p["gamma"] is None else p["gamma"].tolist(),
                           None if p["beta"] is None else p["beta"].tolist(),
-                          1e-5, mode)
+                          1e-5, mode, res)
     np.testing.assert_allclose(got, want, rtol=1e-13, atol=1e-14)
 
 
 # ------------------------------------------- gradients: finite diffs ----
 
-def _loss(p, mode):
+def _loss(p, mode, res=False):
     z = O.forward(p["X"], p["A"], p["B"], p["b1"], p["b2"], p["gamma"],
-                  p["beta"], eps=1e-5, mode=mode)["Z"]
+                  p["beta"], eps=1e-5, mode=mode, residual=res)["Z"]
     return float((z * p["dZ"]).sum())
 
 
-@pytest.mark.parametrize("mode", ["erf", "tanh"])
+@pytest.mark.parametrize("mode,res", [("erf", False), ("tanh", False),
+                                      ("erf", True)])
 @pytest.mark.parametrize("ln", [False, True])
-def test_backward_matches_central_differences(mode, ln):
+def test_backward_matches_central_differences(mode, ln, res):
     """Every gradient entry of L = sum(Z * dZ) against central differences."""
     p = _problem(seed=5, T=3, h=4, f=8, ln=ln, bias=True)
     fwd = O.forward(p["X"], p["A"], p["B"], p["b1"], p["b2"], p["gamma"],
-                    p["beta"], eps=1e-5, mode=mode)
-    g = O.backward(p["dZ"], p["X"], p["A"], p["B"], fwd, p["gamma"], mode)
+                    p["beta"], eps=1e-5, mode=mode, residual=res)
+    g = O.backward(p["dZ"], p["X"], p["A"], p["B"], fwd, p["gamma"], mode,
+                   residual=res)
     names = {"X": "dX", "A": "dA", "B": "dB", "b1": "db1", "b2": "db2"}
     if ln:
         names.update(gamma="dgamma", beta="dbeta")
@@ -171,9 +178,9 @@ def test_backward_matches_central_differences(mode, ln):
             step = 1e-5 * max(1.0, abs(base[idx]))
             keep = base[idx]
             base[idx] = keep + step
-            lp = _loss(p, mode)
+            lp = _loss(p, mode, res)
             base[idx] = keep - step
-            lm = _loss(p, mode)
+            lm = _loss(p, mode, res)
             base[idx] = keep
             fd[idx] = (lp - lm) / (2 * step)
         scale = max(1.0, np.abs(fd).max())
@@ -184,20 +191,21 @@ def test_backward_matches_central_differences(mode, ln):
 # ------------------------------------ the pages' shard identity (f/g) ----
 
 @pytest.mark.parametrize("t", [1, 2, 4, 8])
-@pytest.mark.parametrize("ln,bias", [(False, False), (True, True)])
-def test_shard_identity_forward_and_backward(t, ln, bias):
+@pytest.mark.parametrize("ln,bias,res", [(False, False, False), (True, True, False),
+                                         (True, True, True)])
+def test_shard_identity_forward_and_backward(t, ln, bias, res):
     """sum_i GeLU(X A_i) B_i = GeLU(X A) B, and the f/g backward (dZ to
     every shard, dX = sum_i dX_i) gives the unsharded gradients."""
     p = _problem(seed=11, T=6, h=8, f=32, ln=ln, bias=bias)
     args = (p["X"], p["A"], p["B"])
     full = O.forward(*args, b1=p["b1"], b2=p["b2"], gamma=p["gamma"],
-                     beta=p["beta"])
+                     beta=p["beta"], residual=res)
     sh = O.forward_sharded(*args, t, b1=p["b1"], b2=p["b2"], gamma=p["gamma"],
-                           beta=p["beta"])
+                           beta=p["beta"], residual=res)
     assert len(sh["Z_parts"]) == t
     np.testing.assert_allclose(sh["Z"], full["Z"], rtol=1e-12, atol=1e-13)
-    gf = O.backward(p["dZ"], *args, full, p["gamma"])
-    gs = O.backward_sharded(p["dZ"], *args, t, sh, p["gamma"])
+    gf = O.backward(p["dZ"], *args, full, p["gamma"], residual=res)
+    gs = O.backward_sharded(p["dZ"], *args, t, sh, p["gamma"], residual=res)
     assert len(gs["dXn_parts"]) == t
     for k in ("dX", "dA", "dB", "db1", "db2") + (("dgamma", "dbeta") if ln else ()):
         np.testing.assert_allclose(gs[k], gf[k], rtol=1e-12, atol=1e-13, err_msg=k)
@@ -235,6 +243,17 @@ def test_zero_first_weight():
     assert np.all(g["dX"] == 0) and np.all(g["dB"] == 0)
     np.testing.assert_allclose(g["dA"], 0.5 * p["X"].T @ p["dZ"] @ p["B"].T,
                                rtol=1e-14, atol=1e-15)
+
+
+def test_zero_first_weight_with_residual_is_identity_plus_bias():
+    """Residual sub-block with A = 0 (no b1): Z = X + b2 and dX = dZ."""
+    p = _problem(seed=7, T=4, h=4, f=8, ln=True, bias=True)
+    A0 = np.zeros_like(p["A"])
+    fwd = O.forward(p["X"], A0, p["B"], None, p["b2"], p["gamma"], p["beta"],
+                    residual=True)
+    np.testing.assert_array_equal(fwd["Z"], p["X"] + p["b2"][None, :])
+    g = O.backward(p["dZ"], p["X"], A0, p["B"], fwd, p["gamma"], residual=True)
+    np.testing.assert_array_equal(g["dX"], p["dZ"])
 
 
 def test_empty_token_set():
