@@ -195,7 +195,7 @@ def run_ours(args, w, rank, world, local_rank):
     inp = W.make_inputs(w, seed=0)
     d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
     m = TensorParallelMLP(w.hidden, w.ffn, w.shards, w.tokens, dtype=w.dtype,
-                          layernorm=w.layernorm)
+                          layernorm=w.layernorm, residual=args.residual)
     stream = torch.cuda.current_stream()
     T = w.tokens
     Z = torch.empty((T, w.hidden), dtype=w.torch_dtype, device=dev)
@@ -322,6 +322,7 @@ def run_ours(args, w, rank, world, local_rank):
         "config": {"workload": w.name, "tokens": w.tokens, "batch": w.batch,
                    "seq": w.seq, "hidden": w.hidden, "ffn": w.ffn,
                    "shards": w.shards, "layernorm": w.layernorm,
+                   "residual": bool(args.residual),
                    "pass": "fwd+bwd" if w.backward else "fwd",
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "l2": "inputs larger than L2 (no flush)"},
@@ -437,6 +438,8 @@ def main(argv=None):
     ap.add_argument("--tokens", type=int, default=None)
     ap.add_argument("--shards", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--residual", action="store_true",
+                    help="time the residual sub-block X + MLP(LN(X))")
     ap.add_argument("--sweep", action="store_true",
                     help="token x shard sweep of the workload (one line per "
                          "point) instead of the headline measurement")

@@ -11,6 +11,10 @@
  *                                    normalisation for scaling")
  *     Y_i = GeLU(Xn A_i + b1_i)     A = [A_1 .. A_t] split by columns
  *     Z   = sum_{i=0}^{t-1} Y_i B_i + b2    B split by rows into B_i
+ *     [Z += X]                      optional residual connection: the whole
+ *                                   pre-LN sub-block X + MLP(LN(X)) (same
+ *                                   explainer section on pre-LN: the residual
+ *                                   path carries the raw input)
  *
  * The t shards are logical: they run as independent tiles on one GPU.  The
  * operator g (explainer section "The f and g operators: two lines of code"),
@@ -79,6 +83,7 @@ typedef struct tp_mlp_config {
   int   use_layernorm;   /* 1: pre-LayerNorm on X before the first GEMM      */
   float ln_eps;          /* LayerNorm epsilon (added to the biased variance) */
   int   gelu_mode;       /* TPMLP_GELU_ERF or TPMLP_GELU_TANH                */
+  int   use_residual;    /* 1: Z = X + MLP(...), added before the rounding  */
 } tp_mlp_config;
 
 typedef struct tp_mlp_handle tp_mlp_handle;
@@ -124,7 +129,8 @@ int tp_mlp_forward(tp_mlp_handle* handle, int tokens, const void* X,
  * sum of the per-shard input gradients, here in fixed shard order):
  *   dB_i = Y_i^T dZ;  db2 = sum_T dZ;  dH_i = (dZ B_i^T) * GeLU'(H_i);
  *   db1_i = sum_T dH_i;  dA_i = Xn^T dH_i;  dXn = sum_{i=0}^{t-1} dH_i A_i^T;
- *   dX = LayerNorm-backward(dXn) (or dXn), dgamma, dbeta.
+ *   dX = LayerNorm-backward(dXn) (or dXn) [+ dZ with the residual],
+ *   dgamma, dbeta.
  *   dZ [T,h] (dtype); X, A, B, ln_gamma as passed to the forward call.
  *   workspace   the forward call's workspace (training = 1), unchanged.
  *   dX [T,h] (dtype); dA [h,f], dB [f,h] fp32; all overwritten.

@@ -46,7 +46,8 @@ class tp_mlp_config(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int), ("ffn", ctypes.c_int),
                 ("shards", ctypes.c_int), ("max_tokens", ctypes.c_int),
                 ("dtype", ctypes.c_int), ("use_layernorm", ctypes.c_int),
-                ("ln_eps", ctypes.c_float), ("gelu_mode", ctypes.c_int)]
+                ("ln_eps", ctypes.c_float), ("gelu_mode", ctypes.c_int),
+                ("use_residual", ctypes.c_int)]
 
 
 class TPMLPError(RuntimeError):

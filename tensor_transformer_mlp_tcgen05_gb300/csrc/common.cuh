@@ -35,7 +35,8 @@ struct GemmArgs {
   void* out;              // [M, N] row-major, leading dimension ldo
   long long ldo;
   void* out2;             // EPI_GELU_FWD: H (nullable)
-  const void* aux;        // EPI_GELU_BWD: H, leading dimension ldaux
+  const void* aux;        // EPI_GELU_BWD: H; EPI_SHARDSUM: residual added
+                          // before the rounding (nullable); leading dim ldaux
   long long ldaux;
   const float* bias;      // [N] fp32 (nullable)
   int* status;            // device status word: [0] code, [1] role, [2] block

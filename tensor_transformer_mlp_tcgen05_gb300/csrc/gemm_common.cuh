@@ -90,6 +90,28 @@ __device__ __forceinline__ void add_bias32(const float* bias, int c0,
   }
 }
 
+// Add n bf16 values of a residual row (row, c0 .. c0+n) to v (n % 8 == 0).
+__device__ __forceinline__ void add_residual_bf16(const void* res, long long ld,
+                                                  int row, int M, int c0,
+                                                  float* v, int n) {
+  if (res == nullptr || row >= M) return;
+  const uint4* p = reinterpret_cast<const uint4*>(
+      static_cast<const __nv_bfloat16*>(res) + static_cast<size_t>(row) * ld +
+      c0);
+#pragma unroll
+  for (int i = 0; i < n / 8; ++i) {
+    const uint4 u = p[i];
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float a, b;
+      unpack_bf16x2(w[k], a, b);
+      v[8 * i + 2 * k] += a;
+      v[8 * i + 2 * k + 1] += b;
+    }
+  }
+}
+
 // Epilogue of one 32-column chunk of one row (non-shard-sum epilogues).
 template <int EPI>
 __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, int row,

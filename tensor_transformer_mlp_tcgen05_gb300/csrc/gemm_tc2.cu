@@ -405,6 +405,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               const int c0 = col_base + j * 64;
               if (c0 < args.N) {
                 add_bias_n(args.bias, c0, &S[j * 64], 64);
+                add_residual_bf16(args.aux, args.ldaux, row, args.M, c0,
+                                  &S[j * 64], 64);
                 uint32_t w[32];
                 pack_bf16x64(&S[j * 64], w);
                 st.put(&tmO, c0, row0, w, lane);

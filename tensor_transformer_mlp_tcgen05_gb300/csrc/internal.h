@@ -52,11 +52,12 @@ cudaError_t launch_ln_fwd(bool bf16, const void* X, const float* gamma,
                           float* rstd, int rows, int h, float eps,
                           cudaStream_t stream);
 
-// LayerNorm backward for dX given dXn (fp32).
+// LayerNorm backward for dX given dXn (fp32); dres (nullable, element type
+// of X) is added to dX (the residual connection's gradient).
 cudaError_t launch_ln_bwd(bool bf16, const float* dXn, const void* X,
                           const float* mean, const float* rstd,
-                          const float* gamma, void* dX, int rows, int h,
-                          cudaStream_t stream);
+                          const float* gamma, const void* dres, void* dX,
+                          int rows, int h, cudaStream_t stream);
 
 // Rows per chunk of the two-stage fixed-order column sums.
 constexpr int COLSUM_CHUNK_ROWS = 256;

@@ -118,13 +118,13 @@ __global__ void __launch_bounds__(LN_WARPS * 32)
   }
 }
 
-// dX = rstd * (g - mean(g) - xhat * mean(g * xhat)), g = gamma * dXn.
+// dX = rstd * (g - mean(g) - xhat * mean(g * xhat)) [+ dres], g = gamma * dXn.
 template <typename T>
 __global__ void __launch_bounds__(LN_WARPS * 32)
     ln_bwd_kernel(const float* __restrict__ dXn, const T* __restrict__ X,
                   const float* __restrict__ mean, const float* __restrict__ rstd,
-                  const float* __restrict__ gamma, T* __restrict__ dX, int rows,
-                  int h) {
+                  const float* __restrict__ gamma, const T* __restrict__ dres,
+                  T* __restrict__ dX, int rows, int h) {
   constexpr int V = Vec<T>::N;
   const int row = blockIdx.x * LN_WARPS + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -157,6 +157,12 @@ __global__ void __launch_bounds__(LN_WARPS * 32)
     for (int k = 0; k < V; ++k) {
       const float xhat = (x[k] - mu) * rs;
       o[k] = rs * (g[k] * d[k] - c_g - xhat * c_gx);
+    }
+    if (dres != nullptr) {
+      float r[V];
+      Vec<T>::load(dres + base + i * V, r);
+#pragma unroll
+      for (int k = 0; k < V; ++k) o[k] += r[k];
     }
     Vec<T>::store(dX + base + i * V, o);
   }
@@ -273,17 +279,18 @@ cudaError_t launch_ln_fwd(bool bf16, const void* X, const float* gamma,
 
 cudaError_t launch_ln_bwd(bool bf16, const float* dXn, const void* X,
                           const float* mean, const float* rstd,
-                          const float* gamma, void* dX, int rows, int h,
-                          cudaStream_t stream) {
+                          const float* gamma, const void* dres, void* dX,
+                          int rows, int h, cudaStream_t stream) {
   const int grid = (rows + LN_WARPS - 1) / LN_WARPS;
   if (bf16) {
     ln_bwd_kernel<__nv_bfloat16><<<grid, LN_WARPS * 32, 0, stream>>>(
         dXn, static_cast<const __nv_bfloat16*>(X), mean, rstd, gamma,
+        static_cast<const __nv_bfloat16*>(dres),
         static_cast<__nv_bfloat16*>(dX), rows, h);
   } else {
     ln_bwd_kernel<float><<<grid, LN_WARPS * 32, 0, stream>>>(
         dXn, static_cast<const float*>(X), mean, rstd, gamma,
-        static_cast<float*>(dX), rows, h);
+        static_cast<const float*>(dres), static_cast<float*>(dX), rows, h);
   }
   return cudaGetLastError();
 }

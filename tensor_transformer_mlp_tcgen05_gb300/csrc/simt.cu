@@ -52,9 +52,14 @@ __global__ void __launch_bounds__(TS* TS)
       out[off] = gelu_f32(h, a.gelu_mode);
       break;
     }
-    case EPI_SHARDSUM:
-      out[off] = total + (a.bias ? a.bias[n] : 0.f);
+    case EPI_SHARDSUM: {
+      float v = total + (a.bias ? a.bias[n] : 0.f);
+      if (a.aux) {
+        v += static_cast<const float*>(a.aux)[static_cast<size_t>(m) * a.ldaux + n];
+      }
+      out[off] = v;
       break;
+    }
     case EPI_GELU_BWD: {
       const float h = static_cast<const float*>(
           a.aux)[static_cast<size_t>(m) * a.ldaux + n];

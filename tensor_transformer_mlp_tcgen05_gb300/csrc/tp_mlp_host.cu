@@ -355,6 +355,7 @@ int tp_mlp_create(const tp_mlp_config* cfg, tp_mlp_handle** out) {
   if (cfg->gelu_mode != TPMLP_GELU_ERF && cfg->gelu_mode != TPMLP_GELU_TANH)
     return TPMLP_ERR_ARG;
   if (cfg->use_layernorm != 0 && cfg->use_layernorm != 1) return TPMLP_ERR_ARG;
+  if (cfg->use_residual != 0 && cfg->use_residual != 1) return TPMLP_ERR_ARG;
   if (cfg->use_layernorm &&
       !(cfg->ln_eps >= 0.f && std::isfinite(cfg->ln_eps)))
     return TPMLP_ERR_ARG;
@@ -441,6 +442,10 @@ int tp_mlp_forward(tp_mlp_handle* H, int tokens, const void* X, const void* A,
   GemmArgs g2 = base_args(H, ws, L);
   g2.M = T; g2.N = h; g2.K = f; g2.num_seg = t;
   g2.out = Z; g2.ldo = h; g2.bias = bias2;
+  if (c.use_residual) {  // Z += X (the raw input), before the one rounding
+    g2.aux = X;
+    g2.ldaux = h;
+  }
 
   if (bf16) {
     CUtensorMap ta, tb;
@@ -537,6 +542,12 @@ int tp_mlp_backward(tp_mlp_handle* H, int tokens, const void* dZ,
   GemmArgs gx = base_args(H, ws, L);  // dXn = sum_i dH_i A_i^T
   gx.M = T; gx.N = h; gx.K = f; gx.num_seg = t;
   gx.out = dXdst; gx.ldo = h; gx.out_f32 = (ln || !bf16) ? 1 : 0;
+  if (c.use_residual && !ln) {  // dX = dXn + dZ in the GEMM epilogue
+    gx.aux = dZ;
+    gx.ldaux = h;
+  }
+  // With LayerNorm the residual gradient is added by the LN backward kernel.
+  const void* dres = (c.use_residual && ln) ? dZ : nullptr;
 
   if (bf16) {
     CUtensorMap ta, tb;
@@ -596,7 +607,8 @@ int tp_mlp_backward(tp_mlp_handle* H, int tokens, const void* dZ,
     const float* mean = reinterpret_cast<const float*>(ws + L.mean);
     const float* rstd = reinterpret_cast<const float*>(ws + L.rstd);
     TRY(run(H, "layernorm_bwd", s, [&] {
-      return launch_ln_bwd(bf16, dXn, X, mean, rstd, ln_gamma, dX, T, h, s);
+      return launch_ln_bwd(bf16, dXn, X, mean, rstd, ln_gamma, dres, dX, T, h,
+                           s);
     }));
     if (dgamma || dbeta) {
       float* pg = part + size_t(L.chunks) * (h + f);

@@ -10,16 +10,20 @@ from . import binding as B_
 
 
 class TensorParallelMLP:
-    """Megatron-style column/row-split MLP block with t logical shards."""
+    """Megatron-style column/row-split MLP block with t logical shards
+    (optionally the whole pre-LN sub-block X + MLP(LN(X)) with
+    ``layernorm=True, residual=True``)."""
 
     def __init__(self, hidden: int, ffn: int, shards: int, max_tokens: int,
                  dtype: str = "bf16", layernorm: bool = False,
-                 ln_eps: float = 1e-5, gelu: str = "erf", device=None):
+                 ln_eps: float = 1e-5, gelu: str = "erf", residual: bool = False,
+                 device=None):
         self.cfg = B_.tp_mlp_config(
             hidden=hidden, ffn=ffn, shards=shards, max_tokens=max_tokens,
             dtype=B_.TPMLP_BF16 if dtype == "bf16" else B_.TPMLP_FP32,
             use_layernorm=1 if layernorm else 0, ln_eps=ln_eps,
-            gelu_mode=B_.TPMLP_GELU_ERF if gelu == "erf" else B_.TPMLP_GELU_TANH)
+            gelu_mode=B_.TPMLP_GELU_ERF if gelu == "erf" else B_.TPMLP_GELU_TANH,
+            use_residual=1 if residual else 0)
         if dtype not in ("bf16", "fp32") or gelu not in ("erf", "tanh"):
             raise ValueError("dtype must be bf16|fp32 and gelu erf|tanh")
         self.handle = B_.tp_mlp_create(self.cfg)

@@ -48,11 +48,13 @@ def to_dev(x):
     return None if x is None else x.cuda().contiguous()
 
 
-def run_cuda(w, inp, backward=True, training=True, gelu="erf", repeat=1):
+def run_cuda(w, inp, backward=True, training=True, gelu="erf", repeat=1,
+             residual=False):
     """Forward (+ backward) on cuda:0 through the binding.  Returns a dict of
     CPU tensors; with repeat > 1 a list of such dicts (same inputs)."""
     m = TensorParallelMLP(w.hidden, w.ffn, w.shards, max(w.tokens, 1),
-                          dtype=w.dtype, layernorm=w.layernorm, gelu=gelu)
+                          dtype=w.dtype, layernorm=w.layernorm, gelu=gelu,
+                          residual=residual)
     d = {k: to_dev(v) for k, v in inp.items()}
     outs = []
     for _ in range(repeat):
@@ -70,13 +72,14 @@ def run_cuda(w, inp, backward=True, training=True, gelu="erf", repeat=1):
     return outs if repeat > 1 else outs[0]
 
 
-def oracle_full(inp, mode="erf", backward=True):
+def oracle_full(inp, mode="erf", backward=True, residual=False):
     X, A, B = f64(inp["X"]), f64(inp["A"]), f64(inp["B"])
     fwd = O.forward(X, A, B, f64(inp["b1"]), f64(inp["b2"]), f64(inp["gamma"]),
-                    f64(inp["beta"]), mode=mode)
+                    f64(inp["beta"]), mode=mode, residual=residual)
     out = {"Z": fwd["Z"]}
     if backward:
-        g = O.backward(f64(inp["dZ"]), X, A, B, fwd, f64(inp["gamma"]), mode)
+        g = O.backward(f64(inp["dZ"]), X, A, B, fwd, f64(inp["gamma"]), mode,
+                       residual=residual)
         out.update(dX=g["dX"], dA=g["dA"], dB=g["dB"], db1=g["db1"],
                    db2=g["db2"])
         if inp["gamma"] is not None:

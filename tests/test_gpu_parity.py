@@ -54,6 +54,31 @@ def test_small_bf16_block_full(T, h, f, t, ln, bias, gelu):
     compare_full(got, oracle_full(inp, mode=gelu))
 
 
+RESIDUAL_CASES = [
+    # T, h, f, t, ln, bias  (the pre-LN sub-block X + MLP(LN(X)) and the
+    # plain block with a residual)
+    (300, 256, 1024, 4, True, True),
+    (300, 256, 1024, 1, False, True),
+    (129, 320, 1280, 2, False, False),
+    (1000, 384, 1536, 3, True, False),
+]
+
+
+@pytest.mark.parametrize("T,h,f,t,ln,bias", RESIDUAL_CASES)
+def test_small_bf16_residual_subblock_full(T, h, f, t, ln, bias):
+    w = small(T, h, f, t, ln)
+    inp = W.make_inputs(w, seed=9, with_bias=bias)
+    got = run_cuda(w, inp, residual=True)
+    compare_full(got, oracle_full(inp, residual=True))
+
+
+def test_tiny_fp32_residual_block_full():
+    w = W.WORKLOADS["tiny_fp32"]
+    inp = W.make_inputs(w, seed=0, with_bias=True)
+    got = run_cuda(w, inp, residual=True)
+    compare_full(got, oracle_full(inp, residual=True), fp32=True)
+
+
 def test_small_fp32_layernorm_block_full():
     w = small(200, 128, 512, 4, ln=True, dtype="fp32")
     inp = W.make_inputs(w, seed=2, with_bias=True)
@@ -159,6 +184,17 @@ def test_megatron_8p3b_block_full():
     inp = W.make_inputs(w, seed=0)
     got = run_cuda(w, inp)
     compare_full(got, oracle_full(inp))
+
+
+def test_megatron_8p3b_pre_ln_subblock_full():
+    """The whole pre-LN sub-block X + MLP(LN(X)) at the 8.3B shape, in full,
+    and bitwise identical over two runs."""
+    w = W.WORKLOADS["megatron_8p3b"]
+    inp = W.make_inputs(w, seed=0)
+    r1, r2 = run_cuda(w, inp, residual=True, repeat=2)
+    for k in r1:
+        assert torch.equal(r1[k], r2[k]), k
+    compare_full(r1, oracle_full(inp, residual=True))
 
 
 def _sampled_check(w, inp, got, nrows, ncols, seed):
