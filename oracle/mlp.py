@@ -29,7 +29,14 @@ Readings where the pages are silent (each is listed in the design notes):
   Hendrycks & Gimpel (2016) is available as ``mode="tanh"``.
 * Biases: b1 [f] (split by columns with A) is added before GeLU; b2 [h] is
   added once, after the sum over shards.  Both are optional.
-* Dropout is the identity (p = 0); no workload uses it.
+* Dropout (``dropout=(p, seed, offset)``, training only) acts on the MLP's
+  output Y B + b2 before the residual add, outside the parallel region, so
+  its mask must not depend on the shard count (the notes' "Implementation
+  features": dropout seeds differ inside and outside the model-parallel
+  region).  Mask: element (r, c) is kept when word c % 4 of
+  Philox4x32-10(counter = (c // 4, r, offset_lo, offset_hi),
+  key = (seed_lo, seed_hi)) is >= floor(p 2^32); kept values are scaled by
+  1 / (1 - p).  No workload uses it (p = 0).
 * LayerNorm uses the biased variance over h and eps inside the square root.
 
 The method is an exact re-association of the unsharded block, so the
@@ -45,6 +52,8 @@ import math
 
 import numpy as np
 from scipy.special import erf as _erf
+
+from .philox import philox4x32_10
 
 _SQRT1_2 = 1.0 / math.sqrt(2.0)
 _INV_SQRT_2PI = 1.0 / math.sqrt(2.0 * math.pi)
@@ -120,13 +129,38 @@ def layernorm_backward(dXn, X, mean, rstd, gamma):
     return dX, (dXn * xhat).sum(axis=0), dXn.sum(axis=0)
 
 
+# ------------------------------------------------------------- dropout ----
+
+def dropout_threshold(p: float) -> int:
+    """Keep an element when its 32-bit draw is >= floor(p * 2^32)."""
+    return min(int(p * 4294967296.0), 0xFFFFFFFF)
+
+
+def dropout_mask(rows, cols, p, seed, offset=0):
+    """Boolean keep-mask for token rows `rows` (array) and `cols` columns."""
+    rows = np.asarray(rows, dtype=np.uint64)
+    c = np.arange(cols, dtype=np.uint64)
+    R, C = np.meshgrid(rows, c, indexing="ij")
+    words = philox4x32_10(C // np.uint64(4), R, offset & 0xFFFFFFFF,
+                          offset >> 32, seed & 0xFFFFFFFF, seed >> 32)
+    w = np.choose((C % np.uint64(4)).astype(np.int64), words)
+    return w >= np.uint32(dropout_threshold(p))
+
+
+def _apply_dropout(Zpre, dropout, rows=None):
+    p, seed, offset = dropout
+    rows = np.arange(Zpre.shape[0]) if rows is None else rows
+    mask = dropout_mask(rows, Zpre.shape[1], p, seed, offset)
+    return np.where(mask, Zpre / (1.0 - p), 0.0), mask
+
+
 # ------------------------------------------------- unsharded MLP block ----
 
 def forward(X, A, B, b1=None, b2=None, gamma=None, beta=None, eps=1e-5,
-            mode="erf", residual=False):
+            mode="erf", residual=False, dropout=None):
     """Unsharded block: Xn = LN(X) or X; H = Xn A + b1; Y = GeLU(H);
-    Z = Y B + b2 (+ X with the residual connection).  Returns a dict with
-    Xn, mean, rstd, H, Y, Z (fp64)."""
+    Z = Dropout(Y B + b2) (+ X with the residual connection).  Returns a dict
+    with Xn, mean, rstd, H, Y, Z (fp64) and the dropout mask (or None)."""
     X, A, B = _f64(X), _f64(A), _f64(B)
     mean = rstd = None
     if gamma is not None:
@@ -140,9 +174,13 @@ def forward(X, A, B, b1=None, b2=None, gamma=None, beta=None, eps=1e-5,
     Z = Y @ B
     if b2 is not None:
         Z = Z + _f64(b2)[None, :]
+    mask = None
+    if dropout is not None:
+        Z, mask = _apply_dropout(Z, dropout)
     if residual:
         Z = Z + X
-    return dict(Xn=Xn, mean=mean, rstd=rstd, H=H, Y=Y, Z=Z)
+    return dict(Xn=Xn, mean=mean, rstd=rstd, H=H, Y=Y, Z=Z, mask=mask,
+                dropout=dropout)
 
 
 def backward(dZ, X, A, B, fwd, gamma=None, mode="erf", residual=False):
@@ -154,6 +192,9 @@ def backward(dZ, X, A, B, fwd, gamma=None, mode="erf", residual=False):
     adds dZ to dX.
     """
     dZ, X, A, B = _f64(dZ), _f64(X), _f64(A), _f64(B)
+    dZr = dZ                                    # residual path: unmasked
+    if fwd.get("dropout") is not None:
+        dZ = np.where(fwd["mask"], dZ / (1.0 - fwd["dropout"][0]), 0.0)
     db2 = dZ.sum(axis=0)
     dB = fwd["Y"].T @ dZ
     dY = dZ @ B.T
@@ -168,7 +209,7 @@ def backward(dZ, X, A, B, fwd, gamma=None, mode="erf", residual=False):
     else:
         dX = dXn
     if residual:
-        dX = dX + dZ
+        dX = dX + dZr
     return dict(dX=dX, dA=dA, dB=dB, db1=db1, db2=db2, dgamma=dgamma,
                 dbeta=dbeta, dH=dH, dXn=dXn)
 
@@ -191,7 +232,7 @@ def _f_backward(partials):
 
 
 def forward_sharded(X, A, B, t, b1=None, b2=None, gamma=None, beta=None,
-                    eps=1e-5, mode="erf", residual=False):
+                    eps=1e-5, mode="erf", residual=False, dropout=None):
     """The block as t column/row shards joined by f and g.
 
     Shard i owns columns [i f/t, (i+1) f/t) of A (and of b1) and the same
@@ -220,9 +261,13 @@ def forward_sharded(X, A, B, t, b1=None, b2=None, gamma=None, beta=None,
     Z = _g_forward(Zs)
     if b2 is not None:
         Z = Z + _f64(b2)[None, :]
+    mask = None
+    if dropout is not None:                     # outside the parallel region
+        Z, mask = _apply_dropout(Z, dropout)
     if residual:
         Z = Z + X                               # outside the parallel region
-    return dict(Xn=Xn, mean=mean, rstd=rstd, H=Hs, Y=Ys, Z_parts=Zs, Z=Z)
+    return dict(Xn=Xn, mean=mean, rstd=rstd, H=Hs, Y=Ys, Z_parts=Zs, Z=Z,
+                mask=mask, dropout=dropout)
 
 
 def backward_sharded(dZ, X, A, B, t, fwd_sh, gamma=None, mode="erf",
@@ -231,6 +276,9 @@ def backward_sharded(dZ, X, A, B, t, fwd_sh, gamma=None, mode="erf",
     each shard forms its own dA_i, dB_i, db1_i and dXn_i; f sums the dXn_i."""
     dZ, X, A, B = _f64(dZ), _f64(X), _f64(A), _f64(B)
     ft = A.shape[1] // t
+    dZr = dZ
+    if fwd_sh.get("dropout") is not None:
+        dZ = np.where(fwd_sh["mask"], dZ / (1.0 - fwd_sh["dropout"][0]), 0.0)
     dz = dZ                                     # g: identity going backward
     dA_parts, dB_parts, db1_parts, dXn_parts = [], [], [], []
     for i in range(t):
@@ -249,7 +297,7 @@ def backward_sharded(dZ, X, A, B, t, fwd_sh, gamma=None, mode="erf",
     else:
         dX = dXn
     if residual:
-        dX = dX + dZ
+        dX = dX + dZr
     return dict(dX=dX, dA=np.concatenate(dA_parts, axis=1),
                 dB=np.concatenate(dB_parts, axis=0),
                 db1=np.concatenate(db1_parts), db2=dZ.sum(axis=0),
@@ -268,7 +316,7 @@ def _normalized(X, gamma, beta, eps, rows=None):
 
 
 def forward_rows(X, A, B, rows, b1=None, b2=None, gamma=None, beta=None,
-                 eps=1e-5, mode="erf", residual=False):
+                 eps=1e-5, mode="erf", residual=False, dropout=None):
     """Z[rows, :] (each token row depends only on its own input row)."""
     Xn = _normalized(X, gamma, beta, eps, rows)
     H = Xn @ _f64(A)
@@ -277,6 +325,8 @@ def forward_rows(X, A, B, rows, b1=None, b2=None, gamma=None, beta=None,
     Z = gelu(H, mode) @ _f64(B)
     if b2 is not None:
         Z = Z + _f64(b2)[None, :]
+    if dropout is not None:
+        Z, _ = _apply_dropout(Z, dropout, rows)
     if residual:
         Z = Z + _f64(X)[rows]
     return Z
