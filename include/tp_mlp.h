@@ -11,6 +11,8 @@
  *                                    normalisation for scaling")
  *     Y_i = GeLU(Xn A_i + b1_i)     A = [A_1 .. A_t] split by columns
  *     Z   = sum_{i=0}^{t-1} Y_i B_i + b2    B split by rows into B_i
+ *     Z   = Dropout(Z)              optional, training calls only (the pages'
+ *                                   Z = Dropout(YB)), before the residual
  *     [Z += X]                      optional residual connection: the whole
  *                                   pre-LN sub-block X + MLP(LN(X)) (same
  *                                   explainer section on pre-LN: the residual
@@ -84,6 +86,8 @@ typedef struct tp_mlp_config {
   float ln_eps;          /* LayerNorm epsilon (added to the biased variance) */
   int   gelu_mode;       /* TPMLP_GELU_ERF or TPMLP_GELU_TANH                */
   int   use_residual;    /* 1: Z = X + MLP(...), added before the rounding  */
+  float dropout_p;       /* output dropout probability in [0, 1); training
+                            calls only; 0 = off (see tp_mlp_set_dropout_seed) */
 } tp_mlp_config;
 
 typedef struct tp_mlp_handle tp_mlp_handle;
@@ -204,6 +208,18 @@ int tp_mlp_set_timing(tp_mlp_handle* handle, int enable);
 int tp_mlp_timing_get(tp_mlp_handle* handle, int index, const char** name,
                       long long* launches, double* total_ms);
 int tp_mlp_timing_reset(tp_mlp_handle* handle);
+
+/* Seed and counter offset of the output dropout (default 0, 0).  The mask
+ * is a pure function of (seed, offset, token row, column), so it does not
+ * depend on the shard count or on the launch configuration: element (r, c)
+ * is kept when 32-bit word c % 4 of Philox4x32-10 (Salmon et al., SC 2011)
+ * of counter (c / 4, r, offset low, offset high) under key (seed low, seed
+ * high) is >= floor(dropout_p 2^32); kept values are scaled by
+ * 1 / (1 - dropout_p).  tp_mlp_backward regenerates the same mask from the
+ * handle's current seed and offset, so they must not change between a
+ * forward call and its backward call. */
+int tp_mlp_set_dropout_seed(tp_mlp_handle* handle, unsigned long long seed,
+                            unsigned long long offset);
 
 /* Budget, in nanoseconds, for each bounded wait inside the GEMM kernels
  * (default 2e9).  A wait that exceeds it makes the kernel record

@@ -37,6 +37,7 @@ EXPORTED = (
     "tp_mlp_status_string", "tp_mlp_last_detail", "tp_mlp_launch_count",
     "tp_mlp_set_timing", "tp_mlp_timing_get", "tp_mlp_timing_reset",
     "tp_mlp_set_wait_budget", "tp_mlp_bias_grad_noalloc",
+    "tp_mlp_set_dropout_seed",
 )
 
 TPMLP_NOALLOC_SCRATCH_FLOATS = 1 << 20
@@ -47,7 +48,7 @@ class tp_mlp_config(ctypes.Structure):
                 ("shards", ctypes.c_int), ("max_tokens", ctypes.c_int),
                 ("dtype", ctypes.c_int), ("use_layernorm", ctypes.c_int),
                 ("ln_eps", ctypes.c_float), ("gelu_mode", ctypes.c_int),
-                ("use_residual", ctypes.c_int)]
+                ("use_residual", ctypes.c_int), ("dropout_p", ctypes.c_float)]
 
 
 class TPMLPError(RuntimeError):
@@ -104,6 +105,9 @@ def lib(path: str | None = None) -> ctypes.CDLL:
     L.tp_mlp_timing_reset.restype = _i
     L.tp_mlp_set_wait_budget.argtypes = [_vp, ctypes.c_ulonglong]
     L.tp_mlp_set_wait_budget.restype = _i
+    L.tp_mlp_set_dropout_seed.argtypes = [_vp, ctypes.c_ulonglong,
+                                          ctypes.c_ulonglong]
+    L.tp_mlp_set_dropout_seed.restype = _i
     L.tp_mlp_bias_grad_noalloc.argtypes = [_i, _i, _i, _vp, _vp, _vp]
     L.tp_mlp_bias_grad_noalloc.restype = _i
     if path is None:
@@ -208,6 +212,11 @@ def tp_mlp_timing_get(handle):
 
 def tp_mlp_timing_reset(handle) -> None:
     _check(lib().tp_mlp_timing_reset(handle), "tp_mlp_timing_reset")
+
+
+def tp_mlp_set_dropout_seed(handle, seed: int, offset: int = 0) -> None:
+    _check(lib().tp_mlp_set_dropout_seed(handle, seed, offset),
+           "tp_mlp_set_dropout_seed")
 
 
 def tp_mlp_set_wait_budget(handle, ns: int) -> None:

@@ -41,6 +41,11 @@ struct GemmArgs {
   const float* bias;      // [N] fp32 (nullable)
   int* status;            // device status word: [0] code, [1] role, [2] block
   unsigned long long budget_ns;
+  // EPI_SHARDSUM dropout (applied after the bias, before the residual).
+  int dropout;            // 0 = off
+  uint32_t drop_threshold;  // keep when the 32-bit draw >= threshold
+  float drop_scale;       // 1 / (1 - p)
+  unsigned long long drop_seed, drop_offset;
 };
 
 // Roles recorded in status[1] when a bounded wait gives up.
@@ -67,6 +72,48 @@ __device__ __forceinline__ float gelu_grad_f32(float x, int mode) {
   const float th = tanhf(u);
   const float du = 0.79788456080286536f * (1.0f + 3.0f * 0.044715f * x * x);
   return 0.5f * (1.0f + th) + 0.5f * x * (1.0f - th * th) * du;
+}
+
+// Philox4x32-10 (Salmon, Moraes, Dror and Shaw, SC 2011): 10 rounds; a round
+// multiplies counter words 0 and 2 by 0xD2511F53 and 0xCD9E8D57 and maps
+// (c0, c1, c2, c3) to (hi(M1 c2) ^ c1 ^ k0, lo(M1 c2), hi(M0 c0) ^ c3 ^ k1,
+// lo(M0 c0)); the key advances by (0x9E3779B9, 0xBB67AE85) between rounds.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0,
+                                               uint32_t k1) {
+#pragma unroll
+  for (int i = 0; i < 10; ++i) {
+    const uint32_t lo0 = 0xD2511F53u * c.x;
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x);
+    const uint32_t lo1 = 0xCD9E8D57u * c.z;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z);
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return c;
+}
+
+// Dropout of the block's output: element (row, col) is kept when word
+// col % 4 of Philox4x32-10(counter (col / 4, row, offset), key = seed) is
+// >= threshold; kept values are scaled.  Applies to n consecutive columns
+// from c0 (c0 % 4 == 0, n % 4 == 0).
+__device__ __forceinline__ void apply_dropout(uint32_t threshold, float scale,
+                                              unsigned long long seed,
+                                              unsigned long long offset,
+                                              int row, int c0, float* v,
+                                              int n) {
+#pragma unroll
+  for (int i = 0; i < n / 4; ++i) {
+    const uint4 w = philox4x32_10(
+        make_uint4(static_cast<uint32_t>(c0 / 4 + i), static_cast<uint32_t>(row),
+                   static_cast<uint32_t>(offset),
+                   static_cast<uint32_t>(offset >> 32)),
+        static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
+    v[4 * i + 0] = w.x >= threshold ? v[4 * i + 0] * scale : 0.f;
+    v[4 * i + 1] = w.y >= threshold ? v[4 * i + 1] * scale : 0.f;
+    v[4 * i + 2] = w.z >= threshold ? v[4 * i + 2] * scale : 0.f;
+    v[4 * i + 3] = w.w >= threshold ? v[4 * i + 3] * scale : 0.f;
+  }
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

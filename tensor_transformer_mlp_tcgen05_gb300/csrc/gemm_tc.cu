@@ -308,6 +308,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
               for (int i = 0; i < 32; ++i) v[i] = S[j * 32 + i];
               add_bias32(args.bias, c0, v);
+              if (args.dropout)
+                apply_dropout(args.drop_threshold, args.drop_scale,
+                              args.drop_seed, args.drop_offset, row, c0, v, 32);
               if (!args.out_f32)
                 add_residual_bf16(args.aux, args.ldaux, row, args.M, c0, v, 32);
               const size_t off = static_cast<size_t>(row) * args.ldo + c0;

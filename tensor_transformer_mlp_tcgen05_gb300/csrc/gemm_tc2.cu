@@ -393,6 +393,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               const int c0 = col_base + j * 32;
               if (c0 < args.N) {
                 add_bias_n(args.bias, c0, &S[j * 32], 32);
+                if (args.dropout)
+                  apply_dropout(args.drop_threshold, args.drop_scale,
+                                args.drop_seed, args.drop_offset, row, c0,
+                                &S[j * 32], 32);
                 uint32_t w[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(S[j * 32 + i]);
@@ -405,6 +409,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               const int c0 = col_base + j * 64;
               if (c0 < args.N) {
                 add_bias_n(args.bias, c0, &S[j * 64], 64);
+                if (args.dropout)
+                  apply_dropout(args.drop_threshold, args.drop_scale,
+                                args.drop_seed, args.drop_offset, row, c0,
+                                &S[j * 64], 64);
                 add_residual_bf16(args.aux, args.ldaux, row, args.M, c0,
                                   &S[j * 64], 64);
                 uint32_t w[32];

@@ -80,6 +80,13 @@ cudaError_t launch_ln_param_partial(bool bf16, const float* dXn, const void* X,
 cudaError_t launch_colsum_finalize(const float* part, float* out, int chunks,
                                    int cols, cudaStream_t stream);
 
+// Backward of the output dropout: out = mask * scale * dZ ([rows, cols]).
+cudaError_t launch_dropout_grad(bool bf16, const void* dZ, void* out, int rows,
+                                int cols, uint32_t threshold, float scale,
+                                unsigned long long seed,
+                                unsigned long long offset,
+                                cudaStream_t stream);
+
 // Record a message for tp_mlp_last_detail() on the calling thread.
 void set_last_detail(const char* msg);
 

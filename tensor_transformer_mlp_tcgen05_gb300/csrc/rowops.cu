@@ -191,6 +191,19 @@ __device__ __forceinline__ void load4<__nv_bfloat16>(const __nv_bfloat16* p,
   unpack_bf16x2(u.y, v[2], v[3]);
 }
 
+template <typename T>
+__device__ __forceinline__ void store4(T* p, const float (&v)[4]);
+template <>
+__device__ __forceinline__ void store4<float>(float* p, const float (&v)[4]) {
+  *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+}
+template <>
+__device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* p,
+                                                      const float (&v)[4]) {
+  *reinterpret_cast<uint2*>(p) =
+      make_uint2(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]));
+}
+
 // MODE 0: part1 = sum src.  MODE 1 (LayerNorm parameters): part1 = sum
 // dXn * xhat, part2 = sum dXn, with xhat recomputed from X, mean, rstd.
 template <typename T, int MODE>
@@ -258,7 +271,51 @@ __global__ void colsum_finalize_kernel(const float* __restrict__ part,
   out[c] = s;
 }
 
+// Backward of the output dropout: out = mask * scale * dZ, four columns per
+// thread (one Philox draw), grid-stride over the [rows, cols] matrix.
+template <typename T>
+__global__ void __launch_bounds__(256)
+    dropout_grad_kernel(const T* __restrict__ dZ, T* __restrict__ out, int rows,
+                        int cols, uint32_t threshold, float scale,
+                        unsigned long long seed, unsigned long long offset) {
+  const long long groups = static_cast<long long>(rows) * (cols / 4);
+  for (long long gi = blockIdx.x * static_cast<long long>(blockDim.x) +
+                      threadIdx.x;
+       gi < groups; gi += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int r = static_cast<int>(gi / (cols / 4));
+    const int c0 = static_cast<int>(gi % (cols / 4)) * 4;
+    const size_t off = static_cast<size_t>(r) * cols + c0;
+    float v[4];
+    load4<T>(dZ + off, v);
+    apply_dropout(threshold, scale, seed, offset, r, c0, v, 4);
+    store4<T>(out + off, v);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_dropout_grad(bool bf16, const void* dZ, void* out, int rows,
+                                int cols, uint32_t threshold, float scale,
+                                unsigned long long seed,
+                                unsigned long long offset,
+                                cudaStream_t stream) {
+  const long long groups = static_cast<long long>(rows) * (cols / 4);
+  const int threads = 256;
+  long long blocks = (groups + threads - 1) / threads;
+  if (blocks > 4096) blocks = 4096;
+  if (blocks < 1) blocks = 1;
+  if (bf16) {
+    dropout_grad_kernel<__nv_bfloat16><<<static_cast<int>(blocks), threads, 0,
+                                          stream>>>(
+        static_cast<const __nv_bfloat16*>(dZ), static_cast<__nv_bfloat16*>(out),
+        rows, cols, threshold, scale, seed, offset);
+  } else {
+    dropout_grad_kernel<float><<<static_cast<int>(blocks), threads, 0, stream>>>(
+        static_cast<const float*>(dZ), static_cast<float*>(out), rows, cols,
+        threshold, scale, seed, offset);
+  }
+  return cudaGetLastError();
+}
 
 cudaError_t launch_ln_fwd(bool bf16, const void* X, const float* gamma,
                           const float* beta, void* Xn, float* mean,

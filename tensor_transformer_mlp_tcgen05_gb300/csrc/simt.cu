@@ -54,6 +54,13 @@ __global__ void __launch_bounds__(TS* TS)
     }
     case EPI_SHARDSUM: {
       float v = total + (a.bias ? a.bias[n] : 0.f);
+      if (a.dropout) {
+        float q[4] = {0.f, 0.f, 0.f, 0.f};
+        q[n & 3] = v;
+        apply_dropout(a.drop_threshold, a.drop_scale, a.drop_seed,
+                      a.drop_offset, m, n & ~3, q, 4);
+        v = q[n & 3];
+      }
       if (a.aux) {
         v += static_cast<const float*>(a.aux)[static_cast<size_t>(m) * a.ldaux + n];
       }

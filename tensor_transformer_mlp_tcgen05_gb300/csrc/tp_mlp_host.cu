@@ -43,14 +43,15 @@ void set_detail_msg(const char* msg) {
 
 struct Layout {
   size_t status = 0, xn = 0, mean = 0, rstd = 0, y = 0, h = 0, dh = 0,
-         dxn = 0, part = 0, total = 0;
+         dxn = 0, dze = 0, part = 0, total = 0;
   int chunks = 0;
 };
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Workspace sections, each 256-byte aligned: status word; [Xn, mean, rstd]
-// with LayerNorm; Y; and for training H, dH, [dXn fp32], column-sum partials.
+// with LayerNorm; Y; and for training H, dH, [dXn fp32 with LayerNorm],
+// [the dropout-masked dZ with dropout], column-sum partials.
 Layout make_layout(const tp_mlp_config& c, int tokens, int training) {
   Layout L;
   const size_t es = c.dtype == TPMLP_BF16 ? 2 : 4;
@@ -74,6 +75,7 @@ Layout make_layout(const tp_mlp_config& c, int tokens, int training) {
     L.h = take(T * f * es);
     L.dh = take(T * f * es);
     if (c.use_layernorm) L.dxn = take(T * h * 4);
+    if (c.dropout_p > 0.f) L.dze = take(T * h * es);
     L.chunks = colsum_chunks(tokens);
     L.part = take(static_cast<size_t>(L.chunks) * (f + 3 * h) * 4);
   }
@@ -212,6 +214,7 @@ void tpmlp::set_last_detail(const char* msg) { set_detail_msg(msg); }
 struct tp_mlp_handle {
   tp_mlp_config cfg;
   unsigned long long budget_ns = 2000000000ull;
+  unsigned long long drop_seed = 0, drop_offset = 0;
   long long launches = 0;
   bool timing = false;
   struct Pending {
@@ -287,6 +290,19 @@ GemmArgs base_args(const tp_mlp_handle* H, void* ws, const Layout& L) {
   return a;
 }
 
+// Dropout parameters of the output dropout (keep when the 32-bit Philox
+// draw is >= floor(p 2^32), scale kept values by 1 / (1 - p)).
+void set_dropout(const tp_mlp_handle* H, GemmArgs& a) {
+  const double p = H->cfg.dropout_p;
+  double thr = p * 4294967296.0;
+  if (thr > 4294967295.0) thr = 4294967295.0;
+  a.dropout = 1;
+  a.drop_threshold = static_cast<uint32_t>(thr);
+  a.drop_scale = 1.0f / (1.0f - H->cfg.dropout_p);
+  a.drop_seed = H->drop_seed;
+  a.drop_offset = H->drop_offset;
+}
+
 #define TRY(x)                       \
   do {                               \
     const int rc_ = (x);             \
@@ -356,6 +372,7 @@ int tp_mlp_create(const tp_mlp_config* cfg, tp_mlp_handle** out) {
     return TPMLP_ERR_ARG;
   if (cfg->use_layernorm != 0 && cfg->use_layernorm != 1) return TPMLP_ERR_ARG;
   if (cfg->use_residual != 0 && cfg->use_residual != 1) return TPMLP_ERR_ARG;
+  if (!(cfg->dropout_p >= 0.f && cfg->dropout_p < 1.f)) return TPMLP_ERR_ARG;
   if (cfg->use_layernorm &&
       !(cfg->ln_eps >= 0.f && std::isfinite(cfg->ln_eps)))
     return TPMLP_ERR_ARG;
@@ -446,6 +463,7 @@ int tp_mlp_forward(tp_mlp_handle* H, int tokens, const void* X, const void* A,
     g2.aux = X;
     g2.ldaux = h;
   }
+  if (training && c.dropout_p > 0.f) set_dropout(H, g2);  // training only
 
   if (bf16) {
     CUtensorMap ta, tb;
@@ -526,6 +544,21 @@ int tp_mlp_backward(tp_mlp_handle* H, int tokens, const void* dZ,
   const void* Y = ws + L.y;
   const void* Hb = ws + L.h;
   void* dH = ws + L.dh;
+  // The block's own gradients see the dropout-masked dZ; the residual path
+  // (below) keeps the raw dZ.
+  const void* dZg = dZ;
+  if (c.dropout_p > 0.f) {
+    GemmArgs dp;
+    std::memset(&dp, 0, sizeof(dp));
+    set_dropout(H, dp);
+    void* dze = ws + L.dze;
+    TRY(run(H, "dropout_bwd", s, [&] {
+      return launch_dropout_grad(bf16, dZ, dze, T, h, dp.drop_threshold,
+                                 dp.drop_scale, dp.drop_seed, dp.drop_offset,
+                                 s);
+    }));
+    dZg = dze;
+  }
   const void* Xop = ln ? static_cast<const void*>(ws + L.xn) : X;
   float* part = reinterpret_cast<float*>(ws + L.part);
   void* dXdst = ln ? static_cast<void*>(ws + L.dxn) : dX;
@@ -552,18 +585,18 @@ int tp_mlp_backward(tp_mlp_handle* H, int tokens, const void* dZ,
   if (bf16) {
     CUtensorMap ta, tb;
     gy.kb_per_seg = h / TC_BK;
-    TRY(kmajor_map(&ta, dZ, T, h, TC_BM));
+    TRY(kmajor_map(&ta, dZg, T, h, TC_BM));
     TRY(kmajor_map(&tb, B, f, h, b_box_rows()));
     TRY(tc_gemm(H, "gemm_dh_gelu_bwd", s, sms, EPI_GELU_BWD, false, false, ta,
                 tb, gy));
-    if (dbias2) TRY(colsum(H, "colsum_db2", s, true, dZ, part, dbias2, T, h));
+    if (dbias2) TRY(colsum(H, "colsum_db2", s, true, dZg, part, dbias2, T, h));
     if (dbias1)
       TRY(colsum(H, "colsum_db1", s, true, dH, part + size_t(L.chunks) * h,
                  dbias1, T, f));
     const int kbT = (T + TC_BK - 1) / TC_BK;
     gb.kb_per_seg = kbT;
     TRY(mnmajor_map(&ta, Y, T, f));
-    TRY(mnmajor_map(&tb, dZ, T, h));
+    TRY(mnmajor_map(&tb, dZg, T, h));
     TRY(tc_gemm(H, "gemm_wgrad_dB", s, sms, EPI_STORE_F32, true, true, ta, tb,
                 gb));
     ga.kb_per_seg = kbT;
@@ -578,13 +611,13 @@ int tp_mlp_backward(tp_mlp_handle* H, int tokens, const void* dZ,
                 tb, gx));
   } else {
     const float* fY = static_cast<const float*>(Y);
-    const float* fdZ = static_cast<const float*>(dZ);
+    const float* fdZ = static_cast<const float*>(dZg);
     const float* fdH = static_cast<const float*>(dH);
     gy.kb_per_seg = h;
     const SimtOperands oy{fdZ, h, 1, static_cast<const float*>(B), 1, h};
     TRY(run(H, "simt_gemm_dh_gelu_bwd", s,
             [&] { return launch_gemm_simt(EPI_GELU_BWD, oy, gy, s); }));
-    if (dbias2) TRY(colsum(H, "colsum_db2", s, false, dZ, part, dbias2, T, h));
+    if (dbias2) TRY(colsum(H, "colsum_db2", s, false, dZg, part, dbias2, T, h));
     if (dbias1)
       TRY(colsum(H, "colsum_db1", s, false, dH, part + size_t(L.chunks) * h,
                  dbias1, T, f));
@@ -710,6 +743,14 @@ int tp_mlp_timing_reset(tp_mlp_handle* H) {
   if (H == nullptr) return TPMLP_ERR_ARG;
   tp_mlp_timing_get(H, -1, nullptr, nullptr, nullptr);  // drain pending
   H->stats.clear();
+  return TPMLP_OK;
+}
+
+int tp_mlp_set_dropout_seed(tp_mlp_handle* handle, unsigned long long seed,
+                            unsigned long long offset) {
+  if (handle == nullptr) return TPMLP_ERR_ARG;
+  handle->drop_seed = seed;
+  handle->drop_offset = offset;
   return TPMLP_OK;
 }
 

@@ -17,16 +17,19 @@ class TensorParallelMLP:
     def __init__(self, hidden: int, ffn: int, shards: int, max_tokens: int,
                  dtype: str = "bf16", layernorm: bool = False,
                  ln_eps: float = 1e-5, gelu: str = "erf", residual: bool = False,
-                 device=None):
+                 dropout_p: float = 0.0, dropout_seed: int = 0,
+                 dropout_offset: int = 0, device=None):
         self.cfg = B_.tp_mlp_config(
             hidden=hidden, ffn=ffn, shards=shards, max_tokens=max_tokens,
             dtype=B_.TPMLP_BF16 if dtype == "bf16" else B_.TPMLP_FP32,
             use_layernorm=1 if layernorm else 0, ln_eps=ln_eps,
             gelu_mode=B_.TPMLP_GELU_ERF if gelu == "erf" else B_.TPMLP_GELU_TANH,
-            use_residual=1 if residual else 0)
+            use_residual=1 if residual else 0, dropout_p=dropout_p)
         if dtype not in ("bf16", "fp32") or gelu not in ("erf", "tanh"):
             raise ValueError("dtype must be bf16|fp32 and gelu erf|tanh")
         self.handle = B_.tp_mlp_create(self.cfg)
+        if dropout_p > 0:
+            B_.tp_mlp_set_dropout_seed(self.handle, dropout_seed, dropout_offset)
         self.hidden, self.ffn, self.shards = hidden, ffn, shards
         self.max_tokens = max_tokens
         self.layernorm = layernorm

@@ -49,12 +49,14 @@ def to_dev(x):
 
 
 def run_cuda(w, inp, backward=True, training=True, gelu="erf", repeat=1,
-             residual=False):
+             residual=False, dropout=None):
     """Forward (+ backward) on cuda:0 through the binding.  Returns a dict of
     CPU tensors; with repeat > 1 a list of such dicts (same inputs)."""
+    p, seed, offset = dropout if dropout is not None else (0.0, 0, 0)
     m = TensorParallelMLP(w.hidden, w.ffn, w.shards, max(w.tokens, 1),
                           dtype=w.dtype, layernorm=w.layernorm, gelu=gelu,
-                          residual=residual)
+                          residual=residual, dropout_p=p, dropout_seed=seed,
+                          dropout_offset=offset)
     d = {k: to_dev(v) for k, v in inp.items()}
     outs = []
     for _ in range(repeat):
@@ -72,11 +74,14 @@ def run_cuda(w, inp, backward=True, training=True, gelu="erf", repeat=1,
     return outs if repeat > 1 else outs[0]
 
 
-def oracle_full(inp, mode="erf", backward=True, residual=False):
+def oracle_full(inp, mode="erf", backward=True, residual=False, dropout=None):
     X, A, B = f64(inp["X"]), f64(inp["A"]), f64(inp["B"])
     fwd = O.forward(X, A, B, f64(inp["b1"]), f64(inp["b2"]), f64(inp["gamma"]),
-                    f64(inp["beta"]), mode=mode, residual=residual)
+                    f64(inp["beta"]), mode=mode, residual=residual,
+                    dropout=dropout)
     out = {"Z": fwd["Z"]}
+    if fwd.get("mask") is not None:
+        out["_mask"] = fwd["mask"]
     if backward:
         g = O.backward(f64(inp["dZ"]), X, A, B, fwd, f64(inp["gamma"]), mode,
                        residual=residual)
@@ -90,5 +95,7 @@ def oracle_full(inp, mode="erf", backward=True, residual=False):
 def compare_full(got, ref, fp32=False):
     report = {}
     for k, v in ref.items():
+        if k.startswith("_"):
+            continue
         report[k] = assert_close(k, got[k], v, fp32=fp32)
     return report

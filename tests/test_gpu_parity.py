@@ -79,6 +79,63 @@ def test_tiny_fp32_residual_block_full():
     compare_full(got, oracle_full(inp, residual=True), fp32=True)
 
 
+# ------------------------------------------------------------- dropout ----
+
+DROP = (0.1, 0x5EED1234ABCD, 3)
+
+
+def test_dropout_mask_is_bit_exact():
+    """Every keep/drop decision equals the oracle's Philox mask (integer
+    decisions: compared exactly, not within a tolerance)."""
+    w = small(300, 256, 1024, 4)
+    inp = W.make_inputs(w, seed=12)
+    got = run_cuda(w, inp, backward=False, dropout=DROP)
+    ref = oracle_full(inp, backward=False, dropout=DROP)
+    mask = ref["_mask"]
+    pre = oracle_full(inp, backward=False)["Z"]
+    decided = np.abs(pre) > 1e-3           # a kept value cannot round to 0
+    gz = f64(got["Z"]) != 0
+    assert np.array_equal(gz[decided], mask[decided])
+    assert 0.85 < mask.mean() < 0.95
+    assert_close("Z", got["Z"], ref["Z"])
+
+
+@pytest.mark.parametrize("T,h,f,t,ln,res", [(300, 256, 1024, 4, True, True),
+                                            (513, 192, 768, 2, False, False),
+                                            (129, 320, 1280, 1, False, True)])
+def test_dropout_block_full(T, h, f, t, ln, res):
+    w = small(T, h, f, t, ln)
+    inp = W.make_inputs(w, seed=13, with_bias=True)
+    got = run_cuda(w, inp, residual=res, dropout=DROP)
+    compare_full(got, oracle_full(inp, residual=res, dropout=DROP))
+
+
+def test_tiny_fp32_dropout_block_full():
+    w = W.WORKLOADS["tiny_fp32"]
+    inp = W.make_inputs(w, seed=0, with_bias=True)
+    got = run_cuda(w, inp, residual=True, dropout=(0.25, 77, 0))
+    compare_full(got, oracle_full(inp, residual=True, dropout=(0.25, 77, 0)),
+                 fp32=True)
+
+
+def test_dropout_mask_does_not_depend_on_shards_and_is_deterministic():
+    base = small(256, 256, 2048, 1)
+    inp = W.make_inputs(base, seed=14)
+    z1 = run_cuda(base, inp, backward=False, dropout=DROP)["Z"]
+    z8a, z8b = run_cuda(base.with_(shards=8), inp, backward=False,
+                        dropout=DROP, repeat=2)
+    assert torch.equal(z8a["Z"], z8b["Z"])
+    assert torch.equal(z1 == 0, z8a["Z"] == 0)
+
+
+def test_dropout_only_in_training_calls():
+    w = small(256, 256, 1024, 2)
+    inp = W.make_inputs(w, seed=15)
+    a = run_cuda(w, inp, backward=False, training=False, dropout=DROP)
+    b = run_cuda(w, inp, backward=False, training=False)
+    assert torch.equal(a["Z"], b["Z"])
+
+
 def test_small_fp32_layernorm_block_full():
     w = small(200, 128, 512, 4, ln=True, dtype="fp32")
     inp = W.make_inputs(w, seed=2, with_bias=True)
