@@ -19,6 +19,8 @@ enum Epilogue : int {
   EPI_GELU_BWD = 2,
   // plain fp32 store (weight gradients).
   EPI_STORE_F32 = 3,
+  // acc (+ bias) rounded to bf16 (projections without an activation).
+  EPI_BIAS_BF16 = 4,
 };
 
 // Arguments of one GEMM launch: D[M,N] = sum over K of Aop[m,k] * Bop[k,n],

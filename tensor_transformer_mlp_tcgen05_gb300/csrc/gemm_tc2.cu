@@ -327,7 +327,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (live && c0 < args.N) st.put(&tmO, c0, row0, r, lane);
           }
         } else {
-          // GeLU forward / backward: two 64-column bf16 chunks.
+          // GeLU forward / backward, plain bf16: two 64-column bf16 chunks.
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
             uint32_t r0[32], r1[32];
@@ -343,7 +343,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 v[32 + i] = __uint_as_float(r1[i]);
               }
               uint32_t w[32];
-              if constexpr (EPI == EPI_GELU_FWD) {
+              if constexpr (EPI == EPI_BIAS_BF16) {
+                add_bias_n(args.bias, c0, v, 64);
+              } else if constexpr (EPI == EPI_GELU_FWD) {
                 add_bias_n(args.bias, c0, v, 64);
                 if (args.out2 != nullptr) {
                   pack_bf16x64(v, w);
@@ -495,6 +497,12 @@ cudaError_t launch_gemm_tc2(int epi, bool a_mn, bool b_mn,
   if (a_mn && b_mn && epi == EPI_STORE_F32)
     return launch_impl<true, true, EPI_STORE_F32>(ta, tb, to, to2, args, max_pairs,
                                                   stream);
+  if (!a_mn && b_mn && epi == EPI_BIAS_BF16)
+    return launch_impl<false, true, EPI_BIAS_BF16>(ta, tb, to, to2, args,
+                                                   max_pairs, stream);
+  if (!a_mn && !b_mn && epi == EPI_BIAS_BF16)
+    return launch_impl<false, false, EPI_BIAS_BF16>(ta, tb, to, to2, args,
+                                                    max_pairs, stream);
   return cudaErrorInvalidValue;
 }
 
