@@ -38,7 +38,17 @@ EXPORTED = (
     "tp_mlp_set_timing", "tp_mlp_timing_get", "tp_mlp_timing_reset",
     "tp_mlp_set_wait_budget", "tp_mlp_bias_grad_noalloc",
     "tp_mlp_set_dropout_seed",
+    "tp_attn_create", "tp_attn_destroy", "tp_attn_workspace_bytes",
+    "tp_attn_forward", "tp_attn_backward", "tp_attn_check",
+    "tp_attn_launch_count", "tp_attn_set_timing", "tp_attn_timing_get",
+    "tp_attn_timing_reset", "tp_attn_set_wait_budget",
+    "tp_attn_workspace_offset",
 )
+
+TPATTN_WS_QKV = 0
+TPATTN_WS_CTX = 1
+TPATTN_WS_LSE = 2
+TPATTN_WS_DQKV = 3
 
 TPMLP_NOALLOC_SCRATCH_FLOATS = 1 << 20
 
@@ -49,6 +59,14 @@ class tp_mlp_config(ctypes.Structure):
                 ("dtype", ctypes.c_int), ("use_layernorm", ctypes.c_int),
                 ("ln_eps", ctypes.c_float), ("gelu_mode", ctypes.c_int),
                 ("use_residual", ctypes.c_int), ("dropout_p", ctypes.c_float)]
+
+
+class tp_attn_config(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int), ("heads", ctypes.c_int),
+                ("shards", ctypes.c_int), ("max_tokens", ctypes.c_int),
+                ("seq_len", ctypes.c_int), ("causal", ctypes.c_int),
+                ("use_layernorm", ctypes.c_int), ("ln_eps", ctypes.c_float),
+                ("use_residual", ctypes.c_int)]
 
 
 class TPMLPError(RuntimeError):
@@ -110,6 +128,35 @@ def lib(path: str | None = None) -> ctypes.CDLL:
     L.tp_mlp_set_dropout_seed.restype = _i
     L.tp_mlp_bias_grad_noalloc.argtypes = [_i, _i, _i, _vp, _vp, _vp]
     L.tp_mlp_bias_grad_noalloc.restype = _i
+    L.tp_attn_create.argtypes = [ctypes.POINTER(tp_attn_config),
+                                 ctypes.POINTER(_vp)]
+    L.tp_attn_create.restype = _i
+    L.tp_attn_destroy.argtypes = [_vp]
+    L.tp_attn_destroy.restype = _i
+    L.tp_attn_workspace_bytes.argtypes = [_vp, _i, _i]
+    L.tp_attn_workspace_bytes.restype = _sz
+    L.tp_attn_workspace_offset.argtypes = [_vp, _i, _i, _i]
+    L.tp_attn_workspace_offset.restype = ctypes.c_longlong
+    L.tp_attn_forward.argtypes = [_vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                  _vp, _vp, _sz, _i, _vp]
+    L.tp_attn_forward.restype = _i
+    L.tp_attn_backward.argtypes = [_vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _sz,
+                                   _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+    L.tp_attn_backward.restype = _i
+    L.tp_attn_check.argtypes = [_vp, _vp, _vp]
+    L.tp_attn_check.restype = _i
+    L.tp_attn_launch_count.argtypes = [_vp]
+    L.tp_attn_launch_count.restype = ctypes.c_longlong
+    L.tp_attn_set_timing.argtypes = [_vp, _i]
+    L.tp_attn_set_timing.restype = _i
+    L.tp_attn_timing_get.argtypes = [_vp, _i, ctypes.POINTER(ctypes.c_char_p),
+                                     ctypes.POINTER(ctypes.c_longlong),
+                                     ctypes.POINTER(ctypes.c_double)]
+    L.tp_attn_timing_get.restype = _i
+    L.tp_attn_timing_reset.argtypes = [_vp]
+    L.tp_attn_timing_reset.restype = _i
+    L.tp_attn_set_wait_budget.argtypes = [_vp, ctypes.c_ulonglong]
+    L.tp_attn_set_wait_budget.restype = _i
     if path is None:
         _lib = L
     return L
@@ -230,3 +277,82 @@ def tp_mlp_bias_grad_noalloc(tokens, cols, dtype, grad, dbias, stream=None):
     _check(lib().tp_mlp_bias_grad_noalloc(tokens, cols, dtype, _ptr(grad),
                                           _ptr(dbias), _stream(stream)),
            "tp_mlp_bias_grad_noalloc")
+
+
+# ------------------------------------------------------------- attention --
+
+def tp_attn_create(config: tp_attn_config) -> int:
+    h = _vp()
+    _check(lib().tp_attn_create(ctypes.byref(config), ctypes.byref(h)),
+           "tp_attn_create")
+    return h.value
+
+
+def tp_attn_destroy(handle: int) -> None:
+    _check(lib().tp_attn_destroy(handle), "tp_attn_destroy")
+
+
+def tp_attn_workspace_bytes(handle: int, tokens: int, training: int) -> int:
+    return int(lib().tp_attn_workspace_bytes(handle, tokens, training))
+
+
+def tp_attn_workspace_offset(handle: int, tokens: int, training: int,
+                             which: int) -> int:
+    return int(lib().tp_attn_workspace_offset(handle, tokens, training, which))
+
+
+def tp_attn_forward(handle, tokens, X, Wqkv, Wo, bqkv, bo, ln_gamma, ln_beta,
+                    Z, workspace, workspace_bytes, training, stream=None):
+    _check(lib().tp_attn_forward(
+        handle, tokens, _ptr(X), _ptr(Wqkv), _ptr(Wo), _ptr(bqkv), _ptr(bo),
+        _ptr(ln_gamma), _ptr(ln_beta), _ptr(Z), _ptr(workspace),
+        workspace_bytes, training, _stream(stream)), "tp_attn_forward")
+
+
+def tp_attn_backward(handle, tokens, dZ, X, Wqkv, Wo, ln_gamma, workspace,
+                     workspace_bytes, dX, dWqkv, dWo, dbqkv, dbo, dgamma,
+                     dbeta, stream=None):
+    _check(lib().tp_attn_backward(
+        handle, tokens, _ptr(dZ), _ptr(X), _ptr(Wqkv), _ptr(Wo),
+        _ptr(ln_gamma), _ptr(workspace), workspace_bytes, _ptr(dX),
+        _ptr(dWqkv), _ptr(dWo), _ptr(dbqkv), _ptr(dbo), _ptr(dgamma),
+        _ptr(dbeta), _stream(stream)), "tp_attn_backward")
+
+
+def tp_attn_check(handle, workspace, stream=None) -> int:
+    return int(lib().tp_attn_check(handle, _ptr(workspace), _stream(stream)))
+
+
+def tp_attn_launch_count(handle) -> int:
+    return int(lib().tp_attn_launch_count(handle))
+
+
+def tp_attn_set_timing(handle, enable: bool) -> None:
+    _check(lib().tp_attn_set_timing(handle, 1 if enable else 0),
+           "tp_attn_set_timing")
+
+
+def tp_attn_timing_get(handle):
+    """All per-kernel totals: list of (name, launches, total_ms)."""
+    out = []
+    i = 0
+    while True:
+        name = ctypes.c_char_p()
+        n = ctypes.c_longlong()
+        ms = ctypes.c_double()
+        rc = lib().tp_attn_timing_get(handle, i, ctypes.byref(name),
+                                      ctypes.byref(n), ctypes.byref(ms))
+        if rc == TPMLP_ERR_ARG:
+            break
+        _check(rc, "tp_attn_timing_get")
+        out.append((name.value.decode(), n.value, ms.value))
+        i += 1
+    return out
+
+
+def tp_attn_timing_reset(handle) -> None:
+    _check(lib().tp_attn_timing_reset(handle), "tp_attn_timing_reset")
+
+
+def tp_attn_set_wait_budget(handle, ns: int) -> None:
+    _check(lib().tp_attn_set_wait_budget(handle, ns), "tp_attn_set_wait_budget")

@@ -23,7 +23,8 @@ BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG, "libtpmlp.so")
 
 SOURCES = ["gemm_tc.cu", "gemm_tc2.cu", "rowops.cu", "simt.cu",
-           "tp_mlp_host.cu", "noalloc.cu"]
+           "tp_mlp_host.cu", "noalloc.cu", "attn_fwd.cu", "attn_bwd.cu",
+           "attn_host.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
           "--expt-relaxed-constexpr", "-I" + INCLUDE, "-I" + CSRC]
@@ -40,6 +41,7 @@ def _inputs():
     files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)
              if f.endswith((".cu", ".cuh", ".h"))]
     files.append(os.path.join(INCLUDE, "tp_mlp.h"))
+    files.append(os.path.join(INCLUDE, "tp_attn.h"))
     files.append(os.path.abspath(__file__))
     return files
 

@@ -1,0 +1,407 @@
+// Backward of the attention core (per sequence and head; scaled dot-product
+// attention, Megatron-LM explainer section on attention and notes section
+// "Self-attention block split": the heads stay independent in the backward
+// too, so no shard exchanges anything here).
+//
+// With P = exp2(S log2(e)/sqrt(d) - lse2) (the forward's saved base-2
+// log-sum-exp), dO = dCtx and delta = rowsum(dO * O):
+//   dV = P^T dO,   dP = dO V^T,   dS = P * (dP - delta) / sqrt(d),
+//   dK = dS^T Q,   dQ = dS K.
+// Every output element has exactly one writer and no atomics are used:
+//   * the KV kernel owns 128 keys of one (sequence, head) and walks the
+//     64-query blocks that may see them, accumulating dK and dV in TMEM;
+//   * the Q kernel owns 128 queries and walks the 64-key blocks they see,
+//     recomputing S and dP, accumulating dQ in TMEM.
+// Both are one template: a fixed 128-row pair of operand tiles (A1, A2) and a
+// stream of 64-row tile pairs (B1, B2):
+//           rows   A1  A2   B1  B2   S1 = A1 B1^T  S2 = A2 B2^T    outputs
+//   KV      keys   K   V    Q   dO   S^T           dP^T            dK += dS^T Q, dV += P^T dO
+//   Q       query  Q   dO   K   V    S             dP              dQ += dS K
+// The elementwise step writes dS (and P for KV) as bf16 128 x 64 K-major
+// tiles in shared memory, the A operands of the output MMAs; their B
+// operands are the streamed tiles read M/N-major (the same bytes).
+//
+// Warp roles as in the forward kernel: warp 0 TMA, warp 1 TMEM + MMA issue,
+// warps 4-7 elementwise (thread = row = TMEM lane).  All waits are bounded.
+#include "attn_common.cuh"
+
+namespace tpmlp {
+namespace {
+
+using namespace gemm;
+using namespace attn;
+
+template <int D, bool KV>
+__global__ void __launch_bounds__(ATT_THREADS, 1)
+    attn_bwd_kernel(const __grid_constant__ CUtensorMap tmA1,
+                    const __grid_constant__ CUtensorMap tmA2,
+                    const __grid_constant__ CUtensorMap tmB1,
+                    const __grid_constant__ CUtensorMap tmB2,
+                    const AttnArgs a) {
+  constexpr int KB = D / 64;
+  constexpr uint32_t A_TILE = KB * KBLOCK_BYTES;   // 128 rows x D
+  constexpr uint32_t B_TILE = KB * ATOM_BYTES;     // 64 rows x D
+  constexpr int NE = KV ? 2 : 1;                   // staged tiles per step
+  constexpr uint32_t E_TILE = KBLOCK_BYTES;        // 128 rows x 64
+  constexpr uint32_t VEC_BYTES = 512;              // 64 lse2 + 64 delta
+  constexpr uint32_t B_TX = 2 * B_TILE + (KV ? VEC_BYTES : 0);
+  constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 64, false, false);
+  constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, false, true);
+  constexpr uint32_t TMEM_OUT2 = 256;              // dK (KV) or dQ
+  constexpr uint32_t TMEM_OUT1 = 256 + D;          // dV (KV)
+  constexpr float INV_SQRT_D = D == 64 ? 0.125f : 0.08838834764831845f;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sA1 = ptx::smem_u32(smem);
+  const uint32_t sA2 = sA1 + A_TILE;
+  const uint32_t sB = sA2 + A_TILE;                // [stage][B1 | B2]
+  const uint32_t sE = sB + 4 * B_TILE;             // [stage][dS | P]
+  uint8_t* vec_gen = smem + 2 * A_TILE + 4 * B_TILE + 2 * NE * E_TILE;
+  const uint32_t sVec = ptx::smem_u32(vec_gen);    // [stage][lse2 | delta]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(vec_gen + 2 * VEC_BYTES);
+  const uint32_t b0 = ptx::smem_u32(bars);
+  const uint32_t a_full = b0, b_full = b0 + 8, b_empty = b0 + 24,
+                 s_full = b0 + 40, s_empty = b0 + 56, e_full = b0 + 72,
+                 e_empty = b0 + 88, o_full = b0 + 104, done_bar = b0 + 112;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nq = a.nq;
+  const int rb = KV ? static_cast<int>(blockIdx.x % nq)
+                    : nq - 1 - static_cast<int>(blockIdx.x % nq);
+  const int head = static_cast<int>((blockIdx.x / nq) % a.heads);
+  const int seq = static_cast<int>(blockIdx.x / (nq * a.heads));
+  const int row0 = seq * a.seq_len + rb * 128;
+  // 64-wide column blocks: queries >= the first key (KV), keys <= the last
+  // query (Q) when causal.
+  const int cb_begin = (KV && a.causal) ? 2 * rb : 0;
+  const int cb_end = (!KV && a.causal) ? 2 * rb + 2 : 2 * nq;
+  const int nsteps = cb_end - cb_begin;
+  const HeadCols hc = head_cols(a, head);
+  const int cA1 = KV ? hc.k : hc.q;
+  const int cA2 = KV ? hc.v : head * D;
+  const int cB1 = KV ? hc.q : hc.k;
+  const int cB2 = KV ? head * D : hc.v;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(a_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(b_full + 8 * i, 1);
+      ptx::mbar_init(b_empty + 8 * i, 1);
+      ptx::mbar_init(s_full + 8 * i, 1);
+      ptx::mbar_init(s_empty + 8 * i, 4);
+      ptx::mbar_init(e_full + 8 * i, 4);
+      ptx::mbar_init(e_empty + 8 * i, 1);
+    }
+    ptx::mbar_init(o_full, 1);
+    ptx::mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+  const Ctl ctl{abort_flag, a.status, a.budget_ns};
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------- producer --
+      ptx::mbar_arrive_expect_tx(a_full, 2 * A_TILE);
+#pragma unroll
+      for (int kk = 0; kk < KB; ++kk) {
+        ptx::tma_load_2d(sA1 + kk * KBLOCK_BYTES, &tmA1, a_full, cA1 + 64 * kk,
+                         row0);
+        ptx::tma_load_2d(sA2 + kk * KBLOCK_BYTES, &tmA2, a_full, cA2 + 64 * kk,
+                         row0);
+      }
+      for (int n = 0; n < nsteps; ++n) {
+        const uint32_t st = n & 1, ph = (n >> 1) & 1;
+        if (!wait_bounded(b_empty + 8 * st, ph ^ 1, ctl, ROLE_PRODUCER)) break;
+        const int col0 = seq * a.seq_len + (cb_begin + n) * 64;
+        const uint32_t bf = b_full + 8 * st;
+        const uint32_t dB1 = sB + st * 2 * B_TILE, dB2 = dB1 + B_TILE;
+        ptx::mbar_arrive_expect_tx(bf, B_TX);
+#pragma unroll
+        for (int kk = 0; kk < KB; ++kk) {
+          ptx::tma_load_2d(dB1 + kk * ATOM_BYTES, &tmB1, bf, cB1 + 64 * kk, col0);
+          ptx::tma_load_2d(dB2 + kk * ATOM_BYTES, &tmB2, bf, cB2 + 64 * kk, col0);
+        }
+        if constexpr (KV) {
+          const size_t off = static_cast<size_t>(head) * a.ld_stat + col0;
+          ptx::bulk_load_1d(sVec + st * VEC_BYTES, a.lse + off, 256, bf);
+          ptx::bulk_load_1d(sVec + st * VEC_BYTES + 256, a.delta + off, 256, bf);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // -------------------------------------------------- MMA issuer --
+      bool alive = wait_bounded(a_full, 0, ctl, ROLE_MMA);
+      auto issue_s = [&](int n) -> bool {
+        const uint32_t st = n & 1, ph = (n >> 1) & 1;
+        if (!wait_bounded(b_full + 8 * st, ph, ctl, ROLE_MMA)) return false;
+        if (!wait_bounded(s_empty + 8 * st, ph ^ 1, ctl, ROLE_MMA)) return false;
+        ptx::tc_fence_after();
+        const uint32_t dB1 = sB + st * 2 * B_TILE, dB2 = dB1 + B_TILE;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t ao = (k / 4) * KBLOCK_BYTES + (k % 4) * 32;
+          const uint32_t bo = (k / 4) * ATOM_BYTES + (k % 4) * 32;
+          ptx::mma_bf16(tmem + 64 * st, ptx::sdesc_sw128(sA1 + ao, 16, 1024),
+                        ptx::sdesc_sw128(dB1 + bo, 16, 1024), IDESC_S,
+                        k > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t ao = (k / 4) * KBLOCK_BYTES + (k % 4) * 32;
+          const uint32_t bo = (k / 4) * ATOM_BYTES + (k % 4) * 32;
+          ptx::mma_bf16(tmem + 128 + 64 * st,
+                        ptx::sdesc_sw128(sA2 + ao, 16, 1024),
+                        ptx::sdesc_sw128(dB2 + bo, 16, 1024), IDESC_S,
+                        k > 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(s_full + 8 * st);
+        return true;
+      };
+      auto issue_o = [&](int n) -> bool {
+        const uint32_t st = n & 1, ph = (n >> 1) & 1;
+        if (!wait_bounded(e_full + 8 * st, ph, ctl, ROLE_MMA)) return false;
+        ptx::tc_fence_after();
+        const uint32_t dB1 = sB + st * 2 * B_TILE, dB2 = dB1 + B_TILE;
+        const uint32_t e2 = sE + st * NE * E_TILE, e1 = e2 + E_TILE;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          ptx::mma_bf16(tmem + TMEM_OUT2, ptx::sdesc_sw128(e2 + 32 * k, 16, 1024),
+                        ptx::sdesc_sw128(dB1 + 2048 * k, ATOM_BYTES, 1024),
+                        IDESC_O, (n > 0 || k > 0) ? 1u : 0u);
+        if constexpr (KV) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            ptx::mma_bf16(tmem + TMEM_OUT1,
+                          ptx::sdesc_sw128(e1 + 32 * k, 16, 1024),
+                          ptx::sdesc_sw128(dB2 + 2048 * k, ATOM_BYTES, 1024),
+                          IDESC_O, (n > 0 || k > 0) ? 1u : 0u);
+        }
+        ptx::mma_commit(b_empty + 8 * st);
+        ptx::mma_commit(e_empty + 8 * st);
+        return true;
+      };
+      if (alive) alive = issue_s(0);
+      for (int n = 0; alive && n < nsteps; ++n) {
+        if (n + 1 < nsteps && !(alive = issue_s(n + 1))) break;
+        alive = issue_o(n);
+      }
+      if (alive) ptx::mma_commit(o_full);
+      if (*reinterpret_cast<volatile int*>(abort_flag)) {
+        ptx::mma_commit(done_bar);
+        wait_teardown(done_bar, 0);
+      }
+    }
+    __syncwarp();
+  } else if (warp >= SOFTMAX_WARP0) {
+    // -------------------------------------------------- elementwise --
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    const float sl2 = a.scale_log2;
+    float lse_r = 0.f, delta_r = 0.f;
+    if constexpr (!KV) {
+      const size_t off = static_cast<size_t>(head) * a.ld_stat + row0 + r;
+      lse_r = a.lse[off];
+      delta_r = a.delta[off];
+    }
+    const float* vec = reinterpret_cast<const float*>(vec_gen);
+    bool alive = true;
+    for (int n = 0; n < nsteps; ++n) {
+      const uint32_t st = n & 1, ph = (n >> 1) & 1;
+      if (!warp_wait(s_full + 8 * st, ph, ctl, ROLE_EPILOGUE) ||
+          (KV && !warp_wait(b_full + 8 * st, ph, ctl, ROLE_EPILOGUE)) ||
+          !warp_wait(e_empty + 8 * st, ph ^ 1, ctl, ROLE_EPILOGUE)) {
+        alive = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      const int cb = cb_begin + n;
+      // Causal validity of column c: KV (row = key): c >= lo; Q (row =
+      // query): c <= hi.  Without the mask every column is valid.
+      const int diff = rb * 128 + r - cb * 64;
+      const int lo = (KV && a.causal) ? diff : -1;
+      const int hi = (!KV && a.causal) ? diff : 64;
+      const float* vl = vec + st * (VEC_BYTES / 4);
+      const float* vd = vl + 64;
+      const uint32_t e2 = sE + st * NE * E_TILE, e1 = e2 + E_TILE;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t s1[32], s2[32];
+        ptx::tmem_ld_32x32b_x32(tmem + lane_base + 64 * st + 32 * half, s1);
+        ptx::tmem_ld_32x32b_x32(tmem + lane_base + 128 + 64 * st + 32 * half, s2);
+        ptx::tmem_ld_wait();
+        uint32_t pw[16], dw[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          float ds[2], p[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int c = 32 * half + i + u;
+            const float L = KV ? vl[c] : lse_r;
+            const float Dl = KV ? vd[c] : delta_r;
+            float pv = exp2f(fmaf(__uint_as_float(s1[i + u]), sl2, -L));
+            pv = (c >= lo && c <= hi) ? pv : 0.f;
+            p[u] = pv;
+            ds[u] = pv * (__uint_as_float(s2[i + u]) - Dl) * INV_SQRT_D;
+          }
+          pw[i / 2] = pack_bf16x2(p[0], p[1]);
+          dw[i / 2] = pack_bf16x2(ds[0], ds[1]);
+        }
+        stage_units<16>(e2, r, 4 * half, dw);
+        if constexpr (KV) stage_units<16>(e1, r, 4 * half, pw);
+      }
+      ptx::tc_fence_before();
+      ptx::fence_proxy_async_shared();
+      __syncwarp();
+      if (lane == 0) {
+        ptx::mbar_arrive(s_empty + 8 * st);
+        ptx::mbar_arrive(e_full + 8 * st);
+      }
+    }
+    if (alive && warp_wait(o_full, 0, ctl, ROLE_EPILOGUE)) {
+      ptx::tc_fence_after();
+      __nv_bfloat16* rowp = a.dqkv + static_cast<size_t>(row0 + r) * a.ld_qkv;
+      __nv_bfloat16* out2 = rowp + (KV ? hc.k : hc.q);
+#pragma unroll
+      for (int j = 0; j < D / 32; ++j) {
+        uint32_t ov[32];
+        ptx::tmem_ld_32x32b_x32(tmem + lane_base + TMEM_OUT2 + 32 * j, ov);
+        ptx::tmem_ld_wait();
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(ov[i]);
+        store_bf16x32(out2 + 32 * j, v);
+      }
+      if constexpr (KV) {
+        __nv_bfloat16* out1 = rowp + hc.v;
+#pragma unroll
+        for (int j = 0; j < D / 32; ++j) {
+          uint32_t ov[32];
+          ptx::tmem_ld_32x32b_x32(tmem + lane_base + TMEM_OUT1 + 32 * j, ov);
+          ptx::tmem_ld_wait();
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(ov[i]);
+          store_bf16x32(out1 + 32 * j, v);
+        }
+      }
+    }
+    __syncwarp();
+  }
+
+  // --------------------------------------------------------- teardown --
+  ptx::tc_fence_before();
+  cta_barrier_att();
+  if (*reinterpret_cast<volatile int*>(abort_flag) && threadIdx.x == 0) {
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (ptx::globaltimer_ns() - t0 < ABORT_SETTLE_NS) {
+    }
+  }
+  cta_barrier_att();
+  if (warp == 1) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+// Dynamic shared memory; at least 116 KB so that a second CTA (and its 512
+// TMEM columns) never shares the SM.
+template <int D, bool KV>
+size_t attn_bwd_smem() {
+  constexpr int KB = D / 64;
+  const size_t need = 1024 + 2 * KB * KBLOCK_BYTES + 4 * KB * ATOM_BYTES +
+                      2 * (KV ? 2 : 1) * KBLOCK_BYTES + 1024 + 15 * 8 + 16;
+  return need > 116 * 1024 ? need : 116 * 1024;
+}
+
+template <int D, bool KV>
+cudaError_t launch_bwd(const CUtensorMap& a1, const CUtensorMap& a2,
+                       const CUtensorMap& b1, const CUtensorMap& b2,
+                       const AttnArgs& a, int grid, cudaStream_t s) {
+  auto kern = attn_bwd_kernel<D, KV>;
+  const size_t smem = attn_bwd_smem<D, KV>();
+  cudaError_t e = cudaFuncSetAttribute(
+      kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  kern<<<grid, ATT_THREADS, smem, s>>>(a1, a2, b1, b2, a);
+  return cudaGetLastError();
+}
+
+// delta[j][t] = sum_e dCtx[t][j d + e] * Ctx[t][j d + e]: one warp per
+// (token, head), fp32 accumulation of bf16 products.
+__global__ void attn_delta_kernel(const __nv_bfloat16* __restrict__ dctx,
+                                  const __nv_bfloat16* __restrict__ ctx,
+                                  float* __restrict__ delta, int T, int h,
+                                  int heads, int d, long long ld_stat) {
+  const long long gw = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) +
+                       (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (gw >= static_cast<long long>(T) * heads) return;
+  const int t = static_cast<int>(gw / heads);
+  const int j = static_cast<int>(gw - static_cast<long long>(t) * heads);
+  const size_t base = static_cast<size_t>(t) * h + static_cast<size_t>(j) * d;
+  const uint32_t* pd = reinterpret_cast<const uint32_t*>(dctx + base);
+  const uint32_t* pc = reinterpret_cast<const uint32_t*>(ctx + base);
+  float acc = 0.f;
+  for (int e = lane; e < d / 2; e += 32) {
+    float d0, d1, c0, c1;
+    unpack_bf16x2(pd[e], d0, d1);
+    unpack_bf16x2(pc[e], c0, c1);
+    acc = fmaf(d0, c0, acc);
+    acc = fmaf(d1, c1, acc);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) delta[static_cast<size_t>(j) * ld_stat + t] = acc;
+}
+
+}  // namespace
+
+cudaError_t launch_attn_dkdv(const CUtensorMap& tq128, const CUtensorMap& tq64,
+                             const CUtensorMap& tdo64, const AttnArgs& a,
+                             int grid, cudaStream_t s) {
+  if (a.head_dim == 128)
+    return launch_bwd<128, true>(tq128, tq128, tq64, tdo64, a, grid, s);
+  if (a.head_dim == 64)
+    return launch_bwd<64, true>(tq128, tq128, tq64, tdo64, a, grid, s);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_attn_dq(const CUtensorMap& tq128, const CUtensorMap& tq64,
+                           const CUtensorMap& tdo128, const AttnArgs& a,
+                           int grid, cudaStream_t s) {
+  if (a.head_dim == 128)
+    return launch_bwd<128, false>(tq128, tdo128, tq64, tq64, a, grid, s);
+  if (a.head_dim == 64)
+    return launch_bwd<64, false>(tq128, tdo128, tq64, tq64, a, grid, s);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_attn_delta(const AttnArgs& a, float* delta, int tokens,
+                              cudaStream_t s) {
+  const long long warps = static_cast<long long>(tokens) * a.heads;
+  if (warps == 0) return cudaSuccess;
+  const int blocks = static_cast<int>((warps + 7) / 8);
+  attn_delta_kernel<<<blocks, 256, 0, s>>>(a.dctx, a.ctx, delta, tokens,
+                                           a.heads * a.head_dim, a.heads,
+                                           a.head_dim, a.ld_stat);
+  return cudaGetLastError();
+}
+
+}  // namespace tpmlp

@@ -1,0 +1,338 @@
+// Attention core of the head-parallel self-attention block on sm_103a.
+//
+// The heads are independent (Megatron-LM explainer, section on attention;
+// notes, "Self-attention block split"), so each CTA owns one (sequence,
+// head, 128-query block) and never communicates.  Q, K and V are read in
+// place from the fused projection output QKV [T, 3h] (columns grouped by
+// shard: [Q_i | K_i | V_i], head j of shard i at offset (j mod H/t) d inside
+// each group) through TMA tensor maps; scores and the output accumulator
+// live in TMEM; the probabilities are staged in shared memory as the bf16 A
+// operand of the second MMA.
+//
+// Forward, two passes over the key blocks the query block may see (all of
+// them, or blocks 0..qb when causal):
+//   pass 1: S = Q K^T (tcgen05, M = N = 128, K = d) -> running row max m
+//           and row sum l of exp2(S log2e / sqrt d - m);
+//   pass 2: S again -> P = exp2(S log2e / sqrt d - m) / l (exact
+//           probabilities, so the output accumulator is never rescaled) ->
+//           bf16 P in shared memory -> O += P V.
+// Outputs: the context rows (bf16) and, for the backward, every (head,
+// token) row's log-sum-exp in base 2 of the scores scaled by log2(e)/sqrt(d),
+// lse2 = m + log2(l), so that P = exp2(S log2(e)/sqrt(d) - lse2).
+//
+// Warp roles (256 threads): warp 0 TMA producer, warp 1 TMEM allocator and
+// MMA issuer (one lane), warps 4-7 softmax (thread = query row = TMEM lane).
+// All waits are bounded as in the GEMM kernels.
+#include "attn_common.cuh"
+
+namespace tpmlp {
+namespace {
+
+using namespace gemm;
+using namespace attn;
+
+template <int D>
+__global__ void __launch_bounds__(ATT_THREADS, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQK,
+                    const __grid_constant__ CUtensorMap tmV,
+                    const AttnArgs a) {
+  constexpr int KB = D / 64;                           // 64-wide blocks of d
+  constexpr uint32_t QK_TILE = KB * KBLOCK_BYTES;      // 128 x D
+  constexpr uint32_t V_TILE = 2 * KB * ATOM_BYTES;     // 128 keys x D
+  constexpr uint32_t P_TILE = 2 * KBLOCK_BYTES;        // 128 x 128
+  constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, false, false);
+  constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, false, true);
+  constexpr uint32_t TMEM_O = 256;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sQ = ptx::smem_u32(smem);
+  const uint32_t sK = sQ + QK_TILE;
+  const uint32_t sV = sK + 2 * QK_TILE;
+  const uint32_t sP = sV + 2 * V_TILE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + QK_TILE * 3 + V_TILE * 2 + P_TILE);
+  const uint32_t b0 = ptx::smem_u32(bars);
+  const uint32_t q_full = b0, k_full = b0 + 8, k_empty = b0 + 24,
+                 v_full = b0 + 40, v_empty = b0 + 56, s_full = b0 + 72,
+                 s_empty = b0 + 88, p_full = b0 + 104, p_empty = b0 + 112,
+                 o_full = b0 + 120, done_bar = b0 + 128;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 17);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nq = a.nq;
+  const int qb = nq - 1 - static_cast<int>(blockIdx.x % nq);
+  const int head = static_cast<int>((blockIdx.x / nq) % a.heads);
+  const int seq = static_cast<int>(blockIdx.x / (nq * a.heads));
+  const int row0 = seq * a.seq_len + qb * 128;
+  const int nk = a.causal ? qb + 1 : nq;
+  const HeadCols hc = head_cols(a, head);
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(k_full + 8 * i, 1);
+      ptx::mbar_init(k_empty + 8 * i, 1);
+      ptx::mbar_init(v_full + 8 * i, 1);
+      ptx::mbar_init(v_empty + 8 * i, 1);
+      ptx::mbar_init(s_full + 8 * i, 1);
+      ptx::mbar_init(s_empty + 8 * i, 4);
+    }
+    ptx::mbar_init(p_full, 4);
+    ptx::mbar_init(p_empty, 1);
+    ptx::mbar_init(o_full, 1);
+    ptx::mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+  const Ctl ctl{abort_flag, a.status, a.budget_ns};
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------- producer --
+      bool alive = true;
+      ptx::mbar_arrive_expect_tx(q_full, QK_TILE);
+#pragma unroll
+      for (int kk = 0; kk < KB; ++kk)
+        ptx::tma_load_2d(sQ + kk * KBLOCK_BYTES, &tmQK, q_full, hc.q + 64 * kk, row0);
+      uint32_t kc = 0, vc = 0;
+      for (int pass = 0; alive && pass < 2; ++pass) {
+        for (int kb = 0; alive && kb < nk; ++kb) {
+          const int key0 = seq * a.seq_len + kb * 128;
+          const uint32_t ks = kc & 1, kph = (kc >> 1) & 1;
+          if (!wait_bounded(k_empty + 8 * ks, kph ^ 1, ctl, ROLE_PRODUCER)) {
+            alive = false;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(k_full + 8 * ks, QK_TILE);
+#pragma unroll
+          for (int kk = 0; kk < KB; ++kk)
+            ptx::tma_load_2d(sK + ks * QK_TILE + kk * KBLOCK_BYTES, &tmQK,
+                             k_full + 8 * ks, hc.k + 64 * kk, key0);
+          ++kc;
+          if (pass == 1) {
+            const uint32_t vs = vc & 1, vph = (vc >> 1) & 1;
+            if (!wait_bounded(v_empty + 8 * vs, vph ^ 1, ctl, ROLE_PRODUCER)) {
+              alive = false;
+              break;
+            }
+            ptx::mbar_arrive_expect_tx(v_full + 8 * vs, V_TILE);
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+              for (int at = 0; at < KB; ++at)
+                ptx::tma_load_2d(sV + vs * V_TILE + (h2 * KB + at) * ATOM_BYTES,
+                                 &tmV, v_full + 8 * vs, hc.v + 64 * at,
+                                 key0 + 64 * h2);
+            ++vc;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // -------------------------------------------------- MMA issuer --
+      bool alive = wait_bounded(q_full, 0, ctl, ROLE_MMA);
+      uint32_t kc = 0, sc = 0, vc = 0;
+      auto issue_s = [&]() -> bool {
+        const uint32_t ks = kc & 1, kph = (kc >> 1) & 1;
+        const uint32_t sb = sc & 1, sph = (sc >> 1) & 1;
+        if (!wait_bounded(k_full + 8 * ks, kph, ctl, ROLE_MMA)) return false;
+        if (!wait_bounded(s_empty + 8 * sb, sph ^ 1, ctl, ROLE_MMA)) return false;
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint64_t ad = ptx::sdesc_sw128(
+              sQ + (k / 4) * KBLOCK_BYTES + (k % 4) * 32, 16, 1024);
+          const uint64_t bd = ptx::sdesc_sw128(
+              sK + ks * QK_TILE + (k / 4) * KBLOCK_BYTES + (k % 4) * 32, 16, 1024);
+          ptx::mma_bf16(tmem + sb * 128, ad, bd, IDESC_S, k > 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(k_empty + 8 * ks);
+        ptx::mma_commit(s_full + 8 * sb);
+        ++kc;
+        ++sc;
+        return true;
+      };
+      for (int kb = 0; alive && kb < nk; ++kb) alive = issue_s();  // pass 1
+      if (alive) alive = issue_s();                                  // pass 2
+      for (int kb = 0; alive && kb < nk; ++kb) {
+        if (kb + 1 < nk && !(alive = issue_s())) break;
+        const uint32_t vs = vc & 1, vph = (vc >> 1) & 1;
+        if (!wait_bounded(p_full, kb & 1, ctl, ROLE_MMA) ||
+            !wait_bounded(v_full + 8 * vs, vph, ctl, ROLE_MMA)) {
+          alive = false;
+          break;
+        }
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint64_t ad = ptx::sdesc_sw128(
+              sP + (k / 4) * KBLOCK_BYTES + (k % 4) * 32, 16, 1024);
+          const uint64_t bd = ptx::sdesc_sw128(
+              sV + vs * V_TILE + (k / 4) * KB * ATOM_BYTES + (k % 4) * 2048,
+              ATOM_BYTES, 1024);
+          ptx::mma_bf16(tmem + TMEM_O, ad, bd, IDESC_O,
+                        (kb > 0 || k > 0) ? 1u : 0u);
+        }
+        ptx::mma_commit(v_empty + 8 * vs);
+        ptx::mma_commit(p_empty);
+        ++vc;
+      }
+      if (alive) ptx::mma_commit(o_full);
+      if (*reinterpret_cast<volatile int*>(abort_flag)) {
+        ptx::mma_commit(done_bar);
+        wait_teardown(done_bar, 0);
+      }
+    }
+    __syncwarp();
+  } else if (warp >= SOFTMAX_WARP0) {
+    // ------------------------------------------------------ softmax --
+    // Pass 1 finds the row max m of the scaled scores (log2 units); pass 2
+    // writes P = exp2(x - m) (final max, so nothing is ever rescaled),
+    // accumulates l = sum P in fp32, and the output is O / l.
+    const int q = warp & 3;
+    const int r = q * 32 + lane;          // query row inside the block
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    const float sl2 = a.scale_log2;
+    float m = -INFINITY, l = 0.f;
+    uint32_t sc = 0;
+    bool alive = true;
+    for (int kb = 0; kb < nk; ++kb) {
+      const uint32_t sb = sc & 1, sph = (sc >> 1) & 1;
+      if (!warp_wait(s_full + 8 * sb, sph, ctl, ROLE_EPILOGUE)) {
+        alive = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      uint32_t sv[128];
+      tmem_ld_128(tmem + lane_base + sb * 128, sv);
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(s_empty + 8 * sb);
+      ++sc;
+      const int lim = (a.causal && kb == qb) ? r : 127;
+      float mb = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 128; ++c)
+        if (c <= lim) mb = fmaxf(mb, __uint_as_float(sv[c]));
+      m = fmaxf(m, mb * sl2);
+    }
+    for (int kb = 0; alive && kb < nk; ++kb) {
+      const uint32_t sb = sc & 1, sph = (sc >> 1) & 1;
+      if (!warp_wait(s_full + 8 * sb, sph, ctl, ROLE_EPILOGUE) ||
+          !warp_wait(p_empty, (kb & 1) ^ 1, ctl, ROLE_EPILOGUE)) {
+        alive = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      const int lim = (a.causal && kb == qb) ? r : 127;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t sv[64];
+        uint32_t (&s0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[0]);
+        uint32_t (&s1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[32]);
+        const uint32_t col = tmem + lane_base + sb * 128 + 64 * half;
+        ptx::tmem_ld_32x32b_x32(col, s0);
+        ptx::tmem_ld_32x32b_x32(col + 32, s1);
+        ptx::tmem_ld_wait();
+        uint32_t w[32];
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) {
+          const int cc = 64 * half + c;
+          float p0 = exp2f(fmaf(__uint_as_float(sv[c]), sl2, -m));
+          float p1 = exp2f(fmaf(__uint_as_float(sv[c + 1]), sl2, -m));
+          p0 = cc <= lim ? p0 : 0.f;
+          p1 = cc + 1 <= lim ? p1 : 0.f;
+          l += p0 + p1;
+          w[c / 2] = pack_bf16x2(p0, p1);
+        }
+        stage_row64(sP + half * KBLOCK_BYTES, r, w);
+      }
+      ptx::tc_fence_before();
+      ptx::fence_proxy_async_shared();
+      __syncwarp();
+      if (lane == 0) {
+        ptx::mbar_arrive(s_empty + 8 * sb);
+        ptx::mbar_arrive(p_full);
+      }
+      ++sc;
+    }
+    if (alive && warp_wait(o_full, 0, ctl, ROLE_EPILOGUE)) {
+      ptx::tc_fence_after();
+      const float inv_l = 1.0f / l;
+      __nv_bfloat16* out = a.ctx + static_cast<size_t>(row0 + r) * a.ld_ctx +
+                           head * D;
+#pragma unroll
+      for (int j = 0; j < D / 32; ++j) {
+        uint32_t ov[32];
+        ptx::tmem_ld_32x32b_x32(tmem + lane_base + TMEM_O + 32 * j, ov);
+        ptx::tmem_ld_wait();
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(ov[i]) * inv_l;
+        store_bf16x32(out + 32 * j, v);
+      }
+      a.lse[static_cast<size_t>(head) * a.ld_stat + row0 + r] = m + log2f(l);
+    }
+    __syncwarp();
+  }
+
+  // --------------------------------------------------------- teardown --
+  ptx::tc_fence_before();
+  cta_barrier_att();
+  if (*reinterpret_cast<volatile int*>(abort_flag) && threadIdx.x == 0) {
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (ptx::globaltimer_ns() - t0 < ABORT_SETTLE_NS) {
+    }
+  }
+  cta_barrier_att();
+  if (warp == 1) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+// Dynamic shared memory; at least 116 KB so that a second CTA (and its 512
+// TMEM columns) never shares the SM.
+template <int D>
+size_t attn_fwd_smem() {
+  constexpr int KB = D / 64;
+  const size_t need = 1024 + 3 * KB * KBLOCK_BYTES + 2 * (2 * KB * ATOM_BYTES) +
+                      2 * KBLOCK_BYTES + 17 * 8 + 16;
+  return need > 116 * 1024 ? need : 116 * 1024;
+}
+
+template <int D>
+cudaError_t launch_fwd(const CUtensorMap& tqk, const CUtensorMap& tv,
+                       const AttnArgs& a, int grid, cudaStream_t s) {
+  auto kern = attn_fwd_kernel<D>;
+  const size_t smem = attn_fwd_smem<D>();
+  cudaError_t e = cudaFuncSetAttribute(
+      kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  kern<<<grid, ATT_THREADS, smem, s>>>(tqk, tv, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_fwd(const CUtensorMap& tqk, const CUtensorMap& tv,
+                            const AttnArgs& a, int grid, cudaStream_t s) {
+  if (a.head_dim == 128) return launch_fwd<128>(tqk, tv, a, grid, s);
+  if (a.head_dim == 64) return launch_fwd<64>(tqk, tv, a, grid, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace tpmlp

@@ -245,13 +245,16 @@ inline bool use_pairs() {
 // Box height of a K-major B operand for the selected kernel.
 inline int b_box_rows() { return use_pairs() ? TC2_BN_HALF : TC_BN; }
 
-// One GEMM launch.  The pair kernel writes through output tensor maps,
+// One GEMM launch (the pair kernel when selected or `force_pairs`; K-major B
+// maps must then use TC2_BN_HALF-row boxes).  The pair kernel writes through
+// output tensor maps,
 // encoded here from args.out / args.out2 (row-major, leading dimension
 // args.ldo, element type fp32 for the fp32-output epilogues).
 inline int tc_gemm(HandleCore* H, const char* name, cudaStream_t s, int sms,
             int epi, bool a_mn, bool b_mn, const CUtensorMap& ta,
-            const CUtensorMap& tb, const GemmArgs& args) {
-  if (use_pairs()) {
+            const CUtensorMap& tb, const GemmArgs& args,
+            bool force_pairs = false) {
+  if (force_pairs || use_pairs()) {
     const bool f32 = epi == EPI_STORE_F32 || (epi == EPI_SHARDSUM && args.out_f32);
     CUtensorMap to, to2;
     TRY(out_map(&to, args.out, f32, args.M, args.N, args.ldo));

@@ -87,6 +87,52 @@ cudaError_t launch_dropout_grad(bool bf16, const void* dZ, void* out, int rows,
                                 unsigned long long offset,
                                 cudaStream_t stream);
 
+// ---------------------------------------------------------------- attention
+// Head-parallel attention core over the fused projection QKV [T, 3h]
+// (columns grouped by shard: [Q_i | K_i | V_i], each h/t wide; head j of
+// shard i = j / (H/t) sits at offset (j mod H/t) d inside each group).
+// Tokens are sequence-major: T = batches * seq_len, seq_len % 128 == 0.
+struct AttnArgs {
+  int heads;            // H
+  int heads_per_shard;  // H / t
+  int head_dim;         // d (64 or 128)
+  int shard_width;      // h / t
+  int seq_len;
+  int nq;               // seq_len / 128
+  int causal;
+  float scale_log2;     // log2(e) / sqrt(d)
+  __nv_bfloat16* ctx;   // forward output [T, h], head j in columns j d..
+  long long ld_ctx;
+  float* lse;           // [H, T] base-2 log-sum-exp of the scores scaled by
+                        // log2(e) / sqrt(d)
+  long long ld_stat;    // row pitch of lse / delta (= T)
+  const __nv_bfloat16* dctx;  // backward: dCtx [T, h]
+  const float* delta;         // backward: rowsum(dCtx * Ctx) per head [H, T]
+  __nv_bfloat16* dqkv;        // backward output [T, 3h] (same layout as QKV)
+  long long ld_qkv;
+  int* status;
+  unsigned long long budget_ns;
+};
+
+// Forward: tqk maps QKV with 64 x 128 boxes (Q and K tiles), tv with
+// 64 x 64 boxes (V tiles, M/N-major operand).  grid = batches * H * nq.
+cudaError_t launch_attn_fwd(const CUtensorMap& tqk, const CUtensorMap& tv,
+                            const AttnArgs& a, int grid, cudaStream_t stream);
+
+// Backward, stage 1: delta[j][t] = rowsum(dCtx * Ctx) over head j's columns.
+cudaError_t launch_attn_delta(const AttnArgs& a, float* delta, int tokens,
+                              cudaStream_t stream);
+// Backward, key/value gradients (one CTA per 128 keys of a sequence and
+// head) and query gradients (one CTA per 128 queries).  tq128 / tq64 map
+// QKV with 64 x 128 / 64 x 64 boxes, tdo128 / tdo64 map dCtx [T, h] alike.
+// Both write their columns of a.dqkv; grid = batches * H * nq.
+cudaError_t launch_attn_dkdv(const CUtensorMap& tq128, const CUtensorMap& tq64,
+                             const CUtensorMap& tdo64, const AttnArgs& a,
+                             int grid, cudaStream_t stream);
+cudaError_t launch_attn_dq(const CUtensorMap& tq128, const CUtensorMap& tq64,
+                           const CUtensorMap& tdo128, const AttnArgs& a,
+                           int grid, cudaStream_t stream);
+
 // Record a message for tp_mlp_last_detail() on the calling thread.
 void set_last_detail(const char* msg);
 

@@ -75,6 +75,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m,
       : "memory");
 }
 
+// Plain (untiled) bulk copy global -> shared of `bytes` bytes (multiple of
+// 16, both addresses 16-byte aligned), completing on `bar` as tx bytes.
+__device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src,
+                                             uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 // 2-D tiled store shared -> global (bulk-group completion).  Elements of the
 // box that fall outside the tensor are not written.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, uint32_t src,

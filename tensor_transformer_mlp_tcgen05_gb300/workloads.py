@@ -1,4 +1,4 @@
-"""Seeded synthetic inputs for the tensor-parallel MLP block.
+"""Seeded synthetic inputs for the tensor-parallel MLP and attention blocks.
 
 This module only draws random numbers and names shapes. It holds none of the
 block's arithmetic, so both the CUDA path (through the Python binding) and the
@@ -126,3 +126,88 @@ def sample_indices(n: int, k: int, seed: int) -> torch.Tensor:
     idx = torch.randperm(n, generator=g)[: k - 1]
     idx = torch.unique(torch.cat([idx, torch.tensor([n - 1])]))
     return idx
+
+
+# ------------------------------------------------------------- attention --
+
+@dataclasses.dataclass(frozen=True)
+class AttnWorkload:
+    """Head-parallel self-attention block: T = batch * seq tokens,
+    sequence-major; d = hidden / heads."""
+    name: str
+    batch: int
+    seq: int
+    hidden: int
+    heads: int
+    shards: int
+    causal: bool = True
+    layernorm: bool = False
+    x_std: float = 1.0
+    w_std: float = 0.02
+    dz_std: float = 1.0
+
+    @property
+    def tokens(self) -> int:
+        return self.batch * self.seq
+
+    @property
+    def head_dim(self) -> int:
+        return self.hidden // self.heads
+
+    def score_pairs(self) -> int:
+        """(query, key) pairs the softmax sees, over all sequences and heads."""
+        per = self.seq * (self.seq + 1) // 2 if self.causal else self.seq ** 2
+        return self.batch * self.heads * per
+
+    def flops_fwd(self) -> float:
+        """Projections 2 T h (3h + h) plus Q K^T and P V over the unmasked
+        pairs (2 d each)."""
+        T, h = self.tokens, self.hidden
+        return 8.0 * T * h * h + 4.0 * self.head_dim * self.score_pairs()
+
+    def flops_fwd_bwd(self) -> float:
+        """Forward plus backward: each projection twice more (input and
+        weight gradients), and dV, dP, dQ, dK over the unmasked pairs."""
+        T, h = self.tokens, self.hidden
+        return 24.0 * T * h * h + 12.0 * self.head_dim * self.score_pairs()
+
+    def with_(self, **kw) -> "AttnWorkload":
+        return dataclasses.replace(self, **kw)
+
+
+ATTN_WORKLOADS = {
+    # small cases the oracle finishes in seconds (several 128-row blocks)
+    "attn_tiny_d64": AttnWorkload("attn_tiny_d64", 2, 256, 256, 4, 2,
+                                  w_std=0.0625),
+    "attn_tiny_d128": AttnWorkload("attn_tiny_d128", 2, 384, 512, 4, 2,
+                                   w_std=0.044),
+    # GPT-2-medium-shaped and GPT-3-13B-shaped layers (as the MLP workloads)
+    "attn_gpt2_medium": AttnWorkload("attn_gpt2_medium", 8, 1024, 1024, 16, 4),
+    "attn_gpt3_13b": AttnWorkload("attn_gpt3_13b", 4, 2048, 5120, 40, 8),
+}
+
+
+def make_attn_inputs(w: AttnWorkload, seed: int = 0, with_bias: bool = False,
+                     bias_std: float = 0.5):
+    """CPU tensors for attention workload ``w``: draw order X [T,h],
+    W_qkv [h,3h], W_o [h,h], then b_qkv [3h] and b_o [h] (fp32, only with
+    ``with_bias``), then dZ [T,h]; bf16 storage, LayerNorm gamma = 1,
+    beta = 0 when ``w.layernorm``."""
+    g = torch.Generator("cpu")
+    g.manual_seed(seed)
+    bf = torch.bfloat16
+    T, h = w.tokens, w.hidden
+    X = _normal(g, T, h, w.x_std, bf)
+    Wqkv = _normal(g, h, 3 * h, w.w_std, bf)
+    Wo = _normal(g, h, h, w.w_std, bf)
+    bqkv = bo = None
+    if with_bias:
+        bqkv = _normal(g, 1, 3 * h, bias_std, torch.float32).reshape(3 * h)
+        bo = _normal(g, 1, h, bias_std, torch.float32).reshape(h)
+    dZ = _normal(g, T, h, w.dz_std, bf)
+    gamma = beta = None
+    if w.layernorm:
+        gamma = torch.ones(h, dtype=torch.float32)
+        beta = torch.zeros(h, dtype=torch.float32)
+    return dict(X=X, Wqkv=Wqkv, Wo=Wo, bqkv=bqkv, bo=bo, gamma=gamma,
+                beta=beta, dZ=dZ)

@@ -19,9 +19,12 @@ def lib():
 
 
 def _declared_functions():
-    text = open(os.path.join(ROOT, "include", "tp_mlp.h")).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(tp_mlp_\w+)\s*\(", text)))
+    names = set()
+    for hdr in ("tp_mlp.h", "tp_attn.h"):
+        text = open(os.path.join(ROOT, "include", hdr)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names |= set(re.findall(r"\b(tp_(?:mlp|attn)_\w+)\s*\(", text))
+    return sorted(names)
 
 
 def _cfg(**kw):
@@ -34,7 +37,7 @@ def _cfg(**kw):
 
 def test_every_declared_symbol_is_exported(lib):
     declared = _declared_functions()
-    assert len(declared) >= 13
+    assert len(declared) >= 27
     for name in declared:
         assert hasattr(lib, name), name
     assert sorted(B.EXPORTED) == declared
@@ -122,3 +125,94 @@ def test_layernorm_config_requires_parameters(lib):
         assert rc == B.TPMLP_ERR_ARG
     finally:
         B.tp_mlp_destroy(h)
+
+
+# ------------------------------------------------------------- attention --
+
+def _acfg(**kw):
+    base = dict(hidden=256, heads=4, shards=2, max_tokens=512, seq_len=256,
+                causal=1, use_layernorm=0, ln_eps=1e-5, use_residual=0)
+    base.update(kw)
+    return B.tp_attn_config(**base)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(heads=3), B.TPMLP_ERR_SHAPE),              # h % H
+    (dict(heads=8), B.TPMLP_ERR_SHAPE),              # d = 32
+    (dict(hidden=384, heads=4), B.TPMLP_ERR_SHAPE),  # d = 96
+    (dict(heads=4, shards=3), B.TPMLP_ERR_SHAPE),    # H % t
+    (dict(seq_len=200), B.TPMLP_ERR_SHAPE),          # seq % 128
+    (dict(shards=0), B.TPMLP_ERR_SHAPE),
+    (dict(max_tokens=-1), B.TPMLP_ERR_SHAPE),
+    (dict(causal=2), B.TPMLP_ERR_ARG),
+    (dict(use_residual=5), B.TPMLP_ERR_ARG),
+    (dict(use_layernorm=1, ln_eps=float("inf")), B.TPMLP_ERR_ARG),
+])
+def test_attn_create_rejects_bad_configs(lib, kw, code):
+    h = ctypes.c_void_p()
+    assert lib.tp_attn_create(ctypes.byref(_acfg(**kw)), ctypes.byref(h)) == code
+    assert h.value is None
+
+
+@pytest.mark.parametrize("kw", [
+    dict(hidden=128, heads=2, shards=2),     # h_t = 64, d = 64
+    dict(hidden=5120, heads=40, shards=8),   # d = 128, 5 heads per shard
+    dict(causal=0, use_layernorm=1, use_residual=1, max_tokens=0),
+])
+def test_attn_create_accepts_valid_corners(lib, kw):
+    h = B.tp_attn_create(_acfg(**kw))
+    B.tp_attn_destroy(h)
+
+
+def test_attn_workspace_layout(lib):
+    h = B.tp_attn_create(_acfg(use_layernorm=1))
+    try:
+        T, hd, H = 512, 256, 4
+        inf = B.tp_attn_workspace_bytes(h, T, 0)
+        trn = B.tp_attn_workspace_bytes(h, T, 1)
+        # inference: status, Xn, mean, rstd, QKV, Ctx, lse; training adds
+        # dCtx, delta, dQKV, dXn (fp32) and column-sum partials.
+        assert inf >= 256 + T * hd * 2 + 2 * T * 4 + T * 3 * hd * 2 + \
+            T * hd * 2 + H * T * 4
+        assert trn >= inf + T * hd * 2 + H * T * 4 + T * 3 * hd * 2 + T * hd * 4
+        offs = [B.tp_attn_workspace_offset(h, T, 1, k) for k in range(4)]
+        assert all(o % 256 == 0 for o in offs)
+        assert offs == sorted(offs) and offs[-1] < trn
+        assert B.tp_attn_workspace_offset(h, T, 0, B.TPATTN_WS_DQKV) == -1
+        assert B.tp_attn_workspace_offset(h, T, 1, 9) == -1
+        assert B.tp_attn_workspace_bytes(None, T, 1) == 0
+        assert B.tp_attn_launch_count(h) == 0
+    finally:
+        B.tp_attn_destroy(h)
+
+
+def test_attn_host_validation_before_device(lib):
+    """Argument errors are reported without touching a device (there is
+    none here): bad token counts, NULL weights, misaligned pointers, a small
+    workspace."""
+    h = B.tp_attn_create(_acfg())
+    L = lib
+    try:
+        ws = 1 << 20
+        # tokens not a multiple of seq_len, or above max_tokens
+        assert L.tp_attn_forward(h, 100, 16, 16, 16, None, None, None, None,
+                                 16, 16, ws, 1, None) == B.TPMLP_ERR_SHAPE
+        assert L.tp_attn_forward(h, 768, 16, 16, 16, None, None, None, None,
+                                 16, 16, ws, 1, None) == B.TPMLP_ERR_SHAPE
+        # NULL weights
+        assert L.tp_attn_forward(h, 256, 16, None, 16, None, None, None, None,
+                                 16, 16, ws, 1, None) == B.TPMLP_ERR_ARG
+        # misaligned
+        assert L.tp_attn_forward(h, 256, 18, 16, 16, None, None, None, None,
+                                 16, 16, ws, 1, None) == B.TPMLP_ERR_ALIGN
+        # workspace too small
+        assert L.tp_attn_forward(h, 256, 16, 16, 16, None, None, None, None,
+                                 16, 16, 64, 1, None) == B.TPMLP_ERR_WORKSPACE
+        assert L.tp_attn_backward(h, 256, 16, 16, 16, 16, None, 16, 64, 16,
+                                  16, 16, None, None, None, None,
+                                  None) == B.TPMLP_ERR_WORKSPACE
+        assert L.tp_attn_backward(h, 256, 16, 16, 16, 16, None, 16, ws, 16,
+                                  None, 16, None, None, None, None,
+                                  None) == B.TPMLP_ERR_ARG
+    finally:
+        B.tp_attn_destroy(h)

@@ -1,0 +1,158 @@
+"""GPU parity of the head-parallel attention block (tp_attn_* through the
+binding) against the fp64 oracle in ``oracle/attention.py``.
+
+Element-by-element comparisons on seeded inputs at sizes the oracle finishes
+in seconds (several 128-row blocks per sequence, two sequences, shards 1-4,
+head dims 64 and 128, causal and not, with and without LayerNorm, biases and
+the residual), plus bitwise repeatability and the empty call."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as A
+from tensor_transformer_mlp_tcgen05_gb300 import workloads as W
+
+from parity_helpers import assert_close, errors, f64
+
+pytestmark = pytest.mark.gpu
+
+LOG2E = 1.0 / math.log(2.0)
+
+# Tolerances.  Forward outputs (QKV, Ctx, the log-sum-exp, Z) keep the
+# block's bf16 bar: relative Frobenius error <= 5e-3, max |err| <= 3e-2
+# max |ref|.  The gradients pass through a longer chain of bf16 roundings
+# (the stored QKV and Ctx, dCtx, the staged P and dS operands, dQKV, dX),
+# each adding an independent relative error of about 2^-8 / sqrt(3) ~ 2.3e-3
+# rms at most; six in quadrature give ~5.5e-3, and dS = P (dP - delta)
+# subtracts nearly equal terms, so the gradient bar is 1e-2 (max |err| bar
+# unchanged).  Exact sums (db_o = sum_T dZ of bf16 inputs) land near 1e-8.
+FWD_KEYS = ("Z", "QKV", "Ctx", "lse")
+TOL_GRAD = (1e-2, 3e-2)
+
+
+def run_attn(w, inp, backward=True, residual=False, repeat=1):
+    from tensor_transformer_mlp_tcgen05_gb300.attention import \
+        TensorParallelAttention
+    m = TensorParallelAttention(w.hidden, w.heads, w.shards, w.tokens,
+                                w.seq, causal=w.causal,
+                                layernorm=w.layernorm, residual=residual)
+    d = {k: (None if v is None else v.cuda().contiguous())
+         for k, v in inp.items()}
+    outs = []
+    for _ in range(repeat):
+        Z = m.forward(d["X"], d["Wqkv"], d["Wo"], d["bqkv"], d["bo"],
+                      d["gamma"], d["beta"], training=True)
+        res = {"Z": Z,
+               "QKV": m.saved(w.tokens, "qkv").clone(),
+               "Ctx": m.saved(w.tokens, "ctx").clone(),
+               "lse2": m.saved(w.tokens, "lse2").clone()}
+        if backward:
+            res.update(m.backward(d["dZ"], d["X"], d["Wqkv"], d["Wo"],
+                                  d["gamma"]))
+            res["dQKV"] = m.saved(w.tokens, "dqkv").clone()
+        rc = m.check()
+        assert rc == 0, f"device status {rc}"
+        torch.cuda.synchronize()
+        outs.append({k: v.cpu() for k, v in res.items()})
+    m.close()
+    return outs if repeat > 1 else outs[0]
+
+
+def oracle(w, inp, backward=True, residual=False):
+    kw = dict(bqkv=f64(inp["bqkv"]), bo=f64(inp["bo"]), gamma=f64(inp["gamma"]),
+              beta=f64(inp["beta"]), causal=w.causal, residual=residual)
+    fwd = A.forward(f64(inp["X"]), f64(inp["Wqkv"]), f64(inp["Wo"]), w.heads,
+                    w.seq, w.shards, **kw)
+    out = {"Z": fwd["Z"], "QKV": fwd["QKV"], "Ctx": fwd["Ctx"],
+           "lse": fwd["lse"]}
+    if backward:
+        g = A.backward(f64(inp["dZ"]), f64(inp["X"]), f64(inp["Wqkv"]),
+                       f64(inp["Wo"]), fwd, w.heads, w.seq, w.shards,
+                       gamma=f64(inp["gamma"]), causal=w.causal,
+                       residual=residual)
+        out.update({k: g[k] for k in ("dX", "dWqkv", "dWo", "dbqkv", "dbo",
+                                      "dQKV")})
+        if inp["gamma"] is not None:
+            out.update(dgamma=g["dgamma"], dbeta=g["dbeta"])
+    return out
+
+
+def compare(got, ref):
+    report = {}
+    for k, v in ref.items():
+        if k == "lse":
+            # the kernel keeps log2-sum-exp of log2(e)-scaled scores
+            report[k] = assert_close(k, f64(got["lse2"]).T / LOG2E, v)
+        elif k in FWD_KEYS:
+            report[k] = assert_close(k, got[k], v)
+        else:
+            rel_fro, max_rel = errors(got[k], v)
+            assert np.all(np.isfinite(f64(got[k]))), k
+            assert rel_fro <= TOL_GRAD[0] and max_rel <= TOL_GRAD[1], (
+                f"{k}: rel_fro={rel_fro:.3e} (tol {TOL_GRAD[0]}), "
+                f"max_rel={max_rel:.3e} (tol {TOL_GRAD[1]})")
+            report[k] = (rel_fro, max_rel)
+    return report
+
+
+CASES = [
+    # name, overrides, bias, residual
+    ("d64_causal_t2", {}, True, False),
+    ("d64_causal_t1", dict(shards=1), False, False),
+    ("d64_full_t4", dict(causal=False, shards=4), True, False),
+    ("d128_causal_t2", {}, True, False),
+    ("d128_full_t1_ln_res", dict(causal=False, shards=1, layernorm=True), True,
+     True),
+    ("d128_causal_t4_ln", dict(shards=4, layernorm=True), False, False),
+]
+
+
+def _workload(name, over):
+    base = "attn_tiny_d64" if name.startswith("d64") else "attn_tiny_d128"
+    return W.ATTN_WORKLOADS[base].with_(**over)
+
+
+@pytest.mark.parametrize("name,over,bias,res", CASES, ids=[c[0] for c in CASES])
+def test_attention_forward_backward_parity(name, over, bias, res):
+    w = _workload(name, over)
+    inp = W.make_attn_inputs(w, seed=11, with_bias=bias)
+    if w.layernorm:   # exercise gamma and beta away from (1, 0)
+        g = torch.Generator().manual_seed(5)
+        inp["gamma"] = 1 + 0.2 * torch.randn(w.hidden, generator=g)
+        inp["beta"] = 0.2 * torch.randn(w.hidden, generator=g)
+    got = run_attn(w, inp, residual=res)
+    ref = oracle(w, inp, residual=res)
+    compare(got, ref)
+
+
+def test_attention_bitwise_repeatable():
+    w = W.ATTN_WORKLOADS["attn_tiny_d128"]
+    inp = W.make_attn_inputs(w, seed=3, with_bias=True)
+    a, b = run_attn(w, inp, repeat=2)
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
+
+
+def test_attention_zero_tokens():
+    from tensor_transformer_mlp_tcgen05_gb300.attention import \
+        TensorParallelAttention
+    w = W.ATTN_WORKLOADS["attn_tiny_d64"]
+    m = TensorParallelAttention(w.hidden, w.heads, w.shards, w.tokens, w.seq)
+    h = w.hidden
+    dev = "cuda"
+    X = torch.empty((0, h), dtype=torch.bfloat16, device=dev)
+    Wqkv = torch.zeros((h, 3 * h), dtype=torch.bfloat16, device=dev)
+    Wo = torch.zeros((h, h), dtype=torch.bfloat16, device=dev)
+    Z = m.forward(X, Wqkv, Wo)
+    assert Z.shape == (0, h)
+    g = {k: torch.full(s, 7.0, device=dev)
+         for k, s in (("dWqkv", (h, 3 * h)), ("dWo", (h, h)),
+                      ("dbqkv", (3 * h,)), ("dbo", (h,)))}
+    g = m.backward(torch.empty((0, h), dtype=torch.bfloat16, device=dev), X,
+                   Wqkv, Wo, out=g)
+    assert m.check() == 0
+    for k in ("dWqkv", "dWo", "dbqkv", "dbo"):
+        assert torch.count_nonzero(g[k]) == 0, k
+    m.close()
