@@ -12,6 +12,12 @@ workload has pre-LN).  Algorithmic work: 12 T h f flops per step (forward
 the workload's shapes, resident in device memory before timing starts; the
 weights alone exceed the 129 MB L2, so no flush is inserted between steps.
 
+``--workload attn_gpt3_13b`` (or another ``attn_*`` workload) times the
+head-parallel attention block instead: one step = tp_attn_forward (training)
++ tp_attn_backward (Q/K/V projection, attention core, output projection +
+shard sum, and their gradients); algorithmic work 24 T h^2 for the
+projections plus 12 d per unmasked (query, key) pair for the attention core.
+
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the fp64 CPU
 oracle on a bounded token slice of the same workload instead.  With
 WORLD_SIZE > 1 (torchrun) every rank runs an independent replica on its own
@@ -35,6 +41,8 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "TP-MLP fwd+bwd TFLOP/s and tokens/s on 1 GB300, % of dense bf16 peak"
+METRIC_ATTN = ("TP-attention fwd+bwd TFLOP/s and tokens/s on 1 GB300, "
+               "% of dense bf16 peak")
 DEFAULT_WORKLOAD = "gpt3_13b"
 
 # DRAM traffic per launch of the dominant kernel from an ncu capture
@@ -339,6 +347,221 @@ def run_ours(args, w, rank, world, local_rank):
     return line, inp
 
 
+def attn_kernel_flops(w):
+    """Algorithmic flops per launch of each attention-block kernel."""
+    T, h = w.tokens, w.hidden
+    core = 2.0 * w.head_dim * w.score_pairs()      # one pair-wise matmul
+    return {"gemm_qkv": 6.0 * T * h * h, "gemm_out_shardsum": 2.0 * T * h * h,
+            "gemm_wgrad_dWo": 2.0 * T * h * h, "gemm_dctx": 2.0 * T * h * h,
+            "gemm_wgrad_dWqkv": 6.0 * T * h * h,
+            "gemm_dx_shardsum": 6.0 * T * h * h,
+            "attn_fwd": 2 * core,          # Q K^T, P V
+            "attn_bwd_dkdv": 2 * core,     # dV = P^T dO, dK = dS^T Q
+            "attn_bwd_dq": 2 * core}       # dP = dO V^T, dQ = dS K
+
+
+def run_ours_attn(args, w, rank, world, local_rank):
+    import torch
+    from tensor_transformer_mlp_tcgen05_gb300 import binding as Bn
+    from tensor_transformer_mlp_tcgen05_gb300 import workloads as W
+    from tensor_transformer_mlp_tcgen05_gb300.attention import \
+        TensorParallelAttention
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    inp = W.make_attn_inputs(w, seed=0, with_bias=True)
+    d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
+    m = TensorParallelAttention(w.hidden, w.heads, w.shards, w.tokens, w.seq,
+                                causal=w.causal, layernorm=w.layernorm,
+                                residual=args.residual)
+    stream = torch.cuda.current_stream()
+    T, h = w.tokens, w.hidden
+    Z = torch.empty((T, h), dtype=torch.bfloat16, device=dev)
+    grads = {}
+
+    def step(Xd=None, dZd=None):
+        Xd = d["X"] if Xd is None else Xd
+        dZd = d["dZ"] if dZd is None else dZd
+        m.forward(Xd, d["Wqkv"], d["Wo"], d["bqkv"], d["bo"], d["gamma"],
+                  d["beta"], training=True, out=Z)
+        m.backward(dZd, Xd, d["Wqkv"], d["Wo"], d["gamma"], out=grads)
+
+    for _ in range(args.warmup):
+        step()
+    if m.check() != 0:
+        raise RuntimeError("device status after warm-up: "
+                           + Bn.tp_mlp_last_detail())
+    torch.cuda.synchronize()
+    snap = {"Z": Z.clone(), **{k: v.clone() for k, v in grads.items()}}
+    step()
+    torch.cuda.synchronize()
+    identical = all(torch.equal(snap[k], (Z if k == "Z" else grads[k]))
+                    for k in snap)
+
+    Bn.tp_attn_set_timing(m.handle, True)
+    Bn.tp_attn_timing_reset(m.handle)
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.25)
+    barrier(world)
+    torch.cuda.synchronize()
+    n0 = Bn.tp_attn_launch_count(m.handle)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    launches = Bn.tp_attn_launch_count(m.handle) - n0
+    ms = e0.elapsed_time(e1) / args.steps
+    if m.check() != 0:
+        raise RuntimeError("device status after timing: "
+                           + Bn.tp_mlp_last_detail())
+    kernels = Bn.tp_attn_timing_get(m.handle)
+    Bn.tp_attn_set_timing(m.handle, False)
+    ms_max = max_over_ranks(ms, world)
+
+    hX = inp["X"].pin_memory()
+    hdZ = inp["dZ"].pin_memory()
+    hZ = torch.empty_like(inp["X"]).pin_memory()
+    hdX = torch.empty_like(inp["X"]).pin_memory()
+    Xd = torch.empty_like(d["X"])
+    dZd = torch.empty_like(d["X"])
+    h2d = 2 * hX.numel() * hX.element_size()
+    d2h = 2 * hZ.numel() * hZ.element_size()
+
+    def e2e_step():
+        Xd.copy_(hX, non_blocking=True)
+        dZd.copy_(hdZ, non_blocking=True)
+        step(Xd, dZd)
+        hZ.copy_(Z, non_blocking=True)
+        hdX.copy_(grads["dX"], non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e2 = torch.cuda.Event(enable_timing=True)
+    e3 = torch.cuda.Event(enable_timing=True)
+    e2.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e3.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e2.elapsed_time(e3) / args.steps, world)
+
+    flops = w.flops_fwd_bwd()
+    peak_b, peak_s, hbm, peak_src = _peaks()
+    tflops = world * flops / (ms_max * 1e-3) / 1e12
+    total_ms = sum(k[2] for k in kernels) or 1.0
+    krep = [{"name": n, "launches": c, "avg_ms": round(t / max(c, 1), 4),
+             "share": round(t / total_ms, 4)} for n, c, t in kernels]
+    krep.sort(key=lambda r: -r["share"])
+    kf = attn_kernel_flops(w)
+    for r in krep:
+        if r["name"] in kf:
+            r["tflops"] = round(kf[r["name"]] / (r["avg_ms"] * 1e-3) / 1e12, 1)
+    top = krep[0]
+    roof = None
+    if top["name"] in kf:
+        ach = kf[top["name"]] / (top["avg_ms"] * 1e-3) / 1e12
+        tr = NCU_TRAFFIC.get(top["name"])
+        traffic = tr["bytes"] if tr and tr.get("src") == _src_sha() else None
+        roof = {"kernel": top["name"], "bound": "tensor",
+                "achieved": round(ach, 1), "peak": peak_s, "unit": "TFLOP/s",
+                "frac": round(ach / peak_s, 4),
+                "peak_kind": f"bf16 sustained ({peak_src})",
+                "traffic": traffic}
+    line = {
+        "metric": METRIC_ATTN, "value": round(tflops, 2), "unit": "TFLOP/s",
+        "tokens_per_s": round(world * T / (ms_max * 1e-3), 1),
+        "frac_of_peak": round(tflops / (world * peak_b), 4),
+        "peak_tflops": peak_b, "peak_kind": f"bf16 burst ({peak_src})",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_max, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: seeded N(0,1) activations and upstream gradient, "
+                f"N(0,{w.w_std}^2) weights, N(0,0.25) biases",
+        "config": {"workload": w.name, "tokens": T, "batch": w.batch,
+                   "seq": w.seq, "hidden": h, "heads": w.heads,
+                   "head_dim": w.head_dim, "shards": w.shards,
+                   "causal": w.causal, "layernorm": w.layernorm,
+                   "residual": bool(args.residual), "pass": "fwd+bwd",
+                   "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "l2": "inputs larger than L2 (no flush)"},
+        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2),
+                "unit": "TFLOP/s", "ms_per_step": round(e2e_ms, 4),
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "bitwise_identical_two_runs": identical,
+        "clocks": clocks,
+        "roofline": roof,
+        "kernels": krep,
+    }
+    m.close()
+    return line, inp
+
+
+def attn_oracle_sample(w, inp, seqs, seq_len=None):
+    """Time the fp64 attention oracle's forward + backward on the first
+    `seqs` sequences (optionally cut to their first `seq_len` tokens)."""
+    from oracle import attention as OA
+    S = seq_len or w.seq
+    rows = [r for b in range(seqs) for r in range(b * w.seq, b * w.seq + S)]
+    f = lambda t: None if t is None else t.double().numpy()
+    X, dZ = f(inp["X"][rows]), f(inp["dZ"][rows])
+    Wqkv, Wo = f(inp["Wqkv"]), f(inp["Wo"])
+    t0 = time.perf_counter()
+    fwd = OA.forward(X, Wqkv, Wo, w.heads, S, w.shards, bqkv=f(inp["bqkv"]),
+                     bo=f(inp["bo"]), gamma=f(inp["gamma"]),
+                     beta=f(inp["beta"]), causal=w.causal)
+    OA.backward(dZ, X, Wqkv, Wo, fwd, w.heads, S, w.shards,
+                gamma=f(inp["gamma"]), causal=w.causal)
+    return time.perf_counter() - t0
+
+
+def run_cpu_baseline_attn(w, inp):
+    secs = attn_oracle_sample(w, inp, 1)
+    flops = w.with_(batch=1).flops_fwd_bwd()
+    return {"value": round(flops / secs / 1e12, 5), "unit": "TFLOP/s",
+            "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"first sequence ({w.seq} of {w.tokens} tokens), fp64 "
+                      f"fwd+bwd ({secs:.1f} s)"}
+
+
+def run_reference_attn(args, w):
+    """The oracle as the reference arm for an attention workload: each step
+    is the first sequence cut to its first 256 tokens, fp64 on the host."""
+    from tensor_transformer_mlp_tcgen05_gb300 import workloads as W
+    S = min(256, w.seq)
+    ws = w.with_(batch=1, seq=S)
+    inp = W.make_attn_inputs(ws, seed=0, with_bias=True)
+    for _ in range(args.warmup):
+        attn_oracle_sample(ws, inp, 1)
+    t = sum(attn_oracle_sample(ws, inp, 1) for _ in range(args.steps))
+    sec = t / args.steps
+    val = ws.flops_fwd_bwd() / sec / 1e12
+    return {
+        "impl": "reference", "metric": METRIC_ATTN, "value": round(val, 5),
+        "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "tokens": w.tokens, "hidden": w.hidden,
+                   "heads": w.heads, "shards": w.shards, "seq": w.seq},
+        "cpu_baseline": {"value": round(val, 5), "unit": "TFLOP/s",
+                         "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": f"one sequence of {S} tokens per step, "
+                                   "fp64"},
+        "e2e": {"value": round(val, 5), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+
 def run_cpu_baseline(w, inp):
     import numpy as np  # noqa: F401  (BLAS threads are set at import)
     tokens = oracle_tokens(w)
@@ -448,17 +671,27 @@ def main(argv=None):
         ap.error("--warmup must be at least 3")
 
     from tensor_transformer_mlp_tcgen05_gb300 import workloads as W
-    w = W.WORKLOADS[args.workload]
+    attn = args.workload in W.ATTN_WORKLOADS
+    w = (W.ATTN_WORKLOADS if attn else W.WORKLOADS)[args.workload]
     if args.tokens:
-        w = w.with_(tokens=args.tokens)
+        if attn:
+            if args.tokens % w.seq:
+                ap.error("--tokens must be a multiple of the sequence length")
+            w = w.with_(batch=args.tokens // w.seq)
+        else:
+            w = w.with_(tokens=args.tokens)
     if args.shards:
         w = w.with_(shards=args.shards)
     rank, world, local_rank = dist_info()
 
     if args.impl == "reference":
         if rank == 0:
-            print(json.dumps(run_reference(args, w)), flush=True)
+            line = run_reference_attn(args, w) if attn else \
+                run_reference(args, w)
+            print(json.dumps(line), flush=True)
         return 0
+    if attn and args.sweep:
+        ap.error("--sweep is for the MLP workloads")
 
     if args.sweep:
         from tensor_transformer_mlp_tcgen05_gb300 import build as b
@@ -473,9 +706,13 @@ def main(argv=None):
     if rank == 0:
         b.build()
     barrier(world)
-    line, inp = run_ours(args, w, rank, world, local_rank)
+    if attn:
+        line, inp = run_ours_attn(args, w, rank, world, local_rank)
+    else:
+        line, inp = run_ours(args, w, rank, world, local_rank)
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = run_cpu_baseline(w, inp)
+        line["cpu_baseline"] = (run_cpu_baseline_attn(w, inp) if attn
+                                else run_cpu_baseline(w, inp))
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -97,6 +97,29 @@ def attention_core(q, k, v, seq_len, causal=True):
     return o, probs, lse
 
 
+def core_backward(q, k, v, do, probs, seq_len):
+    """Per sequence and head, given P from attention_core (same order):
+    dV = P^T dO, dP = dO V^T, dS = P * (dP - rowsum(dP * P)),
+    dQ = dS K / sqrt(d), dK = dS^T Q / sqrt(d).  All [T, heads, d]."""
+    T, heads, d = q.shape
+    scale = 1.0 / math.sqrt(d)
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    idx = 0
+    for b in range(T // seq_len):
+        rows = slice(b * seq_len, (b + 1) * seq_len)
+        for j in range(heads):
+            p = probs[idx]
+            idx += 1
+            dv[rows, j] = p.T @ do[rows, j]
+            dp = do[rows, j] @ v[rows, j].T
+            ds = p * (dp - (dp * p).sum(axis=1, keepdims=True))
+            dq[rows, j] = (ds @ k[rows, j]) * scale
+            dk[rows, j] = (ds.T @ q[rows, j]) * scale
+    return dq, dk, dv
+
+
 def forward(X, Wqkv, Wo, heads, seq_len, shards=1, bqkv=None, bo=None,
             gamma=None, beta=None, eps=1e-5, causal=True, residual=False):
     """Unsharded attention block.  Returns a dict with Xn, mean, rstd, QKV,
@@ -136,22 +159,8 @@ def backward(dZ, X, Wqkv, Wo, fwd, heads, seq_len, shards=1, gamma=None,
     dctx = dZ @ Wo.T
     q, k, v = _split(fwd["QKV"], heads, shards)
     d = q.shape[2]
-    scale = 1.0 / math.sqrt(d)
     do = dctx.reshape(T, heads, d)
-    dq = np.zeros_like(q)
-    dk = np.zeros_like(k)
-    dv = np.zeros_like(v)
-    idx = 0
-    for b in range(T // seq_len):
-        rows = slice(b * seq_len, (b + 1) * seq_len)
-        for j in range(heads):
-            p = fwd["P"][idx]
-            idx += 1
-            dv[rows, j] = p.T @ do[rows, j]
-            dp = do[rows, j] @ v[rows, j].T
-            ds = p * (dp - (dp * p).sum(axis=1, keepdims=True))
-            dq[rows, j] = (ds @ k[rows, j]) * scale
-            dk[rows, j] = (ds.T @ q[rows, j]) * scale
+    dq, dk, dv = core_backward(q, k, v, do, fwd["P"], seq_len)
     dqkv = _merge(dq, dk, dv, shards)
     dWqkv = fwd["Xn"].T @ dqkv
     dbqkv = dqkv.sum(axis=0)

@@ -156,3 +156,80 @@ def test_attention_zero_tokens():
     for k in ("dWqkv", "dWo", "dbqkv", "dbo"):
         assert torch.count_nonzero(g[k]) == 0, k
     m.close()
+
+
+def _head_cols(w, j):
+    """Columns of head j's q, k, v inside the shard-grouped projection."""
+    hs, hp, d = w.hidden // w.shards, w.heads // w.shards, w.head_dim
+    i, jj = divmod(j, hp)
+    base = 3 * hs * i + jj * d
+    return (slice(base, base + d), slice(base + hs, base + hs + d),
+            slice(base + 2 * hs, base + 2 * hs + d))
+
+
+def test_attention_gpt3_13b_sampled_invariants_and_bitwise():
+    """The GPT-3-13B-shaped layer (4 x 2048 tokens, h = 5120, 40 heads of
+    128, 8 shards, causal) at full size, in the launch configuration the
+    benchmark times.  Checked against the oracle from the original inputs:
+    Ctx, the log-sum-exp and dQKV of sampled (sequence, head) pairs; Z on
+    every sequence's first 128 rows (causal rows there see keys 0..127
+    only); and over every sequence and head the exact identities
+    sum_keys dK = 0 (each row of dS sums to zero) and sum_keys dV =
+    sum_queries dO.  Two runs are bit-identical."""
+    w = W.ATTN_WORKLOADS["attn_gpt3_13b"]
+    inp = W.make_attn_inputs(w, seed=0, with_bias=True)
+    a, b = run_attn(w, inp, repeat=2)
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
+    del b
+    S, h, d, H = w.seq, w.hidden, w.head_dim, w.heads
+    X, Wqkv, Wo = f64(inp["X"]), f64(inp["Wqkv"]), f64(inp["Wo"])
+    bqkv, bo, dZ = f64(inp["bqkv"]), f64(inp["bo"]), f64(inp["dZ"])
+    ctx, dqkv = f64(a["Ctx"]), f64(a["dQKV"])
+    lse2 = f64(a["lse2"])
+    # sampled heads: forward core and its backward, from the inputs
+    for seq, j in ((0, 0), (1, 17), (3, 39)):
+        rows = slice(seq * S, (seq + 1) * S)
+        cq, ck, cv = _head_cols(w, j)
+        x = X[rows]
+        q = x @ Wqkv[:, cq] + bqkv[cq]
+        k = x @ Wqkv[:, ck] + bqkv[ck]
+        v = x @ Wqkv[:, cv] + bqkv[cv]
+        o, probs, lse = A.attention_core(q[:, None], k[:, None], v[:, None], S,
+                                         causal=True)
+        assert_close(f"Ctx[{seq},{j}]", ctx[rows, j * d:(j + 1) * d], o[:, 0])
+        assert_close(f"lse[{seq},{j}]", lse2[j, rows] / LOG2E, lse[:, 0])
+        do = dZ[rows] @ Wo[j * d:(j + 1) * d, :].T
+        dq, dk, dv = A.core_backward(q[:, None], k[:, None], v[:, None],
+                                     do[:, None], probs, S)
+        for nm, cols, ref in (("dQ", cq, dq), ("dK", ck, dk), ("dV", cv, dv)):
+            rel_fro, max_rel = errors(dqkv[rows, cols], ref[:, 0])
+            assert rel_fro <= TOL_GRAD[0] and max_rel <= TOL_GRAD[1], (
+                nm, seq, j, rel_fro, max_rel)
+    # Z on the first 128 rows of every sequence
+    for seq in range(w.batch):
+        rows = slice(seq * S, seq * S + 128)
+        qkv = X[rows] @ Wqkv + bqkv
+        q, k, v = A._split(qkv, H, w.shards)
+        o, _, _ = A.attention_core(q, k, v, 128, causal=True)
+        Z = o.reshape(128, h) @ Wo + bo
+        assert_close(f"Z[{seq}][:128]", a["Z"][rows], Z)
+    # identities over every sequence and head
+    sum_dO = np.stack([dZ[s * S:(s + 1) * S].sum(axis=0) @ Wo.T
+                       for s in range(w.batch)])          # [batch, h]
+    dk_sum, dk_scale, dv_sum = [], [], []
+    for s in range(w.batch):
+        blk = dqkv[s * S:(s + 1) * S]
+        for j in range(H):
+            _, ck, cv = _head_cols(w, j)
+            dk_sum.append(blk[:, ck].sum(axis=0))
+            dk_scale.append(np.sqrt(S) * np.sqrt((blk[:, ck] ** 2).mean(axis=0)))
+            dv_sum.append(blk[:, cv].sum(axis=0))
+    dk_sum, dk_scale = np.array(dk_sum), np.array(dk_scale)
+    # with no cancellation the sum of S terms has the size sqrt(S) rms
+    assert np.linalg.norm(dk_sum) <= 0.05 * np.linalg.norm(dk_scale)
+    dv_sum = np.array(dv_sum).reshape(w.batch, H * d)
+    rel = np.linalg.norm(dv_sum - sum_dO) / np.linalg.norm(sum_dO)
+    assert rel <= TOL_GRAD[0], rel
+    # db_o is the column sum of dZ
+    assert_close("dbo", a["dbo"], dZ.sum(axis=0))
