@@ -22,7 +22,8 @@
 // operands are the streamed tiles read M/N-major (the same bytes).
 //
 // Warp roles as in the forward kernel: warp 0 TMA, warp 1 TMEM + MMA issue,
-// warps 4-7 elementwise (thread = row = TMEM lane).  All waits are bounded.
+// warps 4-11 elementwise (thread = row = TMEM lane, two warps per row
+// quarter, one per half of the columns).  All waits are bounded.
 #include "attn_common.cuh"
 
 namespace tpmlp {
@@ -92,8 +93,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       ptx::mbar_init(b_full + 8 * i, 1);
       ptx::mbar_init(b_empty + 8 * i, 1);
       ptx::mbar_init(s_full + 8 * i, 1);
-      ptx::mbar_init(s_empty + 8 * i, 4);
-      ptx::mbar_init(e_full + 8 * i, 4);
+      ptx::mbar_init(s_empty + 8 * i, SOFTMAX_WARPS);
+      ptx::mbar_init(e_full + 8 * i, SOFTMAX_WARPS);
       ptx::mbar_init(e_empty + 8 * i, 1);
     }
     ptx::mbar_init(o_full, 1);
@@ -209,7 +210,10 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     __syncwarp();
   } else if (warp >= SOFTMAX_WARP0) {
     // -------------------------------------------------- elementwise --
+    // Two warps per row quarter, each on 32 of the step's 64 columns (and
+    // on half of the output columns at the end).
     const int q = warp & 3;
+    const int hf = (warp - SOFTMAX_WARP0) >> 2;
     const int r = q * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     const float sl2 = a.scale_log2;
@@ -233,38 +237,35 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       const int cb = cb_begin + n;
       // Causal validity of column c: KV (row = key): c >= lo; Q (row =
       // query): c <= hi.  Without the mask every column is valid.
-      const int diff = rb * 128 + r - cb * 64;
+      const int diff = rb * 128 + r - cb * 64 - 32 * hf;
       const int lo = (KV && a.causal) ? diff : -1;
       const int hi = (!KV && a.causal) ? diff : 64;
-      const float* vl = vec + st * (VEC_BYTES / 4);
+      const float* vl = vec + st * (VEC_BYTES / 4) + 32 * hf;
       const float* vd = vl + 64;
       const uint32_t e2 = sE + st * NE * E_TILE, e1 = e2 + E_TILE;
+      uint32_t s1[32], s2[32];
+      ptx::tmem_ld_32x32b_x32(tmem + lane_base + 64 * st + 32 * hf, s1);
+      ptx::tmem_ld_32x32b_x32(tmem + lane_base + 128 + 64 * st + 32 * hf, s2);
+      ptx::tmem_ld_wait();
+      uint32_t pw[16], dw[16];
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t s1[32], s2[32];
-        ptx::tmem_ld_32x32b_x32(tmem + lane_base + 64 * st + 32 * half, s1);
-        ptx::tmem_ld_32x32b_x32(tmem + lane_base + 128 + 64 * st + 32 * half, s2);
-        ptx::tmem_ld_wait();
-        uint32_t pw[16], dw[16];
+      for (int i = 0; i < 32; i += 2) {
+        float ds[2], p[2];
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          float ds[2], p[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int c = 32 * half + i + u;
-            const float L = KV ? vl[c] : lse_r;
-            const float Dl = KV ? vd[c] : delta_r;
-            float pv = exp2f(fmaf(__uint_as_float(s1[i + u]), sl2, -L));
-            pv = (c >= lo && c <= hi) ? pv : 0.f;
-            p[u] = pv;
-            ds[u] = pv * (__uint_as_float(s2[i + u]) - Dl) * INV_SQRT_D;
-          }
-          pw[i / 2] = pack_bf16x2(p[0], p[1]);
-          dw[i / 2] = pack_bf16x2(ds[0], ds[1]);
+        for (int u = 0; u < 2; ++u) {
+          const int c = i + u;
+          const float L = KV ? vl[c] : lse_r;
+          const float Dl = KV ? vd[c] : delta_r;
+          float pv = exp2f(fmaf(__uint_as_float(s1[c]), sl2, -L));
+          pv = (c >= lo && c <= hi) ? pv : 0.f;
+          p[u] = pv;
+          ds[u] = pv * (__uint_as_float(s2[c]) - Dl) * INV_SQRT_D;
         }
-        stage_units<16>(e2, r, 4 * half, dw);
-        if constexpr (KV) stage_units<16>(e1, r, 4 * half, pw);
+        pw[i / 2] = pack_bf16x2(p[0], p[1]);
+        dw[i / 2] = pack_bf16x2(ds[0], ds[1]);
       }
+      stage_units<16>(e2, r, 4 * hf, dw);
+      if constexpr (KV) stage_units<16>(e1, r, 4 * hf, pw);
       ptx::tc_fence_before();
       ptx::fence_proxy_async_shared();
       __syncwarp();
@@ -275,12 +276,14 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     }
     if (alive && warp_wait(o_full, 0, ctl, ROLE_EPILOGUE)) {
       ptx::tc_fence_after();
+      constexpr int OCH = D / 64;          // 32-column chunks per half
       __nv_bfloat16* rowp = a.dqkv + static_cast<size_t>(row0 + r) * a.ld_qkv;
-      __nv_bfloat16* out2 = rowp + (KV ? hc.k : hc.q);
+      __nv_bfloat16* out2 = rowp + (KV ? hc.k : hc.q) + hf * (D / 2);
 #pragma unroll
-      for (int j = 0; j < D / 32; ++j) {
+      for (int j = 0; j < OCH; ++j) {
         uint32_t ov[32];
-        ptx::tmem_ld_32x32b_x32(tmem + lane_base + TMEM_OUT2 + 32 * j, ov);
+        ptx::tmem_ld_32x32b_x32(
+            tmem + lane_base + TMEM_OUT2 + hf * (D / 2) + 32 * j, ov);
         ptx::tmem_ld_wait();
         float v[32];
 #pragma unroll
@@ -288,11 +291,12 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         store_bf16x32(out2 + 32 * j, v);
       }
       if constexpr (KV) {
-        __nv_bfloat16* out1 = rowp + hc.v;
+        __nv_bfloat16* out1 = rowp + hc.v + hf * (D / 2);
 #pragma unroll
-        for (int j = 0; j < D / 32; ++j) {
+        for (int j = 0; j < OCH; ++j) {
           uint32_t ov[32];
-          ptx::tmem_ld_32x32b_x32(tmem + lane_base + TMEM_OUT1 + 32 * j, ov);
+          ptx::tmem_ld_32x32b_x32(
+              tmem + lane_base + TMEM_OUT1 + hf * (D / 2) + 32 * j, ov);
           ptx::tmem_ld_wait();
           float v[32];
 #pragma unroll

@@ -8,14 +8,24 @@ namespace attn {
 using gemm::Ctl;
 using gemm::wait_bounded;
 
-constexpr int ATT_THREADS = 256;
+// 12 warps: 0 TMA producer, 1 TMEM allocator + MMA issuer, 2-3 idle,
+// 4-11 softmax / elementwise.  Softmax warp w reads TMEM lane quarter
+// w mod 4 (its rows) and handles column half (w - 4) / 4 of each tile, so
+// every SM sub-partition runs two softmax warps.
+constexpr int ATT_THREADS = 384;
 constexpr int SOFTMAX_WARP0 = 4;
+constexpr int SOFTMAX_WARPS = 8;
 constexpr uint32_t KBLOCK_BYTES = 128 * 128;  // 128 rows x 64 bf16
 constexpr uint32_t ATOM_BYTES = 64 * 128;     // 64 K-rows x 64 bf16 (MN-major)
 constexpr unsigned long long ABORT_SETTLE_NS = 2000000ull;
 
 __device__ __forceinline__ void cta_barrier_att() {
   asm volatile("bar.sync 1, %0;" ::"n"(ATT_THREADS) : "memory");
+}
+
+// Named barrier among the softmax warps only.
+__device__ __forceinline__ void softmax_barrier() {
+  asm volatile("bar.sync 2, %0;" ::"n"(SOFTMAX_WARPS * 32) : "memory");
 }
 
 // Warp-uniform bounded wait (every lane polls; the result is agreed).

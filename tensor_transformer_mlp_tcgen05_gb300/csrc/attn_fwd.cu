@@ -20,8 +20,9 @@
 // token) row's log-sum-exp in base 2 of the scores scaled by log2(e)/sqrt(d),
 // lse2 = m + log2(l), so that P = exp2(S log2(e)/sqrt(d) - lse2).
 //
-// Warp roles (256 threads): warp 0 TMA producer, warp 1 TMEM allocator and
-// MMA issuer (one lane), warps 4-7 softmax (thread = query row = TMEM lane).
+// Warp roles (384 threads): warp 0 TMA producer, warp 1 TMEM allocator and
+// MMA issuer (one lane), warps 4-11 softmax (thread = query row = TMEM lane,
+// two warps per row quarter, one per half of the columns).
 // All waits are bounded as in the GEMM kernels.
 #include "attn_common.cuh"
 
@@ -59,6 +60,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                  o_full = b0 + 120, done_bar = b0 + 128;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 17);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  // Row max / row sum exchange between the two column halves: [2][2][128].
+  float* red = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + 256);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nq = a.nq;
@@ -77,9 +80,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       ptx::mbar_init(v_full + 8 * i, 1);
       ptx::mbar_init(v_empty + 8 * i, 1);
       ptx::mbar_init(s_full + 8 * i, 1);
-      ptx::mbar_init(s_empty + 8 * i, 4);
+      ptx::mbar_init(s_empty + 8 * i, SOFTMAX_WARPS);
     }
-    ptx::mbar_init(p_full, 4);
+    ptx::mbar_init(p_full, SOFTMAX_WARPS);
     ptx::mbar_init(p_empty, 1);
     ptx::mbar_init(o_full, 1);
     ptx::mbar_init(done_bar, 1);
@@ -198,10 +201,15 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     __syncwarp();
   } else if (warp >= SOFTMAX_WARP0) {
     // ------------------------------------------------------ softmax --
-    // Pass 1 finds the row max m of the scaled scores (log2 units); pass 2
-    // writes P = exp2(x - m) (final max, so nothing is ever rescaled),
-    // accumulates l = sum P in fp32, and the output is O / l.
+    // Two warps share each row quarter: column half `hf` (64 of the 128 key
+    // columns of a block; 64 / 32 of the D output columns).  Pass 1 finds
+    // the row max m of the scaled scores (log2 units), the halves meeting
+    // once through shared memory; pass 2 writes P = exp2(x - m) (final max,
+    // so nothing is ever rescaled) into the half's k-block of the P tile and
+    // accumulates the half's part of l = sum P; the output is O / (l0 + l1).
+    // Every softmax warp passes both named barriers on every path.
     const int q = warp & 3;
+    const int hf = (warp - SOFTMAX_WARP0) >> 2;
     const int r = q * 32 + lane;          // query row inside the block
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     const float sl2 = a.scale_log2;
@@ -215,19 +223,27 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         break;
       }
       ptx::tc_fence_after();
-      uint32_t sv[128];
-      tmem_ld_128(tmem + lane_base + sb * 128, sv);
+      uint32_t sv[64];
+      uint32_t (&s0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[0]);
+      uint32_t (&s1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[32]);
+      const uint32_t col = tmem + lane_base + sb * 128 + 64 * hf;
+      ptx::tmem_ld_32x32b_x32(col, s0);
+      ptx::tmem_ld_32x32b_x32(col + 32, s1);
+      ptx::tmem_ld_wait();
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(s_empty + 8 * sb);
       ++sc;
-      const int lim = (a.causal && kb == qb) ? r : 127;
+      const int lim = (a.causal && kb == qb) ? r - 64 * hf : 63;
       float mb = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 128; ++c)
+      for (int c = 0; c < 64; ++c)
         if (c <= lim) mb = fmaxf(mb, __uint_as_float(sv[c]));
       m = fmaxf(m, mb * sl2);
     }
+    red[hf * 128 + r] = m;
+    softmax_barrier();
+    m = fmaxf(red[r], red[128 + r]);
     for (int kb = 0; alive && kb < nk; ++kb) {
       const uint32_t sb = sc & 1, sph = (sc >> 1) & 1;
       if (!warp_wait(s_full + 8 * sb, sph, ctl, ROLE_EPILOGUE) ||
@@ -236,29 +252,25 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         break;
       }
       ptx::tc_fence_after();
-      const int lim = (a.causal && kb == qb) ? r : 127;
+      const int lim = (a.causal && kb == qb) ? r - 64 * hf : 63;
+      uint32_t sv[64];
+      uint32_t (&s0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[0]);
+      uint32_t (&s1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[32]);
+      const uint32_t col = tmem + lane_base + sb * 128 + 64 * hf;
+      ptx::tmem_ld_32x32b_x32(col, s0);
+      ptx::tmem_ld_32x32b_x32(col + 32, s1);
+      ptx::tmem_ld_wait();
+      uint32_t w[32];
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t sv[64];
-        uint32_t (&s0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[0]);
-        uint32_t (&s1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[32]);
-        const uint32_t col = tmem + lane_base + sb * 128 + 64 * half;
-        ptx::tmem_ld_32x32b_x32(col, s0);
-        ptx::tmem_ld_32x32b_x32(col + 32, s1);
-        ptx::tmem_ld_wait();
-        uint32_t w[32];
-#pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-          const int cc = 64 * half + c;
-          float p0 = exp2f(fmaf(__uint_as_float(sv[c]), sl2, -m));
-          float p1 = exp2f(fmaf(__uint_as_float(sv[c + 1]), sl2, -m));
-          p0 = cc <= lim ? p0 : 0.f;
-          p1 = cc + 1 <= lim ? p1 : 0.f;
-          l += p0 + p1;
-          w[c / 2] = pack_bf16x2(p0, p1);
-        }
-        stage_row64(sP + half * KBLOCK_BYTES, r, w);
+      for (int c = 0; c < 64; c += 2) {
+        float p0 = exp2f(fmaf(__uint_as_float(sv[c]), sl2, -m));
+        float p1 = exp2f(fmaf(__uint_as_float(sv[c + 1]), sl2, -m));
+        p0 = c <= lim ? p0 : 0.f;
+        p1 = c + 1 <= lim ? p1 : 0.f;
+        l += p0 + p1;
+        w[c / 2] = pack_bf16x2(p0, p1);
       }
+      stage_row64(sP + hf * KBLOCK_BYTES, r, w);
       ptx::tc_fence_before();
       ptx::fence_proxy_async_shared();
       __syncwarp();
@@ -268,22 +280,28 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       }
       ++sc;
     }
+    red[256 + hf * 128 + r] = l;
+    softmax_barrier();
+    l = red[256 + r] + red[256 + 128 + r];
     if (alive && warp_wait(o_full, 0, ctl, ROLE_EPILOGUE)) {
       ptx::tc_fence_after();
       const float inv_l = 1.0f / l;
+      constexpr int OCH = D / 64;         // 32-column chunks per half
       __nv_bfloat16* out = a.ctx + static_cast<size_t>(row0 + r) * a.ld_ctx +
-                           head * D;
+                           head * D + hf * (D / 2);
 #pragma unroll
-      for (int j = 0; j < D / 32; ++j) {
+      for (int j = 0; j < OCH; ++j) {
         uint32_t ov[32];
-        ptx::tmem_ld_32x32b_x32(tmem + lane_base + TMEM_O + 32 * j, ov);
+        ptx::tmem_ld_32x32b_x32(
+            tmem + lane_base + TMEM_O + hf * (D / 2) + 32 * j, ov);
         ptx::tmem_ld_wait();
         float v[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(ov[i]) * inv_l;
         store_bf16x32(out + 32 * j, v);
       }
-      a.lse[static_cast<size_t>(head) * a.ld_stat + row0 + r] = m + log2f(l);
+      if (hf == 0)
+        a.lse[static_cast<size_t>(head) * a.ld_stat + row0 + r] = m + log2f(l);
     }
     __syncwarp();
   }
@@ -310,7 +328,7 @@ template <int D>
 size_t attn_fwd_smem() {
   constexpr int KB = D / 64;
   const size_t need = 1024 + 3 * KB * KBLOCK_BYTES + 2 * (2 * KB * ATOM_BYTES) +
-                      2 * KBLOCK_BYTES + 17 * 8 + 16;
+                      2 * KBLOCK_BYTES + 256 + 4 * 128 * 4;
   return need > 116 * 1024 ? need : 116 * 1024;
 }
 
