@@ -1,0 +1,131 @@
+"""Pins for the FP8 (E4M3) oracle: the format's closed-form values, every
+bf16 bit pattern against PyTorch's float8_e4m3fn conversion, saturation,
+round trips, scale invariance, exactness on representable inputs and the
+plain block forward when quantization loses nothing.  No GPU."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import fp8 as F
+from oracle import mlp as O
+
+
+def test_closed_form_values():
+    """E4M3: bias 7, 3 mantissa bits, subnormals m 2^-9, S.1111.111 NaN."""
+    cases = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9,
+             0x08: 2.0 ** -6, 0x38: 1.0, 0x39: 1.125, 0x40: 2.0,
+             0x7E: 448.0, 0x7D: 416.0, 0x77: 240.0, 0xC0: -2.0,
+             0x80: -0.0, 0xFE: -448.0}
+    for code, val in cases.items():
+        assert F.e4m3_decode(np.array([code]))[0] == val, hex(code)
+    assert np.isnan(F.e4m3_decode(np.array([0x7F, 0xFF]))).all()
+
+
+def test_every_bf16_value_matches_torch_float8_e4m3fn():
+    """All 65536 bf16 bit patterns with |x| <= 448 (finite), converted by the
+    oracle and by torch's float8_e4m3fn cast (round to nearest even)."""
+    bits = torch.arange(0, 1 << 16, dtype=torch.int32).to(torch.int16)
+    x = bits.view(torch.bfloat16).to(torch.float32)
+    keep = torch.isfinite(x) & (x.abs() <= 448)
+    x = x[keep]
+    want = x.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = F.e4m3_encode(x.double().numpy())
+    # -0.0 and +0.0 codes: torch keeps the sign of zero, as the oracle does
+    np.testing.assert_array_equal(got, want)
+    assert len(x) > 30000
+
+
+def test_fp32_grid_near_ties_matches_torch():
+    """Random fp32 values and exact midpoints between neighbouring codes."""
+    rng = np.random.default_rng(0)
+    x = (rng.standard_normal(200000) * np.exp2(rng.integers(-12, 9, 200000))
+         ).astype(np.float32)
+    x = x[np.abs(x) <= 448]
+    codes = np.arange(0, 0x7E, dtype=np.uint8)
+    vals = F.e4m3_decode(codes)
+    mids = ((vals[:-1] + vals[1:]) / 2).astype(np.float32)   # exact in fp32
+    allx = np.concatenate([x, mids, -mids])
+    want = torch.from_numpy(allx).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(F.e4m3_encode(allx.astype(np.float64)), want)
+
+
+def test_saturation_and_round_trip():
+    np.testing.assert_array_equal(
+        F.e4m3_encode(np.array([448.0, 460.0, 464.0, 500.0, 1e30, -449.0, -1e9])),
+        [0x7E, 0x7E, 0x7E, 0x7E, 0x7E, 0xFE, 0xFE])
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+    np.testing.assert_array_equal(F.e4m3_encode(F.e4m3_decode(codes)), codes)
+
+
+def test_scale_and_quantize_properties():
+    rng = np.random.default_rng(1)
+    x = (rng.standard_normal((64, 96)) * 3).astype(np.float32)
+    q, s = F.quantize(x)
+    # the largest magnitude lands on +-448 exactly
+    assert np.max(np.abs(F.e4m3_decode(q))) == 448.0
+    assert s == np.float32(np.max(np.abs(x))) / np.float32(448)
+    # a power-of-two rescale changes only the scale
+    q2, s2 = F.quantize(x * np.float32(8))
+    np.testing.assert_array_equal(q2, q)
+    assert s2 == s * 8
+    # relative error of q s against x: at most half an E4M3 step for the
+    # normal range (2^-4), plus the subnormal quantum s 2^-10 absolute
+    err = np.abs(F.e4m3_decode(q) * s - x)
+    assert np.all(err <= np.abs(x) * 2.0 ** -4 + s * 2.0 ** -10 + 1e-30)
+    # all zeros: scale 1, codes 0
+    qz, sz = F.quantize(np.zeros((3, 4), np.float32))
+    assert sz == 1.0 and not qz.any()
+
+
+def test_quantized_matmul_is_exact_for_representable_operands():
+    """Operands that are E4M3 values with amax 448 quantize losslessly
+    (scale 1): the quantized product equals the plain product."""
+    rng = np.random.default_rng(2)
+    codes_a = rng.integers(0, 0x7E, (16, 48)).astype(np.uint8)
+    codes_b = rng.integers(0, 0x7E, (48, 24)).astype(np.uint8)
+    codes_a[0, 0] = 0x7E
+    codes_b[0, 0] = 0xFE
+    a, b = F.e4m3_decode(codes_a), F.e4m3_decode(codes_b)
+    qa, sa = F.quantize(a)
+    qb, sb = F.quantize(b)
+    assert sa == 1.0 and sb == 1.0
+    np.testing.assert_array_equal(F.e4m3_decode(qa), a)
+    np.testing.assert_array_equal(F.quantized_matmul(qa, sa, qb, sb), a @ b)
+
+
+def test_forward_reduces_to_the_block_when_quantization_is_lossless():
+    """X, A, B exactly representable with amax 448: H equals the plain
+    block's X A + b1, and Z equals the plain GEMM2 applied to the bf16 Y the
+    forward quantized (here Y's own quantization is the only loss)."""
+    rng = np.random.default_rng(3)
+    X = F.e4m3_decode(rng.integers(0, 0x7E, (8, 32)).astype(np.uint8)) / 64
+    A = F.e4m3_decode(rng.integers(0, 0x7E, (32, 64)).astype(np.uint8)) / 256
+    B = F.e4m3_decode(rng.integers(0, 0x7E, (64, 32)).astype(np.uint8)) / 256
+    X[0, 0], A[0, 0], B[0, 0] = 448 / 64, 448 / 256, 448 / 256
+    b1 = rng.standard_normal(64)
+    f = F.forward(X, A, B, b1=b1)
+    np.testing.assert_allclose(f["H"], X @ A + b1, rtol=1e-6, atol=1e-12)
+    plain = O.forward(X, A, B, b1=b1)
+    np.testing.assert_allclose(f["Y"], F.to_bf16(plain["Y"]), rtol=1e-2,
+                               atol=1e-3)
+    Yd = F.e4m3_decode(f["qy"]) * f["sy"]
+    np.testing.assert_allclose(f["Z"], Yd @ B, rtol=1e-12, atol=1e-12)
+    # Y's quantization error is within half an E4M3 step of Y
+    assert np.all(np.abs(Yd - f["Y"]) <= np.abs(f["Y"]) * 2.0 ** -4
+                  + f["sy"] * 2.0 ** -10)
+
+
+@pytest.mark.parametrize("ln,res", [(False, False), (True, True)])
+def test_forward_close_to_the_unquantized_block(ln, res):
+    """E4M3's 3 mantissa bits: the block output stays within ~10% of the
+    unquantized fp64 block on Gaussian data."""
+    rng = np.random.default_rng(4)
+    X = rng.standard_normal((64, 128))
+    A = rng.standard_normal((128, 512)) * 0.05
+    B = rng.standard_normal((512, 128)) * 0.05
+    g = (1 + 0.1 * rng.standard_normal(128)) if ln else None
+    bt = (0.1 * rng.standard_normal(128)) if ln else None
+    f = F.forward(X, A, B, gamma=g, beta=bt, residual=res)
+    ref = O.forward(X, A, B, gamma=g, beta=bt, residual=res)["Z"]
+    rel = np.linalg.norm(f["Z"] - ref) / np.linalg.norm(ref)
+    assert rel < 0.1, rel
