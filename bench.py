@@ -18,6 +18,10 @@ head-parallel attention block instead: one step = tp_attn_forward (training)
 shard sum, and their gradients); algorithmic work 24 T h^2 for the
 projections plus 12 d per unmasked (query, key) pair for the attention core.
 
+``--fp8`` times the FP8 (E4M3) forward of an MLP workload instead (weights
+quantized once before timing; per step: quantize Xn, GEMM1 + GeLU, quantize
+Y, GEMM2 + shard sum; 4 T h f flops), against twice the measured bf16 peak.
+
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the fp64 CPU
 oracle on a bounded token slice of the same workload instead.  With
 WORLD_SIZE > 1 (torchrun) every rank runs an independent replica on its own
@@ -41,6 +45,8 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "TP-MLP fwd+bwd TFLOP/s and tokens/s on 1 GB300, % of dense bf16 peak"
+METRIC_FP8 = ("TP-MLP FP8 (E4M3) forward TFLOP/s and tokens/s on 1 GB300, "
+              "% of dense fp8 peak")
 METRIC_ATTN = ("TP-attention fwd+bwd TFLOP/s and tokens/s on 1 GB300, "
                "% of dense bf16 peak")
 DEFAULT_WORKLOAD = "gpt3_13b"
@@ -562,6 +568,169 @@ def run_reference_attn(args, w):
 
 
 
+def run_ours_fp8(args, w, rank, world, local_rank):
+    """FP8 (E4M3) forward of an MLP workload: one step = quantize Xn, GEMM1
+    + GeLU (+ amax of Y), quantize Y, GEMM2 + shard sum; the weights are
+    packed once before timing.  The bf16 forward of the same workload is
+    timed alongside for context."""
+    import torch
+    from tensor_transformer_mlp_tcgen05_gb300 import binding as Bn
+    from tensor_transformer_mlp_tcgen05_gb300 import workloads as W
+    from tensor_transformer_mlp_tcgen05_gb300.mlp import TensorParallelMLP
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    inp = W.make_inputs(w, seed=0, need_grad_input=False)
+    d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
+    m = TensorParallelMLP(w.hidden, w.ffn, w.shards, w.tokens, dtype="bf16",
+                          layernorm=w.layernorm, residual=args.residual)
+    packed = m.pack_fp8_weights(d["A"], d["B"])
+    stream = torch.cuda.current_stream()
+    T = w.tokens
+    Z = torch.empty((T, w.hidden), dtype=torch.bfloat16, device=dev)
+
+    def step(Xd=None):
+        m.forward_fp8(d["X"] if Xd is None else Xd, packed, d["b1"], d["b2"],
+                      d["gamma"], d["beta"], out=Z)
+
+    for _ in range(args.warmup):
+        step()
+    if m.check() != 0:
+        raise RuntimeError("device status after warm-up: "
+                           + Bn.tp_mlp_last_detail())
+    torch.cuda.synchronize()
+    snap = Z.clone()
+    step()
+    torch.cuda.synchronize()
+    identical = torch.equal(snap, Z)
+
+    def timed(fn, n):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    Bn.tp_mlp_set_timing(m.handle, True)
+    Bn.tp_mlp_timing_reset(m.handle)
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.25)
+    barrier(world)
+    torch.cuda.synchronize()
+    n0 = Bn.tp_mlp_launch_count(m.handle)
+    ms = timed(step, args.steps)
+    barrier(world)
+    clocks = sampler.stop()
+    launches = Bn.tp_mlp_launch_count(m.handle) - n0
+    if m.check() != 0:
+        raise RuntimeError("device status after timing: " + Bn.tp_mlp_last_detail())
+    kernels = Bn.tp_mlp_timing_get(m.handle)
+    Bn.tp_mlp_set_timing(m.handle, False)
+    ms_max = max_over_ranks(ms, world)
+
+    # the bf16 forward of the same workload, for context
+    def step_bf16():
+        m.forward(d["X"], d["A"], d["B"], d["b1"], d["b2"], d["gamma"],
+                  d["beta"], training=False, out=Z)
+    for _ in range(3):
+        step_bf16()
+    bf16_ms = timed(step_bf16, args.steps)
+
+    hX = inp["X"].pin_memory()
+    hZ = torch.empty_like(inp["X"]).pin_memory()
+    Xd = torch.empty_like(d["X"])
+
+    def e2e_step():
+        Xd.copy_(hX, non_blocking=True)
+        step(Xd)
+        hZ.copy_(Z, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(timed(e2e_step, args.steps), world)
+
+    flops = w.flops_fwd()
+    peak_b, peak_s, hbm, peak_src = _peaks()
+    fp8_burst, fp8_sust = 2 * peak_b, 2 * peak_s
+    tflops = world * flops / (ms_max * 1e-3) / 1e12
+    total_ms = sum(k[2] for k in kernels) or 1.0
+    krep = [{"name": n, "launches": c, "avg_ms": round(t / max(c, 1), 4),
+             "share": round(t / total_ms, 4)} for n, c, t in kernels]
+    krep.sort(key=lambda r: -r["share"])
+    gemm = 2.0 * w.tokens * w.hidden * w.ffn
+    kf = {"gemm1_gelu_fp8": gemm, "gemm2_shardsum_fp8": gemm}
+    for r in krep:
+        if r["name"] in kf:
+            r["tflops"] = round(kf[r["name"]] / (r["avg_ms"] * 1e-3) / 1e12, 1)
+    top = krep[0]
+    roof = None
+    if top["name"] in kf:
+        ach = kf[top["name"]] / (top["avg_ms"] * 1e-3) / 1e12
+        roof = {"kernel": top["name"], "bound": "tensor",
+                "achieved": round(ach, 1), "peak": fp8_burst,
+                "unit": "TFLOP/s", "frac": round(ach / fp8_burst, 4),
+                "peak_kind": f"fp8 = 2 x measured bf16 burst ({peak_src}; "
+                             "nominal fp8:bf16 ratio 4.5:2.25)",
+                "traffic": None}
+    line = {
+        "metric": METRIC_FP8, "value": round(tflops, 2), "unit": "TFLOP/s",
+        "tokens_per_s": round(world * T / (ms_max * 1e-3), 1),
+        "frac_of_peak": round(tflops / (world * fp8_burst), 4),
+        "peak_tflops": fp8_burst, "peak_kind": "fp8 (2 x measured bf16 burst)",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_max, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+        "data": "synthetic: seeded N(0,1) activations, "
+                f"N(0,{w.w_std}^2) weights; weights quantized once before "
+                "timing, activations quantized every step",
+        "config": {"workload": w.name, "tokens": T, "batch": w.batch,
+                   "seq": w.seq, "hidden": w.hidden, "ffn": w.ffn,
+                   "shards": w.shards, "layernorm": w.layernorm,
+                   "residual": bool(args.residual), "pass": "fwd (fp8)",
+                   "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "l2": "inputs larger than L2 (no flush)"},
+        "bf16_forward": {"ms_per_step": round(bf16_ms, 4),
+                         "value": round(flops / (bf16_ms * 1e-3) / 1e12, 2),
+                         "unit": "TFLOP/s"},
+        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2),
+                "unit": "TFLOP/s", "ms_per_step": round(e2e_ms, 4),
+                "h2d_bytes_per_step": hX.numel() * hX.element_size(),
+                "d2h_bytes_per_step": hZ.numel() * hZ.element_size()},
+        "gpu_launches": launches,
+        "bitwise_identical_two_runs": identical,
+        "clocks": clocks,
+        "roofline": roof,
+        "kernels": krep,
+    }
+    m.close()
+    return line, inp
+
+
+def run_cpu_baseline_fp8(w, inp):
+    """The fp64 FP8 oracle's forward on a bounded token slice."""
+    from oracle import fp8 as OF
+    # the weights' quantization (2 h f elements) is a fixed cost of about
+    # 15 s per GPT-3-13B-sized matrix; the token slice adds little to it
+    tokens = int(max(16, min(w.tokens, 0.1e12 / (4.0 * w.hidden * w.ffn))))
+    f = lambda t: None if t is None else t.double().numpy()
+    t0 = time.perf_counter()
+    OF.forward(f(inp["X"][:tokens]), f(inp["A"]), f(inp["B"]), f(inp["b1"]),
+               f(inp["b2"]), f(inp["gamma"]), f(inp["beta"]))
+    secs = time.perf_counter() - t0
+    flops = w.flops_fwd(tokens)
+    return {"value": round(flops / secs / 1e12, 5), "unit": "TFLOP/s",
+            "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"first {tokens} of {w.tokens} tokens, fp64 FP8 "
+                      f"forward incl. weight quantization ({secs:.1f} s)"}
+
+
+
 def run_cpu_baseline(w, inp):
     import numpy as np  # noqa: F401  (BLAS threads are set at import)
     tokens = oracle_tokens(w)
@@ -663,6 +832,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--residual", action="store_true",
                     help="time the residual sub-block X + MLP(LN(X))")
+    ap.add_argument("--fp8", action="store_true",
+                    help="time the FP8 (E4M3) forward of an MLP workload")
     ap.add_argument("--sweep", action="store_true",
                     help="token x shard sweep of the workload (one line per "
                          "point) instead of the headline measurement")
@@ -690,8 +861,8 @@ def main(argv=None):
                 run_reference(args, w)
             print(json.dumps(line), flush=True)
         return 0
-    if attn and args.sweep:
-        ap.error("--sweep is for the MLP workloads")
+    if attn and (args.sweep or args.fp8):
+        ap.error("--sweep and --fp8 are for the MLP workloads")
 
     if args.sweep:
         from tensor_transformer_mlp_tcgen05_gb300 import build as b
@@ -708,11 +879,17 @@ def main(argv=None):
     barrier(world)
     if attn:
         line, inp = run_ours_attn(args, w, rank, world, local_rank)
+    elif args.fp8:
+        line, inp = run_ours_fp8(args, w, rank, world, local_rank)
     else:
         line, inp = run_ours(args, w, rank, world, local_rank)
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = (run_cpu_baseline_attn(w, inp) if attn
-                                else run_cpu_baseline(w, inp))
+        if attn:
+            line["cpu_baseline"] = run_cpu_baseline_attn(w, inp)
+        elif args.fp8:
+            line["cpu_baseline"] = run_cpu_baseline_fp8(w, inp)
+        else:
+            line["cpu_baseline"] = run_cpu_baseline(w, inp)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -149,6 +149,47 @@ int tp_mlp_backward(tp_mlp_handle* handle, int tokens, const void* dZ,
                     float* dbias1, float* dbias2, float* dgamma, float* dbeta,
                     void* stream);
 
+/* ---- FP8 (E4M3) forward variant ----------------------------------------
+ * The block's forward with both GEMMs on 8-bit E4M3 operands (the
+ * low-precision runs of the Megatron Core determinism article, read as
+ * plain per-tensor FP8): every operand tensor T (Xn, A, B and Y) is scaled
+ * by s_T = amax(T) / 448 (fp32; 1 for an all-zero tensor) and stored as
+ * codes q = e4m3(x / s_T) (x / s_T an fp32 division, nearest-even rounding,
+ * saturation to +-448).  H = (s_x s_a) (Xq Aq) + b1 with fp32 accumulation,
+ * Y = GeLU(H) stored bf16 and quantized with its own current amax, Z =
+ * sum_i (s_y s_b) (Yq_i Bq_i) + b2 [+ X] in fixed shard order, one bf16
+ * rounding.  The handle must be TPMLP_BF16 without dropout, and f / t must
+ * be a multiple of 128 (TPMLP_ERR_ARG / TPMLP_ERR_SHAPE otherwise); there
+ * is no FP8 backward.  The weights are quantized once by
+ * tp_mlp_fp8_pack_weights into a caller-owned buffer of
+ * tp_mlp_fp8_weights_bytes bytes (layout: amax_a, amax_b as fp32 bits and
+ * s_a, s_b as fp32, then A^T codes [f, h] and B^T codes [h, f], each
+ * section 256-byte aligned); the forward quantizes Xn and Y itself. */
+size_t tp_mlp_fp8_weights_bytes(const tp_mlp_handle* handle);
+int tp_mlp_fp8_pack_weights(tp_mlp_handle* handle, const void* A,
+                            const void* B, void* packed, size_t packed_bytes,
+                            void* stream);
+/* Workspace of tp_mlp_forward_fp8 for `tokens` tokens (0 on a bad handle). */
+size_t tp_mlp_fp8_workspace_bytes(const tp_mlp_handle* handle, int tokens);
+/* X [T,h] bf16, packed weights from tp_mlp_fp8_pack_weights, bias1 [f],
+ * bias2 [h], ln_gamma/ln_beta as tp_mlp_forward; Z [T,h] bf16. */
+int tp_mlp_forward_fp8(tp_mlp_handle* handle, int tokens, const void* X,
+                       const void* packed, const float* bias1,
+                       const float* bias2, const float* ln_gamma,
+                       const float* ln_beta, void* Z, void* workspace,
+                       size_t workspace_bytes, void* stream);
+/* Byte offsets of the packed-weight sections and of the forward's
+ * workspace sections (for inspection by tests); -1 if unknown. */
+long long tp_mlp_fp8_offset(const tp_mlp_handle* handle, int tokens,
+                            int which);
+#define TPMLP_FP8_PACK_SCALES 0   /* amax_a, amax_b (u32), s_a, s_b (f32) */
+#define TPMLP_FP8_PACK_AQT    1   /* A^T codes [f, h]                     */
+#define TPMLP_FP8_PACK_BQT    2   /* B^T codes [h, f]                     */
+#define TPMLP_FP8_WS_SCALES   3   /* amax_x, amax_y (u32), s_x, s_y (f32) */
+#define TPMLP_FP8_WS_XQ       4   /* Xn codes [T, h]                      */
+#define TPMLP_FP8_WS_Y        5   /* Y [T, f] bf16                        */
+#define TPMLP_FP8_WS_YQ       6   /* Y codes [T, f]                       */
+
 /* Bias gradient without any device allocation: dbias[c] = sum over the
  * `tokens` rows of grad[r][c], for a row-major [tokens, cols] gradient
  * (e.g. dZ, giving db2).  The pages have no counterpart for this entry

@@ -38,12 +38,22 @@ EXPORTED = (
     "tp_mlp_set_timing", "tp_mlp_timing_get", "tp_mlp_timing_reset",
     "tp_mlp_set_wait_budget", "tp_mlp_bias_grad_noalloc",
     "tp_mlp_set_dropout_seed",
+    "tp_mlp_fp8_weights_bytes", "tp_mlp_fp8_pack_weights",
+    "tp_mlp_fp8_workspace_bytes", "tp_mlp_forward_fp8", "tp_mlp_fp8_offset",
     "tp_attn_create", "tp_attn_destroy", "tp_attn_workspace_bytes",
     "tp_attn_forward", "tp_attn_backward", "tp_attn_check",
     "tp_attn_launch_count", "tp_attn_set_timing", "tp_attn_timing_get",
     "tp_attn_timing_reset", "tp_attn_set_wait_budget",
     "tp_attn_workspace_offset",
 )
+
+TPMLP_FP8_PACK_SCALES = 0
+TPMLP_FP8_PACK_AQT = 1
+TPMLP_FP8_PACK_BQT = 2
+TPMLP_FP8_WS_SCALES = 3
+TPMLP_FP8_WS_XQ = 4
+TPMLP_FP8_WS_Y = 5
+TPMLP_FP8_WS_YQ = 6
 
 TPATTN_WS_QKV = 0
 TPATTN_WS_CTX = 1
@@ -128,6 +138,17 @@ def lib(path: str | None = None) -> ctypes.CDLL:
     L.tp_mlp_set_dropout_seed.restype = _i
     L.tp_mlp_bias_grad_noalloc.argtypes = [_i, _i, _i, _vp, _vp, _vp]
     L.tp_mlp_bias_grad_noalloc.restype = _i
+    L.tp_mlp_fp8_weights_bytes.argtypes = [_vp]
+    L.tp_mlp_fp8_weights_bytes.restype = _sz
+    L.tp_mlp_fp8_pack_weights.argtypes = [_vp, _vp, _vp, _vp, _sz, _vp]
+    L.tp_mlp_fp8_pack_weights.restype = _i
+    L.tp_mlp_fp8_workspace_bytes.argtypes = [_vp, _i]
+    L.tp_mlp_fp8_workspace_bytes.restype = _sz
+    L.tp_mlp_forward_fp8.argtypes = [_vp, _i, _vp, _vp, _vp, _vp, _vp, _vp,
+                                     _vp, _vp, _sz, _vp]
+    L.tp_mlp_forward_fp8.restype = _i
+    L.tp_mlp_fp8_offset.argtypes = [_vp, _i, _i]
+    L.tp_mlp_fp8_offset.restype = ctypes.c_longlong
     L.tp_attn_create.argtypes = [ctypes.POINTER(tp_attn_config),
                                  ctypes.POINTER(_vp)]
     L.tp_attn_create.restype = _i
@@ -277,6 +298,35 @@ def tp_mlp_bias_grad_noalloc(tokens, cols, dtype, grad, dbias, stream=None):
     _check(lib().tp_mlp_bias_grad_noalloc(tokens, cols, dtype, _ptr(grad),
                                           _ptr(dbias), _stream(stream)),
            "tp_mlp_bias_grad_noalloc")
+
+
+# ------------------------------------------------------------------ fp8 --
+
+def tp_mlp_fp8_weights_bytes(handle) -> int:
+    return int(lib().tp_mlp_fp8_weights_bytes(handle))
+
+
+def tp_mlp_fp8_pack_weights(handle, A, B, packed, packed_bytes, stream=None):
+    _check(lib().tp_mlp_fp8_pack_weights(handle, _ptr(A), _ptr(B),
+                                         _ptr(packed), packed_bytes,
+                                         _stream(stream)),
+           "tp_mlp_fp8_pack_weights")
+
+
+def tp_mlp_fp8_workspace_bytes(handle, tokens: int) -> int:
+    return int(lib().tp_mlp_fp8_workspace_bytes(handle, tokens))
+
+
+def tp_mlp_forward_fp8(handle, tokens, X, packed, bias1, bias2, ln_gamma,
+                       ln_beta, Z, workspace, workspace_bytes, stream=None):
+    _check(lib().tp_mlp_forward_fp8(
+        handle, tokens, _ptr(X), _ptr(packed), _ptr(bias1), _ptr(bias2),
+        _ptr(ln_gamma), _ptr(ln_beta), _ptr(Z), _ptr(workspace),
+        workspace_bytes, _stream(stream)), "tp_mlp_forward_fp8")
+
+
+def tp_mlp_fp8_offset(handle, tokens: int, which: int) -> int:
+    return int(lib().tp_mlp_fp8_offset(handle, tokens, which))
 
 
 # ------------------------------------------------------------- attention --

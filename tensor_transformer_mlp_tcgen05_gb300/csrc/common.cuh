@@ -48,6 +48,13 @@ struct GemmArgs {
   uint32_t drop_threshold;  // keep when the 32-bit draw >= threshold
   float drop_scale;       // 1 / (1 - p)
   unsigned long long drop_seed, drop_offset;
+  // E4M3 operand GEMMs: the accumulator is multiplied by *scale_a *
+  // *scale_b (the two operands' per-tensor scales, device memory, product
+  // rounded to fp32) before the bias.  amax_out (nullable): EPI_GELU_FWD
+  // raises it to the largest |Y| written (fp32 bits of a bf16 value).
+  const float* scale_a;
+  const float* scale_b;
+  unsigned int* amax_out;
 };
 
 // Roles recorded in status[1] when a bounded wait gives up.

@@ -29,6 +29,12 @@
 // the one-CTA kernel; in addition both CTAs meet at cluster barriers before
 // the first copy and before TMEM is freed, so no CTA leaves while its peer may
 // still touch its shared memory or barriers.
+//
+// With F8 the operands are E4M3 bytes (both K-major): a k-block is 128
+// elements, still one 128-byte swizzle row, each MMA (kind::f8f6f4, K = 32)
+// consumes the same 32 bytes as a bf16 K = 16 step, so the ring, the
+// descriptors and the tile shapes are unchanged; the epilogue multiplies the
+// fp32 accumulator by the product of the operands' per-tensor scales.
 #include "gemm_common.cuh"
 
 namespace tpmlp {
@@ -92,7 +98,7 @@ __device__ __forceinline__ bool wait_bounded_cluster(uint32_t bar,
   }
 }
 
-template <bool A_MN, bool B_MN, int EPI>
+template <bool A_MN, bool B_MN, int EPI, bool F8>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
@@ -179,7 +185,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (leader) ptx::mbar_arrive_expect_tx(full0 + 8u * stage,
                                                  PAIR_STAGE_BYTES);
           const uint32_t fb = lead_full0 + 8u * stage;
-          const int k0 = kb * BK;
+          const int k0 = kb * (F8 ? 2 * BK : BK);  // 128 bytes of K either way
           const uint32_t da = s_a + stage * A_STAGE_BYTES;
           const uint32_t db = s_b + stage * B_STAGE_BYTES;
           if constexpr (!A_MN) {
@@ -206,7 +212,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     } else if (warp == 1 && lane == 0 && leader) {
       // -------------------------------------------------- MMA issuer --
-      constexpr uint32_t IDESC = idesc_bf16_f32(PM, PN, A_MN, B_MN);
+      constexpr uint32_t IDESC =
+          F8 ? idesc_e4m3_f32(PM, PN) : idesc_bf16_f32(PM, PN, A_MN, B_MN);
       constexpr uint32_t A_KSTEP = A_MN ? 16 * 128 : 32;
       constexpr uint32_t B_KSTEP = B_MN ? 16 * 128 : 32;
       constexpr uint32_t A_LBO = A_MN ? BK * 128 : 16;
@@ -239,8 +246,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                   ptx::sdesc_sw128(a_addr + k * A_KSTEP, A_LBO, 1024);
               const uint64_t bdesc =
                   ptx::sdesc_sw128(b_addr + k * B_KSTEP, B_LBO, 1024);
-              ptx::mma_bf16_pair(d_tmem, adesc, bdesc, IDESC,
+              if constexpr (F8) {
+                ptx::mma_f8_pair(d_tmem, adesc, bdesc, IDESC,
                                  (kb > 0 || k > 0) ? 1u : 0u);
+              } else {
+                ptx::mma_bf16_pair(d_tmem, adesc, bdesc, IDESC,
+                                   (kb > 0 || k > 0) ? 1u : 0u);
+              }
             }
             ptx::mma_commit_pair(empty0 + 8u * stage, BOTH);
             if (++stage == STAGES) {
@@ -280,6 +292,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int half = ew >> 2;    // which 128-column half of the tile
     ChunkStager st{s_epi + static_cast<uint32_t>(ew) * 2u * STAGE_CHUNK_BYTES,
                    0u};
+    // E4M3 operands: the product of the two per-tensor scales.
+    const float acc_scale = F8 ? *args.scale_a * *args.scale_b : 1.f;
     uint32_t acc = 0;
     bool alive = true;
     for (int tile = pair; alive && tile < num_tiles; tile += num_pairs) {
@@ -343,6 +357,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 v[32 + i] = __uint_as_float(r1[i]);
               }
               uint32_t w[32];
+              if constexpr (F8) {
+#pragma unroll
+                for (int i = 0; i < 64; ++i) v[i] *= acc_scale;
+              }
               if constexpr (EPI == EPI_BIAS_BF16) {
                 add_bias_n(args.bias, c0, v, 64);
               } else if constexpr (EPI == EPI_GELU_FWD) {
@@ -353,6 +371,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
 #pragma unroll
                 for (int i = 0; i < 64; ++i) v[i] = gelu_f32(v[i], args.gelu_mode);
+                if (args.amax_out != nullptr) {
+                  // largest |Y| of this warp's rows in range, as stored (bf16)
+                  float mx = 0.f;
+#pragma unroll
+                  for (int i = 0; i < 64; ++i) mx = fmaxf(mx, fabsf(v[i]));
+                  mx = row < args.M ? __bfloat162float(__float2bfloat16_rn(mx))
+                                    : 0.f;
+                  const unsigned int wm =
+                      __reduce_max_sync(0xffffffffu, __float_as_uint(mx));
+                  if (lane == 0) atomicMax(args.amax_out, wm);
+                }
               } else {
                 if (row < args.M) {
                   const uint4* hp = reinterpret_cast<const uint4*>(
@@ -388,6 +417,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
       if constexpr (EPI == EPI_SHARDSUM) {
+        if constexpr (F8) {
+#pragma unroll
+          for (int i = 0; i < 128; ++i) S[i] *= acc_scale;
+        }
         if (alive && live) {
           if (args.out_f32) {
 #pragma unroll
@@ -433,12 +466,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
-template <bool A_MN, bool B_MN, int EPI>
+template <bool A_MN, bool B_MN, int EPI, bool F8 = false>
 cudaError_t launch_impl(const CUtensorMap& ta, const CUtensorMap& tb,
                         const CUtensorMap& to, const CUtensorMap& to2,
                         const GemmArgs& args, int max_pairs,
                         cudaStream_t stream) {
-  auto kern = gemm_tc2_kernel<A_MN, B_MN, EPI>;
+  auto kern = gemm_tc2_kernel<A_MN, B_MN, EPI, F8>;
   cudaFuncAttributes fa;
   cudaError_t e = cudaFuncGetAttributes(&fa, kern);
   if (e != cudaSuccess) return e;
@@ -503,6 +536,21 @@ cudaError_t launch_gemm_tc2(int epi, bool a_mn, bool b_mn,
   if (!a_mn && !b_mn && epi == EPI_BIAS_BF16)
     return launch_impl<false, false, EPI_BIAS_BF16>(ta, tb, to, to2, args,
                                                     max_pairs, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_gemm_tc2_e4m3(int epi, const CUtensorMap& ta,
+                                 const CUtensorMap& tb, const CUtensorMap& to,
+                                 const CUtensorMap& to2, const GemmArgs& args,
+                                 int max_pairs, cudaStream_t stream) {
+  if (args.scale_a == nullptr || args.scale_b == nullptr)
+    return cudaErrorInvalidValue;
+  if (epi == EPI_GELU_FWD)
+    return launch_impl<false, false, EPI_GELU_FWD, true>(ta, tb, to, to2, args,
+                                                         max_pairs, stream);
+  if (epi == EPI_SHARDSUM)
+    return launch_impl<false, false, EPI_SHARDSUM, true>(ta, tb, to, to2, args,
+                                                         max_pairs, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -154,6 +154,36 @@ inline int encode_map_t(CUtensorMap* m, const void* base, bool f32, uint64_t inn
   return TPMLP_OK;
 }
 
+// 8-bit operand [outer, inner] (pitch in bytes), 128-byte swizzle, box =
+// {128 inner bytes (one swizzle row), box_outer}.
+inline int encode_map_u8(CUtensorMap* m, const void* base, uint64_t inner,
+                         uint64_t outer, uint64_t pitch, uint32_t box_outer) {
+  EncodeTiledFn enc = get_encoder();
+  if (enc == nullptr) {
+    set_detail_msg("cuTensorMapEncodeTiled entry point not available");
+    return TPMLP_ERR_CUDA;
+  }
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {pitch};
+  const cuuint32_t box[2] = {128, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                         const_cast<void*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    std::snprintf(g_detail, sizeof(g_detail),
+                  "cuTensorMapEncodeTiled (u8) failed (%d): inner=%llu "
+                  "outer=%llu pitch=%llu",
+                  static_cast<int>(r), (unsigned long long)inner,
+                  (unsigned long long)outer, (unsigned long long)pitch);
+    return TPMLP_ERR_CUDA;
+  }
+  return TPMLP_OK;
+}
+
 // bf16 operand: box = {64 inner elements (one 128-byte swizzle row), box_outer}.
 inline int encode_map(CUtensorMap* m, const void* base, uint64_t inner,
                uint64_t outer, uint64_t pitch, uint32_t box_outer) {

@@ -34,6 +34,29 @@ cudaError_t launch_gemm_tc2(int epi, bool a_mn, bool b_mn,
                             const GemmArgs& args, int max_pairs,
                             cudaStream_t stream);
 
+// The pair GEMM on E4M3 operands (both K-major, 8-bit tensor maps with
+// 128 x 128-byte boxes; args.kb_per_seg counts 128-element k-blocks;
+// args.scale_a and args.scale_b required).  Epilogues EPI_GELU_FWD (optionally raising
+// args.amax_out) and EPI_SHARDSUM.
+cudaError_t launch_gemm_tc2_e4m3(int epi, const CUtensorMap& ta,
+                                 const CUtensorMap& tb, const CUtensorMap& to,
+                                 const CUtensorMap& to2, const GemmArgs& args,
+                                 int max_pairs, cudaStream_t stream);
+
+// FP8 helpers (csrc/fp8.cu).  amax: *amax = max(*amax, max |x|) as fp32
+// bits (the caller zeroes it first).  Quantization: s = amax / 448 in fp32
+// (1 when amax = 0), q = e4m3(x / s) rounded to nearest even with
+// saturation; scale_out (nullable) receives s.
+cudaError_t launch_amax_bf16(const void* x, size_t n, unsigned int* amax,
+                             cudaStream_t stream);
+cudaError_t launch_quantize_e4m3(const void* x, size_t n,
+                                 const unsigned int* amax, uint8_t* q,
+                                 float* scale_out, cudaStream_t stream);
+// Transposing quantization of a bf16 [rows, cols] matrix into q [cols, rows].
+cudaError_t launch_quantize_e4m3_t(const void* x, int rows, int cols,
+                                   const unsigned int* amax, uint8_t* q,
+                                   float* scale_out, cudaStream_t stream);
+
 // fp32 CUDA-core GEMM with the same epilogues.  Element (m, k) of the first
 // operand is a[m * a_sm + k * a_sk]; element (k, n) of the second is
 // b[k * b_sk + n * b_sn].  args.kb_per_seg is the shard segment length in K.

@@ -306,6 +306,20 @@ __device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t adesc,
       : "memory");
 }
 
+// The same with 8-bit E4M3 operands (kind::f8f6f4; K = 32 per instruction,
+// i.e. the same 32 bytes of a 128-byte swizzle row as a bf16 K = 16 step).
+__device__ __forceinline__ void mma_f8_pair(uint32_t d_tmem, uint64_t adesc,
+                                            uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive once on the mbarrier at `bar` (same offset) in every CTA of
 // `cta_mask` when all tcgen05 ops issued so far by this thread are done.
 __device__ __forceinline__ void mma_commit_pair(uint32_t bar,
@@ -345,6 +359,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn,
                                                       bool b_mn) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
          ((b_mn ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Instruction descriptor of tcgen05.mma kind::f8f6f4 with E4M3 A and B
+// (format code 0 in bits 7-9 and 10-12), K-major operands, fp32 accumulator.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 

@@ -72,6 +72,51 @@ Layout make_layout(const tp_mlp_config& c, int tokens, int training) {
   return L;
 }
 
+// FP8 forward: packed weights and workspace.
+struct Fp8Pack {
+  size_t scales = 0, aqt = 0, bqt = 0, total = 0;
+};
+// [amax_a, amax_b (u32), s_a, s_b (f32)] | A^T codes [f, h] | B^T codes [h, f]
+Fp8Pack fp8_pack_layout(const tp_mlp_config& c) {
+  Fp8Pack P;
+  const size_t h = static_cast<size_t>(c.hidden), f = static_cast<size_t>(c.ffn);
+  P.scales = 0;
+  P.aqt = 256;
+  P.bqt = align_up(P.aqt + f * h, 256);
+  P.total = align_up(P.bqt + h * f, 256);
+  return P;
+}
+
+struct Fp8Layout {
+  size_t status = 0, xn = 0, mean = 0, rstd = 0, scales = 0, xq = 0, y = 0,
+         yq = 0, total = 0;
+};
+// status | [Xn, mean, rstd] | [amax_x, amax_y (u32), s_x, s_y (f32)] |
+// Xq [T, h] | Y [T, f] bf16 | Yq [T, f]
+Fp8Layout fp8_layout(const tp_mlp_config& c, int tokens) {
+  Fp8Layout L;
+  const size_t T = static_cast<size_t>(tokens);
+  const size_t h = static_cast<size_t>(c.hidden), f = static_cast<size_t>(c.ffn);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  L.status = take(256);
+  if (c.use_layernorm) {
+    L.xn = take(T * h * 2);
+    L.mean = take(T * 4);
+    L.rstd = take(T * 4);
+  }
+  L.scales = take(16);
+  L.xq = take(T * h);
+  L.y = take(T * f * 2);
+  L.yq = take(T * f);
+  L.total = off;
+  return L;
+}
+
 // ------------------------------------------------------ device checks --
 
 }  // namespace
@@ -88,15 +133,19 @@ struct tp_mlp_handle {
 
 namespace {
 
-GemmArgs base_args(const tp_mlp_handle* H, void* ws, const Layout& L) {
+GemmArgs base_args(const tp_mlp_handle* H, void* ws, size_t status_off) {
   GemmArgs a;
   std::memset(&a, 0, sizeof(a));
   a.group_m = 16;
   a.gelu_mode = H->cfg.gelu_mode;
-  a.status = reinterpret_cast<int*>(static_cast<char*>(ws) + L.status);
+  a.status = reinterpret_cast<int*>(static_cast<char*>(ws) + status_off);
   a.budget_ns = H->core.budget_ns;
   a.num_seg = 1;
   return a;
+}
+
+GemmArgs base_args(const tp_mlp_handle* H, void* ws, const Layout& L) {
+  return base_args(H, ws, L.status);
 }
 
 // Dropout parameters of the output dropout (keep when the 32-bit Philox
@@ -410,6 +459,163 @@ int tp_mlp_backward(tp_mlp_handle* H, int tokens, const void* dZ,
     }
   }
   return TPMLP_OK;
+}
+
+// ============================================================ FP8 ====
+
+static int fp8_config_ok(const tp_mlp_config& c) {
+  if (c.dtype != TPMLP_BF16) return TPMLP_ERR_ARG;
+  if (c.dropout_p > 0.f) return TPMLP_ERR_ARG;
+  // A k-block of 128 E4M3 elements must not straddle two shards.
+  if ((c.ffn / c.shards) % 128 != 0) return TPMLP_ERR_SHAPE;
+  return TPMLP_OK;
+}
+
+size_t tp_mlp_fp8_weights_bytes(const tp_mlp_handle* H) {
+  if (H == nullptr || fp8_config_ok(H->cfg) != TPMLP_OK) return 0;
+  return fp8_pack_layout(H->cfg).total;
+}
+
+size_t tp_mlp_fp8_workspace_bytes(const tp_mlp_handle* H, int tokens) {
+  if (H == nullptr || tokens < 0 || fp8_config_ok(H->cfg) != TPMLP_OK)
+    return 0;
+  return fp8_layout(H->cfg, tokens).total;
+}
+
+long long tp_mlp_fp8_offset(const tp_mlp_handle* H, int tokens, int which) {
+  if (H == nullptr || tokens < 0) return -1;
+  const Fp8Pack P = fp8_pack_layout(H->cfg);
+  const Fp8Layout L = fp8_layout(H->cfg, tokens);
+  switch (which) {
+    case TPMLP_FP8_PACK_SCALES: return static_cast<long long>(P.scales);
+    case TPMLP_FP8_PACK_AQT: return static_cast<long long>(P.aqt);
+    case TPMLP_FP8_PACK_BQT: return static_cast<long long>(P.bqt);
+    case TPMLP_FP8_WS_SCALES: return static_cast<long long>(L.scales);
+    case TPMLP_FP8_WS_XQ: return static_cast<long long>(L.xq);
+    case TPMLP_FP8_WS_Y: return static_cast<long long>(L.y);
+    case TPMLP_FP8_WS_YQ: return static_cast<long long>(L.yq);
+    default: return -1;
+  }
+}
+
+int tp_mlp_fp8_pack_weights(tp_mlp_handle* H, const void* A, const void* B,
+                            void* packed, size_t packed_bytes, void* stream) {
+  if (H == nullptr || !A || !B || !packed) return TPMLP_ERR_ARG;
+  TRY(fp8_config_ok(H->cfg));
+  const void* ptrs[] = {A, B, packed};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return TPMLP_ERR_ALIGN;
+  const Fp8Pack P = fp8_pack_layout(H->cfg);
+  if (packed_bytes < P.total) return TPMLP_ERR_WORKSPACE;
+  int sms = 0;
+  TRY(check_device(&sms));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* pk = static_cast<char*>(packed);
+  const int h = H->cfg.hidden, f = H->cfg.ffn;
+  unsigned int* amax = reinterpret_cast<unsigned int*>(pk + P.scales);
+  float* scl = reinterpret_cast<float*>(pk + P.scales) + 2;
+  cudaError_t e = cudaMemsetAsync(amax, 0, 8, s);
+  if (e != cudaSuccess) {
+    set_detail("cudaMemsetAsync(amax)", e);
+    return TPMLP_ERR_CUDA;
+  }
+  TRY(run(&H->core, "fp8_amax_weights", s, [&] {
+    return launch_amax_bf16(A, size_t(h) * f, amax, s);
+  }));
+  TRY(run(&H->core, "fp8_amax_weights", s, [&] {
+    return launch_amax_bf16(B, size_t(f) * h, amax + 1, s);
+  }));
+  TRY(run(&H->core, "fp8_quantize_weights_t", s, [&] {
+    return launch_quantize_e4m3_t(A, h, f, amax,
+                                  reinterpret_cast<uint8_t*>(pk + P.aqt), scl, s);
+  }));
+  return run(&H->core, "fp8_quantize_weights_t", s, [&] {
+    return launch_quantize_e4m3_t(B, f, h, amax + 1,
+                                  reinterpret_cast<uint8_t*>(pk + P.bqt),
+                                  scl + 1, s);
+  });
+}
+
+int tp_mlp_forward_fp8(tp_mlp_handle* H, int tokens, const void* X,
+                       const void* packed, const float* bias1,
+                       const float* bias2, const float* ln_gamma,
+                       const float* ln_beta, void* Z, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  if (H == nullptr) return TPMLP_ERR_ARG;
+  const tp_mlp_config& c = H->cfg;
+  TRY(fp8_config_ok(c));
+  if (tokens < 0 || tokens > c.max_tokens) return TPMLP_ERR_SHAPE;
+  if (!packed || !workspace || (tokens > 0 && (!X || !Z))) return TPMLP_ERR_ARG;
+  if (c.use_layernorm && (!ln_gamma || !ln_beta)) return TPMLP_ERR_ARG;
+  const void* ptrs[] = {X, packed, Z, workspace, bias1, bias2, ln_gamma, ln_beta};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return TPMLP_ERR_ALIGN;
+  const Fp8Layout L = fp8_layout(c, tokens);
+  if (workspace_bytes < L.total) return TPMLP_ERR_WORKSPACE;
+  int sms = 0;
+  TRY(check_device(&sms));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  const char* pk = static_cast<const char*>(packed);
+  const Fp8Pack P = fp8_pack_layout(c);
+  cudaError_t e = cudaMemsetAsync(ws + L.status, 0, 16, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ws + L.scales, 0, 8, s);
+  if (e != cudaSuccess) {
+    set_detail("cudaMemsetAsync(status, amax)", e);
+    return TPMLP_ERR_CUDA;
+  }
+  if (tokens == 0) return TPMLP_OK;
+  const int T = tokens, h = c.hidden, f = c.ffn, t = c.shards, ft = f / t;
+  const void* Xop = X;
+  if (c.use_layernorm) {
+    void* Xn = ws + L.xn;
+    TRY(run(&H->core, "layernorm_fwd", s, [&] {
+      return launch_ln_fwd(true, X, ln_gamma, ln_beta, Xn,
+                           reinterpret_cast<float*>(ws + L.mean),
+                           reinterpret_cast<float*>(ws + L.rstd), T, h,
+                           c.ln_eps, s);
+    }));
+    Xop = Xn;
+  }
+  unsigned int* amax = reinterpret_cast<unsigned int*>(ws + L.scales);
+  float* scl = reinterpret_cast<float*>(ws + L.scales) + 2;
+  const float* wscl = reinterpret_cast<const float*>(pk + P.scales) + 2;
+  uint8_t* Xq = reinterpret_cast<uint8_t*>(ws + L.xq);
+  void* Y = ws + L.y;
+  uint8_t* Yq = reinterpret_cast<uint8_t*>(ws + L.yq);
+  TRY(run(&H->core, "fp8_amax_x", s,
+          [&] { return launch_amax_bf16(Xop, size_t(T) * h, amax, s); }));
+  TRY(run(&H->core, "fp8_quantize_x", s, [&] {
+    return launch_quantize_e4m3(Xop, size_t(T) * h, amax, Xq, scl, s);
+  }));
+  CUtensorMap ta, tb, to, to2;
+  GemmArgs g1 = base_args(H, ws, L.status);
+  g1.M = T; g1.N = f; g1.K = h; g1.kb_per_seg = (h + 127) / 128;
+  g1.out = Y; g1.ldo = f; g1.bias = bias1;
+  g1.scale_a = scl; g1.scale_b = wscl; g1.amax_out = amax + 1;
+  TRY(encode_map_u8(&ta, Xq, h, T, h, TC_BM));
+  TRY(encode_map_u8(&tb, pk + P.aqt, h, f, h, TC2_BN_HALF));
+  TRY(out_map(&to, Y, false, T, f, f));
+  TRY(run(&H->core, "gemm1_gelu_fp8", s, [&] {
+    return launch_gemm_tc2_e4m3(EPI_GELU_FWD, ta, tb, to, to, g1, sms / 2, s);
+  }));
+  TRY(run(&H->core, "fp8_quantize_y", s, [&] {
+    return launch_quantize_e4m3(Y, size_t(T) * f, amax + 1, Yq, scl + 1, s);
+  }));
+  GemmArgs g2 = base_args(H, ws, L.status);
+  g2.M = T; g2.N = h; g2.K = f; g2.num_seg = t; g2.kb_per_seg = ft / 128;
+  g2.out = Z; g2.ldo = h; g2.bias = bias2;
+  g2.scale_a = scl + 1; g2.scale_b = wscl + 1;
+  if (c.use_residual) {
+    g2.aux = X;
+    g2.ldaux = h;
+  }
+  TRY(encode_map_u8(&ta, Yq, f, T, f, TC_BM));
+  TRY(encode_map_u8(&tb, pk + P.bqt, f, h, f, TC2_BN_HALF));
+  TRY(out_map(&to2, Z, false, T, h, h));
+  return run(&H->core, "gemm2_shardsum_fp8", s, [&] {
+    return launch_gemm_tc2_e4m3(EPI_SHARDSUM, ta, tb, to2, to2, g2, sms / 2, s);
+  });
 }
 
 int tp_mlp_check(tp_mlp_handle* H, void* workspace, void* stream) {

@@ -115,3 +115,61 @@ class TensorParallelMLP:
         if self._ws is None:
             return B_.TPMLP_OK
         return B_.tp_mlp_check(self.handle, self._ws, stream)
+
+    # ------------------------------------------------------- fp8 forward --
+    def pack_fp8_weights(self, A, B, stream=None) -> torch.Tensor:
+        """Quantize A and B to E4M3 (per-tensor scales) into a new packed
+        buffer for forward_fp8 (see tp_mlp_fp8_pack_weights)."""
+        h, f = self.hidden, self.ffn
+        self._chk("A", A, (h, f), torch.bfloat16)
+        self._chk("B", B, (f, h), torch.bfloat16)
+        n = B_.tp_mlp_fp8_weights_bytes(self.handle)
+        if n == 0:
+            raise ValueError("the FP8 variant needs a bf16 handle without "
+                             "dropout and ffn / shards a multiple of 128")
+        packed = torch.empty(n, dtype=torch.uint8, device=A.device)
+        B_.tp_mlp_fp8_pack_weights(self.handle, A, B, packed, n, stream)
+        return packed
+
+    def forward_fp8(self, X, packed, b1=None, b2=None, gamma=None, beta=None,
+                    out=None, stream=None):
+        """FP8 (E4M3) forward with weights from pack_fp8_weights."""
+        T = X.shape[0]
+        h, f = self.hidden, self.ffn
+        self._chk("X", X, (T, h), torch.bfloat16)
+        self._chk("b1", b1, (f,), torch.float32)
+        self._chk("b2", b2, (h,), torch.float32)
+        self._chk("gamma", gamma, (h,), torch.float32)
+        self._chk("beta", beta, (h,), torch.float32)
+        Z = out if out is not None else torch.empty((T, h), dtype=torch.bfloat16,
+                                                   device=X.device)
+        self._chk("Z", Z, (T, h), torch.bfloat16)
+        need = B_.tp_mlp_fp8_workspace_bytes(self.handle, T)
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = torch.empty(max(need, 256), dtype=torch.uint8,
+                                   device=self.device)
+        B_.tp_mlp_forward_fp8(self.handle, T, X, packed, b1, b2, gamma, beta,
+                              Z, self._ws, self._ws.numel(), stream)
+        return Z
+
+    def fp8_saved(self, tokens: int, which: str, packed=None):
+        """Views of the FP8 path's intermediates: "xq" [T,h] / "yq" [T,f]
+        uint8 codes, "y" [T,f] bf16, "scales" (4 words: amax_x, amax_y as
+        fp32 bits, s_x, s_y) in the workspace; "aqt" [f,h], "bqt" [h,f]
+        codes and "wscales" (amax_a, amax_b, s_a, s_b) in `packed`."""
+        h, f = self.hidden, self.ffn
+        spec = {"xq": (B_.TPMLP_FP8_WS_XQ, (tokens, h), torch.uint8, False),
+                "y": (B_.TPMLP_FP8_WS_Y, (tokens, f), torch.bfloat16, False),
+                "yq": (B_.TPMLP_FP8_WS_YQ, (tokens, f), torch.uint8, False),
+                "scales": (B_.TPMLP_FP8_WS_SCALES, (4,), torch.int32, False),
+                "aqt": (B_.TPMLP_FP8_PACK_AQT, (f, h), torch.uint8, True),
+                "bqt": (B_.TPMLP_FP8_PACK_BQT, (h, f), torch.uint8, True),
+                "wscales": (B_.TPMLP_FP8_PACK_SCALES, (4,), torch.int32, True)}
+        code, shape, dt, in_pack = spec[which]
+        buf = packed if in_pack else self._ws
+        off = B_.tp_mlp_fp8_offset(self.handle, tokens, code)
+        n = 1
+        for d in shape:
+            n *= d
+        n *= torch.tensor([], dtype=dt).element_size()
+        return buf[off:off + n].view(dt).view(*shape)
