@@ -43,8 +43,14 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   constexpr uint32_t A_TILE = KB * KBLOCK_BYTES;   // 128 rows x D
   constexpr uint32_t B_TILE = KB * ATOM_BYTES;     // 64 rows x D
   constexpr int NE = KV ? 2 : 1;                   // staged tiles per step
+  // Stages of the streamed tile pair: the load for step n + NB can only
+  // start once step n's gradient MMAs have read its stage, so the ring must
+  // cover the TMA latency (3 fit next to KV's two staged tiles, 4 for Q).
+  constexpr int NB = KV ? 3 : 4;
   constexpr uint32_t E_TILE = KBLOCK_BYTES;        // 128 rows x 64
   constexpr uint32_t VEC_BYTES = 512;              // 64 lse2 + 64 delta
+  constexpr uint32_t VEC_TOTAL = KV ? NB * VEC_BYTES : 0;
+  constexpr int NBARS = 11 + 2 * NB;
   constexpr uint32_t B_TX = 2 * B_TILE + (KV ? VEC_BYTES : 0);
   constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 64, false, false);
   constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, false, true);
@@ -58,15 +64,16 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   const uint32_t sA1 = ptx::smem_u32(smem);
   const uint32_t sA2 = sA1 + A_TILE;
   const uint32_t sB = sA2 + A_TILE;                // [stage][B1 | B2]
-  const uint32_t sE = sB + 4 * B_TILE;             // [stage][dS | P]
-  uint8_t* vec_gen = smem + 2 * A_TILE + 4 * B_TILE + 2 * NE * E_TILE;
+  const uint32_t sE = sB + NB * 2 * B_TILE;        // [buffer][dS | P]
+  uint8_t* vec_gen = smem + 2 * A_TILE + NB * 2 * B_TILE + 2 * NE * E_TILE;
   const uint32_t sVec = ptx::smem_u32(vec_gen);    // [stage][lse2 | delta]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(vec_gen + 2 * VEC_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(vec_gen + VEC_TOTAL);
   const uint32_t b0 = ptx::smem_u32(bars);
-  const uint32_t a_full = b0, b_full = b0 + 8, b_empty = b0 + 24,
-                 s_full = b0 + 40, s_empty = b0 + 56, e_full = b0 + 72,
-                 e_empty = b0 + 88, o_full = b0 + 104, done_bar = b0 + 112;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
+  const uint32_t a_full = b0, b_full = b0 + 8, b_empty = b_full + 8 * NB,
+                 s_full = b_empty + 8 * NB, s_empty = s_full + 16,
+                 e_full = s_empty + 16, e_empty = e_full + 16,
+                 o_full = e_empty + 16, done_bar = o_full + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -89,9 +96,11 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(a_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NB; ++i) {
       ptx::mbar_init(b_full + 8 * i, 1);
       ptx::mbar_init(b_empty + 8 * i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(s_full + 8 * i, 1);
       ptx::mbar_init(s_empty + 8 * i, SOFTMAX_WARPS);
       ptx::mbar_init(e_full + 8 * i, SOFTMAX_WARPS);
@@ -124,11 +133,11 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                          row0);
       }
       for (int n = 0; n < nsteps; ++n) {
-        const uint32_t st = n & 1, ph = (n >> 1) & 1;
-        if (!wait_bounded(b_empty + 8 * st, ph ^ 1, ctl, ROLE_PRODUCER)) break;
+        const uint32_t bs = n % NB, bph = (n / NB) & 1;
+        if (!wait_bounded(b_empty + 8 * bs, bph ^ 1, ctl, ROLE_PRODUCER)) break;
         const int col0 = seq * a.seq_len + (cb_begin + n) * 64;
-        const uint32_t bf = b_full + 8 * st;
-        const uint32_t dB1 = sB + st * 2 * B_TILE, dB2 = dB1 + B_TILE;
+        const uint32_t bf = b_full + 8 * bs;
+        const uint32_t dB1 = sB + bs * 2 * B_TILE, dB2 = dB1 + B_TILE;
         ptx::mbar_arrive_expect_tx(bf, B_TX);
 #pragma unroll
         for (int kk = 0; kk < KB; ++kk) {
@@ -137,8 +146,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         }
         if constexpr (KV) {
           const size_t off = static_cast<size_t>(head) * a.ld_stat + col0;
-          ptx::bulk_load_1d(sVec + st * VEC_BYTES, a.lse + off, 256, bf);
-          ptx::bulk_load_1d(sVec + st * VEC_BYTES + 256, a.delta + off, 256, bf);
+          ptx::bulk_load_1d(sVec + bs * VEC_BYTES, a.lse + off, 256, bf);
+          ptx::bulk_load_1d(sVec + bs * VEC_BYTES + 256, a.delta + off, 256, bf);
         }
       }
     }
@@ -147,52 +156,58 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     if (lane == 0) {
       // -------------------------------------------------- MMA issuer --
       bool alive = wait_bounded(a_full, 0, ctl, ROLE_MMA);
+      const uint64_t dA1 = ptx::sdesc_sw128(sA1, 16, 1024);
+      const uint64_t dA2 = ptx::sdesc_sw128(sA2, 16, 1024);
+      const uint64_t dBk = ptx::sdesc_sw128(sB, 16, 1024);          // K-major
+      const uint64_t dBm = ptx::sdesc_sw128(sB, ATOM_BYTES, 1024);  // MN-major
+      const uint64_t dE = ptx::sdesc_sw128(sE, 16, 1024);
       auto issue_s = [&](int n) -> bool {
         const uint32_t st = n & 1, ph = (n >> 1) & 1;
-        if (!wait_bounded(b_full + 8 * st, ph, ctl, ROLE_MMA)) return false;
+        const uint32_t bs = n % NB, bph = (n / NB) & 1;
+        if (!wait_bounded(b_full + 8 * bs, bph, ctl, ROLE_MMA)) return false;
         if (!wait_bounded(s_empty + 8 * st, ph ^ 1, ctl, ROLE_MMA)) return false;
         ptx::tc_fence_after();
-        const uint32_t dB1 = sB + st * 2 * B_TILE, dB2 = dB1 + B_TILE;
+        const uint64_t b1 = desc_add(dBk, bs * 2 * B_TILE);
+        const uint64_t b2 = desc_add(b1, B_TILE);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t ao = (k / 4) * KBLOCK_BYTES + (k % 4) * 32;
           const uint32_t bo = (k / 4) * ATOM_BYTES + (k % 4) * 32;
-          ptx::mma_bf16(tmem + 64 * st, ptx::sdesc_sw128(sA1 + ao, 16, 1024),
-                        ptx::sdesc_sw128(dB1 + bo, 16, 1024), IDESC_S,
-                        k > 0 ? 1u : 0u);
+          ptx::mma_bf16(tmem + 64 * st, desc_add(dA1, ao), desc_add(b1, bo),
+                        IDESC_S, k > 0 ? 1u : 0u);
         }
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t ao = (k / 4) * KBLOCK_BYTES + (k % 4) * 32;
           const uint32_t bo = (k / 4) * ATOM_BYTES + (k % 4) * 32;
-          ptx::mma_bf16(tmem + 128 + 64 * st,
-                        ptx::sdesc_sw128(sA2 + ao, 16, 1024),
-                        ptx::sdesc_sw128(dB2 + bo, 16, 1024), IDESC_S,
-                        k > 0 ? 1u : 0u);
+          ptx::mma_bf16(tmem + 128 + 64 * st, desc_add(dA2, ao),
+                        desc_add(b2, bo), IDESC_S, k > 0 ? 1u : 0u);
         }
         ptx::mma_commit(s_full + 8 * st);
         return true;
       };
       auto issue_o = [&](int n) -> bool {
         const uint32_t st = n & 1, ph = (n >> 1) & 1;
+        const uint32_t bs = n % NB;
         if (!wait_bounded(e_full + 8 * st, ph, ctl, ROLE_MMA)) return false;
         ptx::tc_fence_after();
-        const uint32_t dB1 = sB + st * 2 * B_TILE, dB2 = dB1 + B_TILE;
-        const uint32_t e2 = sE + st * NE * E_TILE, e1 = e2 + E_TILE;
+        const uint64_t b1 = desc_add(dBm, bs * 2 * B_TILE);
+        const uint64_t b2 = desc_add(b1, B_TILE);
+        const uint64_t e2 = desc_add(dE, st * NE * E_TILE);
+        const uint64_t e1 = desc_add(e2, E_TILE);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          ptx::mma_bf16(tmem + TMEM_OUT2, ptx::sdesc_sw128(e2 + 32 * k, 16, 1024),
-                        ptx::sdesc_sw128(dB1 + 2048 * k, ATOM_BYTES, 1024),
-                        IDESC_O, (n > 0 || k > 0) ? 1u : 0u);
+          ptx::mma_bf16(tmem + TMEM_OUT2, desc_add(e2, 32 * k),
+                        desc_add(b1, 2048 * k), IDESC_O,
+                        (n > 0 || k > 0) ? 1u : 0u);
         if constexpr (KV) {
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            ptx::mma_bf16(tmem + TMEM_OUT1,
-                          ptx::sdesc_sw128(e1 + 32 * k, 16, 1024),
-                          ptx::sdesc_sw128(dB2 + 2048 * k, ATOM_BYTES, 1024),
-                          IDESC_O, (n > 0 || k > 0) ? 1u : 0u);
+            ptx::mma_bf16(tmem + TMEM_OUT1, desc_add(e1, 32 * k),
+                          desc_add(b2, 2048 * k), IDESC_O,
+                          (n > 0 || k > 0) ? 1u : 0u);
         }
-        ptx::mma_commit(b_empty + 8 * st);
+        ptx::mma_commit(b_empty + 8 * bs);
         ptx::mma_commit(e_empty + 8 * st);
         return true;
       };
@@ -227,8 +242,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     bool alive = true;
     for (int n = 0; n < nsteps; ++n) {
       const uint32_t st = n & 1, ph = (n >> 1) & 1;
+      const uint32_t bs = n % NB, bph = (n / NB) & 1;
       if (!warp_wait(s_full + 8 * st, ph, ctl, ROLE_EPILOGUE) ||
-          (KV && !warp_wait(b_full + 8 * st, ph, ctl, ROLE_EPILOGUE)) ||
+          (KV && !warp_wait(b_full + 8 * bs, bph, ctl, ROLE_EPILOGUE)) ||
           !warp_wait(e_empty + 8 * st, ph ^ 1, ctl, ROLE_EPILOGUE)) {
         alive = false;
         break;
@@ -240,7 +256,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       const int diff = rb * 128 + r - cb * 64 - 32 * hf;
       const int lo = (KV && a.causal) ? diff : -1;
       const int hi = (!KV && a.causal) ? diff : 64;
-      const float* vl = vec + st * (VEC_BYTES / 4) + 32 * hf;
+      const float* vl = vec + bs * (VEC_BYTES / 4) + 32 * hf;
       const float* vd = vl + 64;
       const uint32_t e2 = sE + st * NE * E_TILE, e1 = e2 + E_TILE;
       uint32_t s1[32], s2[32];
@@ -329,8 +345,10 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
 template <int D, bool KV>
 size_t attn_bwd_smem() {
   constexpr int KB = D / 64;
-  const size_t need = 1024 + 2 * KB * KBLOCK_BYTES + 4 * KB * ATOM_BYTES +
-                      2 * (KV ? 2 : 1) * KBLOCK_BYTES + 1024 + 15 * 8 + 16;
+  constexpr int NB = KV ? 3 : 4;
+  const size_t need = 1024 + 2 * KB * KBLOCK_BYTES + NB * 2 * KB * ATOM_BYTES +
+                      2 * (KV ? 2 : 1) * KBLOCK_BYTES + (KV ? NB * 512 : 0) +
+                      (11 + 2 * NB) * 8 + 16;
   return need > 116 * 1024 ? need : 116 * 1024;
 }
 

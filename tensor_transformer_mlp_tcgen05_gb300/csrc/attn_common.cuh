@@ -23,6 +23,57 @@ __device__ __forceinline__ void cta_barrier_att() {
   asm volatile("bar.sync 1, %0;" ::"n"(ATT_THREADS) : "memory");
 }
 
+// A shared-memory descriptor moved by `bytes` (a multiple of 16): the start
+// address field holds addr >> 4 in 14 bits and shared-memory addresses are
+// below 2^18, so the addition never carries out of the field.  Lets the MMA
+// issuer build each operand's descriptor once and step it with constants,
+// keeping the single issuing thread ahead of 64-cycle MMAs.
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t bytes) {
+  return desc + (bytes >> 4);
+}
+
+// Named barrier between the two softmax warps of row quarter q (ids 3-6).
+__device__ __forceinline__ void pair_barrier(int q) {
+  asm volatile("bar.sync %0, 64;" ::"r"(3 + q) : "memory");
+}
+
+// 32 TMEM lanes x 32 consecutive 32-bit columns from registers (the store
+// counterpart of ptx::tmem_ld_32x32b_x32), and the wait for such stores.
+__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr,
+                                                   const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
+      "%30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
+      "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]),
+      "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),
+      "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
+      "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]),
+      "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]: bf16 A read from tensor memory (row m in
+// lane m, K packed two bf16 per 32-bit column, lower K index in the low
+// half), B from a shared-memory descriptor, fp32 accumulator.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem,
+                                            uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(
+          d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // Named barrier among the softmax warps only.
 __device__ __forceinline__ void softmax_barrier() {
   asm volatile("bar.sync 2, %0;" ::"n"(SOFTMAX_WARPS * 32) : "memory");

@@ -9,13 +9,13 @@
 // live in TMEM; the probabilities are staged in shared memory as the bf16 A
 // operand of the second MMA.
 //
-// Forward, two passes over the key blocks the query block may see (all of
-// them, or blocks 0..qb when causal):
-//   pass 1: S = Q K^T (tcgen05, M = N = 128, K = d) -> running row max m
-//           and row sum l of exp2(S log2e / sqrt d - m);
-//   pass 2: S again -> P = exp2(S log2e / sqrt d - m) / l (exact
-//           probabilities, so the output accumulator is never rescaled) ->
-//           bf16 P in shared memory -> O += P V.
+// Forward, one pass over the key blocks the query block may see (all of
+// them, or blocks 0..qb when causal): S = Q K^T (tcgen05, M = N = 128,
+// K = d) into one of two TMEM buffers -> P = exp2(S log2e / sqrt d - m_ref)
+// with a lazily raised reference max -> bf16 P stored by the softmax
+// threads into TMEM (one row per lane) -> O += P V with A read from TMEM
+// (only V comes from shared memory, which keeps the MMA's operand reads
+// under the SM's shared-memory bandwidth); O / l at the end.
 // Outputs: the context rows (bf16) and, for the backward, every (head,
 // token) row's log-sum-exp in base 2 of the scores scaled by log2(e)/sqrt(d),
 // lse2 = m + log2(l), so that P = exp2(S log2(e)/sqrt(d) - lse2).
@@ -40,10 +40,10 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   constexpr int KB = D / 64;                           // 64-wide blocks of d
   constexpr uint32_t QK_TILE = KB * KBLOCK_BYTES;      // 128 x D
   constexpr uint32_t V_TILE = 2 * KB * ATOM_BYTES;     // 128 keys x D
-  constexpr uint32_t P_TILE = 2 * KBLOCK_BYTES;        // 128 x 128
   constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, false, false);
   constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, false, true);
   constexpr uint32_t TMEM_O = 256;
+  constexpr uint32_t TMEM_P = 384;   // P, 128 keys as 64 packed bf16 pairs
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -51,8 +51,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   const uint32_t sQ = ptx::smem_u32(smem);
   const uint32_t sK = sQ + QK_TILE;
   const uint32_t sV = sK + 2 * QK_TILE;
-  const uint32_t sP = sV + 2 * V_TILE;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + QK_TILE * 3 + V_TILE * 2 + P_TILE);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + QK_TILE * 3 + V_TILE * 2);
   const uint32_t b0 = ptx::smem_u32(bars);
   const uint32_t q_full = b0, k_full = b0 + 8, k_empty = b0 + 24,
                  v_full = b0 + 40, v_empty = b0 + 56, s_full = b0 + 72,
@@ -60,7 +59,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                  o_full = b0 + 120, done_bar = b0 + 128;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 17);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
-  // Row max / row sum exchange between the two column halves: [2][2][128].
+  // Row max (per block, two parities) and row sum exchange between the two
+  // column halves: [3][2][128].
   float* red = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + 256);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -107,38 +107,30 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
 #pragma unroll
       for (int kk = 0; kk < KB; ++kk)
         ptx::tma_load_2d(sQ + kk * KBLOCK_BYTES, &tmQK, q_full, hc.q + 64 * kk, row0);
-      uint32_t kc = 0, vc = 0;
-      for (int pass = 0; alive && pass < 2; ++pass) {
-        for (int kb = 0; alive && kb < nk; ++kb) {
-          const int key0 = seq * a.seq_len + kb * 128;
-          const uint32_t ks = kc & 1, kph = (kc >> 1) & 1;
-          if (!wait_bounded(k_empty + 8 * ks, kph ^ 1, ctl, ROLE_PRODUCER)) {
-            alive = false;
-            break;
-          }
-          ptx::mbar_arrive_expect_tx(k_full + 8 * ks, QK_TILE);
-#pragma unroll
-          for (int kk = 0; kk < KB; ++kk)
-            ptx::tma_load_2d(sK + ks * QK_TILE + kk * KBLOCK_BYTES, &tmQK,
-                             k_full + 8 * ks, hc.k + 64 * kk, key0);
-          ++kc;
-          if (pass == 1) {
-            const uint32_t vs = vc & 1, vph = (vc >> 1) & 1;
-            if (!wait_bounded(v_empty + 8 * vs, vph ^ 1, ctl, ROLE_PRODUCER)) {
-              alive = false;
-              break;
-            }
-            ptx::mbar_arrive_expect_tx(v_full + 8 * vs, V_TILE);
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2)
-#pragma unroll
-              for (int at = 0; at < KB; ++at)
-                ptx::tma_load_2d(sV + vs * V_TILE + (h2 * KB + at) * ATOM_BYTES,
-                                 &tmV, v_full + 8 * vs, hc.v + 64 * at,
-                                 key0 + 64 * h2);
-            ++vc;
-          }
+      for (int kb = 0; alive && kb < nk; ++kb) {
+        const int key0 = seq * a.seq_len + kb * 128;
+        const uint32_t st = kb & 1, ph = (kb >> 1) & 1;
+        if (!wait_bounded(k_empty + 8 * st, ph ^ 1, ctl, ROLE_PRODUCER)) {
+          alive = false;
+          break;
         }
+        ptx::mbar_arrive_expect_tx(k_full + 8 * st, QK_TILE);
+#pragma unroll
+        for (int kk = 0; kk < KB; ++kk)
+          ptx::tma_load_2d(sK + st * QK_TILE + kk * KBLOCK_BYTES, &tmQK,
+                           k_full + 8 * st, hc.k + 64 * kk, key0);
+        if (!wait_bounded(v_empty + 8 * st, ph ^ 1, ctl, ROLE_PRODUCER)) {
+          alive = false;
+          break;
+        }
+        ptx::mbar_arrive_expect_tx(v_full + 8 * st, V_TILE);
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+          for (int at = 0; at < KB; ++at)
+            ptx::tma_load_2d(sV + st * V_TILE + (h2 * KB + at) * ATOM_BYTES,
+                             &tmV, v_full + 8 * st, hc.v + 64 * at,
+                             key0 + 64 * h2);
       }
     }
     __syncwarp();
@@ -147,19 +139,21 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       // -------------------------------------------------- MMA issuer --
       bool alive = wait_bounded(q_full, 0, ctl, ROLE_MMA);
       uint32_t kc = 0, sc = 0, vc = 0;
+      const uint64_t dQ = ptx::sdesc_sw128(sQ, 16, 1024);
+      const uint64_t dK = ptx::sdesc_sw128(sK, 16, 1024);
+      const uint64_t dV = ptx::sdesc_sw128(sV, ATOM_BYTES, 1024);
       auto issue_s = [&]() -> bool {
         const uint32_t ks = kc & 1, kph = (kc >> 1) & 1;
         const uint32_t sb = sc & 1, sph = (sc >> 1) & 1;
         if (!wait_bounded(k_full + 8 * ks, kph, ctl, ROLE_MMA)) return false;
         if (!wait_bounded(s_empty + 8 * sb, sph ^ 1, ctl, ROLE_MMA)) return false;
         ptx::tc_fence_after();
+        const uint64_t dKs = desc_add(dK, ks * QK_TILE);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint64_t ad = ptx::sdesc_sw128(
-              sQ + (k / 4) * KBLOCK_BYTES + (k % 4) * 32, 16, 1024);
-          const uint64_t bd = ptx::sdesc_sw128(
-              sK + ks * QK_TILE + (k / 4) * KBLOCK_BYTES + (k % 4) * 32, 16, 1024);
-          ptx::mma_bf16(tmem + sb * 128, ad, bd, IDESC_S, k > 0 ? 1u : 0u);
+          const uint32_t off = (k / 4) * KBLOCK_BYTES + (k % 4) * 32;
+          ptx::mma_bf16(tmem + sb * 128, desc_add(dQ, off), desc_add(dKs, off),
+                        IDESC_S, k > 0 ? 1u : 0u);
         }
         ptx::mma_commit(k_empty + 8 * ks);
         ptx::mma_commit(s_full + 8 * sb);
@@ -167,8 +161,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         ++sc;
         return true;
       };
-      for (int kb = 0; alive && kb < nk; ++kb) alive = issue_s();  // pass 1
-      if (alive) alive = issue_s();                                  // pass 2
+      if (alive) alive = issue_s();
       for (int kb = 0; alive && kb < nk; ++kb) {
         if (kb + 1 < nk && !(alive = issue_s())) break;
         const uint32_t vs = vc & 1, vph = (vc >> 1) & 1;
@@ -178,16 +171,12 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
           break;
         }
         ptx::tc_fence_after();
+        const uint64_t dVs = desc_add(dV, vs * V_TILE);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint64_t ad = ptx::sdesc_sw128(
-              sP + (k / 4) * KBLOCK_BYTES + (k % 4) * 32, 16, 1024);
-          const uint64_t bd = ptx::sdesc_sw128(
-              sV + vs * V_TILE + (k / 4) * KB * ATOM_BYTES + (k % 4) * 2048,
-              ATOM_BYTES, 1024);
-          ptx::mma_bf16(tmem + TMEM_O, ad, bd, IDESC_O,
-                        (kb > 0 || k > 0) ? 1u : 0u);
-        }
+        for (int k = 0; k < 8; ++k)
+          mma_bf16_ts(tmem + TMEM_O, tmem + TMEM_P + 8 * k,
+                      desc_add(dVs, (k / 4) * KB * ATOM_BYTES + (k % 4) * 2048),
+                      IDESC_O, (kb > 0 || k > 0) ? 1u : 0u);
         ptx::mma_commit(v_empty + 8 * vs);
         ptx::mma_commit(p_empty);
         ++vc;
@@ -201,95 +190,135 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     __syncwarp();
   } else if (warp >= SOFTMAX_WARP0) {
     // ------------------------------------------------------ softmax --
-    // Two warps share each row quarter: column half `hf` (64 of the 128 key
-    // columns of a block; 64 / 32 of the D output columns).  Pass 1 finds
-    // the row max m of the scaled scores (log2 units), the halves meeting
-    // once through shared memory; pass 2 writes P = exp2(x - m) (final max,
-    // so nothing is ever rescaled) into the half's k-block of the P tile and
-    // accumulates the half's part of l = sum P; the output is O / (l0 + l1).
-    // Every softmax warp passes both named barriers on every path.
+    // One pass with a lazily updated reference max (log2 units of the
+    // scaled scores).  Two warps share each row quarter, one per column
+    // half; per block they exchange their halves' maxima through shared
+    // memory.  P = exp2(x - m_ref) is staged for P V; only when the block
+    // max exceeds m_ref by more than RESCALE_LOG2 does m_ref move up, with
+    // O (each warp its half of the D columns, after the previous P V has
+    // finished) and the partial row sums scaled by exp2(m_old - m_new).
+    // The decision depends only on the scores, so it is deterministic, and
+    // P stays below 2^RESCALE_LOG2.  Output O / (l0 + l1); saved lse2 =
+    // m_ref + log2 l.  Every softmax warp passes the same barriers on
+    // every path.
+    constexpr float RESCALE_LOG2 = 8.f;
     const int q = warp & 3;
     const int hf = (warp - SOFTMAX_WARP0) >> 2;
     const int r = q * 32 + lane;          // query row inside the block
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     const float sl2 = a.scale_log2;
-    float m = -INFINITY, l = 0.f;
-    uint32_t sc = 0;
+    float m_ref = -INFINITY, l = 0.f;
     bool alive = true;
     for (int kb = 0; kb < nk; ++kb) {
-      const uint32_t sb = sc & 1, sph = (sc >> 1) & 1;
-      if (!warp_wait(s_full + 8 * sb, sph, ctl, ROLE_EPILOGUE)) {
-        alive = false;
-        break;
-      }
-      ptx::tc_fence_after();
-      uint32_t sv[64];
-      uint32_t (&s0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[0]);
-      uint32_t (&s1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[32]);
+      const uint32_t sb = kb & 1, sph = (kb >> 1) & 1;
+      bool ok = alive && warp_wait(s_full + 8 * sb, sph, ctl, ROLE_EPILOGUE);
       const uint32_t col = tmem + lane_base + sb * 128 + 64 * hf;
-      ptx::tmem_ld_32x32b_x32(col, s0);
-      ptx::tmem_ld_32x32b_x32(col + 32, s1);
-      ptx::tmem_ld_wait();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(s_empty + 8 * sb);
-      ++sc;
-      const int lim = (a.causal && kb == qb) ? r - 64 * hf : 63;
+      // only the diagonal block of a causal row masks anything
+      const bool diag = a.causal && kb == qb;
+      const int lim = diag ? r - 64 * hf : 63;
+      uint32_t sv[64];
       float mb = -INFINITY;
+      if (ok) {
+        ptx::tc_fence_after();
+        uint32_t (&s0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[0]);
+        uint32_t (&s1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[32]);
+        ptx::tmem_ld_32x32b_x32(col, s0);
+        ptx::tmem_ld_32x32b_x32(col + 32, s1);
+        ptx::tmem_ld_wait();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(s_empty + 8 * sb);
+        if (diag) {
 #pragma unroll
-      for (int c = 0; c < 64; ++c)
-        if (c <= lim) mb = fmaxf(mb, __uint_as_float(sv[c]));
-      m = fmaxf(m, mb * sl2);
-    }
-    red[hf * 128 + r] = m;
-    softmax_barrier();
-    m = fmaxf(red[r], red[128 + r]);
-    for (int kb = 0; alive && kb < nk; ++kb) {
-      const uint32_t sb = sc & 1, sph = (sc >> 1) & 1;
-      if (!warp_wait(s_full + 8 * sb, sph, ctl, ROLE_EPILOGUE) ||
-          !warp_wait(p_empty, (kb & 1) ^ 1, ctl, ROLE_EPILOGUE)) {
+          for (int c = 0; c < 64; ++c)
+            if (c <= lim) mb = fmaxf(mb, __uint_as_float(sv[c]));
+        } else {
+          float m0 = __uint_as_float(sv[0]), m1 = __uint_as_float(sv[1]);
+#pragma unroll
+          for (int c = 2; c < 64; c += 2) {
+            m0 = fmaxf(m0, __uint_as_float(sv[c]));
+            m1 = fmaxf(m1, __uint_as_float(sv[c + 1]));
+          }
+          mb = fmaxf(m0, m1);
+        }
+      }
+      // exchange the halves' maxima (double-buffered by block parity)
+      red[(kb & 1) * 256 + hf * 128 + r] = mb * sl2;
+      pair_barrier(q);
+      mb = fmaxf(red[(kb & 1) * 256 + r], red[(kb & 1) * 256 + 128 + r]);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) {
         alive = false;
-        break;
+        continue;              // keep meeting the sibling's barriers
       }
-      ptx::tc_fence_after();
-      const int lim = (a.causal && kb == qb) ? r - 64 * hf : 63;
-      uint32_t sv[64];
-      uint32_t (&s0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[0]);
-      uint32_t (&s1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[32]);
-      const uint32_t col = tmem + lane_base + sb * 128 + 64 * hf;
-      ptx::tmem_ld_32x32b_x32(col, s0);
-      ptx::tmem_ld_32x32b_x32(col + 32, s1);
-      ptx::tmem_ld_wait();
+      float alpha = 1.f;
+      const bool move = mb > m_ref + RESCALE_LOG2;
+      if (move) {
+        alpha = exp2f(m_ref - mb);       // 0 on the first block
+        m_ref = mb;
+      }
       uint32_t w[32];
+      float lb0 = 0.f, lb1 = 0.f;
+      if (diag) {
 #pragma unroll
-      for (int c = 0; c < 64; c += 2) {
-        float p0 = exp2f(fmaf(__uint_as_float(sv[c]), sl2, -m));
-        float p1 = exp2f(fmaf(__uint_as_float(sv[c + 1]), sl2, -m));
-        p0 = c <= lim ? p0 : 0.f;
-        p1 = c + 1 <= lim ? p1 : 0.f;
-        l += p0 + p1;
-        w[c / 2] = pack_bf16x2(p0, p1);
+        for (int c = 0; c < 64; c += 2) {
+          float p0 = exp2f(fmaf(__uint_as_float(sv[c]), sl2, -m_ref));
+          float p1 = exp2f(fmaf(__uint_as_float(sv[c + 1]), sl2, -m_ref));
+          p0 = c <= lim ? p0 : 0.f;
+          p1 = c + 1 <= lim ? p1 : 0.f;
+          lb0 += p0;
+          lb1 += p1;
+          w[c / 2] = pack_bf16x2(p0, p1);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) {
+          const float p0 = exp2f(fmaf(__uint_as_float(sv[c]), sl2, -m_ref));
+          const float p1 = exp2f(fmaf(__uint_as_float(sv[c + 1]), sl2, -m_ref));
+          lb0 += p0;
+          lb1 += p1;
+          w[c / 2] = pack_bf16x2(p0, p1);
+        }
       }
-      stage_row64(sP + hf * KBLOCK_BYTES, r, w);
+      const float lb = lb0 + lb1;
+      l = l * alpha + lb;
+      if (!warp_wait(p_empty, (kb & 1) ^ 1, ctl, ROLE_EPILOGUE)) {
+        alive = false;
+        continue;
+      }
+      // a rescale of O needs every earlier P V finished (p_empty above)
+      if (__any_sync(0xffffffffu, move) && kb > 0) {
+        ptx::tc_fence_after();
+#pragma unroll 1
+        for (int j = 0; j < D / 64; ++j) {
+          const uint32_t oc = tmem + lane_base + TMEM_O + hf * (D / 2) + 32 * j;
+          uint32_t ov[32];
+          ptx::tmem_ld_32x32b_x32(oc, ov);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+          tmem_st_32x32b_x32(oc, ov);
+        }
+        tmem_st_wait();
+      }
+      // P row into tensor memory: this half's 64 keys = 32 packed columns
+      tmem_st_32x32b_x32(tmem + lane_base + TMEM_P + 32 * hf, w);
+      tmem_st_wait();
       ptx::tc_fence_before();
-      ptx::fence_proxy_async_shared();
       __syncwarp();
-      if (lane == 0) {
-        ptx::mbar_arrive(s_empty + 8 * sb);
-        ptx::mbar_arrive(p_full);
-      }
-      ++sc;
+      if (lane == 0) ptx::mbar_arrive(p_full);
     }
-    red[256 + hf * 128 + r] = l;
+    red[512 + hf * 128 + r] = l;
     softmax_barrier();
-    l = red[256 + r] + red[256 + 128 + r];
+    l = red[512 + r] + red[512 + 128 + r];
     if (alive && warp_wait(o_full, 0, ctl, ROLE_EPILOGUE)) {
       ptx::tc_fence_after();
       const float inv_l = 1.0f / l;
       constexpr int OCH = D / 64;         // 32-column chunks per half
       __nv_bfloat16* out = a.ctx + static_cast<size_t>(row0 + r) * a.ld_ctx +
                            head * D + hf * (D / 2);
-#pragma unroll
+#pragma unroll 1
       for (int j = 0; j < OCH; ++j) {
         uint32_t ov[32];
         ptx::tmem_ld_32x32b_x32(
@@ -301,7 +330,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         store_bf16x32(out + 32 * j, v);
       }
       if (hf == 0)
-        a.lse[static_cast<size_t>(head) * a.ld_stat + row0 + r] = m + log2f(l);
+        a.lse[static_cast<size_t>(head) * a.ld_stat + row0 + r] =
+            m_ref + log2f(l);
     }
     __syncwarp();
   }
@@ -328,7 +358,7 @@ template <int D>
 size_t attn_fwd_smem() {
   constexpr int KB = D / 64;
   const size_t need = 1024 + 3 * KB * KBLOCK_BYTES + 2 * (2 * KB * ATOM_BYTES) +
-                      2 * KBLOCK_BYTES + 256 + 4 * 128 * 4;
+                      256 + 6 * 128 * 4;
   return need > 116 * 1024 ? need : 116 * 1024;
 }
 

@@ -211,3 +211,26 @@ def make_attn_inputs(w: AttnWorkload, seed: int = 0, with_bias: bool = False,
         beta = torch.zeros(h, dtype=torch.float32)
     return dict(X=X, Wqkv=Wqkv, Wo=Wo, bqkv=bqkv, bo=bo, gamma=gamma,
                 beta=beta, dZ=dZ)
+
+
+def make_attn_sign_inputs(w: AttnWorkload, seed: int = 0, c: float = 4.0):
+    """Attention inputs whose projection is exact in bf16: X has random
+    +-1 entries and every column of W_qkv holds a single +-c (random row
+    and sign), so Q, K and V are exactly +-c and each score is an integer
+    multiple of c^2 / sqrt(d) (score std c^2 in natural units: peaked
+    softmax rows with a running maximum that keeps rising across key
+    blocks).  W_o ~ N(0, w_std^2), dZ ~ N(0, 1), no biases, no LayerNorm.
+    Draw order: X signs, W_qkv rows, W_qkv signs, W_o, dZ."""
+    g = torch.Generator("cpu")
+    g.manual_seed(seed)
+    bf = torch.bfloat16
+    T, h = w.tokens, w.hidden
+    X = (torch.randint(0, 2, (T, h), generator=g) * 2 - 1).to(bf)
+    rows = torch.randint(0, h, (3 * h,), generator=g)
+    signs = (torch.randint(0, 2, (3 * h,), generator=g) * 2 - 1).float()
+    Wqkv = torch.zeros((h, 3 * h), dtype=torch.float32)
+    Wqkv[rows, torch.arange(3 * h)] = c * signs
+    Wo = _normal(g, h, h, w.w_std, bf)
+    dZ = _normal(g, T, h, w.dz_std, bf)
+    return dict(X=X, Wqkv=Wqkv.to(bf), Wo=Wo, bqkv=None, bo=None, gamma=None,
+                beta=None, dZ=dZ)
