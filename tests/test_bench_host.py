@@ -73,3 +73,22 @@ def test_oracle_slice_is_bounded():
         n = bench.oracle_tokens(w)
         assert 16 <= n <= max(16, w.tokens)
         assert (12 if w.backward else 4) * n * w.hidden * w.ffn <= 1.6e12
+
+
+def test_attention_reference_arm_runs_the_oracle_on_cpu():
+    """bench.py --impl reference on an attention workload: the fp64 oracle
+    on a bounded one-sequence sample, same metric, a valid JSON line."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"),
+                        "--impl", "reference", "--workload", "attn_tiny_d64",
+                        "--steps", "1", "--warmup", "3"],
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "TFLOP/s"
+    assert line["metric"].startswith("TP-attention")
+    assert line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
