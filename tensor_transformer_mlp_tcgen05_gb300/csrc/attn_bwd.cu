@@ -17,8 +17,9 @@
 //           rows   A1  A2   B1  B2   S1 = A1 B1^T  S2 = A2 B2^T    outputs
 //   KV      keys   K   V    Q   dO   S^T           dP^T            dK += dS^T Q, dV += P^T dO
 //   Q       query  Q   dO   K   V    S             dP              dQ += dS K
-// The elementwise step writes dS (and P for KV) as bf16 128 x 64 K-major
-// tiles in shared memory, the A operands of the output MMAs; their B
+// The elementwise step writes dS (and P for KV) as bf16 into tensor memory,
+// over the score columns it has just read (each column-half warp inside its
+// own columns), where the output MMAs take them as A operands; their B
 // operands are the streamed tiles read M/N-major (the same bytes).
 //
 // Warp roles as in the forward kernel: warp 0 TMA, warp 1 TMEM + MMA issue,
@@ -42,15 +43,14 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   constexpr int KB = D / 64;
   constexpr uint32_t A_TILE = KB * KBLOCK_BYTES;   // 128 rows x D
   constexpr uint32_t B_TILE = KB * ATOM_BYTES;     // 64 rows x D
-  constexpr int NE = KV ? 2 : 1;                   // staged tiles per step
   // Stages of the streamed tile pair: the load for step n + NB can only
   // start once step n's gradient MMAs have read its stage, so the ring must
-  // cover the TMA latency (3 fit next to KV's two staged tiles, 4 for Q).
-  constexpr int NB = KV ? 3 : 4;
-  constexpr uint32_t E_TILE = KBLOCK_BYTES;        // 128 rows x 64
+  // cover the TMA latency (4 fit for KV next to its lse / delta vectors, 5
+  // for Q).
+  constexpr int NB = KV ? 4 : 5;
   constexpr uint32_t VEC_BYTES = 512;              // 64 lse2 + 64 delta
   constexpr uint32_t VEC_TOTAL = KV ? NB * VEC_BYTES : 0;
-  constexpr int NBARS = 11 + 2 * NB;
+  constexpr int NBARS = 9 + 2 * NB;
   constexpr uint32_t B_TX = 2 * B_TILE + (KV ? VEC_BYTES : 0);
   constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 64, false, false);
   constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, false, true);
@@ -64,15 +64,14 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   const uint32_t sA1 = ptx::smem_u32(smem);
   const uint32_t sA2 = sA1 + A_TILE;
   const uint32_t sB = sA2 + A_TILE;                // [stage][B1 | B2]
-  const uint32_t sE = sB + NB * 2 * B_TILE;        // [buffer][dS | P]
-  uint8_t* vec_gen = smem + 2 * A_TILE + NB * 2 * B_TILE + 2 * NE * E_TILE;
+  uint8_t* vec_gen = smem + 2 * A_TILE + NB * 2 * B_TILE;
   const uint32_t sVec = ptx::smem_u32(vec_gen);    // [stage][lse2 | delta]
   uint64_t* bars = reinterpret_cast<uint64_t*>(vec_gen + VEC_TOTAL);
   const uint32_t b0 = ptx::smem_u32(bars);
   const uint32_t a_full = b0, b_full = b0 + 8, b_empty = b_full + 8 * NB,
-                 s_full = b_empty + 8 * NB, s_empty = s_full + 16,
-                 e_full = s_empty + 16, e_empty = e_full + 16,
-                 o_full = e_empty + 16, done_bar = o_full + 8;
+                 s_full = b_empty + 8 * NB, e_full = s_full + 16,
+                 e_empty = e_full + 16, o_full = e_empty + 16,
+                 done_bar = o_full + 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
@@ -102,7 +101,6 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(s_full + 8 * i, 1);
-      ptx::mbar_init(s_empty + 8 * i, SOFTMAX_WARPS);
       ptx::mbar_init(e_full + 8 * i, SOFTMAX_WARPS);
       ptx::mbar_init(e_empty + 8 * i, 1);
     }
@@ -160,12 +158,14 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       const uint64_t dA2 = ptx::sdesc_sw128(sA2, 16, 1024);
       const uint64_t dBk = ptx::sdesc_sw128(sB, 16, 1024);          // K-major
       const uint64_t dBm = ptx::sdesc_sw128(sB, ATOM_BYTES, 1024);  // MN-major
-      const uint64_t dE = ptx::sdesc_sw128(sE, 16, 1024);
       auto issue_s = [&](int n) -> bool {
         const uint32_t st = n & 1, ph = (n >> 1) & 1;
         const uint32_t bs = n % NB, bph = (n / NB) & 1;
         if (!wait_bounded(b_full + 8 * bs, bph, ctl, ROLE_MMA)) return false;
-        if (!wait_bounded(s_empty + 8 * st, ph ^ 1, ctl, ROLE_MMA)) return false;
+        // buffer st still holds step n - 2's P / dS until its gradient MMAs
+        // are done
+        if (n >= 2 && !wait_bounded(e_empty + 8 * st, ph ^ 1, ctl, ROLE_MMA))
+          return false;
         ptx::tc_fence_after();
         const uint64_t b1 = desc_add(dBk, bs * 2 * B_TILE);
         const uint64_t b2 = desc_add(b1, B_TILE);
@@ -193,19 +193,20 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         ptx::tc_fence_after();
         const uint64_t b1 = desc_add(dBm, bs * 2 * B_TILE);
         const uint64_t b2 = desc_add(b1, B_TILE);
-        const uint64_t e2 = desc_add(dE, st * NE * E_TILE);
-        const uint64_t e1 = desc_add(e2, E_TILE);
+        // A operands in TMEM: dS (in S2's buffer) and P (in S1's), 16 packed
+        // columns per 32-column half: k-step k at half k / 2, offset 8 (k % 2)
+        const uint32_t e2 = tmem + 128 + 64 * st, e1 = tmem + 64 * st;
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          ptx::mma_bf16(tmem + TMEM_OUT2, desc_add(e2, 32 * k),
-                        desc_add(b1, 2048 * k), IDESC_O,
-                        (n > 0 || k > 0) ? 1u : 0u);
+          mma_bf16_ts(tmem + TMEM_OUT2, e2 + (k / 2) * 32 + (k % 2) * 8,
+                      desc_add(b1, 2048 * k), IDESC_O,
+                      (n > 0 || k > 0) ? 1u : 0u);
         if constexpr (KV) {
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            ptx::mma_bf16(tmem + TMEM_OUT1, desc_add(e1, 32 * k),
-                          desc_add(b2, 2048 * k), IDESC_O,
-                          (n > 0 || k > 0) ? 1u : 0u);
+            mma_bf16_ts(tmem + TMEM_OUT1, e1 + (k / 2) * 32 + (k % 2) * 8,
+                        desc_add(b2, 2048 * k), IDESC_O,
+                        (n > 0 || k > 0) ? 1u : 0u);
         }
         ptx::mma_commit(b_empty + 8 * bs);
         ptx::mma_commit(e_empty + 8 * st);
@@ -244,8 +245,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       const uint32_t st = n & 1, ph = (n >> 1) & 1;
       const uint32_t bs = n % NB, bph = (n / NB) & 1;
       if (!warp_wait(s_full + 8 * st, ph, ctl, ROLE_EPILOGUE) ||
-          (KV && !warp_wait(b_full + 8 * bs, bph, ctl, ROLE_EPILOGUE)) ||
-          !warp_wait(e_empty + 8 * st, ph ^ 1, ctl, ROLE_EPILOGUE)) {
+          (KV && !warp_wait(b_full + 8 * bs, bph, ctl, ROLE_EPILOGUE))) {
         alive = false;
         break;
       }
@@ -258,7 +258,6 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       const int hi = (!KV && a.causal) ? diff : 64;
       const float* vl = vec + bs * (VEC_BYTES / 4) + 32 * hf;
       const float* vd = vl + 64;
-      const uint32_t e2 = sE + st * NE * E_TILE, e1 = e2 + E_TILE;
       uint32_t s1[32], s2[32];
       ptx::tmem_ld_32x32b_x32(tmem + lane_base + 64 * st + 32 * hf, s1);
       ptx::tmem_ld_32x32b_x32(tmem + lane_base + 128 + 64 * st + 32 * hf, s2);
@@ -280,15 +279,14 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         pw[i / 2] = pack_bf16x2(p[0], p[1]);
         dw[i / 2] = pack_bf16x2(ds[0], ds[1]);
       }
-      stage_units<16>(e2, r, 4 * hf, dw);
-      if constexpr (KV) stage_units<16>(e1, r, 4 * hf, pw);
+      // dS (and P) over this half's own score columns, packed two per column
+      tmem_st_32x32b_x16(tmem + lane_base + 128 + 64 * st + 32 * hf, dw);
+      if constexpr (KV)
+        tmem_st_32x32b_x16(tmem + lane_base + 64 * st + 32 * hf, pw);
+      tmem_st_wait();
       ptx::tc_fence_before();
-      ptx::fence_proxy_async_shared();
       __syncwarp();
-      if (lane == 0) {
-        ptx::mbar_arrive(s_empty + 8 * st);
-        ptx::mbar_arrive(e_full + 8 * st);
-      }
+      if (lane == 0) ptx::mbar_arrive(e_full + 8 * st);
     }
     if (alive && warp_wait(o_full, 0, ctl, ROLE_EPILOGUE)) {
       ptx::tc_fence_after();
@@ -345,10 +343,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
 template <int D, bool KV>
 size_t attn_bwd_smem() {
   constexpr int KB = D / 64;
-  constexpr int NB = KV ? 3 : 4;
+  constexpr int NB = KV ? 4 : 5;
   const size_t need = 1024 + 2 * KB * KBLOCK_BYTES + NB * 2 * KB * ATOM_BYTES +
-                      2 * (KV ? 2 : 1) * KBLOCK_BYTES + (KV ? NB * 512 : 0) +
-                      (11 + 2 * NB) * 8 + 16;
+                      (KV ? NB * 512 : 0) + (9 + 2 * NB) * 8 + 16;
   return need > 116 * 1024 ? need : 116 * 1024;
 }
 
