@@ -42,6 +42,35 @@ def test_wait_timeout_is_reported_and_context_survives():
     m.close()
 
 
+def test_attention_wait_timeout_is_reported_and_context_survives():
+    """The same for the attention block: every bounded wait in the attention
+    forward and backward kernels (and their GEMMs) gives up at once, the
+    calls report TPMLP_ERR_TIMEOUT, and the context then computes the block
+    correctly."""
+    from oracle import attention as OA
+    from tensor_transformer_mlp_tcgen05_gb300.attention import \
+        TensorParallelAttention
+    from parity_helpers import f64
+    w = W.ATTN_WORKLOADS["attn_tiny_d128"]
+    inp = W.make_attn_inputs(w, seed=32, with_bias=True)
+    d = {k: to_dev(v) for k, v in inp.items()}
+    m = TensorParallelAttention(w.hidden, w.heads, w.shards, w.tokens, w.seq)
+    B.tp_attn_set_wait_budget(m.handle, 1)
+    m.forward(d["X"], d["Wqkv"], d["Wo"], d["bqkv"], d["bo"])
+    rc = m.check()
+    assert rc == B.TPMLP_ERR_TIMEOUT, (rc, B.tp_mlp_last_detail())
+    m.backward(d["dZ"], d["X"], d["Wqkv"], d["Wo"])
+    rc = m.check()
+    assert rc == B.TPMLP_ERR_TIMEOUT, (rc, B.tp_mlp_last_detail())
+    B.tp_attn_set_wait_budget(m.handle, 2_000_000_000)
+    Z = m.forward(d["X"], d["Wqkv"], d["Wo"], d["bqkv"], d["bo"])
+    assert m.check() == B.TPMLP_OK
+    ref = OA.forward(f64(inp["X"]), f64(inp["Wqkv"]), f64(inp["Wo"]), w.heads,
+                     w.seq, w.shards, bqkv=f64(inp["bqkv"]), bo=f64(inp["bo"]))
+    assert_close("attention Z after timeout", Z.cpu(), ref["Z"])
+    m.close()
+
+
 _SINGLE_SCRIPT = r"""
 import sys
 sys.path.insert(0, {root!r}); sys.path.insert(0, {tests!r})
