@@ -16,7 +16,7 @@
 // stream of 64-row tile pairs (B1, B2):
 //           rows   A1  A2   B1  B2   S1 = A1 B1^T  S2 = A2 B2^T    outputs
 //   KV      keys   K   V    Q   dO   S^T           dP^T            dK += dS^T Q, dV += P^T dO
-//   Q       query  Q   dO   K   V    S             dP              dQ += dS K
+//   Q       query  Q   dO   K   V    S             dP              dQ += dS K, PK += P K
 // The elementwise step writes dS (and P for KV) as bf16 into tensor memory,
 // over the score columns it has just read (each column-half warp inside its
 // own columns), where the output MMAs take them as A operands; their B
@@ -49,13 +49,15 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   // for Q).
   constexpr int NB = KV ? 4 : 5;
   constexpr uint32_t VEC_BYTES = 512;              // 64 lse2 + 64 delta
-  constexpr uint32_t VEC_TOTAL = KV ? NB * VEC_BYTES : 0;
+  // KV: lse2 / delta of the streamed queries per stage; Q: the two column
+  // halves' partial row sums of dS, exchanged at the end
+  constexpr uint32_t VEC_TOTAL = KV ? NB * VEC_BYTES : 1024;
   constexpr int NBARS = 9 + 2 * NB;
   constexpr uint32_t B_TX = 2 * B_TILE + (KV ? VEC_BYTES : 0);
   constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 64, false, false);
   constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, false, true);
   constexpr uint32_t TMEM_OUT2 = 256;              // dK (KV) or dQ
-  constexpr uint32_t TMEM_OUT1 = 256 + D;          // dV (KV)
+  constexpr uint32_t TMEM_OUT1 = 256 + D;          // dV (KV) or P K (Q)
   constexpr float INV_SQRT_D = D == 64 ? 0.125f : 0.08838834764831845f;
 
   extern __shared__ uint8_t smem_raw[];
@@ -201,13 +203,13 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
           mma_bf16_ts(tmem + TMEM_OUT2, e2 + (k / 2) * 32 + (k % 2) * 8,
                       desc_add(b1, 2048 * k), IDESC_O,
                       (n > 0 || k > 0) ? 1u : 0u);
-        if constexpr (KV) {
+        // KV: dV += P^T dO.  Q: sum_j P_ij k_j += P K (same B as dQ), for
+        // the row-sum correction of dQ below.
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_bf16_ts(tmem + TMEM_OUT1, e1 + (k / 2) * 32 + (k % 2) * 8,
-                        desc_add(b2, 2048 * k), IDESC_O,
-                        (n > 0 || k > 0) ? 1u : 0u);
-        }
+        for (int k = 0; k < 4; ++k)
+          mma_bf16_ts(tmem + TMEM_OUT1, e1 + (k / 2) * 32 + (k % 2) * 8,
+                      desc_add(KV ? b2 : b1, 2048 * k), IDESC_O,
+                      (n > 0 || k > 0) ? 1u : 0u);
         ptx::mma_commit(b_empty + 8 * bs);
         ptx::mma_commit(e_empty + 8 * st);
         return true;
@@ -240,6 +242,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       delta_r = a.delta[off];
     }
     const float* vec = reinterpret_cast<const float*>(vec_gen);
+    float rsum = 0.f;              // Q: this half's sum of dS over its keys
     bool alive = true;
     for (int n = 0; n < nsteps; ++n) {
       const uint32_t st = n & 1, ph = (n >> 1) & 1;
@@ -278,15 +281,29 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         }
         pw[i / 2] = pack_bf16x2(p[0], p[1]);
         dw[i / 2] = pack_bf16x2(ds[0], ds[1]);
+        rsum += ds[0] + ds[1];
       }
       // dS (and P) over this half's own score columns, packed two per column
       tmem_st_32x32b_x16(tmem + lane_base + 128 + 64 * st + 32 * hf, dw);
-      if constexpr (KV)
-        tmem_st_32x32b_x16(tmem + lane_base + 64 * st + 32 * hf, pw);
+      tmem_st_32x32b_x16(tmem + lane_base + 64 * st + 32 * hf, pw);
       tmem_st_wait();
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(e_full + 8 * st);
+    }
+    float rrow = 0.f;
+    if constexpr (!KV) {
+      // Row sums of dS: zero for exact arithmetic, but delta comes from the
+      // forward's rounded context while P and dP are this kernel's own, so
+      // r = (sum_j P dP - delta) / sqrt(d) is not.  Every dS in the row
+      // carries that offset, and the component shared by all keys, which
+      // cancels in the exact dQ, would be amplified; subtracting r sum_j P k
+      // gives dQ = sum_j P (dP - sum_j P dP) k / sqrt(d) with this kernel's
+      // own P and dP.  The halves meet once (every path passes the barrier).
+      float* red = reinterpret_cast<float*>(vec_gen);
+      red[hf * 128 + r] = rsum;
+      pair_barrier(q);
+      rrow = red[r] + red[128 + r];
     }
     if (alive && warp_wait(o_full, 0, ctl, ROLE_EPILOGUE)) {
       ptx::tc_fence_after();
@@ -302,6 +319,15 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         float v[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(ov[i]);
+        if constexpr (!KV) {
+          uint32_t kv[32];
+          ptx::tmem_ld_32x32b_x32(
+              tmem + lane_base + TMEM_OUT1 + hf * (D / 2) + 32 * j, kv);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            v[i] = fmaf(-rrow, __uint_as_float(kv[i]), v[i]);
+        }
         store_bf16x32(out2 + 32 * j, v);
       }
       if constexpr (KV) {
@@ -345,7 +371,7 @@ size_t attn_bwd_smem() {
   constexpr int KB = D / 64;
   constexpr int NB = KV ? 4 : 5;
   const size_t need = 1024 + 2 * KB * KBLOCK_BYTES + NB * 2 * KB * ATOM_BYTES +
-                      (KV ? NB * 512 : 0) + (9 + 2 * NB) * 8 + 16;
+                      (KV ? NB * 512 : 1024) + (9 + 2 * NB) * 8 + 16;
   return need > 116 * 1024 ? need : 116 * 1024;
 }
 

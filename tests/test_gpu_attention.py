@@ -175,16 +175,21 @@ def _head_cols(w, j):
             slice(base + 2 * hs, base + 2 * hs + d))
 
 
-def test_attention_gpt3_13b_sampled_invariants_and_bitwise():
+@pytest.mark.parametrize("name,samples", [
+    ("attn_gpt3_13b", ((0, 0), (1, 17), (3, 39))),
+    ("attn_gpt2_medium", ((0, 0), (5, 9), (7, 15))),
+])
+def test_attention_full_size_sampled_invariants_and_bitwise(name, samples):
     """The GPT-3-13B-shaped layer (4 x 2048 tokens, h = 5120, 40 heads of
-    128, 8 shards, causal) at full size, in the launch configuration the
-    benchmark times.  Checked against the oracle from the original inputs:
+    128, 8 shards, causal) and the GPT-2-medium-shaped one (8 x 1024 tokens,
+    h = 1024, 16 heads of 64, 4 shards) at full size, in the launch
+    configuration the benchmark times.  Checked against the oracle from the original inputs:
     Ctx, the log-sum-exp and dQKV of sampled (sequence, head) pairs; Z on
     every sequence's first 128 rows (causal rows there see keys 0..127
     only); and over every sequence and head the exact identities
     sum_keys dK = 0 (each row of dS sums to zero) and sum_keys dV =
     sum_queries dO.  Two runs are bit-identical."""
-    w = W.ATTN_WORKLOADS["attn_gpt3_13b"]
+    w = W.ATTN_WORKLOADS[name]
     inp = W.make_attn_inputs(w, seed=0, with_bias=True)
     a, b = run_attn(w, inp, repeat=2)
     for k in a:
@@ -196,7 +201,7 @@ def test_attention_gpt3_13b_sampled_invariants_and_bitwise():
     ctx, dqkv = f64(a["Ctx"]), f64(a["dQKV"])
     lse2 = f64(a["lse2"])
     # sampled heads: forward core and its backward, from the inputs
-    for seq, j in ((0, 0), (1, 17), (3, 39)):
+    for seq, j in samples:
         rows = slice(seq * S, (seq + 1) * S)
         cq, ck, cv = _head_cols(w, j)
         x = X[rows]
