@@ -350,7 +350,62 @@ def run_ours(args, w, rank, world, local_rank):
         "kernels": krep,
     }
     m.close()
+    line["spec_peak"] = spec_peak(clocks, tflops / world)
+    line["vendor_context"] = vendor_context(w, d, args)
     return line, inp
+
+
+def spec_peak(clocks, tflops_per_gpu):
+    """Clock-based dense peak: SMs x the per-SM bf16 rate measured by the
+    library's tensor-core probe (one thread per SM issuing back-to-back
+    128 x 256 x 16 MMAs) x the median SM clock seen during the timed region."""
+    from tensor_transformer_mlp_tcgen05_gb300 import binding as Bn
+    rate, sms = Bn.mma_flops_per_cycle(256)
+    mhz = (clocks or {}).get("sm_mhz") or (clocks or {}).get("sm_max_mhz")
+    out = {"flops_per_sm_cycle": round(rate, 1), "sms": sms, "sm_mhz": mhz,
+           "what": "SMs x measured flops/SM/cycle x median SM clock"}
+    if mhz:
+        peak = rate * sms * mhz * 1e6 / 1e12
+        out.update(tflops=round(peak, 1), frac=round(tflops_per_gpu / peak, 4))
+    return out
+
+
+def vendor_context(w, d, args):
+    """torch bf16 matmul + GeLU (cuBLAS), unsharded, same shapes, autograd
+    forward (+ backward), as vendor-library context only."""
+    import torch
+    import torch.nn.functional as F
+    X = d["X"].detach().clone().requires_grad_(w.backward)
+    A = d["A"].detach().clone().requires_grad_(w.backward)
+    B = d["B"].detach().clone().requires_grad_(w.backward)
+
+    def step():
+        Xn = F.layer_norm(X, (w.hidden,), d["gamma"].to(X.dtype),
+                          d["beta"].to(X.dtype)) if w.layernorm else X
+        Z = F.gelu(Xn @ A) @ B
+        if w.backward:
+            X.grad = A.grad = B.grad = None
+            Z.backward(d["dZ"])
+        return Z
+
+    with torch.enable_grad():
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        n = max(3, min(args.steps, 20))
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
+            step()
+        e1.record()
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    flops = w.flops_fwd_bwd() if w.backward else w.flops_fwd()
+    return {"value": round(flops / (ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 4), "steps": n,
+            "what": "torch bf16 matmul + gelu (cuBLAS), unsharded, autograd "
+                    + ("fwd+bwd" if w.backward else "fwd")}
 
 
 def attn_kernel_flops(w):

@@ -190,6 +190,20 @@ long long tp_mlp_fp8_offset(const tp_mlp_handle* handle, int tokens,
 #define TPMLP_FP8_WS_Y        5   /* Y [T, f] bf16                        */
 #define TPMLP_FP8_WS_YQ       6   /* Y codes [T, f]                       */
 
+/* Tensor-core rate calibration (instrumentation, not part of the block):
+ * launches `ctas` CTAs (one per SM when ctas <= the SM count), each with one
+ * thread issuing `n_mma` (a multiple of 4, <= 2^24) back-to-back
+ * tcgen05.mma of shape M = 128, N = n (64, 128 or 256), K = 16, bf16
+ * operands from shared memory, fp32 accumulator in tensor memory, and writes
+ * the SM clock cycles from first issue to last completion of CTA i to
+ * cycles[i] (device memory, >= ctas entries).  status (device int, zeroed
+ * by the caller) becomes TPMLP_ERR_TIMEOUT if a completion wait gave up.
+ * 2 * 128 * n * 16 * n_mma / cycles is the per-SM dense bf16 rate in flops
+ * per cycle.  Asynchronous on `stream`. */
+int tp_mlp_probe_mma_cycles(int n, int ctas, int n_mma,
+                            unsigned long long* cycles, int* status,
+                            void* stream);
+
 /* Bias gradient without any device allocation: dbias[c] = sum over the
  * `tokens` rows of grad[r][c], for a row-major [tokens, cols] gradient
  * (e.g. dZ, giving db2).  The pages have no counterpart for this entry

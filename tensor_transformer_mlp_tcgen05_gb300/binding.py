@@ -40,6 +40,7 @@ EXPORTED = (
     "tp_mlp_set_dropout_seed",
     "tp_mlp_fp8_weights_bytes", "tp_mlp_fp8_pack_weights",
     "tp_mlp_fp8_workspace_bytes", "tp_mlp_forward_fp8", "tp_mlp_fp8_offset",
+    "tp_mlp_probe_mma_cycles",
     "tp_attn_create", "tp_attn_destroy", "tp_attn_workspace_bytes",
     "tp_attn_forward", "tp_attn_backward", "tp_attn_check",
     "tp_attn_launch_count", "tp_attn_set_timing", "tp_attn_timing_get",
@@ -149,6 +150,8 @@ def lib(path: str | None = None) -> ctypes.CDLL:
     L.tp_mlp_forward_fp8.restype = _i
     L.tp_mlp_fp8_offset.argtypes = [_vp, _i, _i]
     L.tp_mlp_fp8_offset.restype = ctypes.c_longlong
+    L.tp_mlp_probe_mma_cycles.argtypes = [_i, _i, _i, _vp, _vp, _vp]
+    L.tp_mlp_probe_mma_cycles.restype = _i
     L.tp_attn_create.argtypes = [ctypes.POINTER(tp_attn_config),
                                  ctypes.POINTER(_vp)]
     L.tp_attn_create.restype = _i
@@ -327,6 +330,28 @@ def tp_mlp_forward_fp8(handle, tokens, X, packed, bias1, bias2, ln_gamma,
 
 def tp_mlp_fp8_offset(handle, tokens: int, which: int) -> int:
     return int(lib().tp_mlp_fp8_offset(handle, tokens, which))
+
+
+def tp_mlp_probe_mma_cycles(n, ctas, n_mma, cycles, status, stream=None):
+    _check(lib().tp_mlp_probe_mma_cycles(n, ctas, n_mma, _ptr(cycles),
+                                         _ptr(status), _stream(stream)),
+           "tp_mlp_probe_mma_cycles")
+
+
+def mma_flops_per_cycle(n=256, n_mma=4096, device=None):
+    """Measured per-SM dense bf16 tensor rate (flops per SM cycle), one CTA
+    per SM, averaged over the SMs."""
+    import torch
+    dev = torch.device(device or "cuda")
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    cycles = torch.zeros(sms, dtype=torch.int64, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    tp_mlp_probe_mma_cycles(n, sms, n_mma, cycles, status)
+    torch.cuda.synchronize(dev)
+    if int(status.item()) != 0:
+        raise TPMLPError(int(status.item()), "mma probe: completion wait gave up")
+    mean = float(cycles.double().mean().item())
+    return 2.0 * 128 * n * 16 * n_mma / mean, sms
 
 
 # ------------------------------------------------------------- attention --

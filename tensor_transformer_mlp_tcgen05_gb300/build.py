@@ -24,7 +24,7 @@ LIB_PATH = os.path.join(PKG, "libtpmlp.so")
 
 SOURCES = ["gemm_tc.cu", "gemm_tc2.cu", "rowops.cu", "simt.cu",
            "tp_mlp_host.cu", "noalloc.cu", "attn_fwd.cu", "attn_bwd.cu",
-           "attn_host.cu", "fp8.cu"]
+           "attn_host.cu", "fp8.cu", "probe.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
           "--expt-relaxed-constexpr", "-I" + INCLUDE, "-I" + CSRC]

@@ -216,3 +216,11 @@ def test_attn_host_validation_before_device(lib):
                                   None) == B.TPMLP_ERR_ARG
     finally:
         B.tp_attn_destroy(h)
+
+
+def test_mma_probe_rejects_bad_arguments(lib):
+    ok = ctypes.c_void_p(16)
+    assert lib.tp_mlp_probe_mma_cycles(128, 4, 100, ok, None, None) == B.TPMLP_ERR_ARG
+    assert lib.tp_mlp_probe_mma_cycles(128, 4, 102, ok, ok, None) == B.TPMLP_ERR_ARG
+    assert lib.tp_mlp_probe_mma_cycles(128, 0, 100, ok, ok, None) == B.TPMLP_ERR_ARG
+    assert lib.tp_mlp_probe_mma_cycles(96, 4, 100, ok, ok, None) == B.TPMLP_ERR_SHAPE
