@@ -51,20 +51,51 @@ METRIC_ATTN = ("TP-attention fwd+bwd TFLOP/s and tokens/s on 1 GB300, "
                "% of dense bf16 peak")
 DEFAULT_WORKLOAD = "gpt3_13b"
 
-# DRAM traffic per launch of the dominant kernel from an ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by kernel name, with
-# the SHA-256 of the kernel source the capture was taken on.  Reported as
-# null once the source has changed.
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum)
+# from full-size ncu captures, keyed by workload then kernel, with the hash of
+# the kernel sources the capture was taken on ("gemm": the pair GEMM,
+# "attn": the attention core).  Reported as null once the source has changed
+# or for a workload without a capture.  See profiles/gemm_tc2_dram_gpt3_13b.md
+# and profiles/attn_fp8_dram_gpt3_13b.md.
+_G, _A = "64c5396a4298cc23", "8d373b4a1f4cdbbc"
 NCU_TRAFFIC = {
-    # GPT-3-13B-shaped step (T=8192, h=5120, f=20480, t=8), CTA-pair kernel
-    # with TMA-store epilogue; see profiles/gemm_tc2_dram_gpt3_13b.md.
-    "gemm1_gelu": {"bytes": 1770.2e6, "src": "64c5396a4298cc23"},
-    "gemm2_shardsum": {"bytes": 2242.8e6, "src": "64c5396a4298cc23"},
-    "gemm_dh_gelu_bwd": {"bytes": 1797.5e6, "src": "64c5396a4298cc23"},
-    "gemm_wgrad_dB": {"bytes": 2501.1e6, "src": "64c5396a4298cc23"},
-    "gemm_wgrad_dA": {"bytes": 2315.4e6, "src": "64c5396a4298cc23"},
-    "gemm_dx_shardsum": {"bytes": 2257.8e6, "src": "64c5396a4298cc23"},
+    # GPT-3-13B-shaped MLP step (T=8192, h=5120, f=20480, t=8)
+    "gpt3_13b": {
+        "gemm1_gelu": (1770.2e6, "gemm", _G),
+        "gemm2_shardsum": (2242.8e6, "gemm", _G),
+        "gemm_dh_gelu_bwd": (1797.5e6, "gemm", _G),
+        "gemm_wgrad_dB": (2501.1e6, "gemm", _G),
+        "gemm_wgrad_dA": (2315.4e6, "gemm", _G),
+        "gemm_dx_shardsum": (2257.8e6, "gemm", _G),
+    },
+    # the same layer's FP8 forward
+    "gpt3_13b_fp8": {
+        "gemm1_gelu_fp8": (558.9e6, "gemm", _G),
+        "gemm2_shardsum_fp8": (1152.2e6, "gemm", _G),
+    },
+    # GPT-3-13B-shaped attention block (4 x 2048 tokens, 40 heads of 128)
+    "attn_gpt3_13b": {
+        "gemm_qkv": (951.5e6, "gemm", _G),
+        "gemm_out_shardsum": (375.7e6, "gemm", _G),
+        "gemm_wgrad_dWo": (622.0e6, "gemm", _G),
+        "gemm_dctx": (378.8e6, "gemm", _G),
+        "gemm_wgrad_dWqkv": (1762.5e6, "gemm", _G),
+        "gemm_dx_shardsum": (1698.7e6, "gemm", _G),
+        "attn_fwd": (317.6e6, "attn", _A),
+        "attn_bwd_dkdv": (473.1e6, "attn", _A),
+        "attn_bwd_dq": (404.1e6, "attn", _A),
+    },
 }
+_SRC_FILES = {"gemm": ("gemm_tc2.cu", "gemm_common.cuh", "ptx.cuh"),
+              "attn": ("attn_fwd.cu", "attn_bwd.cu", "attn_common.cuh")}
+
+
+def traffic_of(workload, kernel):
+    entry = NCU_TRAFFIC.get(workload, {}).get(kernel)
+    if entry is None:
+        return None
+    nbytes, group, sha = entry
+    return nbytes if _src_sha(_SRC_FILES[group]) == sha else None
 
 
 def _peaks():
@@ -77,10 +108,10 @@ def _peaks():
         return 1900.0, 1700.0, 6800.0, "fallback"
 
 
-def _src_sha():
-    """Hash of the GEMM kernel sources the traffic figures depend on."""
+def _src_sha(files=_SRC_FILES["gemm"]):
+    """Hash of the kernel sources a traffic figure depends on."""
     h = hashlib.sha256()
-    for name in ("gemm_tc2.cu", "gemm_common.cuh", "ptx.cuh"):
+    for name in files:
         path = os.path.join(ROOT, "tensor_transformer_mlp_tcgen05_gb300",
                             "csrc", name)
         with open(path, "rb") as fh:
@@ -315,8 +346,8 @@ def run_ours(args, w, rank, world, local_rank):
     }
     if top["name"] in gemm_flops:
         ach = gemm_flops[top["name"]] / (top["avg_ms"] * 1e-3) / 1e12
-        tr = NCU_TRAFFIC.get(top["name"])
-        traffic = tr["bytes"] if tr and tr.get("src") == _src_sha() else None
+        traffic = traffic_of(w.name, top["name"]) \
+            if not (args.tokens or args.shards or args.residual) else None
         roof = {"kernel": top["name"], "bound": "tensor",
                 "achieved": round(ach, 1), "peak": peak_s, "unit": "TFLOP/s",
                 "frac": round(ach / peak_s, 4),
@@ -529,8 +560,8 @@ def run_ours_attn(args, w, rank, world, local_rank):
     roof = None
     if top["name"] in kf:
         ach = kf[top["name"]] / (top["avg_ms"] * 1e-3) / 1e12
-        tr = NCU_TRAFFIC.get(top["name"])
-        traffic = tr["bytes"] if tr and tr.get("src") == _src_sha() else None
+        traffic = traffic_of(w.name, top["name"]) \
+            if not (args.tokens or args.shards or args.residual) else None
         roof = {"kernel": top["name"], "bound": "tensor",
                 "achieved": round(ach, 1), "peak": peak_s, "unit": "TFLOP/s",
                 "frac": round(ach / peak_s, 4),
@@ -732,7 +763,8 @@ def run_ours_fp8(args, w, rank, world, local_rank):
                 "unit": "TFLOP/s", "frac": round(ach / fp8_burst, 4),
                 "peak_kind": f"fp8 = 2 x measured bf16 burst ({peak_src}; "
                              "nominal fp8:bf16 ratio 4.5:2.25)",
-                "traffic": None}
+                "traffic": traffic_of(w.name + "_fp8", top["name"])
+                if not (args.tokens or args.shards or args.residual) else None}
     line = {
         "metric": METRIC_FP8, "value": round(tflops, 2), "unit": "TFLOP/s",
         "tokens_per_s": round(world * T / (ms_max * 1e-3), 1),
