@@ -153,9 +153,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     }
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) {
-      // -------------------------------------------------- MMA issuer --
-      bool alive = wait_bounded(a_full, 0, ctl, ROLE_MMA);
+    {
+      // ------------------------ MMA issuer (whole warp, elected lane) --
+      bool alive = warp_wait(a_full, 0, ctl, ROLE_MMA);
       const uint64_t dA1 = ptx::sdesc_sw128(sA1, 16, 1024);
       const uint64_t dA2 = ptx::sdesc_sw128(sA2, 16, 1024);
       const uint64_t dBk = ptx::sdesc_sw128(sB, 16, 1024);          // K-major
@@ -163,10 +163,10 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       auto issue_s = [&](int n) -> bool {
         const uint32_t st = n & 1, ph = (n >> 1) & 1;
         const uint32_t bs = n % NB, bph = (n / NB) & 1;
-        if (!wait_bounded(b_full + 8 * bs, bph, ctl, ROLE_MMA)) return false;
+        if (!warp_wait(b_full + 8 * bs, bph, ctl, ROLE_MMA)) return false;
         // buffer st still holds step n - 2's P / dS until its gradient MMAs
         // are done
-        if (n >= 2 && !wait_bounded(e_empty + 8 * st, ph ^ 1, ctl, ROLE_MMA))
+        if (n >= 2 && !warp_wait(e_empty + 8 * st, ph ^ 1, ctl, ROLE_MMA))
           return false;
         ptx::tc_fence_after();
         const uint64_t b1 = desc_add(dBk, bs * 2 * B_TILE);
@@ -175,23 +175,23 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t ao = (k / 4) * KBLOCK_BYTES + (k % 4) * 32;
           const uint32_t bo = (k / 4) * ATOM_BYTES + (k % 4) * 32;
-          ptx::mma_bf16(tmem + 64 * st, desc_add(dA1, ao), desc_add(b1, bo),
-                        IDESC_S, k > 0 ? 1u : 0u);
+          mma_ss_el(tmem + 64 * st, desc_add(dA1, ao), desc_add(b1, bo),
+                    IDESC_S, k > 0 ? 1u : 0u);
         }
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t ao = (k / 4) * KBLOCK_BYTES + (k % 4) * 32;
           const uint32_t bo = (k / 4) * ATOM_BYTES + (k % 4) * 32;
-          ptx::mma_bf16(tmem + 128 + 64 * st, desc_add(dA2, ao),
-                        desc_add(b2, bo), IDESC_S, k > 0 ? 1u : 0u);
+          mma_ss_el(tmem + 128 + 64 * st, desc_add(dA2, ao),
+                    desc_add(b2, bo), IDESC_S, k > 0 ? 1u : 0u);
         }
-        ptx::mma_commit(s_full + 8 * st);
+        commit_el(s_full + 8 * st);
         return true;
       };
       auto issue_o = [&](int n) -> bool {
         const uint32_t st = n & 1, ph = (n >> 1) & 1;
         const uint32_t bs = n % NB;
-        if (!wait_bounded(e_full + 8 * st, ph, ctl, ROLE_MMA)) return false;
+        if (!warp_wait(e_full + 8 * st, ph, ctl, ROLE_MMA)) return false;
         ptx::tc_fence_after();
         const uint64_t b1 = desc_add(dBm, bs * 2 * B_TILE);
         const uint64_t b2 = desc_add(b1, B_TILE);
@@ -200,18 +200,18 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         const uint32_t e2 = tmem + 128 + 64 * st, e1 = tmem + 64 * st;
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          mma_bf16_ts(tmem + TMEM_OUT2, e2 + (k / 2) * 32 + (k % 2) * 8,
-                      desc_add(b1, 2048 * k), IDESC_O,
-                      (n > 0 || k > 0) ? 1u : 0u);
+          mma_ts_el(tmem + TMEM_OUT2, e2 + (k / 2) * 32 + (k % 2) * 8,
+                    desc_add(b1, 2048 * k), IDESC_O,
+                    (n > 0 || k > 0) ? 1u : 0u);
         // KV: dV += P^T dO.  Q: sum_j P_ij k_j += P K (same B as dQ), for
         // the row-sum correction of dQ below.
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          mma_bf16_ts(tmem + TMEM_OUT1, e1 + (k / 2) * 32 + (k % 2) * 8,
-                      desc_add(KV ? b2 : b1, 2048 * k), IDESC_O,
-                      (n > 0 || k > 0) ? 1u : 0u);
-        ptx::mma_commit(b_empty + 8 * bs);
-        ptx::mma_commit(e_empty + 8 * st);
+          mma_ts_el(tmem + TMEM_OUT1, e1 + (k / 2) * 32 + (k % 2) * 8,
+                    desc_add(KV ? b2 : b1, 2048 * k), IDESC_O,
+                    (n > 0 || k > 0) ? 1u : 0u);
+        commit_el(b_empty + 8 * bs);
+        commit_el(e_empty + 8 * st);
         return true;
       };
       if (alive) alive = issue_s(0);
@@ -219,9 +219,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         if (n + 1 < nsteps && !(alive = issue_s(n + 1))) break;
         alive = issue_o(n);
       }
-      if (alive) ptx::mma_commit(o_full);
+      if (alive) commit_el(o_full);
       if (*reinterpret_cast<volatile int*>(abort_flag)) {
-        ptx::mma_commit(done_bar);
+        commit_el(done_bar);
         wait_teardown(done_bar, 0);
       }
     }

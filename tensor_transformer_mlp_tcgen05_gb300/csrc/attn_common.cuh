@@ -70,6 +70,34 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem,
       : "memory");
 }
 
+// One lane of a fully active warp (elect.sync).
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\t"
+      "selp.b32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
+// The MMA role runs on all 32 lanes of warp 1, so that its descriptors and
+// addresses stay warp-uniform, and one elected lane issues each tcgen05
+// instruction.  (A loop run by lane 0 alone lost issue slots to the softmax
+// warps sharing its SM sub-partition: its MMAs then ran at 40-50 % rate.)
+__device__ __forceinline__ void mma_ss_el(uint32_t d_tmem, uint64_t adesc,
+                                          uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  if (elect_one()) ptx::mma_bf16(d_tmem, adesc, bdesc, idesc, accumulate);
+}
+__device__ __forceinline__ void mma_ts_el(uint32_t d_tmem, uint32_t a_tmem,
+                                          uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  if (elect_one()) mma_bf16_ts(d_tmem, a_tmem, bdesc, idesc, accumulate);
+}
+__device__ __forceinline__ void commit_el(uint32_t bar) {
+  if (elect_one()) ptx::mma_commit(bar);
+}
+
 // 32 TMEM lanes x 16 consecutive 32-bit columns from registers.
 __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr,
                                                    const uint32_t (&r)[16]) {

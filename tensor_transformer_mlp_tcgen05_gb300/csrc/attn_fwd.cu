@@ -21,8 +21,9 @@
 // lse2 = m + log2(l), so that P = exp2(S log2(e)/sqrt(d) - lse2).
 //
 // Warp roles (384 threads): warp 0 TMA producer, warp 1 TMEM allocator and
-// MMA issuer (one lane), warps 4-11 softmax (thread = query row = TMEM lane,
-// two warps per row quarter, one per half of the columns).
+// MMA issuer (the whole warp; one elected lane issues), warps 4-11 softmax
+// (thread = query row = TMEM lane, two warps per row quarter, one per half
+// of the columns).
 // All waits are bounded as in the GEMM kernels.
 #include "attn_common.cuh"
 
@@ -135,9 +136,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     }
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) {
-      // -------------------------------------------------- MMA issuer --
-      bool alive = wait_bounded(q_full, 0, ctl, ROLE_MMA);
+    {
+      // ------------------------ MMA issuer (whole warp, elected lane) --
+      bool alive = warp_wait(q_full, 0, ctl, ROLE_MMA);
       uint32_t kc = 0, sc = 0, vc = 0;
       const uint64_t dQ = ptx::sdesc_sw128(sQ, 16, 1024);
       const uint64_t dK = ptx::sdesc_sw128(sK, 16, 1024);
@@ -145,18 +146,18 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       auto issue_s = [&]() -> bool {
         const uint32_t ks = kc & 1, kph = (kc >> 1) & 1;
         const uint32_t sb = sc & 1, sph = (sc >> 1) & 1;
-        if (!wait_bounded(k_full + 8 * ks, kph, ctl, ROLE_MMA)) return false;
-        if (!wait_bounded(s_empty + 8 * sb, sph ^ 1, ctl, ROLE_MMA)) return false;
+        if (!warp_wait(k_full + 8 * ks, kph, ctl, ROLE_MMA)) return false;
+        if (!warp_wait(s_empty + 8 * sb, sph ^ 1, ctl, ROLE_MMA)) return false;
         ptx::tc_fence_after();
         const uint64_t dKs = desc_add(dK, ks * QK_TILE);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k / 4) * KBLOCK_BYTES + (k % 4) * 32;
-          ptx::mma_bf16(tmem + sb * 128, desc_add(dQ, off), desc_add(dKs, off),
-                        IDESC_S, k > 0 ? 1u : 0u);
+          mma_ss_el(tmem + sb * 128, desc_add(dQ, off), desc_add(dKs, off),
+                    IDESC_S, k > 0 ? 1u : 0u);
         }
-        ptx::mma_commit(k_empty + 8 * ks);
-        ptx::mma_commit(s_full + 8 * sb);
+        commit_el(k_empty + 8 * ks);
+        commit_el(s_full + 8 * sb);
         ++kc;
         ++sc;
         return true;
@@ -165,8 +166,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       for (int kb = 0; alive && kb < nk; ++kb) {
         if (kb + 1 < nk && !(alive = issue_s())) break;
         const uint32_t vs = vc & 1, vph = (vc >> 1) & 1;
-        if (!wait_bounded(p_full, kb & 1, ctl, ROLE_MMA) ||
-            !wait_bounded(v_full + 8 * vs, vph, ctl, ROLE_MMA)) {
+        if (!warp_wait(p_full, kb & 1, ctl, ROLE_MMA) ||
+            !warp_wait(v_full + 8 * vs, vph, ctl, ROLE_MMA)) {
           alive = false;
           break;
         }
@@ -174,16 +175,16 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         const uint64_t dVs = desc_add(dV, vs * V_TILE);
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          mma_bf16_ts(tmem + TMEM_O, tmem + TMEM_P + 8 * k,
-                      desc_add(dVs, (k / 4) * KB * ATOM_BYTES + (k % 4) * 2048),
-                      IDESC_O, (kb > 0 || k > 0) ? 1u : 0u);
-        ptx::mma_commit(v_empty + 8 * vs);
-        ptx::mma_commit(p_empty);
+          mma_ts_el(tmem + TMEM_O, tmem + TMEM_P + 8 * k,
+                    desc_add(dVs, (k / 4) * KB * ATOM_BYTES + (k % 4) * 2048),
+                    IDESC_O, (kb > 0 || k > 0) ? 1u : 0u);
+        commit_el(v_empty + 8 * vs);
+        commit_el(p_empty);
         ++vc;
       }
-      if (alive) ptx::mma_commit(o_full);
+      if (alive) commit_el(o_full);
       if (*reinterpret_cast<volatile int*>(abort_flag)) {
-        ptx::mma_commit(done_bar);
+        commit_el(done_bar);
         wait_teardown(done_bar, 0);
       }
     }
