@@ -5,25 +5,27 @@
 // head, 128-query block) and never communicates.  Q, K and V are read in
 // place from the fused projection output QKV [T, 3h] (columns grouped by
 // shard: [Q_i | K_i | V_i], head j of shard i at offset (j mod H/t) d inside
-// each group) through TMA tensor maps; scores and the output accumulator
-// live in TMEM; the probabilities are staged in shared memory as the bf16 A
-// operand of the second MMA.
+// each group) through TMA tensor maps; scores, probabilities and the output
+// accumulator live in TMEM.
 //
 // Forward, one pass over the key blocks the query block may see (all of
 // them, or blocks 0..qb when causal): S = Q K^T (tcgen05, M = N = 128,
-// K = d) into one of two TMEM buffers -> P = exp2(S log2e / sqrt d - m_ref)
-// with a lazily raised reference max -> bf16 P stored by the softmax
-// threads into TMEM (one row per lane) -> O += P V with A read from TMEM
-// (only V comes from shared memory, which keeps the MMA's operand reads
-// under the SM's shared-memory bandwidth); O / l at the end.
+// K = d) into TMEM -> P = exp2(S log2e / sqrt d - m_ref) with a lazily
+// raised reference max -> bf16 P stored by the softmax threads over the
+// scores (one row per lane) -> O += P V with A read from TMEM (only V comes
+// from shared memory, which keeps the MMA's operand reads under the SM's
+// shared-memory bandwidth); O / l at the end.
 // Outputs: the context rows (bf16) and, for the backward, every (head,
 // token) row's log-sum-exp in base 2 of the scores scaled by log2(e)/sqrt(d),
 // lse2 = m + log2(l), so that P = exp2(S log2(e)/sqrt(d) - lse2).
 //
-// Warp roles (384 threads): warp 0 TMA producer, warp 1 TMEM allocator and
-// MMA issuer (the whole warp; one elected lane issues), warps 4-11 softmax
+// Warp roles (320 threads): warp 0 TMA producer, warp 1 TMEM allocator and
+// MMA issuer (the whole warp; one elected lane issues), warps 2-9 softmax
 // (thread = query row = TMEM lane, two warps per row quarter, one per half
-// of the columns).
+// of the columns).  Each CTA walks its key blocks strictly in turn (S, then
+// the softmax, then P V, then the next S over the same TMEM columns) and
+// holds 256 TMEM columns and ~100 KB of shared memory, so two CTAs share an
+// SM and the tensor core works for one while the other is in its softmax.
 // All waits are bounded as in the GEMM kernels.
 #include "attn_common.cuh"
 
@@ -33,8 +35,23 @@ namespace {
 using namespace gemm;
 using namespace attn;
 
+constexpr int FWD_THREADS = 320;
+constexpr int FWD_SOFTMAX_WARP0 = 2;
+constexpr uint32_t FWD_TMEM_COLS = 256;
+
+__device__ __forceinline__ void fwd_barrier() {
+  asm volatile("bar.sync 1, %0;" ::"n"(FWD_THREADS) : "memory");
+}
+
+// TMEM column of the packed P values for keys 16k .. 16k + 15: each column
+// half of the softmax writes its 64 keys' P over the first 32 of its own 64
+// score columns.
+__device__ __forceinline__ constexpr uint32_t p_col(int k) {
+  return 64u * static_cast<uint32_t>(k / 4) + 8u * static_cast<uint32_t>(k % 4);
+}
+
 template <int D>
-__global__ void __launch_bounds__(ATT_THREADS, 1)
+__global__ void __launch_bounds__(FWD_THREADS, 2)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQK,
                     const __grid_constant__ CUtensorMap tmV,
                     const AttnArgs a) {
@@ -43,26 +60,24 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   constexpr uint32_t V_TILE = 2 * KB * ATOM_BYTES;     // 128 keys x D
   constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, false, false);
   constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, false, true);
-  constexpr uint32_t TMEM_O = 256;
-  constexpr uint32_t TMEM_P = 384;   // P, 128 keys as 64 packed bf16 pairs
+  constexpr uint32_t TMEM_O = 128;   // S in columns 0-127, P over S
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sQ = ptx::smem_u32(smem);
   const uint32_t sK = sQ + QK_TILE;
-  const uint32_t sV = sK + 2 * QK_TILE;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + QK_TILE * 3 + V_TILE * 2);
+  const uint32_t sV = sK + QK_TILE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 2 * QK_TILE + V_TILE);
   const uint32_t b0 = ptx::smem_u32(bars);
-  const uint32_t q_full = b0, k_full = b0 + 8, k_empty = b0 + 24,
-                 v_full = b0 + 40, v_empty = b0 + 56, s_full = b0 + 72,
-                 s_empty = b0 + 88, p_full = b0 + 104, p_empty = b0 + 112,
-                 o_full = b0 + 120, done_bar = b0 + 128;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 17);
+  const uint32_t q_full = b0, k_full = b0 + 8, k_empty = b0 + 16,
+                 v_full = b0 + 24, v_empty = b0 + 32, s_full = b0 + 40,
+                 p_full = b0 + 48, pv_done = b0 + 56, done_bar = b0 + 64;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 9);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   // Row max (per block, two parities) and row sum exchange between the two
   // column halves: [3][2][128].
-  float* red = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + 256);
+  float* red = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + 128);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nq = a.nq;
@@ -75,23 +90,19 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(q_full, 1);
-    for (int i = 0; i < 2; ++i) {
-      ptx::mbar_init(k_full + 8 * i, 1);
-      ptx::mbar_init(k_empty + 8 * i, 1);
-      ptx::mbar_init(v_full + 8 * i, 1);
-      ptx::mbar_init(v_empty + 8 * i, 1);
-      ptx::mbar_init(s_full + 8 * i, 1);
-      ptx::mbar_init(s_empty + 8 * i, SOFTMAX_WARPS);
-    }
+    ptx::mbar_init(k_full, 1);
+    ptx::mbar_init(k_empty, 1);
+    ptx::mbar_init(v_full, 1);
+    ptx::mbar_init(v_empty, 1);
+    ptx::mbar_init(s_full, 1);
     ptx::mbar_init(p_full, SOFTMAX_WARPS);
-    ptx::mbar_init(p_empty, 1);
-    ptx::mbar_init(o_full, 1);
+    ptx::mbar_init(pv_done, 1);
     ptx::mbar_init(done_bar, 1);
     *abort_flag = 0;
     ptx::fence_barrier_init();
   }
   if (warp == 1) {
-    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), 512);
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), FWD_TMEM_COLS);
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
@@ -103,35 +114,29 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ---------------------------------------------------- producer --
-      bool alive = true;
+      // One stage each for K and V: K(kb) may overwrite K(kb - 1) once
+      // S(kb - 1) is done, V(kb) once P V(kb - 1) is done.
       ptx::mbar_arrive_expect_tx(q_full, QK_TILE);
 #pragma unroll
       for (int kk = 0; kk < KB; ++kk)
         ptx::tma_load_2d(sQ + kk * KBLOCK_BYTES, &tmQK, q_full, hc.q + 64 * kk, row0);
-      for (int kb = 0; alive && kb < nk; ++kb) {
+      for (int kb = 0; kb < nk; ++kb) {
         const int key0 = seq * a.seq_len + kb * 128;
-        const uint32_t st = kb & 1, ph = (kb >> 1) & 1;
-        if (!wait_bounded(k_empty + 8 * st, ph ^ 1, ctl, ROLE_PRODUCER)) {
-          alive = false;
-          break;
-        }
-        ptx::mbar_arrive_expect_tx(k_full + 8 * st, QK_TILE);
+        const uint32_t prev = static_cast<uint32_t>(kb - 1) & 1u;
+        if (kb > 0 && !wait_bounded(k_empty, prev, ctl, ROLE_PRODUCER)) break;
+        ptx::mbar_arrive_expect_tx(k_full, QK_TILE);
 #pragma unroll
         for (int kk = 0; kk < KB; ++kk)
-          ptx::tma_load_2d(sK + st * QK_TILE + kk * KBLOCK_BYTES, &tmQK,
-                           k_full + 8 * st, hc.k + 64 * kk, key0);
-        if (!wait_bounded(v_empty + 8 * st, ph ^ 1, ctl, ROLE_PRODUCER)) {
-          alive = false;
-          break;
-        }
-        ptx::mbar_arrive_expect_tx(v_full + 8 * st, V_TILE);
+          ptx::tma_load_2d(sK + kk * KBLOCK_BYTES, &tmQK, k_full, hc.k + 64 * kk,
+                           key0);
+        if (kb > 0 && !wait_bounded(v_empty, prev, ctl, ROLE_PRODUCER)) break;
+        ptx::mbar_arrive_expect_tx(v_full, V_TILE);
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2)
 #pragma unroll
           for (int at = 0; at < KB; ++at)
-            ptx::tma_load_2d(sV + st * V_TILE + (h2 * KB + at) * ATOM_BYTES,
-                             &tmV, v_full + 8 * st, hc.v + 64 * at,
-                             key0 + 64 * h2);
+            ptx::tma_load_2d(sV + (h2 * KB + at) * ATOM_BYTES, &tmV, v_full,
+                             hc.v + 64 * at, key0 + 64 * h2);
       }
     }
     __syncwarp();
@@ -139,108 +144,100 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     {
       // ------------------------ MMA issuer (whole warp, elected lane) --
       bool alive = warp_wait(q_full, 0, ctl, ROLE_MMA);
-      uint32_t kc = 0, sc = 0, vc = 0;
       const uint64_t dQ = ptx::sdesc_sw128(sQ, 16, 1024);
       const uint64_t dK = ptx::sdesc_sw128(sK, 16, 1024);
       const uint64_t dV = ptx::sdesc_sw128(sV, ATOM_BYTES, 1024);
-      auto issue_s = [&]() -> bool {
-        const uint32_t ks = kc & 1, kph = (kc >> 1) & 1;
-        const uint32_t sb = sc & 1, sph = (sc >> 1) & 1;
-        if (!warp_wait(k_full + 8 * ks, kph, ctl, ROLE_MMA)) return false;
-        if (!warp_wait(s_empty + 8 * sb, sph ^ 1, ctl, ROLE_MMA)) return false;
-        ptx::tc_fence_after();
-        const uint64_t dKs = desc_add(dK, ks * QK_TILE);
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k / 4) * KBLOCK_BYTES + (k % 4) * 32;
-          mma_ss_el(tmem + sb * 128, desc_add(dQ, off), desc_add(dKs, off),
-                    IDESC_S, k > 0 ? 1u : 0u);
-        }
-        commit_el(k_empty + 8 * ks);
-        commit_el(s_full + 8 * sb);
-        ++kc;
-        ++sc;
-        return true;
-      };
-      if (alive) alive = issue_s();
       for (int kb = 0; alive && kb < nk; ++kb) {
-        if (kb + 1 < nk && !(alive = issue_s())) break;
-        const uint32_t vs = vc & 1, vph = (vc >> 1) & 1;
-        if (!warp_wait(p_full, kb & 1, ctl, ROLE_MMA) ||
-            !warp_wait(v_full + 8 * vs, vph, ctl, ROLE_MMA)) {
+        const uint32_t ph = static_cast<uint32_t>(kb) & 1u;
+        // S = Q K^T into the score columns, once P V(kb - 1) has read the
+        // previous block's P from them
+        if (!warp_wait(k_full, ph, ctl, ROLE_MMA) ||
+            (kb > 0 && !warp_wait(pv_done, ph ^ 1u, ctl, ROLE_MMA))) {
           alive = false;
           break;
         }
         ptx::tc_fence_after();
-        const uint64_t dVs = desc_add(dV, vs * V_TILE);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k / 4) * KBLOCK_BYTES + (k % 4) * 32;
+          mma_ss_el(tmem, desc_add(dQ, off), desc_add(dK, off), IDESC_S,
+                    k > 0 ? 1u : 0u);
+        }
+        commit_el(k_empty);
+        commit_el(s_full);
+        // O += P V once the softmax has written P over the scores
+        if (!warp_wait(p_full, ph, ctl, ROLE_MMA) ||
+            !warp_wait(v_full, ph, ctl, ROLE_MMA)) {
+          alive = false;
+          break;
+        }
+        ptx::tc_fence_after();
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          mma_ts_el(tmem + TMEM_O, tmem + TMEM_P + 8 * k,
-                    desc_add(dVs, (k / 4) * KB * ATOM_BYTES + (k % 4) * 2048),
+          mma_ts_el(tmem + TMEM_O, tmem + p_col(k),
+                    desc_add(dV, (k / 4) * KB * ATOM_BYTES + (k % 4) * 2048),
                     IDESC_O, (kb > 0 || k > 0) ? 1u : 0u);
-        commit_el(v_empty + 8 * vs);
-        commit_el(p_empty);
-        ++vc;
+        commit_el(v_empty);
+        commit_el(pv_done);
       }
-      if (alive) commit_el(o_full);
       if (*reinterpret_cast<volatile int*>(abort_flag)) {
         commit_el(done_bar);
         wait_teardown(done_bar, 0);
       }
     }
     __syncwarp();
-  } else if (warp >= SOFTMAX_WARP0) {
+  } else {
     // ------------------------------------------------------ softmax --
-    // One pass with a lazily updated reference max (log2 units of the
-    // scaled scores).  Two warps share each row quarter, one per column
-    // half; per block they exchange their halves' maxima through shared
-    // memory.  P = exp2(x - m_ref) is staged for P V; only when the block
-    // max exceeds m_ref by more than RESCALE_LOG2 does m_ref move up, with
-    // O (each warp its half of the D columns, after the previous P V has
-    // finished) and the partial row sums scaled by exp2(m_old - m_new).
+    // One pass over the key blocks with a lazily updated reference max (log2
+    // units of the scaled scores).  Two warps share each row quarter, one
+    // per column half; per block they exchange their halves' maxima through
+    // shared memory.  P = exp2(x - m_ref) is written as bf16 over the
+    // half's own score columns, 32 columns at a time (the scores are read
+    // twice, for the max and for P, to keep register use low enough for two
+    // CTAs per SM).  Only when the block max exceeds m_ref by more than
+    // RESCALE_LOG2 does m_ref move up, with O (each warp its half of the D
+    // columns) and the partial row sums scaled by exp2(m_old - m_new); the
+    // previous P V is complete by then, since S(kb) was issued after it.
     // The decision depends only on the scores, so it is deterministic, and
     // P stays below 2^RESCALE_LOG2.  Output O / (l0 + l1); saved lse2 =
-    // m_ref + log2 l.  Every softmax warp passes the same barriers on
-    // every path.
+    // m_ref + log2 l.  Every softmax warp passes the same barriers on every
+    // path.
     constexpr float RESCALE_LOG2 = 8.f;
     const int q = warp & 3;
-    const int hf = (warp - SOFTMAX_WARP0) >> 2;
+    const int hf = (warp - FWD_SOFTMAX_WARP0) >> 2;
     const int r = q * 32 + lane;          // query row inside the block
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    const uint32_t scol = tmem + lane_base + 64 * hf;
     const float sl2 = a.scale_log2;
     float m_ref = -INFINITY, l = 0.f;
     bool alive = true;
     for (int kb = 0; kb < nk; ++kb) {
-      const uint32_t sb = kb & 1, sph = (kb >> 1) & 1;
-      bool ok = alive && warp_wait(s_full + 8 * sb, sph, ctl, ROLE_EPILOGUE);
-      const uint32_t col = tmem + lane_base + sb * 128 + 64 * hf;
+      bool ok = alive && warp_wait(s_full, static_cast<uint32_t>(kb) & 1u, ctl,
+                                   ROLE_EPILOGUE);
       // only the diagonal block of a causal row masks anything
       const bool diag = a.causal && kb == qb;
       const int lim = diag ? r - 64 * hf : 63;
-      uint32_t sv[64];
       float mb = -INFINITY;
       if (ok) {
         ptx::tc_fence_after();
-        uint32_t (&s0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[0]);
-        uint32_t (&s1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[32]);
-        ptx::tmem_ld_32x32b_x32(col, s0);
-        ptx::tmem_ld_32x32b_x32(col + 32, s1);
-        ptx::tmem_ld_wait();
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(s_empty + 8 * sb);
-        if (diag) {
 #pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (c <= lim) mb = fmaxf(mb, __uint_as_float(sv[c]));
-        } else {
-          float m0 = __uint_as_float(sv[0]), m1 = __uint_as_float(sv[1]);
+        for (int c = 0; c < 2; ++c) {
+          uint32_t sv[32];
+          ptx::tmem_ld_32x32b_x32(scol + 32 * c, sv);
+          ptx::tmem_ld_wait();
+          if (diag) {
 #pragma unroll
-          for (int c = 2; c < 64; c += 2) {
-            m0 = fmaxf(m0, __uint_as_float(sv[c]));
-            m1 = fmaxf(m1, __uint_as_float(sv[c + 1]));
+            for (int j = 0; j < 32; ++j)
+              if (32 * c + j <= lim) mb = fmaxf(mb, __uint_as_float(sv[j]));
+          } else {
+            float m0 = __uint_as_float(sv[0]), m1 = __uint_as_float(sv[1]);
+#pragma unroll
+            for (int j = 2; j < 32; j += 2) {
+              m0 = fmaxf(m0, __uint_as_float(sv[j]));
+              m1 = fmaxf(m1, __uint_as_float(sv[j + 1]));
+            }
+            mb = fmaxf(mb, fmaxf(m0, m1));
           }
-          mb = fmaxf(m0, m1);
         }
       }
       // exchange the halves' maxima (double-buffered by block parity)
@@ -258,38 +255,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         alpha = exp2f(m_ref - mb);       // 0 on the first block
         m_ref = mb;
       }
-      uint32_t w[32];
-      float lb0 = 0.f, lb1 = 0.f;
-      if (diag) {
-#pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-          float p0 = exp2f(fmaf(__uint_as_float(sv[c]), sl2, -m_ref));
-          float p1 = exp2f(fmaf(__uint_as_float(sv[c + 1]), sl2, -m_ref));
-          p0 = c <= lim ? p0 : 0.f;
-          p1 = c + 1 <= lim ? p1 : 0.f;
-          lb0 += p0;
-          lb1 += p1;
-          w[c / 2] = pack_bf16x2(p0, p1);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-          const float p0 = exp2f(fmaf(__uint_as_float(sv[c]), sl2, -m_ref));
-          const float p1 = exp2f(fmaf(__uint_as_float(sv[c + 1]), sl2, -m_ref));
-          lb0 += p0;
-          lb1 += p1;
-          w[c / 2] = pack_bf16x2(p0, p1);
-        }
-      }
-      const float lb = lb0 + lb1;
-      l = l * alpha + lb;
-      if (!warp_wait(p_empty, (kb & 1) ^ 1, ctl, ROLE_EPILOGUE)) {
-        alive = false;
-        continue;
-      }
-      // a rescale of O needs every earlier P V finished (p_empty above)
       if (__any_sync(0xffffffffu, move) && kb > 0) {
-        ptx::tc_fence_after();
 #pragma unroll 1
         for (int j = 0; j < D / 64; ++j) {
           const uint32_t oc = tmem + lane_base + TMEM_O + hf * (D / 2) + 32 * j;
@@ -301,10 +267,41 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
           tmem_st_32x32b_x32(oc, ov);
         }
-        tmem_st_wait();
       }
-      // P row into tensor memory: this half's 64 keys = 32 packed columns
-      tmem_st_32x32b_x32(tmem + lane_base + TMEM_P + 32 * hf, w);
+      // P: 32 scores at a time, packed two per column over columns that
+      // this warp has already read
+      float lb0 = 0.f, lb1 = 0.f;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t sv[32];
+        ptx::tmem_ld_32x32b_x32(scol + 32 * c, sv);
+        ptx::tmem_ld_wait();
+        uint32_t w[16];
+        if (diag) {
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            float p0 = exp2f(fmaf(__uint_as_float(sv[j]), sl2, -m_ref));
+            float p1 = exp2f(fmaf(__uint_as_float(sv[j + 1]), sl2, -m_ref));
+            p0 = 32 * c + j <= lim ? p0 : 0.f;
+            p1 = 32 * c + j + 1 <= lim ? p1 : 0.f;
+            lb0 += p0;
+            lb1 += p1;
+            w[j / 2] = pack_bf16x2(p0, p1);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            const float p0 = exp2f(fmaf(__uint_as_float(sv[j]), sl2, -m_ref));
+            const float p1 =
+                exp2f(fmaf(__uint_as_float(sv[j + 1]), sl2, -m_ref));
+            lb0 += p0;
+            lb1 += p1;
+            w[j / 2] = pack_bf16x2(p0, p1);
+          }
+        }
+        tmem_st_32x32b_x16(scol + 16 * c, w);
+      }
+      l = l * alpha + (lb0 + lb1);
       tmem_st_wait();
       ptx::tc_fence_before();
       __syncwarp();
@@ -313,7 +310,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     red[512 + hf * 128 + r] = l;
     softmax_barrier();
     l = red[512 + r] + red[512 + 128 + r];
-    if (alive && warp_wait(o_full, 0, ctl, ROLE_EPILOGUE)) {
+    if (alive &&
+        warp_wait(pv_done, static_cast<uint32_t>(nk - 1) & 1u, ctl,
+                  ROLE_EPILOGUE)) {
       ptx::tc_fence_after();
       const float inv_l = 1.0f / l;
       constexpr int OCH = D / 64;         // 32-column chunks per half
@@ -339,28 +338,29 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
 
   // --------------------------------------------------------- teardown --
   ptx::tc_fence_before();
-  cta_barrier_att();
+  fwd_barrier();
   if (*reinterpret_cast<volatile int*>(abort_flag) && threadIdx.x == 0) {
     const uint64_t t0 = ptx::globaltimer_ns();
     while (ptx::globaltimer_ns() - t0 < ABORT_SETTLE_NS) {
     }
   }
-  cta_barrier_att();
+  fwd_barrier();
   if (warp == 1) {
     __syncwarp();
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, 512);
+    ptx::tmem_dealloc(tmem, FWD_TMEM_COLS);
   }
 }
 
-// Dynamic shared memory; at least 116 KB so that a second CTA (and its 512
-// TMEM columns) never shares the SM.
+// Dynamic shared memory: Q, one K and one V stage, barriers and the
+// exchange buffers (~100 KB at d = 128), and at least 80 KB so that never
+// more than two CTAs (2 x 256 TMEM columns) share an SM.
 template <int D>
 size_t attn_fwd_smem() {
   constexpr int KB = D / 64;
-  const size_t need = 1024 + 3 * KB * KBLOCK_BYTES + 2 * (2 * KB * ATOM_BYTES) +
-                      256 + 6 * 128 * 4;
-  return need > 116 * 1024 ? need : 116 * 1024;
+  const size_t need = 1024 + 2 * KB * KBLOCK_BYTES + 2 * KB * ATOM_BYTES +
+                      128 + 6 * 128 * 4;
+  return need > 80 * 1024 ? need : 80 * 1024;
 }
 
 template <int D>
@@ -371,7 +371,7 @@ cudaError_t launch_fwd(const CUtensorMap& tqk, const CUtensorMap& tv,
   cudaError_t e = cudaFuncSetAttribute(
       kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  kern<<<grid, ATT_THREADS, smem, s>>>(tqk, tv, a);
+  kern<<<grid, FWD_THREADS, smem, s>>>(tqk, tv, a);
   return cudaGetLastError();
 }
 
