@@ -4,7 +4,9 @@
 // too, so no shard exchanges anything here).
 //
 // With P = exp2(S log2(e)/sqrt(d) - lse2) (the forward's saved base-2
-// log-sum-exp), dO = dCtx and delta = rowsum(dO * O):
+// log-sum-exp), dO = dCtx and delta = rowsum(dO * O) (computed by the query
+// kernel from its dO tile and the forward's context rows, and written out for
+// the key/value kernel, which therefore runs second):
 //   dV = P^T dO,   dP = dO V^T,   dS = P * (dP - delta) / sqrt(d),
 //   dK = dS^T Q,   dQ = dS K.
 // Every output element has exactly one writer and no atomics are used:
@@ -17,6 +19,9 @@
 //           rows   A1  A2   B1  B2   S1 = A1 B1^T  S2 = A2 B2^T    outputs
 //   KV      keys   K   V    Q   dO   S^T           dP^T            dK += dS^T Q, dV += P^T dO
 //   Q       query  Q   dO   K   V    S             dP              dQ += dS K, PK += P K
+// The Q kernel also forms delta for its 128 queries from its dO tile and the
+// forward's context rows (loaded into the last ring stage before the ring
+// first reaches it) and writes it out for the KV kernel.
 // The elementwise step writes dS (and P for KV) as bf16 into tensor memory,
 // over the score columns it has just read (each column-half warp inside its
 // own columns), where the output MMAs take them as A operands; their B
@@ -39,6 +44,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                     const __grid_constant__ CUtensorMap tmA2,
                     const __grid_constant__ CUtensorMap tmB1,
                     const __grid_constant__ CUtensorMap tmB2,
+                    const __grid_constant__ CUtensorMap tmCtx,
                     const AttnArgs a) {
   constexpr int KB = D / 64;
   constexpr uint32_t A_TILE = KB * KBLOCK_BYTES;   // 128 rows x D
@@ -52,7 +58,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   // KV: lse2 / delta of the streamed queries per stage; Q: the two column
   // halves' partial row sums of dS, exchanged at the end
   constexpr uint32_t VEC_TOTAL = KV ? NB * VEC_BYTES : 1024;
-  constexpr int NBARS = 9 + 2 * NB;
+  constexpr int NBARS = 11 + 2 * NB;
   constexpr uint32_t B_TX = 2 * B_TILE + (KV ? VEC_BYTES : 0);
   constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 64, false, false);
   constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, false, true);
@@ -73,7 +79,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   const uint32_t a_full = b0, b_full = b0 + 8, b_empty = b_full + 8 * NB,
                  s_full = b_empty + 8 * NB, e_full = s_full + 16,
                  e_empty = e_full + 16, o_full = e_empty + 16,
-                 done_bar = o_full + 8;
+                 done_bar = o_full + 8, ctx_full = done_bar + 8,
+                 ctx_free = ctx_full + 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
@@ -108,6 +115,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     }
     ptx::mbar_init(o_full, 1);
     ptx::mbar_init(done_bar, 1);
+    ptx::mbar_init(ctx_full, 1);
+    ptx::mbar_init(ctx_free, SOFTMAX_WARPS);
     *abort_flag = 0;
     ptx::fence_barrier_init();
   }
@@ -132,8 +141,20 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         ptx::tma_load_2d(sA2 + kk * KBLOCK_BYTES, &tmA2, a_full, cA2 + 64 * kk,
                          row0);
       }
+      if constexpr (!KV) {
+        // Q: the forward's context rows of this block, for delta, borrow the
+        // last stage of the ring until the elementwise warps have read them
+        ptx::mbar_arrive_expect_tx(ctx_full, KB * KBLOCK_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < KB; ++kk)
+          ptx::tma_load_2d(sB + (NB - 1) * 2 * B_TILE + kk * KBLOCK_BYTES,
+                           &tmCtx, ctx_full, head * D + 64 * kk, row0);
+      }
       for (int n = 0; n < nsteps; ++n) {
         const uint32_t bs = n % NB, bph = (n / NB) & 1;
+        if (!KV && n == NB - 1 &&
+            !wait_bounded(ctx_free, 0, ctl, ROLE_PRODUCER))
+          break;
         if (!wait_bounded(b_empty + 8 * bs, bph ^ 1, ctl, ROLE_PRODUCER)) break;
         const int col0 = seq * a.seq_len + (cb_begin + n) * 64;
         const uint32_t bf = b_full + 8 * bs;
@@ -236,15 +257,44 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     const float sl2 = a.scale_log2;
     float lse_r = 0.f, delta_r = 0.f;
+    bool alive = true;
     if constexpr (!KV) {
+      // delta of this query row = sum_e dO[r][e] O[r][e], both tiles in shared
+      // memory (128-byte-swizzled rows; O, the forward's context, in the last
+      // ring stage until ctx_free), summed in fp32 in column order by both
+      // warps of the row (so both hold the same value without an exchange);
+      // half 0 writes it out.
       const size_t off = static_cast<size_t>(head) * a.ld_stat + row0 + r;
       lse_r = a.lse[off];
-      delta_r = a.delta[off];
+      alive = warp_wait(a_full, 0, ctl, ROLE_EPILOGUE) &&
+              warp_wait(ctx_full, 0, ctl, ROLE_EPILOGUE);
+      if (alive) {
+#pragma unroll
+        for (int u = 0; u < D / 8; ++u) {
+          const uint32_t at = (u / 8) * KBLOCK_BYTES + r * 128 +
+                              16 * ((u % 8) ^ (r & 7));
+          const uint4 dv = *reinterpret_cast<const uint4*>(smem + A_TILE + at);
+          const uint4 ov = *reinterpret_cast<const uint4*>(
+              smem + 2 * A_TILE + (NB - 1) * 2 * B_TILE + at);
+          const uint32_t dw4[4] = {dv.x, dv.y, dv.z, dv.w};
+          const uint32_t ow4[4] = {ov.x, ov.y, ov.z, ov.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            float d0, d1, o0, o1;
+            unpack_bf16x2(dw4[k], d0, d1);
+            unpack_bf16x2(ow4[k], o0, o1);
+            delta_r = fmaf(d0, o0, delta_r);
+            delta_r = fmaf(d1, o1, delta_r);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ctx_free);
+        if (hf == 0) a.delta[off] = delta_r;
+      }
     }
     const float* vec = reinterpret_cast<const float*>(vec_gen);
     float rsum = 0.f;              // Q: this half's sum of dS over its keys
-    bool alive = true;
-    for (int n = 0; n < nsteps; ++n) {
+    for (int n = 0; alive && n < nsteps; ++n) {
       const uint32_t st = n & 1, ph = (n >> 1) & 1;
       const uint32_t bs = n % NB, bph = (n / NB) & 1;
       if (!warp_wait(s_full + 8 * st, ph, ctl, ROLE_EPILOGUE) ||
@@ -371,49 +421,22 @@ size_t attn_bwd_smem() {
   constexpr int KB = D / 64;
   constexpr int NB = KV ? 4 : 5;
   const size_t need = 1024 + 2 * KB * KBLOCK_BYTES + NB * 2 * KB * ATOM_BYTES +
-                      (KV ? NB * 512 : 1024) + (9 + 2 * NB) * 8 + 16;
+                      (KV ? NB * 512 : 1024) + (11 + 2 * NB) * 8 + 16;
   return need > 116 * 1024 ? need : 116 * 1024;
 }
 
 template <int D, bool KV>
 cudaError_t launch_bwd(const CUtensorMap& a1, const CUtensorMap& a2,
                        const CUtensorMap& b1, const CUtensorMap& b2,
+                       const CUtensorMap& tctx,
                        const AttnArgs& a, int grid, cudaStream_t s) {
   auto kern = attn_bwd_kernel<D, KV>;
   const size_t smem = attn_bwd_smem<D, KV>();
   cudaError_t e = cudaFuncSetAttribute(
       kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  kern<<<grid, ATT_THREADS, smem, s>>>(a1, a2, b1, b2, a);
+  kern<<<grid, ATT_THREADS, smem, s>>>(a1, a2, b1, b2, tctx, a);
   return cudaGetLastError();
-}
-
-// delta[j][t] = sum_e dCtx[t][j d + e] * Ctx[t][j d + e]: one warp per
-// (token, head), fp32 accumulation of bf16 products.
-__global__ void attn_delta_kernel(const __nv_bfloat16* __restrict__ dctx,
-                                  const __nv_bfloat16* __restrict__ ctx,
-                                  float* __restrict__ delta, int T, int h,
-                                  int heads, int d, long long ld_stat) {
-  const long long gw = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) +
-                       (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (gw >= static_cast<long long>(T) * heads) return;
-  const int t = static_cast<int>(gw / heads);
-  const int j = static_cast<int>(gw - static_cast<long long>(t) * heads);
-  const size_t base = static_cast<size_t>(t) * h + static_cast<size_t>(j) * d;
-  const uint32_t* pd = reinterpret_cast<const uint32_t*>(dctx + base);
-  const uint32_t* pc = reinterpret_cast<const uint32_t*>(ctx + base);
-  float acc = 0.f;
-  for (int e = lane; e < d / 2; e += 32) {
-    float d0, d1, c0, c1;
-    unpack_bf16x2(pd[e], d0, d1);
-    unpack_bf16x2(pc[e], c0, c1);
-    acc = fmaf(d0, c0, acc);
-    acc = fmaf(d1, c1, acc);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  if (lane == 0) delta[static_cast<size_t>(j) * ld_stat + t] = acc;
 }
 
 }  // namespace
@@ -422,31 +445,20 @@ cudaError_t launch_attn_dkdv(const CUtensorMap& tq128, const CUtensorMap& tq64,
                              const CUtensorMap& tdo64, const AttnArgs& a,
                              int grid, cudaStream_t s) {
   if (a.head_dim == 128)
-    return launch_bwd<128, true>(tq128, tq128, tq64, tdo64, a, grid, s);
+    return launch_bwd<128, true>(tq128, tq128, tq64, tdo64, tq128, a, grid, s);
   if (a.head_dim == 64)
-    return launch_bwd<64, true>(tq128, tq128, tq64, tdo64, a, grid, s);
+    return launch_bwd<64, true>(tq128, tq128, tq64, tdo64, tq128, a, grid, s);
   return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_attn_dq(const CUtensorMap& tq128, const CUtensorMap& tq64,
-                           const CUtensorMap& tdo128, const AttnArgs& a,
-                           int grid, cudaStream_t s) {
+                           const CUtensorMap& tdo128, const CUtensorMap& tctx128,
+                           const AttnArgs& a, int grid, cudaStream_t s) {
   if (a.head_dim == 128)
-    return launch_bwd<128, false>(tq128, tdo128, tq64, tq64, a, grid, s);
+    return launch_bwd<128, false>(tq128, tdo128, tq64, tq64, tctx128, a, grid, s);
   if (a.head_dim == 64)
-    return launch_bwd<64, false>(tq128, tdo128, tq64, tq64, a, grid, s);
+    return launch_bwd<64, false>(tq128, tdo128, tq64, tq64, tctx128, a, grid, s);
   return cudaErrorInvalidValue;
-}
-
-cudaError_t launch_attn_delta(const AttnArgs& a, float* delta, int tokens,
-                              cudaStream_t s) {
-  const long long warps = static_cast<long long>(tokens) * a.heads;
-  if (warps == 0) return cudaSuccess;
-  const int blocks = static_cast<int>((warps + 7) / 8);
-  attn_delta_kernel<<<blocks, 256, 0, s>>>(a.dctx, a.ctx, delta, tokens,
-                                           a.heads * a.head_dim, a.heads,
-                                           a.head_dim, a.ld_stat);
-  return cudaGetLastError();
 }
 
 }  // namespace tpmlp

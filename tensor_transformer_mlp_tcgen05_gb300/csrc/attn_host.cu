@@ -6,9 +6,9 @@
 //   [LayerNorm] -> QKV = Xn W_qkv + b_qkv (pair GEMM, one column group per
 //   shard) -> attention core per (sequence, head, query block) -> Z =
 //   sum_i Ctx_i W_o,i + b_o (pair GEMM, fixed-order shard sum = g) [+ X].
-// Backward: db_o, dW_o = Ctx^T dZ, dCtx = dZ W_o^T -> delta = rowsum(dCtx *
-//   Ctx) per head -> dK, dV (one CTA per key block) and dQ (one CTA per
-//   query block) -> db_qkv, dW_qkv = Xn^T dQKV, dXn = sum_i dQKV_i W_qkv,i^T
+// Backward: db_o, dW_o = Ctx^T dZ, dCtx = dZ W_o^T -> dQ and delta =
+//   rowsum(dCtx * Ctx) per head (one CTA per query block) -> dK, dV (one CTA
+//   per key block) -> db_qkv, dW_qkv = Xn^T dQKV, dXn = sum_i dQKV_i W_qkv,i^T
 //   (fixed-order shard sum = f's backward) -> [LayerNorm backward] [+ dZ].
 #include <cmath>
 #include <cstring>
@@ -309,22 +309,22 @@ int tp_attn_backward(tp_attn_handle* H, int tokens, const void* dZ,
   // attention core backward
   AttnArgs aa = core_args(H, ws, L, T);
   aa.dctx = static_cast<const __nv_bfloat16*>(dctx);
-  aa.delta = reinterpret_cast<const float*>(ws + L.delta);
+  aa.delta = reinterpret_cast<float*>(ws + L.delta);
   aa.dqkv = static_cast<__nv_bfloat16*>(dqkv);
-  TRY(run(&H->core, "attn_delta", s, [&] {
-    return launch_attn_delta(aa, reinterpret_cast<float*>(ws + L.delta), T, s);
-  }));
-  CUtensorMap tq128, tq64, tdo128, tdo64;
+  CUtensorMap tq128, tq64, tdo128, tdo64, tctx128;
   TRY(encode_map(&tq128, ws + L.qkv, 3ULL * h, T, 3ULL * h, 128));
   TRY(encode_map(&tq64, ws + L.qkv, 3ULL * h, T, 3ULL * h, 64));
   TRY(encode_map(&tdo128, dctx, h, T, h, 128));
   TRY(encode_map(&tdo64, dctx, h, T, h, 64));
+  TRY(encode_map(&tctx128, ctx, h, T, h, 128));
   const int grid = (T / c.seq_len) * c.heads * aa.nq;
+  // the query kernel also writes delta = rowsum(dCtx * Ctx), which the
+  // key/value kernel reads
+  TRY(run(&H->core, "attn_bwd_dq", s, [&] {
+    return launch_attn_dq(tq128, tq64, tdo128, tctx128, aa, grid, s);
+  }));
   TRY(run(&H->core, "attn_bwd_dkdv", s, [&] {
     return launch_attn_dkdv(tq128, tq64, tdo64, aa, grid, s);
-  }));
-  TRY(run(&H->core, "attn_bwd_dq", s, [&] {
-    return launch_attn_dq(tq128, tq64, tdo128, aa, grid, s);
   }));
   if (dbqkv)
     TRY(colsum(&H->core, "colsum_dbqkv", s, true, dqkv,

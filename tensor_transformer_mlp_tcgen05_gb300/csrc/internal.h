@@ -130,7 +130,9 @@ struct AttnArgs {
                         // log2(e) / sqrt(d)
   long long ld_stat;    // row pitch of lse / delta (= T)
   const __nv_bfloat16* dctx;  // backward: dCtx [T, h]
-  const float* delta;         // backward: rowsum(dCtx * Ctx) per head [H, T]
+  float* delta;               // backward: rowsum(dCtx * Ctx) per head [H, T],
+                              // written by the query kernel, read by the
+                              // key/value kernel
   __nv_bfloat16* dqkv;        // backward output [T, 3h] (same layout as QKV)
   long long ld_qkv;
   int* status;
@@ -142,19 +144,19 @@ struct AttnArgs {
 cudaError_t launch_attn_fwd(const CUtensorMap& tqk, const CUtensorMap& tv,
                             const AttnArgs& a, int grid, cudaStream_t stream);
 
-// Backward, stage 1: delta[j][t] = rowsum(dCtx * Ctx) over head j's columns.
-cudaError_t launch_attn_delta(const AttnArgs& a, float* delta, int tokens,
-                              cudaStream_t stream);
 // Backward, key/value gradients (one CTA per 128 keys of a sequence and
 // head) and query gradients (one CTA per 128 queries).  tq128 / tq64 map
-// QKV with 64 x 128 / 64 x 64 boxes, tdo128 / tdo64 map dCtx [T, h] alike.
-// Both write their columns of a.dqkv; grid = batches * H * nq.
+// QKV with 64 x 128 / 64 x 64 boxes, tdo128 / tdo64 map dCtx [T, h] alike,
+// tctx128 maps the forward's Ctx [T, h] with 64 x 128 boxes.
+// Both write their columns of a.dqkv; grid = batches * H * nq.  The query
+// kernel also writes delta = rowsum(dCtx * Ctx) for every (head, token), which
+// the key/value kernel reads: launch the query kernel first.
 cudaError_t launch_attn_dkdv(const CUtensorMap& tq128, const CUtensorMap& tq64,
                              const CUtensorMap& tdo64, const AttnArgs& a,
                              int grid, cudaStream_t stream);
 cudaError_t launch_attn_dq(const CUtensorMap& tq128, const CUtensorMap& tq64,
-                           const CUtensorMap& tdo128, const AttnArgs& a,
-                           int grid, cudaStream_t stream);
+                           const CUtensorMap& tdo128, const CUtensorMap& tctx128,
+                           const AttnArgs& a, int grid, cudaStream_t stream);
 
 // Record a message for tp_mlp_last_detail() on the calling thread.
 void set_last_detail(const char* msg);
