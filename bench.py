@@ -120,6 +120,62 @@ def _kernel_peak(clocks, peak_b, peak_s):
     return peak_s, "sustained"
 
 
+def e2e_overlapped(torch, stream, steps, h_in, h_out, d_in, d_out, compute):
+    """End to end with the host copies overlapped with the compute: step i's
+    inputs go up on one side stream while step i - 1 computes, its results
+    come down on another while step i + 1 computes, through two device
+    buffer slots.  d_in[s] / d_out[s] are slot s's device tensors (in the
+    order of h_in / h_out, pinned host tensors); compute(s) enqueues one
+    step on `stream` from d_in[s] into d_out[s].  Every step still moves
+    all of its inputs up and all of its results down.  Returns ms per step
+    (CUDA events on `stream`, from before the first upload to after the
+    last download)."""
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    done, fetched = [None, None], [None, None]
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    up.wait_event(e0)
+    down.wait_event(e0)
+
+    def upload(i):
+        s = i % 2
+        with torch.cuda.stream(up):
+            if done[s] is not None:       # the slot's previous step has
+                up.wait_event(done[s])    # finished reading its inputs
+            for h, dv in zip(h_in, d_in[s]):
+                dv.copy_(h, non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(up)
+        return ev
+
+    nxt = upload(0)
+    for i in range(steps):
+        s = i % 2
+        stream.wait_event(nxt)
+        if fetched[s] is not None:        # its previous results are down
+            stream.wait_event(fetched[s])
+        compute(s)
+        ev = torch.cuda.Event()
+        ev.record(stream)
+        done[s] = ev
+        if i + 1 < steps:
+            nxt = upload(i + 1)
+        with torch.cuda.stream(down):
+            down.wait_event(ev)
+            for h, dv in zip(h_out, d_out[s]):
+                h.copy_(dv, non_blocking=True)
+            f = torch.cuda.Event()
+            f.record(down)
+            fetched[s] = f
+    for f in fetched:
+        if f is not None:
+            stream.wait_event(f)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
 def _src_sha(files=_SRC_FILES["gemm"]):
     """Hash of the kernel sources a traffic figure depends on."""
     h = hashlib.sha256()
@@ -337,7 +393,35 @@ def run_ours(args, w, rank, world, local_rank):
         e2e_step()
     e3.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e2.elapsed_time(e3) / args.steps, world)
+    e2e_serial_ms = max_over_ranks(e2.elapsed_time(e3) / args.steps, world)
+
+    # the same with the copies overlapped (two slots, side streams)
+    d_in = [[torch.empty_like(d["X"])] + ([torch.empty_like(d["X"])]
+                                          if w.backward else [])
+            for _ in range(2)]
+    d_out = [[torch.empty_like(Z)] + ([torch.empty_like(d["X"])]
+                                      if w.backward else [])
+             for _ in range(2)]
+    slot_grads = [dict(grads, dX=d_out[k][1]) if w.backward else None
+                  for k in range(2)]
+
+    def compute(k):
+        m.forward(d_in[k][0], d["A"], d["B"], d["b1"], d["b2"], d["gamma"],
+                  d["beta"], training=w.backward, out=d_out[k][0])
+        if w.backward:
+            m.backward(d_in[k][1], d_in[k][0], d["A"], d["B"], d["gamma"],
+                       bias_grads=True, out=slot_grads[k])
+
+    h_in = [hX] + ([hdZ] if w.backward else [])
+    h_out = [hZ] + ([hdX] if w.backward else [])
+    e2e_overlapped(torch, stream, 2, h_in, h_out, d_in, d_out, compute)
+    barrier(world)
+    e2e_ms = max_over_ranks(
+        e2e_overlapped(torch, stream, args.steps, h_in, h_out, d_in, d_out,
+                       compute), world)
+    if m.check() != 0:
+        raise RuntimeError("device status after the end-to-end runs: "
+                           + Bn.tp_mlp_last_detail())
 
     flops = w.flops_fwd_bwd() if w.backward else w.flops_fwd()
     peak_b, peak_s, hbm, peak_src = _peaks()
@@ -386,7 +470,12 @@ def run_ours(args, w, rank, world, local_rank):
                    "l2": "inputs larger than L2 (no flush)"},
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2),
                 "unit": "TFLOP/s", "ms_per_step": round(e2e_ms, 4),
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "copies": "overlapped with the compute (side streams, two "
+                          "buffer slots)",
+                "serial_value": round(world * flops / (e2e_serial_ms * 1e-3)
+                                      / 1e12, 2),
+                "serial_ms_per_step": round(e2e_serial_ms, 4)},
         "gpu_launches": launches,
         "bitwise_identical_two_runs": identical,
         "clocks": clocks,
@@ -556,7 +645,28 @@ def run_ours_attn(args, w, rank, world, local_rank):
         e2e_step()
     e3.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e2.elapsed_time(e3) / args.steps, world)
+    e2e_serial_ms = max_over_ranks(e2.elapsed_time(e3) / args.steps, world)
+
+    d_in = [[torch.empty_like(d["X"]), torch.empty_like(d["X"])]
+            for _ in range(2)]
+    d_out = [[torch.empty_like(Z), torch.empty_like(d["X"])] for _ in range(2)]
+    slot_grads = [dict(grads, dX=d_out[k][1]) for k in range(2)]
+
+    def compute(k):
+        m.forward(d_in[k][0], d["Wqkv"], d["Wo"], d["bqkv"], d["bo"],
+                  d["gamma"], d["beta"], out=d_out[k][0])
+        m.backward(d_in[k][1], d_in[k][0], d["Wqkv"], d["Wo"], d["gamma"],
+                   out=slot_grads[k])
+
+    e2e_overlapped(torch, stream, 2, [hX, hdZ], [hZ, hdX], d_in, d_out,
+                   compute)
+    barrier(world)
+    e2e_ms = max_over_ranks(
+        e2e_overlapped(torch, stream, args.steps, [hX, hdZ], [hZ, hdX], d_in,
+                       d_out, compute), world)
+    if m.check() != 0:
+        raise RuntimeError("device status after the end-to-end runs: "
+                           + Bn.tp_mlp_last_detail())
 
     flops = w.flops_fwd_bwd()
     peak_b, peak_s, hbm, peak_src = _peaks()
@@ -600,7 +710,12 @@ def run_ours_attn(args, w, rank, world, local_rank):
                    "l2": "inputs larger than L2 (no flush)"},
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2),
                 "unit": "TFLOP/s", "ms_per_step": round(e2e_ms, 4),
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "copies": "overlapped with the compute (side streams, two "
+                          "buffer slots)",
+                "serial_value": round(world * flops / (e2e_serial_ms * 1e-3)
+                                      / 1e12, 2),
+                "serial_ms_per_step": round(e2e_serial_ms, 4)},
         "gpu_launches": launches,
         "bitwise_identical_two_runs": identical,
         "clocks": clocks,
@@ -753,7 +868,23 @@ def run_ours_fp8(args, w, rank, world, local_rank):
         e2e_step()
     torch.cuda.synchronize()
     barrier(world)
-    e2e_ms = max_over_ranks(timed(e2e_step, args.steps), world)
+    e2e_serial_ms = max_over_ranks(timed(e2e_step, args.steps), world)
+
+    d_in = [[torch.empty_like(d["X"])] for _ in range(2)]
+    d_out = [[torch.empty_like(Z)] for _ in range(2)]
+
+    def compute(k):
+        m.forward_fp8(d_in[k][0], packed, d["b1"], d["b2"], d["gamma"],
+                      d["beta"], out=d_out[k][0])
+
+    e2e_overlapped(torch, stream, 2, [hX], [hZ], d_in, d_out, compute)
+    barrier(world)
+    e2e_ms = max_over_ranks(
+        e2e_overlapped(torch, stream, args.steps, [hX], [hZ], d_in, d_out,
+                       compute), world)
+    if m.check() != 0:
+        raise RuntimeError("device status after the end-to-end runs: "
+                           + Bn.tp_mlp_last_detail())
 
     flops = w.flops_fwd()
     peak_b, peak_s, hbm, peak_src = _peaks()
@@ -803,7 +934,12 @@ def run_ours_fp8(args, w, rank, world, local_rank):
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2),
                 "unit": "TFLOP/s", "ms_per_step": round(e2e_ms, 4),
                 "h2d_bytes_per_step": hX.numel() * hX.element_size(),
-                "d2h_bytes_per_step": hZ.numel() * hZ.element_size()},
+                "d2h_bytes_per_step": hZ.numel() * hZ.element_size(),
+                "copies": "overlapped with the compute (side streams, two "
+                          "buffer slots)",
+                "serial_value": round(world * flops / (e2e_serial_ms * 1e-3)
+                                      / 1e12, 2),
+                "serial_ms_per_step": round(e2e_serial_ms, 4)},
         "gpu_launches": launches,
         "bitwise_identical_two_runs": identical,
         "clocks": clocks,
