@@ -11,11 +11,18 @@
 // its 128 rows of D (all 256 columns) in its own TMEM.  The ring has 5
 // stages (160 KB) next to 64 KB of epilogue staging.
 //
+// Two pairs may share a cluster of 4 (launches prefer 4, fall back to 2):
+// then each k-block's B halves are loaded by one of the two pairs and
+// multicast into both, since the group's two tiles share their B columns.
+//
 // Synchronisation:
-//   full[s]   (rank 0 only) counts the TMA bytes of both CTAs: rank 0 arms it
-//             with the pair's 64 KB, both CTAs' copies complete on it.
-//   empty[s]  (each CTA) arrived by the MMA issuer's multicast commit when the
-//             MMAs have read stage s, releasing both producers.
+//   full[s]   (pair leader only) counts the TMA bytes landing in both CTAs of
+//             the pair: the leader arms it with the pair's 64 KB, both CTAs'
+//             copies (and multicast copies from the other pair) complete on it.
+//   empty[s]  (each CTA) arrived by the MMA issuers' multicast commits when
+//             the MMAs have read stage s, releasing the producers (in a
+//             cluster of 4 both pairs' commits, since either pair's copies
+//             may land in it).
 //   tfull[b]  (each CTA) arrived by a multicast commit when accumulator b is
 //             ready in both TMEMs.
 //   tempty[b] (rank 0 only) 16 arrivals: 8 epilogue warps of each CTA, the
@@ -124,15 +131,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // Work is dealt to groups of four CTAs (two pairs) in blockIdx order: a
+  // group owns a 512 x 256 "super-tile" (its pairs the upper and lower
+  // 256 x 256 tiles, same B columns) whether the launch made it one cluster
+  // of 4 or two clusters of 2.  In a cluster of 4 the two pairs share the B
+  // operand: each k-block's B halves are loaded by one pair (alternating)
+  // and multicast into both.
   const uint32_t rank = ptx::cluster_ctarank();
-  const bool leader = rank == 0;
-  const int pair = blockIdx.x >> 1;
-  const int num_pairs = gridDim.x >> 1;
+  const bool quad = ptx::cluster_nctarank() == 4;
+  const uint32_t prank = rank & 1u;        // rank inside the pair
+  const uint32_t lead_rank = rank & ~1u;   // the pair's even CTA
+  const bool leader = prank == 0;
+  const int pg = static_cast<int>(blockIdx.x >> 1) & 1;  // pair in its group
+  const int group = static_cast<int>(blockIdx.x >> 2);
+  const int num_groups = static_cast<int>(gridDim.x >> 2);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(full0 + 8u * s, 1);
-      ptx::mbar_init(empty0 + 8u * s, 1);
+      ptx::mbar_init(empty0 + 8u * s, quad ? 2 : 1);
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(tfull0 + 8u * b, 1);
@@ -159,11 +176,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const Ctl ctl{abort_flag, args.status, args.budget_ns};
   const int num_m = (args.M + PM - 1) / PM;
   const int num_n = (args.N + PN - 1) / PN;
-  const int num_tiles = num_m * num_n;
+  const int num_msup = (num_m + 1) / 2;   // super-tile rows
+  const int num_super = num_msup * num_n;
+  const int group_sup = args.group_m > 1 ? args.group_m / 2 : 1;
   const int kb_total = args.kb_per_seg * args.num_seg;
   // The even CTA's full and tempty barriers, as cluster addresses.
-  const uint32_t lead_full0 = ptx::mapa_shared(full0, 0);
-  const uint32_t lead_tempty0 = ptx::mapa_shared(tempty0, 0);
+  const uint32_t lead_full0 = ptx::mapa_shared(full0, lead_rank);
+  const uint32_t lead_tempty0 = ptx::mapa_shared(tempty0, lead_rank);
 
   if (warp < FIRST_EPI_WARP) {
     ptx::setmaxnreg_dec<REGS_CONTROL>();
@@ -171,11 +190,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // ---------------------------------------------------- producer --
       uint32_t stage = 0, phase = 0;
       bool alive = true;
-      for (int tile = pair; alive && tile < num_tiles; tile += num_pairs) {
-        int mb, nb;
-        tile_coords(tile, num_m, num_n, args.group_m, mb, nb);
-        const int m0 = mb * PM + static_cast<int>(rank) * HM;
-        const int n0 = nb * PN + static_cast<int>(rank) * HN;
+      const uint16_t bmask =
+          static_cast<uint16_t>((1u << prank) | (1u << (prank + 2u)));
+      for (int sup = group; alive && sup < num_super; sup += num_groups) {
+        int msup, nb;
+        tile_coords(sup, num_msup, num_n, group_sup, msup, nb);
+        const int mb = 2 * msup + pg;   // may lie past M: zero-filled, unused
+        const int m0 = mb * PM + static_cast<int>(prank) * HM;
+        const int n0 = nb * PN + static_cast<int>(prank) * HN;
         for (int kb = 0; kb < kb_total; ++kb) {
           if (!wait_bounded(empty0 + 8u * stage, phase ^ 1u, ctl,
                             ROLE_PRODUCER)) {
@@ -196,13 +218,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               ptx::tma_load_2d_pair(da + j * (BK * 128), &tmA, fb, m0 + 64 * j,
                                     k0);
           }
-          if constexpr (!B_MN) {
-            ptx::tma_load_2d_pair(db, &tmB, fb, k0, n0);
-          } else {
+          if (!quad) {
+            if constexpr (!B_MN) {
+              ptx::tma_load_2d_pair(db, &tmB, fb, k0, n0);
+            } else {
 #pragma unroll
-            for (int j = 0; j < HN / 64; ++j)
-              ptx::tma_load_2d_pair(db + j * (BK * 128), &tmB, fb, n0 + 64 * j,
-                                    k0);
+              for (int j = 0; j < HN / 64; ++j)
+                ptx::tma_load_2d_pair(db + j * (BK * 128), &tmB, fb,
+                                      n0 + 64 * j, k0);
+            }
+          } else if ((kb & 1) == pg) {
+            if constexpr (!B_MN) {
+              ptx::tma_load_2d_pair_mc(db, &tmB, fb, k0, n0, bmask);
+            } else {
+#pragma unroll
+              for (int j = 0; j < HN / 64; ++j)
+                ptx::tma_load_2d_pair_mc(db + j * (BK * 128), &tmB, fb,
+                                         n0 + 64 * j, k0, bmask);
+            }
           }
           if (++stage == STAGES) {
             stage = 0;
@@ -218,10 +251,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       constexpr uint32_t B_KSTEP = B_MN ? 16 * 128 : 32;
       constexpr uint32_t A_LBO = A_MN ? BK * 128 : 16;
       constexpr uint32_t B_LBO = B_MN ? BK * 128 : 16;
-      constexpr uint16_t BOTH = 0x3;
+      // stage release: both pairs' producers write into a shared stage
+      const uint16_t release = quad ? 0xF : 0x3;
+      const uint16_t pair_mask = static_cast<uint16_t>(0x3u << lead_rank);
       uint32_t stage = 0, phase = 0, acc = 0;
       bool alive = true;
-      for (int tile = pair; alive && tile < num_tiles; tile += num_pairs) {
+      for (int sup = group; alive && sup < num_super; sup += num_groups) {
         for (int seg = 0; alive && seg < args.num_seg; ++seg, ++acc) {
           const uint32_t b = acc & 1u;
           const uint32_t aph = (acc >> 1) & 1u;
@@ -254,18 +289,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                    (kb > 0 || k > 0) ? 1u : 0u);
               }
             }
-            ptx::mma_commit_pair(empty0 + 8u * stage, BOTH);
+            ptx::mma_commit_pair(empty0 + 8u * stage, release);
             if (++stage == STAGES) {
               stage = 0;
               phase ^= 1u;
             }
           }
-          if (alive) ptx::mma_commit_pair(tfull0 + 8u * b, BOTH);
+          if (alive) ptx::mma_commit_pair(tfull0 + 8u * b, pair_mask);
         }
       }
       if (*reinterpret_cast<volatile int*>(abort_flag)) {
         // Wait for every MMA this thread issued before TMEM is freed.
-        ptx::mma_commit_pair(done_bar, 0x1);
+        ptx::mma_commit_pair(done_bar, static_cast<uint16_t>(1u << rank));
         wait_teardown(done_bar, 0);
       }
     }
@@ -296,10 +331,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const float acc_scale = F8 ? *args.scale_a * *args.scale_b : 1.f;
     uint32_t acc = 0;
     bool alive = true;
-    for (int tile = pair; alive && tile < num_tiles; tile += num_pairs) {
-      int mb, nb;
-      tile_coords(tile, num_m, num_n, args.group_m, mb, nb);
-      const int row0 = mb * PM + static_cast<int>(rank) * HM + q * 32;
+    for (int sup = group; alive && sup < num_super; sup += num_groups) {
+      int msup, nb;
+      tile_coords(sup, num_msup, num_n, group_sup, msup, nb);
+      const int mb = 2 * msup + pg;
+      const int row0 = mb * PM + static_cast<int>(prank) * HM + q * 32;
       const int row = row0 + lane;
       const bool live = row0 < args.M;  // warp-uniform: any row in range
       const int col_base = nb * PN + half * 128;
@@ -482,7 +518,7 @@ cudaError_t launch_impl(const CUtensorMap& ta, const CUtensorMap& tb,
                            static_cast<int>(SMEM_BYTES));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
@@ -498,10 +534,20 @@ cudaError_t launch_impl(const CUtensorMap& ta, const CUtensorMap& tb,
   e = cudaOccupancyMaxActiveClusters(&resident, kern, &cfg);
   if (e != cudaSuccess) return e;
   if (resident <= 0) return cudaErrorInvalidConfiguration;
-  const long long tiles =
-      static_cast<long long>((args.M + PM - 1) / PM) * ((args.N + PN - 1) / PN);
-  long long pairs = tiles < max_pairs ? tiles : max_pairs;
+  // Work goes to groups of two pairs (an even number of pairs); the launch
+  // prefers clusters of 4 (the two pairs share B) and falls back to 2 where
+  // a GPU processing cluster has no room for 4.
+  const long long sup = static_cast<long long>((args.M + 2 * PM - 1) / (2 * PM)) *
+                        ((args.N + PN - 1) / PN);
+  long long pairs = 2 * sup < max_pairs ? 2 * sup : max_pairs;
   if (pairs > resident) pairs = resident;
+  pairs &= ~1LL;
+  if (pairs < 2) pairs = 2;
+  attr[1].id = cudaLaunchAttributePreferredClusterDimension;
+  attr[1].val.preferredClusterDim.x = 4;
+  attr[1].val.preferredClusterDim.y = 1;
+  attr[1].val.preferredClusterDim.z = 1;
+  cfg.numAttrs = 2;
   cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
   e = cudaLaunchKernelEx(&cfg, kern, ta, tb, to, to2, args);
   if (e != cudaSuccess) return e;
