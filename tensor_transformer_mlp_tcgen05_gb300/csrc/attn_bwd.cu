@@ -45,6 +45,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                     const __grid_constant__ CUtensorMap tmB1,
                     const __grid_constant__ CUtensorMap tmB2,
                     const __grid_constant__ CUtensorMap tmCtx,
+                    const __grid_constant__ CUtensorMap tmOut,
                     const AttnArgs a) {
   constexpr int KB = D / 64;
   constexpr uint32_t A_TILE = KB * KBLOCK_BYTES;   // 128 rows x D
@@ -357,41 +358,77 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     }
     if (alive && warp_wait(o_full, 0, ctl, ROLE_EPILOGUE)) {
       ptx::tc_fence_after();
-      constexpr int OCH = D / 64;          // 32-column chunks per half
-      __nv_bfloat16* rowp = a.dqkv + static_cast<size_t>(row0 + r) * a.ld_qkv;
-      __nv_bfloat16* out2 = rowp + (KV ? hc.k : hc.q) + hf * (D / 2);
+      if constexpr (KV) {
+        // Each warp writes its 32 rows of one output (half 0: dK, half 1:
+        // dV), all D columns, as 32-row x 64-column bf16 chunks staged in
+        // the (now idle) B ring and stored by TMA: full-line writes instead
+        // of one row per thread.
+        ChunkStager st{sB + static_cast<uint32_t>(warp - SOFTMAX_WARP0) * 2u *
+                                STAGE_CHUNK_BYTES,
+                       0u};
+        const uint32_t src =
+            tmem + lane_base + (hf == 0 ? TMEM_OUT2 : TMEM_OUT1);
+        const int col = hf == 0 ? hc.k : hc.v;
+#pragma unroll 1
+        for (int j = 0; j < D / 64; ++j) {
+          uint32_t r0[32], r1[32];
+          ptx::tmem_ld_32x32b_x32(src + 64 * j, r0);
+          ptx::tmem_ld_32x32b_x32(src + 64 * j + 32, r1);
+          ptx::tmem_ld_wait();
+          uint32_t w[32];
 #pragma unroll
-      for (int j = 0; j < OCH; ++j) {
-        uint32_t ov[32];
-        ptx::tmem_ld_32x32b_x32(
-            tmem + lane_base + TMEM_OUT2 + hf * (D / 2) + 32 * j, ov);
-        ptx::tmem_ld_wait();
-        float v[32];
+          for (int i = 0; i < 16; ++i) {
+            w[i] = pack_bf16x2(__uint_as_float(r0[2 * i]),
+                               __uint_as_float(r0[2 * i + 1]));
+            w[16 + i] = pack_bf16x2(__uint_as_float(r1[2 * i]),
+                                    __uint_as_float(r1[2 * i + 1]));
+          }
+          st.put(&tmOut, col + 64 * j, row0 + q * 32, w, lane);
+        }
+        st.drain(lane);
+      } else if constexpr (D == 128) {
+        // dQ: each warp its 32 rows x 64 columns (one chunk), staged and
+        // stored by TMA like the key/value outputs
+        ChunkStager st{sB + static_cast<uint32_t>(warp - SOFTMAX_WARP0) * 2u *
+                                STAGE_CHUNK_BYTES,
+                       0u};
+        const uint32_t src2 = tmem + lane_base + TMEM_OUT2 + hf * 64;
+        const uint32_t src1 = tmem + lane_base + TMEM_OUT1 + hf * 64;
+        uint32_t w[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(ov[i]);
-        if constexpr (!KV) {
-          uint32_t kv[32];
-          ptx::tmem_ld_32x32b_x32(
-              tmem + lane_base + TMEM_OUT1 + hf * (D / 2) + 32 * j, kv);
+        for (int j = 0; j < 2; ++j) {
+          uint32_t ov[32], kv[32];
+          ptx::tmem_ld_32x32b_x32(src2 + 32 * j, ov);
+          ptx::tmem_ld_32x32b_x32(src1 + 32 * j, kv);
           ptx::tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            v[i] = fmaf(-rrow, __uint_as_float(kv[i]), v[i]);
+          for (int i = 0; i < 16; ++i)
+            w[16 * j + i] = pack_bf16x2(
+                fmaf(-rrow, __uint_as_float(kv[2 * i]), __uint_as_float(ov[2 * i])),
+                fmaf(-rrow, __uint_as_float(kv[2 * i + 1]),
+                     __uint_as_float(ov[2 * i + 1])));
         }
-        store_bf16x32(out2 + 32 * j, v);
-      }
-      if constexpr (KV) {
-        __nv_bfloat16* out1 = rowp + hc.v + hf * (D / 2);
+        st.put(&tmOut, hc.q + 64 * hf, row0 + q * 32, w, lane);
+        st.drain(lane);
+      } else {
+        constexpr int OCH = D / 64;        // 32-column chunks per half
+        __nv_bfloat16* out2 = a.dqkv + static_cast<size_t>(row0 + r) * a.ld_qkv +
+                              hc.q + hf * (D / 2);
 #pragma unroll
         for (int j = 0; j < OCH; ++j) {
           uint32_t ov[32];
           ptx::tmem_ld_32x32b_x32(
-              tmem + lane_base + TMEM_OUT1 + hf * (D / 2) + 32 * j, ov);
+              tmem + lane_base + TMEM_OUT2 + hf * (D / 2) + 32 * j, ov);
+          ptx::tmem_ld_wait();
+          uint32_t kv[32];
+          ptx::tmem_ld_32x32b_x32(
+              tmem + lane_base + TMEM_OUT1 + hf * (D / 2) + 32 * j, kv);
           ptx::tmem_ld_wait();
           float v[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(ov[i]);
-          store_bf16x32(out1 + 32 * j, v);
+          for (int i = 0; i < 32; ++i)
+            v[i] = fmaf(-rrow, __uint_as_float(kv[i]), __uint_as_float(ov[i]));
+          store_bf16x32(out2 + 32 * j, v);
         }
       }
     }
@@ -428,36 +465,42 @@ size_t attn_bwd_smem() {
 template <int D, bool KV>
 cudaError_t launch_bwd(const CUtensorMap& a1, const CUtensorMap& a2,
                        const CUtensorMap& b1, const CUtensorMap& b2,
-                       const CUtensorMap& tctx,
+                       const CUtensorMap& tctx, const CUtensorMap& tout,
                        const AttnArgs& a, int grid, cudaStream_t s) {
   auto kern = attn_bwd_kernel<D, KV>;
   const size_t smem = attn_bwd_smem<D, KV>();
   cudaError_t e = cudaFuncSetAttribute(
       kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  kern<<<grid, ATT_THREADS, smem, s>>>(a1, a2, b1, b2, tctx, a);
+  kern<<<grid, ATT_THREADS, smem, s>>>(a1, a2, b1, b2, tctx, tout, a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_attn_dkdv(const CUtensorMap& tq128, const CUtensorMap& tq64,
-                             const CUtensorMap& tdo64, const AttnArgs& a,
+                             const CUtensorMap& tdo64,
+                             const CUtensorMap& tdqkv_out, const AttnArgs& a,
                              int grid, cudaStream_t s) {
   if (a.head_dim == 128)
-    return launch_bwd<128, true>(tq128, tq128, tq64, tdo64, tq128, a, grid, s);
+    return launch_bwd<128, true>(tq128, tq128, tq64, tdo64, tq128, tdqkv_out, a,
+                                 grid, s);
   if (a.head_dim == 64)
-    return launch_bwd<64, true>(tq128, tq128, tq64, tdo64, tq128, a, grid, s);
+    return launch_bwd<64, true>(tq128, tq128, tq64, tdo64, tq128, tdqkv_out, a,
+                                grid, s);
   return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_attn_dq(const CUtensorMap& tq128, const CUtensorMap& tq64,
                            const CUtensorMap& tdo128, const CUtensorMap& tctx128,
-                           const AttnArgs& a, int grid, cudaStream_t s) {
+                           const CUtensorMap& tdqkv_out, const AttnArgs& a,
+                           int grid, cudaStream_t s) {
   if (a.head_dim == 128)
-    return launch_bwd<128, false>(tq128, tdo128, tq64, tq64, tctx128, a, grid, s);
+    return launch_bwd<128, false>(tq128, tdo128, tq64, tq64, tctx128, tdqkv_out,
+                                  a, grid, s);
   if (a.head_dim == 64)
-    return launch_bwd<64, false>(tq128, tdo128, tq64, tq64, tctx128, a, grid, s);
+    return launch_bwd<64, false>(tq128, tdo128, tq64, tq64, tctx128, tdqkv_out,
+                                 a, grid, s);
   return cudaErrorInvalidValue;
 }
 

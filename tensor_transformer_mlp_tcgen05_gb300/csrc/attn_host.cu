@@ -311,20 +311,21 @@ int tp_attn_backward(tp_attn_handle* H, int tokens, const void* dZ,
   aa.dctx = static_cast<const __nv_bfloat16*>(dctx);
   aa.delta = reinterpret_cast<float*>(ws + L.delta);
   aa.dqkv = static_cast<__nv_bfloat16*>(dqkv);
-  CUtensorMap tq128, tq64, tdo128, tdo64, tctx128;
+  CUtensorMap tq128, tq64, tdo128, tdo64, tctx128, tdqkv_out;
   TRY(encode_map(&tq128, ws + L.qkv, 3ULL * h, T, 3ULL * h, 128));
   TRY(encode_map(&tq64, ws + L.qkv, 3ULL * h, T, 3ULL * h, 64));
   TRY(encode_map(&tdo128, dctx, h, T, h, 128));
   TRY(encode_map(&tdo64, dctx, h, T, h, 64));
   TRY(encode_map(&tctx128, ctx, h, T, h, 128));
+  TRY(out_map(&tdqkv_out, dqkv, false, T, 3 * h, 3LL * h));
   const int grid = (T / c.seq_len) * c.heads * aa.nq;
   // the query kernel also writes delta = rowsum(dCtx * Ctx), which the
   // key/value kernel reads
   TRY(run(&H->core, "attn_bwd_dq", s, [&] {
-    return launch_attn_dq(tq128, tq64, tdo128, tctx128, aa, grid, s);
+    return launch_attn_dq(tq128, tq64, tdo128, tctx128, tdqkv_out, aa, grid, s);
   }));
   TRY(run(&H->core, "attn_bwd_dkdv", s, [&] {
-    return launch_attn_dkdv(tq128, tq64, tdo64, aa, grid, s);
+    return launch_attn_dkdv(tq128, tq64, tdo64, tdqkv_out, aa, grid, s);
   }));
   if (dbqkv)
     TRY(colsum(&H->core, "colsum_dbqkv", s, true, dqkv,

@@ -147,16 +147,19 @@ cudaError_t launch_attn_fwd(const CUtensorMap& tqk, const CUtensorMap& tv,
 // Backward, key/value gradients (one CTA per 128 keys of a sequence and
 // head) and query gradients (one CTA per 128 queries).  tq128 / tq64 map
 // QKV with 64 x 128 / 64 x 64 boxes, tdo128 / tdo64 map dCtx [T, h] alike,
-// tctx128 maps the forward's Ctx [T, h] with 64 x 128 boxes.
+// tctx128 maps the forward's Ctx [T, h] with 64 x 128 boxes, tdqkv_out maps
+// dQKV [T, 3h] with 64 x 32 store boxes (both kernels' output).
 // Both write their columns of a.dqkv; grid = batches * H * nq.  The query
 // kernel also writes delta = rowsum(dCtx * Ctx) for every (head, token), which
 // the key/value kernel reads: launch the query kernel first.
 cudaError_t launch_attn_dkdv(const CUtensorMap& tq128, const CUtensorMap& tq64,
-                             const CUtensorMap& tdo64, const AttnArgs& a,
+                             const CUtensorMap& tdo64,
+                             const CUtensorMap& tdqkv_out, const AttnArgs& a,
                              int grid, cudaStream_t stream);
 cudaError_t launch_attn_dq(const CUtensorMap& tq128, const CUtensorMap& tq64,
                            const CUtensorMap& tdo128, const CUtensorMap& tctx128,
-                           const AttnArgs& a, int grid, cudaStream_t stream);
+                           const CUtensorMap& tdqkv_out, const AttnArgs& a,
+                           int grid, cudaStream_t stream);
 
 // Record a message for tp_mlp_last_detail() on the calling thread.
 void set_last_detail(const char* msg);
