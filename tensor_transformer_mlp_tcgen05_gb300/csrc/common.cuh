@@ -55,6 +55,12 @@ struct GemmArgs {
   const float* scale_a;
   const float* scale_b;
   unsigned int* amax_out;
+  // EPI_GELU_BWD (nullable): for every 32-row group g of the output and
+  // column c, the fp32 sum of the stored (bf16) values over the group's rows
+  // (in row order), written to colsum[g * ld_colsum + c] — the first stage of
+  // the bias gradient sum over the tokens.
+  float* colsum;
+  long long ld_colsum;
 };
 
 // Roles recorded in status[1] when a bounded wait gives up.

@@ -161,9 +161,11 @@ struct ChunkStager {
   uint32_t count;  // chunks issued so far (lane 0's bulk groups)
 
   // Write this lane's 128-byte row `w` and store the chunk at element
-  // coordinates (c0, r0) of `map`.
-  __device__ __forceinline__ void put(const CUtensorMap* map, int c0, int r0,
-                                      const uint32_t (&w)[32], int lane) {
+  // coordinates (c0, r0) of `map`; returns the staging buffer used (it holds
+  // the chunk until the next-but-one put).
+  __device__ __forceinline__ uint32_t put(const CUtensorMap* map, int c0,
+                                          int r0, const uint32_t (&w)[32],
+                                          int lane) {
     const uint32_t buf = base + (count & 1u) * STAGE_CHUNK_BYTES;
     if (lane == 0) ptx::bulk_wait_read<1>();  // buffer used two chunks ago
     __syncwarp();
@@ -181,6 +183,7 @@ struct ChunkStager {
       ptx::bulk_commit();
     }
     ++count;
+    return buf;
   }
 
   __device__ __forceinline__ void drain(int lane) {
@@ -188,6 +191,25 @@ struct ChunkStager {
     __syncwarp();
   }
 };
+
+// Column sums of a staged 32-row x 64-column bf16 chunk (128-byte-swizzled
+// rows): lane l gets the fp32 sums of columns 2l and 2l + 1 over the rows in
+// order.  Each row read is 32 consecutive words, one per lane.
+__device__ __forceinline__ float2 chunk_colsum_bf16(uint32_t buf, int lane) {
+  float s0 = 0.f, s1 = 0.f;
+  const uint32_t off = static_cast<uint32_t>(lane & 3) * 4u;
+#pragma unroll 8
+  for (int r = 0; r < 32; ++r) {
+    const uint32_t u = static_cast<uint32_t>((lane >> 2) ^ (r & 7));
+    const uint32_t word =
+        ptx::ld_shared_u32(buf + static_cast<uint32_t>(r) * 128u + u * 16u + off);
+    float a, b;
+    unpack_bf16x2(word, a, b);
+    s0 += a;
+    s1 += b;
+  }
+  return make_float2(s0, s1);
+}
 
 __device__ __forceinline__ void pack_bf16x64(const float* v, uint32_t (&w)[32]) {
 #pragma unroll

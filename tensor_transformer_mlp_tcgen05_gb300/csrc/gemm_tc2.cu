@@ -340,6 +340,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const bool live = row0 < args.M;  // warp-uniform: any row in range
       const int col_base = nb * PN + half * 128;
       float S[EPI == EPI_SHARDSUM ? 128 : 1];
+      uint32_t cbuf[2] = {0u, 0u};   // EPI_GELU_BWD: the staged dH chunks
       for (int seg = 0; seg < args.num_seg; ++seg, ++acc) {
         const uint32_t b = acc & 1u;
         const uint32_t aph = (acc >> 1) & 1u;
@@ -438,7 +439,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
               }
               pack_bf16x64(v, w);
-              st.put(&tmO, c0, row0, w, lane);
+              cbuf[j] = st.put(&tmO, c0, row0, w, lane);
             }
           }
         }
@@ -449,6 +450,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ptx::mbar_arrive(tempty0 + 8u * b);
           } else {
             ptx::mbar_arrive_cluster(lead_tempty0 + 8u * b);
+          }
+        }
+        if constexpr (EPI == EPI_GELU_BWD) {
+          // bias-gradient partials of this warp's 32 rows, from the chunks
+          // still staged in shared memory (after the accumulator is released)
+          if (args.colsum != nullptr && live) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              const int c0 = col_base + j * 64;
+              if (c0 < args.N) {
+                const float2 cs = chunk_colsum_bf16(cbuf[j], lane);
+                *reinterpret_cast<float2*>(
+                    args.colsum + static_cast<size_t>(row0 / 32) * args.ld_colsum +
+                    c0 + 2 * lane) = cs;
+              }
+            }
           }
         }
       }

@@ -261,14 +261,31 @@ __global__ void __launch_bounds__(CS_WARPS * 32)
   }
 }
 
-__global__ void colsum_finalize_kernel(const float* __restrict__ part,
-                                       float* __restrict__ out, int chunks,
-                                       int cols) {
-  const int c = blockIdx.x * blockDim.x + threadIdx.x;
-  if (c >= cols) return;
+// out[c] = sum_k part[k][c] in a fixed order: 32 columns per block, warp y
+// sums the y-th eighth of the chunks in chunk order, then the eight warp
+// sums are added in warp order.  Coalesced 128-byte rows, any chunk count.
+__global__ void __launch_bounds__(256)
+    colsum_finalize_kernel(const float* __restrict__ part,
+                           float* __restrict__ out, int chunks, int cols) {
+  __shared__ float red[8][33];
+  const int tx = threadIdx.x, y = threadIdx.y;
+  const int c = blockIdx.x * 32 + tx;
+  const int per = (chunks + 7) / 8;
+  const int k0 = y * per;
+  const int k1 = min(chunks, k0 + per);
   float s = 0.f;
-  for (int k = 0; k < chunks; ++k) s += part[static_cast<size_t>(k) * cols + c];
-  out[c] = s;
+  if (c < cols) {
+#pragma unroll 4
+    for (int k = k0; k < k1; ++k) s += part[static_cast<size_t>(k) * cols + c];
+  }
+  red[y][tx] = s;
+  __syncthreads();
+  if (y == 0 && c < cols) {
+    float t = red[0][tx];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) t += red[i][tx];
+    out[c] = t;
+  }
 }
 
 // Backward of the output dropout: out = mask * scale * dZ, four columns per
@@ -386,9 +403,9 @@ cudaError_t launch_ln_param_partial(bool bf16, const float* dXn, const void* X,
 
 cudaError_t launch_colsum_finalize(const float* part, float* out, int chunks,
                                    int cols, cudaStream_t stream) {
-  const int threads = 256;
-  colsum_finalize_kernel<<<(cols + threads - 1) / threads, threads, 0,
-                           stream>>>(part, out, chunks, cols);
+  if (cols <= 0) return cudaSuccess;
+  colsum_finalize_kernel<<<(cols + 31) / 32, dim3(32, 8), 0, stream>>>(
+      part, out, chunks, cols);
   return cudaGetLastError();
 }
 

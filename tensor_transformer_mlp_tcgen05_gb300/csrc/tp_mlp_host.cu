@@ -33,14 +33,16 @@ namespace {
 struct Layout {
   size_t status = 0, xn = 0, mean = 0, rstd = 0, y = 0, h = 0, dh = 0,
          dxn = 0, dze = 0, part = 0, total = 0;
-  int chunks = 0;
+  int chunks = 0;   // 256-row column-sum chunks
+  int groups = 0;   // 32-row groups of the dH GEMM's fused db1 partials
 };
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Workspace sections, each 256-byte aligned: status word; [Xn, mean, rstd]
 // with LayerNorm; Y; and for training H, dH, [dXn fp32 with LayerNorm],
-// [the dropout-masked dZ with dropout], column-sum partials.
+// [the dropout-masked dZ with dropout], column-sum partials: db2 (chunks x h),
+// db1 (max(groups, chunks) x f), dgamma and dbeta (chunks x h each).
 Layout make_layout(const tp_mlp_config& c, int tokens, int training) {
   Layout L;
   const size_t es = c.dtype == TPMLP_BF16 ? 2 : 4;
@@ -66,7 +68,9 @@ Layout make_layout(const tp_mlp_config& c, int tokens, int training) {
     if (c.use_layernorm) L.dxn = take(T * h * 4);
     if (c.dropout_p > 0.f) L.dze = take(T * h * es);
     L.chunks = colsum_chunks(tokens);
-    L.part = take(static_cast<size_t>(L.chunks) * (f + 3 * h) * 4);
+    L.groups = (tokens + 31) / 32;
+    const size_t rows1 = static_cast<size_t>(L.groups > L.chunks ? L.groups : L.chunks);
+    L.part = take((static_cast<size_t>(L.chunks) * 3 * h + rows1 * f) * 4);
   }
   L.total = off;
   return L;
@@ -364,6 +368,7 @@ int tp_mlp_backward(tp_mlp_handle* H, int tokens, const void* dZ,
   GemmArgs gy = base_args(H, ws, L);  // dH = (dZ B^T) * GeLU'(H)
   gy.M = T; gy.N = f; gy.K = h;
   gy.out = dH; gy.ldo = f; gy.aux = Hb; gy.ldaux = f;
+  float* part1 = part + size_t(L.chunks) * h;   // db1 partials
   GemmArgs gb = base_args(H, ws, L);  // dB = Y^T dZ
   gb.M = f; gb.N = h; gb.K = T;
   gb.out = dB; gb.ldo = h;
@@ -385,12 +390,24 @@ int tp_mlp_backward(tp_mlp_handle* H, int tokens, const void* dZ,
     gy.kb_per_seg = h / TC_BK;
     TRY(kmajor_map(&ta, dZg, T, h, TC_BM));
     TRY(kmajor_map(&tb, B, f, h, b_box_rows()));
+    // db1 = sum_T dH: 32-row partials from the pair GEMM's epilogue, then
+    // one fixed-order pass over them (the one-CTA GEMM has no such
+    // epilogue: there db1 is summed from dH in memory)
+    const bool fused_db1 = dbias1 != nullptr && use_pairs();
+    if (fused_db1) {
+      gy.colsum = part1;
+      gy.ld_colsum = f;
+    }
     TRY(tc_gemm(&H->core, "gemm_dh_gelu_bwd", s, sms, EPI_GELU_BWD, false, false, ta,
                 tb, gy));
     if (dbias2) TRY(colsum(&H->core, "colsum_db2", s, true, dZg, part, dbias2, T, h));
-    if (dbias1)
-      TRY(colsum(&H->core, "colsum_db1", s, true, dH, part + size_t(L.chunks) * h,
-                 dbias1, T, f));
+    if (fused_db1) {
+      TRY(run(&H->core, "colsum_finalize", s, [&] {
+        return launch_colsum_finalize(part1, dbias1, L.groups, f, s);
+      }));
+    } else if (dbias1) {
+      TRY(colsum(&H->core, "colsum_db1", s, true, dH, part1, dbias1, T, f));
+    }
     const int kbT = (T + TC_BK - 1) / TC_BK;
     gb.kb_per_seg = kbT;
     TRY(mnmajor_map(&ta, Y, T, f));
@@ -417,8 +434,7 @@ int tp_mlp_backward(tp_mlp_handle* H, int tokens, const void* dZ,
             [&] { return launch_gemm_simt(EPI_GELU_BWD, oy, gy, s); }));
     if (dbias2) TRY(colsum(&H->core, "colsum_db2", s, false, dZg, part, dbias2, T, h));
     if (dbias1)
-      TRY(colsum(&H->core, "colsum_db1", s, false, dH, part + size_t(L.chunks) * h,
-                 dbias1, T, f));
+      TRY(colsum(&H->core, "colsum_db1", s, false, dH, part1, dbias1, T, f));
     gb.kb_per_seg = T;
     const SimtOperands ob{fY, 1, f, fdZ, h, 1};
     TRY(run(&H->core, "simt_gemm_wgrad_dB", s,
@@ -442,7 +458,7 @@ int tp_mlp_backward(tp_mlp_handle* H, int tokens, const void* dZ,
                            s);
     }));
     if (dgamma || dbeta) {
-      float* pg = part + size_t(L.chunks) * (h + f);
+      float* pg = part1 + size_t(L.groups > L.chunks ? L.groups : L.chunks) * f;
       float* pb = pg + size_t(L.chunks) * h;
       TRY(run(&H->core, "layernorm_param_partial", s, [&] {
         return launch_ln_param_partial(bf16, dXn, X, mean, rstd, pg, pb, T, h,
