@@ -383,7 +383,13 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             w[16 + i] = pack_bf16x2(__uint_as_float(r1[2 * i]),
                                     __uint_as_float(r1[2 * i + 1]));
           }
-          st.put(&tmOut, col + 64 * j, row0 + q * 32, w, lane);
+          const uint32_t buf = st.put(&tmOut, col + 64 * j, row0 + q * 32, w, lane);
+          if (a.colsum != nullptr) {     // bias-gradient partials, 32 rows
+            const float2 cs = chunk_colsum_bf16(buf, lane);
+            *reinterpret_cast<float2*>(
+                a.colsum + static_cast<size_t>((row0 + q * 32) / 32) * a.ld_colsum +
+                col + 64 * j + 2 * lane) = cs;
+          }
         }
         st.drain(lane);
       } else if constexpr (D == 128) {
@@ -408,7 +414,13 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                 fmaf(-rrow, __uint_as_float(kv[2 * i + 1]),
                      __uint_as_float(ov[2 * i + 1])));
         }
-        st.put(&tmOut, hc.q + 64 * hf, row0 + q * 32, w, lane);
+        const uint32_t buf = st.put(&tmOut, hc.q + 64 * hf, row0 + q * 32, w, lane);
+        if (a.colsum != nullptr) {
+          const float2 cs = chunk_colsum_bf16(buf, lane);
+          *reinterpret_cast<float2*>(
+              a.colsum + static_cast<size_t>((row0 + q * 32) / 32) * a.ld_colsum +
+              hc.q + 64 * hf + 2 * lane) = cs;
+        }
         st.drain(lane);
       } else {
         constexpr int OCH = D / 64;        // 32-column chunks per half

@@ -25,7 +25,8 @@ namespace {
 struct AttnLayout {
   size_t status = 0, xn = 0, mean = 0, rstd = 0, qkv = 0, ctx = 0, lse = 0,
          dctx = 0, delta = 0, dqkv = 0, dxn = 0, part = 0, total = 0;
-  int chunks = 0;
+  int chunks = 0;   // 256-row column-sum chunks
+  int groups = 0;   // 32-row groups of the core kernels' fused db_qkv partials
 };
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -56,7 +57,10 @@ AttnLayout attn_layout(const tp_attn_config& c, int tokens, int training) {
     L.dqkv = take(T * 3 * h * 2);
     if (c.use_layernorm) L.dxn = take(T * h * 4);
     L.chunks = colsum_chunks(tokens);
-    L.part = take(static_cast<size_t>(L.chunks) * 6 * h * 4);
+    L.groups = (tokens + 31) / 32;
+    // db_o (chunks x h), db_qkv (max(groups, chunks) x 3h), dgamma, dbeta
+    const size_t rows3 = static_cast<size_t>(L.groups > L.chunks ? L.groups : L.chunks);
+    L.part = take((static_cast<size_t>(L.chunks) * 3 * h + rows3 * 3 * h) * 4);
   }
   L.total = off;
   return L;
@@ -319,6 +323,14 @@ int tp_attn_backward(tp_attn_handle* H, int tokens, const void* dZ,
   TRY(encode_map(&tctx128, ctx, h, T, h, 128));
   TRY(out_map(&tdqkv_out, dqkv, false, T, 3 * h, 3LL * h));
   const int grid = (T / c.seq_len) * c.heads * aa.nq;
+  // db_qkv = sum_T dQKV: at d = 128 both kernels write 32-row partials of
+  // the chunks they stage for their TMA stores; one fixed-order pass sums them
+  float* part3 = part + size_t(L.chunks) * h;
+  const bool fused_dbqkv = dbqkv != nullptr && c.hidden / c.heads == 128;
+  if (fused_dbqkv) {
+    aa.colsum = part3;
+    aa.ld_colsum = 3LL * h;
+  }
   // the query kernel also writes delta = rowsum(dCtx * Ctx), which the
   // key/value kernel reads
   TRY(run(&H->core, "attn_bwd_dq", s, [&] {
@@ -327,9 +339,13 @@ int tp_attn_backward(tp_attn_handle* H, int tokens, const void* dZ,
   TRY(run(&H->core, "attn_bwd_dkdv", s, [&] {
     return launch_attn_dkdv(tq128, tq64, tdo64, tdqkv_out, aa, grid, s);
   }));
-  if (dbqkv)
-    TRY(colsum(&H->core, "colsum_dbqkv", s, true, dqkv,
-               part + size_t(L.chunks) * h, dbqkv, T, 3 * h));
+  if (fused_dbqkv) {
+    TRY(run(&H->core, "colsum_finalize", s, [&] {
+      return launch_colsum_finalize(part3, dbqkv, L.groups, 3 * h, s);
+    }));
+  } else if (dbqkv) {
+    TRY(colsum(&H->core, "colsum_dbqkv", s, true, dqkv, part3, dbqkv, T, 3 * h));
+  }
   // dW_qkv = Xn^T dQKV
   GemmArgs gwq = gemm_args(H, ws, L);
   gwq.M = h; gwq.N = 3 * h; gwq.K = T; gwq.kb_per_seg = kbT;
@@ -363,7 +379,7 @@ int tp_attn_backward(tp_attn_handle* H, int tokens, const void* dZ,
                            s);
     }));
     if (dgamma || dbeta) {
-      float* pg = part + size_t(L.chunks) * 4 * h;
+      float* pg = part3 + size_t(L.groups > L.chunks ? L.groups : L.chunks) * 3 * h;
       float* pb = pg + size_t(L.chunks) * h;
       TRY(run(&H->core, "layernorm_param_partial", s, [&] {
         return launch_ln_param_partial(true, dXn, X, mean, rstd, pg, pb, T, h,

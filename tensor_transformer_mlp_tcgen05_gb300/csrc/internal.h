@@ -135,6 +135,9 @@ struct AttnArgs {
                               // key/value kernel
   __nv_bfloat16* dqkv;        // backward output [T, 3h] (same layout as QKV)
   long long ld_qkv;
+  float* colsum;              // backward (nullable, d = 128): per 32-row group
+  long long ld_colsum;        // g and dQKV column c, the fp32 sum of the
+                              // stored values, at colsum[g * ld_colsum + c]
   int* status;
   unsigned long long budget_ns;
 };
