@@ -325,7 +325,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
           const int c = i + u;
           const float L = KV ? vl[c] : lse_r;
           const float Dl = KV ? vd[c] : delta_r;
-          float pv = exp2f(fmaf(__uint_as_float(s1[c]), sl2, -L));
+          float pv = ex2_approx(fmaf(__uint_as_float(s1[c]), sl2, -L));
           pv = (c >= lo && c <= hi) ? pv : 0.f;
           p[u] = pv;
           ds[u] = pv * (__uint_as_float(s2[c]) - Dl) * INV_SQRT_D;

@@ -70,6 +70,16 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem,
       : "memory");
 }
 
+// 2^x by the SFU's approximate base-2 exponential (ex2.approx.ftz.f32: the
+// hardware instruction, relative error far below bf16's half ulp; inputs here
+// are at most 8 and results that would be subnormal flush to zero, which the
+// bf16 P and the fp32 row sums never resolve anyway).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // One lane of a fully active warp (elect.sync).
 __device__ __forceinline__ bool elect_one() {
   uint32_t pred = 0;

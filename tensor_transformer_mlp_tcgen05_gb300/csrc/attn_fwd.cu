@@ -280,8 +280,10 @@ __global__ void __launch_bounds__(FWD_THREADS, 2)
         if (diag) {
 #pragma unroll
           for (int j = 0; j < 32; j += 2) {
-            float p0 = exp2f(fmaf(__uint_as_float(sv[j]), sl2, -m_ref));
-            float p1 = exp2f(fmaf(__uint_as_float(sv[j + 1]), sl2, -m_ref));
+            float p0 =
+                ex2_approx(fmaf(__uint_as_float(sv[j]), sl2, -m_ref));
+            float p1 =
+                ex2_approx(fmaf(__uint_as_float(sv[j + 1]), sl2, -m_ref));
             p0 = 32 * c + j <= lim ? p0 : 0.f;
             p1 = 32 * c + j + 1 <= lim ? p1 : 0.f;
             lb0 += p0;
@@ -291,9 +293,10 @@ __global__ void __launch_bounds__(FWD_THREADS, 2)
         } else {
 #pragma unroll
           for (int j = 0; j < 32; j += 2) {
-            const float p0 = exp2f(fmaf(__uint_as_float(sv[j]), sl2, -m_ref));
+            const float p0 =
+                ex2_approx(fmaf(__uint_as_float(sv[j]), sl2, -m_ref));
             const float p1 =
-                exp2f(fmaf(__uint_as_float(sv[j + 1]), sl2, -m_ref));
+                ex2_approx(fmaf(__uint_as_float(sv[j + 1]), sl2, -m_ref));
             lb0 += p0;
             lb1 += p1;
             w[j / 2] = pack_bf16x2(p0, p1);
