@@ -204,6 +204,15 @@ int tp_mlp_probe_mma_cycles(int n, int ctas, int n_mma,
                             unsigned long long* cycles, int* status,
                             void* stream);
 
+/* The library's device GeLU (instrumentation, not part of the block):
+ * y[i] = GeLU(x[i]) and dy[i] = GeLU'(x[i]) for n fp32 values in device
+ * memory, exactly as the GEMM epilogues evaluate them (mode
+ * TPMLP_GELU_ERF or TPMLP_GELU_TANH).  Lets tests check the epilogues' GeLU
+ * against CUDA's erf and the oracle.  TPMLP_ERR_ARG for a bad mode, n < 0 or
+ * null pointers with n > 0.  Asynchronous on `stream`. */
+int tp_mlp_probe_gelu(const float* x, float* y, float* dy, int n, int mode,
+                      void* stream);
+
 /* Bias gradient without any device allocation: dbias[c] = sum over the
  * `tokens` rows of grad[r][c], for a row-major [tokens, cols] gradient
  * (e.g. dZ, giving db2).  The pages have no counterpart for this entry

@@ -41,6 +41,7 @@ EXPORTED = (
     "tp_mlp_fp8_weights_bytes", "tp_mlp_fp8_pack_weights",
     "tp_mlp_fp8_workspace_bytes", "tp_mlp_forward_fp8", "tp_mlp_fp8_offset",
     "tp_mlp_probe_mma_cycles",
+    "tp_mlp_probe_gelu",
     "tp_attn_create", "tp_attn_destroy", "tp_attn_workspace_bytes",
     "tp_attn_forward", "tp_attn_backward", "tp_attn_check",
     "tp_attn_launch_count", "tp_attn_set_timing", "tp_attn_timing_get",
@@ -152,6 +153,8 @@ def lib(path: str | None = None) -> ctypes.CDLL:
     L.tp_mlp_fp8_offset.restype = ctypes.c_longlong
     L.tp_mlp_probe_mma_cycles.argtypes = [_i, _i, _i, _vp, _vp, _vp]
     L.tp_mlp_probe_mma_cycles.restype = _i
+    L.tp_mlp_probe_gelu.argtypes = [_vp, _vp, _vp, _i, _i, _vp]
+    L.tp_mlp_probe_gelu.restype = _i
     L.tp_attn_create.argtypes = [ctypes.POINTER(tp_attn_config),
                                  ctypes.POINTER(_vp)]
     L.tp_attn_create.restype = _i
@@ -336,6 +339,24 @@ def tp_mlp_probe_mma_cycles(n, ctas, n_mma, cycles, status, stream=None):
     _check(lib().tp_mlp_probe_mma_cycles(n, ctas, n_mma, _ptr(cycles),
                                          _ptr(status), _stream(stream)),
            "tp_mlp_probe_mma_cycles")
+
+
+def tp_mlp_probe_gelu(x, y, dy, n, mode, stream=None):
+    _check(lib().tp_mlp_probe_gelu(_ptr(x), _ptr(y), _ptr(dy), int(n),
+                                   int(mode), _stream(stream)),
+           "tp_mlp_probe_gelu")
+
+
+def device_gelu(x, mode=None):
+    """(GeLU(x), GeLU'(x)) as the library's GEMM epilogues compute them, for
+    a contiguous fp32 CUDA tensor x."""
+    import torch
+    mode = TPMLP_GELU_ERF if mode is None else mode
+    x = x.contiguous()
+    y = torch.empty_like(x)
+    dy = torch.empty_like(x)
+    tp_mlp_probe_gelu(x, y, dy, x.numel(), mode)
+    return y, dy
 
 
 def mma_flops_per_cycle(n=256, n_mma=4096, device=None):

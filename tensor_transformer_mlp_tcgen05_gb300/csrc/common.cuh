@@ -67,11 +67,49 @@ struct GemmArgs {
 enum WaitRole : int { ROLE_PRODUCER = 1, ROLE_MMA = 2, ROLE_EPILOGUE = 3 };
 
 // GeLU and its derivative in fp32.  Exact form: GeLU(x) = x Phi(x) with
-// Phi(x) = (1 + erf(x / sqrt 2)) / 2, GeLU'(x) = Phi(x) + x phi(x).  Tanh form
+// Phi the standard normal CDF, GeLU'(x) = Phi(x) + x phi(x).  Tanh form
 // (Hendrycks & Gimpel): 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))).
+//
+// Phi comes from the upper tail Q(|x|) = erfc(|x| / sqrt 2) / 2 with erfc
+// from the rational approximation of Abramowitz & Stegun, formula 7.1.26
+// (Hastings): erfc(z) = t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) exp(-z^2),
+// t = 1 / (1 + p z), z >= 0, |error| <= 1.5e-7 on erf (so <= 7.5e-8 on
+// Phi), and Phi(x) = 1 - Q(x) for x >= 0, Q(-x) otherwise.  exp(-z^2) =
+// exp(-x^2 / 2) is also phi(x) sqrt(2 pi), so GeLU' takes one exponential.
+// The reciprocal and the exponential are the SFU's approximate
+// instructions (rcp.approx, ex2.approx: relative errors near 2^-23 and
+// 2^-22), far below the bf16 rounding every GeLU output goes through.
+// tp_mlp_probe_gelu evaluates these on a device array for the tests.
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float ex2_approx_f32(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Phi(x) and exp(-x^2 / 2).
+__device__ __forceinline__ void normal_cdf_exp(float x, float& cdf, float& e) {
+  const float z = fabsf(x) * 0.70710678118654752f;          // |x| / sqrt 2
+  const float t = rcp_approx(fmaf(0.3275911f, z, 1.0f));
+  e = ex2_approx_f32(-(z * z) * 1.44269504088896341f);      // exp(-z^2)
+  float poly = fmaf(1.061405429f, t, -1.453152027f);
+  poly = fmaf(poly, t, 1.421413741f);
+  poly = fmaf(poly, t, -0.284496736f);
+  poly = fmaf(poly, t, 0.254829592f);
+  const float q = 0.5f * (poly * t) * e;                    // Q(|x|)
+  cdf = x >= 0.f ? 1.0f - q : q;
+}
+
 __device__ __forceinline__ float gelu_f32(float x, int mode) {
   if (mode == TPMLP_GELU_ERF) {
-    return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
+    float cdf, e;
+    normal_cdf_exp(x, cdf, e);
+    return x * cdf;
   }
   const float u = 0.79788456080286536f * (x + 0.044715f * x * x * x);
   return 0.5f * x * (1.0f + tanhf(u));
@@ -79,9 +117,9 @@ __device__ __forceinline__ float gelu_f32(float x, int mode) {
 
 __device__ __forceinline__ float gelu_grad_f32(float x, int mode) {
   if (mode == TPMLP_GELU_ERF) {
-    const float cdf = 0.5f * (1.0f + erff(x * 0.70710678118654752f));
-    const float pdf = 0.39894228040143268f * expf(-0.5f * x * x);
-    return cdf + x * pdf;
+    float cdf, e;
+    normal_cdf_exp(x, cdf, e);
+    return fmaf(x * 0.39894228040143268f, e, cdf);          // Phi + x phi
   }
   const float u = 0.79788456080286536f * (x + 0.044715f * x * x * x);
   const float th = tanhf(u);

@@ -97,8 +97,36 @@ cudaError_t launch_probe(int ctas, int n_mma, unsigned long long* cycles,
   return cudaGetLastError();
 }
 
+__global__ void gelu_probe_kernel(const float* __restrict__ x,
+                                  float* __restrict__ y,
+                                  float* __restrict__ dy, int n, int mode) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += gridDim.x * blockDim.x) {
+    y[i] = gelu_f32(x[i], mode);
+    dy[i] = gelu_grad_f32(x[i], mode);
+  }
+}
+
 }  // namespace
 }  // namespace tpmlp
+
+extern "C" int tp_mlp_probe_gelu(const float* x, float* y, float* dy, int n,
+                                 int mode, void* stream) {
+  using namespace tpmlp;
+  if (n < 0 || (n > 0 && (x == nullptr || y == nullptr || dy == nullptr)) ||
+      (mode != TPMLP_GELU_ERF && mode != TPMLP_GELU_TANH))
+    return TPMLP_ERR_ARG;
+  if (n == 0) return TPMLP_OK;
+  const int blocks = (n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024;
+  gelu_probe_kernel<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      x, y, dy, n, mode);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_last_detail(cudaGetErrorString(e));
+    return TPMLP_ERR_CUDA;
+  }
+  return TPMLP_OK;
+}
 
 extern "C" int tp_mlp_probe_mma_cycles(int n, int ctas, int n_mma,
                                        unsigned long long* cycles,

@@ -224,3 +224,14 @@ def test_mma_probe_rejects_bad_arguments(lib):
     assert lib.tp_mlp_probe_mma_cycles(128, 4, 102, ok, ok, None) == B.TPMLP_ERR_ARG
     assert lib.tp_mlp_probe_mma_cycles(128, 0, 100, ok, ok, None) == B.TPMLP_ERR_ARG
     assert lib.tp_mlp_probe_mma_cycles(96, 4, 100, ok, ok, None) == B.TPMLP_ERR_SHAPE
+
+
+def test_gelu_probe_rejects_bad_arguments(lib):
+    ok = ctypes.c_void_p(16)
+    assert lib.tp_mlp_probe_gelu(ok, ok, ok, 4, 7, None) == B.TPMLP_ERR_ARG
+    assert lib.tp_mlp_probe_gelu(None, ok, ok, 4, B.TPMLP_GELU_ERF,
+                                 None) == B.TPMLP_ERR_ARG
+    assert lib.tp_mlp_probe_gelu(ok, ok, ok, -1, B.TPMLP_GELU_ERF,
+                                 None) == B.TPMLP_ERR_ARG
+    assert lib.tp_mlp_probe_gelu(None, None, None, 0, B.TPMLP_GELU_ERF,
+                                 None) == B.TPMLP_OK
