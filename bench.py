@@ -55,8 +55,8 @@ DEFAULT_WORKLOAD = "gpt3_13b"
 # from full-size ncu captures, keyed by workload then kernel, with the hash of
 # the kernel sources the capture was taken on ("gemm": the pair GEMM,
 # "attn": the attention core).  Reported as null once the source has changed
-# or for a workload without a capture.  See profiles/gemm_tc2_dram_gpt3_13b.md
-# and profiles/attn_fp8_dram_gpt3_13b.md.
+# or for a workload without a capture.  The captures' commands and per-launch
+# figures are kept with the other ncu summaries under profiles/.
 _G, _A = "0f13d42e52d9fea7", "7fd4db85cf70d337"
 NCU_TRAFFIC = {
     # GPT-3-13B-shaped MLP step (T=8192, h=5120, f=20480, t=8)
