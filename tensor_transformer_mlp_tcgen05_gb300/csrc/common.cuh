@@ -79,7 +79,9 @@ enum WaitRole : int { ROLE_PRODUCER = 1, ROLE_MMA = 2, ROLE_EPILOGUE = 3 };
 // The reciprocal and the exponential are the SFU's approximate
 // instructions (rcp.approx, ex2.approx: relative errors near 2^-23 and
 // 2^-22), far below the bf16 rounding every GeLU output goes through.
-// tp_mlp_probe_gelu evaluates these on a device array for the tests.
+// The GEMM epilogues use the paired forms below (gelu2_f32, gelu_grad2_f32,
+// identical results); tp_mlp_probe_gelu evaluates those on a device array
+// for the tests.
 __device__ __forceinline__ float rcp_approx(float x) {
   float y;
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -125,6 +127,83 @@ __device__ __forceinline__ float gelu_grad_f32(float x, int mode) {
   const float th = tanhf(u);
   const float du = 0.79788456080286536f * (1.0f + 3.0f * 0.044715f * x * x);
   return 0.5f * (1.0f + th) + 0.5f * x * (1.0f - th * th) * du;
+}
+
+// The same for two values at once, with packed fp32x2 arithmetic
+// (fma/mul.rn.f32x2: two IEEE fp32 operations per instruction, results
+// identical to the scalar ones).  The factor 1/2 of Q is folded into the
+// polynomial's coefficients (an exact scaling).
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// (Phi(x0), Phi(x1)) and (exp(-x0^2/2), exp(-x1^2/2)).
+__device__ __forceinline__ void normal_cdf_exp2(float x0, float x1, float& c0,
+                                                float& c1, float& e0,
+                                                float& e1) {
+  const uint64_t z = f2_mul(f2_pack(fabsf(x0), fabsf(x1)),
+                            f2_pack(0.70710678118654752f, 0.70710678118654752f));
+  float d0, d1;
+  f2_unpack(f2_fma(z, f2_pack(0.3275911f, 0.3275911f), f2_pack(1.0f, 1.0f)),
+            d0, d1);
+  const uint64_t t = f2_pack(rcp_approx(d0), rcp_approx(d1));
+  float a0, a1;
+  f2_unpack(f2_mul(f2_mul(z, z),
+                   f2_pack(-1.44269504088896341f, -1.44269504088896341f)),
+            a0, a1);
+  e0 = ex2_approx_f32(a0);
+  e1 = ex2_approx_f32(a1);
+  // 0.5 * (a1 + t (a2 + t (a3 + t (a4 + t a5))))
+  uint64_t p = f2_fma(f2_pack(0.5307027145f, 0.5307027145f), t,
+                      f2_pack(-0.7265760135f, -0.7265760135f));
+  p = f2_fma(p, t, f2_pack(0.7107068705f, 0.7107068705f));
+  p = f2_fma(p, t, f2_pack(-0.142248368f, -0.142248368f));
+  p = f2_fma(p, t, f2_pack(0.127414796f, 0.127414796f));
+  float q0, q1;
+  f2_unpack(f2_mul(f2_mul(p, t), f2_pack(e0, e1)), q0, q1);
+  c0 = x0 >= 0.f ? 1.0f - q0 : q0;
+  c1 = x1 >= 0.f ? 1.0f - q1 : q1;
+}
+
+__device__ __forceinline__ void gelu2_f32(float& x0, float& x1, int mode) {
+  if (mode == TPMLP_GELU_ERF) {
+    float c0, c1, e0, e1;
+    normal_cdf_exp2(x0, x1, c0, c1, e0, e1);
+    f2_unpack(f2_mul(f2_pack(x0, x1), f2_pack(c0, c1)), x0, x1);
+    return;
+  }
+  x0 = gelu_f32(x0, mode);
+  x1 = gelu_f32(x1, mode);
+}
+
+// (GeLU'(x0), GeLU'(x1)).
+__device__ __forceinline__ void gelu_grad2_f32(float x0, float x1, float& g0,
+                                               float& g1, int mode) {
+  if (mode == TPMLP_GELU_ERF) {
+    float c0, c1, e0, e1;
+    normal_cdf_exp2(x0, x1, c0, c1, e0, e1);
+    const uint64_t xp = f2_mul(f2_pack(x0, x1),
+                               f2_pack(0.39894228040143268f, 0.39894228040143268f));
+    f2_unpack(f2_fma(xp, f2_pack(e0, e1), f2_pack(c0, c1)), g0, g1);
+    return;
+  }
+  g0 = gelu_grad_f32(x0, mode);
+  g1 = gelu_grad_f32(x1, mode);
 }
 
 // Philox4x32-10 (Salmon, Moraes, Dror and Shaw, SC 2011): 10 rounds; a round

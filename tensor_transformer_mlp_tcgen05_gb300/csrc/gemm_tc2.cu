@@ -407,7 +407,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                   st.put(&tmO2, c0, row0, w, lane);
                 }
 #pragma unroll
-                for (int i = 0; i < 64; ++i) v[i] = gelu_f32(v[i], args.gelu_mode);
+                for (int i = 0; i < 64; i += 2)
+                  gelu2_f32(v[i], v[i + 1], args.gelu_mode);
                 if (args.amax_out != nullptr) {
                   // largest |Y| of this warp's rows in range, as stored (bf16)
                   float mx = 0.f;
@@ -432,8 +433,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     for (int k = 0; k < 4; ++k) {
                       float h0, h1;
                       unpack_bf16x2(hw[k], h0, h1);
-                      v[8 * i + 2 * k + 0] *= gelu_grad_f32(h0, args.gelu_mode);
-                      v[8 * i + 2 * k + 1] *= gelu_grad_f32(h1, args.gelu_mode);
+                      float g0, g1;
+                      gelu_grad2_f32(h0, h1, g0, g1, args.gelu_mode);
+                      v[8 * i + 2 * k + 0] *= g0;
+                      v[8 * i + 2 * k + 1] *= g1;
                     }
                   }
                 }

@@ -100,10 +100,20 @@ cudaError_t launch_probe(int ctas, int n_mma, unsigned long long* cycles,
 __global__ void gelu_probe_kernel(const float* __restrict__ x,
                                   float* __restrict__ y,
                                   float* __restrict__ dy, int n, int mode) {
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n;
-       i += gridDim.x * blockDim.x) {
-    y[i] = gelu_f32(x[i], mode);
-    dy[i] = gelu_grad_f32(x[i], mode);
+  // pairs, as the GEMM epilogues evaluate them
+  for (int i = 2 * (blockIdx.x * blockDim.x + threadIdx.x); i < n;
+       i += 2 * gridDim.x * blockDim.x) {
+    const bool two = i + 1 < n;
+    float a = x[i], b = two ? x[i + 1] : 0.f;
+    float ga, gb;
+    gelu_grad2_f32(a, b, ga, gb, mode);
+    gelu2_f32(a, b, mode);
+    y[i] = a;
+    dy[i] = ga;
+    if (two) {
+      y[i + 1] = b;
+      dy[i + 1] = gb;
+    }
   }
 }
 
