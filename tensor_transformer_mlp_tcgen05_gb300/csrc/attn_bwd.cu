@@ -317,22 +317,29 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       ptx::tmem_ld_32x32b_x32(tmem + lane_base + 128 + 64 * st + 32 * hf, s2);
       ptx::tmem_ld_wait();
       uint32_t pw[16], dw[16];
+      // column pairs with packed fp32x2 arithmetic:
+      // P = 2^(S sl2 - L), dS = P (dP - delta) / sqrt(d)
+      const uint64_t scale = f2_pack(sl2, sl2);
+      const uint64_t inv_sqrt_d = f2_pack(INV_SQRT_D, INV_SQRT_D);
 #pragma unroll
       for (int i = 0; i < 32; i += 2) {
-        float ds[2], p[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int c = i + u;
-          const float L = KV ? vl[c] : lse_r;
-          const float Dl = KV ? vd[c] : delta_r;
-          float pv = ex2_approx(fmaf(__uint_as_float(s1[c]), sl2, -L));
-          pv = (c >= lo && c <= hi) ? pv : 0.f;
-          p[u] = pv;
-          ds[u] = pv * (__uint_as_float(s2[c]) - Dl) * INV_SQRT_D;
-        }
-        pw[i / 2] = pack_bf16x2(p[0], p[1]);
-        dw[i / 2] = pack_bf16x2(ds[0], ds[1]);
-        rsum += ds[0] + ds[1];
+        const float L0 = KV ? vl[i] : lse_r, L1 = KV ? vl[i + 1] : lse_r;
+        const float D0 = KV ? vd[i] : delta_r, D1 = KV ? vd[i + 1] : delta_r;
+        float a0, a1;
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(s1[i]), __uint_as_float(s1[i + 1])),
+                         scale, f2_pack(-L0, -L1)),
+                  a0, a1);
+        float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+        p0 = (i >= lo && i <= hi) ? p0 : 0.f;
+        p1 = (i + 1 >= lo && i + 1 <= hi) ? p1 : 0.f;
+        const uint64_t dp = f2_add(
+            f2_pack(__uint_as_float(s2[i]), __uint_as_float(s2[i + 1])),
+            f2_pack(-D0, -D1));
+        float ds0, ds1;
+        f2_unpack(f2_mul(f2_mul(f2_pack(p0, p1), dp), inv_sqrt_d), ds0, ds1);
+        pw[i / 2] = pack_bf16x2(p0, p1);
+        dw[i / 2] = pack_bf16x2(ds0, ds1);
+        rsum += ds0 + ds1;
       }
       // dS (and P) over this half's own score columns, packed two per column
       tmem_st_32x32b_x16(tmem + lane_base + 128 + 64 * st + 32 * hf, dw);

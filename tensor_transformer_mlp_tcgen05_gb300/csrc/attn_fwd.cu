@@ -277,7 +277,26 @@ __global__ void __launch_bounds__(FWD_THREADS, 2)
         ptx::tmem_ld_32x32b_x32(scol + 32 * c, sv);
         ptx::tmem_ld_wait();
         uint32_t w[16];
-        if (diag) {
+        if (!diag) {
+          // pairs of columns with packed fp32x2 arithmetic (same results as
+          // the scalar form below; lb0 / lb1 are the pair's two lanes)
+          const uint64_t scale = f2_pack(sl2, sl2);
+          const uint64_t shift = f2_pack(-m_ref, -m_ref);
+          uint64_t lb = f2_pack(lb0, lb1);
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            float a0, a1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[j]),
+                                     __uint_as_float(sv[j + 1])),
+                             scale, shift),
+                      a0, a1);
+            const float p0 = ex2_approx(a0);
+            const float p1 = ex2_approx(a1);
+            lb = f2_add(lb, f2_pack(p0, p1));
+            w[j / 2] = pack_bf16x2(p0, p1);
+          }
+          f2_unpack(lb, lb0, lb1);
+        } else {
 #pragma unroll
           for (int j = 0; j < 32; j += 2) {
             float p0 =
@@ -286,17 +305,6 @@ __global__ void __launch_bounds__(FWD_THREADS, 2)
                 ex2_approx(fmaf(__uint_as_float(sv[j + 1]), sl2, -m_ref));
             p0 = 32 * c + j <= lim ? p0 : 0.f;
             p1 = 32 * c + j + 1 <= lim ? p1 : 0.f;
-            lb0 += p0;
-            lb1 += p1;
-            w[j / 2] = pack_bf16x2(p0, p1);
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            const float p0 =
-                ex2_approx(fmaf(__uint_as_float(sv[j]), sl2, -m_ref));
-            const float p1 =
-                ex2_approx(fmaf(__uint_as_float(sv[j + 1]), sl2, -m_ref));
             lb0 += p0;
             lb1 += p1;
             w[j / 2] = pack_bf16x2(p0, p1);
