@@ -230,13 +230,14 @@ __global__ void __launch_bounds__(FWD_THREADS, 2)
             for (int j = 0; j < 32; ++j)
               if (32 * c + j <= lim) mb = fmaxf(mb, __uint_as_float(sv[j]));
           } else {
-            float m0 = __uint_as_float(sv[0]), m1 = __uint_as_float(sv[1]);
+            // two chains of three-input maxima
+            float m0 = mb, m1 = mb;
 #pragma unroll
-            for (int j = 2; j < 32; j += 2) {
-              m0 = fmaxf(m0, __uint_as_float(sv[j]));
-              m1 = fmaxf(m1, __uint_as_float(sv[j + 1]));
+            for (int j = 0; j < 32; j += 4) {
+              m0 = max3(m0, __uint_as_float(sv[j]), __uint_as_float(sv[j + 1]));
+              m1 = max3(m1, __uint_as_float(sv[j + 2]), __uint_as_float(sv[j + 3]));
             }
-            mb = fmaxf(mb, fmaxf(m0, m1));
+            mb = fmaxf(m0, m1);
           }
         }
       }
