@@ -24,26 +24,47 @@ __device__ __forceinline__ uint8_t to_e4m3(float x, float s) {
       __nv_cvt_float_to_fp8(__fdiv_rn(x, s), __NV_SATFINITE, __NV_E4M3));
 }
 
-// 8 bf16 values per thread step (one 16-byte load).
-__global__ void amax_bf16_kernel(const uint4* __restrict__ x, size_t n8,
-                                 const __nv_bfloat16* __restrict__ tail,
-                                 int ntail, unsigned int* amax) {
-  float mx = 0.f;
-  for (size_t i = blockIdx.x * size_t(QT) + threadIdx.x; i < n8;
-       i += size_t(gridDim.x) * QT) {
-    const uint4 u = x[i];
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+__device__ __forceinline__ float absmax8(const uint4 u, float mx) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      float a, b;
-      unpack_bf16x2(w[k], a, b);
-      mx = fmaxf(mx, fmaxf(fabsf(a), fabsf(b)));
-    }
+  for (int k = 0; k < 4; ++k) {
+    float a, b;
+    unpack_bf16x2(w[k], a, b);
+    mx = fmaxf(mx, fmaxf(fabsf(a), fabsf(b)));
   }
+  return mx;
+}
+
+// 8 bf16 values per 16-byte load, four independent loads in flight per
+// thread; one atomic per block after a block-wide maximum.
+__global__ void __launch_bounds__(QT)
+    amax_bf16_kernel(const uint4* __restrict__ x, size_t n8,
+                     const __nv_bfloat16* __restrict__ tail, int ntail,
+                     unsigned int* amax) {
+  __shared__ unsigned int wmax[QT / 32];
+  float mx = 0.f;
+  const size_t stride = size_t(gridDim.x) * QT;
+  size_t i = blockIdx.x * size_t(QT) + threadIdx.x;
+  for (; i + 3 * stride < n8; i += 4 * stride) {
+    const uint4 u0 = x[i], u1 = x[i + stride], u2 = x[i + 2 * stride],
+                u3 = x[i + 3 * stride];
+    mx = absmax8(u0, mx);
+    mx = absmax8(u1, mx);
+    mx = absmax8(u2, mx);
+    mx = absmax8(u3, mx);
+  }
+  for (; i < n8; i += stride) mx = absmax8(x[i], mx);
   if (blockIdx.x == 0 && threadIdx.x < ntail)
     mx = fmaxf(mx, fabsf(__bfloat162float(tail[threadIdx.x])));
   const unsigned int wm = __reduce_max_sync(0xffffffffu, __float_as_uint(mx));
-  if ((threadIdx.x & 31) == 0) atomicMax(amax, wm);
+  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = wm;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned int m = 0;
+#pragma unroll
+    for (int k = 0; k < QT / 32; ++k) m = m > wmax[k] ? m : wmax[k];
+    atomicMax(amax, m);
+  }
 }
 
 __global__ void quantize_kernel(const uint4* __restrict__ x, size_t n8,
@@ -137,7 +158,10 @@ cudaError_t launch_amax_bf16(const void* x, size_t n, unsigned int* amax,
                              cudaStream_t s) {
   const size_t n8 = n / 8;
   const int ntail = static_cast<int>(n - n8 * 8);
-  amax_bf16_kernel<<<stream_blocks(n8), QT, 0, s>>>(
+  // about eight resident blocks per SM, each thread four loads deep
+  const size_t want = (n8 + 4 * QT - 1) / (4 * QT);
+  const int blocks = static_cast<int>(want < 1216 ? (want > 0 ? want : 1) : 1216);
+  amax_bf16_kernel<<<blocks, QT, 0, s>>>(
       static_cast<const uint4*>(x), n8,
       static_cast<const __nv_bfloat16*>(x) + n8 * 8, ntail, amax);
   return cudaGetLastError();
