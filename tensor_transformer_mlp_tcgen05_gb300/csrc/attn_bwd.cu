@@ -26,10 +26,14 @@
 // over the score columns it has just read (each column-half warp inside its
 // own columns), where the output MMAs take them as A operands; their B
 // operands are the streamed tiles read M/N-major (the same bytes).
+// Outputs leave as 32-row x 64-column bf16 chunks staged in the idle B ring
+// and stored by TMA; at d = 128 each chunk is also summed over its 32 rows
+// into the partials of the QKV bias gradient.
 //
-// Warp roles as in the forward kernel: warp 0 TMA, warp 1 TMEM + MMA issue,
-// warps 4-11 elementwise (thread = row = TMEM lane, two warps per row
-// quarter, one per half of the columns).  All waits are bounded.
+// Warp roles: warp 0 TMA producer, warp 1 TMEM allocator and MMA issuer (the
+// whole warp; one elected lane issues), warps 4-11 elementwise (thread = row
+// = TMEM lane, two warps per row quarter, one per half of the columns).  All
+// waits are bounded.
 #include "attn_common.cuh"
 
 namespace tpmlp {
