@@ -67,6 +67,20 @@ __global__ void __launch_bounds__(QT)
   }
 }
 
+// Eight bf16 values (one 16-byte load) to eight E4M3 codes (8 bytes).
+__device__ __forceinline__ uint2 e4m3x8(const uint4 u, float s) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+  uint32_t o[2] = {0u, 0u};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    float a, b;
+    unpack_bf16x2(w[k], a, b);
+    const uint32_t pair = uint32_t(to_e4m3(a, s)) | (uint32_t(to_e4m3(b, s)) << 8);
+    o[k >> 1] |= pair << (16 * (k & 1));
+  }
+  return make_uint2(o[0], o[1]);
+}
+
 __global__ void quantize_kernel(const uint4* __restrict__ x, size_t n8,
                                 const __nv_bfloat16* __restrict__ tail,
                                 int ntail, const unsigned int* __restrict__ amax,
@@ -75,20 +89,15 @@ __global__ void quantize_kernel(const uint4* __restrict__ x, size_t n8,
   const float s = scale_from_amax(*amax);
   if (blockIdx.x == 0 && threadIdx.x == 0 && scale_out != nullptr)
     *scale_out = s;
-  for (size_t i = blockIdx.x * size_t(QT) + threadIdx.x; i < n8;
-       i += size_t(gridDim.x) * QT) {
-    const uint4 u = x[i];
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-    uint32_t o[2] = {0u, 0u};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      float a, b;
-      unpack_bf16x2(w[k], a, b);
-      const uint32_t pair = uint32_t(to_e4m3(a, s)) | (uint32_t(to_e4m3(b, s)) << 8);
-      o[k >> 1] |= pair << (16 * (k & 1));
-    }
-    q[i] = make_uint2(o[0], o[1]);
+  const size_t stride = size_t(gridDim.x) * QT;
+  size_t i = blockIdx.x * size_t(QT) + threadIdx.x;
+  // two independent 16-byte loads in flight per thread
+  for (; i + stride < n8; i += 2 * stride) {
+    const uint4 u0 = x[i], u1 = x[i + stride];
+    q[i] = e4m3x8(u0, s);
+    q[i + stride] = e4m3x8(u1, s);
   }
+  for (; i < n8; i += stride) q[i] = e4m3x8(x[i], s);
   if (blockIdx.x == 0 && threadIdx.x < ntail)
     qtail[threadIdx.x] = to_e4m3(__bfloat162float(tail[threadIdx.x]), s);
 }
