@@ -168,6 +168,88 @@ __global__ void __launch_bounds__(LN_WARPS * 32)
   }
 }
 
+// The backward with the row held in registers (h = 32 * VPL * V): X and dXn
+// are read once and both passes run from registers, with all of a lane's
+// loads in flight together.  Same per-lane accumulation order as
+// ln_bwd_kernel, so the same results.
+template <typename T>
+__device__ __forceinline__ void unpack_vec(const uint4 u, float (&v)[Vec<T>::N]);
+template <>
+__device__ __forceinline__ void unpack_vec<__nv_bfloat16>(const uint4 u,
+                                                          float (&v)[8]) {
+  unpack_bf16x2(u.x, v[0], v[1]);
+  unpack_bf16x2(u.y, v[2], v[3]);
+  unpack_bf16x2(u.z, v[4], v[5]);
+  unpack_bf16x2(u.w, v[6], v[7]);
+}
+template <>
+__device__ __forceinline__ void unpack_vec<float>(const uint4 u, float (&v)[4]) {
+  v[0] = __uint_as_float(u.x);
+  v[1] = __uint_as_float(u.y);
+  v[2] = __uint_as_float(u.z);
+  v[3] = __uint_as_float(u.w);
+}
+
+template <typename T, int VPL>
+__global__ void __launch_bounds__(LN_WARPS * 32)
+    ln_bwd_reg_kernel(const float* __restrict__ dXn, const T* __restrict__ X,
+                      const float* __restrict__ mean,
+                      const float* __restrict__ rstd,
+                      const float* __restrict__ gamma,
+                      const T* __restrict__ dres, T* __restrict__ dX, int rows,
+                      int h) {
+  constexpr int V = Vec<T>::N;
+  const int row = blockIdx.x * LN_WARPS + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const size_t base = static_cast<size_t>(row) * h;
+  const float mu = mean[row], rs = rstd[row];
+  const uint4* xr = reinterpret_cast<const uint4*>(X + base);
+  uint4 raw[VPL];
+  float d[VPL][V];
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) {
+    const int i = lane + 32 * j;
+    raw[j] = xr[i];
+    load_f32<V>(dXn + base + i * V, d[j]);
+  }
+  float sg = 0.f, sgx = 0.f;
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) {
+    float x[V], g[V];
+    unpack_vec<T>(raw[j], x);
+    load_f32<V>(gamma + (lane + 32 * j) * V, g);
+#pragma unroll
+    for (int k = 0; k < V; ++k) {
+      const float gg = g[k] * d[j][k];
+      sg += gg;
+      sgx += gg * (x[k] - mu) * rs;
+    }
+  }
+  const float inv_h = 1.0f / static_cast<float>(h);
+  const float c_g = warp_sum(sg) * inv_h;
+  const float c_gx = warp_sum(sgx) * inv_h;
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) {
+    const int i = lane + 32 * j;
+    float x[V], g[V], o[V];
+    unpack_vec<T>(raw[j], x);
+    load_f32<V>(gamma + i * V, g);
+#pragma unroll
+    for (int k = 0; k < V; ++k) {
+      const float xhat = (x[k] - mu) * rs;
+      o[k] = rs * (g[k] * d[j][k] - c_g - xhat * c_gx);
+    }
+    if (dres != nullptr) {
+      float r[V];
+      Vec<T>::load(dres + base + i * V, r);
+#pragma unroll
+      for (int k = 0; k < V; ++k) o[k] += r[k];
+    }
+    Vec<T>::store(dX + base + i * V, o);
+  }
+}
+
 // ------------------------------------------------------- column sums --
 
 constexpr int CS_WARPS = 8;
@@ -356,7 +438,22 @@ cudaError_t launch_ln_bwd(bool bf16, const float* dXn, const void* X,
                           const float* gamma, const void* dres, void* dX,
                           int rows, int h, cudaStream_t stream) {
   const int grid = (rows + LN_WARPS - 1) / LN_WARPS;
-  if (bf16) {
+  const int nv = h / (bf16 ? 8 : 4);
+  const int vpl = nv % 32 == 0 ? nv / 32 : 0;
+#define TPMLP_LN_BWD_REG(TY, N)                                              \
+  ln_bwd_reg_kernel<TY, N><<<grid, LN_WARPS * 32, 0, stream>>>(             \
+      dXn, static_cast<const TY*>(X), mean, rstd, gamma,                    \
+      static_cast<const TY*>(dres), static_cast<TY*>(dX), rows, h)
+  if (bf16 && (vpl == 4 || vpl == 8 || vpl == 12)) {
+    if (vpl == 4) TPMLP_LN_BWD_REG(__nv_bfloat16, 4);
+    else if (vpl == 8) TPMLP_LN_BWD_REG(__nv_bfloat16, 8);
+    else TPMLP_LN_BWD_REG(__nv_bfloat16, 12);
+  } else if (!bf16 && (vpl == 4 || vpl == 8 || vpl == 12)) {
+    if (vpl == 4) TPMLP_LN_BWD_REG(float, 4);
+    else if (vpl == 8) TPMLP_LN_BWD_REG(float, 8);
+    else TPMLP_LN_BWD_REG(float, 12);
+  } else if (bf16) {
+#undef TPMLP_LN_BWD_REG
     ln_bwd_kernel<__nv_bfloat16><<<grid, LN_WARPS * 32, 0, stream>>>(
         dXn, static_cast<const __nv_bfloat16*>(X), mean, rstd, gamma,
         static_cast<const __nv_bfloat16*>(dres),
