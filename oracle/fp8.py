@@ -30,7 +30,7 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from .mlp import gelu, layernorm_forward
+from .mlp import gelu, gelu_grad, layernorm_backward, layernorm_forward
 
 E4M3_MAX = 448.0
 _MIN_NORMAL = 2.0 ** -6
@@ -111,8 +111,9 @@ def forward(X, A, B, b1=None, b2=None, gamma=None, beta=None, eps=1e-5,
     Returns the codes and scales of every quantized operand, Y (bf16
     values) and Z (before its final bf16 rounding)."""
     X = np.asarray(X, dtype=np.float64)
+    mean = rstd = None
     if gamma is not None:
-        Xn, _, _ = layernorm_forward(X, gamma, beta, eps)
+        Xn, mean, rstd = layernorm_forward(X, gamma, beta, eps)
         Xn = to_bf16(Xn)
     else:
         Xn = X
@@ -129,5 +130,45 @@ def forward(X, A, B, b1=None, b2=None, gamma=None, beta=None, eps=1e-5,
         Z = Z + np.asarray(b2, dtype=np.float64)[None, :]
     if residual:
         Z = Z + X
-    return dict(Xn=Xn, qx=qx, sx=sx, qa=qa, sa=sa, qb=qb, sb=sb, H=H, Y=Y,
-                qy=qy, sy=sy, Z=Z)
+    return dict(Xn=Xn, mean=mean, rstd=rstd, qx=qx, sx=sx, qa=qa, sa=sa,
+                qb=qb, sb=sb, H=H, Y=Y, qy=qy, sy=sy, Z=Z)
+
+
+def backward(dZ, X, fwd, gamma=None, mode="erf", residual=False):
+    """The FP8 (E4M3) backward of ``forward``, every GEMM on codes with
+    per-tensor current scaling as in the forward (E4M3 for the gradients
+    too; the pages name no gradient format):
+
+    * dZ is quantized (codes qdz, scale sdz); db2 = sum_T dZ;
+    * dY = (sdz sb) (dZq . Bq^T); dH = dY * GeLU'(H) with H as stored
+      (bf16), rounded to bf16; db1 = sum_T dH (of the bf16 values);
+    * dH is quantized (qdh, sdh);
+    * dXn = (sdh sa) (dHq . Aq^T), then LayerNorm's backward (with the
+      forward's statistics) or dXn itself, plus dZ with the residual;
+    * dA = (sx sdh) (Xq^T . dHq), dB = (sy sdz) (Yq^T . dZq), fp32 results.
+
+    Each scale product is rounded to fp32, as in the forward.  Returns the
+    gradients and the codes and scales of dZ and dH."""
+    dZ = np.asarray(dZ, dtype=np.float64)
+    X = np.asarray(X, dtype=np.float64)
+    qdz, sdz = quantize(dZ)
+    db2 = dZ.sum(axis=0)
+    Hb = to_bf16(fwd["H"])
+    dY = quantized_matmul(qdz, sdz, fwd["qb"].T, fwd["sb"])
+    dH = to_bf16(dY * gelu_grad(Hb, mode))
+    db1 = dH.sum(axis=0)
+    qdh, sdh = quantize(dH)
+    dXn = quantized_matmul(qdh, sdh, fwd["qa"].T, fwd["sa"])
+    dA = quantized_matmul(fwd["qx"].T, fwd["sx"], qdh, sdh)
+    dB = quantized_matmul(fwd["qy"].T, fwd["sy"], qdz, sdz)
+    dgamma = dbeta = None
+    if gamma is not None:
+        dX, dgamma, dbeta = layernorm_backward(dXn, X, fwd["mean"],
+                                               fwd["rstd"], gamma)
+    else:
+        dX = dXn
+    if residual:
+        dX = dX + dZ
+    return dict(dX=dX, dXn=dXn, dA=dA, dB=dB, db1=db1, db2=db2, dH=dH,
+                qdz=qdz, sdz=sdz, qdh=qdh, sdh=sdh, dgamma=dgamma,
+                dbeta=dbeta)

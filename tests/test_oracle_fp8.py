@@ -1,7 +1,7 @@
 """Pins for the FP8 (E4M3) oracle: the format's closed-form values, every
 bf16 bit pattern against PyTorch's float8_e4m3fn conversion, saturation,
-round trips, scale invariance, exactness on representable inputs and the
-plain block forward when quantization loses nothing.  No GPU."""
+round trips, scale invariance, exactness on representable inputs, and the
+plain block forward and backward when quantization loses nothing.  No GPU."""
 import numpy as np
 import pytest
 import torch
@@ -129,3 +129,89 @@ def test_forward_close_to_the_unquantized_block(ln, res):
     ref = O.forward(X, A, B, gamma=g, beta=bt, residual=res)["Z"]
     rel = np.linalg.norm(f["Z"] - ref) / np.linalg.norm(ref)
     assert rel < 0.1, rel
+
+
+def _e4m3_values(rng, shape, lo=0, hi=0x7E):
+    return F.e4m3_decode(rng.integers(lo, hi, shape).astype(np.uint8))
+
+
+def test_backward_equals_the_plain_backward_when_quantization_is_lossless():
+    """A construction where every quantization step loses nothing: X and A
+    hold E4M3 values (scales 1/64 and 1/256), B holds E4M3 values with
+    max |B| = 448 (scale 1), b1 = 20 makes H >= 20 so that GeLU'(H) = 1
+    exactly in fp64, and each row of dZ is one-hot with 448 (scale 1).  Then
+    dY = dZ B^T = 448 B[:, c(r)]^T, s_dh = 448 and dH / s_dh are B's own
+    E4M3 values, so dXn, dA, db1 and db2 must equal the unquantized backward
+    of the same block (up to fp64 rounding) — a swapped operand, a wrong
+    transpose or a scale taken from the wrong tensor breaks the equality."""
+    rng = np.random.default_rng(11)
+    T, h, f = 16, 32, 64
+    X = _e4m3_values(rng, (T, h)) / 64
+    X[0, 0] = 448 / 64
+    A = _e4m3_values(rng, (h, f)) / 256
+    A[0, 0] = 448 / 256
+    B = F.e4m3_decode(rng.integers(0, 0xFF, (f, h)).astype(np.uint8))
+    B = np.where(np.isnan(B), 0.0, B)
+    B[0, 0] = 448.0
+    b1 = np.full(f, 20.0)
+    dZ = np.zeros((T, h))
+    cols = rng.integers(0, h, T)
+    cols[0] = 0
+    dZ[np.arange(T), cols] = 448.0
+    fwd = F.forward(X, A, B, b1=b1)
+    bwd = F.backward(dZ, X, fwd)
+    assert bwd["sdz"] == 1.0
+    plain = O.backward(dZ, X, A, B, O.forward(X, A, B, b1=b1))
+    np.testing.assert_array_equal(O.gelu_grad(F.to_bf16(fwd["H"])), 1.0)
+    # dH is representable in bf16 too (448 x E4M3 values), so rounding is exact
+    np.testing.assert_allclose(bwd["dH"], plain["dH"], rtol=0, atol=0)
+    np.testing.assert_array_equal(F.e4m3_decode(bwd["qdh"]) * bwd["sdh"],
+                                  bwd["dH"])
+    for k in ("dXn", "dA", "db1", "db2"):
+        np.testing.assert_allclose(bwd[k], plain[k], rtol=1e-13, atol=1e-9,
+                                   err_msg=k)
+
+
+def test_backward_weight_gradient_dB_exact_when_Y_is_lossless():
+    """dB = Yq^T dZq: with A = 0 (scale 1, codes 0), H = b1, chosen from the
+    E4M3 values 16..28 (so that GeLU(H) = H to bf16 and Y / s_y = 16 b1 are
+    E4M3 numbers), and dZ one-hot with 448, Y and dZ quantize losslessly and
+    dB equals Y^T dZ of the plain block."""
+    rng = np.random.default_rng(12)
+    T, h, f = 24, 32, 48
+    X = _e4m3_values(rng, (T, h)) / 64
+    A = np.zeros((h, f))
+    B = _e4m3_values(rng, (f, h)) / 256
+    b1 = rng.choice([16.0, 18.0, 20.0, 22.0, 24.0, 26.0], f)
+    b1[0] = 28.0
+    dZ = np.zeros((T, h))
+    dZ[np.arange(T), rng.integers(0, h, T)] = rng.choice([-448.0, 448.0], T)
+    fwd = F.forward(X, A, B, b1=b1)
+    np.testing.assert_array_equal(fwd["Y"], np.broadcast_to(b1, (T, f)))
+    bwd = F.backward(dZ, X, fwd)
+    plain = O.backward(dZ, X, A, B, O.forward(X, A, B, b1=b1))
+    np.testing.assert_allclose(bwd["dB"], plain["dB"], rtol=1e-13, atol=1e-9)
+    np.testing.assert_allclose(bwd["db2"], plain["db2"], rtol=0, atol=0)
+    # A = 0: dXn is exactly zero on both sides
+    np.testing.assert_array_equal(bwd["dXn"], 0.0)
+
+
+@pytest.mark.parametrize("ln,res", [(False, False), (True, True)])
+def test_backward_close_to_the_unquantized_block(ln, res):
+    """E4M3 gradients: within ~15 % (relative Frobenius) of the fp64 block's
+    gradients on Gaussian data, and the LayerNorm / residual paths wired
+    like the plain backward's."""
+    rng = np.random.default_rng(13)
+    X = rng.standard_normal((64, 128))
+    A = rng.standard_normal((128, 512)) * 0.05
+    B = rng.standard_normal((512, 128)) * 0.05
+    dZ = rng.standard_normal((64, 128))
+    g = (1 + 0.1 * rng.standard_normal(128)) if ln else None
+    bt = (0.1 * rng.standard_normal(128)) if ln else None
+    fwd = F.forward(X, A, B, gamma=g, beta=bt, residual=res)
+    bwd = F.backward(dZ, X, fwd, gamma=g, residual=res)
+    pf = O.forward(X, A, B, gamma=g, beta=bt, residual=res)
+    pb = O.backward(dZ, X, A, B, pf, gamma=g, residual=res)
+    for k in ("dX", "dA", "dB", "db1", "db2") + (("dgamma", "dbeta") if ln else ()):
+        rel = np.linalg.norm(bwd[k] - pb[k]) / np.linalg.norm(pb[k])
+        assert rel < 0.15, (k, rel)
