@@ -21,6 +21,8 @@ projections plus 12 d per unmasked (query, key) pair for the attention core.
 ``--fp8`` times the FP8 (E4M3) forward of an MLP workload instead (weights
 quantized once before timing; per step: quantize Xn, GEMM1 + GeLU, quantize
 Y, GEMM2 + shard sum; 4 T h f flops), against twice the measured bf16 peak.
+``--fp8 --train`` times the FP8 training step (that forward keeping what the
+backward needs, then the FP8 backward; 12 T h f flops).
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the fp64 CPU
 oracle on a bounded token slice of the same workload instead.  With
@@ -47,6 +49,8 @@ if ROOT not in sys.path:
 METRIC = "TP-MLP fwd+bwd TFLOP/s and tokens/s on 1 GB300, % of dense bf16 peak"
 METRIC_FP8 = ("TP-MLP FP8 (E4M3) forward TFLOP/s and tokens/s on 1 GB300, "
               "% of dense fp8 peak")
+METRIC_FP8_TRAIN = ("TP-MLP FP8 (E4M3) fwd+bwd TFLOP/s and tokens/s on 1 "
+                    "GB300, % of dense fp8 peak")
 METRIC_ATTN = ("TP-attention fwd+bwd TFLOP/s and tokens/s on 1 GB300, "
                "% of dense bf16 peak")
 DEFAULT_WORKLOAD = "gpt3_13b"
@@ -786,8 +790,12 @@ def run_reference_attn(args, w):
 def run_ours_fp8(args, w, rank, world, local_rank):
     """FP8 (E4M3) forward of an MLP workload: one step = quantize Xn, GEMM1
     + GeLU (+ amax of Y), quantize Y, GEMM2 + shard sum; the weights are
-    packed once before timing.  The bf16 forward of the same workload is
-    timed alongside for context."""
+    packed once before timing.  With --train a step is the FP8 training
+    step: that forward keeping H and the transposed codes, then the FP8
+    backward (quantize dZ, dH GEMM + GeLU' + amax + db1 partials, quantize
+    dH, db2 and db1 sums, dB and dA GEMMs, dX GEMM + shard sum [+ LayerNorm
+    backward]).  The bf16 pass of the same workload is timed alongside for
+    context."""
     import torch
     from tensor_transformer_mlp_tcgen05_gb300 import binding as Bn
     from tensor_transformer_mlp_tcgen05_gb300 import workloads as W
@@ -795,7 +803,8 @@ def run_ours_fp8(args, w, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    inp = W.make_inputs(w, seed=0, need_grad_input=False)
+    train = bool(args.train)
+    inp = W.make_inputs(w, seed=0, need_grad_input=train)
     d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
     m = TensorParallelMLP(w.hidden, w.ffn, w.shards, w.tokens, dtype="bf16",
                           layernorm=w.layernorm, residual=args.residual)
@@ -803,21 +812,31 @@ def run_ours_fp8(args, w, rank, world, local_rank):
     stream = torch.cuda.current_stream()
     T = w.tokens
     Z = torch.empty((T, w.hidden), dtype=torch.bfloat16, device=dev)
+    grads = {}
 
-    def step(Xd=None):
-        m.forward_fp8(d["X"] if Xd is None else Xd, packed, d["b1"], d["b2"],
-                      d["gamma"], d["beta"], out=Z)
+    def step(Xd=None, dZd=None, Zd=None, dXd=None):
+        Xd = d["X"] if Xd is None else Xd
+        m.forward_fp8(Xd, packed, d["b1"], d["b2"], d["gamma"], d["beta"],
+                      out=Z if Zd is None else Zd, train=train)
+        if train:
+            g = grads if dXd is None else {**grads, "dX": dXd}
+            m.backward_fp8(d["dZ"] if dZd is None else dZd, Xd, packed,
+                           d["gamma"], bias_grads=True, grads=g)
 
     for _ in range(args.warmup):
         step()
     if m.check() != 0:
         raise RuntimeError("device status after warm-up: "
                            + Bn.tp_mlp_last_detail())
+    if train:  # keep the gradient buffers from here on
+        grads.update(m.backward_fp8(d["dZ"], d["X"], packed, d["gamma"],
+                                    bias_grads=True))
     torch.cuda.synchronize()
-    snap = Z.clone()
+    snap = {"Z": Z.clone(), **{k: v.clone() for k, v in grads.items()}}
     step()
     torch.cuda.synchronize()
-    identical = torch.equal(snap, Z)
+    identical = all(torch.equal(snap[k], Z if k == "Z" else grads[k])
+                    for k in snap)
 
     def timed(fn, n):
         e0 = torch.cuda.Event(enable_timing=True)
@@ -847,10 +866,15 @@ def run_ours_fp8(args, w, rank, world, local_rank):
     Bn.tp_mlp_set_timing(m.handle, False)
     ms_max = max_over_ranks(ms, world)
 
-    # the bf16 forward of the same workload, for context
+    # the bf16 pass of the same workload, for context
+    bgrads = {}
+
     def step_bf16():
         m.forward(d["X"], d["A"], d["B"], d["b1"], d["b2"], d["gamma"],
-                  d["beta"], training=False, out=Z)
+                  d["beta"], training=train, out=Z)
+        if train:
+            m.backward(d["dZ"], d["X"], d["A"], d["B"], d["gamma"],
+                       bias_grads=True, out=bgrads)
     for _ in range(3):
         step_bf16()
     bf16_ms = timed(step_bf16, args.steps)
@@ -858,11 +882,18 @@ def run_ours_fp8(args, w, rank, world, local_rank):
     hX = inp["X"].pin_memory()
     hZ = torch.empty_like(inp["X"]).pin_memory()
     Xd = torch.empty_like(d["X"])
+    hdZ = inp["dZ"].pin_memory() if train else None
+    hdX = torch.empty_like(inp["X"]).pin_memory() if train else None
+    dZd = torch.empty_like(d["X"]) if train else None
 
     def e2e_step():
         Xd.copy_(hX, non_blocking=True)
-        step(Xd)
+        if train:
+            dZd.copy_(hdZ, non_blocking=True)
+        step(Xd, dZd)
         hZ.copy_(Z, non_blocking=True)
+        if train:
+            hdX.copy_(grads["dX"], non_blocking=True)
 
     for _ in range(2):
         e2e_step()
@@ -870,23 +901,26 @@ def run_ours_fp8(args, w, rank, world, local_rank):
     barrier(world)
     e2e_serial_ms = max_over_ranks(timed(e2e_step, args.steps), world)
 
-    d_in = [[torch.empty_like(d["X"])] for _ in range(2)]
-    d_out = [[torch.empty_like(Z)] for _ in range(2)]
+    nio = 2 if train else 1
+    d_in = [[torch.empty_like(d["X"]) for _ in range(nio)] for _ in range(2)]
+    d_out = [[torch.empty_like(Z) for _ in range(nio)] for _ in range(2)]
+    h_in = [hX] + ([hdZ] if train else [])
+    h_out = [hZ] + ([hdX] if train else [])
 
     def compute(k):
-        m.forward_fp8(d_in[k][0], packed, d["b1"], d["b2"], d["gamma"],
-                      d["beta"], out=d_out[k][0])
+        step(d_in[k][0], d_in[k][1] if train else None, d_out[k][0],
+             d_out[k][1] if train else None)
 
-    e2e_overlapped(torch, stream, 2, [hX], [hZ], d_in, d_out, compute)
+    e2e_overlapped(torch, stream, 2, h_in, h_out, d_in, d_out, compute)
     barrier(world)
     e2e_ms = max_over_ranks(
-        e2e_overlapped(torch, stream, args.steps, [hX], [hZ], d_in, d_out,
+        e2e_overlapped(torch, stream, args.steps, h_in, h_out, d_in, d_out,
                        compute), world)
     if m.check() != 0:
         raise RuntimeError("device status after the end-to-end runs: "
                            + Bn.tp_mlp_last_detail())
 
-    flops = w.flops_fwd()
+    flops = w.flops_fwd_bwd() if train else w.flops_fwd()
     peak_b, peak_s, hbm, peak_src = _peaks()
     fp8_burst, fp8_sust = 2 * peak_b, 2 * peak_s
     tflops = world * flops / (ms_max * 1e-3) / 1e12
@@ -895,7 +929,9 @@ def run_ours_fp8(args, w, rank, world, local_rank):
              "share": round(t / total_ms, 4)} for n, c, t in kernels]
     krep.sort(key=lambda r: -r["share"])
     gemm = 2.0 * w.tokens * w.hidden * w.ffn
-    kf = {"gemm1_gelu_fp8": gemm, "gemm2_shardsum_fp8": gemm}
+    kf = {k: gemm for k in ("gemm1_gelu_fp8", "gemm2_shardsum_fp8",
+                            "gemm_dh_gelu_bwd_fp8", "gemm_wgrad_dB_fp8",
+                            "gemm_wgrad_dA_fp8", "gemm_dx_shardsum_fp8")}
     for r in krep:
         if r["name"] in kf:
             r["tflops"] = round(kf[r["name"]] / (r["avg_ms"] * 1e-3) / 1e12, 1)
@@ -910,9 +946,11 @@ def run_ours_fp8(args, w, rank, world, local_rank):
                 "peak_kind": f"fp8 = 2 x measured bf16 {pkind} ({peak_src}; "
                              "nominal fp8:bf16 ratio 4.5:2.25)",
                 "traffic": traffic_of(w.name + "_fp8", top["name"])
-                if not (args.tokens or args.shards or args.residual) else None}
+                if not (args.tokens or args.shards or args.residual or train)
+                else None}
     line = {
-        "metric": METRIC_FP8, "value": round(tflops, 2), "unit": "TFLOP/s",
+        "metric": METRIC_FP8_TRAIN if train else METRIC_FP8,
+        "value": round(tflops, 2), "unit": "TFLOP/s",
         "tokens_per_s": round(world * T / (ms_max * 1e-3), 1),
         "frac_of_peak": round(tflops / (world * fp8_burst), 4),
         "peak_tflops": fp8_burst, "peak_kind": "fp8 (2 x measured bf16 burst)",
@@ -920,21 +958,27 @@ def run_ours_fp8(args, w, rank, world, local_rank):
         "ms_per_step": round(ms_max, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
         "data": "synthetic: seeded N(0,1) activations, "
-                f"N(0,{w.w_std}^2) weights; weights quantized once before "
-                "timing, activations quantized every step",
+                f"N(0,{w.w_std}^2) weights"
+                + (f", N(0,{w.dz_std}^2) output gradients" if train else "")
+                + "; weights quantized once before timing, activations "
+                + ("and gradients " if train else "") + "quantized every step",
         "config": {"workload": w.name, "tokens": T, "batch": w.batch,
                    "seq": w.seq, "hidden": w.hidden, "ffn": w.ffn,
                    "shards": w.shards, "layernorm": w.layernorm,
-                   "residual": bool(args.residual), "pass": "fwd (fp8)",
+                   "residual": bool(args.residual),
+                   "pass": "fwd+bwd (fp8)" if train else "fwd (fp8)",
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "l2": "inputs larger than L2 (no flush)"},
-        "bf16_forward": {"ms_per_step": round(bf16_ms, 4),
+        ("bf16_train_step" if train else "bf16_forward"): {
+                         "ms_per_step": round(bf16_ms, 4),
                          "value": round(flops / (bf16_ms * 1e-3) / 1e12, 2),
                          "unit": "TFLOP/s"},
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2),
                 "unit": "TFLOP/s", "ms_per_step": round(e2e_ms, 4),
-                "h2d_bytes_per_step": hX.numel() * hX.element_size(),
-                "d2h_bytes_per_step": hZ.numel() * hZ.element_size(),
+                "h2d_bytes_per_step": sum(t.numel() * t.element_size()
+                                          for t in h_in),
+                "d2h_bytes_per_step": sum(t.numel() * t.element_size()
+                                          for t in h_out),
                 "copies": "overlapped with the compute (side streams, two "
                           "buffer slots)",
                 "serial_value": round(world * flops / (e2e_serial_ms * 1e-3)
@@ -950,23 +994,27 @@ def run_ours_fp8(args, w, rank, world, local_rank):
     return line, inp
 
 
-def run_cpu_baseline_fp8(w, inp):
-    """The fp64 FP8 oracle's forward on a bounded token slice."""
+def run_cpu_baseline_fp8(w, inp, train=False):
+    """The fp64 FP8 oracle's forward (and, with train, backward) on a
+    bounded token slice."""
     from oracle import fp8 as OF
     # the weights' quantization (2 h f elements) is a fixed cost of about
     # 15 s per GPT-3-13B-sized matrix; the token slice adds little to it
     tokens = int(max(16, min(w.tokens, 0.1e12 / (4.0 * w.hidden * w.ffn))))
     f = lambda t: None if t is None else t.double().numpy()
+    X = f(inp["X"][:tokens])
     t0 = time.perf_counter()
-    OF.forward(f(inp["X"][:tokens]), f(inp["A"]), f(inp["B"]), f(inp["b1"]),
-               f(inp["b2"]), f(inp["gamma"]), f(inp["beta"]))
+    fwd = OF.forward(X, f(inp["A"]), f(inp["B"]), f(inp["b1"]), f(inp["b2"]),
+                     f(inp["gamma"]), f(inp["beta"]))
+    if train:
+        OF.backward(f(inp["dZ"][:tokens]), X, fwd, f(inp["gamma"]))
     secs = time.perf_counter() - t0
-    flops = w.flops_fwd(tokens)
+    flops = w.flops_fwd_bwd(tokens) if train else w.flops_fwd(tokens)
+    what = "forward + backward" if train else "forward"
     return {"value": round(flops / secs / 1e12, 5), "unit": "TFLOP/s",
             "cores": os.cpu_count(), "kind": "oracle",
             "sample": f"first {tokens} of {w.tokens} tokens, fp64 FP8 "
-                      f"forward incl. weight quantization ({secs:.1f} s)"}
-
+                      f"{what} incl. weight quantization ({secs:.1f} s)"}
 
 
 def run_cpu_baseline(w, inp):
@@ -1072,6 +1120,9 @@ def main(argv=None):
                     help="time the residual sub-block X + MLP(LN(X))")
     ap.add_argument("--fp8", action="store_true",
                     help="time the FP8 (E4M3) forward of an MLP workload")
+    ap.add_argument("--train", action="store_true",
+                    help="with --fp8: time the FP8 training step (forward "
+                         "+ backward) instead")
     ap.add_argument("--sweep", action="store_true",
                     help="token x shard sweep of the workload (one line per "
                          "point) instead of the headline measurement")
@@ -1101,6 +1152,9 @@ def main(argv=None):
         return 0
     if attn and (args.sweep or args.fp8):
         ap.error("--sweep and --fp8 are for the MLP workloads")
+    if args.train and not args.fp8:
+        ap.error("--train goes with --fp8 (the bf16 workloads set their "
+                 "own pass)")
 
     if args.sweep:
         from tensor_transformer_mlp_tcgen05_gb300 import build as b
@@ -1125,7 +1179,7 @@ def main(argv=None):
         if attn:
             line["cpu_baseline"] = run_cpu_baseline_attn(w, inp)
         elif args.fp8:
-            line["cpu_baseline"] = run_cpu_baseline_fp8(w, inp)
+            line["cpu_baseline"] = run_cpu_baseline_fp8(w, inp, args.train)
         else:
             line["cpu_baseline"] = run_cpu_baseline(w, inp)
     if rank == 0:

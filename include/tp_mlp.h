@@ -149,7 +149,7 @@ int tp_mlp_backward(tp_mlp_handle* handle, int tokens, const void* dZ,
                     float* dbias1, float* dbias2, float* dgamma, float* dbeta,
                     void* stream);
 
-/* ---- FP8 (E4M3) forward variant ----------------------------------------
+/* ---- FP8 (E4M3) variant: forward and backward --------------------------
  * The block's forward with both GEMMs on 8-bit E4M3 operands (the
  * low-precision runs of the Megatron Core determinism article, read as
  * plain per-tensor FP8): every operand tensor T (Xn, A, B and Y) is scaled
@@ -159,12 +159,13 @@ int tp_mlp_backward(tp_mlp_handle* handle, int tokens, const void* dZ,
  * Y = GeLU(H) stored bf16 and quantized with its own current amax, Z =
  * sum_i (s_y s_b) (Yq_i Bq_i) + b2 [+ X] in fixed shard order, one bf16
  * rounding.  The handle must be TPMLP_BF16 without dropout, and f / t must
- * be a multiple of 128 (TPMLP_ERR_ARG / TPMLP_ERR_SHAPE otherwise); there
- * is no FP8 backward.  The weights are quantized once by
- * tp_mlp_fp8_pack_weights into a caller-owned buffer of
- * tp_mlp_fp8_weights_bytes bytes (layout: amax_a, amax_b as fp32 bits and
- * s_a, s_b as fp32, then A^T codes [f, h] and B^T codes [h, f], each
- * section 256-byte aligned); the forward quantizes Xn and Y itself. */
+ * be a multiple of 128 (TPMLP_ERR_ARG / TPMLP_ERR_SHAPE otherwise).  The
+ * weights are quantized once by tp_mlp_fp8_pack_weights into a
+ * caller-owned buffer of tp_mlp_fp8_weights_bytes bytes (layout: amax_a,
+ * amax_b as fp32 bits and s_a, s_b as fp32, then A^T codes [f, h], B^T
+ * codes [h, f], A codes [h, f] and B codes [f, h], each section 256-byte
+ * aligned: the forward reads the transposed codes, the backward the plain
+ * ones); the forward quantizes Xn and Y itself. */
 size_t tp_mlp_fp8_weights_bytes(const tp_mlp_handle* handle);
 int tp_mlp_fp8_pack_weights(tp_mlp_handle* handle, const void* A,
                             const void* B, void* packed, size_t packed_bytes,
@@ -178,8 +179,46 @@ int tp_mlp_forward_fp8(tp_mlp_handle* handle, int tokens, const void* X,
                        const float* bias2, const float* ln_gamma,
                        const float* ln_beta, void* Z, void* workspace,
                        size_t workspace_bytes, void* stream);
-/* Byte offsets of the packed-weight sections and of the forward's
- * workspace sections (for inspection by tests); -1 if unknown. */
+/* Training step in FP8.  The backward uses E4M3 for the gradients too,
+ * with the same per-tensor current scaling (the determinism article names
+ * no gradient format; this is the plain reading):
+ *   dZq = e4m3(dZ / s_dz);  db2 = sum_T dZ;
+ *   dH = bf16((s_dz s_b) (dZq Bq^T) * GeLU'(H)) with H as the training
+ *     forward stored it (bf16);  db1 = sum_T dH;  dHq = e4m3(dH / s_dh);
+ *   dXn = sum_i (s_dh s_a) (dHq_i Aq_i^T) in fixed shard order (fp32),
+ *     then LayerNorm's backward with the forward's statistics, or dXn
+ *     itself; + dZ with the residual; dX rounded to bf16 once;
+ *   dA = (s_x s_dh) (Xq^T dHq), dB = (s_y s_dz) (Yq^T dZq), fp32.
+ * Every scale product is rounded to fp32.  Bias and LayerNorm-parameter
+ * sums run in fixed order (bitwise reproducible), as in tp_mlp_backward.
+ *
+ * tp_mlp_forward_fp8_train is tp_mlp_forward_fp8 that also keeps what the
+ * backward needs in its workspace (H bf16, Xq^T and Yq^T codes); its
+ * workspace has tp_mlp_fp8_train_workspace_bytes bytes (the sections of
+ * the plain forward at the same offsets, then the training sections) and
+ * must be passed, unchanged, to tp_mlp_backward_fp8 with the same tokens,
+ * X and packed weights.  tp_mlp_backward_fp8 arguments as tp_mlp_backward
+ * (dZ, X, dX bf16 [T,h]; dA [h,f], dB [f,h] and the nullable bias and
+ * LayerNorm-parameter gradients fp32, all overwritten); with T = 0 the
+ * weight and bias gradients are set to zero.  Errors as the forward. */
+size_t tp_mlp_fp8_train_workspace_bytes(const tp_mlp_handle* handle,
+                                        int tokens);
+int tp_mlp_forward_fp8_train(tp_mlp_handle* handle, int tokens,
+                             const void* X, const void* packed,
+                             const float* bias1, const float* bias2,
+                             const float* ln_gamma, const float* ln_beta,
+                             void* Z, void* workspace, size_t workspace_bytes,
+                             void* stream);
+int tp_mlp_backward_fp8(tp_mlp_handle* handle, int tokens, const void* dZ,
+                        const void* X, const void* packed,
+                        const float* ln_gamma, void* workspace,
+                        size_t workspace_bytes, void* dX, float* dA, float* dB,
+                        float* dbias1, float* dbias2, float* dgamma,
+                        float* dbeta, void* stream);
+/* Byte offsets of the packed-weight sections and of the forward's and the
+ * training step's workspace sections (for inspection by tests); -1 if
+ * unknown.  Transposed code sections of T columns have a row pitch of
+ * T rounded up to a multiple of 16 bytes. */
 long long tp_mlp_fp8_offset(const tp_mlp_handle* handle, int tokens,
                             int which);
 #define TPMLP_FP8_PACK_SCALES 0   /* amax_a, amax_b (u32), s_a, s_b (f32) */
@@ -189,6 +228,17 @@ long long tp_mlp_fp8_offset(const tp_mlp_handle* handle, int tokens,
 #define TPMLP_FP8_WS_XQ       4   /* Xn codes [T, h]                      */
 #define TPMLP_FP8_WS_Y        5   /* Y [T, f] bf16                        */
 #define TPMLP_FP8_WS_YQ       6   /* Y codes [T, f]                       */
+#define TPMLP_FP8_PACK_AQ     7   /* A codes [h, f]                       */
+#define TPMLP_FP8_PACK_BQ     8   /* B codes [f, h]                       */
+#define TPMLP_FP8_WS_H        9   /* H [T, f] bf16 (training)             */
+#define TPMLP_FP8_WS_XQT     10   /* Xn codes transposed [h, T]           */
+#define TPMLP_FP8_WS_YQT     11   /* Y codes transposed [f, T]            */
+#define TPMLP_FP8_WS_BSCALES 12   /* amax_dz, amax_dh (u32), s_dz, s_dh   */
+#define TPMLP_FP8_WS_DZQ     13   /* dZ codes [T, h]                      */
+#define TPMLP_FP8_WS_DZQT    14   /* dZ codes transposed [h, T]           */
+#define TPMLP_FP8_WS_DH      15   /* dH [T, f] bf16                       */
+#define TPMLP_FP8_WS_DHQ     16   /* dH codes [T, f]                      */
+#define TPMLP_FP8_WS_DHQT    17   /* dH codes transposed [f, T]           */
 
 /* Tensor-core rate calibration (instrumentation, not part of the block):
  * launches `ctas` CTAs (one per SM when ctas <= the SM count), each with one

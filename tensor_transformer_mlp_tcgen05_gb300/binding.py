@@ -40,6 +40,8 @@ EXPORTED = (
     "tp_mlp_set_dropout_seed",
     "tp_mlp_fp8_weights_bytes", "tp_mlp_fp8_pack_weights",
     "tp_mlp_fp8_workspace_bytes", "tp_mlp_forward_fp8", "tp_mlp_fp8_offset",
+    "tp_mlp_fp8_train_workspace_bytes", "tp_mlp_forward_fp8_train",
+    "tp_mlp_backward_fp8",
     "tp_mlp_probe_mma_cycles",
     "tp_mlp_probe_gelu",
     "tp_attn_create", "tp_attn_destroy", "tp_attn_workspace_bytes",
@@ -56,6 +58,17 @@ TPMLP_FP8_WS_SCALES = 3
 TPMLP_FP8_WS_XQ = 4
 TPMLP_FP8_WS_Y = 5
 TPMLP_FP8_WS_YQ = 6
+TPMLP_FP8_PACK_AQ = 7
+TPMLP_FP8_PACK_BQ = 8
+TPMLP_FP8_WS_H = 9
+TPMLP_FP8_WS_XQT = 10
+TPMLP_FP8_WS_YQT = 11
+TPMLP_FP8_WS_BSCALES = 12
+TPMLP_FP8_WS_DZQ = 13
+TPMLP_FP8_WS_DZQT = 14
+TPMLP_FP8_WS_DH = 15
+TPMLP_FP8_WS_DHQ = 16
+TPMLP_FP8_WS_DHQT = 17
 
 TPATTN_WS_QKV = 0
 TPATTN_WS_CTX = 1
@@ -149,6 +162,14 @@ def lib(path: str | None = None) -> ctypes.CDLL:
     L.tp_mlp_forward_fp8.argtypes = [_vp, _i, _vp, _vp, _vp, _vp, _vp, _vp,
                                      _vp, _vp, _sz, _vp]
     L.tp_mlp_forward_fp8.restype = _i
+    L.tp_mlp_fp8_train_workspace_bytes.argtypes = [_vp, _i]
+    L.tp_mlp_fp8_train_workspace_bytes.restype = _sz
+    L.tp_mlp_forward_fp8_train.argtypes = [_vp, _i, _vp, _vp, _vp, _vp, _vp,
+                                           _vp, _vp, _vp, _sz, _vp]
+    L.tp_mlp_forward_fp8_train.restype = _i
+    L.tp_mlp_backward_fp8.argtypes = [_vp, _i, _vp, _vp, _vp, _vp, _vp, _sz,
+                                      _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+    L.tp_mlp_backward_fp8.restype = _i
     L.tp_mlp_fp8_offset.argtypes = [_vp, _i, _i]
     L.tp_mlp_fp8_offset.restype = ctypes.c_longlong
     L.tp_mlp_probe_mma_cycles.argtypes = [_i, _i, _i, _vp, _vp, _vp]
@@ -329,6 +350,29 @@ def tp_mlp_forward_fp8(handle, tokens, X, packed, bias1, bias2, ln_gamma,
         handle, tokens, _ptr(X), _ptr(packed), _ptr(bias1), _ptr(bias2),
         _ptr(ln_gamma), _ptr(ln_beta), _ptr(Z), _ptr(workspace),
         workspace_bytes, _stream(stream)), "tp_mlp_forward_fp8")
+
+
+def tp_mlp_fp8_train_workspace_bytes(handle, tokens: int) -> int:
+    return int(lib().tp_mlp_fp8_train_workspace_bytes(handle, tokens))
+
+
+def tp_mlp_forward_fp8_train(handle, tokens, X, packed, bias1, bias2,
+                             ln_gamma, ln_beta, Z, workspace, workspace_bytes,
+                             stream=None):
+    _check(lib().tp_mlp_forward_fp8_train(
+        handle, tokens, _ptr(X), _ptr(packed), _ptr(bias1), _ptr(bias2),
+        _ptr(ln_gamma), _ptr(ln_beta), _ptr(Z), _ptr(workspace),
+        workspace_bytes, _stream(stream)), "tp_mlp_forward_fp8_train")
+
+
+def tp_mlp_backward_fp8(handle, tokens, dZ, X, packed, ln_gamma, workspace,
+                        workspace_bytes, dX, dA, dB, dbias1, dbias2, dgamma,
+                        dbeta, stream=None):
+    _check(lib().tp_mlp_backward_fp8(
+        handle, tokens, _ptr(dZ), _ptr(X), _ptr(packed), _ptr(ln_gamma),
+        _ptr(workspace), workspace_bytes, _ptr(dX), _ptr(dA), _ptr(dB),
+        _ptr(dbias1), _ptr(dbias2), _ptr(dgamma), _ptr(dbeta),
+        _stream(stream)), "tp_mlp_backward_fp8")
 
 
 def tp_mlp_fp8_offset(handle, tokens: int, which: int) -> int:

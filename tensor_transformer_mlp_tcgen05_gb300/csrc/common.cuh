@@ -51,7 +51,8 @@ struct GemmArgs {
   // E4M3 operand GEMMs: the accumulator is multiplied by *scale_a *
   // *scale_b (the two operands' per-tensor scales, device memory, product
   // rounded to fp32) before the bias.  amax_out (nullable): EPI_GELU_FWD
-  // raises it to the largest |Y| written (fp32 bits of a bf16 value).
+  // and EPI_GELU_BWD raise it to the largest |Y| or |dH| written (fp32 bits
+  // of a bf16 value).
   const float* scale_a;
   const float* scale_b;
   unsigned int* amax_out;

@@ -1,7 +1,7 @@
 // Per-tensor E4M3 scaling for the FP8 forward of the MLP block: the current
 // maximum magnitude of a bf16 tensor, and quantization with the scale it
 // gives (s = amax / 448 in fp32, q = e4m3(x / s), nearest-even rounding with
-// saturation to +-448).  A maximum does not depend on the order its inputs
+// saturation to +-448), in the plain layout, transposed, or both at once.  A maximum does not depend on the order its inputs
 // are combined in, so the fp32-bit atomicMax keeps the result deterministic.
 // All three kernels are HBM-bound streaming passes with 16-byte loads.
 #include <cuda_fp8.h>
@@ -102,27 +102,33 @@ __global__ void quantize_kernel(const uint4* __restrict__ x, size_t n8,
     qtail[threadIdx.x] = to_e4m3(__bfloat162float(tail[threadIdx.x]), s);
 }
 
-// x [rows, cols] bf16 -> q [cols, rows] E4M3, 64 x 64 tiles through shared
+// x [rows, cols] bf16 -> qt [cols, ld_t] E4M3 (element (r, c) at
+// qt[c * ld_t + r]) and, when q_row is not null, also q_row [rows, cols]
+// (the plain layout), from one read of x: 64 x 64 tiles through shared
 // memory (coalesced 16-byte reads, 8-byte writes).
-__global__ void quantize_t_kernel(const __nv_bfloat16* __restrict__ x,
-                                  int rows, int cols,
-                                  const unsigned int* __restrict__ amax,
-                                  uint8_t* __restrict__ q, float* scale_out) {
+__global__ void __launch_bounds__(QT)
+    quantize_t_kernel(const __nv_bfloat16* __restrict__ x, int rows, int cols,
+                      const unsigned int* __restrict__ amax,
+                      uint8_t* __restrict__ qt, long long ld_t,
+                      uint8_t* __restrict__ q_row, float* scale_out) {
   __shared__ uint8_t tile[64][64 + 8];
   const float s = scale_from_amax(*amax);
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0 &&
       scale_out != nullptr)
     *scale_out = s;
   const int r0 = blockIdx.y * 64, c0 = blockIdx.x * 64;
+  const bool vec_in = (cols & 7) == 0;
   // load: 64 rows x 8 chunks of 8 columns; 256 threads, 2 chunks each
-  for (int t = threadIdx.x; t < 64 * 8; t += QT) {
+#pragma unroll
+  for (int it = 0; it < 2; ++it) {
+    const int t = threadIdx.x + it * QT;
     const int r = t >> 3, ch = t & 7;
     const int gr = r0 + r, gc = c0 + ch * 8;
     uint8_t v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     if (gr < rows) {
-      if (gc + 8 <= cols && (cols & 7) == 0) {
-        const uint4 u = *reinterpret_cast<const uint4*>(
-            x + static_cast<size_t>(gr) * cols + gc);
+      const size_t base = static_cast<size_t>(gr) * cols + gc;
+      if (gc + 8 <= cols && vec_in) {
+        const uint4 u = *reinterpret_cast<const uint4*>(x + base);
         const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -131,10 +137,19 @@ __global__ void quantize_t_kernel(const __nv_bfloat16* __restrict__ x,
           v[2 * k] = to_e4m3(a, s);
           v[2 * k + 1] = to_e4m3(b, s);
         }
+        if (q_row != nullptr) {
+          uint2 o;
+          o.x = uint32_t(v[0]) | (uint32_t(v[1]) << 8) | (uint32_t(v[2]) << 16) |
+                (uint32_t(v[3]) << 24);
+          o.y = uint32_t(v[4]) | (uint32_t(v[5]) << 8) | (uint32_t(v[6]) << 16) |
+                (uint32_t(v[7]) << 24);
+          *reinterpret_cast<uint2*>(q_row + base) = o;
+        }
       } else {
-        for (int k = 0; k < 8 && gc + k < cols; ++k)
-          v[k] = to_e4m3(
-              __bfloat162float(x[static_cast<size_t>(gr) * cols + gc + k]), s);
+        for (int k = 0; k < 8 && gc + k < cols; ++k) {
+          v[k] = to_e4m3(__bfloat162float(x[base + k]), s);
+          if (q_row != nullptr) q_row[base + k] = v[k];
+        }
       }
     }
 #pragma unroll
@@ -142,11 +157,13 @@ __global__ void quantize_t_kernel(const __nv_bfloat16* __restrict__ x,
   }
   __syncthreads();
   // store: 64 output rows (input columns) x 8 chunks of 8 bytes
-  for (int t = threadIdx.x; t < 64 * 8; t += QT) {
+#pragma unroll
+  for (int it = 0; it < 2; ++it) {
+    const int t = threadIdx.x + it * QT;
     const int oc = t >> 3, ch = t & 7;
     const int grow = c0 + oc, gcol = r0 + ch * 8;
     if (grow >= cols) continue;
-    uint8_t* dst = q + static_cast<size_t>(grow) * rows + gcol;
+    uint8_t* dst = qt + static_cast<size_t>(grow) * ld_t + gcol;
     if (gcol + 8 <= rows && (reinterpret_cast<uintptr_t>(dst) & 7u) == 0) {
       *reinterpret_cast<uint2*>(dst) =
           *reinterpret_cast<const uint2*>(&tile[oc][ch * 8]);
@@ -188,13 +205,16 @@ cudaError_t launch_quantize_e4m3(const void* x, size_t n,
   return cudaGetLastError();
 }
 
-cudaError_t launch_quantize_e4m3_t(const void* x, int rows, int cols,
-                                   const unsigned int* amax, uint8_t* q,
-                                   float* scale_out, cudaStream_t s) {
+cudaError_t launch_quantize_e4m3_rt(const void* x, int rows, int cols,
+                                    const unsigned int* amax, uint8_t* q_row,
+                                    uint8_t* qt, long long ld_t,
+                                    float* scale_out, cudaStream_t s) {
   if (rows <= 0 || cols <= 0) return cudaSuccess;
+  if (ld_t < rows) return cudaErrorInvalidValue;
   const dim3 grid((cols + 63) / 64, (rows + 63) / 64);
   quantize_t_kernel<<<grid, QT, 0, s>>>(static_cast<const __nv_bfloat16*>(x),
-                                        rows, cols, amax, q, scale_out);
+                                        rows, cols, amax, qt, ld_t, q_row,
+                                        scale_out);
   return cudaGetLastError();
 }
 

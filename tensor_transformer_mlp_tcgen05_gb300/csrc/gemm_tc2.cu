@@ -375,6 +375,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ptx::tmem_ld_32x32b_x32(taddr + j * 32, r);
             ptx::tmem_ld_wait();
             const int c0 = col_base + j * 32;
+            if constexpr (F8) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                r[i] = __float_as_uint(__uint_as_float(r[i]) * acc_scale);
+            }
             if (live && c0 < args.N) st.put(&tmO, c0, row0, r, lane);
           }
         } else {
@@ -439,6 +444,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                       v[8 * i + 2 * k + 1] *= g1;
                     }
                   }
+                }
+                if (F8 && args.amax_out != nullptr) {
+                  // largest |dH| of this warp's rows in range, as stored
+                  float mx = 0.f;
+#pragma unroll
+                  for (int i = 0; i < 64; ++i) mx = fmaxf(mx, fabsf(v[i]));
+                  mx = row < args.M ? __bfloat162float(__float2bfloat16_rn(mx))
+                                    : 0.f;
+                  const unsigned int wm =
+                      __reduce_max_sync(0xffffffffu, __float_as_uint(mx));
+                  if (lane == 0) atomicMax(args.amax_out, wm);
                 }
               }
               pack_bf16x64(v, w);
@@ -617,6 +633,12 @@ cudaError_t launch_gemm_tc2_e4m3(int epi, const CUtensorMap& ta,
   if (epi == EPI_SHARDSUM)
     return launch_impl<false, false, EPI_SHARDSUM, true>(ta, tb, to, to2, args,
                                                          max_pairs, stream);
+  if (epi == EPI_GELU_BWD)
+    return launch_impl<false, false, EPI_GELU_BWD, true>(ta, tb, to, to2, args,
+                                                         max_pairs, stream);
+  if (epi == EPI_STORE_F32)
+    return launch_impl<false, false, EPI_STORE_F32, true>(ta, tb, to, to2, args,
+                                                          max_pairs, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -36,8 +36,10 @@ cudaError_t launch_gemm_tc2(int epi, bool a_mn, bool b_mn,
 
 // The pair GEMM on E4M3 operands (both K-major, 8-bit tensor maps with
 // 128 x 128-byte boxes; args.kb_per_seg counts 128-element k-blocks;
-// args.scale_a and args.scale_b required).  Epilogues EPI_GELU_FWD (optionally raising
-// args.amax_out) and EPI_SHARDSUM.
+// args.scale_a and args.scale_b required).  Epilogues EPI_GELU_FWD and
+// EPI_GELU_BWD (each optionally raising args.amax_out to the largest |out|
+// stored; EPI_GELU_BWD also with the args.colsum partials), EPI_SHARDSUM and
+// EPI_STORE_F32.
 cudaError_t launch_gemm_tc2_e4m3(int epi, const CUtensorMap& ta,
                                  const CUtensorMap& tb, const CUtensorMap& to,
                                  const CUtensorMap& to2, const GemmArgs& args,
@@ -52,10 +54,14 @@ cudaError_t launch_amax_bf16(const void* x, size_t n, unsigned int* amax,
 cudaError_t launch_quantize_e4m3(const void* x, size_t n,
                                  const unsigned int* amax, uint8_t* q,
                                  float* scale_out, cudaStream_t stream);
-// Transposing quantization of a bf16 [rows, cols] matrix into q [cols, rows].
-cudaError_t launch_quantize_e4m3_t(const void* x, int rows, int cols,
-                                   const unsigned int* amax, uint8_t* q,
-                                   float* scale_out, cudaStream_t stream);
+// Quantization of a bf16 [rows, cols] matrix into both layouts from one
+// read: q_row [rows, cols] (nullable) and qt [cols,
+// ld_t] (element (r, c) at qt[c * ld_t + r], ld_t >= rows; columns past
+// `rows` are left untouched).
+cudaError_t launch_quantize_e4m3_rt(const void* x, int rows, int cols,
+                                    const unsigned int* amax, uint8_t* q_row,
+                                    uint8_t* qt, long long ld_t,
+                                    float* scale_out, cudaStream_t stream);
 
 // fp32 CUDA-core GEMM with the same epilogues.  Element (m, k) of the first
 // operand is a[m * a_sm + k * a_sk]; element (k, n) of the second is

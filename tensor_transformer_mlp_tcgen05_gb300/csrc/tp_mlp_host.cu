@@ -76,27 +76,40 @@ Layout make_layout(const tp_mlp_config& c, int tokens, int training) {
   return L;
 }
 
-// FP8 forward: packed weights and workspace.
+// FP8: packed weights and workspace.
 struct Fp8Pack {
-  size_t scales = 0, aqt = 0, bqt = 0, total = 0;
+  size_t scales = 0, aqt = 0, bqt = 0, aq = 0, bq = 0, total = 0;
 };
-// [amax_a, amax_b (u32), s_a, s_b (f32)] | A^T codes [f, h] | B^T codes [h, f]
+// [amax_a, amax_b (u32), s_a, s_b (f32)] | A^T codes [f, h] | B^T codes
+// [h, f] | A codes [h, f] | B codes [f, h]
 Fp8Pack fp8_pack_layout(const tp_mlp_config& c) {
   Fp8Pack P;
   const size_t h = static_cast<size_t>(c.hidden), f = static_cast<size_t>(c.ffn);
   P.scales = 0;
   P.aqt = 256;
   P.bqt = align_up(P.aqt + f * h, 256);
-  P.total = align_up(P.bqt + h * f, 256);
+  P.aq = align_up(P.bqt + h * f, 256);
+  P.bq = align_up(P.aq + h * f, 256);
+  P.total = align_up(P.bq + f * h, 256);
   return P;
 }
 
 struct Fp8Layout {
   size_t status = 0, xn = 0, mean = 0, rstd = 0, scales = 0, xq = 0, y = 0,
          yq = 0, total = 0;
+  // training sections
+  size_t tpitch = 0;  // row pitch (bytes) of the transposed code sections
+  size_t hb = 0, xqt = 0, yqt = 0, bscales = 0, dzq = 0, dzqt = 0, dh = 0,
+         dhq = 0, dhqt = 0, dxn = 0, part = 0, train_total = 0;
+  int chunks = 0, groups = 0;
 };
 // status | [Xn, mean, rstd] | [amax_x, amax_y (u32), s_x, s_y (f32)] |
-// Xq [T, h] | Y [T, f] bf16 | Yq [T, f]
+// Xq [T, h] | Y [T, f] bf16 | Yq [T, f] -- the forward's workspace; the
+// training workspace goes on with H [T, f] bf16 | Xq^T [h, Tp] | Yq^T
+// [f, Tp] | [amax_dz, amax_dh (u32), s_dz, s_dh (f32)] | dZq [T, h] |
+// dZq^T [h, Tp] | dH [T, f] bf16 | dHq [T, f] | dHq^T [f, Tp] | [dXn fp32
+// [T, h] with LayerNorm] | column-sum partials (as the bf16 backward's),
+// Tp = T rounded up to 16 (the tensor-map row pitch rule).
 Fp8Layout fp8_layout(const tp_mlp_config& c, int tokens) {
   Fp8Layout L;
   const size_t T = static_cast<size_t>(tokens);
@@ -118,6 +131,22 @@ Fp8Layout fp8_layout(const tp_mlp_config& c, int tokens) {
   L.y = take(T * f * 2);
   L.yq = take(T * f);
   L.total = off;
+  L.tpitch = align_up(T, 16);
+  L.hb = take(T * f * 2);
+  L.xqt = take(h * L.tpitch);
+  L.yqt = take(f * L.tpitch);
+  L.bscales = take(16);
+  L.dzq = take(T * h);
+  L.dzqt = take(h * L.tpitch);
+  L.dh = take(T * f * 2);
+  L.dhq = take(T * f);
+  L.dhqt = take(f * L.tpitch);
+  if (c.use_layernorm) L.dxn = take(T * h * 4);
+  L.chunks = colsum_chunks(tokens);
+  L.groups = (tokens + 31) / 32;
+  const size_t rows1 = static_cast<size_t>(L.groups > L.chunks ? L.groups : L.chunks);
+  L.part = take((static_cast<size_t>(L.chunks) * 3 * h + rows1 * f) * 4);
+  L.train_total = off;
   return L;
 }
 
@@ -498,6 +527,12 @@ size_t tp_mlp_fp8_workspace_bytes(const tp_mlp_handle* H, int tokens) {
   return fp8_layout(H->cfg, tokens).total;
 }
 
+size_t tp_mlp_fp8_train_workspace_bytes(const tp_mlp_handle* H, int tokens) {
+  if (H == nullptr || tokens < 0 || fp8_config_ok(H->cfg) != TPMLP_OK)
+    return 0;
+  return fp8_layout(H->cfg, tokens).train_total;
+}
+
 long long tp_mlp_fp8_offset(const tp_mlp_handle* H, int tokens, int which) {
   if (H == nullptr || tokens < 0) return -1;
   const Fp8Pack P = fp8_pack_layout(H->cfg);
@@ -506,10 +541,21 @@ long long tp_mlp_fp8_offset(const tp_mlp_handle* H, int tokens, int which) {
     case TPMLP_FP8_PACK_SCALES: return static_cast<long long>(P.scales);
     case TPMLP_FP8_PACK_AQT: return static_cast<long long>(P.aqt);
     case TPMLP_FP8_PACK_BQT: return static_cast<long long>(P.bqt);
+    case TPMLP_FP8_PACK_AQ: return static_cast<long long>(P.aq);
+    case TPMLP_FP8_PACK_BQ: return static_cast<long long>(P.bq);
     case TPMLP_FP8_WS_SCALES: return static_cast<long long>(L.scales);
     case TPMLP_FP8_WS_XQ: return static_cast<long long>(L.xq);
     case TPMLP_FP8_WS_Y: return static_cast<long long>(L.y);
     case TPMLP_FP8_WS_YQ: return static_cast<long long>(L.yq);
+    case TPMLP_FP8_WS_H: return static_cast<long long>(L.hb);
+    case TPMLP_FP8_WS_XQT: return static_cast<long long>(L.xqt);
+    case TPMLP_FP8_WS_YQT: return static_cast<long long>(L.yqt);
+    case TPMLP_FP8_WS_BSCALES: return static_cast<long long>(L.bscales);
+    case TPMLP_FP8_WS_DZQ: return static_cast<long long>(L.dzq);
+    case TPMLP_FP8_WS_DZQT: return static_cast<long long>(L.dzqt);
+    case TPMLP_FP8_WS_DH: return static_cast<long long>(L.dh);
+    case TPMLP_FP8_WS_DHQ: return static_cast<long long>(L.dhq);
+    case TPMLP_FP8_WS_DHQT: return static_cast<long long>(L.dhqt);
     default: return -1;
   }
 }
@@ -541,22 +587,27 @@ int tp_mlp_fp8_pack_weights(tp_mlp_handle* H, const void* A, const void* B,
   TRY(run(&H->core, "fp8_amax_weights", s, [&] {
     return launch_amax_bf16(B, size_t(f) * h, amax + 1, s);
   }));
-  TRY(run(&H->core, "fp8_quantize_weights_t", s, [&] {
-    return launch_quantize_e4m3_t(A, h, f, amax,
-                                  reinterpret_cast<uint8_t*>(pk + P.aqt), scl, s);
+  // both layouts of each weight from one read
+  TRY(run(&H->core, "fp8_quantize_weights", s, [&] {
+    return launch_quantize_e4m3_rt(A, h, f, amax,
+                                   reinterpret_cast<uint8_t*>(pk + P.aq),
+                                   reinterpret_cast<uint8_t*>(pk + P.aqt), h,
+                                   scl, s);
   }));
-  return run(&H->core, "fp8_quantize_weights_t", s, [&] {
-    return launch_quantize_e4m3_t(B, f, h, amax + 1,
-                                  reinterpret_cast<uint8_t*>(pk + P.bqt),
-                                  scl + 1, s);
+  return run(&H->core, "fp8_quantize_weights", s, [&] {
+    return launch_quantize_e4m3_rt(B, f, h, amax + 1,
+                                   reinterpret_cast<uint8_t*>(pk + P.bq),
+                                   reinterpret_cast<uint8_t*>(pk + P.bqt), f,
+                                   scl + 1, s);
   });
 }
 
-int tp_mlp_forward_fp8(tp_mlp_handle* H, int tokens, const void* X,
-                       const void* packed, const float* bias1,
-                       const float* bias2, const float* ln_gamma,
-                       const float* ln_beta, void* Z, void* workspace,
-                       size_t workspace_bytes, void* stream) {
+static int forward_fp8_impl(tp_mlp_handle* H, int tokens, const void* X,
+                            const void* packed, const float* bias1,
+                            const float* bias2, const float* ln_gamma,
+                            const float* ln_beta, void* Z, void* workspace,
+                            size_t workspace_bytes, cudaStream_t s,
+                            bool train) {
   if (H == nullptr) return TPMLP_ERR_ARG;
   const tp_mlp_config& c = H->cfg;
   TRY(fp8_config_ok(c));
@@ -567,10 +618,10 @@ int tp_mlp_forward_fp8(tp_mlp_handle* H, int tokens, const void* X,
   for (const void* p : ptrs)
     if (p && !aligned16(p)) return TPMLP_ERR_ALIGN;
   const Fp8Layout L = fp8_layout(c, tokens);
-  if (workspace_bytes < L.total) return TPMLP_ERR_WORKSPACE;
+  if (workspace_bytes < (train ? L.train_total : L.total))
+    return TPMLP_ERR_WORKSPACE;
   int sms = 0;
   TRY(check_device(&sms));
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
   const char* pk = static_cast<const char*>(packed);
   const Fp8Pack P = fp8_pack_layout(c);
@@ -602,6 +653,10 @@ int tp_mlp_forward_fp8(tp_mlp_handle* H, int tokens, const void* X,
   TRY(run(&H->core, "fp8_amax_x", s,
           [&] { return launch_amax_bf16(Xop, size_t(T) * h, amax, s); }));
   TRY(run(&H->core, "fp8_quantize_x", s, [&] {
+    if (train)  // Xq and, for dA, Xq^T
+      return launch_quantize_e4m3_rt(Xop, T, h, amax, Xq,
+                                     reinterpret_cast<uint8_t*>(ws + L.xqt),
+                                     static_cast<long long>(L.tpitch), scl, s);
     return launch_quantize_e4m3(Xop, size_t(T) * h, amax, Xq, scl, s);
   }));
   CUtensorMap ta, tb, to, to2;
@@ -612,10 +667,20 @@ int tp_mlp_forward_fp8(tp_mlp_handle* H, int tokens, const void* X,
   TRY(encode_map_u8(&ta, Xq, h, T, h, TC_BM));
   TRY(encode_map_u8(&tb, pk + P.aqt, h, f, h, TC2_BN_HALF));
   TRY(out_map(&to, Y, false, T, f, f));
+  to2 = to;
+  if (train) {  // H for GeLU's derivative in the backward
+    g1.out2 = ws + L.hb;
+    TRY(out_map(&to2, g1.out2, false, T, f, f));
+  }
   TRY(run(&H->core, "gemm1_gelu_fp8", s, [&] {
-    return launch_gemm_tc2_e4m3(EPI_GELU_FWD, ta, tb, to, to, g1, sms / 2, s);
+    return launch_gemm_tc2_e4m3(EPI_GELU_FWD, ta, tb, to, to2, g1, sms / 2, s);
   }));
   TRY(run(&H->core, "fp8_quantize_y", s, [&] {
+    if (train)  // Yq and, for dB, Yq^T
+      return launch_quantize_e4m3_rt(Y, T, f, amax + 1, Yq,
+                                     reinterpret_cast<uint8_t*>(ws + L.yqt),
+                                     static_cast<long long>(L.tpitch), scl + 1,
+                                     s);
     return launch_quantize_e4m3(Y, size_t(T) * f, amax + 1, Yq, scl + 1, s);
   }));
   GemmArgs g2 = base_args(H, ws, L.status);
@@ -632,6 +697,195 @@ int tp_mlp_forward_fp8(tp_mlp_handle* H, int tokens, const void* X,
   return run(&H->core, "gemm2_shardsum_fp8", s, [&] {
     return launch_gemm_tc2_e4m3(EPI_SHARDSUM, ta, tb, to2, to2, g2, sms / 2, s);
   });
+}
+
+int tp_mlp_forward_fp8(tp_mlp_handle* H, int tokens, const void* X,
+                       const void* packed, const float* bias1,
+                       const float* bias2, const float* ln_gamma,
+                       const float* ln_beta, void* Z, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  return forward_fp8_impl(H, tokens, X, packed, bias1, bias2, ln_gamma,
+                          ln_beta, Z, workspace, workspace_bytes,
+                          static_cast<cudaStream_t>(stream), false);
+}
+
+int tp_mlp_forward_fp8_train(tp_mlp_handle* H, int tokens, const void* X,
+                             const void* packed, const float* bias1,
+                             const float* bias2, const float* ln_gamma,
+                             const float* ln_beta, void* Z, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  return forward_fp8_impl(H, tokens, X, packed, bias1, bias2, ln_gamma,
+                          ln_beta, Z, workspace, workspace_bytes,
+                          static_cast<cudaStream_t>(stream), true);
+}
+
+int tp_mlp_backward_fp8(tp_mlp_handle* H, int tokens, const void* dZ,
+                        const void* X, const void* packed,
+                        const float* ln_gamma, void* workspace,
+                        size_t workspace_bytes, void* dX, float* dA, float* dB,
+                        float* dbias1, float* dbias2, float* dgamma,
+                        float* dbeta, void* stream) {
+  if (H == nullptr) return TPMLP_ERR_ARG;
+  const tp_mlp_config& c = H->cfg;
+  TRY(fp8_config_ok(c));
+  if (tokens < 0 || tokens > c.max_tokens) return TPMLP_ERR_SHAPE;
+  if (!packed || !workspace || !dA || !dB ||
+      (tokens > 0 && (!dZ || !X || !dX)))
+    return TPMLP_ERR_ARG;
+  if (c.use_layernorm && !ln_gamma) return TPMLP_ERR_ARG;
+  const void* ptrs[] = {dZ, X, packed, ln_gamma, workspace, dX, dA, dB,
+                        dbias1, dbias2, dgamma, dbeta};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return TPMLP_ERR_ALIGN;
+  const Fp8Layout L = fp8_layout(c, tokens);
+  if (workspace_bytes < L.train_total) return TPMLP_ERR_WORKSPACE;
+  int sms = 0;
+  TRY(check_device(&sms));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  const char* pk = static_cast<const char*>(packed);
+  const Fp8Pack P = fp8_pack_layout(c);
+  const int T = tokens, h = c.hidden, f = c.ffn, t = c.shards, ft = f / t;
+  const bool ln = c.use_layernorm != 0;
+
+  if (T == 0) {  // sums over an empty token set
+    struct Zero {
+      void* p;
+      size_t n;
+    } zs[] = {{dA, size_t(h) * f * 4},
+              {dB, size_t(f) * h * 4},
+              {dbias1, size_t(f) * 4},
+              {dbias2, size_t(h) * 4},
+              {ln ? dgamma : nullptr, size_t(h) * 4},
+              {ln ? dbeta : nullptr, size_t(h) * 4}};
+    for (auto& z : zs) {
+      if (!z.p) continue;
+      const cudaError_t e = cudaMemsetAsync(z.p, 0, z.n, s);
+      if (e != cudaSuccess) {
+        set_detail("cudaMemsetAsync(zero gradients)", e);
+        return TPMLP_ERR_CUDA;
+      }
+    }
+    return TPMLP_OK;
+  }
+
+  unsigned int* bamax = reinterpret_cast<unsigned int*>(ws + L.bscales);
+  float* bscl = reinterpret_cast<float*>(ws + L.bscales) + 2;  // s_dz, s_dh
+  const float* fscl = reinterpret_cast<const float*>(ws + L.scales) + 2;  // s_x, s_y
+  const float* wscl = reinterpret_cast<const float*>(pk + P.scales) + 2;  // s_a, s_b
+  const cudaError_t e = cudaMemsetAsync(bamax, 0, 8, s);
+  if (e != cudaSuccess) {
+    set_detail("cudaMemsetAsync(amax)", e);
+    return TPMLP_ERR_CUDA;
+  }
+  const long long tp = static_cast<long long>(L.tpitch);
+  uint8_t* dZq = reinterpret_cast<uint8_t*>(ws + L.dzq);
+  uint8_t* dZqT = reinterpret_cast<uint8_t*>(ws + L.dzqt);
+  void* dH = ws + L.dh;
+  uint8_t* dHq = reinterpret_cast<uint8_t*>(ws + L.dhq);
+  uint8_t* dHqT = reinterpret_cast<uint8_t*>(ws + L.dhqt);
+  float* part = reinterpret_cast<float*>(ws + L.part);
+  float* part1 = part + size_t(L.chunks) * h;  // db1 partials
+
+  // dZ: current amax, then codes in both layouts from one read
+  TRY(run(&H->core, "fp8_amax_dz", s,
+          [&] { return launch_amax_bf16(dZ, size_t(T) * h, bamax, s); }));
+  TRY(run(&H->core, "fp8_quantize_dz", s, [&] {
+    return launch_quantize_e4m3_rt(dZ, T, h, bamax, dZq, dZqT, tp, bscl, s);
+  }));
+  // dH = (s_dz s_b) (dZq Bq^T) * GeLU'(H), raising amax_dh, with the db1
+  // partials of 32-row groups
+  CUtensorMap ta, tb, to;
+  GemmArgs gy = base_args(H, ws, L.status);
+  gy.M = T; gy.N = f; gy.K = h; gy.kb_per_seg = (h + 127) / 128;
+  gy.out = dH; gy.ldo = f; gy.aux = ws + L.hb; gy.ldaux = f;
+  gy.scale_a = bscl; gy.scale_b = wscl + 1; gy.amax_out = bamax + 1;
+  if (dbias1) {
+    gy.colsum = part1;
+    gy.ld_colsum = f;
+  }
+  TRY(encode_map_u8(&ta, dZq, h, T, h, TC_BM));
+  TRY(encode_map_u8(&tb, pk + P.bq, h, f, h, TC2_BN_HALF));
+  TRY(out_map(&to, dH, false, T, f, f));
+  TRY(run(&H->core, "gemm_dh_gelu_bwd_fp8", s, [&] {
+    return launch_gemm_tc2_e4m3(EPI_GELU_BWD, ta, tb, to, to, gy, sms / 2, s);
+  }));
+  TRY(run(&H->core, "fp8_quantize_dh", s, [&] {
+    return launch_quantize_e4m3_rt(dH, T, f, bamax + 1, dHq, dHqT, tp,
+                                   bscl + 1, s);
+  }));
+  if (dbias2) TRY(colsum(&H->core, "colsum_db2", s, true, dZ, part, dbias2, T, h));
+  if (dbias1)
+    TRY(run(&H->core, "colsum_finalize", s, [&] {
+      return launch_colsum_finalize(part1, dbias1, L.groups, f, s);
+    }));
+  // dB = (s_y s_dz) (Yq^T dZq): K = T over the transposed codes
+  const int kbT = (T + 127) / 128;
+  GemmArgs gb = base_args(H, ws, L.status);
+  gb.M = f; gb.N = h; gb.K = T; gb.kb_per_seg = kbT;
+  gb.out = dB; gb.ldo = h;
+  gb.scale_a = fscl + 1; gb.scale_b = bscl;
+  TRY(encode_map_u8(&ta, ws + L.yqt, T, f, tp, TC_BM));
+  TRY(encode_map_u8(&tb, dZqT, T, h, tp, TC2_BN_HALF));
+  TRY(out_map(&to, dB, true, f, h, h));
+  TRY(run(&H->core, "gemm_wgrad_dB_fp8", s, [&] {
+    return launch_gemm_tc2_e4m3(EPI_STORE_F32, ta, tb, to, to, gb, sms / 2, s);
+  }));
+  // dA = (s_x s_dh) (Xq^T dHq)
+  GemmArgs ga = base_args(H, ws, L.status);
+  ga.M = h; ga.N = f; ga.K = T; ga.kb_per_seg = kbT;
+  ga.out = dA; ga.ldo = f;
+  ga.scale_a = fscl; ga.scale_b = bscl + 1;
+  TRY(encode_map_u8(&ta, ws + L.xqt, T, h, tp, TC_BM));
+  TRY(encode_map_u8(&tb, dHqT, T, f, tp, TC2_BN_HALF));
+  TRY(out_map(&to, dA, true, h, f, f));
+  TRY(run(&H->core, "gemm_wgrad_dA_fp8", s, [&] {
+    return launch_gemm_tc2_e4m3(EPI_STORE_F32, ta, tb, to, to, ga, sms / 2, s);
+  }));
+  // dXn = sum_i (s_dh s_a) (dHq_i Aq_i^T) in shard order: fp32 for the
+  // LayerNorm backward, else dX itself (+ dZ with the residual)
+  void* dXdst = ln ? static_cast<void*>(ws + L.dxn) : dX;
+  GemmArgs gx = base_args(H, ws, L.status);
+  gx.M = T; gx.N = h; gx.K = f; gx.num_seg = t; gx.kb_per_seg = ft / 128;
+  gx.out = dXdst; gx.ldo = h; gx.out_f32 = ln ? 1 : 0;
+  gx.scale_a = bscl + 1; gx.scale_b = wscl;
+  if (c.use_residual && !ln) {
+    gx.aux = dZ;
+    gx.ldaux = h;
+  }
+  TRY(encode_map_u8(&ta, dHq, f, T, f, TC_BM));
+  TRY(encode_map_u8(&tb, pk + P.aq, f, h, f, TC2_BN_HALF));
+  TRY(out_map(&to, dXdst, ln, T, h, h));
+  TRY(run(&H->core, "gemm_dx_shardsum_fp8", s, [&] {
+    return launch_gemm_tc2_e4m3(EPI_SHARDSUM, ta, tb, to, to, gx, sms / 2, s);
+  }));
+  if (ln) {
+    const float* dXn = reinterpret_cast<const float*>(ws + L.dxn);
+    const float* mean = reinterpret_cast<const float*>(ws + L.mean);
+    const float* rstd = reinterpret_cast<const float*>(ws + L.rstd);
+    const void* dres = c.use_residual ? dZ : nullptr;
+    TRY(run(&H->core, "layernorm_bwd", s, [&] {
+      return launch_ln_bwd(true, dXn, X, mean, rstd, ln_gamma, dres, dX, T, h,
+                           s);
+    }));
+    if (dgamma || dbeta) {
+      float* pg = part1 + size_t(L.groups > L.chunks ? L.groups : L.chunks) * f;
+      float* pb = pg + size_t(L.chunks) * h;
+      TRY(run(&H->core, "layernorm_param_partial", s, [&] {
+        return launch_ln_param_partial(true, dXn, X, mean, rstd, pg, pb, T, h,
+                                       s);
+      }));
+      if (dgamma)
+        TRY(run(&H->core, "colsum_finalize", s, [&] {
+          return launch_colsum_finalize(pg, dgamma, L.chunks, h, s);
+        }));
+      if (dbeta)
+        TRY(run(&H->core, "colsum_finalize", s, [&] {
+          return launch_colsum_finalize(pb, dbeta, L.chunks, h, s);
+        }));
+    }
+  }
+  return TPMLP_OK;
 }
 
 int tp_mlp_check(tp_mlp_handle* H, void* workspace, void* stream) {

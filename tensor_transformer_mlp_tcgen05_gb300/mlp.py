@@ -116,7 +116,7 @@ class TensorParallelMLP:
             return B_.TPMLP_OK
         return B_.tp_mlp_check(self.handle, self._ws, stream)
 
-    # ------------------------------------------------------- fp8 forward --
+    # ------------------------------------------------------------- fp8 --
     def pack_fp8_weights(self, A, B, stream=None) -> torch.Tensor:
         """Quantize A and B to E4M3 (per-tensor scales) into a new packed
         buffer for forward_fp8 (see tp_mlp_fp8_pack_weights)."""
@@ -132,8 +132,10 @@ class TensorParallelMLP:
         return packed
 
     def forward_fp8(self, X, packed, b1=None, b2=None, gamma=None, beta=None,
-                    out=None, stream=None):
-        """FP8 (E4M3) forward with weights from pack_fp8_weights."""
+                    out=None, stream=None, train=False):
+        """FP8 (E4M3) forward with weights from pack_fp8_weights; with
+        train=True it keeps what backward_fp8 needs in the workspace
+        (tp_mlp_forward_fp8_train)."""
         T = X.shape[0]
         h, f = self.hidden, self.ffn
         self._chk("X", X, (T, h), torch.bfloat16)
@@ -144,21 +146,75 @@ class TensorParallelMLP:
         Z = out if out is not None else torch.empty((T, h), dtype=torch.bfloat16,
                                                    device=X.device)
         self._chk("Z", Z, (T, h), torch.bfloat16)
-        need = B_.tp_mlp_fp8_workspace_bytes(self.handle, T)
+        need = (B_.tp_mlp_fp8_train_workspace_bytes if train
+                else B_.tp_mlp_fp8_workspace_bytes)(self.handle, T)
         if self._ws is None or self._ws.numel() < need:
             self._ws = torch.empty(max(need, 256), dtype=torch.uint8,
                                    device=self.device)
-        B_.tp_mlp_forward_fp8(self.handle, T, X, packed, b1, b2, gamma, beta,
-                              Z, self._ws, self._ws.numel(), stream)
+        fwd = B_.tp_mlp_forward_fp8_train if train else B_.tp_mlp_forward_fp8
+        fwd(self.handle, T, X, packed, b1, b2, gamma, beta, Z, self._ws,
+            self._ws.numel(), stream)
         return Z
+
+    def backward_fp8(self, dZ, X, packed, gamma=None, bias_grads=True,
+                     grads=None, stream=None):
+        """FP8 backward after forward_fp8(..., train=True) on the same X and
+        packed weights (tp_mlp_backward_fp8): returns dX (bf16), dA, dB and
+        the bias / LayerNorm-parameter gradients (fp32)."""
+        T = X.shape[0]
+        h, f = self.hidden, self.ffn
+        self._chk("dZ", dZ, (T, h), torch.bfloat16)
+        self._chk("X", X, (T, h), torch.bfloat16)
+        self._chk("gamma", gamma, (h,), torch.float32)
+        need = B_.tp_mlp_fp8_train_workspace_bytes(self.handle, T)
+        if self._ws is None or self._ws.numel() < need:
+            raise RuntimeError("backward_fp8 needs the workspace of "
+                               "forward_fp8(..., train=True)")
+        dev = X.device
+        g = dict(grads or {})
+        g.setdefault("dX", torch.empty((T, h), dtype=torch.bfloat16, device=dev))
+        g.setdefault("dA", torch.empty((h, f), dtype=torch.float32, device=dev))
+        g.setdefault("dB", torch.empty((f, h), dtype=torch.float32, device=dev))
+        if bias_grads:
+            g.setdefault("db1", torch.empty(f, dtype=torch.float32, device=dev))
+            g.setdefault("db2", torch.empty(h, dtype=torch.float32, device=dev))
+        if self.layernorm:
+            g.setdefault("dgamma", torch.empty(h, dtype=torch.float32, device=dev))
+            g.setdefault("dbeta", torch.empty(h, dtype=torch.float32, device=dev))
+        B_.tp_mlp_backward_fp8(self.handle, T, dZ, X, packed, gamma, self._ws,
+                               self._ws.numel(), g["dX"], g["dA"], g["dB"],
+                               g.get("db1"), g.get("db2"), g.get("dgamma"),
+                               g.get("dbeta"), stream)
+        return g
 
     def fp8_saved(self, tokens: int, which: str, packed=None):
         """Views of the FP8 path's intermediates: "xq" [T,h] / "yq" [T,f]
         uint8 codes, "y" [T,f] bf16, "scales" (4 words: amax_x, amax_y as
-        fp32 bits, s_x, s_y) in the workspace; "aqt" [f,h], "bqt" [h,f]
-        codes and "wscales" (amax_a, amax_b, s_a, s_b) in `packed`."""
+        fp32 bits, s_x, s_y) in the workspace; "aqt" [f,h], "bqt" [h,f],
+        "aq" [h,f], "bq" [f,h] codes and "wscales" (amax_a, amax_b, s_a,
+        s_b) in `packed`; after a training step also "h" [T,f] and "dh"
+        [T,f] bf16, "dzq" [T,h] / "dhq" [T,f] codes, the transposed codes
+        "xqt" [h,T], "yqt" [f,T], "dzqt" [h,T], "dhqt" [f,T] (strided views:
+        rows are T rounded up to 16 bytes apart) and "bscales" (amax_dz,
+        amax_dh, s_dz, s_dh)."""
         h, f = self.hidden, self.ffn
+        tp = (tokens + 15) // 16 * 16
+        transposed = {"xqt": (B_.TPMLP_FP8_WS_XQT, h),
+                      "yqt": (B_.TPMLP_FP8_WS_YQT, f),
+                      "dzqt": (B_.TPMLP_FP8_WS_DZQT, h),
+                      "dhqt": (B_.TPMLP_FP8_WS_DHQT, f)}
+        if which in transposed:
+            code, rows = transposed[which]
+            off = B_.tp_mlp_fp8_offset(self.handle, tokens, code)
+            return self._ws[off:off + rows * tp].view(rows, tp)[:, :tokens]
         spec = {"xq": (B_.TPMLP_FP8_WS_XQ, (tokens, h), torch.uint8, False),
+                "h": (B_.TPMLP_FP8_WS_H, (tokens, f), torch.bfloat16, False),
+                "dh": (B_.TPMLP_FP8_WS_DH, (tokens, f), torch.bfloat16, False),
+                "dzq": (B_.TPMLP_FP8_WS_DZQ, (tokens, h), torch.uint8, False),
+                "dhq": (B_.TPMLP_FP8_WS_DHQ, (tokens, f), torch.uint8, False),
+                "bscales": (B_.TPMLP_FP8_WS_BSCALES, (4,), torch.int32, False),
+                "aq": (B_.TPMLP_FP8_PACK_AQ, (h, f), torch.uint8, True),
+                "bq": (B_.TPMLP_FP8_PACK_BQ, (f, h), torch.uint8, True),
                 "y": (B_.TPMLP_FP8_WS_Y, (tokens, f), torch.bfloat16, False),
                 "yq": (B_.TPMLP_FP8_WS_YQ, (tokens, f), torch.uint8, False),
                 "scales": (B_.TPMLP_FP8_WS_SCALES, (4,), torch.int32, False),
