@@ -184,3 +184,58 @@ def test_fp8_training_step_gpt3_13b_layer():
         assert same, k
     for k in ("dX", "dA", "dB", "db1", "db2"):
         assert torch.isfinite(a[k].float()).all(), k
+
+
+def _all_bf16_up_to(v, n):
+    """Every finite bf16 value with |x| <= v (both signs, zeros, the
+    subnormals), then v itself, zero-padded to n entries."""
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    vals = (bits.astype(np.uint32) << 16).view(np.float32)
+    vals = vals[np.isfinite(vals) & (np.abs(vals) <= v)]
+    out = np.zeros(n, dtype=np.float32)
+    out[:vals.size] = vals
+    out[-1] = v
+    return torch.from_numpy(out).to(torch.bfloat16)
+
+
+# amax values: 448 (s = 1: every midpoint exact, ties to even), 1344
+# (s = 3), powers of two, a spread of bf16 values with many mantissa bits,
+# and amax so small that 1 / s overflows (1e-37) or s is an fp32 denormal
+AMAXES = [448.0, 1344.0, 1.0, 2.0 ** -20, 0.0302734375, 0.71484375, 3.140625,
+          5.15625, 11.8125, 97.5, 1000.0, 3.3e4, 6.5e5, 1.17e-7, 2.3e-3,
+          0.1796875, 7.90625, 250.0, 1.1e9, 1.9e-30, 1.0e-37, 1.0e-39]
+
+
+@pytest.mark.parametrize("amax", AMAXES)
+def test_fp8_quantizers_on_every_bf16_value(amax):
+    """Every finite bf16 value below a scale's amax, through the weight
+    quantizer (plain and transposed codes) and the activation quantizer,
+    bit for bit against the oracle's fp32 division and E4M3 rounding."""
+    from tensor_transformer_mlp_tcgen05_gb300.mlp import TensorParallelMLP
+    v = float(torch.tensor(amax).to(torch.bfloat16))
+    A = _all_bf16_up_to(v, 128 * 512).reshape(128, 512)
+    qa, sa = F.quantize(f64(A))
+    m = TensorParallelMLP(128, 512, 1, 128, dtype="bf16")
+    B = torch.zeros((512, 128), dtype=torch.bfloat16)
+    packed = m.pack_fp8_weights(A.cuda(), B.cuda())
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(m.fp8_saved(128, "aq", packed).cpu().numpy(), qa)
+    np.testing.assert_array_equal(m.fp8_saved(128, "aqt", packed).cpu().numpy(),
+                                  qa.T)
+    assert _f32(m.fp8_saved(128, "wscales", packed).cpu().numpy()[2]) == sa
+    m.close()
+    # the activation quantizer (plain and, in a training forward, transposed)
+    X = _all_bf16_up_to(v, 128 * 512).reshape(128, 512)
+    qx, sx = F.quantize(f64(X))
+    m = TensorParallelMLP(512, 512, 1, 128, dtype="bf16")
+    Aw = torch.zeros((512, 512), dtype=torch.bfloat16, device="cuda")
+    packed = m.pack_fp8_weights(Aw, Aw)
+    for train in (False, True):
+        m.forward_fp8(X.cuda(), packed, train=train)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(m.fp8_saved(128, "xq").cpu().numpy(), qx)
+        assert _f32(m.fp8_saved(128, "scales").cpu().numpy()[2]) == sx
+        if train:
+            np.testing.assert_array_equal(
+                m.fp8_saved(128, "xqt").cpu().numpy(), qx.T)
+    m.close()
