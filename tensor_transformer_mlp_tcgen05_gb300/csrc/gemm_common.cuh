@@ -186,6 +186,11 @@ struct ChunkStager {
     return buf;
   }
 
+  // The buffer the k-th next put will use.
+  __device__ __forceinline__ uint32_t buffer(uint32_t k) const {
+    return base + ((count + k) & 1u) * STAGE_CHUNK_BYTES;
+  }
+
   __device__ __forceinline__ void drain(int lane) {
     if (lane == 0) ptx::bulk_wait_all();
     __syncwarp();

@@ -69,7 +69,9 @@ constexpr uint32_t B_STAGE_BYTES = HN * BK * 2;  // 16 KiB
 constexpr uint32_t STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
 constexpr uint32_t PAIR_STAGE_BYTES = 2 * STAGE_BYTES;
 constexpr uint32_t TMEM_COLS = 2 * PN;
-constexpr int NUM_BARRIERS = 2 * STAGES + 5;
+// full, empty (per stage), tfull, tempty (per accumulator), done, and one
+// per epilogue warp for EPI_GELU_BWD's H chunks
+constexpr int NUM_BARRIERS = 2 * STAGES + 5 + NUM_EPI_WARPS;
 constexpr uint32_t EPI_STAGING_BYTES = NUM_EPI_WARPS * 2 * STAGE_CHUNK_BYTES;
 constexpr size_t SMEM_BYTES = 1024 + size_t(STAGES) * STAGE_BYTES +
                               EPI_STAGING_BYTES + NUM_BARRIERS * 8 + 16;
@@ -126,6 +128,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tfull0 = bar0 + 16u * STAGES;
   const uint32_t tempty0 = tfull0 + 16u;
   const uint32_t done_bar = tempty0 + 16u;
+  const uint32_t hbar0 = done_bar + 8u;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARRIERS);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
@@ -156,6 +159,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ptx::mbar_init(tempty0 + 8u * b, 2 * NUM_EPI_WARPS);
     }
     ptx::mbar_init(done_bar, 1);
+    for (int w = 0; w < NUM_EPI_WARPS; ++w) ptx::mbar_init(hbar0 + 8u * w, 1);
     *abort_flag = 0;
     ptx::fence_barrier_init();
   }
@@ -163,6 +167,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ptx::prefetch_tmap(&tmA);
     ptx::prefetch_tmap(&tmB);
     ptx::prefetch_tmap(&tmO);
+    if constexpr (EPI == EPI_GELU_BWD) ptx::prefetch_tmap(&tmO2);
   }
   if (warp == 1) {
     ptx::tmem_alloc_pair(ptx::smem_u32(tmem_slot), TMEM_COLS);
@@ -329,6 +334,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                    0u};
     // E4M3 operands: the product of the two per-tensor scales.
     const float acc_scale = F8 ? *args.scale_a * *args.scale_b : 1.f;
+    // EPI_GELU_BWD: this warp's barrier for its H chunks, and its phase
+    const uint32_t hbar = hbar0 + 8u * static_cast<uint32_t>(ew);
+    uint32_t hphase = 0;
     uint32_t acc = 0;
     bool alive = true;
     for (int sup = group; alive && sup < num_super; sup += num_groups) {
@@ -341,6 +349,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int col_base = nb * PN + half * 128;
       float S[EPI == EPI_SHARDSUM ? 128 : 1];
       uint32_t cbuf[2] = {0u, 0u};   // EPI_GELU_BWD: the staged dH chunks
+      // EPI_GELU_BWD: this warp's two 32 x 64 chunks of H are copied by TMA
+      // into the two staging buffers the dH chunks will be written from
+      // (once those buffers' earlier stores have read them), in flight
+      // while the accumulator is computed; each lane then reads its row
+      // there, writes its dH row over it and stores the chunk.  One full-line
+      // copy per chunk instead of row-strided loads.
+      const int hchunks = (EPI == EPI_GELU_BWD && live)
+                              ? (col_base < args.N) + (col_base + 64 < args.N)
+                              : 0;
+      if constexpr (EPI == EPI_GELU_BWD) {
+        if (hchunks > 0) {
+          ptx::fence_proxy_async_shared();  // earlier reads of the buffers
+          __syncwarp();
+          if (lane == 0) {
+            ptx::bulk_wait_read<0>();
+            ptx::mbar_arrive_expect_tx(hbar, hchunks * STAGE_CHUNK_BYTES);
+            for (int j = 0; j < hchunks; ++j)
+              ptx::tma_load_2d(st.buffer(j), &tmO2, hbar, col_base + 64 * j,
+                               row0);
+          }
+        }
+      }
       for (int seg = 0; seg < args.num_seg; ++seg, ++acc) {
         const uint32_t b = acc & 1u;
         const uint32_t aph = (acc >> 1) & 1u;
@@ -349,6 +379,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!ok) {
           alive = false;
           break;
+        }
+        if constexpr (EPI == EPI_GELU_BWD) {
+          if (hchunks > 0) {
+            bool hok = wait_bounded(hbar, hphase, ctl, ROLE_EPILOGUE);
+            hok = __all_sync(0xffffffffu, hok);
+            hphase ^= 1u;
+            if (!hok) {
+              alive = false;
+              break;
+            }
+          }
         }
         ptx::tc_fence_after();
         const uint32_t taddr =
@@ -426,23 +467,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                   if (lane == 0) atomicMax(args.amax_out, wm);
                 }
               } else {
-                if (row < args.M) {
-                  const uint4* hp = reinterpret_cast<const uint4*>(
-                      static_cast<const __nv_bfloat16*>(args.aux) +
-                      static_cast<size_t>(row) * args.ldaux + c0);
+                // H from the staged chunk (128-byte-swizzled rows)
+                const uint32_t hrow =
+                    st.buffer(0) + static_cast<uint32_t>(lane) * 128u;
 #pragma unroll
-                  for (int i = 0; i < 8; ++i) {
-                    const uint4 u = hp[i];
-                    const uint32_t hw[4] = {u.x, u.y, u.z, u.w};
+                for (int i = 0; i < 8; ++i) {
+                  uint32_t hw[4];
+                  ptx::ld_shared_v4(
+                      hrow + static_cast<uint32_t>(i ^ (lane & 7)) * 16u, hw);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                      float h0, h1;
-                      unpack_bf16x2(hw[k], h0, h1);
-                      float g0, g1;
-                      gelu_grad2_f32(h0, h1, g0, g1, args.gelu_mode);
-                      v[8 * i + 2 * k + 0] *= g0;
-                      v[8 * i + 2 * k + 1] *= g1;
-                    }
+                  for (int k = 0; k < 4; ++k) {
+                    float h0, h1;
+                    unpack_bf16x2(hw[k], h0, h1);
+                    float g0, g1;
+                    gelu_grad2_f32(h0, h1, g0, g1, args.gelu_mode);
+                    v[8 * i + 2 * k + 0] *= g0;
+                    v[8 * i + 2 * k + 1] *= g1;
                   }
                 }
                 if (F8 && args.amax_out != nullptr) {

@@ -279,7 +279,8 @@ inline int b_box_rows() { return use_pairs() ? TC2_BN_HALF : TC_BN; }
 // maps must then use TC2_BN_HALF-row boxes).  The pair kernel writes through
 // output tensor maps,
 // encoded here from args.out / args.out2 (row-major, leading dimension
-// args.ldo, element type fp32 for the fp32-output epilogues).
+// args.ldo, element type fp32 for the fp32-output epilogues); EPI_GELU_BWD
+// reads H through the second map (args.aux, leading dimension args.ldaux).
 inline int tc_gemm(HandleCore* H, const char* name, cudaStream_t s, int sms,
             int epi, bool a_mn, bool b_mn, const CUtensorMap& ta,
             const CUtensorMap& tb, const GemmArgs& args,
@@ -288,7 +289,9 @@ inline int tc_gemm(HandleCore* H, const char* name, cudaStream_t s, int sms,
     const bool f32 = epi == EPI_STORE_F32 || (epi == EPI_SHARDSUM && args.out_f32);
     CUtensorMap to, to2;
     TRY(out_map(&to, args.out, f32, args.M, args.N, args.ldo));
-    if (args.out2 != nullptr) {
+    if (epi == EPI_GELU_BWD) {
+      TRY(out_map(&to2, args.aux, false, args.M, args.N, args.ldaux));
+    } else if (args.out2 != nullptr) {
       TRY(out_map(&to2, args.out2, false, args.M, args.N, args.ldo));
     } else {
       to2 = to;  // unused by the kernel

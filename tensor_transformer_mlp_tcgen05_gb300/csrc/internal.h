@@ -25,7 +25,8 @@ cudaError_t launch_gemm_tc(int epi, bool a_mn, bool b_mn, const CUtensorMap& ta,
 // K-major B operands must be encoded with 128-row boxes (each CTA stages half
 // of the tile's N).  Outputs are written through tensor maps: `to` for
 // args.out and `to2` for args.out2 (EPI_GELU_FWD's H), 128-byte-swizzled
-// boxes of 32 rows x 128 bytes (64 bf16 or 32 fp32 columns).  At most
+// boxes of 32 rows x 128 bytes (64 bf16 or 32 fp32 columns); EPI_GELU_BWD
+// reads H (args.aux) through `to2`, encoded the same way.  At most
 // `max_pairs` clusters are launched.
 constexpr int TC2_BN_HALF = 128;
 cudaError_t launch_gemm_tc2(int epi, bool a_mn, bool b_mn,

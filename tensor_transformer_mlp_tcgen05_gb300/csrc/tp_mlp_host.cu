@@ -806,9 +806,11 @@ int tp_mlp_backward_fp8(tp_mlp_handle* H, int tokens, const void* dZ,
   }
   TRY(encode_map_u8(&ta, dZq, h, T, h, TC_BM));
   TRY(encode_map_u8(&tb, pk + P.bq, h, f, h, TC2_BN_HALF));
+  CUtensorMap th;  // H, read by the epilogue through a tensor map
   TRY(out_map(&to, dH, false, T, f, f));
+  TRY(out_map(&th, ws + L.hb, false, T, f, f));
   TRY(run(&H->core, "gemm_dh_gelu_bwd_fp8", s, [&] {
-    return launch_gemm_tc2_e4m3(EPI_GELU_BWD, ta, tb, to, to, gy, sms / 2, s);
+    return launch_gemm_tc2_e4m3(EPI_GELU_BWD, ta, tb, to, th, gy, sms / 2, s);
   }));
   TRY(run(&H->core, "fp8_quantize_dh", s, [&] {
     return launch_quantize_e4m3_rt(dH, T, f, bamax + 1, dHq, dHqT, tp,
