@@ -96,8 +96,11 @@ inline int colsum_chunks(int rows) {
 }
 
 // part[chunk][c] = sum over the chunk's rows of src[r][c] (src bf16/fp32).
+// amax (nullable): raised to the largest |src| (fp32 bits), as
+// launch_amax_bf16 does, from the same read.
 cudaError_t launch_colsum_partial(bool bf16, const void* src, float* part,
-                                  int rows, int cols, cudaStream_t stream);
+                                  int rows, int cols, cudaStream_t stream,
+                                  unsigned int* amax = nullptr);
 
 // LayerNorm parameter gradients, stage 1: part_g[chunk][c] = sum dXn * xhat,
 // part_b[chunk][c] = sum dXn over the chunk's rows.

@@ -286,8 +286,10 @@ __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* p,
       make_uint2(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]));
 }
 
-// MODE 0: part1 = sum src.  MODE 1 (LayerNorm parameters): part1 = sum
-// dXn * xhat, part2 = sum dXn, with xhat recomputed from X, mean, rstd.
+// MODE 0: part1 = sum src, and, when amax is not null, *amax raised to the
+// largest |src| (fp32 bits; a maximum is order-free, so deterministic).
+// MODE 1 (LayerNorm parameters): part1 = sum dXn * xhat, part2 = sum dXn,
+// with xhat recomputed from X, mean, rstd.
 template <typename T, int MODE>
 __global__ void __launch_bounds__(CS_WARPS * 32)
     colsum_partial_kernel(const T* __restrict__ src,
@@ -295,8 +297,9 @@ __global__ void __launch_bounds__(CS_WARPS * 32)
                           const float* __restrict__ mean,
                           const float* __restrict__ rstd,
                           float* __restrict__ part1, float* __restrict__ part2,
-                          int rows, int cols) {
+                          int rows, int cols, unsigned int* amax) {
   __shared__ float red[2][CS_WARPS][CS_COLS];
+  float mx = 0.f;
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x * CS_COLS + lane * 4;
   const int chunk = blockIdx.y;
@@ -310,7 +313,10 @@ __global__ void __launch_bounds__(CS_WARPS * 32)
         float v[4];
         load4<T>(src + off, v);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) a1[k] += v[k];
+        for (int k = 0; k < 4; ++k) {
+          a1[k] += v[k];
+          mx = fmaxf(mx, fabsf(v[k]));
+        }
       } else {
         float x[4], d[4];
         load4<T>(src + off, x);
@@ -328,6 +334,10 @@ __global__ void __launch_bounds__(CS_WARPS * 32)
   for (int k = 0; k < 4; ++k) {
     red[0][w][lane * 4 + k] = a1[k];
     red[1][w][lane * 4 + k] = a2[k];
+  }
+  if (MODE == 0 && amax != nullptr) {
+    const unsigned int wm = __reduce_max_sync(0xffffffffu, __float_as_uint(mx));
+    if (lane == 0) atomicMax(amax, wm);
   }
   __syncthreads();
   const int nout = (MODE == 0) ? 1 : 2;
@@ -467,16 +477,17 @@ cudaError_t launch_ln_bwd(bool bf16, const float* dXn, const void* X,
 }
 
 cudaError_t launch_colsum_partial(bool bf16, const void* src, float* part,
-                                  int rows, int cols, cudaStream_t stream) {
+                                  int rows, int cols, cudaStream_t stream,
+                                  unsigned int* amax) {
   const dim3 grid((cols + CS_COLS - 1) / CS_COLS, colsum_chunks(rows));
   if (bf16) {
     colsum_partial_kernel<__nv_bfloat16, 0><<<grid, CS_WARPS * 32, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(src), nullptr, nullptr, nullptr,
-        part, nullptr, rows, cols);
+        part, nullptr, rows, cols, amax);
   } else {
     colsum_partial_kernel<float, 0><<<grid, CS_WARPS * 32, 0, stream>>>(
         static_cast<const float*>(src), nullptr, nullptr, nullptr, part,
-        nullptr, rows, cols);
+        nullptr, rows, cols, amax);
   }
   return cudaGetLastError();
 }
@@ -489,11 +500,11 @@ cudaError_t launch_ln_param_partial(bool bf16, const float* dXn, const void* X,
   if (bf16) {
     colsum_partial_kernel<__nv_bfloat16, 1><<<grid, CS_WARPS * 32, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(X), dXn, mean, rstd, part_g, part_b,
-        rows, h);
+        rows, h, nullptr);
   } else {
     colsum_partial_kernel<float, 1><<<grid, CS_WARPS * 32, 0, stream>>>(
         static_cast<const float*>(X), dXn, mean, rstd, part_g, part_b, rows,
-        h);
+        h, nullptr);
   }
   return cudaGetLastError();
 }

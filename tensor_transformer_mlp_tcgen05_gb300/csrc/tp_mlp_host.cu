@@ -787,9 +787,16 @@ int tp_mlp_backward_fp8(tp_mlp_handle* H, int tokens, const void* dZ,
   float* part = reinterpret_cast<float*>(ws + L.part);
   float* part1 = part + size_t(L.chunks) * h;  // db1 partials
 
-  // dZ: current amax, then codes in both layouts from one read
-  TRY(run(&H->core, "fp8_amax_dz", s,
-          [&] { return launch_amax_bf16(dZ, size_t(T) * h, bamax, s); }));
+  // dZ: current amax (from the db2 column-sum pass when db2 is wanted, which
+  // reads dZ anyway), then codes in both layouts from one read
+  if (dbias2) {
+    TRY(run(&H->core, "colsum_db2_amax_dz", s, [&] {
+      return launch_colsum_partial(true, dZ, part, T, h, s, bamax);
+    }));
+  } else {
+    TRY(run(&H->core, "fp8_amax_dz", s,
+            [&] { return launch_amax_bf16(dZ, size_t(T) * h, bamax, s); }));
+  }
   TRY(run(&H->core, "fp8_quantize_dz", s, [&] {
     return launch_quantize_e4m3_rt(dZ, T, h, bamax, dZq, dZqT, tp, bscl, s);
   }));
@@ -816,7 +823,10 @@ int tp_mlp_backward_fp8(tp_mlp_handle* H, int tokens, const void* dZ,
     return launch_quantize_e4m3_rt(dH, T, f, bamax + 1, dHq, dHqT, tp,
                                    bscl + 1, s);
   }));
-  if (dbias2) TRY(colsum(&H->core, "colsum_db2", s, true, dZ, part, dbias2, T, h));
+  if (dbias2)
+    TRY(run(&H->core, "colsum_finalize", s, [&] {
+      return launch_colsum_finalize(part, dbias2, L.chunks, h, s);
+    }));
   if (dbias1)
     TRY(run(&H->core, "colsum_finalize", s, [&] {
       return launch_colsum_finalize(part1, dbias1, L.groups, f, s);
