@@ -215,3 +215,30 @@ def test_backward_close_to_the_unquantized_block(ln, res):
     for k in ("dX", "dA", "dB", "db1", "db2") + (("dgamma", "dbeta") if ln else ()):
         rel = np.linalg.norm(bwd[k] - pb[k]) / np.linalg.norm(pb[k])
         assert rel < 0.15, (k, rel)
+
+
+@pytest.mark.parametrize("amax", [448.0, 1.0, 3.140625, 97.5, 6.5e5, 1.9e-30,
+                                  2.0 ** 100 * 1.5])
+def test_codes_vanish_22_binades_below_amax(amax):
+    """The GPU quantizers enumerate the codes of the 22 binades at and below
+    amax's and take every smaller magnitude as code +-0: with s = amax / 448
+    any |x| < 2^(e_amax - 21) has |x / s| < 448 * 2^-21 < 2^-10, half the
+    smallest E4M3 subnormal.  Every bf16 value of those smaller binades
+    (both signs) must quantize to a zero code; and the binade 18 below
+    amax's, whose top exceeds amax 2^-18 >= 2^-10 s, must still give
+    nonzero codes (the table's 22 binades leave a margin of three)."""
+    v = float(torch.tensor(amax).to(torch.bfloat16))
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    vals = (bits.astype(np.uint32) << 16).view(np.float32)
+    e_amax = (np.array([v], dtype=np.float32).view(np.uint32)[0] >> 23) & 0xFF
+    ebits = (vals.view(np.uint32) >> 23) & 0xFF
+    below = np.isfinite(vals) & (ebits < e_amax - 21)
+    x = np.append(vals[below], v).astype(np.float64)
+    codes, s = F.quantize(x)
+    assert s == np.float32(v) / np.float32(448.0)
+    assert not (codes[:-1] & 0x7F).any()
+    assert codes[-1] & 0x7F == 0x7E                      # amax itself: 448
+    # the binade 18 below amax's still reaches the smallest subnormal
+    near = np.isfinite(vals) & (ebits == e_amax - 18) & (vals > 0)
+    c2, _ = F.quantize(np.append(vals[near], v).astype(np.float64))
+    assert (c2[:-1] & 0x7F).max() >= 1
