@@ -9,6 +9,7 @@
 #include <cuda_fp8.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace tpmlp {
 namespace {
@@ -80,11 +81,13 @@ __global__ void __launch_bounds__(QT)
 // load per value.  When that range would reach the bf16 subnormals (amax
 // below 2^-105) or amax is 0, every value takes the division instead.
 constexpr int QTAB_E = 22;
-constexpr int QTAB_N = 1 + QTAB_E * 128;   // entry 0: code 0 (below range)
+// entries 0 .. QTAB_E * 128 - 1: the magnitudes from 2^(e_amax - 21) up;
+// the last entry, code 0, takes every magnitude outside that range
+constexpr int QTAB_N = QTAB_E * 128 + 1;
 
 struct Quantizer {
-  const uint8_t* tab;   // shared memory, QTAB_N codes
-  int base1;            // index = (bits & 0x7fff) - base1, clamped
+  uint32_t tab;         // shared-memory address of the QTAB_N codes
+  uint32_t base;        // index = (bits & 0x7fff) - base, unsigned, clamped
   float s;
   bool use_tab;
 };
@@ -94,14 +97,13 @@ __device__ __forceinline__ Quantizer make_quantizer(uint8_t* tab,
                                                     unsigned int amax_bits) {
   const float s = scale_from_amax(amax_bits);
   const int e_lo = static_cast<int>((amax_bits >> 23) & 0xFFu) - (QTAB_E - 1);
-  const Quantizer z{tab, (e_lo << 7) - 1, s, amax_bits != 0u && e_lo >= 1};
+  const Quantizer z{ptx::smem_u32(tab), static_cast<uint32_t>(e_lo) << 7, s,
+                    amax_bits != 0u && e_lo >= 1};
   if (z.use_tab) {
     for (int i = threadIdx.x; i < QTAB_N; i += blockDim.x) {
       uint8_t code = 0;
-      if (i > 0) {
-        const uint32_t mag = static_cast<uint32_t>((e_lo << 7) + i - 1);
-        code = to_e4m3(__uint_as_float(mag << 16), s);
-      }
+      if (i < QTAB_N - 1)
+        code = to_e4m3(__uint_as_float((z.base + static_cast<uint32_t>(i)) << 16), s);
       tab[i] = code;
     }
   }
@@ -109,16 +111,22 @@ __device__ __forceinline__ Quantizer make_quantizer(uint8_t* tab,
   return z;
 }
 
+__device__ __forceinline__ uint32_t ld_shared_u8(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
 // Two bf16 values (one word) to two codes in the low 16 bits, the first
-// value lowest.
+// value lowest.  A magnitude below the table's range wraps around in the
+// unsigned subtraction and lands, like one above it, on the last entry.
 __device__ __forceinline__ uint32_t q_pair(const Quantizer& z, uint32_t w) {
   if (z.use_tab) {
-    const int tlo =
-        min(max(static_cast<int>(w & 0x7FFFu) - z.base1, 0), QTAB_N - 1);
-    const int thi =
-        min(max(static_cast<int>((w >> 16) & 0x7FFFu) - z.base1, 0), QTAB_N - 1);
-    const uint32_t lo = z.tab[tlo], hi = z.tab[thi];
-    return lo | (hi << 8) | ((w >> 8) & 0x80u) | ((w >> 16) & 0x8000u);
+    const uint32_t tlo = min((w & 0x7FFFu) - z.base, uint32_t(QTAB_N - 1));
+    const uint32_t thi = min(((w >> 16) & 0x7FFFu) - z.base, uint32_t(QTAB_N - 1));
+    // the two sign bits, moved to bits 7 and 15
+    const uint32_t signs = __byte_perm(w, 0u, 0x4431u) & 0x8080u;
+    return ld_shared_u8(z.tab + tlo) | (ld_shared_u8(z.tab + thi) << 8) | signs;
   }
   float a, b;
   unpack_bf16x2(w, a, b);
