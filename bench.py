@@ -945,8 +945,9 @@ def run_ours_fp8(args, w, rank, world, local_rank):
                 "unit": "TFLOP/s", "frac": round(ach / pk, 4),
                 "peak_kind": f"fp8 = 2 x measured bf16 {pkind} ({peak_src}; "
                              "nominal fp8:bf16 ratio 4.5:2.25)",
-                "traffic": traffic_of(w.name + "_fp8", top["name"])
-                if not (args.tokens or args.shards or args.residual or train)
+                "traffic": traffic_of(w.name + ("_fp8_train" if train
+                                                else "_fp8"), top["name"])
+                if not (args.tokens or args.shards or args.residual)
                 else None}
     line = {
         "metric": METRIC_FP8_TRAIN if train else METRIC_FP8,
