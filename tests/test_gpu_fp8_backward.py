@@ -24,15 +24,15 @@ SECTIONS = ("xq", "yq", "h", "dh", "dzq", "dhq", "xqt", "yqt", "dzqt", "dhqt",
             "scales", "bscales")
 
 
-def _mlp(w, residual=False):
+def _mlp(w, residual=False, gelu="erf"):
     from tensor_transformer_mlp_tcgen05_gb300.mlp import TensorParallelMLP
     return TensorParallelMLP(w.hidden, w.ffn, w.shards, max(w.tokens, 1),
                              dtype="bf16", layernorm=w.layernorm,
-                             residual=residual)
+                             residual=residual, gelu=gelu)
 
 
-def run_step(w, inp, residual=False, repeat=1, bias_grads=True):
-    m = _mlp(w, residual)
+def run_step(w, inp, residual=False, repeat=1, bias_grads=True, gelu="erf"):
+    m = _mlp(w, residual, gelu)
     d = {k: (None if v is None else v.cuda().contiguous()) for k, v in inp.items()}
     packed = m.pack_fp8_weights(d["A"], d["B"])
     outs = []
@@ -60,12 +60,12 @@ def _f32(word):
     return np.array([word], dtype=np.int32).view(np.float32)[0]
 
 
-def check(inp, got, residual=False, bias_grads=True):
+def check(inp, got, residual=False, bias_grads=True, gelu="erf"):
     fwd = F.forward(f64(inp["X"]), f64(inp["A"]), f64(inp["B"]),
                     f64(inp["b1"]), f64(inp["b2"]), f64(inp["gamma"]),
-                    f64(inp["beta"]), residual=residual)
+                    f64(inp["beta"]), mode=gelu, residual=residual)
     ref = F.backward(f64(inp["dZ"]), f64(inp["X"]), fwd, f64(inp["gamma"]),
-                     residual=residual)
+                     mode=gelu, residual=residual)
     # the plain weight codes the backward reads: exactly the oracle's
     np.testing.assert_array_equal(got["aq"], fwd["qa"])
     np.testing.assert_array_equal(got["bq"], fwd["qb"])
@@ -92,18 +92,19 @@ def check(inp, got, residual=False, bias_grads=True):
         assert_close("dbeta", got["dbeta"], ref["dbeta"])
 
 
-CASES = [  # tokens, hidden, ffn, shards, layernorm, bias, residual
-    (300, 256, 1024, 2, False, True, False),
-    (129, 256, 1024, 8, False, False, True),
-    (1, 128, 512, 1, False, True, False),
-    (513, 384, 1536, 4, True, True, True),
-    (1000, 192, 768, 3, False, True, True),
-    (77, 256, 512, 2, True, False, False),
+CASES = [  # tokens, hidden, ffn, shards, layernorm, bias, residual, GeLU
+    (300, 256, 1024, 2, False, True, False, "erf"),
+    (129, 256, 1024, 8, False, False, True, "erf"),
+    (1, 128, 512, 1, False, True, False, "erf"),
+    (513, 384, 1536, 4, True, True, True, "erf"),
+    (1000, 192, 768, 3, False, True, True, "erf"),
+    (77, 256, 512, 2, True, False, False, "erf"),
+    (640, 256, 1024, 4, True, True, True, "tanh"),
 ]
 
 
-@pytest.mark.parametrize("T,h,f,t,ln,bias,res", CASES)
-def test_fp8_training_step_parity(T, h, f, t, ln, bias, res):
+@pytest.mark.parametrize("T,h,f,t,ln,bias,res,gelu", CASES)
+def test_fp8_training_step_parity(T, h, f, t, ln, bias, res, gelu):
     w = W.WORKLOADS["gpt3_13b"].with_(tokens=T, hidden=h, ffn=f, shards=t,
                                        layernorm=ln, w_std=0.05)
     inp = W.make_inputs(w, seed=3 * T + t, with_bias=bias,
@@ -112,8 +113,8 @@ def test_fp8_training_step_parity(T, h, f, t, ln, bias, res):
         g = torch.Generator().manual_seed(11)
         inp["gamma"] = 1 + 0.2 * torch.randn(h, generator=g)
         inp["beta"] = 0.2 * torch.randn(h, generator=g)
-    check(inp, run_step(w, inp, residual=res, bias_grads=bias),
-          residual=res, bias_grads=bias)
+    check(inp, run_step(w, inp, residual=res, bias_grads=bias, gelu=gelu),
+          residual=res, bias_grads=bias, gelu=gelu)
 
 
 def test_fp8_backward_zero_tokens_and_zero_gradient():
