@@ -1032,10 +1032,39 @@ def run_cpu_baseline(w, inp):
     tokens = oracle_tokens(w)
     secs = oracle_sample(w, inp, tokens)
     flops = (w.flops_fwd_bwd(tokens) if w.backward else w.flops_fwd(tokens))
-    return {"value": round(flops / secs / 1e12, 5), "unit": "TFLOP/s",
+    line = {"value": round(flops / secs / 1e12, 5), "unit": "TFLOP/s",
             "cores": os.cpu_count(), "kind": "oracle",
             "sample": f"first {tokens} of {w.tokens} tokens, fp64 "
                       f"{'fwd+bwd' if w.backward else 'fwd'} ({secs:.1f} s)"}
+    line["one_core"] = oracle_one_core(w, max(16, tokens // 16))
+    return line
+
+
+def oracle_one_core(w, tokens):
+    """The same oracle sample on one host thread: a child process started
+    with the BLAS and OpenMP thread counts set to 1 before numpy loads,
+    on the same seeded inputs (regenerated there), `tokens` rows."""
+    code = (
+        "import sys, json; sys.path.insert(0, %r); import bench; "
+        "from tensor_transformer_mlp_tcgen05_gb300 import workloads as W; "
+        "w = W.WORKLOADS[%r].with_(tokens=%d, shards=%d); "
+        "inp = W.make_inputs(w, seed=0); "
+        "print(json.dumps(bench.oracle_sample(w, inp, %d)))"
+        % (ROOT, w.name, w.tokens, w.shards, tokens))
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS",
+              "BLIS_NUM_THREADS", "VECLIB_MAXIMUM_THREADS"):
+        env[k] = "1"
+    try:
+        out = subprocess.run([sys.executable, "-c", code], env=env,
+                             capture_output=True, text=True, timeout=600)
+        secs = float(out.stdout.strip().splitlines()[-1])
+    except Exception as e:  # reported, not fatal: the all-core figure stands
+        return {"error": f"{type(e).__name__}: {e}"[:200]}
+    flops = (w.flops_fwd_bwd(tokens) if w.backward else w.flops_fwd(tokens))
+    return {"value": round(flops / secs / 1e12, 5), "unit": "TFLOP/s",
+            "threads": 1, "sample": f"first {tokens} of {w.tokens} tokens "
+                                    f"({secs:.1f} s)"}
 
 
 def run_reference(args, w):
