@@ -200,6 +200,22 @@ def _src_sha(files=_SRC_FILES["gemm"]):
     return h.hexdigest()[:16]
 
 
+def timed_steps(torch, stream, step, steps):
+    """Run `steps` steps with a CUDA event on `stream` before each and after
+    the last; returns (mean ms per step over the whole region, per-step
+    median / min / max in ms)."""
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    evs[0].record(stream)
+    for i in range(steps):
+        step()
+        evs[i + 1].record(stream)
+    torch.cuda.synchronize()
+    per = [evs[i].elapsed_time(evs[i + 1]) for i in range(steps)]
+    stats = {"median": round(statistics.median(per), 4),
+             "min": round(min(per), 4), "max": round(max(per), 4)}
+    return evs[0].elapsed_time(evs[-1]) / steps, stats
+
+
 # ------------------------------------------------------------ clocks ----
 
 class ClockSampler:
@@ -359,17 +375,10 @@ def run_ours(args, w, rank, world, local_rank):
     barrier(world)
     torch.cuda.synchronize()
     n0 = Bn.tp_mlp_launch_count(m.handle)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        step()
-    e1.record(stream)
-    torch.cuda.synchronize()
+    ms, step_ms = timed_steps(torch, stream, step, args.steps)
     barrier(world)
     clocks = sampler.stop()
     launches = Bn.tp_mlp_launch_count(m.handle) - n0
-    ms = e0.elapsed_time(e1) / args.steps
     if m.check() != 0:
         raise RuntimeError("device status after timing: " + Bn.tp_mlp_last_detail())
     kernels = Bn.tp_mlp_timing_get(m.handle)
@@ -470,7 +479,8 @@ def run_ours(args, w, rank, world, local_rank):
         "frac_of_peak": round(tflops / (world * peak_b), 4),
         "peak_tflops": peak_b, "peak_kind": f"bf16 burst ({peak_src})",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(ms_max, 4), "higher_is_better": True,
+        "ms_per_step": round(ms_max, 4), "step_ms": step_ms,
+        "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic: seeded N(0,1) activations and upstream gradient, "
                 f"N(0,{w.w_std}^2) weights",
@@ -613,17 +623,10 @@ def run_ours_attn(args, w, rank, world, local_rank):
     barrier(world)
     torch.cuda.synchronize()
     n0 = Bn.tp_attn_launch_count(m.handle)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        step()
-    e1.record(stream)
-    torch.cuda.synchronize()
+    ms, step_ms = timed_steps(torch, stream, step, args.steps)
     barrier(world)
     clocks = sampler.stop()
     launches = Bn.tp_attn_launch_count(m.handle) - n0
-    ms = e0.elapsed_time(e1) / args.steps
     if m.check() != 0:
         raise RuntimeError("device status after timing: "
                            + Bn.tp_mlp_last_detail())
@@ -710,7 +713,8 @@ def run_ours_attn(args, w, rank, world, local_rank):
         "frac_of_peak": round(tflops / (world * peak_b), 4),
         "peak_tflops": peak_b, "peak_kind": f"bf16 burst ({peak_src})",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(ms_max, 4), "higher_is_better": True,
+        "ms_per_step": round(ms_max, 4), "step_ms": step_ms,
+        "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic: seeded N(0,1) activations and upstream gradient, "
                 f"N(0,{w.w_std}^2) weights, N(0,0.25) biases",
@@ -865,7 +869,7 @@ def run_ours_fp8(args, w, rank, world, local_rank):
     barrier(world)
     torch.cuda.synchronize()
     n0 = Bn.tp_mlp_launch_count(m.handle)
-    ms = timed(step, args.steps)
+    ms, step_ms = timed_steps(torch, stream, step, args.steps)
     barrier(world)
     clocks = sampler.stop()
     launches = Bn.tp_mlp_launch_count(m.handle) - n0
@@ -965,7 +969,8 @@ def run_ours_fp8(args, w, rank, world, local_rank):
         "frac_of_peak": round(tflops / (world * fp8_burst), 4),
         "peak_tflops": fp8_burst, "peak_kind": "fp8 (2 x measured bf16 burst)",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(ms_max, 4), "higher_is_better": True,
+        "ms_per_step": round(ms_max, 4), "step_ms": step_ms,
+        "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
         "data": "synthetic: seeded N(0,1) activations, "
                 f"N(0,{w.w_std}^2) weights"
