@@ -24,7 +24,8 @@ namespace {
 
 struct AttnLayout {
   size_t status = 0, xn = 0, mean = 0, rstd = 0, qkv = 0, ctx = 0, lse = 0,
-         dctx = 0, delta = 0, dqkv = 0, dxn = 0, part = 0, total = 0;
+         dctx = 0, delta = 0, dqkv = 0, dxn = 0, part = 0, tailp = 0,
+         total = 0;
   int chunks = 0;   // 256-row column-sum chunks
   int groups = 0;   // 32-row groups of the core kernels' fused db_qkv partials
 };
@@ -51,6 +52,7 @@ AttnLayout attn_layout(const tp_attn_config& c, int tokens, int training) {
   L.qkv = take(T * 3 * h * 2);
   L.ctx = take(T * h * 2);
   L.lse = take(H * T * 4);
+  L.tailp = take(static_cast<size_t>(TAIL_PART_BYTES));  // GEMM tail split
   if (training) {
     L.dctx = take(T * h * 2);
     L.delta = take(H * T * 4);
@@ -82,6 +84,8 @@ GemmArgs gemm_args(const tp_attn_handle* H, char* ws, const AttnLayout& L) {
   a.status = reinterpret_cast<int*>(ws + L.status);
   a.budget_ns = H->core.budget_ns;
   a.num_seg = 1;
+  a.part = reinterpret_cast<float*>(ws + L.tailp);
+  a.part_bytes = TAIL_PART_BYTES;
   return a;
 }
 

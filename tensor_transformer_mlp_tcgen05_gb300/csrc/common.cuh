@@ -62,6 +62,17 @@ struct GemmArgs {
   // the bias gradient sum over the tokens.
   float* colsum;
   long long ld_colsum;
+  // Tail split (EPI_SHARDSUM with num_seg >= 2, EPI_STORE_F32; pair kernel).
+  // part / part_bytes (nullable / 0 = off): a caller-owned fp32 buffer.  The
+  // launcher sets tail, pieces and nslots when the last round of super-tiles
+  // would leave groups idle: the last `tail` super-tiles are then computed
+  // as `pieces` items each, over consecutive k-ranges (whole shard segments
+  // for EPI_SHARDSUM, k-blocks for EPI_STORE_F32), whose raw fp32
+  // accumulators go to `part` (nslots 512 x 256 slots per tail super-tile)
+  // and are combined in a fixed order by launch_gemm_tc2_tail.
+  float* part;
+  long long part_bytes;
+  int tail, pieces, nslots;
 };
 
 // Roles recorded in status[1] when a bounded wait gives up.

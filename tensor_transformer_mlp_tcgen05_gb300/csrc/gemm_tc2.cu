@@ -42,7 +42,11 @@
 // consumes the same 32 bytes as a bf16 K = 16 step, so the ring, the
 // descriptors and the tile shapes are unchanged; the epilogue multiplies the
 // fp32 accumulator by the product of the operands' per-tensor scales.
+#include <cstdlib>
+#include <cstring>
+
 #include "gemm_common.cuh"
+#include "host_common.cuh"
 
 namespace tpmlp {
 namespace {
@@ -105,6 +109,47 @@ __device__ __forceinline__ bool wait_bounded_cluster(uint32_t bar,
       return false;
     }
   }
+}
+
+// One unit of a group's work: a whole super-tile, or one piece of a tail
+// super-tile (see GemmArgs::part): segments [seg_lo, seg_hi) and k-blocks
+// [kb_lo, kb_hi), kbs k-blocks per accumulator.
+struct Item {
+  int sup, piece;  // piece -1: the whole super-tile
+  int seg_lo, seg_hi, kb_lo, kb_hi, kbs;
+};
+
+__device__ __forceinline__ Item decode_item(int item, int num_full,
+                                            const GemmArgs& a) {
+  Item it;
+  const int kb_total = a.kb_per_seg * a.num_seg;
+  if (item < num_full) {
+    it.sup = item;
+    it.piece = -1;
+    it.seg_lo = 0;
+    it.seg_hi = a.num_seg;
+    it.kb_lo = 0;
+    it.kb_hi = kb_total;
+    it.kbs = a.kb_per_seg;
+    return it;
+  }
+  const int j = item - num_full;
+  it.sup = num_full + j / a.pieces;
+  it.piece = j % a.pieces;
+  if (a.num_seg > 1) {  // whole shard segments
+    it.seg_lo = a.num_seg * it.piece / a.pieces;
+    it.seg_hi = a.num_seg * (it.piece + 1) / a.pieces;
+    it.kb_lo = it.seg_lo * a.kb_per_seg;
+    it.kb_hi = it.seg_hi * a.kb_per_seg;
+    it.kbs = a.kb_per_seg;
+  } else {              // k-blocks of the single accumulation
+    it.seg_lo = 0;
+    it.seg_hi = 1;
+    it.kb_lo = kb_total * it.piece / a.pieces;
+    it.kb_hi = kb_total * (it.piece + 1) / a.pieces;
+    it.kbs = it.kb_hi - it.kb_lo;
+  }
+  return it;
 }
 
 template <bool A_MN, bool B_MN, int EPI, bool F8>
@@ -184,7 +229,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int num_msup = (num_m + 1) / 2;   // super-tile rows
   const int num_super = num_msup * num_n;
   const int group_sup = args.group_m > 1 ? args.group_m / 2 : 1;
-  const int kb_total = args.kb_per_seg * args.num_seg;
+  // tail split: the first num_full super-tiles whole, then the pieces
+  const int num_full = num_super - args.tail;
+  const int num_items = num_full + args.tail * args.pieces;
   // The even CTA's full and tempty barriers, as cluster addresses.
   const uint32_t lead_full0 = ptx::mapa_shared(full0, lead_rank);
   const uint32_t lead_tempty0 = ptx::mapa_shared(tempty0, lead_rank);
@@ -197,13 +244,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       bool alive = true;
       const uint16_t bmask =
           static_cast<uint16_t>((1u << prank) | (1u << (prank + 2u)));
-      for (int sup = group; alive && sup < num_super; sup += num_groups) {
+      for (int item = group; alive && item < num_items; item += num_groups) {
+        const Item it = decode_item(item, num_full, args);
         int msup, nb;
-        tile_coords(sup, num_msup, num_n, group_sup, msup, nb);
+        tile_coords(it.sup, num_msup, num_n, group_sup, msup, nb);
         const int mb = 2 * msup + pg;   // may lie past M: zero-filled, unused
         const int m0 = mb * PM + static_cast<int>(prank) * HM;
         const int n0 = nb * PN + static_cast<int>(prank) * HN;
-        for (int kb = 0; kb < kb_total; ++kb) {
+        for (int kb = it.kb_lo; kb < it.kb_hi; ++kb) {
           if (!wait_bounded(empty0 + 8u * stage, phase ^ 1u, ctl,
                             ROLE_PRODUCER)) {
             alive = false;
@@ -261,8 +309,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint16_t pair_mask = static_cast<uint16_t>(0x3u << lead_rank);
       uint32_t stage = 0, phase = 0, acc = 0;
       bool alive = true;
-      for (int sup = group; alive && sup < num_super; sup += num_groups) {
-        for (int seg = 0; alive && seg < args.num_seg; ++seg, ++acc) {
+      for (int item = group; alive && item < num_items; item += num_groups) {
+        const Item it = decode_item(item, num_full, args);
+        for (int seg = it.seg_lo; alive && seg < it.seg_hi; ++seg, ++acc) {
           const uint32_t b = acc & 1u;
           const uint32_t aph = (acc >> 1) & 1u;
           if (!wait_bounded_cluster(tempty0 + 8u * b, aph ^ 1u, ctl,
@@ -272,7 +321,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           ptx::tc_fence_after();
           const uint32_t d_tmem = tmem_base + b * PN;
-          for (int kb = 0; kb < args.kb_per_seg; ++kb) {
+          for (int kb = 0; kb < it.kbs; ++kb) {
             if (!wait_bounded(full0 + 8u * stage, phase, ctl, ROLE_MMA)) {
               alive = false;
               break;
@@ -339,11 +388,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t hphase = 0;
     uint32_t acc = 0;
     bool alive = true;
-    for (int sup = group; alive && sup < num_super; sup += num_groups) {
+    for (int item = group; alive && item < num_items; item += num_groups) {
+      const Item it = decode_item(item, num_full, args);
       int msup, nb;
-      tile_coords(sup, num_msup, num_n, group_sup, msup, nb);
+      tile_coords(it.sup, num_msup, num_n, group_sup, msup, nb);
       const int mb = 2 * msup + pg;
       const int row0 = mb * PM + static_cast<int>(prank) * HM + q * 32;
+      // a tail piece's partials: slot rows of this warp in `part` (tmO2)
+      const int prow0 = ((it.sup - num_full) * args.nslots) * 2 * PM +
+                        (row0 - msup * 2 * PM);
+      const int pcol0 = half * 128;
+      // EPI_SHARDSUM: the first later segment (slots 1..) of a tail piece
+      const int s1 = args.pieces > 0 ? args.num_seg / args.pieces : 0;
       const int row = row0 + lane;
       const bool live = row0 < args.M;  // warp-uniform: any row in range
       const int col_base = nb * PN + half * 128;
@@ -371,7 +427,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
       }
-      for (int seg = 0; seg < args.num_seg; ++seg, ++acc) {
+      for (int seg = it.seg_lo; seg < it.seg_hi; ++seg, ++acc) {
         const uint32_t b = acc & 1u;
         const uint32_t aph = (acc >> 1) & 1u;
         bool ok = wait_bounded(tfull0 + 8u * b, aph, ctl, ROLE_EPILOGUE);
@@ -401,7 +457,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t r[32];
             ptx::tmem_ld_32x32b_x32(taddr + j * 32, r);
             ptx::tmem_ld_wait();
-            if (seg == 0) {
+            if (it.piece > 0) {
+              // a later piece of a tail super-tile: each segment's raw
+              // accumulator to its own slot
+              st.put(&tmO2, pcol0 + j * 32,
+                     prow0 + (1 + seg - s1) * 2 * PM, r, lane);
+            } else if (seg == it.seg_lo) {
 #pragma unroll
               for (int i = 0; i < 32; ++i) S[j * 32 + i] = __uint_as_float(r[i]);
             } else {
@@ -416,6 +477,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ptx::tmem_ld_32x32b_x32(taddr + j * 32, r);
             ptx::tmem_ld_wait();
             const int c0 = col_base + j * 32;
+            if (it.piece >= 0) {
+              // a piece of a tail super-tile: the raw accumulator to its slot
+              st.put(&tmO2, pcol0 + j * 32, prow0 + it.piece * 2 * PM, r,
+                     lane);
+              continue;
+            }
             if constexpr (F8) {
 #pragma unroll
               for (int i = 0; i < 32; ++i)
@@ -529,6 +596,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
       if constexpr (EPI == EPI_SHARDSUM) {
+        if (it.piece == 0) {
+          // first piece of a tail super-tile: its running sum, raw, to slot 0
+          if (alive) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              uint32_t w[32];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(S[j * 32 + i]);
+              st.put(&tmO2, pcol0 + j * 32, prow0, w, lane);
+            }
+          }
+        } else if (it.piece < 0) {
         if constexpr (F8) {
 #pragma unroll
           for (int i = 0; i < 128; ++i) S[i] *= acc_scale;
@@ -569,6 +648,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
           }
         }
+        }
       }
     }
     st.drain(lane);
@@ -578,11 +658,77 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
+// Test knobs, read once: TPMLP_GEMM_MAX_PAIRS caps the pairs a launch uses
+// (so that small problems run several rounds); TPMLP_TAIL_SPLIT=0 turns the
+// tail split off, =2 makes it whenever it fits (no cost threshold).
+int env_max_pairs() {
+  static const int v = [] {
+    const char* e = std::getenv("TPMLP_GEMM_MAX_PAIRS");
+    const int n = e ? std::atoi(e) : 0;
+    return n >= 2 ? n : 0;
+  }();
+  return v;
+}
+int env_tail_split() {
+  static const int v = [] {
+    const char* e = std::getenv("TPMLP_TAIL_SPLIT");
+    if (e != nullptr && std::strcmp(e, "0") == 0) return 0;
+    if (e != nullptr && std::strcmp(e, "2") == 0) return 2;
+    return 1;
+  }();
+  return v;
+}
+
+// Tail split plan for `groups` groups of two pairs (see GemmArgs::part):
+// the remainder of the super-tiles over the groups, each cut into as many
+// pieces as there are groups for it (at most the split units: shard
+// segments or k-blocks), reduced until the partials fit `part_bytes`.  Only
+// worth it when the k-blocks taken off the last round, kb_total (P-1)/P,
+// outweigh the pieces' own overhead and the combine pass (about 10 us);
+// measured on the GPT-3-13B-shaped layer, that holds from roughly 96
+// k-blocks (a k-block of MMAs is ~0.27 us at full rate), so shorter splits
+// are not made.
+constexpr int TAIL_MIN_SAVED_KB = 96;
+template <int EPI>
+TailPlan plan_tail(const GemmArgs& a, int groups) {
+  TailPlan p;
+  if (!(EPI == EPI_SHARDSUM || EPI == EPI_STORE_F32)) return p;
+  if (a.part == nullptr || env_tail_split() == 0 || groups < 2 ||
+      a.N % 32 != 0)
+    return p;
+  if (EPI == EPI_SHARDSUM && a.num_seg < 2) return p;
+  const int num_m = (a.M + PM - 1) / PM;
+  const int num_n = (a.N + PN - 1) / PN;
+  const int num_msup = (num_m + 1) / 2;
+  const long long num_super = static_cast<long long>(num_msup) * num_n;
+  const int rem = static_cast<int>(num_super % groups);
+  if (rem == 0) return p;
+  const int units = EPI == EPI_SHARDSUM ? a.num_seg : a.kb_per_seg * a.num_seg;
+  const long long kb_total = static_cast<long long>(a.kb_per_seg) * a.num_seg;
+  for (int P = std::min(groups / rem, units); P >= 2; --P) {
+    if (env_tail_split() != 2 && kb_total * (P - 1) / P < TAIL_MIN_SAVED_KB)
+      break;
+    const int nslots = EPI == EPI_SHARDSUM ? 1 + a.num_seg - a.num_seg / P : P;
+    const long long need =
+        static_cast<long long>(rem) * nslots * (2 * PM) * PN * 4;
+    if (need > a.part_bytes) continue;
+    p.tail = rem;
+    p.pieces = P;
+    p.nslots = nslots;
+    p.num_full = static_cast<int>(num_super) - rem;
+    p.num_msup = num_msup;
+    p.num_n = num_n;
+    p.group_sup = a.group_m > 1 ? a.group_m / 2 : 1;
+    break;
+  }
+  return p;
+}
+
 template <bool A_MN, bool B_MN, int EPI, bool F8 = false>
 cudaError_t launch_impl(const CUtensorMap& ta, const CUtensorMap& tb,
                         const CUtensorMap& to, const CUtensorMap& to2,
                         const GemmArgs& args, int max_pairs,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, TailPlan* plan) {
   auto kern = gemm_tc2_kernel<A_MN, B_MN, EPI, F8>;
   cudaFuncAttributes fa;
   cudaError_t e = cudaFuncGetAttributes(&fa, kern);
@@ -604,6 +750,8 @@ cudaError_t launch_impl(const CUtensorMap& ta, const CUtensorMap& tb,
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (env_max_pairs() > 0 && max_pairs > env_max_pairs())
+    max_pairs = env_max_pairs();
   // Never more pairs than can be resident at once (the kernel is persistent).
   cfg.gridDim = dim3(2 * max_pairs);
   int resident = 0;
@@ -625,9 +773,94 @@ cudaError_t launch_impl(const CUtensorMap& ta, const CUtensorMap& tb,
   attr[1].val.preferredClusterDim.z = 1;
   cfg.numAttrs = 2;
   cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
-  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, to, to2, args);
+  GemmArgs a = args;
+  a.tail = a.pieces = a.nslots = 0;
+  CUtensorMap tp = to2;
+  TailPlan tpl;
+  if (plan != nullptr) tpl = plan_tail<EPI>(args, static_cast<int>(pairs / 2));
+  if (tpl.tail > 0) {
+    // the partials: fp32 [tail x nslots x 512 rows, 256 columns]
+    if (host::out_map(&tp, args.part, true, tpl.tail * tpl.nslots * 2 * PM, PN,
+                      PN) != TPMLP_OK)
+      return cudaErrorInvalidValue;
+    a.tail = tpl.tail;
+    a.pieces = tpl.pieces;
+    a.nslots = tpl.nslots;
+  }
+  if (plan != nullptr) *plan = tpl;
+  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, to, tp, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+// Tail combine: one thread per (tail super-tile, row of 512, 8 columns):
+// two 16-byte loads per slot, up to eight slots' loads in flight at once.
+// Slots are added in slot order, which for EPI_SHARDSUM is the shard order
+// (slot 0: the first piece's running sum; then one slot per later segment),
+// then the epilogue's own steps in its order.
+constexpr int TC_COLS = 8;
+template <int EPI>
+__global__ void __launch_bounds__(256)
+    tail_combine_kernel(const GemmArgs a, const TailPlan p) {
+  const long long gid = blockIdx.x * 256ll + threadIdx.x;
+  const int cc = static_cast<int>(gid % (PN / TC_COLS));
+  const int lr = static_cast<int>((gid / (PN / TC_COLS)) % (2 * PM));
+  const int r = static_cast<int>(gid / (PN / TC_COLS) / (2 * PM));
+  if (r >= p.tail) return;
+  int msup, nb;
+  tile_coords(p.num_full + r, p.num_msup, p.num_n, p.group_sup, msup, nb);
+  const int row = msup * 2 * PM + lr;
+  const int c0 = nb * PN + cc * TC_COLS;
+  if (row >= a.M || c0 >= a.N) return;
+  const float4* src = reinterpret_cast<const float4*>(
+      a.part + (static_cast<size_t>(r) * p.nslots * 2 * PM + lr) * PN +
+      cc * TC_COLS);
+  const size_t stride4 = static_cast<size_t>(2 * PM) * PN / 4;
+  float v[TC_COLS] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int s0 = 0; s0 < p.nslots; s0 += 8) {
+    float4 t[8][2];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (s0 + k < p.nslots) {
+        t[k][0] = src[(s0 + k) * stride4];
+        t[k][1] = src[(s0 + k) * stride4 + 1];
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (s0 + k >= p.nslots) break;
+      if (s0 + k == 0) {
+        v[0] = t[0][0].x; v[1] = t[0][0].y; v[2] = t[0][0].z; v[3] = t[0][0].w;
+        v[4] = t[0][1].x; v[5] = t[0][1].y; v[6] = t[0][1].z; v[7] = t[0][1].w;
+      } else {
+        v[0] += t[k][0].x; v[1] += t[k][0].y; v[2] += t[k][0].z; v[3] += t[k][0].w;
+        v[4] += t[k][1].x; v[5] += t[k][1].y; v[6] += t[k][1].z; v[7] += t[k][1].w;
+      }
+    }
+  }
+  if (a.scale_a != nullptr) {  // E4M3 operands
+    const float acc_scale = *a.scale_a * *a.scale_b;
+#pragma unroll
+    for (int i = 0; i < TC_COLS; ++i) v[i] *= acc_scale;
+  }
+  if constexpr (EPI == EPI_SHARDSUM) {
+    add_bias_n(a.bias, c0, v, TC_COLS);
+    if (a.dropout)
+      apply_dropout(a.drop_threshold, a.drop_scale, a.drop_seed, a.drop_offset,
+                    row, c0, v, TC_COLS);
+    if (!a.out_f32) add_residual_bf16(a.aux, a.ldaux, row, a.M, c0, v, TC_COLS);
+  }
+  if (EPI == EPI_STORE_F32 || a.out_f32) {
+    float4* d = reinterpret_cast<float4*>(static_cast<float*>(a.out) +
+                                          static_cast<size_t>(row) * a.ldo + c0);
+    d[0] = make_float4(v[0], v[1], v[2], v[3]);
+    d[1] = make_float4(v[4], v[5], v[6], v[7]);
+  } else {
+    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) +
+                              static_cast<size_t>(row) * a.ldo + c0) =
+        make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                   pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+  }
 }
 
 }  // namespace
@@ -636,50 +869,68 @@ cudaError_t launch_gemm_tc2(int epi, bool a_mn, bool b_mn,
                             const CUtensorMap& ta, const CUtensorMap& tb,
                             const CUtensorMap& to, const CUtensorMap& to2,
                             const GemmArgs& args, int max_pairs,
-                            cudaStream_t stream) {
+                            cudaStream_t stream, TailPlan* plan) {
+  if (plan != nullptr) *plan = TailPlan{};
   if (!a_mn && b_mn && epi == EPI_GELU_FWD)
-    return launch_impl<false, true, EPI_GELU_FWD>(ta, tb, to, to2, args, max_pairs,
-                                                  stream);
+    return launch_impl<false, true, EPI_GELU_FWD>(ta, tb, to, to2, args,
+                                                  max_pairs, stream, plan);
   if (!a_mn && b_mn && epi == EPI_SHARDSUM)
-    return launch_impl<false, true, EPI_SHARDSUM>(ta, tb, to, to2, args, max_pairs,
-                                                  stream);
+    return launch_impl<false, true, EPI_SHARDSUM>(ta, tb, to, to2, args,
+                                                  max_pairs, stream, plan);
   if (!a_mn && !b_mn && epi == EPI_GELU_BWD)
-    return launch_impl<false, false, EPI_GELU_BWD>(ta, tb, to, to2, args, max_pairs,
-                                                   stream);
+    return launch_impl<false, false, EPI_GELU_BWD>(ta, tb, to, to2, args,
+                                                   max_pairs, stream, plan);
   if (!a_mn && !b_mn && epi == EPI_SHARDSUM)
-    return launch_impl<false, false, EPI_SHARDSUM>(ta, tb, to, to2, args, max_pairs,
-                                                   stream);
+    return launch_impl<false, false, EPI_SHARDSUM>(ta, tb, to, to2, args,
+                                                   max_pairs, stream, plan);
   if (a_mn && b_mn && epi == EPI_STORE_F32)
-    return launch_impl<true, true, EPI_STORE_F32>(ta, tb, to, to2, args, max_pairs,
-                                                  stream);
+    return launch_impl<true, true, EPI_STORE_F32>(ta, tb, to, to2, args,
+                                                  max_pairs, stream, plan);
   if (!a_mn && b_mn && epi == EPI_BIAS_BF16)
     return launch_impl<false, true, EPI_BIAS_BF16>(ta, tb, to, to2, args,
-                                                   max_pairs, stream);
+                                                   max_pairs, stream, plan);
   if (!a_mn && !b_mn && epi == EPI_BIAS_BF16)
     return launch_impl<false, false, EPI_BIAS_BF16>(ta, tb, to, to2, args,
-                                                    max_pairs, stream);
+                                                    max_pairs, stream, plan);
   return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_gemm_tc2_e4m3(int epi, const CUtensorMap& ta,
                                  const CUtensorMap& tb, const CUtensorMap& to,
                                  const CUtensorMap& to2, const GemmArgs& args,
-                                 int max_pairs, cudaStream_t stream) {
+                                 int max_pairs, cudaStream_t stream,
+                                 TailPlan* plan) {
+  if (plan != nullptr) *plan = TailPlan{};
   if (args.scale_a == nullptr || args.scale_b == nullptr)
     return cudaErrorInvalidValue;
   if (epi == EPI_GELU_FWD)
     return launch_impl<false, false, EPI_GELU_FWD, true>(ta, tb, to, to2, args,
-                                                         max_pairs, stream);
+                                                         max_pairs, stream, plan);
   if (epi == EPI_SHARDSUM)
     return launch_impl<false, false, EPI_SHARDSUM, true>(ta, tb, to, to2, args,
-                                                         max_pairs, stream);
+                                                         max_pairs, stream, plan);
   if (epi == EPI_GELU_BWD)
     return launch_impl<false, false, EPI_GELU_BWD, true>(ta, tb, to, to2, args,
-                                                         max_pairs, stream);
+                                                         max_pairs, stream, plan);
   if (epi == EPI_STORE_F32)
     return launch_impl<false, false, EPI_STORE_F32, true>(ta, tb, to, to2, args,
-                                                          max_pairs, stream);
+                                                          max_pairs, stream, plan);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_gemm_tc2_tail(int epi, const GemmArgs& args,
+                                 const TailPlan& plan, cudaStream_t stream) {
+  if (plan.tail <= 0) return cudaSuccess;
+  const long long threads =
+      static_cast<long long>(plan.tail) * 2 * PM * (PN / TC_COLS);
+  const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
+  if (epi == EPI_SHARDSUM)
+    tail_combine_kernel<EPI_SHARDSUM><<<blocks, 256, 0, stream>>>(args, plan);
+  else if (epi == EPI_STORE_F32)
+    tail_combine_kernel<EPI_STORE_F32><<<blocks, 256, 0, stream>>>(args, plan);
+  else
+    return cudaErrorInvalidValue;
+  return cudaGetLastError();
 }
 
 }  // namespace tpmlp

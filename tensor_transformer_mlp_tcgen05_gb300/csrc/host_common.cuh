@@ -296,9 +296,14 @@ inline int tc_gemm(HandleCore* H, const char* name, cudaStream_t s, int sms,
     } else {
       to2 = to;  // unused by the kernel
     }
-    return run(H, name, s, [&] {
+    TailPlan plan;
+    TRY(run(H, name, s, [&] {
       return launch_gemm_tc2(epi, a_mn, b_mn, ta, tb, to, to2, args, sms / 2,
-                             s);
+                             s, args.part != nullptr ? &plan : nullptr);
+    }));
+    if (plan.tail == 0) return TPMLP_OK;
+    return run(H, "gemm_tail_combine", s, [&] {
+      return launch_gemm_tc2_tail(epi, args, plan, s);
     });
   }
   const int grid = grid_for(args.M, args.N, sms);

@@ -29,11 +29,25 @@ cudaError_t launch_gemm_tc(int epi, bool a_mn, bool b_mn, const CUtensorMap& ta,
 // reads H (args.aux) through `to2`, encoded the same way.  At most
 // `max_pairs` clusters are launched.
 constexpr int TC2_BN_HALF = 128;
+// The tail split a pair-GEMM launch used (see GemmArgs::part); tail = 0
+// when it used none.  launch_gemm_tc2_tail then combines the partials.
+struct TailPlan {
+  int tail = 0, pieces = 0, nslots = 0;
+  int num_full = 0, num_msup = 0, num_n = 0, group_sup = 0;
+};
+// Partial-sum capacity the library's workspaces reserve for the tail split.
+constexpr long long TAIL_PART_BYTES = 64ll << 20;
 cudaError_t launch_gemm_tc2(int epi, bool a_mn, bool b_mn,
                             const CUtensorMap& ta, const CUtensorMap& tb,
                             const CUtensorMap& to, const CUtensorMap& to2,
                             const GemmArgs& args, int max_pairs,
-                            cudaStream_t stream);
+                            cudaStream_t stream, TailPlan* plan = nullptr);
+// Combine a tail split's partials (fixed order) and apply the launch's
+// epilogue to the tail super-tiles: EPI_SHARDSUM (bias, dropout, residual,
+// bf16 or fp32 output, bitwise equal to the unsplit epilogue) or
+// EPI_STORE_F32.  `args` as given to the GEMM launch.
+cudaError_t launch_gemm_tc2_tail(int epi, const GemmArgs& args,
+                                 const TailPlan& plan, cudaStream_t stream);
 
 // The pair GEMM on E4M3 operands (both K-major, 8-bit tensor maps with
 // 128 x 128-byte boxes; args.kb_per_seg counts 128-element k-blocks;
@@ -44,7 +58,8 @@ cudaError_t launch_gemm_tc2(int epi, bool a_mn, bool b_mn,
 cudaError_t launch_gemm_tc2_e4m3(int epi, const CUtensorMap& ta,
                                  const CUtensorMap& tb, const CUtensorMap& to,
                                  const CUtensorMap& to2, const GemmArgs& args,
-                                 int max_pairs, cudaStream_t stream);
+                                 int max_pairs, cudaStream_t stream,
+                                 TailPlan* plan = nullptr);
 
 // FP8 helpers (csrc/fp8.cu).  amax: *amax = max(*amax, max |x|) as fp32
 // bits (the caller zeroes it first).  Quantization: s = amax / 448 in fp32

@@ -32,7 +32,7 @@ namespace {
 
 struct Layout {
   size_t status = 0, xn = 0, mean = 0, rstd = 0, y = 0, h = 0, dh = 0,
-         dxn = 0, dze = 0, part = 0, total = 0;
+         dxn = 0, dze = 0, part = 0, tailp = 0, total = 0;
   int chunks = 0;   // 256-row column-sum chunks
   int groups = 0;   // 32-row groups of the dH GEMM's fused db1 partials
 };
@@ -40,9 +40,10 @@ struct Layout {
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Workspace sections, each 256-byte aligned: status word; [Xn, mean, rstd]
-// with LayerNorm; Y; and for training H, dH, [dXn fp32 with LayerNorm],
-// [the dropout-masked dZ with dropout], column-sum partials: db2 (chunks x h),
-// db1 (max(groups, chunks) x f), dgamma and dbeta (chunks x h each).
+// with LayerNorm; Y; [bf16: the GEMM tail-split partials, TAIL_PART_BYTES];
+// and for training H, dH, [dXn fp32 with LayerNorm], [the dropout-masked dZ
+// with dropout], column-sum partials: db2 (chunks x h), db1 (max(groups,
+// chunks) x f), dgamma and dbeta (chunks x h each).
 Layout make_layout(const tp_mlp_config& c, int tokens, int training) {
   Layout L;
   const size_t es = c.dtype == TPMLP_BF16 ? 2 : 4;
@@ -62,6 +63,7 @@ Layout make_layout(const tp_mlp_config& c, int tokens, int training) {
     L.rstd = take(T * 4);
   }
   L.y = take(T * f * es);
+  if (c.dtype == TPMLP_BF16) L.tailp = take(static_cast<size_t>(TAIL_PART_BYTES));
   if (training) {
     L.h = take(T * f * es);
     L.dh = take(T * f * es);
@@ -96,7 +98,7 @@ Fp8Pack fp8_pack_layout(const tp_mlp_config& c) {
 
 struct Fp8Layout {
   size_t status = 0, xn = 0, mean = 0, rstd = 0, scales = 0, xq = 0, y = 0,
-         yq = 0, total = 0;
+         yq = 0, tailp = 0, total = 0;
   // training sections
   size_t tpitch = 0;  // row pitch (bytes) of the transposed code sections
   size_t hb = 0, xqt = 0, yqt = 0, bscales = 0, dzq = 0, dzqt = 0, dh = 0,
@@ -104,7 +106,8 @@ struct Fp8Layout {
   int chunks = 0, groups = 0;
 };
 // status | [Xn, mean, rstd] | [amax_x, amax_y (u32), s_x, s_y (f32)] |
-// Xq [T, h] | Y [T, f] bf16 | Yq [T, f] -- the forward's workspace; the
+// Xq [T, h] | Y [T, f] bf16 | Yq [T, f] | GEMM tail-split partials
+// (TAIL_PART_BYTES) -- the forward's workspace; the
 // training workspace goes on with H [T, f] bf16 | Xq^T [h, Tp] | Yq^T
 // [f, Tp] | [amax_dz, amax_dh (u32), s_dz, s_dh (f32)] | dZq [T, h] |
 // dZq^T [h, Tp] | dH [T, f] bf16 | dHq [T, f] | dHq^T [f, Tp] | [dXn fp32
@@ -130,6 +133,7 @@ Fp8Layout fp8_layout(const tp_mlp_config& c, int tokens) {
   L.xq = take(T * h);
   L.y = take(T * f * 2);
   L.yq = take(T * f);
+  L.tailp = take(static_cast<size_t>(TAIL_PART_BYTES));
   L.total = off;
   L.tpitch = align_up(T, 16);
   L.hb = take(T * f * 2);
@@ -178,7 +182,26 @@ GemmArgs base_args(const tp_mlp_handle* H, void* ws, size_t status_off) {
 }
 
 GemmArgs base_args(const tp_mlp_handle* H, void* ws, const Layout& L) {
-  return base_args(H, ws, L.status);
+  GemmArgs a = base_args(H, ws, L.status);
+  if (L.tailp != 0) {
+    a.part = reinterpret_cast<float*>(static_cast<char*>(ws) + L.tailp);
+    a.part_bytes = TAIL_PART_BYTES;
+  }
+  return a;
+}
+
+// An E4M3 pair GEMM, with the tail split when args.part is given.
+int f8_gemm(HandleCore* H, const char* name, cudaStream_t s, int sms, int epi,
+            const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to,
+            const CUtensorMap& to2, const GemmArgs& g) {
+  TailPlan plan;
+  TRY(run(H, name, s, [&] {
+    return launch_gemm_tc2_e4m3(epi, ta, tb, to, to2, g, sms / 2, s,
+                                g.part != nullptr ? &plan : nullptr);
+  }));
+  if (plan.tail == 0) return TPMLP_OK;
+  return run(H, "gemm_tail_combine", s,
+             [&] { return launch_gemm_tc2_tail(epi, g, plan, s); });
 }
 
 // Dropout parameters of the output dropout (keep when the 32-bit Philox
@@ -687,6 +710,8 @@ static int forward_fp8_impl(tp_mlp_handle* H, int tokens, const void* X,
   g2.M = T; g2.N = h; g2.K = f; g2.num_seg = t; g2.kb_per_seg = ft / 128;
   g2.out = Z; g2.ldo = h; g2.bias = bias2;
   g2.scale_a = scl + 1; g2.scale_b = wscl + 1;
+  g2.part = reinterpret_cast<float*>(ws + L.tailp);
+  g2.part_bytes = TAIL_PART_BYTES;
   if (c.use_residual) {
     g2.aux = X;
     g2.ldaux = h;
@@ -694,9 +719,8 @@ static int forward_fp8_impl(tp_mlp_handle* H, int tokens, const void* X,
   TRY(encode_map_u8(&ta, Yq, f, T, f, TC_BM));
   TRY(encode_map_u8(&tb, pk + P.bqt, f, h, f, TC2_BN_HALF));
   TRY(out_map(&to2, Z, false, T, h, h));
-  return run(&H->core, "gemm2_shardsum_fp8", s, [&] {
-    return launch_gemm_tc2_e4m3(EPI_SHARDSUM, ta, tb, to2, to2, g2, sms / 2, s);
-  });
+  return f8_gemm(&H->core, "gemm2_shardsum_fp8", s, sms, EPI_SHARDSUM, ta, tb,
+                 to2, to2, g2);
 }
 
 int tp_mlp_forward_fp8(tp_mlp_handle* H, int tokens, const void* X,
@@ -837,23 +861,25 @@ int tp_mlp_backward_fp8(tp_mlp_handle* H, int tokens, const void* dZ,
   gb.M = f; gb.N = h; gb.K = T; gb.kb_per_seg = kbT;
   gb.out = dB; gb.ldo = h;
   gb.scale_a = fscl + 1; gb.scale_b = bscl;
+  gb.part = reinterpret_cast<float*>(ws + L.tailp);
+  gb.part_bytes = TAIL_PART_BYTES;
   TRY(encode_map_u8(&ta, ws + L.yqt, T, f, tp, TC_BM));
   TRY(encode_map_u8(&tb, dZqT, T, h, tp, TC2_BN_HALF));
   TRY(out_map(&to, dB, true, f, h, h));
-  TRY(run(&H->core, "gemm_wgrad_dB_fp8", s, [&] {
-    return launch_gemm_tc2_e4m3(EPI_STORE_F32, ta, tb, to, to, gb, sms / 2, s);
-  }));
+  TRY(f8_gemm(&H->core, "gemm_wgrad_dB_fp8", s, sms, EPI_STORE_F32, ta, tb, to,
+              to, gb));
   // dA = (s_x s_dh) (Xq^T dHq)
   GemmArgs ga = base_args(H, ws, L.status);
   ga.M = h; ga.N = f; ga.K = T; ga.kb_per_seg = kbT;
   ga.out = dA; ga.ldo = f;
   ga.scale_a = fscl; ga.scale_b = bscl + 1;
+  ga.part = reinterpret_cast<float*>(ws + L.tailp);
+  ga.part_bytes = TAIL_PART_BYTES;
   TRY(encode_map_u8(&ta, ws + L.xqt, T, h, tp, TC_BM));
   TRY(encode_map_u8(&tb, dHqT, T, f, tp, TC2_BN_HALF));
   TRY(out_map(&to, dA, true, h, f, f));
-  TRY(run(&H->core, "gemm_wgrad_dA_fp8", s, [&] {
-    return launch_gemm_tc2_e4m3(EPI_STORE_F32, ta, tb, to, to, ga, sms / 2, s);
-  }));
+  TRY(f8_gemm(&H->core, "gemm_wgrad_dA_fp8", s, sms, EPI_STORE_F32, ta, tb, to,
+              to, ga));
   // dXn = sum_i (s_dh s_a) (dHq_i Aq_i^T) in shard order: fp32 for the
   // LayerNorm backward, else dX itself (+ dZ with the residual)
   void* dXdst = ln ? static_cast<void*>(ws + L.dxn) : dX;
@@ -861,6 +887,8 @@ int tp_mlp_backward_fp8(tp_mlp_handle* H, int tokens, const void* dZ,
   gx.M = T; gx.N = h; gx.K = f; gx.num_seg = t; gx.kb_per_seg = ft / 128;
   gx.out = dXdst; gx.ldo = h; gx.out_f32 = ln ? 1 : 0;
   gx.scale_a = bscl + 1; gx.scale_b = wscl;
+  gx.part = reinterpret_cast<float*>(ws + L.tailp);
+  gx.part_bytes = TAIL_PART_BYTES;
   if (c.use_residual && !ln) {
     gx.aux = dZ;
     gx.ldaux = h;
@@ -868,9 +896,8 @@ int tp_mlp_backward_fp8(tp_mlp_handle* H, int tokens, const void* dZ,
   TRY(encode_map_u8(&ta, dHq, f, T, f, TC_BM));
   TRY(encode_map_u8(&tb, pk + P.aq, f, h, f, TC2_BN_HALF));
   TRY(out_map(&to, dXdst, ln, T, h, h));
-  TRY(run(&H->core, "gemm_dx_shardsum_fp8", s, [&] {
-    return launch_gemm_tc2_e4m3(EPI_SHARDSUM, ta, tb, to, to, gx, sms / 2, s);
-  }));
+  TRY(f8_gemm(&H->core, "gemm_dx_shardsum_fp8", s, sms, EPI_SHARDSUM, ta, tb,
+              to, to, gx));
   if (ln) {
     const float* dXn = reinterpret_cast<const float*>(ws + L.dxn);
     const float* mean = reinterpret_cast<const float*>(ws + L.mean);
