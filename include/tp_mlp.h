@@ -102,8 +102,12 @@ int tp_mlp_destroy(tp_mlp_handle* handle);
 
 /* Bytes of device workspace a call with `tokens` tokens needs.  training = 1
  * sizes it for tp_mlp_forward(training = 1) followed by tp_mlp_backward on
- * the same workspace; training = 0 for inference-only forward calls.
- * Returns 0 for a NULL handle or a negative token count. */
+ * the same workspace; training = 0 for inference-only forward calls.  Besides
+ * the saved activations and gradient partial sums, a bf16 handle's
+ * workspace (and the FP8 and attention workspaces) holds 64 MiB of fp32
+ * partial results for the GEMMs' last round of tiles, which the library
+ * splits along K when that round would leave SMs idle (summed again in a
+ * fixed order).  Returns 0 for a NULL handle or a negative token count. */
 size_t tp_mlp_workspace_bytes(const tp_mlp_handle* handle, int tokens,
                               int training);
 
