@@ -92,3 +92,44 @@ def test_attention_reference_arm_runs_the_oracle_on_cpu():
     assert line["metric"].startswith("TP-attention")
     assert line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+class _FakeEvent:
+    """A CUDA event stand-in: record() reads a scripted clock (ms)."""
+    clock = []
+
+    def __init__(self, enable_timing=True):
+        self.t = None
+
+    def record(self, stream=None):
+        self.t = _FakeEvent.clock.pop(0)
+
+    def elapsed_time(self, other):
+        return other.t - self.t
+
+
+class _FakeTorch:
+    class cuda:
+        Event = _FakeEvent
+
+        @staticmethod
+        def synchronize():
+            pass
+
+
+def test_timed_steps_reports_mean_and_per_step_stats():
+    # events at 0, 2, 5, 6, 10 ms: steps of 2, 3, 1, 4 ms
+    _FakeEvent.clock = [0.0, 2.0, 5.0, 6.0, 10.0]
+    calls = []
+    ms, st = bench.timed_steps(_FakeTorch, None, lambda: calls.append(1), 4)
+    assert len(calls) == 4
+    assert ms == 2.5
+    assert st == {"median": 2.5, "min": 1.0, "max": 4.0}
+
+
+def test_oracle_one_core_runs_in_a_single_threaded_child():
+    from tensor_transformer_mlp_tcgen05_gb300 import workloads as W
+    r = bench.oracle_one_core(W.WORKLOADS["tiny_fp32"], 16)
+    assert "error" not in r, r
+    assert r["threads"] == 1 and r["value"] > 0
+    assert r["sample"].startswith("first 16 of 32 tokens")
