@@ -353,6 +353,76 @@ __global__ void __launch_bounds__(CS_WARPS * 32)
   }
 }
 
+// MODE 0 for bf16 with cols % 8 == 0: the same sums in the same order (per
+// column: warp w adds rows w, w + 8, ... of the chunk in row order, then the
+// eight warp sums in warp order, so the results equal colsum_partial_kernel's
+// bit for bit), 8 columns per lane from one 16-byte load, four rows' loads
+// in flight, 256 columns per block.
+constexpr int CS8_COLS = 256;
+__global__ void __launch_bounds__(CS_WARPS * 32)
+    colsum_partial_bf16x8_kernel(const __nv_bfloat16* __restrict__ src,
+                                 float* __restrict__ part, int rows, int cols,
+                                 unsigned int* amax) {
+  __shared__ float red[CS_WARPS][CS8_COLS];
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.x * CS8_COLS + lane * 8;
+  const int chunk = blockIdx.y;
+  const int r0 = chunk * COLSUM_CHUNK_ROWS;
+  const int r1 = min(rows, r0 + COLSUM_CHUNK_ROWS);
+  float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float mx = 0.f;
+  if (c < cols) {
+    int r = r0 + w;
+    for (; r + 3 * CS_WARPS < r1; r += 4 * CS_WARPS) {
+      uint4 u[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        u[k] = *reinterpret_cast<const uint4*>(
+            src + static_cast<size_t>(r + k * CS_WARPS) * cols + c);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t q[4] = {u[k].x, u[k].y, u[k].z, u[k].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float lo, hi;
+          unpack_bf16x2(q[j], lo, hi);
+          a[2 * j] += lo;
+          a[2 * j + 1] += hi;
+          mx = fmaxf(mx, fmaxf(fabsf(lo), fabsf(hi)));
+        }
+      }
+    }
+    for (; r < r1; r += CS_WARPS) {
+      const uint4 u = *reinterpret_cast<const uint4*>(
+          src + static_cast<size_t>(r) * cols + c);
+      const uint32_t q[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float lo, hi;
+        unpack_bf16x2(q[j], lo, hi);
+        a[2 * j] += lo;
+        a[2 * j + 1] += hi;
+        mx = fmaxf(mx, fmaxf(fabsf(lo), fabsf(hi)));
+      }
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < 8; ++k) red[w][lane * 8 + k] = a[k];
+  if (amax != nullptr) {
+    const unsigned int wm = __reduce_max_sync(0xffffffffu, __float_as_uint(mx));
+    if (lane == 0) atomicMax(amax, wm);
+  }
+  __syncthreads();
+  for (int cc = threadIdx.x; cc < CS8_COLS; cc += blockDim.x) {
+    const int col = blockIdx.x * CS8_COLS + cc;
+    if (col >= cols) continue;
+    float t = 0.f;
+#pragma unroll
+    for (int ww = 0; ww < CS_WARPS; ++ww) t += red[ww][cc];
+    part[static_cast<size_t>(chunk) * cols + col] = t;
+  }
+}
+
 // out[c] = sum_k part[k][c] in a fixed order: 32 columns per block, warp y
 // sums the y-th eighth of the chunks in chunk order, then the eight warp
 // sums are added in warp order.  Coalesced 128-byte rows, any chunk count.
@@ -480,7 +550,12 @@ cudaError_t launch_colsum_partial(bool bf16, const void* src, float* part,
                                   int rows, int cols, cudaStream_t stream,
                                   unsigned int* amax) {
   const dim3 grid((cols + CS_COLS - 1) / CS_COLS, colsum_chunks(rows));
-  if (bf16) {
+  if (bf16 && cols % 8 == 0 &&
+      (reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
+    const dim3 grid8((cols + CS8_COLS - 1) / CS8_COLS, colsum_chunks(rows));
+    colsum_partial_bf16x8_kernel<<<grid8, CS_WARPS * 32, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(src), part, rows, cols, amax);
+  } else if (bf16) {
     colsum_partial_kernel<__nv_bfloat16, 0><<<grid, CS_WARPS * 32, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(src), nullptr, nullptr, nullptr,
         part, nullptr, rows, cols, amax);
