@@ -289,8 +289,11 @@ int tp_mlp_probe_gelu(const float* x, float* y, float* dy, int n, int mode,
  * call shares the array and it keeps the last call's contents (each call
  * overwrites all it reads, so nothing needs clearing); calls that overlap on
  * the GPU, on different streams, race on it.  The result is bit-identical to
- * tp_mlp_backward's bias gradients for the same input.  No cudaMalloc,
- * cudaFree or allocating library routine is called. */
+ * the db2 of tp_mlp_backward for the same dZ (the same two fixed-order
+ * kernels), and to its db1 in the fp32 configuration; the bf16 path sums
+ * db1 from 32-row partials written by the dH GEMM's epilogue instead, which
+ * agrees within fp32 rounding, not bitwise.  No cudaMalloc, cudaFree or
+ * allocating library routine is called. */
 #define TPMLP_NOALLOC_SCRATCH_FLOATS (1 << 20)
 int tp_mlp_bias_grad_noalloc(int tokens, int cols, int dtype, const void* grad,
                              float* dbias, void* stream);

@@ -22,7 +22,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG, "libtpmlp.so")
 
-SOURCES = ["gemm_tc.cu", "gemm_tc2.cu", "rowops.cu", "simt.cu",
+SOURCES = ["gemm_tc2.cu", "rowops.cu", "simt.cu",
            "tp_mlp_host.cu", "noalloc.cu", "attn_fwd.cu", "attn_bwd.cu",
            "attn_host.cu", "fp8.cu", "probe.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -221,7 +221,7 @@ int tp_attn_forward(tp_attn_handle* H, int tokens, const void* X,
   TRY(kmajor_map(&ta, Xop, T, h, TC_BM));
   TRY(mnmajor_map(&tb, Wqkv, h, 3 * h));
   TRY(tc_gemm(&H->core, "gemm_qkv", s, sms, EPI_BIAS_BF16, false, true, ta, tb,
-              gq, true));
+              gq));
   // attention core
   const AttnArgs aa = core_args(H, ws, L, T);
   CUtensorMap tqk, tv;
@@ -242,7 +242,7 @@ int tp_attn_forward(tp_attn_handle* H, int tokens, const void* X,
   TRY(kmajor_map(&ta, ws + L.ctx, T, h, TC_BM));
   TRY(mnmajor_map(&tb, Wo, h, h));
   return tc_gemm(&H->core, "gemm_out_shardsum", s, sms, EPI_SHARDSUM, false,
-                 true, ta, tb, go, true);
+                 true, ta, tb, go);
 }
 
 int tp_attn_backward(tp_attn_handle* H, int tokens, const void* dZ,
@@ -305,7 +305,7 @@ int tp_attn_backward(tp_attn_handle* H, int tokens, const void* dZ,
   TRY(mnmajor_map(&ta, ctx, T, h));
   TRY(mnmajor_map(&tb, dZ, T, h));
   TRY(tc_gemm(&H->core, "gemm_wgrad_dWo", s, sms, EPI_STORE_F32, true, true, ta,
-              tb, gw, true));
+              tb, gw));
   // dCtx = dZ W_o^T
   GemmArgs gc = gemm_args(H, ws, L);
   gc.M = T; gc.N = h; gc.K = h; gc.kb_per_seg = h / TC_BK;
@@ -313,7 +313,7 @@ int tp_attn_backward(tp_attn_handle* H, int tokens, const void* dZ,
   TRY(kmajor_map(&ta, dZ, T, h, TC_BM));
   TRY(kmajor_map(&tb, Wo, h, h, TC2_BN_HALF));
   TRY(tc_gemm(&H->core, "gemm_dctx", s, sms, EPI_BIAS_BF16, false, false, ta,
-              tb, gc, true));
+              tb, gc));
   // attention core backward
   AttnArgs aa = core_args(H, ws, L, T);
   aa.dctx = static_cast<const __nv_bfloat16*>(dctx);
@@ -357,7 +357,7 @@ int tp_attn_backward(tp_attn_handle* H, int tokens, const void* dZ,
   TRY(mnmajor_map(&ta, Xop, T, h));
   TRY(mnmajor_map(&tb, dqkv, T, 3 * h));
   TRY(tc_gemm(&H->core, "gemm_wgrad_dWqkv", s, sms, EPI_STORE_F32, true, true,
-              ta, tb, gwq, true));
+              ta, tb, gwq));
   // dXn = sum_i dQKV_i W_qkv,i^T (segment i = shard i's 3 h_t columns)
   GemmArgs gx = gemm_args(H, ws, L);
   gx.M = T; gx.N = h; gx.K = 3 * h; gx.num_seg = c.shards;
@@ -372,7 +372,7 @@ int tp_attn_backward(tp_attn_handle* H, int tokens, const void* dZ,
   TRY(kmajor_map(&ta, dqkv, T, 3 * h, TC_BM));
   TRY(kmajor_map(&tb, Wqkv, h, 3 * h, TC2_BN_HALF));
   TRY(tc_gemm(&H->core, "gemm_dx_shardsum", s, sms, EPI_SHARDSUM, false, false,
-              ta, tb, gx, true));
+              ta, tb, gx));
   if (ln) {
     const float* dXn = reinterpret_cast<const float*>(ws + L.dxn);
     const float* mean = reinterpret_cast<const float*>(ws + L.mean);

@@ -1,30 +1,49 @@
-// CTA-pair tcgen05 GEMM for sm_103a (cta_group::2), same operands, shard
-// sum and epilogues as gemm_tc.cu, with a 256 x 256 output tile per pair.
+// Persistent, warp-specialised CTA-pair tcgen05 GEMM for sm_103a
+// (cta_group::2) with fused epilogues, 256 x 256 output tile per pair.
 //
 // Clusters of 2 CTAs; the pair (CTA ranks 0 and 1) owns one 256 x 256 tile
 // at a time, persistent over the tile list.  Per k-block each CTA loads only
 // its half of the operands into its own shared memory: rank r loads A rows
-// [m0 + 128 r, +128) and B columns [n0 + 128 r, +128), 32 KB per stage, and
-// each CTA moves half as many B bytes per flop as the one-CTA kernel.  The even CTA issues
-// tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16): the tensor cores of
-// both SMs read A from their own CTA and B from both, and each CTA receives
-// its 128 rows of D (all 256 columns) in its own TMEM.  The ring has 5
-// stages (160 KB) next to 64 KB of epilogue staging.
+// [m0 + 128 r, +128) and B columns [n0 + 128 r, +128), 32 KB per stage.  The
+// even CTA issues tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16): the
+// tensor cores of both SMs read A from their own CTA and B from both, and
+// each CTA receives its 128 rows of D (all 256 columns) in its own TMEM.  The
+// ring has 5 stages (160 KB) next to 64 KB of epilogue staging.
 //
-// Two pairs may share a cluster of 4 (launches prefer 4, fall back to 2):
-// then each k-block's B halves are loaded by one of the two pairs and
-// multicast into both, since the group's two tiles share their B columns.
+// 12 warps in 3 warpgroups per CTA:
+//   warp 0      TMA producer (one lane).
+//   warp 1      allocates 512 TMEM columns (two 128 x 256 fp32 accumulators,
+//               so the epilogue of one tile runs while the MMAs of the next
+//               proceed); on the even CTA one lane issues the MMAs and
+//               commits.
+//   warps 2-3   idle.
+//   warps 4-11  epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 (its
+//               sub-partition) and one 128-column half of the tile.
+// Registers: the CTA is launched with 168 per thread (384 x 168 = 64512); the
+// first warpgroup gives registers back (down to REGS_CONTROL) and the two
+// epilogue warpgroups take them (up to REGS_EPILOGUE), enough to hold a
+// 128-column fp32 shard-sum row per thread.
+//
+// Shard sum (the on-device form of the pages' g forward and f backward
+// all-reduces): the K range is cut into `num_seg` segments, one per shard.
+// Each segment starts a fresh accumulator (the MMA's accumulate flag is off
+// on its first k-step); the epilogue adds the segment partials into fp32
+// registers in segment order 0..t-1, adds the bias and rounds once.  Every
+// output element has one writer and a fixed summation order, so results are
+// bitwise reproducible.
+//
+// Every pair loads its own operands: the launch uses clusters of exactly two
+// CTAs, and no copy writes into another pair's shared memory.
 //
 // Synchronisation:
 //   full[s]   (pair leader only) counts the TMA bytes landing in both CTAs of
 //             the pair: the leader arms it with the pair's 64 KB, both CTAs'
-//             copies (and multicast copies from the other pair) complete on it.
-//   empty[s]  (each CTA) arrived by the MMA issuers' multicast commits when
-//             the MMAs have read stage s, releasing the producers (in a
-//             cluster of 4 both pairs' commits, since either pair's copies
-//             may land in it).
-//   tfull[b]  (each CTA) arrived by a multicast commit when accumulator b is
-//             ready in both TMEMs.
+//             copies complete on it.
+//   empty[s]  (each CTA) arrived by the MMA issuer's commit (signalled to
+//             both CTAs of the pair) when the MMAs have read stage s,
+//             releasing the producers.
+//   tfull[b]  (each CTA) arrived by a commit signalled to both CTAs when
+//             accumulator b is ready in both TMEMs.
 //   tempty[b] (rank 0 only) 16 arrivals: 8 epilogue warps of each CTA, the
 //             peer's arriving remotely.
 // Epilogue: each warp turns its 32 TMEM lanes into 32-row x 128-byte chunks
@@ -32,10 +51,12 @@
 // with asynchronous TMA stores (coalesced full-line writes; rows or columns
 // past the tensor's edge are clipped by the TMA unit), double-buffered per
 // warp, so the epilogue never issues row-strided global stores.
-// Registers, the shard sum, the bounded waits and the abort path are as in
-// the one-CTA kernel; in addition both CTAs meet at cluster barriers before
-// the first copy and before TMEM is freed, so no CTA leaves while its peer may
-// still touch its shared memory or barriers.
+// Every mbarrier wait is bounded by a time budget; on expiry the CTA records
+// TPMLP_ERR_TIMEOUT in the status word, the other roles see a shared abort
+// flag and stop, outstanding copies and MMAs are waited for (bounded), TMEM
+// is freed and the kernel returns.  Both CTAs meet at cluster barriers
+// before the first copy and before TMEM is freed, so no CTA leaves while its
+// peer may still touch its shared memory or barriers.
 //
 // With F8 the operands are E4M3 bytes (both K-major): a k-block is 128
 // elements, still one 128-byte swizzle row, each MMA (kind::f8f6f4, K = 32)
@@ -179,16 +200,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // Work is dealt to groups of four CTAs (two pairs) in blockIdx order: a
-  // group owns a 512 x 256 "super-tile" (its pairs the upper and lower
-  // 256 x 256 tiles, same B columns) whether the launch made it one cluster
-  // of 4 or two clusters of 2.  In a cluster of 4 the two pairs share the B
-  // operand: each k-block's B halves are loaded by one pair (alternating)
-  // and multicast into both.
-  const uint32_t rank = ptx::cluster_ctarank();
-  const bool quad = ptx::cluster_nctarank() == 4;
-  const uint32_t prank = rank & 1u;        // rank inside the pair
-  const uint32_t lead_rank = rank & ~1u;   // the pair's even CTA
+  // Work is dealt to groups of four CTAs (two pairs, two clusters) in
+  // blockIdx order: a group owns a 512 x 256 "super-tile", its pairs the
+  // upper and lower 256 x 256 tiles, which read the same B columns at about
+  // the same time (one trip from DRAM to L2 for both).
+  const uint32_t prank = ptx::cluster_ctarank();  // rank inside the pair
   const bool leader = prank == 0;
   const int pg = static_cast<int>(blockIdx.x >> 1) & 1;  // pair in its group
   const int group = static_cast<int>(blockIdx.x >> 2);
@@ -197,7 +213,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(full0 + 8u * s, 1);
-      ptx::mbar_init(empty0 + 8u * s, quad ? 2 : 1);
+      ptx::mbar_init(empty0 + 8u * s, 1);
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(tfull0 + 8u * b, 1);
@@ -233,8 +249,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int num_full = num_super - args.tail;
   const int num_items = num_full + args.tail * args.pieces;
   // The even CTA's full and tempty barriers, as cluster addresses.
-  const uint32_t lead_full0 = ptx::mapa_shared(full0, lead_rank);
-  const uint32_t lead_tempty0 = ptx::mapa_shared(tempty0, lead_rank);
+  const uint32_t lead_full0 = ptx::mapa_shared(full0, 0u);
+  const uint32_t lead_tempty0 = ptx::mapa_shared(tempty0, 0u);
 
   if (warp < FIRST_EPI_WARP) {
     ptx::setmaxnreg_dec<REGS_CONTROL>();
@@ -242,8 +258,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // ---------------------------------------------------- producer --
       uint32_t stage = 0, phase = 0;
       bool alive = true;
-      const uint16_t bmask =
-          static_cast<uint16_t>((1u << prank) | (1u << (prank + 2u)));
       for (int item = group; alive && item < num_items; item += num_groups) {
         const Item it = decode_item(item, num_full, args);
         int msup, nb;
@@ -271,24 +285,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               ptx::tma_load_2d_pair(da + j * (BK * 128), &tmA, fb, m0 + 64 * j,
                                     k0);
           }
-          if (!quad) {
-            if constexpr (!B_MN) {
-              ptx::tma_load_2d_pair(db, &tmB, fb, k0, n0);
-            } else {
+          if constexpr (!B_MN) {
+            ptx::tma_load_2d_pair(db, &tmB, fb, k0, n0);
+          } else {
 #pragma unroll
-              for (int j = 0; j < HN / 64; ++j)
-                ptx::tma_load_2d_pair(db + j * (BK * 128), &tmB, fb,
-                                      n0 + 64 * j, k0);
-            }
-          } else if ((kb & 1) == pg) {
-            if constexpr (!B_MN) {
-              ptx::tma_load_2d_pair_mc(db, &tmB, fb, k0, n0, bmask);
-            } else {
-#pragma unroll
-              for (int j = 0; j < HN / 64; ++j)
-                ptx::tma_load_2d_pair_mc(db + j * (BK * 128), &tmB, fb,
-                                         n0 + 64 * j, k0, bmask);
-            }
+            for (int j = 0; j < HN / 64; ++j)
+              ptx::tma_load_2d_pair(db + j * (BK * 128), &tmB, fb, n0 + 64 * j,
+                                    k0);
           }
           if (++stage == STAGES) {
             stage = 0;
@@ -304,9 +307,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       constexpr uint32_t B_KSTEP = B_MN ? 16 * 128 : 32;
       constexpr uint32_t A_LBO = A_MN ? BK * 128 : 16;
       constexpr uint32_t B_LBO = B_MN ? BK * 128 : 16;
-      // stage release: both pairs' producers write into a shared stage
-      const uint16_t release = quad ? 0xF : 0x3;
-      const uint16_t pair_mask = static_cast<uint16_t>(0x3u << lead_rank);
+      // commits signal the barrier of both CTAs of the pair
+      constexpr uint16_t pair_mask = 0x3;
       uint32_t stage = 0, phase = 0, acc = 0;
       bool alive = true;
       for (int item = group; alive && item < num_items; item += num_groups) {
@@ -343,7 +345,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                    (kb > 0 || k > 0) ? 1u : 0u);
               }
             }
-            ptx::mma_commit_pair(empty0 + 8u * stage, release);
+            ptx::mma_commit_pair(empty0 + 8u * stage, pair_mask);
             if (++stage == STAGES) {
               stage = 0;
               phase ^= 1u;
@@ -354,7 +356,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       if (*reinterpret_cast<volatile int*>(abort_flag)) {
         // Wait for every MMA this thread issued before TMEM is freed.
-        ptx::mma_commit_pair(done_bar, static_cast<uint16_t>(1u << rank));
+        ptx::mma_commit_pair(done_bar, static_cast<uint16_t>(1u << prank));
         wait_teardown(done_bar, 0);
       }
     }
@@ -740,7 +742,7 @@ cudaError_t launch_impl(const CUtensorMap& ta, const CUtensorMap& tb,
                            static_cast<int>(SMEM_BYTES));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
@@ -752,26 +754,24 @@ cudaError_t launch_impl(const CUtensorMap& ta, const CUtensorMap& tb,
   cfg.numAttrs = 1;
   if (env_max_pairs() > 0 && max_pairs > env_max_pairs())
     max_pairs = env_max_pairs();
-  // Never more pairs than can be resident at once (the kernel is persistent).
-  cfg.gridDim = dim3(2 * max_pairs);
+  cfg.gridDim = dim3(2);
   int resident = 0;
   e = cudaOccupancyMaxActiveClusters(&resident, kern, &cfg);
   if (e != cudaSuccess) return e;
   if (resident <= 0) return cudaErrorInvalidConfiguration;
-  // Work goes to groups of two pairs (an even number of pairs); the launch
-  // prefers clusters of 4 (the two pairs share B) and falls back to 2 where
-  // a GPU processing cluster has no room for 4.
+  // Work goes to groups of two pairs (an even number of pairs).  The pair
+  // count, and with it the tail-split plan (and so the last bits of the
+  // split fp32 weight gradients), is a function of `max_pairs` (half the
+  // device's SM count) and the shape alone: the runtime's residency answer
+  // is not used, so that two processes on the same GPU model compute the
+  // same bits.  If fewer pairs fit at once (an SM limit imposed by the
+  // environment), the later clusters start when earlier ones finish: the
+  // work each does is fixed by its index, so results do not change.
   const long long sup = static_cast<long long>((args.M + 2 * PM - 1) / (2 * PM)) *
                         ((args.N + PN - 1) / PN);
   long long pairs = 2 * sup < max_pairs ? 2 * sup : max_pairs;
-  if (pairs > resident) pairs = resident;
   pairs &= ~1LL;
   if (pairs < 2) pairs = 2;
-  attr[1].id = cudaLaunchAttributePreferredClusterDimension;
-  attr[1].val.preferredClusterDim.x = 4;
-  attr[1].val.preferredClusterDim.y = 1;
-  attr[1].val.preferredClusterDim.z = 1;
-  cfg.numAttrs = 2;
   cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
   GemmArgs a = args;
   a.tail = a.pieces = a.nslots = 0;

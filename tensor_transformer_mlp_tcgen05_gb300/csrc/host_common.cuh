@@ -250,65 +250,38 @@ inline int run(HandleCore* H, const char* name, cudaStream_t s, F&& launch) {
   return TPMLP_OK;
 }
 
-inline int grid_for(int M, int N, int sms) {
-  const long long tiles = static_cast<long long>((M + TC_BM - 1) / TC_BM) *
-                          ((N + TC_BN - 1) / TC_BN);
-  return static_cast<int>(tiles < sms ? tiles : sms);
-}
-
 #define TRY(x)                       \
   do {                               \
     const int rc_ = (x);             \
     if (rc_ != TPMLP_OK) return rc_; \
   } while (0)
 
-// GEMM kernel selection: CTA pairs (256 x 256 tiles) by default; setting
-// TPMLP_GEMM_VARIANT=single in the environment selects the one-CTA kernel.
-inline bool use_pairs() {
-  static const bool pairs = [] {
-    const char* v = std::getenv("TPMLP_GEMM_VARIANT");
-    return !(v != nullptr && std::strcmp(v, "single") == 0);
-  }();
-  return pairs;
-}
-
-// Box height of a K-major B operand for the selected kernel.
-inline int b_box_rows() { return use_pairs() ? TC2_BN_HALF : TC_BN; }
-
-// One GEMM launch (the pair kernel when selected or `force_pairs`; K-major B
-// maps must then use TC2_BN_HALF-row boxes).  The pair kernel writes through
-// output tensor maps,
+// One GEMM launch on the pair kernel (K-major B maps use TC2_BN_HALF-row
+// boxes).  The kernel writes through output tensor maps,
 // encoded here from args.out / args.out2 (row-major, leading dimension
 // args.ldo, element type fp32 for the fp32-output epilogues); EPI_GELU_BWD
 // reads H through the second map (args.aux, leading dimension args.ldaux).
 inline int tc_gemm(HandleCore* H, const char* name, cudaStream_t s, int sms,
             int epi, bool a_mn, bool b_mn, const CUtensorMap& ta,
-            const CUtensorMap& tb, const GemmArgs& args,
-            bool force_pairs = false) {
-  if (force_pairs || use_pairs()) {
-    const bool f32 = epi == EPI_STORE_F32 || (epi == EPI_SHARDSUM && args.out_f32);
-    CUtensorMap to, to2;
-    TRY(out_map(&to, args.out, f32, args.M, args.N, args.ldo));
-    if (epi == EPI_GELU_BWD) {
-      TRY(out_map(&to2, args.aux, false, args.M, args.N, args.ldaux));
-    } else if (args.out2 != nullptr) {
-      TRY(out_map(&to2, args.out2, false, args.M, args.N, args.ldo));
-    } else {
-      to2 = to;  // unused by the kernel
-    }
-    TailPlan plan;
-    TRY(run(H, name, s, [&] {
-      return launch_gemm_tc2(epi, a_mn, b_mn, ta, tb, to, to2, args, sms / 2,
-                             s, args.part != nullptr ? &plan : nullptr);
-    }));
-    if (plan.tail == 0) return TPMLP_OK;
-    return run(H, "gemm_tail_combine", s, [&] {
-      return launch_gemm_tc2_tail(epi, args, plan, s);
-    });
+            const CUtensorMap& tb, const GemmArgs& args) {
+  const bool f32 = epi == EPI_STORE_F32 || (epi == EPI_SHARDSUM && args.out_f32);
+  CUtensorMap to, to2;
+  TRY(out_map(&to, args.out, f32, args.M, args.N, args.ldo));
+  if (epi == EPI_GELU_BWD) {
+    TRY(out_map(&to2, args.aux, false, args.M, args.N, args.ldaux));
+  } else if (args.out2 != nullptr) {
+    TRY(out_map(&to2, args.out2, false, args.M, args.N, args.ldo));
+  } else {
+    to2 = to;  // unused by the kernel
   }
-  const int grid = grid_for(args.M, args.N, sms);
-  return run(H, name, s, [&] {
-    return launch_gemm_tc(epi, a_mn, b_mn, ta, tb, args, grid, s);
+  TailPlan plan;
+  TRY(run(H, name, s, [&] {
+    return launch_gemm_tc2(epi, a_mn, b_mn, ta, tb, to, to2, args, sms / 2,
+                           s, args.part != nullptr ? &plan : nullptr);
+  }));
+  if (plan.tail == 0) return TPMLP_OK;
+  return run(H, "gemm_tail_combine", s, [&] {
+    return launch_gemm_tc2_tail(epi, args, plan, s);
   });
 }
 

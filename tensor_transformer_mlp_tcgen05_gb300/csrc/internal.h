@@ -7,21 +7,17 @@
 
 namespace tpmlp {
 
-// Tensor-core GEMM tile: 128 x 256 output tile, 64-deep k-blocks (one
-// 128-byte swizzle row of bf16).
+// Tensor-core GEMM k-blocks are 64 deep (one 128-byte swizzle row of
+// bf16); each CTA stages 128 rows of the A operand (the box height of
+// K-major A maps).
 constexpr int TC_BM = 128;
-constexpr int TC_BN = 256;
 constexpr int TC_BK = 64;
 
-// D = Aop * Bop on the tensor cores.  a_mn / b_mn select M/N-major operands
-// (the tensor map's innermost dimension runs along M or N) instead of
-// K-major ones.  Supported combinations: (K, MN, GELU_FWD), (K, MN,
-// SHARDSUM), (K, K, GELU_BWD), (K, K, SHARDSUM), (MN, MN, STORE_F32).
-cudaError_t launch_gemm_tc(int epi, bool a_mn, bool b_mn, const CUtensorMap& ta,
-                           const CUtensorMap& tb, const GemmArgs& args,
-                           int grid, cudaStream_t stream);
-
-// The same GEMM on CTA pairs (tcgen05 cta_group::2, 256 x 256 tile per pair).
+// D = Aop * Bop on CTA pairs (tcgen05 cta_group::2, 256 x 256 tile per
+// pair).  a_mn / b_mn select M/N-major operands (the tensor map's innermost
+// dimension runs along M or N) instead of K-major ones.  Supported
+// combinations: (K, MN, GELU_FWD), (K, MN, SHARDSUM), (K, K, GELU_BWD),
+// (K, K, SHARDSUM), (MN, MN, STORE_F32), (K, MN or K, BIAS_BF16).
 // K-major B operands must be encoded with 128-row boxes (each CTA stages half
 // of the tile's N).  Outputs are written through tensor maps: `to` for
 // args.out and `to2` for args.out2 (EPI_GELU_FWD's H), 128-byte-swizzled

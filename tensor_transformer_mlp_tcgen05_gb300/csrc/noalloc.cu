@@ -4,7 +4,9 @@
 // file-scope device array instead, so the caller passes only the input and
 // the output.  It reuses the same two fixed-order kernels (per-chunk partial
 // sums, then the chunk partials added in chunk order), so its result is
-// bit-identical to the bias gradients tp_mlp_backward produces.
+// bit-identical to the db2 that tp_mlp_backward produces (and to its db1 in
+// the fp32 configuration; the bf16 db1 there comes from the dH GEMM's
+// 32-row partials instead).
 #include <cstdio>
 #include <mutex>
 

@@ -236,12 +236,6 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
   return r;
 }
 
-__device__ __forceinline__ uint32_t cluster_nctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-  return r;
-}
-
 // Address of the same shared-memory location in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   uint32_t r;
@@ -288,23 +282,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst,
       "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile."
       "mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(c0), "r"(c1)
-      : "memory");
-}
-
-// The same, multicast: the tile lands at the same offset in every CTA of
-// `cta_mask`, and each destination's completion is counted on the barrier at
-// `bar_cluster`'s offset in that CTA's pair leader.
-__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst,
-                                                    const CUtensorMap* m,
-                                                    uint32_t bar_cluster,
-                                                    int c0, int c1,
-                                                    uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile."
-      "mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, {%3, %4}], "
-      "[%2], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(c0), "r"(c1),
-      "h"(cta_mask)
       : "memory");
 }
 

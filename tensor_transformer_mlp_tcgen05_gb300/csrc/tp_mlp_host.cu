@@ -441,24 +441,20 @@ int tp_mlp_backward(tp_mlp_handle* H, int tokens, const void* dZ,
     CUtensorMap ta, tb;
     gy.kb_per_seg = h / TC_BK;
     TRY(kmajor_map(&ta, dZg, T, h, TC_BM));
-    TRY(kmajor_map(&tb, B, f, h, b_box_rows()));
-    // db1 = sum_T dH: 32-row partials from the pair GEMM's epilogue, then
-    // one fixed-order pass over them (the one-CTA GEMM has no such
-    // epilogue: there db1 is summed from dH in memory)
-    const bool fused_db1 = dbias1 != nullptr && use_pairs();
-    if (fused_db1) {
+    TRY(kmajor_map(&tb, B, f, h, TC2_BN_HALF));
+    // db1 = sum_T dH: 32-row partials from the GEMM's epilogue, then one
+    // fixed-order pass over them
+    if (dbias1 != nullptr) {
       gy.colsum = part1;
       gy.ld_colsum = f;
     }
     TRY(tc_gemm(&H->core, "gemm_dh_gelu_bwd", s, sms, EPI_GELU_BWD, false, false, ta,
                 tb, gy));
     if (dbias2) TRY(colsum(&H->core, "colsum_db2", s, true, dZg, part, dbias2, T, h));
-    if (fused_db1) {
+    if (dbias1 != nullptr) {
       TRY(run(&H->core, "colsum_finalize", s, [&] {
         return launch_colsum_finalize(part1, dbias1, L.groups, f, s);
       }));
-    } else if (dbias1) {
-      TRY(colsum(&H->core, "colsum_db1", s, true, dH, part1, dbias1, T, f));
     }
     const int kbT = (T + TC_BK - 1) / TC_BK;
     gb.kb_per_seg = kbT;
@@ -473,7 +469,7 @@ int tp_mlp_backward(tp_mlp_handle* H, int tokens, const void* dZ,
                 ga));
     gx.kb_per_seg = ft / TC_BK;
     TRY(kmajor_map(&ta, dH, T, f, TC_BM));
-    TRY(kmajor_map(&tb, A, h, f, b_box_rows()));
+    TRY(kmajor_map(&tb, A, h, f, TC2_BN_HALF));
     TRY(tc_gemm(&H->core, "gemm_dx_shardsum", s, sms, EPI_SHARDSUM, false, false, ta,
                 tb, gx));
   } else {

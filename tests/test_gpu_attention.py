@@ -14,6 +14,7 @@ import torch
 from oracle import attention as A
 from tensor_transformer_mlp_tcgen05_gb300 import workloads as W
 
+from fingerprint import ATTN_KERNEL, ATTN_ORDER, assert_bitwise
 from parity_helpers import assert_close, errors, f64
 
 pytestmark = pytest.mark.gpu
@@ -139,8 +140,7 @@ def test_attention_bitwise_repeatable():
     w = W.ATTN_WORKLOADS["attn_tiny_d128"]
     inp = W.make_attn_inputs(w, seed=3, with_bias=True)
     a, b = run_attn(w, inp, repeat=2)
-    for k in a:
-        assert torch.equal(a[k], b[k]), k
+    assert_bitwise(a, b, ATTN_ORDER, ATTN_KERNEL)
 
 
 def test_attention_zero_tokens():
@@ -192,8 +192,7 @@ def test_attention_full_size_sampled_invariants_and_bitwise(name, samples):
     w = W.ATTN_WORKLOADS[name]
     inp = W.make_attn_inputs(w, seed=0, with_bias=True)
     a, b = run_attn(w, inp, repeat=2)
-    for k in a:
-        assert torch.equal(a[k], b[k]), k
+    assert_bitwise(a, b, ATTN_ORDER, ATTN_KERNEL)
     del b
     S, h, d, H = w.seq, w.hidden, w.head_dim, w.heads
     X, Wqkv, Wo = f64(inp["X"]), f64(inp["Wqkv"]), f64(inp["Wo"])

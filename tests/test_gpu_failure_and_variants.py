@@ -1,4 +1,4 @@
-"""Bounded-wait failure reporting and the one-CTA GEMM variant, on the GPU.
+"""Bounded-wait failure reporting on the GPU.
 
 The timeout test makes every bounded wait inside the GEMM kernels give up at
 once (a 1 ns budget): the kernels must return on their own, report
@@ -69,25 +69,3 @@ def test_attention_wait_timeout_is_reported_and_context_survives():
                      w.seq, w.shards, bqkv=f64(inp["bqkv"]), bo=f64(inp["bo"]))
     assert_close("attention Z after timeout", Z.cpu(), ref["Z"])
     m.close()
-
-
-_SINGLE_SCRIPT = r"""
-import sys
-sys.path.insert(0, {root!r}); sys.path.insert(0, {tests!r})
-from tensor_transformer_mlp_tcgen05_gb300 import workloads as W
-from parity_helpers import run_cuda, oracle_full, compare_full
-for (T, h, f, t, ln) in [(300, 256, 1024, 2, True), (513, 192, 768, 4, False)]:
-    w = W.Workload("single", T, h, f, t, "bf16", ln, True)
-    inp = W.make_inputs(w, seed=41, with_bias=True)
-    compare_full(run_cuda(w, inp), oracle_full(inp))
-print("single-cta ok")
-"""
-
-
-def test_one_cta_gemm_variant_matches_oracle():
-    env = dict(os.environ, TPMLP_GEMM_VARIANT="single")
-    script = _SINGLE_SCRIPT.format(root=ROOT, tests=os.path.join(ROOT, "tests"))
-    r = subprocess.run([sys.executable, "-c", script], env=env,
-                       capture_output=True, text=True, timeout=600)
-    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]
-    assert "single-cta ok" in r.stdout

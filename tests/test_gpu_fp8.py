@@ -14,6 +14,7 @@ import torch
 from oracle import fp8 as F
 from tensor_transformer_mlp_tcgen05_gb300 import workloads as W
 
+from fingerprint import assert_bitwise
 from parity_helpers import assert_close, f64
 
 pytestmark = pytest.mark.gpu
@@ -137,8 +138,5 @@ def test_fp8_gpt3_13b_layer():
     w = W.WORKLOADS["gpt3_13b"]
     inp = W.make_inputs(w, seed=0, need_grad_input=False)
     a, b = run_fp8(w, inp, repeat=2)
-    for k in a:
-        same = torch.equal(a[k], b[k]) if torch.is_tensor(a[k]) else \
-            np.array_equal(a[k], b[k])
-        assert same, k
+    assert_bitwise(a, b)
     assert np.isfinite(f64(a["Z"])).all()

@@ -16,6 +16,7 @@ import torch
 from oracle import fp8 as F
 from tensor_transformer_mlp_tcgen05_gb300 import workloads as W
 
+from fingerprint import assert_bitwise
 from parity_helpers import assert_close, f64
 
 pytestmark = pytest.mark.gpu
@@ -179,10 +180,7 @@ def test_fp8_training_step_gpt3_13b_layer():
     w = W.WORKLOADS["gpt3_13b"]
     inp = W.make_inputs(w, seed=0, with_bias=True, need_grad_input=True)
     a, b = run_step(w, inp, repeat=2)
-    for k in a:
-        same = torch.equal(a[k], b[k]) if torch.is_tensor(a[k]) else \
-            np.array_equal(a[k], b[k])
-        assert same, k
+    assert_bitwise(a, b)
     for k in ("dX", "dA", "dB", "db1", "db2"):
         assert torch.isfinite(a[k].float()).all(), k
 

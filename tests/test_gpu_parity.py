@@ -12,6 +12,7 @@ from oracle import mlp as O
 from tensor_transformer_mlp_tcgen05_gb300 import workloads as W
 from tensor_transformer_mlp_tcgen05_gb300.mlp import TensorParallelMLP
 
+from fingerprint import assert_bitwise
 from parity_helpers import (assert_close, compare_full, f64, oracle_full,
                             run_cuda, to_dev)
 
@@ -124,7 +125,7 @@ def test_dropout_mask_does_not_depend_on_shards_and_is_deterministic():
     z1 = run_cuda(base, inp, backward=False, dropout=DROP)["Z"]
     z8a, z8b = run_cuda(base.with_(shards=8), inp, backward=False,
                         dropout=DROP, repeat=2)
-    assert torch.equal(z8a["Z"], z8b["Z"])
+    assert_bitwise(z8a, z8b)
     assert torch.equal(z1 == 0, z8a["Z"] == 0)
 
 
@@ -156,8 +157,7 @@ def test_two_runs_bitwise_identical_small(t):
     w = small(700, 256, 2048, t, ln=True)
     inp = W.make_inputs(w, seed=4, with_bias=True)
     r1, r2 = run_cuda(w, inp, repeat=2)
-    for k in r1:
-        assert torch.equal(r1[k], r2[k]), k
+    assert_bitwise(r1, r2)
 
 
 def test_shard_count_changes_only_rounding():
@@ -249,8 +249,7 @@ def test_megatron_8p3b_pre_ln_subblock_full():
     w = W.WORKLOADS["megatron_8p3b"]
     inp = W.make_inputs(w, seed=0)
     r1, r2 = run_cuda(w, inp, residual=True, repeat=2)
-    for k in r1:
-        assert torch.equal(r1[k], r2[k]), k
+    assert_bitwise(r1, r2)
     compare_full(r1, oracle_full(inp, residual=True))
 
 
@@ -280,13 +279,5 @@ def test_gpt3_13b_sampled_and_bitwise_identical():
     w = W.WORKLOADS["gpt3_13b"]
     inp = W.make_inputs(w, seed=0)
     r1, r2 = run_cuda(w, inp, repeat=2)
-    for k in r1:
-        assert torch.equal(r1[k], r2[k]), f"{k} differs between two runs"
+    assert_bitwise(r1, r2)
     _sampled_check(w, inp, r1, nrows=256, ncols=256, seed=11)
-
-
-def test_bloom_176b_sampled():
-    w = W.WORKLOADS["bloom_176b"]
-    inp = W.make_inputs(w, seed=0)
-    got = run_cuda(w, inp)
-    _sampled_check(w, inp, got, nrows=64, ncols=64, seed=12)
