@@ -4,9 +4,10 @@
 // too, so no shard exchanges anything here).
 //
 // With P = exp2(S log2(e)/sqrt(d) - lse2) (the forward's saved base-2
-// log-sum-exp), dO = dCtx and delta = rowsum(dO * O) (computed by the query
-// kernel from its dO tile and the forward's context rows, and written out for
-// the key/value kernel, which therefore runs second):
+// log-sum-exp), dO = dCtx and delta = rowsum(dO * O) = sum_j P dP (the query
+// kernel starts from the first form, from its dO tile and the forward's
+// context rows, and writes the second, from its own P and dP, for the
+// key/value kernel, which therefore runs second):
 //   dV = P^T dO,   dP = dO V^T,   dS = P * (dP - delta) / sqrt(d),
 //   dK = dS^T Q,   dQ = dS K.
 // Every output element has exactly one writer and no atomics are used:
@@ -21,13 +22,15 @@
 //   Q       query  Q   dO   K   V    S             dP              dQ += dS K, PK += P K
 // The Q kernel also forms delta for its 128 queries from its dO tile and the
 // forward's context rows (loaded into the last ring stage before the ring
-// first reaches it) and writes it out for the KV kernel.
+// first reaches it), and at its end writes sum_j P dP for the KV kernel.
 // The elementwise step writes dS (and P for KV) as bf16 into tensor memory,
 // over the score columns it has just read (each column-half warp inside its
 // own columns), where the output MMAs take them as A operands; their B
 // operands are the streamed tiles read M/N-major (the same bytes).
 // Outputs leave as 32-row x 64-column bf16 chunks staged in the idle B ring
-// and stored by TMA; at d = 128 each chunk is also summed over its 32 rows
+// and stored by TMA (at d = 96 the last 32 columns of dK and dV, and dQ,
+// with plain 16-byte stores); at d = 128 each chunk is also summed over its
+// 32 rows
 // into the partials of the QKV bias gradient.
 //
 // Warp roles: warp 0 TMA producer, warp 1 TMEM allocator and MMA issuer (the
@@ -51,7 +54,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                     const __grid_constant__ CUtensorMap tmCtx,
                     const __grid_constant__ CUtensorMap tmOut,
                     const AttnArgs a) {
-  constexpr int KB = D / 64;
+  // 64-wide blocks of d (d = 96: the second block's upper 32 columns are
+  // loaded but never used; the MMAs stop at K = d and N = d)
+  constexpr int KB = (D + 63) / 64;
   constexpr uint32_t A_TILE = KB * KBLOCK_BYTES;   // 128 rows x D
   constexpr uint32_t B_TILE = KB * ATOM_BYTES;     // 64 rows x D
   // Stages of the streamed tile pair: the load for step n + NB can only
@@ -68,8 +73,11 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 64, false, false);
   constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, false, true);
   constexpr uint32_t TMEM_OUT2 = 256;              // dK (KV) or dQ
-  constexpr uint32_t TMEM_OUT1 = 256 + D;          // dV (KV) or P K (Q)
-  constexpr float INV_SQRT_D = D == 64 ? 0.125f : 0.08838834764831845f;
+  constexpr uint32_t TMEM_OUT1 = 256 + 64 * KB;    // dV (KV) or P K (Q)
+  constexpr float INV_SQRT_D = D == 64   ? 0.125f
+                               : D == 96 ? 0.10206207261596575f
+                                         : 0.08838834764831845f;
+  static_assert(D == 64 || D == 96 || D == 128, "head dim");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -267,8 +275,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       // delta of this query row = sum_e dO[r][e] O[r][e], both tiles in shared
       // memory (128-byte-swizzled rows; O, the forward's context, in the last
       // ring stage until ctx_free), summed in fp32 in column order by both
-      // warps of the row (so both hold the same value without an exchange);
-      // half 0 writes it out.
+      // warps of the row (so both hold the same value without an exchange).
       const size_t off = static_cast<size_t>(head) * a.ld_stat + row0 + r;
       lse_r = a.lse[off];
       alive = warp_wait(a_full, 0, ctl, ROLE_EPILOGUE) &&
@@ -294,7 +301,6 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         }
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(ctx_free);
-        if (hf == 0) a.delta[off] = delta_r;
       }
     }
     const float* vec = reinterpret_cast<const float*>(vec_gen);
@@ -366,6 +372,15 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       red[hf * 128 + r] = rsum;
       pair_barrier(q);
       rrow = red[r] + red[128 + r];
+      // For the key/value kernel: delta' = sum_j P dP with this kernel's own
+      // P and dP (= delta + r sqrt(d), the P of a row summing to 1), so that
+      // its dS rows, formed from its own recomputed P and dP, carry no
+      // offset either.  With delta from the rounded context instead, every
+      // dS of a query row would be off by P times that rounding error,
+      // which dK = dS^T Q does not cancel.
+      if (alive && hf == 0)
+        a.delta[static_cast<size_t>(head) * a.ld_stat + row0 + r] =
+            delta_r + rrow / INV_SQRT_D;
     }
     if (alive && warp_wait(o_full, 0, ctl, ROLE_EPILOGUE)) {
       ptx::tc_fence_after();
@@ -402,6 +417,19 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                 col + 64 * j + 2 * lane) = cs;
           }
         }
+        if constexpr (D % 64 != 0) {
+          // the last 32 columns (a 64-column chunk would reach into the next
+          // head's columns): each thread its own row, 64 bytes
+          uint32_t rr[32];
+          ptx::tmem_ld_32x32b_x32(src + 64 * (D / 64), rr);
+          ptx::tmem_ld_wait();
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(rr[i]);
+          store_bf16x32(a.dqkv + static_cast<size_t>(row0 + r) * a.ld_qkv + col +
+                            64 * (D / 64),
+                        v);
+        }
         st.drain(lane);
       } else if constexpr (D == 128) {
         // dQ: each warp its 32 rows x 64 columns (one chunk), staged and
@@ -434,24 +462,22 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         }
         st.drain(lane);
       } else {
-        constexpr int OCH = D / 64;        // 32-column chunks per half
+        // dQ: this warp's D / 2 columns of its row, 16 at a time
         __nv_bfloat16* out2 = a.dqkv + static_cast<size_t>(row0 + r) * a.ld_qkv +
                               hc.q + hf * (D / 2);
 #pragma unroll
-        for (int j = 0; j < OCH; ++j) {
-          uint32_t ov[32];
-          ptx::tmem_ld_32x32b_x32(
-              tmem + lane_base + TMEM_OUT2 + hf * (D / 2) + 32 * j, ov);
+        for (int j = 0; j < D / 32; ++j) {
+          uint32_t ov[16], kv[16];
+          ptx::tmem_ld_32x32b_x16(
+              tmem + lane_base + TMEM_OUT2 + hf * (D / 2) + 16 * j, ov);
+          ptx::tmem_ld_32x32b_x16(
+              tmem + lane_base + TMEM_OUT1 + hf * (D / 2) + 16 * j, kv);
           ptx::tmem_ld_wait();
-          uint32_t kv[32];
-          ptx::tmem_ld_32x32b_x32(
-              tmem + lane_base + TMEM_OUT1 + hf * (D / 2) + 32 * j, kv);
-          ptx::tmem_ld_wait();
-          float v[32];
+          float v[16];
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
+          for (int i = 0; i < 16; ++i)
             v[i] = fmaf(-rrow, __uint_as_float(kv[i]), __uint_as_float(ov[i]));
-          store_bf16x32(out2 + 32 * j, v);
+          store_bf16x16(out2 + 16 * j, v);
         }
       }
     }
@@ -478,7 +504,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
 // TMEM columns) never shares the SM.
 template <int D, bool KV>
 size_t attn_bwd_smem() {
-  constexpr int KB = D / 64;
+  constexpr int KB = (D + 63) / 64;
   constexpr int NB = KV ? 4 : 5;
   const size_t need = 1024 + 2 * KB * KBLOCK_BYTES + NB * 2 * KB * ATOM_BYTES +
                       (KV ? NB * 512 : 1024) + (11 + 2 * NB) * 8 + 16;
@@ -508,6 +534,9 @@ cudaError_t launch_attn_dkdv(const CUtensorMap& tq128, const CUtensorMap& tq64,
   if (a.head_dim == 128)
     return launch_bwd<128, true>(tq128, tq128, tq64, tdo64, tq128, tdqkv_out, a,
                                  grid, s);
+  if (a.head_dim == 96)
+    return launch_bwd<96, true>(tq128, tq128, tq64, tdo64, tq128, tdqkv_out, a,
+                                grid, s);
   if (a.head_dim == 64)
     return launch_bwd<64, true>(tq128, tq128, tq64, tdo64, tq128, tdqkv_out, a,
                                 grid, s);
@@ -521,6 +550,9 @@ cudaError_t launch_attn_dq(const CUtensorMap& tq128, const CUtensorMap& tq64,
   if (a.head_dim == 128)
     return launch_bwd<128, false>(tq128, tdo128, tq64, tq64, tctx128, tdqkv_out,
                                   a, grid, s);
+  if (a.head_dim == 96)
+    return launch_bwd<96, false>(tq128, tdo128, tq64, tq64, tctx128, tdqkv_out,
+                                 a, grid, s);
   if (a.head_dim == 64)
     return launch_bwd<64, false>(tq128, tdo128, tq64, tq64, tctx128, tdqkv_out,
                                  a, grid, s);

@@ -55,7 +55,10 @@ __global__ void __launch_bounds__(FWD_THREADS, 2)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQK,
                     const __grid_constant__ CUtensorMap tmV,
                     const AttnArgs a) {
-  constexpr int KB = D / 64;                           // 64-wide blocks of d
+  // 64-wide blocks of d (d = 96: the second block's upper 32 columns belong
+  // to the next head or lie past the tensor; they are loaded, never used:
+  // the MMAs below stop at K = d and N = d)
+  constexpr int KB = (D + 63) / 64;
   constexpr uint32_t QK_TILE = KB * KBLOCK_BYTES;      // 128 x D
   constexpr uint32_t V_TILE = 2 * KB * ATOM_BYTES;     // 128 keys x D
   constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, false, false);
@@ -257,16 +260,17 @@ __global__ void __launch_bounds__(FWD_THREADS, 2)
         m_ref = mb;
       }
       if (__any_sync(0xffffffffu, move) && kb > 0) {
+        // this warp's D / 2 output columns, 16 at a time
 #pragma unroll 1
-        for (int j = 0; j < D / 64; ++j) {
-          const uint32_t oc = tmem + lane_base + TMEM_O + hf * (D / 2) + 32 * j;
-          uint32_t ov[32];
-          ptx::tmem_ld_32x32b_x32(oc, ov);
+        for (int j = 0; j < D / 32; ++j) {
+          const uint32_t oc = tmem + lane_base + TMEM_O + hf * (D / 2) + 16 * j;
+          uint32_t ov[16];
+          ptx::tmem_ld_32x32b_x16(oc, ov);
           ptx::tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
+          for (int i = 0; i < 16; ++i)
             ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-          tmem_st_32x32b_x32(oc, ov);
+          tmem_st_32x32b_x16(oc, ov);
         }
       }
       // P: 32 scores at a time, packed two per column over columns that
@@ -327,19 +331,19 @@ __global__ void __launch_bounds__(FWD_THREADS, 2)
                   ROLE_EPILOGUE)) {
       ptx::tc_fence_after();
       const float inv_l = 1.0f / l;
-      constexpr int OCH = D / 64;         // 32-column chunks per half
+      // this warp's D / 2 context columns, 16 at a time (32 bytes a row)
       __nv_bfloat16* out = a.ctx + static_cast<size_t>(row0 + r) * a.ld_ctx +
                            head * D + hf * (D / 2);
 #pragma unroll 1
-      for (int j = 0; j < OCH; ++j) {
-        uint32_t ov[32];
-        ptx::tmem_ld_32x32b_x32(
-            tmem + lane_base + TMEM_O + hf * (D / 2) + 32 * j, ov);
+      for (int j = 0; j < D / 32; ++j) {
+        uint32_t ov[16];
+        ptx::tmem_ld_32x32b_x16(
+            tmem + lane_base + TMEM_O + hf * (D / 2) + 16 * j, ov);
         ptx::tmem_ld_wait();
-        float v[32];
+        float v[16];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(ov[i]) * inv_l;
-        store_bf16x32(out + 32 * j, v);
+        for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(ov[i]) * inv_l;
+        store_bf16x16(out + 16 * j, v);
       }
       if (hf == 0)
         a.lse[static_cast<size_t>(head) * a.ld_stat + row0 + r] =
@@ -369,7 +373,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 2)
 // more than two CTAs (2 x 256 TMEM columns) share an SM.
 template <int D>
 size_t attn_fwd_smem() {
-  constexpr int KB = D / 64;
+  constexpr int KB = (D + 63) / 64;
   const size_t need = 1024 + 2 * KB * KBLOCK_BYTES + 2 * KB * ATOM_BYTES +
                       128 + 6 * 128 * 4;
   return need > 80 * 1024 ? need : 80 * 1024;
@@ -392,6 +396,7 @@ cudaError_t launch_fwd(const CUtensorMap& tqk, const CUtensorMap& tv,
 cudaError_t launch_attn_fwd(const CUtensorMap& tqk, const CUtensorMap& tv,
                             const AttnArgs& a, int grid, cudaStream_t s) {
   if (a.head_dim == 128) return launch_fwd<128>(tqk, tv, a, grid, s);
+  if (a.head_dim == 96) return launch_fwd<96>(tqk, tv, a, grid, s);
   if (a.head_dim == 64) return launch_fwd<64>(tqk, tv, a, grid, s);
   return cudaErrorInvalidValue;
 }

@@ -137,7 +137,7 @@ int tp_attn_create(const tp_attn_config* cfg, tp_attn_handle** out) {
   if (cfg->hidden % cfg->heads != 0 || cfg->heads % cfg->shards != 0)
     return TPMLP_ERR_SHAPE;
   const int d = cfg->hidden / cfg->heads;
-  if (d != 64 && d != 128) return TPMLP_ERR_SHAPE;
+  if (d != 64 && d != 96 && d != 128) return TPMLP_ERR_SHAPE;
   if ((cfg->hidden / cfg->shards) % 64 != 0) return TPMLP_ERR_SHAPE;
   if (cfg->seq_len % 128 != 0) return TPMLP_ERR_SHAPE;
   if (static_cast<long long>(cfg->max_tokens) > (1LL << 28) ||

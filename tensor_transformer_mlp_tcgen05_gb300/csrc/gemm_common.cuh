@@ -68,6 +68,18 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* p,
   }
 }
 
+__device__ __forceinline__ void store_bf16x16(__nv_bfloat16* p,
+                                              const float (&v)[16]) {
+  uint4* q = reinterpret_cast<uint4*>(p);
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    q[i] = make_uint4(pack_bf16x2(v[8 * i + 0], v[8 * i + 1]),
+                      pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                      pack_bf16x2(v[8 * i + 4], v[8 * i + 5]),
+                      pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+  }
+}
+
 __device__ __forceinline__ void store_f32x32(float* p, const float (&v)[32]) {
   float4* q = reinterpret_cast<float4*>(p);
 #pragma unroll

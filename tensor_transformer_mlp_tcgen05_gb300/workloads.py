@@ -181,9 +181,14 @@ ATTN_WORKLOADS = {
                                   w_std=0.0625),
     "attn_tiny_d128": AttnWorkload("attn_tiny_d128", 2, 384, 512, 4, 2,
                                    w_std=0.044),
+    "attn_tiny_d96": AttnWorkload("attn_tiny_d96", 2, 256, 768, 8, 2,
+                                  w_std=0.036),
     # GPT-2-medium-shaped and GPT-3-13B-shaped layers (as the MLP workloads)
     "attn_gpt2_medium": AttnWorkload("attn_gpt2_medium", 8, 1024, 1024, 16, 4),
     "attn_gpt3_13b": AttnWorkload("attn_gpt3_13b", 4, 2048, 5120, 40, 8),
+    # the 8.3B GPT-2 of the scaling study: h = 3072, 32 heads of 96, pre-LN
+    "attn_megatron_8p3b": AttnWorkload("attn_megatron_8p3b", 8, 1024, 3072,
+                                       32, 8, layernorm=True),
 }
 
 

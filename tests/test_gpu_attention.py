@@ -112,11 +112,18 @@ CASES = [
     # rescale threshold across key blocks
     ("d64_causal_peaked", dict(seq=512, batch=1), "sign", False),
     ("d128_full_peaked", dict(causal=False), "sign", False),
+    # head dim 96, the 8.3B model's 3072 / 32
+    ("d96_causal_t2", {}, True, False),
+    ("d96_full_t1", dict(causal=False, shards=1), False, False),
+    ("d96_causal_t4_ln_res", dict(shards=4, layernorm=True), True, True),
+    ("d96_full_t2_ln", dict(causal=False, layernorm=True), True, False),
+    ("d96_causal_peaked", dict(seq=384, batch=1), "sign", False),
 ]
 
 
 def _workload(name, over):
-    base = "attn_tiny_d64" if name.startswith("d64") else "attn_tiny_d128"
+    base = {"d64": "attn_tiny_d64", "d96": "attn_tiny_d96",
+            "d128": "attn_tiny_d128"}[name.split("_")[0]]
     return W.ATTN_WORKLOADS[base].with_(**over)
 
 
@@ -133,7 +140,9 @@ def test_attention_forward_backward_parity(name, over, bias, res):
         inp["beta"] = 0.2 * torch.randn(w.hidden, generator=g)
     got = run_attn(w, inp, residual=res)
     ref = oracle(w, inp, residual=res)
-    compare(got, ref)
+    report = compare(got, ref)
+    print(name, " ".join(f"{k}={v[0]:.2e}/{v[1]:.2e}"
+                         for k, v in sorted(report.items())))
 
 
 def test_attention_bitwise_repeatable():
@@ -178,11 +187,13 @@ def _head_cols(w, j):
 @pytest.mark.parametrize("name,samples", [
     ("attn_gpt3_13b", ((0, 0), (1, 17), (3, 39))),
     ("attn_gpt2_medium", ((0, 0), (5, 9), (7, 15))),
+    ("attn_megatron_8p3b", ((0, 0), (3, 13), (7, 31))),
 ])
 def test_attention_full_size_sampled_invariants_and_bitwise(name, samples):
     """The GPT-3-13B-shaped layer (4 x 2048 tokens, h = 5120, 40 heads of
-    128, 8 shards, causal) and the GPT-2-medium-shaped one (8 x 1024 tokens,
-    h = 1024, 16 heads of 64, 4 shards) at full size, in the launch
+    128, 8 shards, causal), the GPT-2-medium-shaped one (8 x 1024 tokens,
+    h = 1024, 16 heads of 64, 4 shards) and the Megatron-8.3B one (8 x 1024
+    tokens, h = 3072, 32 heads of 96, 8 shards, pre-LN) at full size, in the launch
     configuration the benchmark times.  Checked against the oracle from the original inputs:
     Ctx, the log-sum-exp and dQKV of sampled (sequence, head) pairs; Z on
     every sequence's first 128 rows (causal rows there see keys 0..127
@@ -197,6 +208,8 @@ def test_attention_full_size_sampled_invariants_and_bitwise(name, samples):
     S, h, d, H = w.seq, w.hidden, w.head_dim, w.heads
     X, Wqkv, Wo = f64(inp["X"]), f64(inp["Wqkv"]), f64(inp["Wo"])
     bqkv, bo, dZ = f64(inp["bqkv"]), f64(inp["bo"]), f64(inp["dZ"])
+    if w.layernorm:   # the projections see LN(X) (gamma = 1, beta = 0)
+        X = A.layernorm_forward(X, f64(inp["gamma"]), f64(inp["beta"]))[0]
     ctx, dqkv = f64(a["Ctx"]), f64(a["dQKV"])
     lse2 = f64(a["lse2"])
     # sampled heads: forward core and its backward, from the inputs

@@ -56,9 +56,13 @@ def _brute(X, Wqkv, Wo, bqkv, bo, heads, s, shards, causal):
                       for o in range(h)] for r in range(T)])
 
 
-@pytest.mark.parametrize("causal,shards", [(True, 1), (True, 2), (False, 2)])
-def test_forward_matches_brute_force(causal, shards):
-    p, c = _problem(seed=1, heads=2)
+@pytest.mark.parametrize("causal,shards,h,heads", [
+    (True, 1, 8, 2), (True, 2, 8, 2), (False, 2, 8, 2),
+    # a head dim that is not a power of two (d = 3, as 96 = 3 * 32): the
+    # 1 / sqrt(d) scale and the head columns at multiples of d
+    (True, 2, 12, 4), (False, 1, 12, 4)])
+def test_forward_matches_brute_force(causal, shards, h, heads):
+    p, c = _problem(seed=1, h=h, heads=heads)
     got = A.forward(p["X"], p["Wqkv"], p["Wo"], c["heads"], c["seq_len"], shards,
                     bqkv=p["bqkv"], bo=p["bo"], causal=causal)["Z"]
     want = _brute(p["X"].tolist(), p["Wqkv"].tolist(), p["Wo"].tolist(),
