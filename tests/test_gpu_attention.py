@@ -14,6 +14,7 @@ import torch
 from oracle import attention as A
 from tensor_transformer_mlp_tcgen05_gb300 import workloads as W
 
+import attention_rounding as R
 from fingerprint import ATTN_KERNEL, ATTN_ORDER, assert_bitwise
 from parity_helpers import assert_close, errors, f64
 
@@ -23,14 +24,22 @@ LOG2E = 1.0 / math.log(2.0)
 
 # Tolerances.  Forward outputs (QKV, Ctx, the log-sum-exp, Z) keep the
 # block's bf16 bar: relative Frobenius error <= 5e-3, max |err| <= 3e-2
-# max |ref|.  The gradients pass through a longer chain of bf16 roundings
-# (the stored QKV and Ctx, dCtx, the staged P and dS operands, dQKV, dX),
-# each adding an independent relative error of about 2^-8 / sqrt(3) ~ 2.3e-3
-# rms at most; six in quadrature give ~5.5e-3, and dS = P (dP - delta)
-# subtracts nearly equal terms, so the gradient bar is 1e-2 (max |err| bar
-# unchanged).  Exact sums (db_o = sum_T dZ of bf16 inputs) land near 1e-8.
+# max |ref|.  The gradients are bounded by the bf16 storage of the block's
+# intermediates: the fp64 block with bf16 rounding at the kernels' seven
+# storage points (tests/attention_rounding.py: LayerNorm output, Q/K/V, the
+# staged P, Ctx, dCtx, the staged dS, dQ/dK/dV) has, against the exact
+# block, the same errors the kernels show (e.g. dQKV 5.61e-3 emulated and
+# 5.61e-3 measured for the full-attention, LayerNorm, residual case; Q/K/V
+# alone 3-3.6e-3, the LayerNorm output alone ~3e-3).  The gradient bar is
+# set just above the measured worst case, 6.4e-3 (dK of the 8.3B layer's
+# sampled heads), with the max |err| bar unchanged.  In addition the
+# gradients must agree with that emulation within TOL_EMU (measured <=
+# 2.5e-3: the forward stages P before its normalisation and the query
+# kernel stages dS before its row correction, so those two roundings fall
+# on different values).  Exact sums (db_o = sum_T dZ) land near 1e-8.
 FWD_KEYS = ("Z", "QKV", "Ctx", "lse")
-TOL_GRAD = (1e-2, 3e-2)
+TOL_GRAD = (7e-3, 3e-2)
+TOL_EMU = (4e-3, 3e-2)
 
 
 def run_attn(w, inp, backward=True, residual=False, repeat=1):
@@ -143,6 +152,14 @@ def test_attention_forward_backward_parity(name, over, bias, res):
     report = compare(got, ref)
     print(name, " ".join(f"{k}={v[0]:.2e}/{v[1]:.2e}"
                          for k, v in sorted(report.items())))
+    emu = R.backward_rounded(inp, w.heads, w.seq, w.shards, w.causal, res,
+                             R.POINTS)
+    emu["dX"] = R.bf16(emu["dX"])          # the output's own dtype
+    for k in ("dQKV", "dX", "dWqkv", "dWo"):
+        rel_fro, max_rel = errors(got[k], emu[k])
+        print(name, "vs emulated", k, f"{rel_fro:.2e}/{max_rel:.2e}")
+        assert rel_fro <= TOL_EMU[0] and max_rel <= TOL_EMU[1], (
+            k, rel_fro, max_rel)
 
 
 def test_attention_bitwise_repeatable():
@@ -229,6 +246,7 @@ def test_attention_full_size_sampled_invariants_and_bitwise(name, samples):
                                      do[:, None], probs, S)
         for nm, cols, ref in (("dQ", cq, dq), ("dK", ck, dk), ("dV", cv, dv)):
             rel_fro, max_rel = errors(dqkv[rows, cols], ref[:, 0])
+            print(name, nm, seq, j, f"{rel_fro:.2e}/{max_rel:.2e}")
             assert rel_fro <= TOL_GRAD[0] and max_rel <= TOL_GRAD[1], (
                 nm, seq, j, rel_fro, max_rel)
     # Z on the first 128 rows of every sequence
