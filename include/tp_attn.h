@@ -56,7 +56,7 @@ extern "C" {
 
 typedef struct tp_attn_config {
   int   hidden;          /* h; multiple of 64                                */
-  int   heads;           /* H; d = h / H must be 64 or 128; H % t == 0       */
+  int   heads;           /* H; d = h / H must be 64, 96 or 128; H % t == 0   */
   int   shards;          /* t; h_t = h / t multiple of 64                    */
   int   max_tokens;      /* largest T any call will pass                     */
   int   seq_len;         /* tokens per sequence; multiple of 128             */

@@ -25,7 +25,7 @@ namespace {
 struct AttnLayout {
   size_t status = 0, xn = 0, mean = 0, rstd = 0, qkv = 0, ctx = 0, lse = 0,
          dctx = 0, delta = 0, dqkv = 0, dxn = 0, part = 0, tailp = 0,
-         total = 0;
+         total = 0, lnp = 0;
   int chunks = 0;   // 256-row column-sum chunks
   int groups = 0;   // 32-row groups of the core kernels' fused db_qkv partials
 };
@@ -60,9 +60,12 @@ AttnLayout attn_layout(const tp_attn_config& c, int tokens, int training) {
     if (c.use_layernorm) L.dxn = take(T * h * 4);
     L.chunks = colsum_chunks(tokens);
     L.groups = (tokens + 31) / 32;
-    // db_o (chunks x h), db_qkv (max(groups, chunks) x 3h), dgamma, dbeta
+    // db_o (chunks x h), db_qkv (max(groups, chunks) x 3h), dgamma and
+    // dbeta (lnp x h each)
     const size_t rows3 = static_cast<size_t>(L.groups > L.chunks ? L.groups : L.chunks);
-    L.part = take((static_cast<size_t>(L.chunks) * 3 * h + rows3 * 3 * h) * 4);
+    L.lnp = static_cast<size_t>(L.chunks);
+    L.part = take((static_cast<size_t>(L.chunks) * h + rows3 * 3 * h +
+                   2 * L.lnp * h) * 4);
   }
   L.total = off;
   return L;
@@ -378,26 +381,10 @@ int tp_attn_backward(tp_attn_handle* H, int tokens, const void* dZ,
     const float* mean = reinterpret_cast<const float*>(ws + L.mean);
     const float* rstd = reinterpret_cast<const float*>(ws + L.rstd);
     const void* dres = c.use_residual ? dZ : nullptr;
-    TRY(run(&H->core, "layernorm_bwd", s, [&] {
-      return launch_ln_bwd(true, dXn, X, mean, rstd, ln_gamma, dres, dX, T, h,
-                           s);
-    }));
-    if (dgamma || dbeta) {
-      float* pg = part3 + size_t(L.groups > L.chunks ? L.groups : L.chunks) * 3 * h;
-      float* pb = pg + size_t(L.chunks) * h;
-      TRY(run(&H->core, "layernorm_param_partial", s, [&] {
-        return launch_ln_param_partial(true, dXn, X, mean, rstd, pg, pb, T, h,
-                                       s);
-      }));
-      if (dgamma)
-        TRY(run(&H->core, "colsum_finalize", s, [&] {
-          return launch_colsum_finalize(pg, dgamma, L.chunks, h, s);
-        }));
-      if (dbeta)
-        TRY(run(&H->core, "colsum_finalize", s, [&] {
-          return launch_colsum_finalize(pb, dbeta, L.chunks, h, s);
-        }));
-    }
+    float* pg = part3 + size_t(L.groups > L.chunks ? L.groups : L.chunks) * 3 * h;
+    float* pb = pg + L.lnp * h;
+    TRY(ln_backward(&H->core, s, true, dXn, X, mean, rstd, ln_gamma, dres, dX,
+                    pg, pb, dgamma, dbeta, T, h));
   }
   return TPMLP_OK;
 }

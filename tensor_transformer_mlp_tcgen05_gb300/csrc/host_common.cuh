@@ -285,6 +285,33 @@ inline int tc_gemm(HandleCore* H, const char* name, cudaStream_t s, int sms,
   });
 }
 
+// LayerNorm backward (dX from dXn, plus dres when not null) and, when asked
+// for, its parameter gradients (partial sums over 256-row chunks, then the
+// fixed-order finalizes).  pg and pb hold colsum_chunks(T) x h floats each.
+inline int ln_backward(HandleCore* H, cudaStream_t s, bool bf16,
+                       const float* dXn, const void* X, const float* mean,
+                       const float* rstd, const float* gamma, const void* dres,
+                       void* dX, float* pg, float* pb, float* dgamma,
+                       float* dbeta, int T, int h) {
+  TRY(run(H, "layernorm_bwd", s, [&] {
+    return launch_ln_bwd(bf16, dXn, X, mean, rstd, gamma, dres, dX, T, h, s);
+  }));
+  if (dgamma == nullptr && dbeta == nullptr) return TPMLP_OK;
+  TRY(run(H, "layernorm_param_partial", s, [&] {
+    return launch_ln_param_partial(bf16, dXn, X, mean, rstd, pg, pb, T, h, s);
+  }));
+  const int chunks = colsum_chunks(T);
+  if (dgamma)
+    TRY(run(H, "colsum_finalize", s, [&] {
+      return launch_colsum_finalize(pg, dgamma, chunks, h, s);
+    }));
+  if (dbeta)
+    TRY(run(H, "colsum_finalize", s, [&] {
+      return launch_colsum_finalize(pb, dbeta, chunks, h, s);
+    }));
+  return TPMLP_OK;
+}
+
 inline int colsum(HandleCore* H, const char* name, cudaStream_t s, bool bf16,
            const void* src, float* part, float* out, int rows, int cols) {
   const int chunks = colsum_chunks(rows);

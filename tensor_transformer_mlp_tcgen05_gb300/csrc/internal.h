@@ -114,7 +114,9 @@ cudaError_t launch_colsum_partial(bool bf16, const void* src, float* part,
                                   unsigned int* amax = nullptr);
 
 // LayerNorm parameter gradients, stage 1: part_g[chunk][c] = sum dXn * xhat,
-// part_b[chunk][c] = sum dXn over the chunk's rows.
+// part_b[chunk][c] = sum dXn over the chunk's rows (colsum_chunks(rows)
+// chunks; the chunks are visited last first, so that the rows the LayerNorm
+// backward read last are still in L2).
 cudaError_t launch_ln_param_partial(bool bf16, const float* dXn, const void* X,
                                     const float* mean, const float* rstd,
                                     float* part_g, float* part_b, int rows,

@@ -250,6 +250,83 @@ __global__ void __launch_bounds__(LN_WARPS * 32)
   }
 }
 
+// LayerNorm forward with the row in registers (h = 256 VPL, bf16): each
+// lane loads its VPL 16-byte vectors of the row at once (one DRAM round
+// trip per row), then the mean, the variance about it and the normalised
+// row come from registers.  Each lane adds its values in vector order, then
+// the butterfly, as in ln_fwd_kernel (same two-pass formula).
+// Keeps the compiler from carrying unpacked copies of the row from one pass
+// to the next (the raw vectors are all that stays live between passes).
+template <int VPL>
+__device__ __forceinline__ void opaque(uint4 (&raw)[VPL]) {
+#pragma unroll
+  for (int j = 0; j < VPL; ++j)
+    asm volatile("" : "+r"(raw[j].x), "+r"(raw[j].y), "+r"(raw[j].z),
+                 "+r"(raw[j].w));
+}
+
+template <int VPL>
+__global__ void __launch_bounds__(LN_WARPS * 32, 2)
+    ln_fwd_reg_kernel(const __nv_bfloat16* __restrict__ X,
+                      const float* __restrict__ gamma,
+                      const float* __restrict__ beta,
+                      __nv_bfloat16* __restrict__ Xn,
+                      float* __restrict__ mean_out,
+                      float* __restrict__ rstd_out, int rows, int h,
+                      float eps) {
+  const int row = blockIdx.x * LN_WARPS + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const size_t base = static_cast<size_t>(row) * h;
+  const uint4* xr = reinterpret_cast<const uint4*>(X + base);
+  uint4 raw[VPL];
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) raw[j] = xr[lane + 32 * j];
+  float s = 0.f;
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) {
+    float v[8];
+    unpack_vec<__nv_bfloat16>(raw[j], v);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) s += v[k];
+  }
+  const float inv_h = 1.0f / static_cast<float>(h);
+  const float mu = warp_sum(s) * inv_h;
+  opaque(raw);
+  float ss = 0.f;
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) {
+    float v[8];
+    unpack_vec<__nv_bfloat16>(raw[j], v);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float d = v[k] - mu;
+      ss += d * d;
+    }
+  }
+  const float rs = rsqrtf(warp_sum(ss) * inv_h + eps);
+  opaque(raw);
+  uint4* yr = reinterpret_cast<uint4*>(Xn + base);
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) {
+    const int i = lane + 32 * j;
+    float v[8], g[8], b[8];
+    unpack_vec<__nv_bfloat16>(raw[j], v);
+    load_f32<8>(gamma + 8 * i, g);
+    load_f32<8>(beta + 8 * i, b);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v[k] = (v[k] - mu) * rs * g[k] + b[k];
+    yr[i] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                       pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+    // gamma / beta are L1 hits: no need to load them ahead of this store
+    asm volatile("" ::: "memory");
+  }
+  if (lane == 0) {
+    mean_out[row] = mu;
+    rstd_out[row] = rs;
+  }
+}
+
 // ------------------------------------------------------- column sums --
 
 constexpr int CS_WARPS = 8;
@@ -423,6 +500,86 @@ __global__ void __launch_bounds__(CS_WARPS * 32)
   }
 }
 
+// MODE 1 for bf16 X with h % 8 == 0: the same sums in the same order as
+// colsum_partial_kernel<bf16, 1> (per column: warp w adds rows w, w + 8, ...
+// of the chunk in row order, then the eight warp sums in warp order), 8
+// columns per lane from one 16-byte load of X and two of dXn, four rows'
+// loads in flight, 256 columns per block.  Chunks run last first
+// (blockIdx.y = 0 takes the last chunk): the LayerNorm backward has just
+// read the last rows, which are then still in L2.
+__global__ void __launch_bounds__(CS_WARPS * 32)
+    ln_param_partial_bf16x8_kernel(const __nv_bfloat16* __restrict__ X,
+                                   const float* __restrict__ dxn,
+                                   const float* __restrict__ mean,
+                                   const float* __restrict__ rstd,
+                                   float* __restrict__ part_g,
+                                   float* __restrict__ part_b, int rows,
+                                   int cols) {
+  __shared__ float red[2][CS_WARPS][CS8_COLS];
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.x * CS8_COLS + lane * 8;
+  const int chunk = static_cast<int>(gridDim.y - 1 - blockIdx.y);
+  const int r0 = chunk * COLSUM_CHUNK_ROWS;
+  const int r1 = min(rows, r0 + COLSUM_CHUNK_ROWS);
+  float ag[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float ab[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  auto accumulate = [&](const uint4 xu, const float4 d0, const float4 d1,
+                        float mu, float rs) {
+    const uint32_t q[4] = {xu.x, xu.y, xu.z, xu.w};
+    const float d[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float lo, hi;
+      unpack_bf16x2(q[j], lo, hi);
+      ag[2 * j] += d[2 * j] * ((lo - mu) * rs);
+      ag[2 * j + 1] += d[2 * j + 1] * ((hi - mu) * rs);
+      ab[2 * j] += d[2 * j];
+      ab[2 * j + 1] += d[2 * j + 1];
+    }
+  };
+  if (c < cols) {
+    int r = r0 + w;
+    for (; r + 3 * CS_WARPS < r1; r += 4 * CS_WARPS) {
+      uint4 xu[4];
+      float4 d0[4], d1[4];
+      float mu[4], rs[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const size_t off = static_cast<size_t>(r + k * CS_WARPS) * cols + c;
+        xu[k] = *reinterpret_cast<const uint4*>(X + off);
+        d0[k] = *reinterpret_cast<const float4*>(dxn + off);
+        d1[k] = *reinterpret_cast<const float4*>(dxn + off + 4);
+        mu[k] = mean[r + k * CS_WARPS];
+        rs[k] = rstd[r + k * CS_WARPS];
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) accumulate(xu[k], d0[k], d1[k], mu[k], rs[k]);
+    }
+    for (; r < r1; r += CS_WARPS) {
+      const size_t off = static_cast<size_t>(r) * cols + c;
+      accumulate(*reinterpret_cast<const uint4*>(X + off),
+                 *reinterpret_cast<const float4*>(dxn + off),
+                 *reinterpret_cast<const float4*>(dxn + off + 4), mean[r],
+                 rstd[r]);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    red[0][w][lane * 8 + k] = ag[k];
+    red[1][w][lane * 8 + k] = ab[k];
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < 2 * CS8_COLS; idx += blockDim.x) {
+    const int which = idx / CS8_COLS, cc = idx % CS8_COLS;
+    const int col = blockIdx.x * CS8_COLS + cc;
+    if (col >= cols) continue;
+    float t = 0.f;
+#pragma unroll
+    for (int ww = 0; ww < CS_WARPS; ++ww) t += red[which][ww][cc];
+    (which == 0 ? part_g : part_b)[static_cast<size_t>(chunk) * cols + col] = t;
+  }
+}
+
 // out[c] = sum_k part[k][c] in a fixed order: 32 columns per block, warp y
 // sums the y-th eighth of the chunks in chunk order, then the eight warp
 // sums are added in warp order.  Coalesced 128-byte rows, any chunk count.
@@ -500,7 +657,28 @@ cudaError_t launch_ln_fwd(bool bf16, const void* X, const float* gamma,
                           const float* beta, void* Xn, float* mean,
                           float* rstd, int rows, int h, float eps,
                           cudaStream_t stream) {
+  if (rows <= 0) return cudaSuccess;
   const int grid = (rows + LN_WARPS - 1) / LN_WARPS;
+  const int vpl = h % 256 == 0 ? h / 256 : 0;
+#define TPMLP_LN_FWD_REG(N)                                                  \
+  ln_fwd_reg_kernel<N><<<grid, LN_WARPS * 32, 0, stream>>>(                  \
+      static_cast<const __nv_bfloat16*>(X), gamma, beta,                     \
+      static_cast<__nv_bfloat16*>(Xn), mean, rstd, rows, h, eps)
+  if (bf16 && vpl >= 1 && vpl <= 12) {
+    switch (vpl) {
+      case 1: TPMLP_LN_FWD_REG(1); break;
+      case 2: TPMLP_LN_FWD_REG(2); break;
+      case 3: TPMLP_LN_FWD_REG(3); break;
+      case 4: TPMLP_LN_FWD_REG(4); break;
+      case 6: TPMLP_LN_FWD_REG(6); break;
+      case 8: TPMLP_LN_FWD_REG(8); break;
+      case 12: TPMLP_LN_FWD_REG(12); break;
+      default: goto generic;
+    }
+#undef TPMLP_LN_FWD_REG
+    return cudaGetLastError();
+  }
+generic:
   if (bf16) {
     ln_fwd_kernel<__nv_bfloat16><<<grid, LN_WARPS * 32, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(X), gamma, beta,
@@ -517,6 +695,7 @@ cudaError_t launch_ln_bwd(bool bf16, const float* dXn, const void* X,
                           const float* mean, const float* rstd,
                           const float* gamma, const void* dres, void* dX,
                           int rows, int h, cudaStream_t stream) {
+  if (rows <= 0) return cudaSuccess;
   const int grid = (rows + LN_WARPS - 1) / LN_WARPS;
   const int nv = h / (bf16 ? 8 : 4);
   const int vpl = nv % 32 == 0 ? nv / 32 : 0;
@@ -572,7 +751,14 @@ cudaError_t launch_ln_param_partial(bool bf16, const float* dXn, const void* X,
                                     float* part_g, float* part_b, int rows,
                                     int h, cudaStream_t stream) {
   const dim3 grid((h + CS_COLS - 1) / CS_COLS, colsum_chunks(rows));
-  if (bf16) {
+  if (bf16 && h % 8 == 0 &&
+      (reinterpret_cast<uintptr_t>(X) & 15u) == 0 &&
+      (reinterpret_cast<uintptr_t>(dXn) & 15u) == 0) {
+    const dim3 grid8((h + CS8_COLS - 1) / CS8_COLS, colsum_chunks(rows));
+    ln_param_partial_bf16x8_kernel<<<grid8, CS_WARPS * 32, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(X), dXn, mean, rstd, part_g, part_b,
+        rows, h);
+  } else if (bf16) {
     colsum_partial_kernel<__nv_bfloat16, 1><<<grid, CS_WARPS * 32, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(X), dXn, mean, rstd, part_g, part_b,
         rows, h, nullptr);

@@ -33,6 +33,7 @@ namespace {
 struct Layout {
   size_t status = 0, xn = 0, mean = 0, rstd = 0, y = 0, h = 0, dh = 0,
          dxn = 0, dze = 0, part = 0, tailp = 0, total = 0;
+  size_t lnp = 0;   // rows of each LayerNorm-parameter partial section
   int chunks = 0;   // 256-row column-sum chunks
   int groups = 0;   // 32-row groups of the dH GEMM's fused db1 partials
 };
@@ -43,7 +44,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // with LayerNorm; Y; [bf16: the GEMM tail-split partials, TAIL_PART_BYTES];
 // and for training H, dH, [dXn fp32 with LayerNorm], [the dropout-masked dZ
 // with dropout], column-sum partials: db2 (chunks x h), db1 (max(groups,
-// chunks) x f), dgamma and dbeta (chunks x h each).
+// chunks) x f), dgamma and dbeta (lnp = chunks x h each).
 Layout make_layout(const tp_mlp_config& c, int tokens, int training) {
   Layout L;
   const size_t es = c.dtype == TPMLP_BF16 ? 2 : 4;
@@ -72,7 +73,10 @@ Layout make_layout(const tp_mlp_config& c, int tokens, int training) {
     L.chunks = colsum_chunks(tokens);
     L.groups = (tokens + 31) / 32;
     const size_t rows1 = static_cast<size_t>(L.groups > L.chunks ? L.groups : L.chunks);
-    L.part = take((static_cast<size_t>(L.chunks) * 3 * h + rows1 * f) * 4);
+    // db2 (chunks x h), db1 (rows1 x f), then the LayerNorm parameter
+    // partials (2 x chunks x h)
+    L.lnp = static_cast<size_t>(L.chunks);
+    L.part = take((static_cast<size_t>(L.chunks) * h + rows1 * f + 2 * L.lnp * h) * 4);
   }
   L.total = off;
   return L;
@@ -103,6 +107,7 @@ struct Fp8Layout {
   size_t tpitch = 0;  // row pitch (bytes) of the transposed code sections
   size_t hb = 0, xqt = 0, yqt = 0, bscales = 0, dzq = 0, dzqt = 0, dh = 0,
          dhq = 0, dhqt = 0, dxn = 0, part = 0, train_total = 0;
+  size_t lnp = 0;
   int chunks = 0, groups = 0;
 };
 // status | [Xn, mean, rstd] | [amax_x, amax_y (u32), s_x, s_y (f32)] |
@@ -149,7 +154,8 @@ Fp8Layout fp8_layout(const tp_mlp_config& c, int tokens) {
   L.chunks = colsum_chunks(tokens);
   L.groups = (tokens + 31) / 32;
   const size_t rows1 = static_cast<size_t>(L.groups > L.chunks ? L.groups : L.chunks);
-  L.part = take((static_cast<size_t>(L.chunks) * 3 * h + rows1 * f) * 4);
+  L.lnp = static_cast<size_t>(L.chunks);
+  L.part = take((static_cast<size_t>(L.chunks) * h + rows1 * f + 2 * L.lnp * h) * 4);
   L.train_total = off;
   return L;
 }
@@ -501,26 +507,10 @@ int tp_mlp_backward(tp_mlp_handle* H, int tokens, const void* dZ,
     const float* dXn = reinterpret_cast<const float*>(ws + L.dxn);
     const float* mean = reinterpret_cast<const float*>(ws + L.mean);
     const float* rstd = reinterpret_cast<const float*>(ws + L.rstd);
-    TRY(run(&H->core, "layernorm_bwd", s, [&] {
-      return launch_ln_bwd(bf16, dXn, X, mean, rstd, ln_gamma, dres, dX, T, h,
-                           s);
-    }));
-    if (dgamma || dbeta) {
-      float* pg = part1 + size_t(L.groups > L.chunks ? L.groups : L.chunks) * f;
-      float* pb = pg + size_t(L.chunks) * h;
-      TRY(run(&H->core, "layernorm_param_partial", s, [&] {
-        return launch_ln_param_partial(bf16, dXn, X, mean, rstd, pg, pb, T, h,
-                                       s);
-      }));
-      if (dgamma)
-        TRY(run(&H->core, "colsum_finalize", s, [&] {
-          return launch_colsum_finalize(pg, dgamma, L.chunks, h, s);
-        }));
-      if (dbeta)
-        TRY(run(&H->core, "colsum_finalize", s, [&] {
-          return launch_colsum_finalize(pb, dbeta, L.chunks, h, s);
-        }));
-    }
+    float* pg = part1 + size_t(L.groups > L.chunks ? L.groups : L.chunks) * f;
+    float* pb = pg + L.lnp * h;
+    TRY(ln_backward(&H->core, s, bf16, dXn, X, mean, rstd, ln_gamma, dres, dX,
+                    pg, pb, dgamma, dbeta, T, h));
   }
   return TPMLP_OK;
 }
@@ -899,26 +889,10 @@ int tp_mlp_backward_fp8(tp_mlp_handle* H, int tokens, const void* dZ,
     const float* mean = reinterpret_cast<const float*>(ws + L.mean);
     const float* rstd = reinterpret_cast<const float*>(ws + L.rstd);
     const void* dres = c.use_residual ? dZ : nullptr;
-    TRY(run(&H->core, "layernorm_bwd", s, [&] {
-      return launch_ln_bwd(true, dXn, X, mean, rstd, ln_gamma, dres, dX, T, h,
-                           s);
-    }));
-    if (dgamma || dbeta) {
-      float* pg = part1 + size_t(L.groups > L.chunks ? L.groups : L.chunks) * f;
-      float* pb = pg + size_t(L.chunks) * h;
-      TRY(run(&H->core, "layernorm_param_partial", s, [&] {
-        return launch_ln_param_partial(true, dXn, X, mean, rstd, pg, pb, T, h,
-                                       s);
-      }));
-      if (dgamma)
-        TRY(run(&H->core, "colsum_finalize", s, [&] {
-          return launch_colsum_finalize(pg, dgamma, L.chunks, h, s);
-        }));
-      if (dbeta)
-        TRY(run(&H->core, "colsum_finalize", s, [&] {
-          return launch_colsum_finalize(pb, dbeta, L.chunks, h, s);
-        }));
-    }
+    float* pg = part1 + size_t(L.groups > L.chunks ? L.groups : L.chunks) * f;
+    float* pb = pg + L.lnp * h;
+    TRY(ln_backward(&H->core, s, true, dXn, X, mean, rstd, ln_gamma, dres, dX,
+                    pg, pb, dgamma, dbeta, T, h));
   }
   return TPMLP_OK;
 }

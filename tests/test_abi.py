@@ -139,7 +139,7 @@ def _acfg(**kw):
 @pytest.mark.parametrize("kw,code", [
     (dict(heads=3), B.TPMLP_ERR_SHAPE),              # h % H
     (dict(heads=8), B.TPMLP_ERR_SHAPE),              # d = 32
-    (dict(hidden=384, heads=4), B.TPMLP_ERR_SHAPE),  # d = 96
+    (dict(hidden=320, heads=4), B.TPMLP_ERR_SHAPE),  # d = 80
     (dict(heads=4, shards=3), B.TPMLP_ERR_SHAPE),    # H % t
     (dict(seq_len=200), B.TPMLP_ERR_SHAPE),          # seq % 128
     (dict(shards=0), B.TPMLP_ERR_SHAPE),
@@ -157,6 +157,7 @@ def test_attn_create_rejects_bad_configs(lib, kw, code):
 @pytest.mark.parametrize("kw", [
     dict(hidden=128, heads=2, shards=2),     # h_t = 64, d = 64
     dict(hidden=5120, heads=40, shards=8),   # d = 128, 5 heads per shard
+    dict(hidden=3072, heads=32, shards=8),   # d = 96, the 8.3B layer
     dict(causal=0, use_layernorm=1, use_residual=1, max_tokens=0),
 ])
 def test_attn_create_accepts_valid_corners(lib, kw):

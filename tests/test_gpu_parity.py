@@ -55,6 +55,22 @@ def test_small_bf16_block_full(T, h, f, t, ln, bias, gelu):
     compare_full(got, oracle_full(inp, mode=gelu))
 
 
+# LayerNorm paths with gamma, beta away from (1, 0): the kernels that hold
+# the row in registers (h = 3072, forward and backward) and the generic
+# row-per-warp loops (h = 192, with lanes idle in the last round of vectors;
+# h = 4352 and 8448); the 8-column parameter sums on every case.
+@pytest.mark.parametrize("T,h,t,res", [(77, 192, 2, False), (301, 3072, 1, True),
+                                       (45, 4352, 2, False), (37, 8448, 1, True)])
+def test_layernorm_paths_full(T, h, t, res):
+    w = small(T, h, 256 * t, t, ln=True)
+    inp = W.make_inputs(w, seed=17, with_bias=True)
+    g = torch.Generator().manual_seed(19)
+    inp["gamma"] = 1 + 0.3 * torch.randn(h, generator=g)
+    inp["beta"] = 0.3 * torch.randn(h, generator=g)
+    got = run_cuda(w, inp, residual=res)
+    compare_full(got, oracle_full(inp, residual=res))
+
+
 RESIDUAL_CASES = [
     # T, h, f, t, ln, bias  (the pre-LN sub-block X + MLP(LN(X)) and the
     # plain block with a residual)
