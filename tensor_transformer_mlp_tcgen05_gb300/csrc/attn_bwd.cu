@@ -23,10 +23,13 @@
 // The Q kernel also forms delta for its 128 queries from its dO tile and the
 // forward's context rows (loaded into the last ring stage before the ring
 // first reaches it), and at its end writes sum_j P dP for the KV kernel.
-// The elementwise step writes dS (and P for KV) as bf16 into tensor memory,
-// over the score columns it has just read (each column-half warp inside its
-// own columns), where the output MMAs take them as A operands; their B
-// operands are the streamed tiles read M/N-major (the same bytes).
+// The elementwise step writes P and dS as bf16 into one of two tensor-memory
+// buffers of their own, where the output MMAs take them as A operands (their
+// B operands are the streamed tiles read M/N-major, the same bytes); S and
+// dP have one buffer, which the next step's score MMAs overwrite as soon as
+// the elementwise warps have loaded it, so the tensor pipe goes from one
+// step's gradient MMAs to the next step's score MMAs without waiting for
+// the former to finish.
 // Outputs leave as 32-row x 64-column bf16 chunks staged in the idle B ring
 // and stored by TMA (at d = 96 the last 32 columns of dK and dV, and dQ,
 // with plain 16-byte stores); at d = 128 each chunk is also summed over its
@@ -72,6 +75,10 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   constexpr uint32_t B_TX = 2 * B_TILE + (KV ? VEC_BYTES : 0);
   constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 64, false, false);
   constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, false, true);
+  // TMEM columns: S1 (S or S^T) and S2 (dP or dP^T) of the current step,
+  // 64 each; two buffers of the bf16 P and dS operands, 64 each (P then
+  // dS, 32 packed columns apiece); the two fp32 accumulators.
+  constexpr uint32_t TMEM_S1 = 0, TMEM_S2 = 64, TMEM_PDS = 128;
   constexpr uint32_t TMEM_OUT2 = 256;              // dK (KV) or dQ
   constexpr uint32_t TMEM_OUT1 = 256 + 64 * KB;    // dV (KV) or P K (Q)
   constexpr float INV_SQRT_D = D == 64   ? 0.125f
@@ -89,9 +96,14 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   const uint32_t sVec = ptx::smem_u32(vec_gen);    // [stage][lse2 | delta]
   uint64_t* bars = reinterpret_cast<uint64_t*>(vec_gen + VEC_TOTAL);
   const uint32_t b0 = ptx::smem_u32(bars);
+  // s_full: S and dP of the step are in TMEM (one buffer); s_read: the
+  // elementwise warps have loaded them, so the next step's MMAs may
+  // overwrite them; e_full / e_empty: P and dS of the step are in their
+  // TMEM buffer (two, by step parity) / its gradient MMAs have read them.
   const uint32_t a_full = b0, b_full = b0 + 8, b_empty = b_full + 8 * NB,
-                 s_full = b_empty + 8 * NB, e_full = s_full + 16,
-                 e_empty = e_full + 16, o_full = e_empty + 16,
+                 s_full = b_empty + 8 * NB, s_read = s_full + 8,
+                 e_full = s_full + 16, e_empty = e_full + 16,
+                 o_full = e_empty + 16,
                  done_bar = o_full + 8, ctx_full = done_bar + 8,
                  ctx_free = ctx_full + 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
@@ -121,8 +133,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       ptx::mbar_init(b_full + 8 * i, 1);
       ptx::mbar_init(b_empty + 8 * i, 1);
     }
+    ptx::mbar_init(s_full, 1);
+    ptx::mbar_init(s_read, SOFTMAX_WARPS);
     for (int i = 0; i < 2; ++i) {
-      ptx::mbar_init(s_full + 8 * i, 1);
       ptx::mbar_init(e_full + 8 * i, SOFTMAX_WARPS);
       ptx::mbar_init(e_empty + 8 * i, 1);
     }
@@ -195,12 +208,12 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       const uint64_t dBk = ptx::sdesc_sw128(sB, 16, 1024);          // K-major
       const uint64_t dBm = ptx::sdesc_sw128(sB, ATOM_BYTES, 1024);  // MN-major
       auto issue_s = [&](int n) -> bool {
-        const uint32_t st = n & 1, ph = (n >> 1) & 1;
         const uint32_t bs = n % NB, bph = (n / NB) & 1;
         if (!warp_wait(b_full + 8 * bs, bph, ctl, ROLE_MMA)) return false;
-        // buffer st still holds step n - 2's P / dS until its gradient MMAs
-        // are done
-        if (n >= 2 && !warp_wait(e_empty + 8 * st, ph ^ 1, ctl, ROLE_MMA))
+        // the score buffer still holds step n - 1's S and dP until the
+        // elementwise warps have loaded them
+        if (n >= 1 && !warp_wait(s_read, static_cast<uint32_t>(n - 1) & 1u,
+                                 ctl, ROLE_MMA))
           return false;
         ptx::tc_fence_after();
         const uint64_t b1 = desc_add(dBk, bs * 2 * B_TILE);
@@ -209,17 +222,17 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t ao = (k / 4) * KBLOCK_BYTES + (k % 4) * 32;
           const uint32_t bo = (k / 4) * ATOM_BYTES + (k % 4) * 32;
-          mma_ss_el(tmem + 64 * st, desc_add(dA1, ao), desc_add(b1, bo),
+          mma_ss_el(tmem + TMEM_S1, desc_add(dA1, ao), desc_add(b1, bo),
                     IDESC_S, k > 0 ? 1u : 0u);
         }
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t ao = (k / 4) * KBLOCK_BYTES + (k % 4) * 32;
           const uint32_t bo = (k / 4) * ATOM_BYTES + (k % 4) * 32;
-          mma_ss_el(tmem + 128 + 64 * st, desc_add(dA2, ao),
+          mma_ss_el(tmem + TMEM_S2, desc_add(dA2, ao),
                     desc_add(b2, bo), IDESC_S, k > 0 ? 1u : 0u);
         }
-        commit_el(s_full + 8 * st);
+        commit_el(s_full);
         return true;
       };
       auto issue_o = [&](int n) -> bool {
@@ -229,19 +242,19 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         ptx::tc_fence_after();
         const uint64_t b1 = desc_add(dBm, bs * 2 * B_TILE);
         const uint64_t b2 = desc_add(b1, B_TILE);
-        // A operands in TMEM: dS (in S2's buffer) and P (in S1's), 16 packed
-        // columns per 32-column half: k-step k at half k / 2, offset 8 (k % 2)
-        const uint32_t e2 = tmem + 128 + 64 * st, e1 = tmem + 64 * st;
+        // A operands in TMEM: P and dS of buffer st, 32 packed columns each
+        // (the column half hf of the elementwise warps wrote its 32 queries
+        // or keys at +16 hf): k-step k (16 of the step's 64) at +8 k
+        const uint32_t e1 = tmem + TMEM_PDS + 64 * st, e2 = e1 + 32;
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          mma_ts_el(tmem + TMEM_OUT2, e2 + (k / 2) * 32 + (k % 2) * 8,
-                    desc_add(b1, 2048 * k), IDESC_O,
-                    (n > 0 || k > 0) ? 1u : 0u);
+          mma_ts_el(tmem + TMEM_OUT2, e2 + 8 * k, desc_add(b1, 2048 * k),
+                    IDESC_O, (n > 0 || k > 0) ? 1u : 0u);
         // KV: dV += P^T dO.  Q: sum_j P_ij k_j += P K (same B as dQ), for
         // the row-sum correction of dQ below.
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          mma_ts_el(tmem + TMEM_OUT1, e1 + (k / 2) * 32 + (k % 2) * 8,
+          mma_ts_el(tmem + TMEM_OUT1, e1 + 8 * k,
                     desc_add(KV ? b2 : b1, 2048 * k), IDESC_O,
                     (n > 0 || k > 0) ? 1u : 0u);
         commit_el(b_empty + 8 * bs);
@@ -308,7 +321,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     for (int n = 0; alive && n < nsteps; ++n) {
       const uint32_t st = n & 1, ph = (n >> 1) & 1;
       const uint32_t bs = n % NB, bph = (n / NB) & 1;
-      if (!warp_wait(s_full + 8 * st, ph, ctl, ROLE_EPILOGUE) ||
+      if (!warp_wait(s_full, static_cast<uint32_t>(n) & 1u, ctl,
+                     ROLE_EPILOGUE) ||
           (KV && !warp_wait(b_full + 8 * bs, bph, ctl, ROLE_EPILOGUE))) {
         alive = false;
         break;
@@ -323,9 +337,14 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       const float* vl = vec + bs * (VEC_BYTES / 4) + 32 * hf;
       const float* vd = vl + 64;
       uint32_t s1[32], s2[32];
-      ptx::tmem_ld_32x32b_x32(tmem + lane_base + 64 * st + 32 * hf, s1);
-      ptx::tmem_ld_32x32b_x32(tmem + lane_base + 128 + 64 * st + 32 * hf, s2);
+      ptx::tmem_ld_32x32b_x32(tmem + lane_base + TMEM_S1 + 32 * hf, s1);
+      ptx::tmem_ld_32x32b_x32(tmem + lane_base + TMEM_S2 + 32 * hf, s2);
       ptx::tmem_ld_wait();
+      // S and dP are in registers: the next step's score MMAs may overwrite
+      // them while this step's P and dS are formed
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(s_read);
       uint32_t pw[16], dw[16];
       // column pairs with packed fp32x2 arithmetic:
       // P = 2^(S sl2 - L), dS = P (dP - delta) / sqrt(d)
@@ -351,9 +370,16 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         dw[i / 2] = pack_bf16x2(ds0, ds1);
         rsum += ds0 + ds1;
       }
-      // dS (and P) over this half's own score columns, packed two per column
-      tmem_st_32x32b_x16(tmem + lane_base + 128 + 64 * st + 32 * hf, dw);
-      tmem_st_32x32b_x16(tmem + lane_base + 64 * st + 32 * hf, pw);
+      // P and dS into buffer st, this half's 32 columns packed two per
+      // column, once step n - 2's gradient MMAs have read that buffer
+      if (n >= 2 && !warp_wait(e_empty + 8 * st, ph ^ 1u, ctl, ROLE_EPILOGUE)) {
+        alive = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      tmem_st_32x32b_x16(tmem + lane_base + TMEM_PDS + 64 * st + 16 * hf, pw);
+      tmem_st_32x32b_x16(tmem + lane_base + TMEM_PDS + 64 * st + 32 + 16 * hf,
+                         dw);
       tmem_st_wait();
       ptx::tc_fence_before();
       __syncwarp();
