@@ -130,6 +130,8 @@ int tp_attn_timing_get(tp_attn_handle* handle, int index, const char** name,
                        long long* launches, double* total_ms);
 int tp_attn_timing_reset(tp_attn_handle* handle);
 int tp_attn_set_wait_budget(tp_attn_handle* handle, unsigned long long ns);
+/* NVTX ranges around each launch, as tp_mlp_set_nvtx. */
+int tp_attn_set_nvtx(tp_attn_handle* handle, int enable);
 
 /* Offsets in bytes, inside a workspace laid out for (tokens, training), of
  * the saved QKV [T,3h] bf16, Ctx [T,h] bf16, log-sum-exp [H,T] fp32 and

@@ -69,6 +69,9 @@ extern "C" {
 #define TPMLP_ERR_CUDA       -5  /* a CUDA runtime/driver call failed        */
 #define TPMLP_ERR_TIMEOUT    -6  /* a bounded on-device wait gave up         */
 #define TPMLP_ERR_WORKSPACE  -7  /* workspace too small for this call        */
+#define TPMLP_ERR_CHECK      -8  /* a device-side check of a debug build
+                                    (TPMLP_CHECKS) failed; see
+                                    tp_mlp_last_detail for the site        */
 
 /* ---- configuration values --------------------------------------------- */
 #define TPMLP_BF16        0      /* bf16 storage, fp32 accumulate (tcgen05) */
@@ -346,6 +349,15 @@ int tp_mlp_set_dropout_seed(tp_mlp_handle* handle, unsigned long long seed,
  * (default 2e9).  A wait that exceeds it makes the kernel record
  * TPMLP_ERR_TIMEOUT in the status word and return early. */
 int tp_mlp_set_wait_budget(tp_mlp_handle* handle, unsigned long long ns);
+
+/* Enable (1) or disable (0, the default) an NVTX range around the enqueue
+ * of every kernel this handle launches, named for the kernel (the names
+ * tp_mlp_timing_get reports), so that a profiler recording NVTX (ncu
+ * --nvtx, Nsight Systems) can attribute each launch to its step of the
+ * block.  Without a tool attached the ranges cost a function call each.
+ * The SURVEY's tracing layer; the pages print no counterpart.
+ * TPMLP_ERR_ARG for a NULL handle or another value. */
+int tp_mlp_set_nvtx(tp_mlp_handle* handle, int enable);
 
 #ifdef __cplusplus
 }

@@ -14,7 +14,9 @@ import os
 
 from . import build as _build
 
-LIB_PATH = _build.LIB_PATH
+# TPMLP_LIB selects another build of the library (e.g. the debug variant
+# libtpmlp_checks.so); by default the in-tree libtpmlp.so.
+LIB_PATH = os.environ.get("TPMLP_LIB") or _build.LIB_PATH
 
 TPMLP_OK = 0
 TPMLP_ERR_ARG = -1
@@ -24,6 +26,7 @@ TPMLP_ERR_ARCH = -4
 TPMLP_ERR_CUDA = -5
 TPMLP_ERR_TIMEOUT = -6
 TPMLP_ERR_WORKSPACE = -7
+TPMLP_ERR_CHECK = -8
 
 TPMLP_BF16 = 0
 TPMLP_FP32 = 1
@@ -36,7 +39,7 @@ EXPORTED = (
     "tp_mlp_forward", "tp_mlp_backward", "tp_mlp_check",
     "tp_mlp_status_string", "tp_mlp_last_detail", "tp_mlp_launch_count",
     "tp_mlp_set_timing", "tp_mlp_timing_get", "tp_mlp_timing_reset",
-    "tp_mlp_set_wait_budget", "tp_mlp_bias_grad_noalloc",
+    "tp_mlp_set_wait_budget", "tp_mlp_set_nvtx", "tp_mlp_bias_grad_noalloc",
     "tp_mlp_set_dropout_seed",
     "tp_mlp_fp8_weights_bytes", "tp_mlp_fp8_pack_weights",
     "tp_mlp_fp8_workspace_bytes", "tp_mlp_forward_fp8", "tp_mlp_fp8_offset",
@@ -47,7 +50,7 @@ EXPORTED = (
     "tp_attn_create", "tp_attn_destroy", "tp_attn_workspace_bytes",
     "tp_attn_forward", "tp_attn_backward", "tp_attn_check",
     "tp_attn_launch_count", "tp_attn_set_timing", "tp_attn_timing_get",
-    "tp_attn_timing_reset", "tp_attn_set_wait_budget",
+    "tp_attn_timing_reset", "tp_attn_set_wait_budget", "tp_attn_set_nvtx",
     "tp_attn_workspace_offset",
 )
 
@@ -148,6 +151,8 @@ def lib(path: str | None = None) -> ctypes.CDLL:
     L.tp_mlp_timing_reset.restype = _i
     L.tp_mlp_set_wait_budget.argtypes = [_vp, ctypes.c_ulonglong]
     L.tp_mlp_set_wait_budget.restype = _i
+    L.tp_mlp_set_nvtx.argtypes = [_vp, _i]
+    L.tp_mlp_set_nvtx.restype = _i
     L.tp_mlp_set_dropout_seed.argtypes = [_vp, ctypes.c_ulonglong,
                                           ctypes.c_ulonglong]
     L.tp_mlp_set_dropout_seed.restype = _i
@@ -203,6 +208,8 @@ def lib(path: str | None = None) -> ctypes.CDLL:
     L.tp_attn_timing_get.restype = _i
     L.tp_attn_timing_reset.argtypes = [_vp]
     L.tp_attn_timing_reset.restype = _i
+    L.tp_attn_set_nvtx.argtypes = [_vp, _i]
+    L.tp_attn_set_nvtx.restype = _i
     L.tp_attn_set_wait_budget.argtypes = [_vp, ctypes.c_ulonglong]
     L.tp_attn_set_wait_budget.restype = _i
     if path is None:
@@ -316,6 +323,10 @@ def tp_mlp_set_dropout_seed(handle, seed: int, offset: int = 0) -> None:
 
 def tp_mlp_set_wait_budget(handle, ns: int) -> None:
     _check(lib().tp_mlp_set_wait_budget(handle, ns), "tp_mlp_set_wait_budget")
+
+
+def tp_mlp_set_nvtx(handle, enable: bool) -> None:
+    _check(lib().tp_mlp_set_nvtx(handle, 1 if enable else 0), "tp_mlp_set_nvtx")
 
 
 def tp_mlp_bias_grad_noalloc(tokens, cols, dtype, grad, dbias, stream=None):
@@ -492,6 +503,10 @@ def tp_attn_timing_get(handle):
 
 def tp_attn_timing_reset(handle) -> None:
     _check(lib().tp_attn_timing_reset(handle), "tp_attn_timing_reset")
+
+
+def tp_attn_set_nvtx(handle, enable: bool) -> None:
+    _check(lib().tp_attn_set_nvtx(handle, 1 if enable else 0), "tp_attn_set_nvtx")
 
 
 def tp_attn_set_wait_budget(handle, ns: int) -> None:

@@ -6,6 +6,12 @@ linked statically; the driver API is reached through the runtime's entry-point
 lookup, so the library does not link libcuda).  Object files go to
 ``_build/`` at the repository root.  A rebuild is skipped when the library is
 newer than every source and header.
+
+``build(checks=True)`` makes the debug variant ``libtpmlp_checks.so`` (objects
+in ``_build/checks``) with ``-DTPMLP_CHECKS``: device-side checks of TMA
+coordinates and store indices that report ``TPMLP_ERR_CHECK`` instead of
+letting a bad access happen.  Load it by setting ``TPMLP_LIB`` to its path
+before the binding is imported.
 """
 from __future__ import annotations
 
@@ -21,6 +27,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG, "libtpmlp.so")
+CHECKS_LIB_PATH = os.path.join(PKG, "libtpmlp_checks.so")
 
 SOURCES = ["gemm_tc2.cu", "rowops.cu", "simt.cu",
            "tp_mlp_host.cu", "noalloc.cu", "attn_fwd.cu", "attn_bwd.cu",
@@ -46,24 +53,29 @@ def _inputs():
     return files
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+def up_to_date(lib_path: str = LIB_PATH) -> bool:
+    if not os.path.exists(lib_path):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(lib_path)
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
 def build(force: bool = False, verbose: bool = False,
-          ptxas_info: bool = False) -> str:
-    """Compile and link; returns the library path.  Raises on failure."""
-    if not force and up_to_date():
-        return LIB_PATH
+          ptxas_info: bool = False, checks: bool = False) -> str:
+    """Compile and link; returns the library path.  Raises on failure.
+    checks=True builds the debug variant (see the module docstring)."""
+    lib_path = CHECKS_LIB_PATH if checks else LIB_PATH
+    if not force and up_to_date(lib_path):
+        return lib_path
     nvcc = nvcc_path()
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    obj_dir = os.path.join(BUILD_DIR, "checks") if checks else BUILD_DIR
+    os.makedirs(obj_dir, exist_ok=True)
     extra = ["-Xptxas", "-v"] if ptxas_info else []
+    if checks:
+        extra.append("-DTPMLP_CHECKS")
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
+        obj = os.path.join(obj_dir, os.path.splitext(src)[0] + ".o")
         cmd = [nvcc, *ARCH, *CFLAGS, *extra, "-c", os.path.join(CSRC, src),
                "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -77,15 +89,16 @@ def build(force: bool = False, verbose: bool = False,
         for obj, log in results:
             if log.strip():
                 print(f"--- {os.path.basename(obj)}\n{log}", file=sys.stderr)
-    tmp = LIB_PATH + ".tmp"
+    tmp = lib_path + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results]]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose=True,
-                ptxas_info="--ptxas-info" in sys.argv))
+                ptxas_info="--ptxas-info" in sys.argv,
+                checks="--checks" in sys.argv))

@@ -159,6 +159,14 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ---------------------------------------------------- producer --
+      // (debug builds: the copies' innermost coordinates on a 16-byte
+      // boundary, the 1-D copies of lse2 / delta on 16-byte addresses)
+      if (TPMLP_CHECK(cA1 % 8 == 0 && cA2 % 8 == 0 && cB1 % 8 == 0 &&
+                          cB2 % 8 == 0 && (head * D) % 8 == 0 &&
+                          (static_cast<long long>(head) * a.ld_stat +
+                           seq * a.seq_len) % 4 == 0,
+                      a.status, abort_flag, SITE_ATTN_BWD_LOAD))
+      {
       ptx::mbar_arrive_expect_tx(a_full, 2 * A_TILE);
 #pragma unroll
       for (int kk = 0; kk < KB; ++kk) {
@@ -196,6 +204,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
           ptx::bulk_load_1d(sVec + bs * VEC_BYTES, a.lse + off, 256, bf);
           ptx::bulk_load_1d(sVec + bs * VEC_BYTES + 256, a.delta + off, 256, bf);
         }
+      }
       }
     }
     __syncwarp();
@@ -446,15 +455,22 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         if constexpr (D % 64 != 0) {
           // the last 32 columns (a 64-column chunk would reach into the next
           // head's columns): each thread its own row, 64 bytes
+          const bool st_ok = TPMLP_CHECK(
+              __all_sync(0xffffffffu,
+                         (reinterpret_cast<uintptr_t>(
+                              a.dqkv + static_cast<size_t>(row0 + r) * a.ld_qkv +
+                              col + 64 * (D / 64)) & 15u) == 0),
+              a.status, abort_flag, SITE_ATTN_BWD_STORE);
           uint32_t rr[32];
           ptx::tmem_ld_32x32b_x32(src + 64 * (D / 64), rr);
           ptx::tmem_ld_wait();
           float v[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(rr[i]);
-          store_bf16x32(a.dqkv + static_cast<size_t>(row0 + r) * a.ld_qkv + col +
-                            64 * (D / 64),
-                        v);
+          if (st_ok)
+            store_bf16x32(a.dqkv + static_cast<size_t>(row0 + r) * a.ld_qkv +
+                              col + 64 * (D / 64),
+                          v);
         }
         st.drain(lane);
       } else if constexpr (D == 128) {

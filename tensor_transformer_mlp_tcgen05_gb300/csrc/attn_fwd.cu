@@ -118,7 +118,12 @@ __global__ void __launch_bounds__(FWD_THREADS, 2)
     if (lane == 0) {
       // ---------------------------------------------------- producer --
       // One stage each for K and V: K(kb) may overwrite K(kb - 1) once
-      // S(kb - 1) is done, V(kb) once P V(kb - 1) is done.
+      // S(kb - 1) is done, V(kb) once P V(kb - 1) is done.  (Debug builds:
+      // the head's column offsets, the copies' innermost coordinates, on a
+      // 16-byte boundary.)
+      if (TPMLP_CHECK(hc.q % 8 == 0 && hc.k % 8 == 0 && hc.v % 8 == 0,
+                      a.status, abort_flag, SITE_ATTN_FWD_LOAD))
+      {
       ptx::mbar_arrive_expect_tx(q_full, QK_TILE);
 #pragma unroll
       for (int kk = 0; kk < KB; ++kk)
@@ -140,6 +145,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 2)
           for (int at = 0; at < KB; ++at)
             ptx::tma_load_2d(sV + (h2 * KB + at) * ATOM_BYTES, &tmV, v_full,
                              hc.v + 64 * at, key0 + 64 * h2);
+      }
       }
     }
     __syncwarp();
@@ -334,6 +340,11 @@ __global__ void __launch_bounds__(FWD_THREADS, 2)
       // this warp's D / 2 context columns, 16 at a time (32 bytes a row)
       __nv_bfloat16* out = a.ctx + static_cast<size_t>(row0 + r) * a.ld_ctx +
                            head * D + hf * (D / 2);
+      // (warp-uniform: the loop's TMEM loads are warp-collective)
+      if (TPMLP_CHECK(__all_sync(0xffffffffu,
+                                 (reinterpret_cast<uintptr_t>(out) & 15u) == 0 &&
+                                     row0 + r < a.ld_stat),
+                      a.status, abort_flag, SITE_ATTN_FWD_STORE))
 #pragma unroll 1
       for (int j = 0; j < D / 32; ++j) {
         uint32_t ov[16];

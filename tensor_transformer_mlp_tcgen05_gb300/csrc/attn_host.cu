@@ -417,6 +417,12 @@ int tp_attn_timing_reset(tp_attn_handle* H) {
   return TPMLP_OK;
 }
 
+int tp_attn_set_nvtx(tp_attn_handle* handle, int enable) {
+  if (handle == nullptr || (enable != 0 && enable != 1)) return TPMLP_ERR_ARG;
+  handle->core.nvtx = enable != 0;
+  return TPMLP_OK;
+}
+
 int tp_attn_set_wait_budget(tp_attn_handle* handle, unsigned long long ns) {
   if (handle == nullptr) return TPMLP_ERR_ARG;
   handle->core.budget_ns = ns;

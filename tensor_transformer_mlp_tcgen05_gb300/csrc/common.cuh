@@ -75,8 +75,42 @@ struct GemmArgs {
   int tail, pieces, nslots;
 };
 
-// Roles recorded in status[1] when a bounded wait gives up.
-enum WaitRole : int { ROLE_PRODUCER = 1, ROLE_MMA = 2, ROLE_EPILOGUE = 3 };
+// Roles recorded in status[1] when a bounded wait gives up (ROLE_CHECK: a
+// debug-build device check failed; status[3] then names the site).
+enum WaitRole : int {
+  ROLE_PRODUCER = 1, ROLE_MMA = 2, ROLE_EPILOGUE = 3, ROLE_CHECK = 4
+};
+
+// Debug builds (-DTPMLP_CHECKS) verify, before each TMA copy and each
+// computed store, the conditions the hardware does not check itself (the
+// innermost tile coordinate of a tensor copy on a 16-byte boundary, index
+// ranges of plain stores).  A failed check records TPMLP_ERR_CHECK and its
+// site in the status word, raises the kernel's abort flag (the other roles
+// stop at their next bounded wait) and the access is skipped.  Release
+// builds compile the checks out.
+enum CheckSite : int {
+  SITE_GEMM_LOAD_A = 1, SITE_GEMM_LOAD_B = 2, SITE_GEMM_STORE = 3,
+  SITE_GEMM_COLSUM = 4, SITE_ATTN_FWD_LOAD = 5, SITE_ATTN_FWD_STORE = 6,
+  SITE_ATTN_BWD_LOAD = 7, SITE_ATTN_BWD_VEC = 8, SITE_ATTN_BWD_STORE = 9
+};
+#ifdef TPMLP_CHECKS
+__device__ __forceinline__ bool device_check(bool ok, int* status,
+                                             int* abort_flag, int site) {
+  if (ok) return true;
+  if (atomicCAS(status, 0, TPMLP_ERR_CHECK) == 0) {
+    status[1] = ROLE_CHECK;
+    status[2] = static_cast<int>(blockIdx.x);
+    status[3] = site;
+  }
+  *reinterpret_cast<volatile int*>(abort_flag) = 1;
+  __threadfence();
+  return false;
+}
+#define TPMLP_CHECK(ok, status, abort_flag, site) \
+  device_check((ok), (status), (abort_flag), (site))
+#else
+#define TPMLP_CHECK(ok, status, abort_flag, site) ((void)sizeof(ok), true)
+#endif
 
 // GeLU and its derivative in fp32.  Exact form: GeLU(x) = x Phi(x) with
 // Phi the standard normal CDF, GeLU'(x) = Phi(x) + x phi(x).  Tanh form

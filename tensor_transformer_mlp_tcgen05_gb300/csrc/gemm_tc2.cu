@@ -271,10 +271,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             alive = false;
             break;
           }
+          const int k0 = kb * (F8 ? 2 * BK : BK);  // 128 bytes of K either way
+          // the innermost coordinate of each copy on a 16-byte boundary
+          constexpr int XAL = F8 ? 16 : 8;
+          if (!TPMLP_CHECK((A_MN ? m0 : k0) % XAL == 0, ctl.status, abort_flag,
+                           SITE_GEMM_LOAD_A) ||
+              !TPMLP_CHECK((B_MN ? n0 : k0) % XAL == 0, ctl.status, abort_flag,
+                           SITE_GEMM_LOAD_B)) {
+            alive = false;
+            break;
+          }
           if (leader) ptx::mbar_arrive_expect_tx(full0 + 8u * stage,
                                                  PAIR_STAGE_BYTES);
           const uint32_t fb = lead_full0 + 8u * stage;
-          const int k0 = kb * (F8 ? 2 * BK : BK);  // 128 bytes of K either way
           const uint32_t da = s_a + stage * A_STAGE_BYTES;
           const uint32_t db = s_b + stage * B_STAGE_BYTES;
           if constexpr (!A_MN) {
@@ -587,7 +596,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
               const int c0 = col_base + j * 64;
-              if (c0 < args.N) {
+              if (c0 < args.N &&
+                  TPMLP_CHECK(c0 + 64 <= args.ld_colsum && c0 % 8 == 0,
+                              ctl.status, abort_flag, SITE_GEMM_COLSUM)) {
                 const float2 cs = chunk_colsum_bf16(cbuf[j], lane);
                 *reinterpret_cast<float2*>(
                     args.colsum + static_cast<size_t>(row0 / 32) * args.ld_colsum +

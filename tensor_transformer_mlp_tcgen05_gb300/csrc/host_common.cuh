@@ -2,6 +2,7 @@
 // device checks, TMA tensor-map encoding, per-launch timing and the GEMM /
 // column-sum launch wrappers.  Header-only (inline), one copy per program.
 #pragma once
+#include <nvtx3/nvToolsExt.h>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -25,6 +26,7 @@ struct HandleCore {
   unsigned long long budget_ns = 2000000000ull;
   long long launches = 0;
   bool timing = false;
+  bool nvtx = false;  // an NVTX range, named for the kernel, around each launch
   struct Pending {
     int stat;
     cudaEvent_t a, b;
@@ -237,7 +239,12 @@ inline int run(HandleCore* H, const char* name, cudaStream_t s, F&& launch) {
     b = take_event(H);
     if (a && b) cudaEventRecord(a, s);
   }
+  // NVTX ranges mark the host-side enqueue of each kernel; a profiler that
+  // records them (ncu --nvtx, Nsight Systems) attributes the launch to the
+  // range.  Without a tool attached the calls return at once.
+  if (H->nvtx) nvtxRangePushA(name);
   const cudaError_t e = launch();
+  if (H->nvtx) nvtxRangePop();
   H->launches++;
   if (H->timing && a && b) {
     cudaEventRecord(b, s);
@@ -361,15 +368,22 @@ inline int check_status(void* status, cudaStream_t s) {
     return TPMLP_ERR_CUDA;
   }
   if (st[0] != 0) {
-    std::snprintf(g_detail, sizeof(g_detail),
-                  "device status %d (role %d, block %d)", st[0], st[1], st[2]);
+    if (st[0] == TPMLP_ERR_CHECK) {
+      std::snprintf(g_detail, sizeof(g_detail),
+                    "device check failed at site %d (block %d)", st[3], st[2]);
+    } else {
+      std::snprintf(g_detail, sizeof(g_detail),
+                    "device status %d (role %d, block %d)", st[0], st[1], st[2]);
+    }
     e = cudaMemsetAsync(status, 0, 16, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) {
       set_detail("clearing the status word", e);
       return TPMLP_ERR_CUDA;
     }
-    return st[0] == TPMLP_ERR_TIMEOUT ? TPMLP_ERR_TIMEOUT : TPMLP_ERR_CUDA;
+    return (st[0] == TPMLP_ERR_TIMEOUT || st[0] == TPMLP_ERR_CHECK)
+               ? st[0]
+               : TPMLP_ERR_CUDA;
   }
   return TPMLP_OK;
 }

@@ -912,6 +912,7 @@ const char* tp_mlp_status_string(int status) {
     case TPMLP_ERR_CUDA: return "CUDA error";
     case TPMLP_ERR_TIMEOUT: return "bounded device wait timed out";
     case TPMLP_ERR_WORKSPACE: return "workspace too small";
+    case TPMLP_ERR_CHECK: return "device-side check failed (debug build)";
     default: return "unknown status";
   }
 }
@@ -952,6 +953,12 @@ int tp_mlp_set_dropout_seed(tp_mlp_handle* handle, unsigned long long seed,
 int tp_mlp_set_wait_budget(tp_mlp_handle* handle, unsigned long long ns) {
   if (handle == nullptr) return TPMLP_ERR_ARG;
   handle->core.budget_ns = ns;
+  return TPMLP_OK;
+}
+
+int tp_mlp_set_nvtx(tp_mlp_handle* handle, int enable) {
+  if (handle == nullptr || (enable != 0 && enable != 1)) return TPMLP_ERR_ARG;
+  handle->core.nvtx = enable != 0;
   return TPMLP_OK;
 }
 

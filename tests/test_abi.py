@@ -236,3 +236,17 @@ def test_gelu_probe_rejects_bad_arguments(lib):
                                  None) == B.TPMLP_ERR_ARG
     assert lib.tp_mlp_probe_gelu(None, None, None, 0, B.TPMLP_GELU_ERF,
                                  None) == B.TPMLP_OK
+
+
+def test_nvtx_switch_validates_arguments(lib):
+    assert lib.tp_mlp_set_nvtx(None, 1) == B.TPMLP_ERR_ARG
+    assert lib.tp_attn_set_nvtx(None, 0) == B.TPMLP_ERR_ARG
+    h = ctypes.c_void_p()
+    assert lib.tp_mlp_create(ctypes.byref(B.tp_mlp_config(
+        hidden=128, ffn=256, shards=2, max_tokens=64, dtype=B.TPMLP_BF16,
+        use_layernorm=0, ln_eps=1e-5, gelu_mode=B.TPMLP_GELU_ERF,
+        use_residual=0, dropout_p=0.0)), ctypes.byref(h)) == B.TPMLP_OK
+    assert lib.tp_mlp_set_nvtx(h, 2) == B.TPMLP_ERR_ARG
+    assert lib.tp_mlp_set_nvtx(h, 1) == B.TPMLP_OK
+    assert lib.tp_mlp_set_nvtx(h, 0) == B.TPMLP_OK
+    assert lib.tp_mlp_destroy(h) == B.TPMLP_OK

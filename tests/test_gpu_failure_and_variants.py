@@ -69,3 +69,27 @@ def test_attention_wait_timeout_is_reported_and_context_survives():
                      w.seq, w.shards, bqkv=f64(inp["bqkv"]), bo=f64(inp["bo"]))
     assert_close("attention Z after timeout", Z.cpu(), ref["Z"])
     m.close()
+
+
+def test_nvtx_ranges_change_nothing():
+    """NVTX ranges around the launches (no tool attached): the same kernels,
+    the same launch count and bitwise the same results."""
+    w = W.Workload("nvtx", 300, 256, 1024, 4, "bf16", True, True)
+    inp = W.make_inputs(w, seed=33, with_bias=True)
+    d = {k: to_dev(v) for k, v in inp.items()}
+    outs = []
+    for enable in (False, True):
+        m = TensorParallelMLP(w.hidden, w.ffn, w.shards, w.tokens,
+                              layernorm=True)
+        B.tp_mlp_set_nvtx(m.handle, enable)
+        Z = m.forward(d["X"], d["A"], d["B"], d["b1"], d["b2"], d["gamma"],
+                      d["beta"])
+        g = m.backward(d["dZ"], d["X"], d["A"], d["B"], d["gamma"])
+        assert m.check() == B.TPMLP_OK
+        g["Z"] = Z
+        outs.append(({k: v.cpu() for k, v in g.items()},
+                     B.tp_mlp_launch_count(m.handle)))
+        m.close()
+    assert outs[0][1] == outs[1][1]
+    for k in outs[0][0]:
+        assert torch.equal(outs[0][0][k], outs[1][0][k]), k
