@@ -359,17 +359,19 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       // P = 2^(S sl2 - L), dS = P (dP - delta) / sqrt(d)
       const uint64_t scale = f2_pack(sl2, sl2);
       const uint64_t inv_sqrt_d = f2_pack(INV_SQRT_D, INV_SQRT_D);
-#pragma unroll
-      for (int i = 0; i < 32; i += 2) {
-        const float L0 = KV ? vl[i] : lse_r, L1 = KV ? vl[i + 1] : lse_r;
-        const float D0 = KV ? vd[i] : delta_r, D1 = KV ? vd[i + 1] : delta_r;
+      // the causal mask touches no column of this warp's rows: no selects
+      const bool unmasked = __all_sync(0xffffffffu, lo <= 0 && hi >= 31);
+      auto pair = [&](int i, float L0, float L1, float D0, float D1,
+                      bool masked) {
         float a0, a1;
         f2_unpack(f2_fma(f2_pack(__uint_as_float(s1[i]), __uint_as_float(s1[i + 1])),
                          scale, f2_pack(-L0, -L1)),
                   a0, a1);
         float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
-        p0 = (i >= lo && i <= hi) ? p0 : 0.f;
-        p1 = (i + 1 >= lo && i + 1 <= hi) ? p1 : 0.f;
+        if (masked) {
+          p0 = (i >= lo && i <= hi) ? p0 : 0.f;
+          p1 = (i + 1 >= lo && i + 1 <= hi) ? p1 : 0.f;
+        }
         const uint64_t dp = f2_add(
             f2_pack(__uint_as_float(s2[i]), __uint_as_float(s2[i + 1])),
             f2_pack(-D0, -D1));
@@ -378,6 +380,26 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         pw[i / 2] = pack_bf16x2(p0, p1);
         dw[i / 2] = pack_bf16x2(ds0, ds1);
         rsum += ds0 + ds1;
+      };
+      auto columns = [&](bool masked) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          if constexpr (KV) {
+            // the streamed queries' lse2 and delta, four columns per load
+            const float4 l4 = *reinterpret_cast<const float4*>(vl + i);
+            const float4 d4 = *reinterpret_cast<const float4*>(vd + i);
+            pair(i, l4.x, l4.y, d4.x, d4.y, masked);
+            pair(i + 2, l4.z, l4.w, d4.z, d4.w, masked);
+          } else {
+            pair(i, lse_r, lse_r, delta_r, delta_r, masked);
+            pair(i + 2, lse_r, lse_r, delta_r, delta_r, masked);
+          }
+        }
+      };
+      if (unmasked) {
+        columns(false);
+      } else {
+        columns(true);
       }
       // P and dS into buffer st, this half's 32 columns packed two per
       // column, once step n - 2's gradient MMAs have read that buffer
