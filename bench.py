@@ -337,7 +337,8 @@ def run_ours(args, w, rank, world, local_rank):
     inp = W.make_inputs(w, seed=0)
     d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
     m = TensorParallelMLP(w.hidden, w.ffn, w.shards, w.tokens, dtype=w.dtype,
-                          layernorm=w.layernorm, residual=args.residual)
+                          layernorm=w.layernorm, residual=args.residual,
+                          ln_prologue=not args.ln_standalone)
     stream = torch.cuda.current_stream()
     T = w.tokens
     Z = torch.empty((T, w.hidden), dtype=w.torch_dtype, device=dev)
@@ -456,6 +457,7 @@ def run_ours(args, w, rank, world, local_rank):
     roof = None
     gemm_flops = {
         "gemm1_gelu": 2.0 * w.tokens * w.hidden * w.ffn,
+        "gemm1_ln_gelu": 2.0 * w.tokens * w.hidden * w.ffn,
         "gemm2_shardsum": 2.0 * w.tokens * w.hidden * w.ffn,
         "gemm_dh_gelu_bwd": 2.0 * w.tokens * w.hidden * w.ffn,
         "gemm_wgrad_dB": 2.0 * w.tokens * w.hidden * w.ffn,
@@ -487,6 +489,7 @@ def run_ours(args, w, rank, world, local_rank):
         "config": {"workload": w.name, "tokens": w.tokens, "batch": w.batch,
                    "seq": w.seq, "hidden": w.hidden, "ffn": w.ffn,
                    "shards": w.shards, "layernorm": w.layernorm,
+                   "ln_prologue": bool(w.layernorm and not args.ln_standalone),
                    "residual": bool(args.residual),
                    "pass": "fwd+bwd" if w.backward else "fwd",
                    "parallelism": f"replicas{world}" if world > 1 else "single",
@@ -1162,6 +1165,10 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--residual", action="store_true",
                     help="time the residual sub-block X + MLP(LN(X))")
+    ap.add_argument("--ln-standalone", action="store_true",
+                    help="bf16 MLP with LayerNorm: run the LayerNorm as its "
+                         "own launch before GEMM1 instead of GEMM1's fused "
+                         "prologue")
     ap.add_argument("--fp8", action="store_true",
                     help="time the FP8 (E4M3) forward of an MLP workload")
     ap.add_argument("--train", action="store_true",

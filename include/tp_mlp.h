@@ -355,9 +355,26 @@ int tp_mlp_set_wait_budget(tp_mlp_handle* handle, unsigned long long ns);
  * tp_mlp_timing_get reports), so that a profiler recording NVTX (ncu
  * --nvtx, Nsight Systems) can attribute each launch to its step of the
  * block.  Without a tool attached the ranges cost a function call each.
- * The SURVEY's tracing layer; the pages print no counterpart.
+ * Tracing only: the pages describe no profiling hooks.
  * TPMLP_ERR_ARG for a NULL handle or another value. */
 int tp_mlp_set_nvtx(tp_mlp_handle* handle, int enable);
+
+/* Enable (1, the default) or disable (0) the fused pre-LayerNorm prologue
+ * of the bf16 forward (pre-LN placement: Megatron-LM explainer, "Fixing
+ * BERT: reordering layer normalisation for scaling").  Enabled, with
+ * use_layernorm, dtype TPMLP_BF16 and hidden = 256 v for v <= 24 (hidden
+ * <= 6144), the LayerNorm runs inside the first GEMM's launch: that
+ * kernel's epilogue warps normalise the token rows (one row per warp at a
+ * time, the row held in registers: coalesced 16-byte loads, warp-shuffle
+ * reductions) before their first tile, and each 128-row block of the GEMM's
+ * A operand is loaded as soon as its rows are written, so the LayerNorm
+ * overlaps the GEMM instead of running as its own launch.  Disabled, or for
+ * other shapes, a stand-alone LayerNorm kernel runs first.  Both compute
+ * the same bits (one device function normalises a row on either path):
+ * Xn, mean, rstd and every output are identical.  Takes effect from the
+ * next tp_mlp_forward call.  TPMLP_ERR_ARG for a NULL handle or another
+ * value. */
+int tp_mlp_set_ln_prologue(tp_mlp_handle* handle, int enable);
 
 #ifdef __cplusplus
 }

@@ -39,7 +39,8 @@ EXPORTED = (
     "tp_mlp_forward", "tp_mlp_backward", "tp_mlp_check",
     "tp_mlp_status_string", "tp_mlp_last_detail", "tp_mlp_launch_count",
     "tp_mlp_set_timing", "tp_mlp_timing_get", "tp_mlp_timing_reset",
-    "tp_mlp_set_wait_budget", "tp_mlp_set_nvtx", "tp_mlp_bias_grad_noalloc",
+    "tp_mlp_set_wait_budget", "tp_mlp_set_nvtx", "tp_mlp_set_ln_prologue",
+    "tp_mlp_bias_grad_noalloc",
     "tp_mlp_set_dropout_seed",
     "tp_mlp_fp8_weights_bytes", "tp_mlp_fp8_pack_weights",
     "tp_mlp_fp8_workspace_bytes", "tp_mlp_forward_fp8", "tp_mlp_fp8_offset",
@@ -153,6 +154,8 @@ def lib(path: str | None = None) -> ctypes.CDLL:
     L.tp_mlp_set_wait_budget.restype = _i
     L.tp_mlp_set_nvtx.argtypes = [_vp, _i]
     L.tp_mlp_set_nvtx.restype = _i
+    L.tp_mlp_set_ln_prologue.argtypes = [_vp, _i]
+    L.tp_mlp_set_ln_prologue.restype = _i
     L.tp_mlp_set_dropout_seed.argtypes = [_vp, ctypes.c_ulonglong,
                                           ctypes.c_ulonglong]
     L.tp_mlp_set_dropout_seed.restype = _i
@@ -327,6 +330,11 @@ def tp_mlp_set_wait_budget(handle, ns: int) -> None:
 
 def tp_mlp_set_nvtx(handle, enable: bool) -> None:
     _check(lib().tp_mlp_set_nvtx(handle, 1 if enable else 0), "tp_mlp_set_nvtx")
+
+
+def tp_mlp_set_ln_prologue(handle, enable: bool) -> None:
+    _check(lib().tp_mlp_set_ln_prologue(handle, 1 if enable else 0),
+           "tp_mlp_set_ln_prologue")
 
 
 def tp_mlp_bias_grad_noalloc(tokens, cols, dtype, grad, dbias, stream=None):

@@ -23,6 +23,10 @@ enum Epilogue : int {
   EPI_BIAS_BF16 = 4,
 };
 
+// Rows of LayerNorm held in registers by one warp (ln_row.cuh): h = 256 vpl
+// with vpl <= LN_VMAX, i.e. h <= 6144 (96 registers of raw row per lane).
+constexpr int LN_VMAX = 24;
+
 // Arguments of one GEMM launch: D[M,N] = sum over K of Aop[m,k] * Bop[k,n],
 // K split into `num_seg` equal segments of `kb_per_seg` k-blocks; each
 // segment accumulates into a fresh accumulator (used for the shard sum).
@@ -73,12 +77,29 @@ struct GemmArgs {
   float* part;
   long long part_bytes;
   int tail, pieces, nslots;
+  // Fused LayerNorm prologue (EPI_GELU_FWD with K-major bf16 A; ln_x null =
+  // off).  The A tensor map points at ln_xn.  The epilogue warps of every
+  // CTA first normalise rows of ln_x [M, K] (K = 256 vpl, vpl <= LN_VMAX)
+  // into ln_xn and write ln_mean / ln_rstd, claiming one or two rows at a
+  // time from ln_sync[0]; after a claim's rows are written they add their
+  // count to ln_sync[1 + r / 128].  The producer loads a 128-row A block only
+  // once its count is complete.  ln_sync (1 + ceil(M / 128) words) must be
+  // zero at launch.
+  const __nv_bfloat16* ln_x;
+  const float* ln_gamma;
+  const float* ln_beta;
+  __nv_bfloat16* ln_xn;
+  float* ln_mean;
+  float* ln_rstd;
+  float ln_eps;
+  unsigned int* ln_sync;
 };
 
 // Roles recorded in status[1] when a bounded wait gives up (ROLE_CHECK: a
 // debug-build device check failed; status[3] then names the site).
 enum WaitRole : int {
-  ROLE_PRODUCER = 1, ROLE_MMA = 2, ROLE_EPILOGUE = 3, ROLE_CHECK = 4
+  ROLE_PRODUCER = 1, ROLE_MMA = 2, ROLE_EPILOGUE = 3, ROLE_CHECK = 4,
+  ROLE_LN_READY = 5   // the producer waiting for fused-LayerNorm rows
 };
 
 // Debug builds (-DTPMLP_CHECKS) verify, before each TMA copy and each
@@ -91,7 +112,8 @@ enum WaitRole : int {
 enum CheckSite : int {
   SITE_GEMM_LOAD_A = 1, SITE_GEMM_LOAD_B = 2, SITE_GEMM_STORE = 3,
   SITE_GEMM_COLSUM = 4, SITE_ATTN_FWD_LOAD = 5, SITE_ATTN_FWD_STORE = 6,
-  SITE_ATTN_BWD_LOAD = 7, SITE_ATTN_BWD_VEC = 8, SITE_ATTN_BWD_STORE = 9
+  SITE_ATTN_BWD_LOAD = 7, SITE_ATTN_BWD_VEC = 8, SITE_ATTN_BWD_STORE = 9,
+  SITE_GEMM_LN = 10
 };
 #ifdef TPMLP_CHECKS
 __device__ __forceinline__ bool device_check(bool ok, int* status,

@@ -2,6 +2,7 @@
 // waits, tile rasterisation and the fused epilogue stores.
 #pragma once
 #include "internal.h"
+#include "ln_row.cuh"
 #include "ptx.cuh"
 
 namespace tpmlp {
@@ -31,6 +32,101 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
       }
       __threadfence();
       return false;
+    }
+  }
+}
+
+// Bounded wait until the counter reaches `target` (gpu-scope acquire), then
+// a proxy fence so that this thread's later TMA reads of global memory see
+// what the counted writers released.  Same time budget and abort protocol
+// as wait_bounded.
+__device__ __forceinline__ bool wait_count(const unsigned int* count,
+                                           uint32_t target, const Ctl& c,
+                                           int role) {
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (ptx::ld_acquire_gpu(count) < target) {
+    if (*c.abort_flag) return false;
+    if (ptx::globaltimer_ns() - t0 > c.budget) {
+      *c.abort_flag = 1;
+      if (atomicCAS(c.status, 0, TPMLP_ERR_TIMEOUT) == 0) {
+        c.status[1] = role;
+        c.status[2] = static_cast<int>(blockIdx.x);
+      }
+      __threadfence();
+      return false;
+    }
+  }
+  ptx::fence_proxy_async_global();
+  return true;
+}
+
+// Fused LayerNorm prologue (GemmArgs::ln_x), run by one warp: claims rows
+// from a shared counter until every row is taken (two at a time when a row
+// fits in half the register budget, both loaded before either is
+// normalised, so that a warp keeps two rows in flight; else one),
+// normalises each (lnrow::norm_row, the stand-alone kernel's arithmetic)
+// into ln_xn with its mean and rstd, then publishes the claim's row count on
+// its 128-row block: every lane fences its stores for the async proxy (the
+// TMA loads that read them), the warp synchronises, and one lane adds the
+// count with gpu-scope release semantics.  A warp never waits here, and rows
+// go to whichever warps are running, so the producers' waits on these counts
+// end whatever CTAs are resident.
+__device__ __forceinline__ void ln_publish(unsigned int* ready, uint32_t r0,
+                                           int n, int lane) {
+  ptx::fence_proxy_async_global();
+  __syncwarp();
+  if (lane == 0) ptx::red_release_gpu_add(ready + r0 / 128, n);
+}
+
+// gamma / beta: the LayerNorm parameters staged in shared memory by the
+// caller.
+__device__ __forceinline__ void ln_prologue(const GemmArgs& a,
+                                            const float* gamma,
+                                            const float* beta, int lane) {
+  const int vpl = a.K / 256;
+  unsigned int* claim = a.ln_sync;
+  unsigned int* ready = a.ln_sync + 1;
+  const bool two = vpl <= LN_VMAX / 2;
+  const uint32_t step = two ? 2u : 1u;
+  while (true) {
+    uint32_t r0 = 0;
+    if (lane == 0) r0 = atomicAdd(claim, step);
+    r0 = __shfl_sync(0xffffffffu, r0, 0);
+    if (r0 >= static_cast<uint32_t>(a.M)) break;
+    const size_t row = r0;
+    float mu, rs;
+    if (two) {
+      const bool second = r0 + 1 < static_cast<uint32_t>(a.M);
+      uint4 ra[LN_VMAX / 2], rb[LN_VMAX / 2];
+      lnrow::load_row<LN_VMAX / 2>(a.ln_x + row * a.K, vpl, lane, ra);
+      if (second)
+        lnrow::load_row<LN_VMAX / 2>(a.ln_x + (row + 1) * a.K, vpl, lane, rb);
+      lnrow::norm_row<LN_VMAX / 2, false>(ra, gamma, beta,
+                                   a.ln_xn + row * a.K, vpl, a.K, a.ln_eps,
+                                   lane, mu, rs);
+      if (lane == 0) {
+        a.ln_mean[row] = mu;
+        a.ln_rstd[row] = rs;
+      }
+      if (second) {
+        lnrow::norm_row<LN_VMAX / 2, false>(rb, gamma, beta,
+                                     a.ln_xn + (row + 1) * a.K, vpl, a.K,
+                                     a.ln_eps, lane, mu, rs);
+        if (lane == 0) {
+          a.ln_mean[row + 1] = mu;
+          a.ln_rstd[row + 1] = rs;
+        }
+      }
+      ln_publish(ready, r0, second ? 2 : 1, lane);
+    } else {
+      lnrow::row_bf16<LN_VMAX, false>(a.ln_x + row * a.K, gamma, beta,
+                               a.ln_xn + row * a.K, vpl, a.K, a.ln_eps, lane,
+                               mu, rs);
+      if (lane == 0) {
+        a.ln_mean[row] = mu;
+        a.ln_rstd[row] = rs;
+      }
+      ln_publish(ready, r0, 1, lane);
     }
   }
 }

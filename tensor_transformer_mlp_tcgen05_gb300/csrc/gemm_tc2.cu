@@ -18,7 +18,12 @@
 //               commits.
 //   warps 2-3   idle.
 //   warps 4-11  epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 (its
-//               sub-partition) and one 128-column half of the tile.
+//               sub-partition) and one 128-column half of the tile.  With
+//               the fused LayerNorm prologue (GemmArgs::ln_x) they first
+//               normalise rows of the raw input into the A operand, one row
+//               per warp at a time, claimed from a counter shared by the
+//               whole grid, while the producers of tiles whose 128-row A
+//               blocks are complete already load and the MMAs run.
 // Registers: the CTA is launched with 168 per thread (384 x 168 = 64512); the
 // first warpgroup gives registers back (down to REGS_CONTROL) and the two
 // epilogue warpgroups take them (up to REGS_EPILOGUE), enough to hold a
@@ -110,6 +115,16 @@ static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 __device__ __forceinline__ void cta_barrier() {
   asm volatile("bar.sync 1, %0;" ::"n"(NUM_THREADS) : "memory");
 }
+
+// The epilogue warps only.
+__device__ __forceinline__ void epilogue_barrier() {
+  asm volatile("bar.sync 2, %0;" ::"n"(NUM_EPI_WARPS * 32) : "memory");
+}
+
+// The fused LayerNorm prologue stages gamma and beta (fp32, up to 256
+// LN_VMAX values each) in the epilogue staging buffers before their first use.
+static_assert(2 * 256 * LN_VMAX * 4 <= EPI_STAGING_BYTES,
+              "LayerNorm parameters exceed the staging buffers");
 
 // Bounded wait with cluster-scope acquire (tempty: arrivals from both CTAs).
 __device__ __forceinline__ bool wait_bounded_cluster(uint32_t bar,
@@ -265,6 +280,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int mb = 2 * msup + pg;   // may lie past M: zero-filled, unused
         const int m0 = mb * PM + static_cast<int>(prank) * HM;
         const int n0 = nb * PN + static_cast<int>(prank) * HN;
+        if constexpr (EPI == EPI_GELU_FWD && !A_MN && !F8) {
+          // fused LayerNorm: this CTA's 128 A rows must all be written
+          if (args.ln_x != nullptr && m0 < args.M &&
+              !wait_count(args.ln_sync + 1 + m0 / HM,
+                          static_cast<uint32_t>(min(HM, args.M - m0)), ctl,
+                          ROLE_LN_READY)) {
+            alive = false;
+            break;
+          }
+        }
         for (int kb = it.kb_lo; kb < it.kb_hi; ++kb) {
           if (!wait_bounded(empty0 + 8u * stage, phase ^ 1u, ctl,
                             ROLE_PRODUCER)) {
@@ -386,6 +411,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else {
     ptx::setmaxnreg_inc<REGS_EPILOGUE>();
+    if constexpr (EPI == EPI_GELU_FWD && !A_MN && !F8) {
+      // ------------------------------------ fused LayerNorm prologue --
+      // gamma and beta go to the staging buffers (not yet in use: the
+      // epilogue starts after the second barrier), read from there by
+      // every row
+      if (args.ln_x != nullptr &&
+          TPMLP_CHECK(args.K % 256 == 0 && args.K / 256 <= LN_VMAX,
+                      ctl.status, abort_flag, SITE_GEMM_LN)) {
+        float* sg = reinterpret_cast<float*>(smem + size_t(STAGES) * STAGE_BYTES);
+        float* sb = sg + args.K;
+        const int et = static_cast<int>(threadIdx.x) - FIRST_EPI_WARP * 32;
+        for (int i = 4 * et; i < args.K; i += 4 * NUM_EPI_WARPS * 32) {
+          *reinterpret_cast<float4*>(sg + i) =
+              __ldg(reinterpret_cast<const float4*>(args.ln_gamma + i));
+          *reinterpret_cast<float4*>(sb + i) =
+              __ldg(reinterpret_cast<const float4*>(args.ln_beta + i));
+        }
+        epilogue_barrier();
+        ln_prologue(args, sg, sb, lane);
+        epilogue_barrier();
+      }
+    }
     // ------------------------------------------------------ epilogue --
     const int ew = warp - FIRST_EPI_WARP;
     const int q = warp & 3;      // TMEM sub-partition this warp may read

@@ -13,6 +13,7 @@
 // the chunk in order and the 8 warp partials are added in warp order; stage
 // 2 adds the chunk partials in chunk order.  No atomics anywhere.
 #include "internal.h"
+#include "ln_row.cuh"
 
 namespace tpmlp {
 namespace {
@@ -250,21 +251,10 @@ __global__ void __launch_bounds__(LN_WARPS * 32)
   }
 }
 
-// LayerNorm forward with the row in registers (h = 256 VPL, bf16): each
-// lane loads its VPL 16-byte vectors of the row at once (one DRAM round
-// trip per row), then the mean, the variance about it and the normalised
-// row come from registers.  Each lane adds its values in vector order, then
-// the butterfly, as in ln_fwd_kernel (same two-pass formula).
-// Keeps the compiler from carrying unpacked copies of the row from one pass
-// to the next (the raw vectors are all that stays live between passes).
-template <int VPL>
-__device__ __forceinline__ void opaque(uint4 (&raw)[VPL]) {
-#pragma unroll
-  for (int j = 0; j < VPL; ++j)
-    asm volatile("" : "+r"(raw[j].x), "+r"(raw[j].y), "+r"(raw[j].z),
-                 "+r"(raw[j].w));
-}
-
+// LayerNorm forward with the row in registers (h = 256 VPL, bf16): one warp
+// per row, the row's arithmetic in lnrow::row_bf16 (ln_row.cuh), shared with
+// the GEMM's fused LayerNorm prologue.  VPL = 0: any vpl up to LN_VMAX, read
+// at run time (same arithmetic for the same vpl).
 template <int VPL>
 __global__ void __launch_bounds__(LN_WARPS * 32, 2)
     ln_fwd_reg_kernel(const __nv_bfloat16* __restrict__ X,
@@ -278,49 +268,10 @@ __global__ void __launch_bounds__(LN_WARPS * 32, 2)
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
   const size_t base = static_cast<size_t>(row) * h;
-  const uint4* xr = reinterpret_cast<const uint4*>(X + base);
-  uint4 raw[VPL];
-#pragma unroll
-  for (int j = 0; j < VPL; ++j) raw[j] = xr[lane + 32 * j];
-  float s = 0.f;
-#pragma unroll
-  for (int j = 0; j < VPL; ++j) {
-    float v[8];
-    unpack_vec<__nv_bfloat16>(raw[j], v);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) s += v[k];
-  }
-  const float inv_h = 1.0f / static_cast<float>(h);
-  const float mu = warp_sum(s) * inv_h;
-  opaque(raw);
-  float ss = 0.f;
-#pragma unroll
-  for (int j = 0; j < VPL; ++j) {
-    float v[8];
-    unpack_vec<__nv_bfloat16>(raw[j], v);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const float d = v[k] - mu;
-      ss += d * d;
-    }
-  }
-  const float rs = rsqrtf(warp_sum(ss) * inv_h + eps);
-  opaque(raw);
-  uint4* yr = reinterpret_cast<uint4*>(Xn + base);
-#pragma unroll
-  for (int j = 0; j < VPL; ++j) {
-    const int i = lane + 32 * j;
-    float v[8], g[8], b[8];
-    unpack_vec<__nv_bfloat16>(raw[j], v);
-    load_f32<8>(gamma + 8 * i, g);
-    load_f32<8>(beta + 8 * i, b);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) v[k] = (v[k] - mu) * rs * g[k] + b[k];
-    yr[i] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
-                       pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
-    // gamma / beta are L1 hits: no need to load them ahead of this store
-    asm volatile("" ::: "memory");
-  }
+  float mu, rs;
+  constexpr int VMAX = VPL > 0 ? VPL : LN_VMAX;
+  lnrow::row_bf16<VMAX>(X + base, gamma, beta, Xn + base,
+                        VPL > 0 ? VPL : h / 256, h, eps, lane, mu, rs);
   if (lane == 0) {
     mean_out[row] = mu;
     rstd_out[row] = rs;
@@ -664,7 +615,7 @@ cudaError_t launch_ln_fwd(bool bf16, const void* X, const float* gamma,
   ln_fwd_reg_kernel<N><<<grid, LN_WARPS * 32, 0, stream>>>(                  \
       static_cast<const __nv_bfloat16*>(X), gamma, beta,                     \
       static_cast<__nv_bfloat16*>(Xn), mean, rstd, rows, h, eps)
-  if (bf16 && vpl >= 1 && vpl <= 12) {
+  if (bf16 && vpl >= 1 && vpl <= LN_VMAX) {
     switch (vpl) {
       case 1: TPMLP_LN_FWD_REG(1); break;
       case 2: TPMLP_LN_FWD_REG(2); break;
@@ -673,7 +624,10 @@ cudaError_t launch_ln_fwd(bool bf16, const void* X, const float* gamma,
       case 6: TPMLP_LN_FWD_REG(6); break;
       case 8: TPMLP_LN_FWD_REG(8); break;
       case 12: TPMLP_LN_FWD_REG(12); break;
-      default: goto generic;
+      default:
+        if (vpl > LN_VMAX) goto generic;
+        TPMLP_LN_FWD_REG(0);
+        break;
     }
 #undef TPMLP_LN_FWD_REG
     return cudaGetLastError();

@@ -33,6 +33,9 @@ namespace {
 struct Layout {
   size_t status = 0, xn = 0, mean = 0, rstd = 0, y = 0, h = 0, dh = 0,
          dxn = 0, dze = 0, part = 0, tailp = 0, total = 0;
+  // the fused LayerNorm prologue's counters (GemmArgs::ln_sync), right
+  // after the 16-byte status word so one memset clears both
+  size_t lnsync = 0, lnsync_words = 0;
   size_t lnp = 0;   // rows of each LayerNorm-parameter partial section
   int chunks = 0;   // 256-row column-sum chunks
   int groups = 0;   // 32-row groups of the dH GEMM's fused db1 partials
@@ -40,8 +43,9 @@ struct Layout {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Workspace sections, each 256-byte aligned: status word; [Xn, mean, rstd]
-// with LayerNorm; Y; [bf16: the GEMM tail-split partials, TAIL_PART_BYTES];
+// Workspace sections, each 256-byte aligned: status word [+ with bf16
+// LayerNorm, the prologue's row counters: 1 + ceil(T / 128) words];
+// [Xn, mean, rstd] with LayerNorm; Y; [bf16: the GEMM tail-split partials, TAIL_PART_BYTES];
 // and for training H, dH, [dXn fp32 with LayerNorm], [the dropout-masked dZ
 // with dropout], column-sum partials: db2 (chunks x h), db1 (max(groups,
 // chunks) x f), dgamma and dbeta (lnp = chunks x h each).
@@ -57,7 +61,13 @@ Layout make_layout(const tp_mlp_config& c, int tokens, int training) {
     off = align_up(off + bytes, 256);
     return o;
   };
-  L.status = take(256);
+  if (c.use_layernorm && c.dtype == TPMLP_BF16) {
+    L.lnsync_words = 1 + (T + 127) / 128;
+    L.lnsync = 16;
+    L.status = take(16 + 4 * L.lnsync_words);
+  } else {
+    L.status = take(256);
+  }
   if (c.use_layernorm) {
     L.xn = take(T * h * es);
     L.mean = take(T * 4);
@@ -172,6 +182,7 @@ struct tp_mlp_handle {
   tpmlp::host::HandleCore core;
   tp_mlp_config cfg;
   unsigned long long drop_seed = 0, drop_offset = 0;
+  bool ln_prologue = true;   // tp_mlp_set_ln_prologue
 };
 
 namespace {
@@ -290,19 +301,26 @@ int tp_mlp_forward(tp_mlp_handle* H, int tokens, const void* X, const void* A,
   TRY(check_device(&sms));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
-  cudaError_t e = cudaMemsetAsync(ws + L.status, 0, 16, s);
+  const bool bf16 = c.dtype == TPMLP_BF16;
+  const int T = tokens, h = c.hidden, f = c.ffn, t = c.shards, ft = f / t;
+  // LayerNorm inside GEMM1's launch (GemmArgs::ln_x)
+  const bool ln_fused = c.use_layernorm && bf16 && H->ln_prologue &&
+                        h % 256 == 0 && h / 256 <= LN_VMAX;
+  // the status word, and with the fused LayerNorm its counters, cleared
+  const size_t clear = ln_fused ? 16 + 4 * L.lnsync_words : 16;
+  cudaError_t e = cudaMemsetAsync(ws + L.status, 0, clear, s);
   if (e != cudaSuccess) {
     set_detail("cudaMemsetAsync(status)", e);
     return TPMLP_ERR_CUDA;
   }
   if (tokens == 0) return TPMLP_OK;
 
-  const bool bf16 = c.dtype == TPMLP_BF16;
-  const int T = tokens, h = c.hidden, f = c.ffn, t = c.shards, ft = f / t;
   void* Y = ws + L.y;
   void* Hbuf = training ? ws + L.h : nullptr;
   const void* Xop = X;
-  if (c.use_layernorm) {
+  if (ln_fused) {
+    Xop = ws + L.xn;
+  } else if (c.use_layernorm) {
     void* Xn = ws + L.xn;
     TRY(run(&H->core, "layernorm_fwd", s, [&] {
       return launch_ln_fwd(bf16, X, ln_gamma, ln_beta, Xn,
@@ -316,6 +334,16 @@ int tp_mlp_forward(tp_mlp_handle* H, int tokens, const void* X, const void* A,
   GemmArgs g1 = base_args(H, ws, L);
   g1.M = T; g1.N = f; g1.K = h;
   g1.out = Y; g1.ldo = f; g1.out2 = Hbuf; g1.bias = bias1;
+  if (ln_fused) {
+    g1.ln_x = static_cast<const __nv_bfloat16*>(X);
+    g1.ln_gamma = ln_gamma;
+    g1.ln_beta = ln_beta;
+    g1.ln_xn = reinterpret_cast<__nv_bfloat16*>(ws + L.xn);
+    g1.ln_mean = reinterpret_cast<float*>(ws + L.mean);
+    g1.ln_rstd = reinterpret_cast<float*>(ws + L.rstd);
+    g1.ln_eps = c.ln_eps;
+    g1.ln_sync = reinterpret_cast<unsigned int*>(ws + L.status + L.lnsync);
+  }
   GemmArgs g2 = base_args(H, ws, L);
   g2.M = T; g2.N = h; g2.K = f; g2.num_seg = t;
   g2.out = Z; g2.ldo = h; g2.bias = bias2;
@@ -330,8 +358,8 @@ int tp_mlp_forward(tp_mlp_handle* H, int tokens, const void* X, const void* A,
     g1.kb_per_seg = h / TC_BK;
     TRY(kmajor_map(&ta, Xop, T, h, TC_BM));
     TRY(mnmajor_map(&tb, A, h, f));
-    TRY(tc_gemm(&H->core, "gemm1_gelu", s, sms, EPI_GELU_FWD, false, true, ta, tb,
-                g1));
+    TRY(tc_gemm(&H->core, ln_fused ? "gemm1_ln_gelu" : "gemm1_gelu", s, sms,
+                EPI_GELU_FWD, false, true, ta, tb, g1));
     g2.kb_per_seg = ft / TC_BK;
     TRY(kmajor_map(&ta, Y, T, f, TC_BM));
     TRY(mnmajor_map(&tb, B, f, h));
@@ -959,6 +987,12 @@ int tp_mlp_set_wait_budget(tp_mlp_handle* handle, unsigned long long ns) {
 int tp_mlp_set_nvtx(tp_mlp_handle* handle, int enable) {
   if (handle == nullptr || (enable != 0 && enable != 1)) return TPMLP_ERR_ARG;
   handle->core.nvtx = enable != 0;
+  return TPMLP_OK;
+}
+
+int tp_mlp_set_ln_prologue(tp_mlp_handle* handle, int enable) {
+  if (handle == nullptr || (enable != 0 && enable != 1)) return TPMLP_ERR_ARG;
+  handle->ln_prologue = enable != 0;
   return TPMLP_OK;
 }
 

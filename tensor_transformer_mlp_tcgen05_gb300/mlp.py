@@ -18,7 +18,8 @@ class TensorParallelMLP:
                  dtype: str = "bf16", layernorm: bool = False,
                  ln_eps: float = 1e-5, gelu: str = "erf", residual: bool = False,
                  dropout_p: float = 0.0, dropout_seed: int = 0,
-                 dropout_offset: int = 0, device=None):
+                 dropout_offset: int = 0, device=None,
+                 ln_prologue: bool = True):
         self.cfg = B_.tp_mlp_config(
             hidden=hidden, ffn=ffn, shards=shards, max_tokens=max_tokens,
             dtype=B_.TPMLP_BF16 if dtype == "bf16" else B_.TPMLP_FP32,
@@ -30,6 +31,8 @@ class TensorParallelMLP:
         self.handle = B_.tp_mlp_create(self.cfg)
         if dropout_p > 0:
             B_.tp_mlp_set_dropout_seed(self.handle, dropout_seed, dropout_offset)
+        if not ln_prologue:   # the LayerNorm as its own launch before GEMM1
+            B_.tp_mlp_set_ln_prologue(self.handle, False)
         self.hidden, self.ffn, self.shards = hidden, ffn, shards
         self.max_tokens = max_tokens
         self.layernorm = layernorm

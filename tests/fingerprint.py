@@ -30,7 +30,8 @@ TILE_M, TILE_N = 128, 256
 MLP_ORDER = ["Xn", "H", "Y", "Z", "dH", "db2", "db1", "dB", "dA", "dX",
              "dgamma", "dbeta"]
 MLP_KERNEL = {
-    "Xn": "layernorm_fwd", "H": "gemm1_gelu", "Y": "gemm1_gelu",
+    "Xn": "layernorm_fwd (fused: gemm1_ln_gelu's prologue)",
+    "H": "gemm1_gelu / gemm1_ln_gelu", "Y": "gemm1_gelu / gemm1_ln_gelu",
     "Z": "gemm2_shardsum (tail: gemm_tail_combine)",
     "dH": "gemm_dh_gelu_bwd", "db2": "colsum_db2 + colsum_finalize",
     "db1": "gemm_dh_gelu_bwd partials + colsum_finalize",

@@ -238,6 +238,42 @@ def test_gelu_probe_rejects_bad_arguments(lib):
                                  None) == B.TPMLP_OK
 
 
+def test_ln_prologue_switch_validates_arguments(lib):
+    assert lib.tp_mlp_set_ln_prologue(None, 1) == B.TPMLP_ERR_ARG
+    h = B.tp_mlp_create(B.tp_mlp_config(hidden=256, ffn=1024, shards=4,
+                                        max_tokens=64, dtype=B.TPMLP_BF16,
+                                        use_layernorm=1, ln_eps=1e-5))
+    try:
+        assert lib.tp_mlp_set_ln_prologue(h, 2) == B.TPMLP_ERR_ARG
+        assert lib.tp_mlp_set_ln_prologue(h, 0) == B.TPMLP_OK
+        assert lib.tp_mlp_set_ln_prologue(h, 1) == B.TPMLP_OK
+    finally:
+        B.tp_mlp_destroy(h)
+
+
+def test_workspace_holds_the_layernorm_row_counters(lib):
+    """With bf16 LayerNorm the status section also holds the fused
+    prologue's counters (1 + ceil(T / 128) words): the workspace grows with
+    the token count by that much beyond the token-sized buffers."""
+    cfg = dict(hidden=256, ffn=1024, shards=4, max_tokens=1 << 20,
+               dtype=B.TPMLP_BF16, ln_eps=1e-5)
+    with_ln = B.tp_mlp_create(B.tp_mlp_config(use_layernorm=1, **cfg))
+    no_ln = B.tp_mlp_create(B.tp_mlp_config(use_layernorm=0, **cfg))
+    try:
+        for T in (1, 128, 129, 70000):
+            a = B.tp_mlp_workspace_bytes(with_ln, T, 0)
+            b = B.tp_mlp_workspace_bytes(no_ln, T, 0)
+            # Xn (bf16), mean and rstd (fp32), each section 256-aligned,
+            # and the counters beyond the plain 256-byte status section
+            up = lambda x: (x + 255) // 256 * 256
+            words = 1 + (T + 127) // 128
+            assert a - b == (up(T * 256 * 2) + 2 * up(T * 4)
+                             + up(16 + 4 * words) - 256), T
+    finally:
+        B.tp_mlp_destroy(with_ln)
+        B.tp_mlp_destroy(no_ln)
+
+
 def test_nvtx_switch_validates_arguments(lib):
     assert lib.tp_mlp_set_nvtx(None, 1) == B.TPMLP_ERR_ARG
     assert lib.tp_attn_set_nvtx(None, 0) == B.TPMLP_ERR_ARG

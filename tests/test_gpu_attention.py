@@ -3,7 +3,7 @@ binding) against the fp64 oracle in ``oracle/attention.py``.
 
 Element-by-element comparisons on seeded inputs at sizes the oracle finishes
 in seconds (several 128-row blocks per sequence, two sequences, shards 1-4,
-head dims 64 and 128, causal and not, with and without LayerNorm, biases and
+head dims 64, 96 and 128, causal and not, with and without LayerNorm, biases and
 the residual), plus bitwise repeatability and the empty call."""
 import math
 
