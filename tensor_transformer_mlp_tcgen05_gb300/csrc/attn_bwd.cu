@@ -7,7 +7,9 @@
 // log-sum-exp), dO = dCtx and delta = rowsum(dO * O) = sum_j P dP (the query
 // kernel starts from the first form, from its dO tile and the forward's
 // context rows, and writes the second, from its own P and dP, for the
-// key/value kernel, which therefore runs second):
+// key/value kernel, which therefore runs second; it writes -lse2 and
+// -delta', so that the key/value kernel's per-column terms enter its packed
+// fused multiply-adds and additions without a negation):
 //   dV = P^T dO,   dP = dO V^T,   dS = P * (dP - delta) / sqrt(d),
 //   dK = dS^T Q,   dQ = dS K.
 // Every output element has exactly one writer and no atomics are used:
@@ -36,10 +38,13 @@
 // 32 rows
 // into the partials of the QKV bias gradient.
 //
-// Warp roles: warp 0 TMA producer, warp 1 TMEM allocator and MMA issuer (the
-// whole warp; one elected lane issues), warps 4-11 elementwise (thread = row
-// = TMEM lane, two warps per row quarter, one per half of the columns).  All
-// waits are bounded.
+// Warp roles: warp 0 TMA producer, warp 1 TMEM allocator and issuer of the
+// score MMAs, warp 2 issuer of the gradient MMAs (each the whole warp, one
+// elected lane issuing), warps 4-11 elementwise (thread = row = TMEM lane,
+// two warps per row quarter, one per half of the columns).  With one issuer
+// per kind, the next step's score MMAs are queued while this step's
+// gradient MMAs are still being issued, so the tensor pipe does not idle
+// between them.  All waits are bounded.
 #include "attn_common.cuh"
 
 namespace tpmlp {
@@ -67,11 +72,11 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   // cover the TMA latency (4 fit for KV next to its lse / delta vectors, 5
   // for Q).
   constexpr int NB = KV ? 4 : 5;
-  constexpr uint32_t VEC_BYTES = 512;              // 64 lse2 + 64 delta
+  constexpr uint32_t VEC_BYTES = 512;              // 64 -lse2 + 64 -delta
   // KV: lse2 / delta of the streamed queries per stage; Q: the two column
   // halves' partial row sums of dS, exchanged at the end
   constexpr uint32_t VEC_TOTAL = KV ? NB * VEC_BYTES : 1024;
-  constexpr int NBARS = 11 + 2 * NB;
+  constexpr int NBARS = 12 + 2 * NB;
   constexpr uint32_t B_TX = 2 * B_TILE + (KV ? VEC_BYTES : 0);
   constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 64, false, false);
   constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, false, true);
@@ -93,7 +98,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   const uint32_t sA2 = sA1 + A_TILE;
   const uint32_t sB = sA2 + A_TILE;                // [stage][B1 | B2]
   uint8_t* vec_gen = smem + 2 * A_TILE + NB * 2 * B_TILE;
-  const uint32_t sVec = ptx::smem_u32(vec_gen);    // [stage][lse2 | delta]
+  const uint32_t sVec = ptx::smem_u32(vec_gen);    // [stage][-lse2 | -delta]
   uint64_t* bars = reinterpret_cast<uint64_t*>(vec_gen + VEC_TOTAL);
   const uint32_t b0 = ptx::smem_u32(bars);
   // s_full: S and dP of the step are in TMEM (one buffer); s_read: the
@@ -105,7 +110,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                  e_full = s_full + 16, e_empty = e_full + 16,
                  o_full = e_empty + 16,
                  done_bar = o_full + 8, ctx_full = done_bar + 8,
-                 ctx_free = ctx_full + 8;
+                 ctx_free = ctx_full + 8, done2 = ctx_free + 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
@@ -143,6 +148,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     ptx::mbar_init(done_bar, 1);
     ptx::mbar_init(ctx_full, 1);
     ptx::mbar_init(ctx_free, SOFTMAX_WARPS);
+    ptx::mbar_init(done2, 1);
     *abort_flag = 0;
     ptx::fence_barrier_init();
   }
@@ -201,17 +207,25 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         }
         if constexpr (KV) {
           const size_t off = static_cast<size_t>(head) * a.ld_stat + col0;
-          ptx::bulk_load_1d(sVec + bs * VEC_BYTES, a.lse + off, 256, bf);
-          ptx::bulk_load_1d(sVec + bs * VEC_BYTES + 256, a.delta + off, 256, bf);
+          const size_t plane = static_cast<size_t>(a.heads) * a.ld_stat;
+          ptx::bulk_load_1d(sVec + bs * VEC_BYTES, a.delta + off, 256, bf);
+          ptx::bulk_load_1d(sVec + bs * VEC_BYTES + 256, a.delta + plane + off,
+                            256, bf);
         }
       }
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == 2) {
     {
-      // ------------------------ MMA issuer (whole warp, elected lane) --
-      bool alive = warp_wait(a_full, 0, ctl, ROLE_MMA);
+      // ------------------------ MMA issuers (whole warp, elected lane) --
+      // warp 1: S1, S2 of every step; warp 2: the step's gradient MMAs.
+      // Each tcgen05.commit tracks its own thread's MMAs only: s_full the
+      // score MMAs; b_empty, e_empty and o_full the gradient MMAs, which
+      // start after the same step's score MMAs have completed (e_full is
+      // arrived after s_full), so a ring stage is released only when both
+      // kinds have read it.
+      bool alive = warp == 2 || warp_wait(a_full, 0, ctl, ROLE_MMA);
       const uint64_t dA1 = ptx::sdesc_sw128(sA1, 16, 1024);
       const uint64_t dA2 = ptx::sdesc_sw128(sA2, 16, 1024);
       const uint64_t dBk = ptx::sdesc_sw128(sB, 16, 1024);          // K-major
@@ -246,8 +260,12 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       };
       auto issue_o = [&](int n) -> bool {
         const uint32_t st = n & 1, ph = (n >> 1) & 1;
-        const uint32_t bs = n % NB;
-        if (!warp_wait(e_full + 8 * st, ph, ctl, ROLE_MMA)) return false;
+        const uint32_t bs = n % NB, bph = (n / NB) & 1;
+        // (the stage's b_full phase is still step n's: its refill for step
+        // n + NB waits for this step's commit to b_empty)
+        if (!warp_wait(e_full + 8 * st, ph, ctl, ROLE_MMA) ||
+            !warp_wait(b_full + 8 * bs, bph, ctl, ROLE_MMA))
+          return false;
         ptx::tc_fence_after();
         const uint64_t b1 = desc_add(dBm, bs * 2 * B_TILE);
         const uint64_t b2 = desc_add(b1, B_TILE);
@@ -270,15 +288,17 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         commit_el(e_empty + 8 * st);
         return true;
       };
-      if (alive) alive = issue_s(0);
-      for (int n = 0; alive && n < nsteps; ++n) {
-        if (n + 1 < nsteps && !(alive = issue_s(n + 1))) break;
-        alive = issue_o(n);
+      if (warp == 1) {
+        for (int n = 0; alive && n < nsteps; ++n) alive = issue_s(n);
+      } else {
+        for (int n = 0; alive && n < nsteps; ++n) alive = issue_o(n);
+        if (alive) commit_el(o_full);
       }
-      if (alive) commit_el(o_full);
       if (*reinterpret_cast<volatile int*>(abort_flag)) {
-        commit_el(done_bar);
-        wait_teardown(done_bar, 0);
+        // every MMA this warp issued has completed before TMEM is freed
+        const uint32_t db = warp == 1 ? done_bar : done2;
+        commit_el(db);
+        wait_teardown(db, 0);
       }
     }
     __syncwarp();
@@ -325,7 +345,6 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         if (lane == 0) ptx::mbar_arrive(ctx_free);
       }
     }
-    const float* vec = reinterpret_cast<const float*>(vec_gen);
     float rsum = 0.f;              // Q: this half's sum of dS over its keys
     for (int n = 0; alive && n < nsteps; ++n) {
       const uint32_t st = n & 1, ph = (n >> 1) & 1;
@@ -343,8 +362,6 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       const int diff = rb * 128 + r - cb * 64 - 32 * hf;
       const int lo = (KV && a.causal) ? diff : -1;
       const int hi = (!KV && a.causal) ? diff : 64;
-      const float* vl = vec + bs * (VEC_BYTES / 4) + 32 * hf;
-      const float* vd = vl + 64;
       uint32_t s1[32], s2[32];
       ptx::tmem_ld_32x32b_x32(tmem + lane_base + TMEM_S1 + 32 * hf, s1);
       ptx::tmem_ld_32x32b_x32(tmem + lane_base + TMEM_S2 + 32 * hf, s2);
@@ -356,16 +373,17 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       if (lane == 0) ptx::mbar_arrive(s_read);
       uint32_t pw[16], dw[16];
       // column pairs with packed fp32x2 arithmetic:
-      // P = 2^(S sl2 - L), dS = P (dP - delta) / sqrt(d)
+      // P = 2^(S sl2 - L), dS = P (dP - delta) / sqrt(d), from nL = -L and
+      // nD = -delta
       const uint64_t scale = f2_pack(sl2, sl2);
       const uint64_t inv_sqrt_d = f2_pack(INV_SQRT_D, INV_SQRT_D);
       // the causal mask touches no column of this warp's rows: no selects
       const bool unmasked = __all_sync(0xffffffffu, lo <= 0 && hi >= 31);
-      auto pair = [&](int i, float L0, float L1, float D0, float D1,
+      auto pair = [&](int i, float nL0, float nL1, float nD0, float nD1,
                       bool masked) {
         float a0, a1;
         f2_unpack(f2_fma(f2_pack(__uint_as_float(s1[i]), __uint_as_float(s1[i + 1])),
-                         scale, f2_pack(-L0, -L1)),
+                         scale, f2_pack(nL0, nL1)),
                   a0, a1);
         float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
         if (masked) {
@@ -374,7 +392,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         }
         const uint64_t dp = f2_add(
             f2_pack(__uint_as_float(s2[i]), __uint_as_float(s2[i + 1])),
-            f2_pack(-D0, -D1));
+            f2_pack(nD0, nD1));
         float ds0, ds1;
         f2_unpack(f2_mul(f2_mul(f2_pack(p0, p1), dp), inv_sqrt_d), ds0, ds1);
         pw[i / 2] = pack_bf16x2(p0, p1);
@@ -382,17 +400,35 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         rsum += ds0 + ds1;
       };
       auto columns = [&](bool masked) {
+        if constexpr (KV) {
+          // the streamed queries' -lse2 and -delta', four columns a load,
+          // each loaded two groups ahead of its use (the loads' latency
+          // otherwise lies on the chain)
+          const uint32_t va = sVec + bs * VEC_BYTES + 128u * hf;
+          uint32_t l4[3][4], d4[3][4];
+          ptx::ld_shared_v4(va, l4[0]);
+          ptx::ld_shared_v4(va + 256u, d4[0]);
+          ptx::ld_shared_v4(va + 16u, l4[1]);
+          ptx::ld_shared_v4(va + 256u + 16u, d4[1]);
 #pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          if constexpr (KV) {
-            // the streamed queries' lse2 and delta, four columns per load
-            const float4 l4 = *reinterpret_cast<const float4*>(vl + i);
-            const float4 d4 = *reinterpret_cast<const float4*>(vd + i);
-            pair(i, l4.x, l4.y, d4.x, d4.y, masked);
-            pair(i + 2, l4.z, l4.w, d4.z, d4.w, masked);
-          } else {
-            pair(i, lse_r, lse_r, delta_r, delta_r, masked);
-            pair(i + 2, lse_r, lse_r, delta_r, delta_r, masked);
+          for (int i = 0; i < 32; i += 4) {
+            const int g = i / 4;
+            if (i + 8 < 32) {
+              ptx::ld_shared_v4(va + 4u * (i + 8), l4[(g + 2) % 3]);
+              ptx::ld_shared_v4(va + 256u + 4u * (i + 8), d4[(g + 2) % 3]);
+            }
+            const uint32_t(&l)[4] = l4[g % 3];
+            const uint32_t(&d)[4] = d4[g % 3];
+            pair(i, __uint_as_float(l[0]), __uint_as_float(l[1]),
+                 __uint_as_float(d[0]), __uint_as_float(d[1]), masked);
+            pair(i + 2, __uint_as_float(l[2]), __uint_as_float(l[3]),
+                 __uint_as_float(d[2]), __uint_as_float(d[3]), masked);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            pair(i, -lse_r, -lse_r, -delta_r, -delta_r, masked);
+            pair(i + 2, -lse_r, -lse_r, -delta_r, -delta_r, masked);
           }
         }
       };
@@ -435,9 +471,12 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       // offset either.  With delta from the rounded context instead, every
       // dS of a query row would be off by P times that rounding error,
       // which dK = dS^T Q does not cancel.
-      if (alive && hf == 0)
-        a.delta[static_cast<size_t>(head) * a.ld_stat + row0 + r] =
-            delta_r + rrow / INV_SQRT_D;
+      if (alive && hf == 0) {
+        const size_t off = static_cast<size_t>(head) * a.ld_stat + row0 + r;
+        a.delta[off] = -lse_r;
+        a.delta[static_cast<size_t>(a.heads) * a.ld_stat + off] =
+            -(delta_r + rrow / INV_SQRT_D);
+      }
     }
     if (alive && warp_wait(o_full, 0, ctl, ROLE_EPILOGUE)) {
       ptx::tc_fence_after();
@@ -571,7 +610,7 @@ size_t attn_bwd_smem() {
   constexpr int KB = (D + 63) / 64;
   constexpr int NB = KV ? 4 : 5;
   const size_t need = 1024 + 2 * KB * KBLOCK_BYTES + NB * 2 * KB * ATOM_BYTES +
-                      (KV ? NB * 512 : 1024) + (11 + 2 * NB) * 8 + 16;
+                      (KV ? NB * 512 : 1024) + (12 + 2 * NB) * 8 + 16;
   return need > 116 * 1024 ? need : 116 * 1024;
 }
 

@@ -55,7 +55,7 @@ AttnLayout attn_layout(const tp_attn_config& c, int tokens, int training) {
   L.tailp = take(static_cast<size_t>(TAIL_PART_BYTES));  // GEMM tail split
   if (training) {
     L.dctx = take(T * h * 2);
-    L.delta = take(H * T * 4);
+    L.delta = take(2 * H * T * 4);   // -lse2 and -delta' (AttnArgs::delta)
     L.dqkv = take(T * 3 * h * 2);
     if (c.use_layernorm) L.dxn = take(T * h * 4);
     L.chunks = colsum_chunks(tokens);

@@ -153,9 +153,12 @@ struct AttnArgs {
                         // log2(e) / sqrt(d)
   long long ld_stat;    // row pitch of lse / delta (= T)
   const __nv_bfloat16* dctx;  // backward: dCtx [T, h]
-  float* delta;               // backward: rowsum(dCtx * Ctx) per head [H, T],
-                              // written by the query kernel, read by the
-                              // key/value kernel
+  float* delta;               // backward, [2][H][T]: written by the query
+                              // kernel, read by the key/value kernel:
+                              // [0] -lse2 of each query row, [1] -delta'
+                              // (delta' = sum_j P dP with the query
+                              // kernel's own P and dP), negated so that the
+                              // key/value kernel adds them
   __nv_bfloat16* dqkv;        // backward output [T, 3h] (same layout as QKV)
   long long ld_qkv;
   float* colsum;              // backward (nullable, d = 128): per 32-row group
