@@ -25,13 +25,17 @@
 // The Q kernel also forms delta for its 128 queries from its dO tile and the
 // forward's context rows (loaded into the last ring stage before the ring
 // first reaches it), and at its end writes sum_j P dP for the KV kernel.
-// The elementwise step writes P and dS as bf16 into one of two tensor-memory
-// buffers of their own, where the output MMAs take them as A operands (their
-// B operands are the streamed tiles read M/N-major, the same bytes); S and
-// dP have one buffer, which the next step's score MMAs overwrite as soon as
-// the elementwise warps have loaded it, so the tensor pipe goes from one
-// step's gradient MMAs to the next step's score MMAs without waiting for
-// the former to finish.
+// The elementwise step writes P and dS as bf16 into a tensor-memory buffer of
+// their own, where the output MMAs take them as A operands (their B operands
+// are the streamed tiles read M/N-major, the same bytes); S and dP have one
+// buffer, which the next step's score MMAs overwrite as soon as the
+// elementwise warps have loaded it, so the tensor pipe goes from one step's
+// gradient MMAs to the next step's score MMAs without waiting for the former
+// to finish.  A1 (K for KV, Q for Q) is copied once into tensor memory by
+// the elementwise warps, so the S1 MMAs read only the streamed tile from
+// shared memory (a 128 x 64 x 16 MMA with both operands in shared memory
+// needs 6 KB per instruction and runs at the shared-memory operand rate,
+// 48 cycles; with A in tensor memory, 2 KB and 32 cycles).
 // Outputs leave as 32-row x 64-column bf16 chunks staged in the idle B ring
 // and stored by TMA (at d = 96 the last 32 columns of dK and dV, and dQ,
 // with plain 16-byte stores); at d = 128 each chunk is also summed over its
@@ -81,9 +85,11 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 64, false, false);
   constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, false, true);
   // TMEM columns: S1 (S or S^T) and S2 (dP or dP^T) of the current step,
-  // 64 each; two buffers of the bf16 P and dS operands, 64 each (P then
-  // dS, 32 packed columns apiece); the two fp32 accumulators.
+  // 64 each; the bf16 P and dS operands (P then dS, 32 packed columns
+  // apiece); A1 as a bf16 MMA operand (row m in lane m, two elements per
+  // column, D / 2 columns); the two fp32 accumulators.
   constexpr uint32_t TMEM_S1 = 0, TMEM_S2 = 64, TMEM_PDS = 128;
+  constexpr uint32_t TMEM_A1 = 192;
   constexpr uint32_t TMEM_OUT2 = 256;              // dK (KV) or dQ
   constexpr uint32_t TMEM_OUT1 = 256 + 64 * KB;    // dV (KV) or P K (Q)
   constexpr float INV_SQRT_D = D == 64   ? 0.125f
@@ -103,11 +109,13 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   const uint32_t b0 = ptx::smem_u32(bars);
   // s_full: S and dP of the step are in TMEM (one buffer); s_read: the
   // elementwise warps have loaded them, so the next step's MMAs may
-  // overwrite them; e_full / e_empty: P and dS of the step are in their
+  // overwrite them; a1_full: A1 is in tensor memory; e_full / e_empty: P
+  // and dS of the step are in their
   // TMEM buffer (two, by step parity) / its gradient MMAs have read them.
   const uint32_t a_full = b0, b_full = b0 + 8, b_empty = b_full + 8 * NB,
                  s_full = b_empty + 8 * NB, s_read = s_full + 8,
-                 e_full = s_full + 16, e_empty = e_full + 16,
+                 e_full = s_full + 16, a1_full = e_full + 8,
+                 e_empty = e_full + 16,
                  o_full = e_empty + 16,
                  done_bar = o_full + 8, ctx_full = done_bar + 8,
                  ctx_free = ctx_full + 8, done2 = ctx_free + 8;
@@ -141,7 +149,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     ptx::mbar_init(s_full, 1);
     ptx::mbar_init(s_read, SOFTMAX_WARPS);
     for (int i = 0; i < 2; ++i) {
-      ptx::mbar_init(e_full + 8 * i, SOFTMAX_WARPS);
+      ptx::mbar_init(e_full + 8 * i, SOFTMAX_WARPS);   // [1]: a1_full
       ptx::mbar_init(e_empty + 8 * i, 1);
     }
     ptx::mbar_init(o_full, 1);
@@ -226,7 +234,6 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       // arrived after s_full), so a ring stage is released only when both
       // kinds have read it.
       bool alive = warp == 2 || warp_wait(a_full, 0, ctl, ROLE_MMA);
-      const uint64_t dA1 = ptx::sdesc_sw128(sA1, 16, 1024);
       const uint64_t dA2 = ptx::sdesc_sw128(sA2, 16, 1024);
       const uint64_t dBk = ptx::sdesc_sw128(sB, 16, 1024);          // K-major
       const uint64_t dBm = ptx::sdesc_sw128(sB, ATOM_BYTES, 1024);  // MN-major
@@ -238,14 +245,14 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         if (n >= 1 && !warp_wait(s_read, static_cast<uint32_t>(n - 1) & 1u,
                                  ctl, ROLE_MMA))
           return false;
+        if (n == 0 && !warp_wait(a1_full, 0, ctl, ROLE_MMA)) return false;
         ptx::tc_fence_after();
         const uint64_t b1 = desc_add(dBk, bs * 2 * B_TILE);
         const uint64_t b2 = desc_add(b1, B_TILE);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t ao = (k / 4) * KBLOCK_BYTES + (k % 4) * 32;
           const uint32_t bo = (k / 4) * ATOM_BYTES + (k % 4) * 32;
-          mma_ss_el(tmem + TMEM_S1, desc_add(dA1, ao), desc_add(b1, bo),
+          mma_ts_el(tmem + TMEM_S1, tmem + TMEM_A1 + 8 * k, desc_add(b1, bo),
                     IDESC_S, k > 0 ? 1u : 0u);
         }
 #pragma unroll
@@ -259,20 +266,19 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         return true;
       };
       auto issue_o = [&](int n) -> bool {
-        const uint32_t st = n & 1, ph = (n >> 1) & 1;
         const uint32_t bs = n % NB, bph = (n / NB) & 1;
         // (the stage's b_full phase is still step n's: its refill for step
         // n + NB waits for this step's commit to b_empty)
-        if (!warp_wait(e_full + 8 * st, ph, ctl, ROLE_MMA) ||
+        if (!warp_wait(e_full, static_cast<uint32_t>(n) & 1u, ctl, ROLE_MMA) ||
             !warp_wait(b_full + 8 * bs, bph, ctl, ROLE_MMA))
           return false;
         ptx::tc_fence_after();
         const uint64_t b1 = desc_add(dBm, bs * 2 * B_TILE);
         const uint64_t b2 = desc_add(b1, B_TILE);
-        // A operands in TMEM: P and dS of buffer st, 32 packed columns each
-        // (the column half hf of the elementwise warps wrote its 32 queries
-        // or keys at +16 hf): k-step k (16 of the step's 64) at +8 k
-        const uint32_t e1 = tmem + TMEM_PDS + 64 * st, e2 = e1 + 32;
+        // A operands in TMEM: P and dS, 32 packed columns each (the column
+        // half hf of the elementwise warps wrote its 32 queries or keys at
+        // +16 hf): k-step k (16 of the step's 64) at +8 k
+        const uint32_t e1 = tmem + TMEM_PDS, e2 = e1 + 32;
 #pragma unroll
         for (int k = 0; k < 4; ++k)
           mma_ts_el(tmem + TMEM_OUT2, e2 + 8 * k, desc_add(b1, 2048 * k),
@@ -285,7 +291,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                     desc_add(KV ? b2 : b1, 2048 * k), IDESC_O,
                     (n > 0 || k > 0) ? 1u : 0u);
         commit_el(b_empty + 8 * bs);
-        commit_el(e_empty + 8 * st);
+        commit_el(e_empty);
         return true;
       };
       if (warp == 1) {
@@ -312,7 +318,41 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     const float sl2 = a.scale_log2;
     float lse_r = 0.f, delta_r = 0.f;
-    bool alive = true;
+    bool alive = warp_wait(a_full, 0, ctl, ROLE_EPILOGUE);
+    if (alive) {
+      // A1 into tensor memory for the S1 MMAs: this warp's 32 rows of
+      // k-block hf (64 elements, or D - 64 of them; none for hf = 1 when
+      // D = 64), column 32 hf + j holding elements 2j and 2j + 1 of the
+      // k-block (16-byte unit u of row r sits at u ^ (r mod 8))
+      constexpr int U1 = D > 64 ? (D - 64) / 8 : 0;
+      const int units = hf == 0 ? 8 : U1;
+      if (units > 0) {
+        const uint32_t rowa = sA1 + static_cast<uint32_t>(hf) * KBLOCK_BYTES +
+                              static_cast<uint32_t>(r) * 128u;
+        uint32_t w[32];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          uint32_t v[4] = {0u, 0u, 0u, 0u};
+          if (u < units)
+            ptx::ld_shared_v4(rowa + 16u * static_cast<uint32_t>(u ^ (r & 7)), v);
+#pragma unroll
+          for (int t = 0; t < 4; ++t) w[4 * u + t] = v[t];
+        }
+        const uint32_t dst = tmem + lane_base + TMEM_A1 + 32u * hf;
+        if (units == 8) {
+          tmem_st_32x32b_x32(dst, w);
+        } else {
+          uint32_t w16[16];
+#pragma unroll
+          for (int t = 0; t < 16; ++t) w16[t] = w[t];
+          tmem_st_32x32b_x16(dst, w16);
+        }
+        tmem_st_wait();
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(a1_full);
+    }
     if constexpr (!KV) {
       // delta of this query row = sum_e dO[r][e] O[r][e], both tiles in shared
       // memory (128-byte-swizzled rows; O, the forward's context, in the last
@@ -320,8 +360,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       // warps of the row (so both hold the same value without an exchange).
       const size_t off = static_cast<size_t>(head) * a.ld_stat + row0 + r;
       lse_r = a.lse[off];
-      alive = warp_wait(a_full, 0, ctl, ROLE_EPILOGUE) &&
-              warp_wait(ctx_full, 0, ctl, ROLE_EPILOGUE);
+      alive = alive && warp_wait(ctx_full, 0, ctl, ROLE_EPILOGUE);
       if (alive) {
 #pragma unroll
         for (int u = 0; u < D / 8; ++u) {
@@ -347,7 +386,6 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     }
     float rsum = 0.f;              // Q: this half's sum of dS over its keys
     for (int n = 0; alive && n < nsteps; ++n) {
-      const uint32_t st = n & 1, ph = (n >> 1) & 1;
       const uint32_t bs = n % NB, bph = (n / NB) & 1;
       if (!warp_wait(s_full, static_cast<uint32_t>(n) & 1u, ctl,
                      ROLE_EPILOGUE) ||
@@ -437,20 +475,21 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       } else {
         columns(true);
       }
-      // P and dS into buffer st, this half's 32 columns packed two per
-      // column, once step n - 2's gradient MMAs have read that buffer
-      if (n >= 2 && !warp_wait(e_empty + 8 * st, ph ^ 1u, ctl, ROLE_EPILOGUE)) {
+      // P and dS into their buffer, this half's 32 columns packed two per
+      // column, once step n - 1's gradient MMAs have read it
+      if (n >= 1 &&
+          !warp_wait(e_empty, static_cast<uint32_t>(n - 1) & 1u, ctl,
+                     ROLE_EPILOGUE)) {
         alive = false;
         break;
       }
       ptx::tc_fence_after();
-      tmem_st_32x32b_x16(tmem + lane_base + TMEM_PDS + 64 * st + 16 * hf, pw);
-      tmem_st_32x32b_x16(tmem + lane_base + TMEM_PDS + 64 * st + 32 + 16 * hf,
-                         dw);
+      tmem_st_32x32b_x16(tmem + lane_base + TMEM_PDS + 16 * hf, pw);
+      tmem_st_32x32b_x16(tmem + lane_base + TMEM_PDS + 32 + 16 * hf, dw);
       tmem_st_wait();
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(e_full + 8 * st);
+      if (lane == 0) ptx::mbar_arrive(e_full);
     }
     float rrow = 0.f;
     if constexpr (!KV) {
