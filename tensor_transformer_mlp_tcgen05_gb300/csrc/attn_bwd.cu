@@ -124,10 +124,10 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nq = a.nq;
-  const int rb = KV ? static_cast<int>(blockIdx.x % nq)
-                    : nq - 1 - static_cast<int>(blockIdx.x % nq);
-  const int head = static_cast<int>((blockIdx.x / nq) % a.heads);
-  const int seq = static_cast<int>(blockIdx.x / (nq * a.heads));
+  const CoreItem item = core_item(nq, a.heads, a.hs_group);
+  const int rb = KV ? item.rank : nq - 1 - item.rank;
+  const int head = item.head;
+  const int seq = item.seq;
   const int row0 = seq * a.seq_len + rb * 128;
   // 64-wide column blocks: queries >= the first key (KV), keys <= the last
   // query (Q) when causal.

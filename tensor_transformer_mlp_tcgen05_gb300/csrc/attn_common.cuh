@@ -32,6 +32,32 @@ __device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t bytes) {
   return desc + (bytes >> 4);
 }
 
+// The (sequence, head, block rank) of this CTA of a core kernel (grid =
+// sequences x heads x nq).  CTAs are dealt in groups of hs_group (sequence,
+// head) pairs, about one wave of CTAs, so that a group's K and V stay in L2
+// while its CTAs run; inside a group the CTAs with the most blocks to walk
+// come first (rank 0 = the longest: the last query block of a causal forward
+// or query kernel, the first key block of the key/value kernel), so the
+// short ones fill the end of the launch.  A bijection of the CTA index: each
+// CTA's work, and so every result, does not depend on the grouping.
+struct CoreItem {
+  int rank, head, seq;
+};
+__device__ __forceinline__ CoreItem core_item(int nq, int heads, int hs_group) {
+  const int hs_total = static_cast<int>(gridDim.x) / nq;
+  const int G = hs_group > 0 ? hs_group : 1;
+  const int b = static_cast<int>(blockIdx.x);
+  const int g = b / (G * nq);
+  const int within = b - g * G * nq;
+  const int count = min(G, hs_total - g * G);
+  CoreItem it;
+  it.rank = within / count;
+  const int hs = g * G + within % count;
+  it.head = hs % heads;
+  it.seq = hs / heads;
+  return it;
+}
+
 // Named barrier between the two softmax warps of row quarter q (ids 3-6).
 __device__ __forceinline__ void pair_barrier(int q) {
   asm volatile("bar.sync %0, 64;" ::"r"(3 + q) : "memory");

@@ -84,9 +84,10 @@ __global__ void __launch_bounds__(FWD_THREADS, 2)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nq = a.nq;
-  const int qb = nq - 1 - static_cast<int>(blockIdx.x % nq);
-  const int head = static_cast<int>((blockIdx.x / nq) % a.heads);
-  const int seq = static_cast<int>(blockIdx.x / (nq * a.heads));
+  const CoreItem item = core_item(nq, a.heads, a.hs_group);
+  const int qb = nq - 1 - item.rank;
+  const int head = item.head;
+  const int seq = item.seq;
   const int row0 = seq * a.seq_len + qb * 128;
   const int nk = a.causal ? qb + 1 : nq;
   const HeadCols hc = head_cols(a, head);

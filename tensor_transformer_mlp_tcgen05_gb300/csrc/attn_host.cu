@@ -10,6 +10,7 @@
 //   rowsum(dCtx * Ctx) per head (one CTA per query block) -> dK, dV (one CTA
 //   per key block) -> db_qkv, dW_qkv = Xn^T dQKV, dXn = sum_i dQKV_i W_qkv,i^T
 //   (fixed-order shard sum = f's backward) -> [LayerNorm backward] [+ dZ].
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <new>
@@ -226,11 +227,12 @@ int tp_attn_forward(tp_attn_handle* H, int tokens, const void* X,
   TRY(tc_gemm(&H->core, "gemm_qkv", s, sms, EPI_BIAS_BF16, false, true, ta, tb,
               gq));
   // attention core
-  const AttnArgs aa = core_args(H, ws, L, T);
+  AttnArgs aa = core_args(H, ws, L, T);
   CUtensorMap tqk, tv;
   TRY(encode_map(&tqk, ws + L.qkv, 3ULL * h, T, 3ULL * h, 128));
   TRY(encode_map(&tv, ws + L.qkv, 3ULL * h, T, 3ULL * h, 64));
   const int grid = (T / c.seq_len) * c.heads * aa.nq;
+  aa.hs_group = 1;   // each (sequence, head)'s blocks together, longest first
   TRY(run(&H->core, "attn_fwd", s,
           [&] { return launch_attn_fwd(tqk, tv, aa, grid, s); }));
   // Z = sum_i Ctx_i W_o,i + b_o [+ X]
@@ -330,6 +332,7 @@ int tp_attn_backward(tp_attn_handle* H, int tokens, const void* dZ,
   TRY(encode_map(&tctx128, ctx, h, T, h, 128));
   TRY(out_map(&tdqkv_out, dqkv, false, T, 3 * h, 3LL * h));
   const int grid = (T / c.seq_len) * c.heads * aa.nq;
+  aa.hs_group = std::max(1, sms / aa.nq);   // one backward CTA per SM
   // db_qkv = sum_T dQKV: at d = 128 both kernels write 32-row partials of
   // the chunks they stage for their TMA stores; one fixed-order pass sums them
   float* part3 = part + size_t(L.chunks) * h;

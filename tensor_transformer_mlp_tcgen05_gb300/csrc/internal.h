@@ -166,6 +166,8 @@ struct AttnArgs {
                               // stored values, at colsum[g * ld_colsum + c]
   int* status;
   unsigned long long budget_ns;
+  int hs_group;               // (sequence, head) pairs per scheduling group
+                              // of the core kernels (attn::core_item)
 };
 
 // Forward: tqk maps QKV with 64 x 128 boxes (Q and K tiles), tv with
