@@ -124,7 +124,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nq = a.nq;
-  const CoreItem item = core_item(nq, a.heads, a.hs_group);
+  const CoreItem item =
+      core_item(static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x) / nq,
+                nq, a.heads, a.hs_group);
   const int rb = KV ? item.rank : nq - 1 - item.rank;
   const int head = item.head;
   const int seq = item.seq;

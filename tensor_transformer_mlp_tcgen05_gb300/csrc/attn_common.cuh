@@ -32,21 +32,20 @@ __device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t bytes) {
   return desc + (bytes >> 4);
 }
 
-// The (sequence, head, block rank) of this CTA of a core kernel (grid =
-// sequences x heads x nq).  CTAs are dealt in groups of hs_group (sequence,
-// head) pairs, about one wave of CTAs, so that a group's K and V stay in L2
-// while its CTAs run; inside a group the CTAs with the most blocks to walk
-// come first (rank 0 = the longest: the last query block of a causal forward
-// or query kernel, the first key block of the key/value kernel), so the
-// short ones fill the end of the launch.  A bijection of the CTA index: each
-// CTA's work, and so every result, does not depend on the grouping.
+// The (sequence, head, block rank) of work item b of a core kernel (items =
+// hs_total (sequence, head) pairs x nq blocks).  Items come in groups of
+// hs_group (sequence, head) pairs, about one wave of CTAs, so that a group's
+// K and V stay in L2 while it runs; inside a group the items with the most
+// blocks to walk come first (rank 0 = the longest: the last query block of a
+// causal forward or query kernel, the first key block of the key/value
+// kernel), so the short ones fill the end.  A bijection of the item index:
+// each item's work, and so every result, does not depend on the grouping.
 struct CoreItem {
   int rank, head, seq;
 };
-__device__ __forceinline__ CoreItem core_item(int nq, int heads, int hs_group) {
-  const int hs_total = static_cast<int>(gridDim.x) / nq;
+__device__ __forceinline__ CoreItem core_item(int b, int hs_total, int nq,
+                                              int heads, int hs_group) {
   const int G = hs_group > 0 ? hs_group : 1;
-  const int b = static_cast<int>(blockIdx.x);
   const int g = b / (G * nq);
   const int within = b - g * G * nq;
   const int count = min(G, hs_total - g * G);
@@ -161,6 +160,20 @@ __device__ __forceinline__ void tmem_st_wait() {
 // Named barrier among the softmax warps only.
 __device__ __forceinline__ void softmax_barrier() {
   asm volatile("bar.sync 2, %0;" ::"n"(SOFTMAX_WARPS * 32) : "memory");
+}
+
+// The same barrier, ANDing a predicate over the softmax warps: every warp
+// leaves with the same answer (a persistent kernel's warps agree on whether
+// to go on to the next item, so none waits at a named barrier alone).
+__device__ __forceinline__ bool softmax_barrier_and(bool p) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\t"
+      "bar.red.and.pred po, 2, %2, pi;\n\tselp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"(p ? 1u : 0u), "n"(SOFTMAX_WARPS * 32)
+      : "memory");
+  return r != 0;
 }
 
 // Warp-uniform bounded wait (every lane polls; the result is agreed).

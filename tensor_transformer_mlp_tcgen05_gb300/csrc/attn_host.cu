@@ -231,8 +231,11 @@ int tp_attn_forward(tp_attn_handle* H, int tokens, const void* X,
   CUtensorMap tqk, tv;
   TRY(encode_map(&tqk, ws + L.qkv, 3ULL * h, T, 3ULL * h, 128));
   TRY(encode_map(&tv, ws + L.qkv, 3ULL * h, T, 3ULL * h, 64));
-  const int grid = (T / c.seq_len) * c.heads * aa.nq;
-  aa.hs_group = 1;   // each (sequence, head)'s blocks together, longest first
+  // persistent forward: two CTAs per SM walk the items, one group of
+  // (sequence, head) pairs per round
+  const int items = (T / c.seq_len) * c.heads * aa.nq;
+  const int grid = std::min(items, 2 * sms);
+  aa.hs_group = std::max(1, grid / aa.nq);
   TRY(run(&H->core, "attn_fwd", s,
           [&] { return launch_attn_fwd(tqk, tv, aa, grid, s); }));
   // Z = sum_i Ctx_i W_o,i + b_o [+ X]
