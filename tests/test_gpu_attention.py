@@ -2,7 +2,8 @@
 binding) against the fp64 oracle in ``oracle/attention.py``.
 
 Element-by-element comparisons on seeded inputs at sizes the oracle finishes
-in seconds (several 128-row blocks per sequence, two sequences, shards 1-4,
+in seconds (several 128-row blocks per sequence, two to forty sequences
+(more query blocks than the persistent forward has CTAs), shards 1-4,
 head dims 64, 96 and 128, causal and not, with and without LayerNorm, biases and
 the residual), plus bitwise repeatability and the empty call."""
 import math
@@ -127,6 +128,11 @@ CASES = [
     ("d96_causal_t4_ln_res", dict(shards=4, layernorm=True), True, True),
     ("d96_full_t2_ln", dict(causal=False, layernorm=True), True, False),
     ("d96_causal_peaked", dict(seq=384, batch=1), "sign", False),
+    # more (sequence, head, query block) items than the persistent forward
+    # has CTAs (two per SM): a CTA walks several items, in rounds
+    ("d64_causal_items320", dict(batch=40), True, False),
+    ("d96_full_t4_items320", dict(batch=20, causal=False, shards=4), False,
+     False),
 ]
 
 
