@@ -1,8 +1,9 @@
 // Attention core of the head-parallel self-attention block on sm_103a.
 //
 // The heads are independent (Megatron-LM explainer, section on attention;
-// notes, "Self-attention block split"), so each CTA owns one (sequence,
-// head, 128-query block) and never communicates.  Q, K and V are read in
+// notes, "Self-attention block split"), so each (sequence, head, 128-query
+// block) item is computed on its own and no CTA communicates with another.
+// Q, K and V are read in
 // place from the fused projection output QKV [T, 3h] (columns grouped by
 // shard: [Q_i | K_i | V_i], head j of shard i at offset (j mod H/t) d inside
 // each group) through TMA tensor maps; scores, probabilities and the output

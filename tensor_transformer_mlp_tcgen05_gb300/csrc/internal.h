@@ -171,7 +171,9 @@ struct AttnArgs {
 };
 
 // Forward: tqk maps QKV with 64 x 128 boxes (Q and K tiles), tv with
-// 64 x 64 boxes (V tiles, M/N-major operand).  grid = batches * H * nq.
+// 64 x 64 boxes (V tiles, M/N-major operand).  Persistent: any grid of at
+// least one CTA walks the batches * H * nq items (the host launches two CTAs
+// per SM, at most one per item).
 cudaError_t launch_attn_fwd(const CUtensorMap& tqk, const CUtensorMap& tv,
                             const AttnArgs& a, int grid, cudaStream_t stream);
 
