@@ -42,6 +42,26 @@ def test_wait_timeout_is_reported_and_context_survives():
     m.close()
 
 
+def test_layernorm_prologue_wait_timeout_is_reported_and_context_survives():
+    """The same with the LayerNorm inside GEMM1's launch: the producers' waits
+    for the normalised row blocks give up with the rest, and afterwards the
+    same handle computes the block (LayerNorm included) correctly."""
+    w = W.Workload("timeout_ln", 1000, 512, 2048, 2, "bf16", True, True)
+    inp = W.make_inputs(w, seed=33, with_bias=True)
+    d = {k: to_dev(v) for k, v in inp.items()}
+    m = TensorParallelMLP(w.hidden, w.ffn, w.shards, w.tokens, layernorm=True)
+    B.tp_mlp_set_wait_budget(m.handle, 1)
+    m.forward(d["X"], d["A"], d["B"], d["b1"], d["b2"], d["gamma"], d["beta"])
+    rc = m.check()
+    assert rc == B.TPMLP_ERR_TIMEOUT, (rc, B.tp_mlp_last_detail())
+    B.tp_mlp_set_wait_budget(m.handle, 2_000_000_000)
+    Z = m.forward(d["X"], d["A"], d["B"], d["b1"], d["b2"], d["gamma"],
+                  d["beta"])
+    assert m.check() == B.TPMLP_OK
+    assert_close("Z after timeout", Z.cpu(), oracle_full(inp, backward=False)["Z"])
+    m.close()
+
+
 def test_attention_wait_timeout_is_reported_and_context_survives():
     """The same for the attention block: every bounded wait in the attention
     forward and backward kernels (and their GEMMs) gives up at once, the
@@ -51,7 +71,9 @@ def test_attention_wait_timeout_is_reported_and_context_survives():
     from tensor_transformer_mlp_tcgen05_gb300.attention import \
         TensorParallelAttention
     from parity_helpers import f64
-    w = W.ATTN_WORKLOADS["attn_tiny_d128"]
+    # 40 sequences: 320 query-block items, more than the persistent forward
+    # has CTAs, so CTAs that give up leave items of theirs unwalked
+    w = W.ATTN_WORKLOADS["attn_tiny_d64"].with_(batch=40)
     inp = W.make_attn_inputs(w, seed=32, with_bias=True)
     d = {k: to_dev(v) for k, v in inp.items()}
     m = TensorParallelAttention(w.hidden, w.heads, w.shards, w.tokens, w.seq)
