@@ -38,9 +38,8 @@
 // 48 cycles; with A in tensor memory, 2 KB and 32 cycles).
 // Outputs leave as 32-row x 64-column bf16 chunks staged in the idle B ring
 // and stored by TMA (at d = 96 the last 32 columns of dK and dV, and dQ,
-// with plain 16-byte stores); at d = 128 each chunk is also summed over its
-// 32 rows
-// into the partials of the QKV bias gradient.
+// with plain 16-byte stores); at d = 64 and 128 each chunk is also summed
+// over its 32 rows into the partials of the QKV bias gradient.
 //
 // Warp roles: warp 0 TMA producer, warp 1 TMEM allocator and issuer of the
 // score MMAs, warp 2 issuer of the gradient MMAs (each the whole warp, one
@@ -575,36 +574,39 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                           v);
         }
         st.drain(lane);
-      } else if constexpr (D == 128) {
-        // dQ: each warp its 32 rows x 64 columns (one chunk), staged and
-        // stored by TMA like the key/value outputs
-        ChunkStager st{sB + static_cast<uint32_t>(warp - SOFTMAX_WARP0) * 2u *
-                                STAGE_CHUNK_BYTES,
-                       0u};
-        const uint32_t src2 = tmem + lane_base + TMEM_OUT2 + hf * 64;
-        const uint32_t src1 = tmem + lane_base + TMEM_OUT1 + hf * 64;
-        uint32_t w[32];
+      } else if constexpr (D == 128 || D == 64) {
+        // dQ: each warp its 32 rows x 64 columns (one chunk; at d = 64 the
+        // first column half's warps hold all of them), staged and stored by
+        // TMA like the key/value outputs
+        if (hf * 64 < D) {
+          ChunkStager st{sB + static_cast<uint32_t>(warp - SOFTMAX_WARP0) * 2u *
+                                  STAGE_CHUNK_BYTES,
+                         0u};
+          const uint32_t src2 = tmem + lane_base + TMEM_OUT2 + hf * 64;
+          const uint32_t src1 = tmem + lane_base + TMEM_OUT1 + hf * 64;
+          uint32_t w[32];
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          uint32_t ov[32], kv[32];
-          ptx::tmem_ld_32x32b_x32(src2 + 32 * j, ov);
-          ptx::tmem_ld_32x32b_x32(src1 + 32 * j, kv);
-          ptx::tmem_ld_wait();
+          for (int j = 0; j < 2; ++j) {
+            uint32_t ov[32], kv[32];
+            ptx::tmem_ld_32x32b_x32(src2 + 32 * j, ov);
+            ptx::tmem_ld_32x32b_x32(src1 + 32 * j, kv);
+            ptx::tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            w[16 * j + i] = pack_bf16x2(
-                fmaf(-rrow, __uint_as_float(kv[2 * i]), __uint_as_float(ov[2 * i])),
-                fmaf(-rrow, __uint_as_float(kv[2 * i + 1]),
-                     __uint_as_float(ov[2 * i + 1])));
+            for (int i = 0; i < 16; ++i)
+              w[16 * j + i] = pack_bf16x2(
+                  fmaf(-rrow, __uint_as_float(kv[2 * i]), __uint_as_float(ov[2 * i])),
+                  fmaf(-rrow, __uint_as_float(kv[2 * i + 1]),
+                       __uint_as_float(ov[2 * i + 1])));
+          }
+          const uint32_t buf = st.put(&tmOut, hc.q + 64 * hf, row0 + q * 32, w, lane);
+          if (a.colsum != nullptr) {
+            const float2 cs = chunk_colsum_bf16(buf, lane);
+            *reinterpret_cast<float2*>(
+                a.colsum + static_cast<size_t>((row0 + q * 32) / 32) * a.ld_colsum +
+                hc.q + 64 * hf + 2 * lane) = cs;
+          }
+          st.drain(lane);
         }
-        const uint32_t buf = st.put(&tmOut, hc.q + 64 * hf, row0 + q * 32, w, lane);
-        if (a.colsum != nullptr) {
-          const float2 cs = chunk_colsum_bf16(buf, lane);
-          *reinterpret_cast<float2*>(
-              a.colsum + static_cast<size_t>((row0 + q * 32) / 32) * a.ld_colsum +
-              hc.q + 64 * hf + 2 * lane) = cs;
-        }
-        st.drain(lane);
       } else {
         // dQ: this warp's D / 2 columns of its row, 16 at a time
         __nv_bfloat16* out2 = a.dqkv + static_cast<size_t>(row0 + r) * a.ld_qkv +

@@ -336,10 +336,12 @@ int tp_attn_backward(tp_attn_handle* H, int tokens, const void* dZ,
   TRY(out_map(&tdqkv_out, dqkv, false, T, 3 * h, 3LL * h));
   const int grid = (T / c.seq_len) * c.heads * aa.nq;
   aa.hs_group = std::max(1, sms / aa.nq);   // one backward CTA per SM
-  // db_qkv = sum_T dQKV: at d = 128 both kernels write 32-row partials of
-  // the chunks they stage for their TMA stores; one fixed-order pass sums them
+  // db_qkv = sum_T dQKV: at d = 64 and 128 both kernels write 32-row
+  // partials of the chunks they stage for their TMA stores; one fixed-order
+  // pass sums them
   float* part3 = part + size_t(L.chunks) * h;
-  const bool fused_dbqkv = dbqkv != nullptr && c.hidden / c.heads == 128;
+  const bool fused_dbqkv = dbqkv != nullptr &&
+                           (c.hidden / c.heads == 128 || c.hidden / c.heads == 64);
   if (fused_dbqkv) {
     aa.colsum = part3;
     aa.ld_colsum = 3LL * h;
