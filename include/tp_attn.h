@@ -133,6 +133,17 @@ int tp_attn_set_wait_budget(tp_attn_handle* handle, unsigned long long ns);
 /* NVTX ranges around each launch, as tp_mlp_set_nvtx. */
 int tp_attn_set_nvtx(tp_attn_handle* handle, int enable);
 
+/* Enable (1, the default) or disable (0) the fused pre-LayerNorm prologue
+ * of the forward (pre-LN placement: Megatron-LM explainer, "Fixing BERT:
+ * reordering layer normalisation for scaling"), as tp_mlp_set_ln_prologue
+ * for the MLP block: with use_layernorm and hidden = 256 v for v <= 24, the
+ * QKV projection's launch normalises the token rows itself (its epilogue
+ * warps, before their first tile) and loads each 128-row block of its A
+ * operand once written; otherwise a stand-alone LayerNorm kernel runs
+ * first.  Both compute the same bits.  TPMLP_ERR_ARG for a NULL handle or
+ * another value. */
+int tp_attn_set_ln_prologue(tp_attn_handle* handle, int enable);
+
 /* Offsets in bytes, inside a workspace laid out for (tokens, training), of
  * the saved QKV [T,3h] bf16, Ctx [T,h] bf16, log-sum-exp [H,T] fp32 and
  * (training layouts only) dQKV [T,3h] bf16, for inspection by tests; -1 for

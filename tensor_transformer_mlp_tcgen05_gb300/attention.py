@@ -17,13 +17,16 @@ class TensorParallelAttention:
 
     def __init__(self, hidden: int, heads: int, shards: int, max_tokens: int,
                  seq_len: int, causal: bool = True, layernorm: bool = False,
-                 ln_eps: float = 1e-5, residual: bool = False, device=None):
+                 ln_eps: float = 1e-5, residual: bool = False, device=None,
+                 ln_prologue: bool = True):
         self.cfg = B_.tp_attn_config(
             hidden=hidden, heads=heads, shards=shards, max_tokens=max_tokens,
             seq_len=seq_len, causal=1 if causal else 0,
             use_layernorm=1 if layernorm else 0, ln_eps=ln_eps,
             use_residual=1 if residual else 0)
         self.handle = B_.tp_attn_create(self.cfg)
+        if not ln_prologue:   # the LayerNorm as its own launch before QKV
+            B_.tp_attn_set_ln_prologue(self.handle, False)
         self.hidden, self.heads, self.shards = hidden, heads, shards
         self.seq_len = seq_len
         self.layernorm = layernorm

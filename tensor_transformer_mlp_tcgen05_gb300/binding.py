@@ -52,6 +52,7 @@ EXPORTED = (
     "tp_attn_forward", "tp_attn_backward", "tp_attn_check",
     "tp_attn_launch_count", "tp_attn_set_timing", "tp_attn_timing_get",
     "tp_attn_timing_reset", "tp_attn_set_wait_budget", "tp_attn_set_nvtx",
+    "tp_attn_set_ln_prologue",
     "tp_attn_workspace_offset",
 )
 
@@ -213,6 +214,8 @@ def lib(path: str | None = None) -> ctypes.CDLL:
     L.tp_attn_timing_reset.restype = _i
     L.tp_attn_set_nvtx.argtypes = [_vp, _i]
     L.tp_attn_set_nvtx.restype = _i
+    L.tp_attn_set_ln_prologue.argtypes = [_vp, _i]
+    L.tp_attn_set_ln_prologue.restype = _i
     L.tp_attn_set_wait_budget.argtypes = [_vp, ctypes.c_ulonglong]
     L.tp_attn_set_wait_budget.restype = _i
     if path is None:
@@ -515,6 +518,11 @@ def tp_attn_timing_reset(handle) -> None:
 
 def tp_attn_set_nvtx(handle, enable: bool) -> None:
     _check(lib().tp_attn_set_nvtx(handle, 1 if enable else 0), "tp_attn_set_nvtx")
+
+
+def tp_attn_set_ln_prologue(handle, enable: bool) -> None:
+    _check(lib().tp_attn_set_ln_prologue(handle, 1 if enable else 0),
+           "tp_attn_set_ln_prologue")
 
 
 def tp_attn_set_wait_budget(handle, ns: int) -> None:

@@ -27,6 +27,7 @@ struct AttnLayout {
   size_t status = 0, xn = 0, mean = 0, rstd = 0, qkv = 0, ctx = 0, lse = 0,
          dctx = 0, delta = 0, dqkv = 0, dxn = 0, part = 0, tailp = 0,
          total = 0, lnp = 0;
+  size_t lnsync_words = 0;   // the LayerNorm prologue's counters
   int chunks = 0;   // 256-row column-sum chunks
   int groups = 0;   // 32-row groups of the core kernels' fused db_qkv partials
 };
@@ -44,7 +45,14 @@ AttnLayout attn_layout(const tp_attn_config& c, int tokens, int training) {
     off = align_up(off + bytes, 256);
     return o;
   };
-  L.status = take(256);
+  if (c.use_layernorm) {
+    // the status word, then the LayerNorm prologue's row counters
+    // (GemmArgs::ln_sync: 1 + ceil(T / 128) words)
+    L.lnsync_words = 1 + (T + 127) / 128;
+    L.status = take(16 + 4 * L.lnsync_words);
+  } else {
+    L.status = take(256);
+  }
   if (c.use_layernorm) {
     L.xn = take(T * h * 2);
     L.mean = take(T * 4);
@@ -77,6 +85,7 @@ AttnLayout attn_layout(const tp_attn_config& c, int tokens, int training) {
 struct tp_attn_handle {
   HandleCore core;
   tp_attn_config cfg;
+  bool ln_prologue = true;   // tp_attn_set_ln_prologue
 };
 
 namespace {
@@ -198,7 +207,12 @@ int tp_attn_forward(tp_attn_handle* H, int tokens, const void* X,
   TRY(check_device(&sms));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
-  cudaError_t e = cudaMemsetAsync(ws + L.status, 0, 16, s);
+  // LayerNorm inside the QKV projection's launch (GemmArgs::ln_x)
+  const bool ln_fused = c.use_layernorm && H->ln_prologue &&
+                        c.hidden % 256 == 0 && c.hidden / 256 <= LN_VMAX;
+  // the status word, and with the fused LayerNorm its counters, cleared
+  const size_t clear = ln_fused ? 16 + 4 * L.lnsync_words : 16;
+  cudaError_t e = cudaMemsetAsync(ws + L.status, 0, clear, s);
   if (e != cudaSuccess) {
     set_detail("cudaMemsetAsync(status)", e);
     return TPMLP_ERR_CUDA;
@@ -207,7 +221,9 @@ int tp_attn_forward(tp_attn_handle* H, int tokens, const void* X,
 
   const int T = tokens, h = c.hidden, ht = h / c.shards;
   const void* Xop = X;
-  if (c.use_layernorm) {
+  if (ln_fused) {
+    Xop = ws + L.xn;
+  } else if (c.use_layernorm) {
     void* Xn = ws + L.xn;
     TRY(run(&H->core, "layernorm_fwd", s, [&] {
       return launch_ln_fwd(true, X, ln_gamma, ln_beta, Xn,
@@ -222,10 +238,20 @@ int tp_attn_forward(tp_attn_handle* H, int tokens, const void* X,
   GemmArgs gq = gemm_args(H, ws, L);
   gq.M = T; gq.N = 3 * h; gq.K = h; gq.kb_per_seg = h / TC_BK;
   gq.out = ws + L.qkv; gq.ldo = 3LL * h; gq.bias = bqkv;
+  if (ln_fused) {
+    gq.ln_x = static_cast<const __nv_bfloat16*>(X);
+    gq.ln_gamma = ln_gamma;
+    gq.ln_beta = ln_beta;
+    gq.ln_xn = reinterpret_cast<__nv_bfloat16*>(ws + L.xn);
+    gq.ln_mean = reinterpret_cast<float*>(ws + L.mean);
+    gq.ln_rstd = reinterpret_cast<float*>(ws + L.rstd);
+    gq.ln_eps = c.ln_eps;
+    gq.ln_sync = reinterpret_cast<unsigned int*>(ws + L.status + 16);
+  }
   TRY(kmajor_map(&ta, Xop, T, h, TC_BM));
   TRY(mnmajor_map(&tb, Wqkv, h, 3 * h));
-  TRY(tc_gemm(&H->core, "gemm_qkv", s, sms, EPI_BIAS_BF16, false, true, ta, tb,
-              gq));
+  TRY(tc_gemm(&H->core, ln_fused ? "gemm_ln_qkv" : "gemm_qkv", s, sms,
+              EPI_BIAS_BF16, false, true, ta, tb, gq));
   // attention core
   AttnArgs aa = core_args(H, ws, L, T);
   CUtensorMap tqk, tv;
@@ -428,6 +454,12 @@ int tp_attn_timing_reset(tp_attn_handle* H) {
 int tp_attn_set_nvtx(tp_attn_handle* handle, int enable) {
   if (handle == nullptr || (enable != 0 && enable != 1)) return TPMLP_ERR_ARG;
   handle->core.nvtx = enable != 0;
+  return TPMLP_OK;
+}
+
+int tp_attn_set_ln_prologue(tp_attn_handle* handle, int enable) {
+  if (handle == nullptr || (enable != 0 && enable != 1)) return TPMLP_ERR_ARG;
+  handle->ln_prologue = enable != 0;
   return TPMLP_OK;
 }
 

@@ -77,8 +77,8 @@ struct GemmArgs {
   float* part;
   long long part_bytes;
   int tail, pieces, nslots;
-  // Fused LayerNorm prologue (EPI_GELU_FWD with K-major bf16 A; ln_x null =
-  // off).  The A tensor map points at ln_xn.  The epilogue warps of every
+  // Fused LayerNorm prologue (EPI_GELU_FWD or EPI_BIAS_BF16 with K-major
+  // bf16 A and M/N-major B; ln_x null = off).  The A tensor map points at ln_xn.  The epilogue warps of every
   // CTA first normalise rows of ln_x [M, K] (K = 256 vpl, vpl <= LN_VMAX)
   // into ln_xn and write ln_mean / ln_rstd, claiming one or two rows at a
   // time from ln_sync[0]; after a claim's rows are written they add their

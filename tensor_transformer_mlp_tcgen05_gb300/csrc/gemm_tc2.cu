@@ -215,6 +215,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // The fused LayerNorm prologue is compiled only into the GEMMs that take
+  // it: the first GEMM of the MLP block and the attention block's QKV
+  // projection (K-major bf16 A, B M/N-major).
+  constexpr bool LN_PROLOGUE = (EPI == EPI_GELU_FWD || EPI == EPI_BIAS_BF16) &&
+                               !A_MN && B_MN && !F8;
   // Work is dealt to groups of four CTAs (two pairs, two clusters) in
   // blockIdx order: a group owns a 512 x 256 "super-tile", its pairs the
   // upper and lower 256 x 256 tiles, which read the same B columns at about
@@ -280,7 +285,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int mb = 2 * msup + pg;   // may lie past M: zero-filled, unused
         const int m0 = mb * PM + static_cast<int>(prank) * HM;
         const int n0 = nb * PN + static_cast<int>(prank) * HN;
-        if constexpr (EPI == EPI_GELU_FWD && !A_MN && !F8) {
+        if constexpr (LN_PROLOGUE) {
           // fused LayerNorm: this CTA's 128 A rows must all be written
           if (args.ln_x != nullptr && m0 < args.M &&
               !wait_count(args.ln_sync + 1 + m0 / HM,
@@ -411,7 +416,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else {
     ptx::setmaxnreg_inc<REGS_EPILOGUE>();
-    if constexpr (EPI == EPI_GELU_FWD && !A_MN && !F8) {
+    if constexpr (LN_PROLOGUE) {
       // ------------------------------------ fused LayerNorm prologue --
       // gamma and beta go to the staging buffers (not yet in use: the
       // epilogue starts after the second barrier), read from there by

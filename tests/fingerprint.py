@@ -44,7 +44,7 @@ MLP_KERNEL = {
 ATTN_ORDER = ["QKV", "Ctx", "lse", "Z", "dbo", "dWo", "dQKV", "dbqkv", "dWqkv",
               "dX", "dgamma", "dbeta"]
 ATTN_KERNEL = {
-    "QKV": "gemm_qkv", "Ctx": "attn_fwd", "lse": "attn_fwd",
+    "QKV": "gemm_qkv / gemm_ln_qkv", "Ctx": "attn_fwd", "lse": "attn_fwd",
     "Z": "gemm_out_shardsum", "dbo": "colsum_dbo", "dWo": "gemm_wgrad_dWo",
     "dQKV": "attn_bwd_dq (dQ) / attn_bwd_dkdv (dK, dV)",
     "dbqkv": "attn_bwd_* partials + colsum_finalize (or colsum_dbqkv)",

@@ -240,6 +240,7 @@ def test_gelu_probe_rejects_bad_arguments(lib):
 
 def test_ln_prologue_switch_validates_arguments(lib):
     assert lib.tp_mlp_set_ln_prologue(None, 1) == B.TPMLP_ERR_ARG
+    assert lib.tp_attn_set_ln_prologue(None, 1) == B.TPMLP_ERR_ARG
     h = B.tp_mlp_create(B.tp_mlp_config(hidden=256, ffn=1024, shards=4,
                                         max_tokens=64, dtype=B.TPMLP_BF16,
                                         use_layernorm=1, ln_eps=1e-5))

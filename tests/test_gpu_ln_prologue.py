@@ -159,3 +159,52 @@ def test_megatron_8p3b_fused_equals_standalone():
     # (GEMM2's tail split adds its combine launch on both paths)
     assert n_b == n_a + 1 and "layernorm_fwd" not in names_a
     assert_bitwise(a, b, MLP_ORDER, MLP_KERNEL)
+
+
+def _run_attn(w, inp, fused):
+    from tensor_transformer_mlp_tcgen05_gb300 import binding as B
+    from tensor_transformer_mlp_tcgen05_gb300.attention import \
+        TensorParallelAttention
+    m = TensorParallelAttention(w.hidden, w.heads, w.shards, w.tokens, w.seq,
+                                causal=w.causal, layernorm=True,
+                                residual=True, ln_prologue=fused)
+    d = {k: (None if v is None else v.cuda().contiguous())
+         for k, v in inp.items()}
+    B.tp_attn_set_timing(m.handle, True)
+    Z = m.forward(d["X"], d["Wqkv"], d["Wo"], d["bqkv"], d["bo"], d["gamma"],
+                  d["beta"])
+    n_fwd = B.tp_attn_launch_count(m.handle)
+    g = m.backward(d["dZ"], d["X"], d["Wqkv"], d["Wo"], d["gamma"])
+    rc = m.check()
+    assert rc == 0, (rc, B.tp_mlp_last_detail())
+    names = [n for n, _, _ in B.tp_attn_timing_get(m.handle)]
+    out = {"Z": Z, **g}
+    torch.cuda.synchronize()
+    out = {k: v.cpu() for k, v in out.items()}
+    m.close()
+    return out, n_fwd, names
+
+
+@pytest.mark.parametrize("name,over", [
+    ("attn_tiny_d64", {}),
+    ("attn_tiny_d96", dict(causal=False, shards=4)),
+    ("attn_tiny_d128", dict(batch=3)),
+    ("attn_megatron_8p3b", {}),
+])
+def test_attention_fused_prologue_is_bitwise_the_standalone_layernorm(name,
+                                                                     over):
+    """The attention block's QKV projection with the same prologue (pre-LN
+    sub-block with the residual): every output bitwise equal to the
+    stand-alone LayerNorm path, one launch fewer in the forward."""
+    from fingerprint import ATTN_KERNEL, ATTN_ORDER
+    w = W.ATTN_WORKLOADS[name].with_(layernorm=True, **over)
+    inp = W.make_attn_inputs(w, seed=17, with_bias=True)
+    g = torch.Generator().manual_seed(18)
+    inp["gamma"] = 1 + 0.2 * torch.randn(w.hidden, generator=g)
+    inp["beta"] = 0.2 * torch.randn(w.hidden, generator=g)
+    a, n_a, names_a = _run_attn(w, inp, True)
+    b, n_b, names_b = _run_attn(w, inp, False)
+    assert n_b == n_a + 1, (n_a, n_b)
+    assert "gemm_ln_qkv" in names_a and "layernorm_fwd" not in names_a
+    assert "layernorm_fwd" in names_b
+    assert_bitwise(a, b, ATTN_ORDER, ATTN_KERNEL)
