@@ -37,9 +37,9 @@
 // needs 6 KB per instruction and runs at the shared-memory operand rate,
 // 48 cycles; with A in tensor memory, 2 KB and 32 cycles).
 // Outputs leave as 32-row x 64-column bf16 chunks staged in the idle B ring
-// and stored by TMA (at d = 96 the last 32 columns of dK and dV, and dQ,
-// with plain 16-byte stores); at d = 64 and 128 each chunk is also summed
-// over its 32 rows into the partials of the QKV bias gradient.
+// and stored by TMA (at d = 96 the last 32 columns of dK, dV and dQ with
+// plain 16-byte stores); each chunk, and each such 32-column tail, is also
+// summed over its 32 rows into the partials of the QKV bias gradient.
 //
 // Warp roles: warp 0 TMA producer, warp 1 TMEM allocator and issuer of the
 // score MMAs, warp 2 issuer of the gradient MMAs (each the whole warp, one
@@ -572,6 +572,72 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             store_bf16x32(a.dqkv + static_cast<size_t>(row0 + r) * a.ld_qkv +
                               col + 64 * (D / 64),
                           v);
+          if (a.colsum != nullptr) {     // their bias-gradient partials
+            const float2 cs = tail_colsum_bf16(st, v, lane);
+            if (lane < 16)
+              *reinterpret_cast<float2*>(
+                  a.colsum +
+                  static_cast<size_t>((row0 + q * 32) / 32) * a.ld_colsum +
+                  col + 64 * (D / 64) + 2 * lane) = cs;
+          }
+        }
+        st.drain(lane);
+      } else if constexpr (D == 96) {
+        // dQ: the first column half's warps 64 columns as one chunk (staged,
+        // stored by TMA, summed for the bias-gradient partials), the second
+        // half's warps the last 32 columns with 16-byte stores of their rows
+        ChunkStager st{sB + static_cast<uint32_t>(warp - SOFTMAX_WARP0) * 2u *
+                                STAGE_CHUNK_BYTES,
+                       0u};
+        const uint32_t src2 = tmem + lane_base + TMEM_OUT2 + hf * 64;
+        const uint32_t src1 = tmem + lane_base + TMEM_OUT1 + hf * 64;
+        if (hf == 0) {
+          uint32_t w[32];
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            uint32_t ov[32], kv[32];
+            ptx::tmem_ld_32x32b_x32(src2 + 32 * j, ov);
+            ptx::tmem_ld_32x32b_x32(src1 + 32 * j, kv);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              w[16 * j + i] = pack_bf16x2(
+                  fmaf(-rrow, __uint_as_float(kv[2 * i]),
+                       __uint_as_float(ov[2 * i])),
+                  fmaf(-rrow, __uint_as_float(kv[2 * i + 1]),
+                       __uint_as_float(ov[2 * i + 1])));
+          }
+          const uint32_t buf = st.put(&tmOut, hc.q, row0 + q * 32, w, lane);
+          if (a.colsum != nullptr) {
+            const float2 cs = chunk_colsum_bf16(buf, lane);
+            *reinterpret_cast<float2*>(
+                a.colsum +
+                static_cast<size_t>((row0 + q * 32) / 32) * a.ld_colsum +
+                hc.q + 2 * lane) = cs;
+          }
+        } else {
+          uint32_t ov[32], kv[32];
+          ptx::tmem_ld_32x32b_x32(src2, ov);
+          ptx::tmem_ld_32x32b_x32(src1, kv);
+          ptx::tmem_ld_wait();
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            v[i] = fmaf(-rrow, __uint_as_float(kv[i]), __uint_as_float(ov[i]));
+          __nv_bfloat16* out2 =
+              a.dqkv + static_cast<size_t>(row0 + r) * a.ld_qkv + hc.q + 64;
+          if (TPMLP_CHECK(__all_sync(0xffffffffu,
+                                     (reinterpret_cast<uintptr_t>(out2) & 15u) == 0),
+                          a.status, abort_flag, SITE_ATTN_BWD_STORE))
+            store_bf16x32(out2, v);
+          if (a.colsum != nullptr) {
+            const float2 cs = tail_colsum_bf16(st, v, lane);
+            if (lane < 16)
+              *reinterpret_cast<float2*>(
+                  a.colsum +
+                  static_cast<size_t>((row0 + q * 32) / 32) * a.ld_colsum +
+                  hc.q + 64 + 2 * lane) = cs;
+          }
         }
         st.drain(lane);
       } else if constexpr (D == 128 || D == 64) {

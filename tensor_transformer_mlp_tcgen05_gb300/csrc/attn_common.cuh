@@ -57,6 +57,33 @@ __device__ __forceinline__ CoreItem core_item(int b, int hs_total, int nq,
   return it;
 }
 
+// The fp32 column sums over a warp's 32 rows (in row order) of 32 bf16
+// columns that the warp stores itself (the last 32 columns of a d = 96 head,
+// which a 64-column chunk store would overrun): each lane's row is written,
+// as the first half of a 128-byte-swizzled chunk row, into the stager's next
+// buffer once earlier stores have read it, and summed like a staged chunk.
+// Lanes 0-15 get columns 2l and 2l + 1; the buffer is free again on return.
+__device__ __forceinline__ float2 tail_colsum_bf16(const gemm::ChunkStager& st,
+                                                   const float (&v)[32],
+                                                   int lane) {
+  const uint32_t buf = st.buffer(0);   // the buffer put two chunks ago
+  if (lane == 0) ptx::bulk_wait_read<1>();
+  __syncwarp();
+  const uint32_t row = buf + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint32_t u = static_cast<uint32_t>(c ^ (lane & 7));
+    ptx::st_shared_v4(row + u * 16u, pack_bf16x2(v[8 * c], v[8 * c + 1]),
+                      pack_bf16x2(v[8 * c + 2], v[8 * c + 3]),
+                      pack_bf16x2(v[8 * c + 4], v[8 * c + 5]),
+                      pack_bf16x2(v[8 * c + 6], v[8 * c + 7]));
+  }
+  __syncwarp();
+  const float2 cs = gemm::chunk_colsum_bf16(buf, lane);
+  __syncwarp();
+  return cs;
+}
+
 // Named barrier between the two softmax warps of row quarter q (ids 3-6).
 __device__ __forceinline__ void pair_barrier(int q) {
   asm volatile("bar.sync %0, 64;" ::"r"(3 + q) : "memory");

@@ -362,12 +362,11 @@ int tp_attn_backward(tp_attn_handle* H, int tokens, const void* dZ,
   TRY(out_map(&tdqkv_out, dqkv, false, T, 3 * h, 3LL * h));
   const int grid = (T / c.seq_len) * c.heads * aa.nq;
   aa.hs_group = std::max(1, sms / aa.nq);   // one backward CTA per SM
-  // db_qkv = sum_T dQKV: at d = 64 and 128 both kernels write 32-row
-  // partials of the chunks they stage for their TMA stores; one fixed-order
-  // pass sums them
+  // db_qkv = sum_T dQKV: both kernels write 32-row partials of what they
+  // store (the chunks they stage for their TMA stores, and at d = 96 the
+  // 32-column tails); one fixed-order pass sums them
   float* part3 = part + size_t(L.chunks) * h;
-  const bool fused_dbqkv = dbqkv != nullptr &&
-                           (c.hidden / c.heads == 128 || c.hidden / c.heads == 64);
+  const bool fused_dbqkv = dbqkv != nullptr;
   if (fused_dbqkv) {
     aa.colsum = part3;
     aa.ld_colsum = 3LL * h;
@@ -384,8 +383,6 @@ int tp_attn_backward(tp_attn_handle* H, int tokens, const void* dZ,
     TRY(run(&H->core, "colsum_finalize", s, [&] {
       return launch_colsum_finalize(part3, dbqkv, L.groups, 3 * h, s);
     }));
-  } else if (dbqkv) {
-    TRY(colsum(&H->core, "colsum_dbqkv", s, true, dqkv, part3, dbqkv, T, 3 * h));
   }
   // dW_qkv = Xn^T dQKV
   GemmArgs gwq = gemm_args(H, ws, L);

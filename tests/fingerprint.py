@@ -47,7 +47,7 @@ ATTN_KERNEL = {
     "QKV": "gemm_qkv / gemm_ln_qkv", "Ctx": "attn_fwd", "lse": "attn_fwd",
     "Z": "gemm_out_shardsum", "dbo": "colsum_dbo", "dWo": "gemm_wgrad_dWo",
     "dQKV": "attn_bwd_dq (dQ) / attn_bwd_dkdv (dK, dV)",
-    "dbqkv": "attn_bwd_* partials + colsum_finalize (or colsum_dbqkv)",
+    "dbqkv": "attn_bwd_* partials + colsum_finalize",
     "dWqkv": "gemm_wgrad_dWqkv",
     "dX": "gemm_dx_shardsum (with LayerNorm: layernorm_bwd)",
     "dgamma": "layernorm_param_partial", "dbeta": "layernorm_param_partial",
