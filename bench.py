@@ -61,42 +61,64 @@ DEFAULT_WORKLOAD = "gpt3_13b"
 # "attn": the attention core).  Reported as null once the source has changed
 # or for a workload without a capture.  The captures' commands and per-launch
 # figures are kept with the other ncu summaries under profiles/.
-_G, _A = "3eb87affcc584e67", "adace5b1b0a0bf87"
+_G, _A = "18b0408e27aa2715", "6f5294747167f930"
 NCU_TRAFFIC = {
     # GPT-3-13B-shaped MLP step (T=8192, h=5120, f=20480, t=8)
     "gpt3_13b": {
-        "gemm1_gelu": (1896.8e6, "gemm", _G),
+        "gemm1_gelu": (1811.8e6, "gemm", _G),
         "gemm2_shardsum": (2255.5e6, "gemm", _G),
-        "gemm_dh_gelu_bwd": (1901.8e6, "gemm", _G),
-        "gemm_wgrad_dB": (2511.2e6, "gemm", _G),
-        "gemm_wgrad_dA": (2325.5e6, "gemm", _G),
-        "gemm_dx_shardsum": (2256.0e6, "gemm", _G),
+        "gemm_dh_gelu_bwd": (1812.7e6, "gemm", _G),
+        "gemm_wgrad_dB": (2499.1e6, "gemm", _G),
+        "gemm_wgrad_dA": (2315.8e6, "gemm", _G),
+        "gemm_dx_shardsum": (2255.8e6, "gemm", _G),
     },
     # the same layer's FP8 forward
     "gpt3_13b_fp8": {
-        "gemm1_gelu_fp8": (555.2e6, "gemm", _G),
-        "gemm2_shardsum_fp8": (1150.9e6, "gemm", _G),
+        "gemm1_gelu_fp8": (557.2e6, "gemm", _G),
+        "gemm2_shardsum_fp8": (1151.1e6, "gemm", _G),
     },
     # the same layer's FP8 training step
     "gpt3_13b_fp8_train": {
-        "gemm1_gelu_fp8": (903.2e6, "gemm", _G),
-        "gemm2_shardsum_fp8": (1150.9e6, "gemm", _G),
-        "gemm_dh_gelu_bwd_fp8": (946.4e6, "gemm", _G),
-        "gemm_wgrad_dB_fp8": (982.0e6, "gemm", _G),
-        "gemm_wgrad_dA_fp8": (901.5e6, "gemm", _G),
-        "gemm_dx_shardsum_fp8": (1152.2e6, "gemm", _G),
+        "gemm1_gelu_fp8": (913.6e6, "gemm", _G),
+        "gemm2_shardsum_fp8": (1151.7e6, "gemm", _G),
+        "gemm_dh_gelu_bwd_fp8": (954.4e6, "gemm", _G),
+        "gemm_wgrad_dB_fp8": (971.3e6, "gemm", _G),
+        "gemm_wgrad_dA_fp8": (894.5e6, "gemm", _G),
+        "gemm_dx_shardsum_fp8": (1150.3e6, "gemm", _G),
+    },
+    # Megatron-8.3B-shaped pre-LN MLP step (T=8192, h=3072, f=12288, t=8)
+    "megatron_8p3b": {
+        "gemm1_ln_gelu": (697.4e6, "gemm", _G),
+        "gemm2_shardsum": (828.7e6, "gemm", _G),
+        "gemm_dh_gelu_bwd": (639.6e6, "gemm", _G),
+        "gemm_wgrad_dB": (913.9e6, "gemm", _G),
+        "gemm_wgrad_dA": (737.5e6, "gemm", _G),
+        "gemm_dx_shardsum": (870.7e6, "gemm", _G),
     },
     # GPT-3-13B-shaped attention block (4 x 2048 tokens, 40 heads of 128)
     "attn_gpt3_13b": {
-        "gemm_qkv": (956.6e6, "gemm", _G),
-        "gemm_out_shardsum": (378.9e6, "gemm", _G),
-        "gemm_wgrad_dWo": (622.2e6, "gemm", _G),
-        "gemm_dctx": (377.2e6, "gemm", _G),
-        "gemm_wgrad_dWqkv": (1762.9e6, "gemm", _G),
-        "gemm_dx_shardsum": (1711.7e6, "gemm", _G),
-        "attn_fwd": (312.1e6, "attn", _A),
-        "attn_bwd_dq": (496.1e6, "attn", _A),
-        "attn_bwd_dkdv": (483.1e6, "attn", _A),
+        "gemm_qkv": (924.9e6, "gemm", _G),
+        "gemm_out_shardsum": (367.3e6, "gemm", _G),
+        "gemm_wgrad_dWo": (619.6e6, "gemm", _G),
+        "gemm_dctx": (366.9e6, "gemm", _G),
+        "gemm_wgrad_dWqkv": (1756.4e6, "gemm", _G),
+        "gemm_dx_shardsum": (1710.2e6, "gemm", _G),
+        "attn_fwd": (311.4e6, "attn", _A),
+        "attn_bwd_dq": (495.7e6, "attn", _A),
+        "attn_bwd_dkdv": (483.0e6, "attn", _A),
+    },
+    # Megatron-8.3B-shaped pre-LN attention block (8 x 1024 tokens, 32 heads
+    # of 96)
+    "attn_megatron_8p3b": {
+        "gemm_ln_qkv": (384.3e6, "gemm", _G),
+        "gemm_out_shardsum": (105.9e6, "gemm", _G),
+        "gemm_wgrad_dWo": (171.8e6, "gemm", _G),
+        "gemm_dctx": (107.4e6, "gemm", _G),
+        "gemm_wgrad_dWqkv": (554.6e6, "gemm", _G),
+        "gemm_dx_shardsum": (667.8e6, "gemm", _G),
+        "attn_fwd": (177.3e6, "attn", _A),
+        "attn_bwd_dq": (293.4e6, "attn", _A),
+        "attn_bwd_dkdv": (279.0e6, "attn", _A),
     },
 }
 _SRC_FILES = {"gemm": ("gemm_tc2.cu", "gemm_common.cuh", "ptx.cuh", "common.cuh"),
