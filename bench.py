@@ -143,14 +143,12 @@ def _peaks():
         return 1900.0, 1700.0, 6800.0, "fallback"
 
 
-def _kernel_peak(clocks, peak_b, peak_s):
-    """The dense bf16 peak a kernel inside the timed step is held to: the
-    burst figure when the timed region ran at (near) the maximum SM clock
-    with no power cap, the sustained figure otherwise."""
-    c = clocks or {}
-    mhz, top = c.get("sm_mhz"), c.get("sm_max_mhz")
-    capped = "sw_power_cap" in (c.get("reasons") or [])
-    if mhz and top and mhz >= 0.97 * top and not capped:
+def _kernel_peak(region_s, peak_b, peak_s):
+    """The dense peak a kernel inside the timed step is held to: the burst
+    figure (a GEMM timed alone) unless the timed region lasts a second or
+    more, the length of the sustained figure's own loop under the power cap,
+    whatever clock the region's samples show."""
+    if region_s < SUSTAINED_REGION_S:
         return peak_b, "burst"
     return peak_s, "sustained"
 
@@ -222,6 +220,19 @@ def _src_sha(files=_SRC_FILES["gemm"]):
     return h.hexdigest()[:16]
 
 
+# Idle pause before each timed region (the device-timed steps and the two
+# end-to-end runs), so that each starts from the same power state instead of
+# the later ones inheriting the power-capped clock of the earlier ones.
+SETTLE_S = 1.0
+# Timed regions at least this long are held to the sustained peak.
+SUSTAINED_REGION_S = 1.0
+
+
+def settle(torch):
+    torch.cuda.synchronize()
+    time.sleep(SETTLE_S)
+
+
 def timed_steps(torch, stream, step, steps):
     """Run `steps` steps with a CUDA event on `stream` before each and after
     the last; returns (mean ms per step over the whole region, per-step
@@ -253,6 +264,7 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.lines = []
+        self.t0 = None
 
     def start(self):
         try:
@@ -266,11 +278,18 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
+
+    def begin(self):
+        """Marks the start of the timed region: the summary keeps the
+        samples from here to stop() (all of them if none falls inside)."""
+        self.t0 = time.monotonic()
 
     def stop(self):
         if self.proc is None:
             return None
+        t1 = time.monotonic()
+        time.sleep(0.15)                  # the sample taken at the end
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -279,7 +298,9 @@ class ClockSampler:
         sm, mx, pw, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
                  "sw_power_cap"]
-        for ln in self.lines:
+        lines = [ln for t, ln in self.lines
+                 if self.t0 is None or self.t0 <= t <= t1 + 0.12]
+        for ln in lines or [ln for _, ln in self.lines]:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -392,11 +413,13 @@ def run_ours(args, w, rank, world, local_rank):
     # ---- timed region: K steps, events on the launching stream ----
     Bn.tp_mlp_set_timing(m.handle, True)
     Bn.tp_mlp_timing_reset(m.handle)
+    settle(torch)
     sampler = ClockSampler(local_rank)
     sampler.start()
     time.sleep(0.25)
     barrier(world)
     torch.cuda.synchronize()
+    sampler.begin()
     n0 = Bn.tp_mlp_launch_count(m.handle)
     ms, step_ms = timed_steps(torch, stream, step, args.steps)
     barrier(world)
@@ -427,19 +450,6 @@ def run_ours(args, w, rank, world, local_rank):
         if w.backward:
             hdX.copy_(grads["dX"], non_blocking=True)
 
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize()
-    barrier(world)
-    e2 = torch.cuda.Event(enable_timing=True)
-    e3 = torch.cuda.Event(enable_timing=True)
-    e2.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e3.record(stream)
-    torch.cuda.synchronize()
-    e2e_serial_ms = max_over_ranks(e2.elapsed_time(e3) / args.steps, world)
-
     # the same with the copies overlapped (two slots, side streams)
     d_in = [[torch.empty_like(d["X"])] + ([torch.empty_like(d["X"])]
                                           if w.backward else [])
@@ -460,10 +470,24 @@ def run_ours(args, w, rank, world, local_rank):
     h_in = [hX] + ([hdZ] if w.backward else [])
     h_out = [hZ] + ([hdX] if w.backward else [])
     e2e_overlapped(torch, stream, 2, h_in, h_out, d_in, d_out, compute)
+    settle(torch)
     barrier(world)
     e2e_ms = max_over_ranks(
         e2e_overlapped(torch, stream, args.steps, h_in, h_out, d_in, d_out,
                        compute), world)
+    # the same with the copies serialised on the compute stream
+    for _ in range(2):
+        e2e_step()
+    settle(torch)
+    barrier(world)
+    e2 = torch.cuda.Event(enable_timing=True)
+    e3 = torch.cuda.Event(enable_timing=True)
+    e2.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e3.record(stream)
+    torch.cuda.synchronize()
+    e2e_serial_ms = max_over_ranks(e2.elapsed_time(e3) / args.steps, world)
     if m.check() != 0:
         raise RuntimeError("device status after the end-to-end runs: "
                            + Bn.tp_mlp_last_detail())
@@ -490,7 +514,7 @@ def run_ours(args, w, rank, world, local_rank):
         ach = gemm_flops[top["name"]] / (top["avg_ms"] * 1e-3) / 1e12
         traffic = traffic_of(w.name, top["name"]) \
             if not (args.tokens or args.shards or args.residual) else None
-        pk, pkind = _kernel_peak(clocks, peak_b, peak_s)
+        pk, pkind = _kernel_peak(ms_max * args.steps / 1e3, peak_b, peak_s)
         roof = {"kernel": top["name"], "bound": "tensor",
                 "achieved": round(ach, 1), "peak": pk, "unit": "TFLOP/s",
                 "frac": round(ach / pk, 4),
@@ -515,7 +539,8 @@ def run_ours(args, w, rank, world, local_rank):
                    "residual": bool(args.residual),
                    "pass": "fwd+bwd" if w.backward else "fwd",
                    "parallelism": f"replicas{world}" if world > 1 else "single",
-                   "l2": "inputs larger than L2 (no flush)"},
+                   "l2": "inputs larger than L2 (no flush)",
+                   "idle_before_timed_s": SETTLE_S},
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2),
                 "unit": "TFLOP/s", "ms_per_step": round(e2e_ms, 4),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -572,7 +597,7 @@ def vendor_context(w, d, args):
     with torch.enable_grad():
         for _ in range(3):
             step()
-        torch.cuda.synchronize()
+        settle(torch)
         n = max(3, min(args.steps, 20))
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
@@ -642,11 +667,13 @@ def run_ours_attn(args, w, rank, world, local_rank):
 
     Bn.tp_attn_set_timing(m.handle, True)
     Bn.tp_attn_timing_reset(m.handle)
+    settle(torch)
     sampler = ClockSampler(local_rank)
     sampler.start()
     time.sleep(0.25)
     barrier(world)
     torch.cuda.synchronize()
+    sampler.begin()
     n0 = Bn.tp_attn_launch_count(m.handle)
     ms, step_ms = timed_steps(torch, stream, step, args.steps)
     barrier(world)
@@ -675,19 +702,6 @@ def run_ours_attn(args, w, rank, world, local_rank):
         hZ.copy_(Z, non_blocking=True)
         hdX.copy_(grads["dX"], non_blocking=True)
 
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize()
-    barrier(world)
-    e2 = torch.cuda.Event(enable_timing=True)
-    e3 = torch.cuda.Event(enable_timing=True)
-    e2.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e3.record(stream)
-    torch.cuda.synchronize()
-    e2e_serial_ms = max_over_ranks(e2.elapsed_time(e3) / args.steps, world)
-
     d_in = [[torch.empty_like(d["X"]), torch.empty_like(d["X"])]
             for _ in range(2)]
     d_out = [[torch.empty_like(Z), torch.empty_like(d["X"])] for _ in range(2)]
@@ -701,10 +715,24 @@ def run_ours_attn(args, w, rank, world, local_rank):
 
     e2e_overlapped(torch, stream, 2, [hX, hdZ], [hZ, hdX], d_in, d_out,
                    compute)
+    settle(torch)
     barrier(world)
     e2e_ms = max_over_ranks(
         e2e_overlapped(torch, stream, args.steps, [hX, hdZ], [hZ, hdX], d_in,
                        d_out, compute), world)
+    # the same with the copies serialised on the compute stream
+    for _ in range(2):
+        e2e_step()
+    settle(torch)
+    barrier(world)
+    e2 = torch.cuda.Event(enable_timing=True)
+    e3 = torch.cuda.Event(enable_timing=True)
+    e2.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e3.record(stream)
+    torch.cuda.synchronize()
+    e2e_serial_ms = max_over_ranks(e2.elapsed_time(e3) / args.steps, world)
     if m.check() != 0:
         raise RuntimeError("device status after the end-to-end runs: "
                            + Bn.tp_mlp_last_detail())
@@ -726,7 +754,7 @@ def run_ours_attn(args, w, rank, world, local_rank):
         ach = kf[top["name"]] / (top["avg_ms"] * 1e-3) / 1e12
         traffic = traffic_of(w.name, top["name"]) \
             if not (args.tokens or args.shards or args.residual) else None
-        pk, pkind = _kernel_peak(clocks, peak_b, peak_s)
+        pk, pkind = _kernel_peak(ms_max * args.steps / 1e3, peak_b, peak_s)
         roof = {"kernel": top["name"], "bound": "tensor",
                 "achieved": round(ach, 1), "peak": pk, "unit": "TFLOP/s",
                 "frac": round(ach / pk, 4),
@@ -749,7 +777,8 @@ def run_ours_attn(args, w, rank, world, local_rank):
                    "causal": w.causal, "layernorm": w.layernorm,
                    "residual": bool(args.residual), "pass": "fwd+bwd",
                    "parallelism": f"replicas{world}" if world > 1 else "single",
-                   "l2": "inputs larger than L2 (no flush)"},
+                   "l2": "inputs larger than L2 (no flush)",
+                   "idle_before_timed_s": SETTLE_S},
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2),
                 "unit": "TFLOP/s", "ms_per_step": round(e2e_ms, 4),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -888,11 +917,13 @@ def run_ours_fp8(args, w, rank, world, local_rank):
 
     Bn.tp_mlp_set_timing(m.handle, True)
     Bn.tp_mlp_timing_reset(m.handle)
+    settle(torch)
     sampler = ClockSampler(local_rank)
     sampler.start()
     time.sleep(0.25)
     barrier(world)
     torch.cuda.synchronize()
+    sampler.begin()
     n0 = Bn.tp_mlp_launch_count(m.handle)
     ms, step_ms = timed_steps(torch, stream, step, args.steps)
     barrier(world)
@@ -933,12 +964,6 @@ def run_ours_fp8(args, w, rank, world, local_rank):
         if train:
             hdX.copy_(grads["dX"], non_blocking=True)
 
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize()
-    barrier(world)
-    e2e_serial_ms = max_over_ranks(timed(e2e_step, args.steps), world)
-
     nio = 2 if train else 1
     d_in = [[torch.empty_like(d["X"]) for _ in range(nio)] for _ in range(2)]
     d_out = [[torch.empty_like(Z) for _ in range(nio)] for _ in range(2)]
@@ -950,10 +975,17 @@ def run_ours_fp8(args, w, rank, world, local_rank):
              d_out[k][1] if train else None)
 
     e2e_overlapped(torch, stream, 2, h_in, h_out, d_in, d_out, compute)
+    settle(torch)
     barrier(world)
     e2e_ms = max_over_ranks(
         e2e_overlapped(torch, stream, args.steps, h_in, h_out, d_in, d_out,
                        compute), world)
+    # the same with the copies serialised on the compute stream
+    for _ in range(2):
+        e2e_step()
+    settle(torch)
+    barrier(world)
+    e2e_serial_ms = max_over_ranks(timed(e2e_step, args.steps), world)
     if m.check() != 0:
         raise RuntimeError("device status after the end-to-end runs: "
                            + Bn.tp_mlp_last_detail())
@@ -977,7 +1009,8 @@ def run_ours_fp8(args, w, rank, world, local_rank):
     roof = None
     if top["name"] in kf:
         ach = kf[top["name"]] / (top["avg_ms"] * 1e-3) / 1e12
-        pk, pkind = _kernel_peak(clocks, fp8_burst, fp8_sust)
+        pk, pkind = _kernel_peak(ms_max * args.steps / 1e3, fp8_burst,
+                                 fp8_sust)
         roof = {"kernel": top["name"], "bound": "tensor",
                 "achieved": round(ach, 1), "peak": pk,
                 "unit": "TFLOP/s", "frac": round(ach / pk, 4),
@@ -1008,7 +1041,8 @@ def run_ours_fp8(args, w, rank, world, local_rank):
                    "residual": bool(args.residual),
                    "pass": "fwd+bwd (fp8)" if train else "fwd (fp8)",
                    "parallelism": f"replicas{world}" if world > 1 else "single",
-                   "l2": "inputs larger than L2 (no flush)"},
+                   "l2": "inputs larger than L2 (no flush)",
+                   "idle_before_timed_s": SETTLE_S},
         ("bf16_train_step" if train else "bf16_forward"): {
                          "ms_per_step": round(bf16_ms, 4),
                          "value": round(flops / (bf16_ms * 1e-3) / 1e12, 2),

@@ -3,6 +3,7 @@ reduction of the replica mode (world size 2, gloo), the clock-sample parser
 and the oracle slice sizing."""
 import os
 import socket
+import time
 
 import pytest
 import torch.multiprocessing as mp
@@ -46,11 +47,18 @@ def test_max_over_ranks_single_process_is_identity():
 
 def test_clock_sampler_parses_nvidia_smi_lines():
     s = bench.ClockSampler(0)
+    now = time.monotonic()
     s.lines = [
-        "0, 1650, 2070, 1361.2, 0x4, Not Active, Not Active, Not Active, Active",
-        "0, 1605, 2070, 1370.0, 0x4, Not Active, Not Active, Not Active, Active",
-        "garbage",
+        # idle, before the timed region began: left out of the summary
+        (now - 5.0, "0, 1980, 2070, 180.0, 0x0, Not Active, Not Active, "
+                    "Not Active, Not Active"),
+        (now - 1.0, "0, 1650, 2070, 1361.2, 0x4, Not Active, Not Active, "
+                    "Not Active, Active"),
+        (now - 0.9, "0, 1605, 2070, 1370.0, 0x4, Not Active, Not Active, "
+                    "Not Active, Active"),
+        (now - 0.8, "garbage"),
     ]
+    s.t0 = now - 2.0
 
     class FinishedProcess:  # stand-in for the nvidia-smi child process
         def terminate(self):
