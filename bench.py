@@ -61,7 +61,7 @@ DEFAULT_WORKLOAD = "gpt3_13b"
 # "attn": the attention core).  Reported as null once the source has changed
 # or for a workload without a capture.  The captures' commands and per-launch
 # figures are kept with the other ncu summaries under profiles/.
-_G, _A = "18b0408e27aa2715", "6f5294747167f930"
+_G, _A = "73fa3dd9ac5d98d6", "6f5294747167f930"
 NCU_TRAFFIC = {
     # GPT-3-13B-shaped MLP step (T=8192, h=5120, f=20480, t=8)
     "gpt3_13b": {

@@ -373,6 +373,8 @@ __device__ __forceinline__ void mma_f8_pair(uint32_t d_tmem, uint64_t adesc,
 
 // Arrive once on the mbarrier at `bar` (same offset) in every CTA of
 // `cta_mask` when all tcgen05 ops issued so far by this thread are done.
+// (The multicast here is of the arrive signal within the CTA pair, not of
+// data: no copy in this library multicasts.)
 __device__ __forceinline__ void mma_commit_pair(uint32_t bar,
                                                 uint16_t cta_mask) {
   asm volatile(
