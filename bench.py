@@ -220,9 +220,10 @@ def _src_sha(files=_SRC_FILES["gemm"]):
     return h.hexdigest()[:16]
 
 
-# Idle pause before each timed region (the device-timed steps and the two
-# end-to-end runs), so that each starts from the same power state instead of
-# the later ones inheriting the power-capped clock of the earlier ones.
+# Idle pause before each timed region (the device-timed steps, the two
+# end-to-end runs and the cuBLAS context), each followed by a few untimed
+# steps, so that every region starts warm from the same power state instead
+# of the later ones inheriting the power-capped clock of the earlier ones.
 SETTLE_S = 1.0
 # Timed regions at least this long are held to the sustained peak.
 SUSTAINED_REGION_S = 1.0
@@ -417,6 +418,10 @@ def run_ours(args, w, rank, world, local_rank):
     sampler = ClockSampler(local_rank)
     sampler.start()
     time.sleep(0.25)
+    for _ in range(3):            # back from the pause, untimed
+        step()
+    torch.cuda.synchronize()
+    Bn.tp_mlp_timing_reset(m.handle)
     barrier(world)
     torch.cuda.synchronize()
     sampler.begin()
@@ -469,16 +474,17 @@ def run_ours(args, w, rank, world, local_rank):
 
     h_in = [hX] + ([hdZ] if w.backward else [])
     h_out = [hZ] + ([hdX] if w.backward else [])
-    e2e_overlapped(torch, stream, 2, h_in, h_out, d_in, d_out, compute)
     settle(torch)
+    e2e_overlapped(torch, stream, 2, h_in, h_out, d_in, d_out, compute)
     barrier(world)
     e2e_ms = max_over_ranks(
         e2e_overlapped(torch, stream, args.steps, h_in, h_out, d_in, d_out,
                        compute), world)
     # the same with the copies serialised on the compute stream
+    settle(torch)
     for _ in range(2):
         e2e_step()
-    settle(torch)
+    torch.cuda.synchronize()
     barrier(world)
     e2 = torch.cuda.Event(enable_timing=True)
     e3 = torch.cuda.Event(enable_timing=True)
@@ -595,9 +601,10 @@ def vendor_context(w, d, args):
         return Z
 
     with torch.enable_grad():
+        settle(torch)
         for _ in range(3):
             step()
-        settle(torch)
+        torch.cuda.synchronize()
         n = max(3, min(args.steps, 20))
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
@@ -618,7 +625,8 @@ def attn_kernel_flops(w):
     """Algorithmic flops per launch of each attention-block kernel."""
     T, h = w.tokens, w.hidden
     core = 2.0 * w.head_dim * w.score_pairs()      # one pair-wise matmul
-    return {"gemm_qkv": 6.0 * T * h * h, "gemm_out_shardsum": 2.0 * T * h * h,
+    return {"gemm_qkv": 6.0 * T * h * h, "gemm_ln_qkv": 6.0 * T * h * h,
+            "gemm_out_shardsum": 2.0 * T * h * h,
             "gemm_wgrad_dWo": 2.0 * T * h * h, "gemm_dctx": 2.0 * T * h * h,
             "gemm_wgrad_dWqkv": 6.0 * T * h * h,
             "gemm_dx_shardsum": 6.0 * T * h * h,
@@ -671,6 +679,10 @@ def run_ours_attn(args, w, rank, world, local_rank):
     sampler = ClockSampler(local_rank)
     sampler.start()
     time.sleep(0.25)
+    for _ in range(3):            # back from the pause, untimed
+        step()
+    torch.cuda.synchronize()
+    Bn.tp_attn_timing_reset(m.handle)
     barrier(world)
     torch.cuda.synchronize()
     sampler.begin()
@@ -713,17 +725,18 @@ def run_ours_attn(args, w, rank, world, local_rank):
         m.backward(d_in[k][1], d_in[k][0], d["Wqkv"], d["Wo"], d["gamma"],
                    out=slot_grads[k])
 
+    settle(torch)
     e2e_overlapped(torch, stream, 2, [hX, hdZ], [hZ, hdX], d_in, d_out,
                    compute)
-    settle(torch)
     barrier(world)
     e2e_ms = max_over_ranks(
         e2e_overlapped(torch, stream, args.steps, [hX, hdZ], [hZ, hdX], d_in,
                        d_out, compute), world)
     # the same with the copies serialised on the compute stream
+    settle(torch)
     for _ in range(2):
         e2e_step()
-    settle(torch)
+    torch.cuda.synchronize()
     barrier(world)
     e2 = torch.cuda.Event(enable_timing=True)
     e3 = torch.cuda.Event(enable_timing=True)
@@ -921,6 +934,10 @@ def run_ours_fp8(args, w, rank, world, local_rank):
     sampler = ClockSampler(local_rank)
     sampler.start()
     time.sleep(0.25)
+    for _ in range(3):            # back from the pause, untimed
+        step()
+    torch.cuda.synchronize()
+    Bn.tp_mlp_timing_reset(m.handle)
     barrier(world)
     torch.cuda.synchronize()
     sampler.begin()
@@ -974,16 +991,17 @@ def run_ours_fp8(args, w, rank, world, local_rank):
         step(d_in[k][0], d_in[k][1] if train else None, d_out[k][0],
              d_out[k][1] if train else None)
 
-    e2e_overlapped(torch, stream, 2, h_in, h_out, d_in, d_out, compute)
     settle(torch)
+    e2e_overlapped(torch, stream, 2, h_in, h_out, d_in, d_out, compute)
     barrier(world)
     e2e_ms = max_over_ranks(
         e2e_overlapped(torch, stream, args.steps, h_in, h_out, d_in, d_out,
                        compute), world)
     # the same with the copies serialised on the compute stream
+    settle(torch)
     for _ in range(2):
         e2e_step()
-    settle(torch)
+    torch.cuda.synchronize()
     barrier(world)
     e2e_serial_ms = max_over_ranks(timed(e2e_step, args.steps), world)
     if m.check() != 0:
