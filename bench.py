@@ -9,8 +9,11 @@ One step = one training pass of the block over one batch: tp_mlp_forward
 weight-gradient GEMMs, dX GEMM + shard sum, and the LayerNorm kernels when the
 workload has pre-LN).  Algorithmic work: 12 T h f flops per step (forward
 4 T h f), whatever the shard count.  Inputs are seeded synthetic tensors of
-the workload's shapes, resident in device memory before timing starts; the
-weights alone exceed the 129 MB L2, so no flush is inserted between steps.
+the workload's shapes, resident in device memory before timing starts.
+Where the weights alone exceed the 129 MB L2 (GPT-3-13B, 8.3B, BLOOM MLP
+blocks; the GPT-3-13B attention block) no flush is inserted between steps;
+otherwise a 256 MiB write evicts L2 before every timed step, outside the
+step's events (config "l2" says which).
 
 ``--workload attn_gpt3_13b`` (or another ``attn_*`` workload) times the
 head-parallel attention block instead: one step = tp_attn_forward (training)
@@ -234,10 +237,46 @@ def settle(torch):
     time.sleep(SETTLE_S)
 
 
-def timed_steps(torch, stream, step, steps):
+# GB300's L2; a workload whose weights fit in it is timed with a flush
+# (a 256 MiB write) before every timed step.
+L2_BYTES = 129 * 10 ** 6
+
+
+def l2_flusher(torch, weight_bytes):
+    """None when the weights alone exceed L2 (then every step streams more
+    than L2 holds); otherwise a callable that writes a 256 MiB buffer on the
+    current stream, evicting what the last step left in L2."""
+    if weight_bytes > L2_BYTES:
+        return None
+    buf = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    return buf.zero_
+
+
+def l2_note(flush):
+    return ("inputs larger than L2 (no flush)" if flush is None else
+            "L2 flushed (256 MiB write) before each timed step, the flush "
+            "not timed; end-to-end runs not flushed")
+
+
+def timed_steps(torch, stream, step, steps, flush=None):
     """Run `steps` steps with a CUDA event on `stream` before each and after
     the last; returns (mean ms per step over the whole region, per-step
-    median / min / max in ms)."""
+    median / min / max in ms).  With `flush`, it runs before every step
+    between the step's own pair of events, and the mean is over the steps'
+    own times."""
+    if flush is not None:
+        ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        for i in range(steps):
+            flush()
+            ev0[i].record(stream)
+            step()
+            ev1[i].record(stream)
+        torch.cuda.synchronize()
+        per = [ev0[i].elapsed_time(ev1[i]) for i in range(steps)]
+        stats = {"median": round(statistics.median(per), 4),
+                 "min": round(min(per), 4), "max": round(max(per), 4)}
+        return sum(per) / steps, stats
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
     evs[0].record(stream)
     for i in range(steps):
@@ -414,6 +453,7 @@ def run_ours(args, w, rank, world, local_rank):
     # ---- timed region: K steps, events on the launching stream ----
     Bn.tp_mlp_set_timing(m.handle, True)
     Bn.tp_mlp_timing_reset(m.handle)
+    flush = l2_flusher(torch, 4 * w.hidden * w.ffn)   # weight bytes
     settle(torch)
     sampler = ClockSampler(local_rank)
     sampler.start()
@@ -426,7 +466,7 @@ def run_ours(args, w, rank, world, local_rank):
     torch.cuda.synchronize()
     sampler.begin()
     n0 = Bn.tp_mlp_launch_count(m.handle)
-    ms, step_ms = timed_steps(torch, stream, step, args.steps)
+    ms, step_ms = timed_steps(torch, stream, step, args.steps, flush)
     barrier(world)
     clocks = sampler.stop()
     launches = Bn.tp_mlp_launch_count(m.handle) - n0
@@ -545,7 +585,7 @@ def run_ours(args, w, rank, world, local_rank):
                    "residual": bool(args.residual),
                    "pass": "fwd+bwd" if w.backward else "fwd",
                    "parallelism": f"replicas{world}" if world > 1 else "single",
-                   "l2": "inputs larger than L2 (no flush)",
+                   "l2": l2_note(flush),
                    "idle_before_timed_s": SETTLE_S},
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2),
                 "unit": "TFLOP/s", "ms_per_step": round(e2e_ms, 4),
@@ -675,6 +715,7 @@ def run_ours_attn(args, w, rank, world, local_rank):
 
     Bn.tp_attn_set_timing(m.handle, True)
     Bn.tp_attn_timing_reset(m.handle)
+    flush = l2_flusher(torch, 8 * w.hidden * w.hidden)   # weight bytes
     settle(torch)
     sampler = ClockSampler(local_rank)
     sampler.start()
@@ -687,7 +728,7 @@ def run_ours_attn(args, w, rank, world, local_rank):
     torch.cuda.synchronize()
     sampler.begin()
     n0 = Bn.tp_attn_launch_count(m.handle)
-    ms, step_ms = timed_steps(torch, stream, step, args.steps)
+    ms, step_ms = timed_steps(torch, stream, step, args.steps, flush)
     barrier(world)
     clocks = sampler.stop()
     launches = Bn.tp_attn_launch_count(m.handle) - n0
@@ -790,7 +831,7 @@ def run_ours_attn(args, w, rank, world, local_rank):
                    "causal": w.causal, "layernorm": w.layernorm,
                    "residual": bool(args.residual), "pass": "fwd+bwd",
                    "parallelism": f"replicas{world}" if world > 1 else "single",
-                   "l2": "inputs larger than L2 (no flush)",
+                   "l2": l2_note(flush),
                    "idle_before_timed_s": SETTLE_S},
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2),
                 "unit": "TFLOP/s", "ms_per_step": round(e2e_ms, 4),
@@ -930,6 +971,7 @@ def run_ours_fp8(args, w, rank, world, local_rank):
 
     Bn.tp_mlp_set_timing(m.handle, True)
     Bn.tp_mlp_timing_reset(m.handle)
+    flush = l2_flusher(torch, 2 * w.hidden * w.ffn)   # weight bytes
     settle(torch)
     sampler = ClockSampler(local_rank)
     sampler.start()
@@ -942,7 +984,7 @@ def run_ours_fp8(args, w, rank, world, local_rank):
     torch.cuda.synchronize()
     sampler.begin()
     n0 = Bn.tp_mlp_launch_count(m.handle)
-    ms, step_ms = timed_steps(torch, stream, step, args.steps)
+    ms, step_ms = timed_steps(torch, stream, step, args.steps, flush)
     barrier(world)
     clocks = sampler.stop()
     launches = Bn.tp_mlp_launch_count(m.handle) - n0
@@ -1059,7 +1101,7 @@ def run_ours_fp8(args, w, rank, world, local_rank):
                    "residual": bool(args.residual),
                    "pass": "fwd+bwd (fp8)" if train else "fwd (fp8)",
                    "parallelism": f"replicas{world}" if world > 1 else "single",
-                   "l2": "inputs larger than L2 (no flush)",
+                   "l2": l2_note(flush),
                    "idle_before_timed_s": SETTLE_S},
         ("bf16_train_step" if train else "bf16_forward"): {
                          "ms_per_step": round(bf16_ms, 4),

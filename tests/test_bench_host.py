@@ -141,3 +141,14 @@ def test_oracle_one_core_runs_in_a_single_threaded_child():
     assert "error" not in r, r
     assert r["threads"] == 1 and r["value"] > 0
     assert r["sample"].startswith("first 16 of 32 tokens")
+
+
+def test_l2_flush_only_where_the_weights_fit_in_l2():
+    import torch
+    # GPT-3-13B MLP weights (A and B in bf16) exceed L2: no flush, no
+    # allocation
+    assert bench.l2_flusher(torch, 4 * 5120 * 20480) is None
+    assert "no flush" in bench.l2_note(None)
+    assert "flushed" in bench.l2_note(lambda: None)
+    # GPT-2-medium's do not (a flush would be made on the device)
+    assert 4 * 1024 * 4096 < bench.L2_BYTES
