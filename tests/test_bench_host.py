@@ -152,3 +152,12 @@ def test_l2_flush_only_where_the_weights_fit_in_l2():
     assert "flushed" in bench.l2_note(lambda: None)
     # GPT-2-medium's do not (a flush would be made on the device)
     assert 4 * 1024 * 4096 < bench.L2_BYTES
+
+
+def test_roofline_peak_is_burst_for_short_regions():
+    # a 20-step region of the GPT-3-13B step lasts ~0.12 s: burst peak
+    # whatever its clock samples show; a region of a second or more is held
+    # to the sustained figure
+    assert bench._kernel_peak(0.12, 1885.6, 1707.6) == (1885.6, "burst")
+    assert bench._kernel_peak(bench.SUSTAINED_REGION_S, 1885.6, 1707.6) == \
+        (1707.6, "sustained")
